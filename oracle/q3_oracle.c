@@ -1,0 +1,586 @@
+/*
+ * q3_oracle.c -- plain CPU oracle for the token-round forward of a dense
+ * Qwen3-style decoder.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check
+ * and the bench's CPU-baseline leg call it; the CUDA path never does.
+ *
+ * Sources (Kipp pages): "Kipp Model Support" (sections "The registry",
+ * "What the gates check", "qwen3-0.6b-base", "Quantization (Q8_0)"),
+ * "Kipp Roadmap" (status v0.0.2: paged KV and batched evaluation), and
+ * "Reproducing Kipp" (section "Model-backed CPU and Metal gates").  Where the
+ * pages leave the layer math open, the oracle takes the plain reading of a
+ * standard dense Qwen3 decoder; each such reading is marked "reading".
+ *
+ * Every function is written to be checked by eye: one output at a time, in
+ * logical order, FP64 accumulators, FP32 storage.  Threads only split the
+ * list of independent outputs; each output is computed the same way whatever
+ * the thread count, so results do not depend on it.
+ */
+#include "q3_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* scalar conversions                                                  */
+/* ------------------------------------------------------------------ */
+
+/* A bf16 value is the upper 16 bits of the float with the same value. */
+float orc_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Round a float to the nearest bf16, ties to the even pattern.  Adding
+ * 0x7fff (+1 when the kept part is odd) to the bits carries into the kept
+ * half exactly when the dropped half is above the tie, or at the tie with an
+ * odd kept half. */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u)         /* NaN: keep it a quiet NaN */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+float orc_f16_to_f32(uint16_t h)
+{
+    int sign = h >> 15, e = (h >> 10) & 0x1f, m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);     /* (1 + m/1024) * 2^(e-15) */
+    return (float)(sign ? -v : v);
+}
+
+/* Nearest binary16, ties to even (the default rounding mode of nearbyint). */
+uint16_t orc_f32_to_f16(float f)
+{
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    double a = fabs((double)f);
+    if (isnan(f))
+        return sign | 0x7e00;
+    if (isinf(f))
+        return sign | 0x7c00;
+    if (a < ldexp(1.0, -14)) {                     /* subnormal range, quantum 2^-24 */
+        double r = nearbyint(a * ldexp(1.0, 24));  /* exact scaling, then round */
+        return sign | (uint16_t)r;                 /* r == 1024 encodes 2^-14 */
+    }
+    int e;
+    frexp(a, &e);                                  /* a = f * 2^e, f in [0.5, 1) */
+    double r = nearbyint(ldexp(a, 11 - e));        /* 11 significant bits: [1024, 2048] */
+    int E = e - 1 + 15;
+    if (r == 2048.0) { r = 1024.0; E += 1; }
+    if (E >= 31)
+        return sign | 0x7c00;                      /* overflow to infinity */
+    return (uint16_t)(sign | (E << 10) | ((int)r - 1024));
+}
+
+int orc_argmax(const float* v, int n)
+{
+    int best = 0;
+    for (int i = 1; i < n; i++)
+        if (v[i] > v[best]) best = i;              /* strict: lowest index wins ties */
+    return best;
+}
+
+/* ------------------------------------------------------------------ */
+/* Q8_0 ("Kipp Model Support", section "Quantization (Q8_0)")          */
+/* ------------------------------------------------------------------ */
+
+/* Reading: per block of 32 weights, d = absmax/127 in FP32; the stored
+ * scale is fp16(d); quants are round-half-even(w/d) against the FP32 d,
+ * clamped to [-127, 127]; an all-zero block has d = 0 and zero quants. */
+void orc_q8_0_pack(const float* w, long n, uint8_t* blocks)
+{
+    for (long b = 0; b < n / ORC_BLOCK; b++) {
+        const float* x = w + b * ORC_BLOCK;
+        uint8_t* out = blocks + b * ORC_Q8_0_BYTES;
+        float amax = 0.0f;
+        for (int i = 0; i < ORC_BLOCK; i++)
+            if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+        float d = amax / 127.0f;
+        uint16_t dh = orc_f32_to_f16(d);
+        out[0] = (uint8_t)(dh & 0xff);
+        out[1] = (uint8_t)(dh >> 8);
+        for (int i = 0; i < ORC_BLOCK; i++) {
+            int q = 0;
+            if (d != 0.0f) {
+                float r = nearbyintf(x[i] / d);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                q = (int)r;
+            }
+            out[2 + i] = (uint8_t)(int8_t)q;
+        }
+    }
+}
+
+/* w = f32(fp16 scale) * q; the product is exact in FP32 (11 x 8 bits). */
+void orc_q8_0_unpack(const uint8_t* blocks, long n, float* w)
+{
+    for (long b = 0; b < n / ORC_BLOCK; b++) {
+        const uint8_t* in = blocks + b * ORC_Q8_0_BYTES;
+        float d = orc_f16_to_f32((uint16_t)(in[0] | (in[1] << 8)));
+        for (int i = 0; i < ORC_BLOCK; i++)
+            w[b * ORC_BLOCK + i] = d * (float)(int8_t)in[2 + i];
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* threads: split [0, n) into contiguous ranges, one per thread         */
+/* ------------------------------------------------------------------ */
+
+typedef void (*range_fn)(void* ctx, long i0, long i1);
+typedef struct { range_fn fn; void* ctx; long i0, i1; } range_job;
+
+static void* range_main(void* a)
+{
+    range_job* j = (range_job*)a;
+    j->fn(j->ctx, j->i0, j->i1);
+    return NULL;
+}
+
+static void parallel_for(long n, int n_threads, range_fn fn, void* ctx)
+{
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > n) n_threads = (int)(n > 0 ? n : 1);
+    if (n_threads == 1) { fn(ctx, 0, n); return; }
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * n_threads);
+    range_job* jobs = (range_job*)malloc(sizeof(range_job) * n_threads);
+    for (int k = 0; k < n_threads; k++) {
+        jobs[k].fn = fn; jobs[k].ctx = ctx;
+        jobs[k].i0 = n * k / n_threads;
+        jobs[k].i1 = n * (k + 1) / n_threads;
+        pthread_create(&th[k], NULL, range_main, &jobs[k]);
+    }
+    for (int k = 0; k < n_threads; k++) pthread_join(th[k], NULL);
+    free(th);
+    free(jobs);
+}
+
+/* ------------------------------------------------------------------ */
+/* components                                                          */
+/* ------------------------------------------------------------------ */
+
+/* RMSNorm (reading): y = x / sqrt(mean(x^2) + eps) * g, eps inside the root,
+ * the gain multiplies as stored (not 1 + g). */
+void orc_rmsnorm(const float* x, const uint16_t* gain, int n, double eps, float* y)
+{
+    double ss = 0.0;
+    for (int i = 0; i < n; i++) ss += (double)x[i] * (double)x[i];
+    double r = 1.0 / sqrt(ss / n + eps);
+    for (int i = 0; i < n; i++)
+        y[i] = (float)((double)x[i] * r * (double)orc_bf16_to_f32(gain[i]));
+}
+
+/* RoPE (reading: rotate-half pairing).  For i < d/2 the pair (v[i],
+ * v[i + d/2]) turns by the angle pos * theta^(-2i/d):
+ *   v[i]       <- v[i] cos a - v[i+d/2] sin a
+ *   v[i + d/2] <- v[i+d/2] cos a + v[i] sin a
+ * pos is the absolute 0-based position in the session. */
+void orc_rope(float* v, int head_dim, int pos, double theta)
+{
+    int half = head_dim / 2;
+    for (int i = 0; i < half; i++) {
+        double inv_freq = pow(theta, -(2.0 * i) / head_dim);
+        double a = (double)pos * inv_freq;
+        double c = cos(a), s = sin(a);
+        double x1 = v[i], x2 = v[i + half];
+        v[i] = (float)(x1 * c - x2 * s);
+        v[i + half] = (float)(x2 * c + x1 * s);
+    }
+}
+
+/* SiLU(z) = z / (1 + e^-z) */
+float orc_silu(float z)
+{
+    return (float)((double)z / (1.0 + exp(-(double)z)));
+}
+
+typedef struct {
+    const void* W; int scheme, n_out, n_in;
+    const float* x; int n_tok; float* y;
+} matmul_job;
+
+static void matmul_rows(void* a, long o0, long o1)
+{
+    matmul_job* j = (matmul_job*)a;
+    double* w = (double*)malloc(sizeof(double) * j->n_in);
+    float* wq = (float*)malloc(sizeof(float) * j->n_in);
+    for (long o = o0; o < o1; o++) {
+        if (j->scheme == ORC_BF16) {
+            const uint16_t* row = (const uint16_t*)j->W + o * (long)j->n_in;
+            for (int i = 0; i < j->n_in; i++) w[i] = orc_bf16_to_f32(row[i]);
+        } else {
+            const uint8_t* row = (const uint8_t*)j->W
+                               + o * (long)(j->n_in / ORC_BLOCK) * ORC_Q8_0_BYTES;
+            orc_q8_0_unpack(row, j->n_in, wq);
+            for (int i = 0; i < j->n_in; i++) w[i] = wq[i];
+        }
+        for (int t = 0; t < j->n_tok; t++) {
+            const float* xt = j->x + (long)t * j->n_in;
+            double acc = 0.0;
+            for (int i = 0; i < j->n_in; i++) acc += w[i] * (double)xt[i];
+            j->y[(long)t * j->n_out + o] = (float)acc;
+        }
+    }
+    free(w);
+    free(wq);
+}
+
+/* y[t][o] = sum_i W[o][i] x[t][i], W row-major [n_out][n_in] (nn.Linear). */
+void orc_matmul(const void* W, int scheme, int n_out, int n_in,
+                const float* x, int n_tok, float* y, int n_threads)
+{
+    matmul_job j = { W, scheme, n_out, n_in, x, n_tok, y };
+    parallel_for(n_out, n_threads, matmul_rows, &j);
+}
+
+/* Causal softmax attention of one query row over ctx cached positions
+ * (reading: scale 1/sqrt(d), the max subtracted before exp, contiguous GQA
+ * grouping: query head h reads KV head h / (n_q / n_kv)). */
+void orc_gqa_attend(const float* q, const uint16_t* K, const uint16_t* V,
+                    int ctx, int n_q, int n_kv, int d, float* o)
+{
+    int group = n_q / n_kv;
+    double scale = 1.0 / sqrt((double)d);
+    double* s = (double*)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+    for (int h = 0; h < n_q; h++) {
+        int kvh = h / group;
+        const float* qh = q + (long)h * d;
+        double mx = -INFINITY;
+        for (int j = 0; j < ctx; j++) {
+            const uint16_t* kj = K + ((long)j * n_kv + kvh) * d;
+            double dot = 0.0;
+            for (int i = 0; i < d; i++) dot += (double)qh[i] * orc_bf16_to_f32(kj[i]);
+            s[j] = dot * scale;
+            if (s[j] > mx) mx = s[j];
+        }
+        double z = 0.0;
+        for (int j = 0; j < ctx; j++) { s[j] = exp(s[j] - mx); z += s[j]; }
+        for (int i = 0; i < d; i++) {
+            double acc = 0.0;
+            for (int j = 0; j < ctx; j++)
+                acc += s[j] * orc_bf16_to_f32(V[((long)j * n_kv + kvh) * d + i]);
+            o[(long)h * d + i] = (float)(acc / z);
+        }
+    }
+    free(s);
+}
+
+/* ------------------------------------------------------------------ */
+/* model, KV storage, sessions                                         */
+/* ------------------------------------------------------------------ */
+
+struct orc_model {
+    orc_cfg c;
+    const uint16_t *embed, *final_norm, *lm_head;
+    orc_layer* layers;
+    int n_threads;
+};
+
+struct orc_pool {
+    orc_model* m;
+    int n_blocks;
+    uint16_t *k, *v;        /* [L][n_blocks][32][n_kv][d] bf16 */
+    unsigned char* used;
+};
+
+struct orc_session {
+    orc_model* m;
+    orc_pool* pool;         /* NULL: contiguous */
+    int max_ctx, pos;
+    uint16_t *k, *v;        /* contiguous: [L][max_ctx][n_kv][d] bf16 */
+    int32_t* table;         /* paged: block id per 32 positions */
+    int n_table, n_given;   /* blocks taken; entries given by the caller */
+};
+
+orc_model* orc_model_create(const orc_cfg* cfg, const uint16_t* embed,
+                            const uint16_t* final_norm, const uint16_t* lm_head,
+                            const orc_layer* layers, int n_threads)
+{
+    if (cfg->n_q_heads % cfg->n_kv_heads || cfg->head_dim % 2 ||
+        (cfg->scheme == ORC_Q8_0 && (cfg->hidden % ORC_BLOCK || cfg->ffn % ORC_BLOCK ||
+                                     (cfg->n_q_heads * cfg->head_dim) % ORC_BLOCK)))
+        return NULL;
+    orc_model* m = (orc_model*)calloc(1, sizeof(orc_model));
+    m->c = *cfg;
+    m->embed = embed;
+    m->final_norm = final_norm;
+    m->lm_head = cfg->tied ? embed : lm_head;
+    m->layers = (orc_layer*)malloc(sizeof(orc_layer) * cfg->n_layers);
+    memcpy(m->layers, layers, sizeof(orc_layer) * cfg->n_layers);
+    m->n_threads = n_threads > 0 ? n_threads : 1;
+    return m;
+}
+
+void orc_model_free(orc_model* m)
+{
+    if (!m) return;
+    free(m->layers);
+    free(m);
+}
+
+static long kv_row(const orc_cfg* c) { return (long)c->n_kv_heads * c->head_dim; }
+
+orc_pool* orc_pool_create(orc_model* m, int n_blocks)
+{
+    orc_pool* p = (orc_pool*)calloc(1, sizeof(orc_pool));
+    long n = (long)m->c.n_layers * n_blocks * ORC_BLOCK * kv_row(&m->c);
+    p->m = m;
+    p->n_blocks = n_blocks;
+    p->k = (uint16_t*)calloc(n, 2);
+    p->v = (uint16_t*)calloc(n, 2);
+    p->used = (unsigned char*)calloc(n_blocks, 1);
+    if (!p->k || !p->v || !p->used) { orc_pool_free(p); return NULL; }
+    return p;
+}
+
+void orc_pool_free(orc_pool* p)
+{
+    if (!p) return;
+    free(p->k); free(p->v); free(p->used); free(p);
+}
+
+orc_session* orc_session_create(orc_model* m, orc_pool* pool, int max_ctx)
+{
+    orc_session* s = (orc_session*)calloc(1, sizeof(orc_session));
+    s->m = m;
+    s->pool = pool;
+    s->max_ctx = max_ctx;
+    if (!pool) {
+        long n = (long)m->c.n_layers * max_ctx * kv_row(&m->c);
+        s->k = (uint16_t*)calloc(n, 2);
+        s->v = (uint16_t*)calloc(n, 2);
+        if (!s->k || !s->v) { orc_session_free(s); return NULL; }
+    } else {
+        s->table = (int32_t*)calloc((max_ctx + ORC_BLOCK - 1) / ORC_BLOCK, sizeof(int32_t));
+    }
+    return s;
+}
+
+void orc_session_free(orc_session* s)
+{
+    if (!s) return;
+    if (s->pool)
+        for (int b = 0; b < s->n_table; b++) s->pool->used[s->table[b]] = 0;
+    free(s->k); free(s->v); free(s->table); free(s);
+}
+
+/* The caller fixes which pool blocks back the session's positions, in
+ * order: block i holds positions [32 i, 32 i + 32). */
+int orc_session_set_block_table(orc_session* s, const int32_t* ids, int n)
+{
+    if (!s->pool || s->pos != 0 || n > (s->max_ctx + ORC_BLOCK - 1) / ORC_BLOCK) return -1;
+    for (int b = 0; b < s->n_table; b++) s->pool->used[s->table[b]] = 0;
+    for (int i = 0; i < n; i++) {
+        if (ids[i] < 0 || ids[i] >= s->pool->n_blocks || s->pool->used[ids[i]]) return -1;
+        s->pool->used[ids[i]] = 1;
+        s->table[i] = ids[i];
+    }
+    s->n_table = n;
+    s->n_given = n;
+    return 0;
+}
+
+int orc_session_pos(const orc_session* s) { return s->pos; }
+
+int orc_session_truncate(orc_session* s, int n_pos)
+{
+    if (n_pos < 0 || n_pos > s->pos) return -1;
+    s->pos = n_pos;
+    return 0;
+}
+
+/* make room for positions [0, end): take the lowest free pool blocks */
+static int reserve(orc_session* s, int end)
+{
+    if (end > s->max_ctx) return -1;
+    if (!s->pool) return 0;
+    int need = (end + ORC_BLOCK - 1) / ORC_BLOCK;
+    while (s->n_table < need) {
+        int b = 0;
+        while (b < s->pool->n_blocks && s->pool->used[b]) b++;
+        if (b == s->pool->n_blocks) return -1;
+        s->pool->used[b] = 1;
+        s->table[s->n_table++] = b;
+    }
+    return 0;
+}
+
+/* address of the K (or V) row of position p in layer l */
+static uint16_t* kv_slot(orc_session* s, int l, int p, int is_v)
+{
+    const orc_cfg* c = &s->m->c;
+    if (!s->pool) {
+        uint16_t* base = is_v ? s->v : s->k;
+        return base + ((long)l * s->max_ctx + p) * kv_row(c);
+    }
+    uint16_t* base = is_v ? s->pool->v : s->pool->k;
+    long blk = s->table[p / ORC_BLOCK];
+    return base + (((long)l * s->pool->n_blocks + blk) * ORC_BLOCK + p % ORC_BLOCK) * kv_row(c);
+}
+
+/* ---- one round over a set of rows (one or more sessions) ---- */
+
+typedef struct {
+    orc_session* const* S;
+    const int* row_sess;     /* session of each row */
+    const int* row_pos;      /* absolute position of each row */
+    const float* q;          /* [T][n_q d] */
+    float* att;              /* [T][n_q d] */
+    int layer;
+} attn_job;
+
+static void attn_rows(void* a, long t0, long t1)
+{
+    attn_job* j = (attn_job*)a;
+    for (long t = t0; t < t1; t++) {
+        orc_session* s = j->S[j->row_sess[t]];
+        const orc_cfg* c = &s->m->c;
+        int ctx = j->row_pos[t] + 1;               /* causal: positions 0..pos */
+        long kvr = kv_row(c);
+        uint16_t* K = (uint16_t*)malloc(sizeof(uint16_t) * ctx * kvr);
+        uint16_t* V = (uint16_t*)malloc(sizeof(uint16_t) * ctx * kvr);
+        for (int p = 0; p < ctx; p++) {            /* gather through the layout */
+            memcpy(K + p * kvr, kv_slot(s, j->layer, p, 0), sizeof(uint16_t) * kvr);
+            memcpy(V + p * kvr, kv_slot(s, j->layer, p, 1), sizeof(uint16_t) * kvr);
+        }
+        long qw = (long)c->n_q_heads * c->head_dim;
+        orc_gqa_attend(j->q + t * qw, K, V, ctx, c->n_q_heads, c->n_kv_heads,
+                       c->head_dim, j->att + t * qw);
+        free(K);
+        free(V);
+    }
+}
+
+static int eval_rows(orc_session* const* S, const int32_t* const* toks, const int* n,
+                     int ns, float* logits_last, float* logits_all)
+{
+    orc_model* m = S[0]->m;
+    const orc_cfg* c = &m->c;
+    const int H = c->hidden, F = c->ffn, d = c->head_dim;
+    const int QW = c->n_q_heads * d, KW = c->n_kv_heads * d;
+    int T = 0;
+    for (int b = 0; b < ns; b++) {
+        if (S[b]->m != m || n[b] < 1) return -1;
+        for (int i = 0; i < n[b]; i++)
+            if (toks[b][i] < 0 || toks[b][i] >= c->vocab) return -1;
+        if (reserve(S[b], S[b]->pos + n[b])) return -1;
+        T += n[b];
+    }
+    int* row_sess = (int*)malloc(sizeof(int) * T);
+    int* row_pos = (int*)malloc(sizeof(int) * T);
+    int* row_tok = (int*)malloc(sizeof(int) * T);
+    for (int b = 0, t = 0; b < ns; b++)
+        for (int i = 0; i < n[b]; i++, t++) {
+            row_sess[t] = b;
+            row_pos[t] = S[b]->pos + i;
+            row_tok[t] = toks[b][i];
+        }
+
+    float* x = (float*)malloc(sizeof(float) * (long)T * H);
+    float* h = (float*)malloc(sizeof(float) * (long)T * H);
+    float* y = (float*)malloc(sizeof(float) * (long)T * H);
+    float* q = (float*)malloc(sizeof(float) * (long)T * QW);
+    float* k = (float*)malloc(sizeof(float) * (long)T * KW);
+    float* v = (float*)malloc(sizeof(float) * (long)T * KW);
+    float* att = (float*)malloc(sizeof(float) * (long)T * QW);
+    float* g = (float*)malloc(sizeof(float) * (long)T * F);
+    float* u = (float*)malloc(sizeof(float) * (long)T * F);
+
+    /* token embedding: x = f32(E[token]) */
+    for (int t = 0; t < T; t++)
+        for (int i = 0; i < H; i++)
+            x[(long)t * H + i] = orc_bf16_to_f32(m->embed[(long)row_tok[t] * H + i]);
+
+    for (int l = 0; l < c->n_layers; l++) {
+        const orc_layer* W = &m->layers[l];
+        /* attention block */
+        for (int t = 0; t < T; t++)
+            orc_rmsnorm(x + (long)t * H, W->attn_norm, H, c->rms_eps, h + (long)t * H);
+        orc_matmul(W->wq, c->scheme, QW, H, h, T, q, m->n_threads);
+        orc_matmul(W->wk, c->scheme, KW, H, h, T, k, m->n_threads);
+        orc_matmul(W->wv, c->scheme, KW, H, h, T, v, m->n_threads);
+        for (int t = 0; t < T; t++) {
+            for (int hh = 0; hh < c->n_q_heads; hh++) {   /* q-norm, then RoPE */
+                float* qh = q + (long)t * QW + (long)hh * d;
+                orc_rmsnorm(qh, W->q_norm, d, c->rms_eps, qh);
+                orc_rope(qh, d, row_pos[t], c->rope_theta);
+            }
+            for (int hh = 0; hh < c->n_kv_heads; hh++) {  /* k-norm, then RoPE */
+                float* kh = k + (long)t * KW + (long)hh * d;
+                orc_rmsnorm(kh, W->k_norm, d, c->rms_eps, kh);
+                orc_rope(kh, d, row_pos[t], c->rope_theta);
+            }
+            /* store K and V rounded to bf16 (the KV storage contract) */
+            uint16_t* ks = kv_slot(S[row_sess[t]], l, row_pos[t], 0);
+            uint16_t* vs = kv_slot(S[row_sess[t]], l, row_pos[t], 1);
+            for (int i = 0; i < KW; i++) {
+                ks[i] = orc_f32_to_bf16(k[(long)t * KW + i]);
+                vs[i] = orc_f32_to_bf16(v[(long)t * KW + i]);
+            }
+        }
+        attn_job aj = { S, row_sess, row_pos, q, att, l };
+        parallel_for(T, m->n_threads, attn_rows, &aj);
+        orc_matmul(W->wo, c->scheme, H, QW, att, T, y, m->n_threads);
+        for (long i = 0; i < (long)T * H; i++) x[i] = x[i] + y[i];
+
+        /* FFN block: x += down(silu(gate(h)) * up(h)) */
+        for (int t = 0; t < T; t++)
+            orc_rmsnorm(x + (long)t * H, W->ffn_norm, H, c->rms_eps, h + (long)t * H);
+        orc_matmul(W->wg, c->scheme, F, H, h, T, g, m->n_threads);
+        orc_matmul(W->wu, c->scheme, F, H, h, T, u, m->n_threads);
+        for (long i = 0; i < (long)T * F; i++)
+            g[i] = (float)((double)orc_silu(g[i]) * (double)u[i]);
+        orc_matmul(W->wd, c->scheme, H, F, g, T, y, m->n_threads);
+        for (long i = 0; i < (long)T * H; i++) x[i] = x[i] + y[i];
+    }
+
+    /* final norm and lm_head on the requested rows */
+    for (int b = 0, t0 = 0; b < ns; t0 += n[b], b++) {
+        int r0 = logits_all ? t0 : t0 + n[b] - 1;
+        int nr = t0 + n[b] - r0;
+        for (int t = r0; t < r0 + nr; t++)
+            orc_rmsnorm(x + (long)t * H, m->final_norm, H, c->rms_eps, h + (long)(t - r0) * H);
+        float* out = (float*)malloc(sizeof(float) * (long)nr * c->vocab);
+        orc_matmul(m->lm_head, ORC_BF16, c->vocab, H, h, nr, out, m->n_threads);
+        if (logits_all)
+            memcpy(logits_all + (long)t0 * c->vocab, out, sizeof(float) * (long)nr * c->vocab);
+        if (logits_last)
+            memcpy(logits_last + (long)b * c->vocab, out + (long)(nr - 1) * c->vocab,
+                   sizeof(float) * c->vocab);
+        free(out);
+    }
+    for (int b = 0; b < ns; b++) S[b]->pos += n[b];
+
+    free(x); free(h); free(y); free(q); free(k); free(v); free(att); free(g); free(u);
+    free(row_sess); free(row_pos); free(row_tok);
+    return 0;
+}
+
+int orc_eval(orc_session* s, const int32_t* tokens, int n, float* logits_last,
+             float* logits_all)
+{
+    return eval_rows(&s, &tokens, &n, 1, logits_last, logits_all);
+}
+
+int orc_eval_batch(orc_session* const* s, const int32_t* const* tokens,
+                   const int* n, int ns, float* logits)
+{
+    for (int a = 0; a < ns; a++)
+        for (int b = 0; b < a; b++)
+            if (s[a] == s[b]) return -1;
+    return eval_rows(s, tokens, n, ns, logits, NULL);
+}

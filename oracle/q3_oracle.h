@@ -1,0 +1,124 @@
+/*
+ * q3_oracle.h -- plain CPU oracle for the token-round forward of a dense
+ * Qwen3-style decoder.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg use this library.  It shares no code, header, table or
+ * helper with the CUDA path under qwen3_dense_decoder_gb300/csrc.
+ *
+ * What it follows (Kipp pages):
+ *  - "Kipp Model Support", section "The registry": dense Qwen3 decoders,
+ *    8 KV heads, head width 128, RMS epsilon 1e-6, per-checkpoint RoPE theta
+ *    and embedding tying.
+ *  - "Kipp Model Support", section "qwen3-0.6b-base": K/V are stored in BF16
+ *    (the "storage contract"); attention width may exceed the hidden width.
+ *  - "Kipp Model Support", section "Quantization (Q8_0)": the seven per-layer
+ *    projections in 32-weight blocks of fp16 scale + int8 quants; embedding,
+ *    lm_head and all norms stay BF16.
+ *  - "Kipp Roadmap", status v0.0.2: paged KV through a per-session
+ *    32-position block table, bitwise equal to the contiguous layout;
+ *    batched evaluation equal to isolated evaluation.
+ *  - "Reproducing Kipp", section "Model-backed CPU and Metal gates": cached
+ *    decode must equal recomputation; the CPU oracle is FP32.
+ * The layer math itself is not printed on the pages; the oracle takes the
+ * plain reading of a standard dense Qwen3 decoder (pre-norm RMSNorm blocks,
+ * per-head q/k RMSNorm before rotate-half RoPE, causal GQA softmax attention,
+ * SwiGLU FFN, no biases).
+ *
+ * Precision: activations are stored in FP32; every dot product, mean square
+ * and softmax sum accumulates in FP64 and is rounded to FP32 when stored;
+ * RoPE angles and their cos/sin are evaluated in FP64.
+ */
+#ifndef Q3_ORACLE_H
+#define Q3_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_BF16 = 0, ORC_Q8_0 = 1 };
+enum { ORC_BLOCK = 32 };          /* KV positions per block, Q8_0 weights per block */
+enum { ORC_Q8_0_BYTES = 34 };     /* fp16 scale + 32 int8 quants */
+
+typedef struct orc_cfg {
+    int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+    int tied;     /* 1: lm_head is the token embedding */
+    int scheme;   /* ORC_BF16 or ORC_Q8_0 (the seven projections only) */
+    double rope_theta, rms_eps;
+} orc_cfg;
+
+/* Per-layer weights, host memory, row-major [out][in].  BF16 tensors are
+ * uint16 bit patterns.  With ORC_Q8_0 the seven projections point at
+ * canonical blocks: [out][in/32] records of 34 bytes (little-endian fp16
+ * scale, then 32 int8 quants). */
+typedef struct orc_layer {
+    const uint16_t *attn_norm, *q_norm, *k_norm, *ffn_norm;
+    const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
+} orc_layer;
+
+typedef struct orc_model orc_model;
+typedef struct orc_pool orc_pool;
+typedef struct orc_session orc_session;
+
+/* ---- scalar conversions ---- */
+float    orc_bf16_to_f32(uint16_t b);
+uint16_t orc_f32_to_bf16(float f);              /* round to nearest even */
+float    orc_f16_to_f32(uint16_t h);
+uint16_t orc_f32_to_f16(float f);               /* round to nearest even */
+
+/* ---- Q8_0 ---- */
+/* w: n floats (n % 32 == 0) -> n/32 canonical blocks. */
+void orc_q8_0_pack(const float* w, long n, uint8_t* blocks);
+void orc_q8_0_unpack(const uint8_t* blocks, long n, float* w);
+
+/* ---- components (exported so the tests can pin each one) ---- */
+void  orc_rmsnorm(const float* x, const uint16_t* gain, int n, double eps, float* y);
+void  orc_rope(float* v, int head_dim, int pos, double theta);       /* in place */
+float orc_silu(float z);
+/* y[t][o] = sum_i W[o][i] * x[t][i]; W bf16 (scheme 0) or Q8_0 blocks (1). */
+void  orc_matmul(const void* W, int scheme, int n_out, int n_in,
+                 const float* x, int n_tok, float* y, int n_threads);
+/* One query row of GQA attention over ctx cached positions.
+ * q: [n_q][d] f32; K, V: [ctx][n_kv][d] bf16; o: [n_q][d]. */
+void  orc_gqa_attend(const float* q, const uint16_t* K, const uint16_t* V,
+                     int ctx, int n_q, int n_kv, int d, float* o);
+
+/* ---- model / KV / sessions ---- */
+orc_model* orc_model_create(const orc_cfg* cfg, const uint16_t* embed,
+                            const uint16_t* final_norm, const uint16_t* lm_head,
+                            const orc_layer* layers, int n_threads);
+void orc_model_free(orc_model* m);
+
+/* A pool of 32-position KV blocks shared by paged sessions. */
+orc_pool* orc_pool_create(orc_model* m, int n_blocks);
+void orc_pool_free(orc_pool* p);
+
+/* pool == NULL: contiguous per-session KV of max_ctx positions.
+ * pool != NULL: paged KV; blocks come from the pool in order unless a
+ * table is set with orc_session_set_block_table. */
+orc_session* orc_session_create(orc_model* m, orc_pool* pool, int max_ctx);
+void orc_session_free(orc_session* s);
+int  orc_session_set_block_table(orc_session* s, const int32_t* ids, int n);
+int  orc_session_pos(const orc_session* s);
+int  orc_session_truncate(orc_session* s, int n_pos);
+
+/* One round of n tokens appended at the session's position.  logits_last:
+ * [vocab] logits of the round's last token (may be NULL).  logits_all:
+ * [n][vocab] logits of every row (may be NULL).  Returns 0 or -1. */
+int orc_eval(orc_session* s, const int32_t* tokens, int n,
+             float* logits_last, float* logits_all);
+
+/* One round over several sessions, processed layer by layer over all rows
+ * at once.  logits: [ns][vocab], the last row of each session's round. */
+int orc_eval_batch(orc_session* const* s, const int32_t* const* tokens,
+                   const int* n, int ns, float* logits);
+
+/* argmax with the lowest index on ties */
+int orc_argmax(const float* v, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,210 @@
+"""Whole-forward pins of the oracle.
+
+- Brute force on tiny shapes: an independent float64 NumPy statement with no
+  cache and a materialised causal score matrix must agree with the oracle.
+- The gates the Kipp pages fix: cached decode equals no-cache recomputation at
+  every position ("Reproducing Kipp", section "Model-backed CPU and Metal
+  gates"; "Kipp Model Support", section "What the gates check", Phase 2); the
+  paged layout is bitwise equal to the contiguous one under permuted block
+  tables and batched evaluation equals isolated evaluation ("Kipp Roadmap",
+  status v0.0.2); truncate/resume replays ("Kipp Model Support", Phase 3).
+- Invariants: the split of a prompt into rounds does not change the result,
+  and logits never depend on later tokens (causality).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from synthetic import BF16, Q8_0, Shape, make_block_permutation, make_tokens, make_weights
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_facts.json")))
+
+TINY = Shape("oracle-tiny", 2, 64, 4, 2, 16, 96, 128, True, rope_theta=1e4)
+TINY_UNTIED = TINY.replace(name="oracle-tiny-untied", tied=False, n_layers=1)
+TINY_Q8 = TINY.replace(name="oracle-tiny-q8", scheme=Q8_0, tied=False)
+
+
+def _model(orc, shape, seed=7, threads=2):
+    w = make_weights(shape, seed=seed)
+    return orc.Model(shape, w, n_threads=threads), w
+
+
+def _bf16r(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def brute_force_logits(shape, w, tokens, weights64=None):
+    """float64 statement of the forward with no cache: every row's logits."""
+    f = (lambda t: t.double().numpy()) if weights64 is None else weights64
+    eps, d = shape.rms_eps, shape.head_dim
+    T = len(tokens)
+    x = w["embed"].double().numpy()[np.asarray(tokens)]
+
+    def rms(v, g):
+        return v / np.sqrt((v * v).mean(-1, keepdims=True) + eps) * g
+
+    inv = shape.rope_theta ** (-np.arange(0, d, 2) / d)
+    ang = np.arange(T)[:, None] * inv[None, :]
+    cos, sin = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+
+    def rope(v):
+        a, b = v[..., : d // 2], v[..., d // 2:]
+        return np.concatenate([a * cos - b * sin, b * cos + a * sin], -1)
+
+    group = shape.n_q_heads // shape.n_kv_heads
+    causal = np.triu(np.ones((T, T), bool), 1)
+    for lw in w["layers"]:
+        g = {k: lw[k].double().numpy() for k in ("attn_norm", "q_norm", "k_norm", "ffn_norm")}
+        W = {k: f(lw[k]) for k in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")}
+        h = rms(x, g["attn_norm"])
+        q = (h @ W["wq"].T).reshape(T, shape.n_q_heads, d)
+        k = (h @ W["wk"].T).reshape(T, shape.n_kv_heads, d)
+        v = (h @ W["wv"].T).reshape(T, shape.n_kv_heads, d)
+        q = rope(rms(q, g["q_norm"]))
+        k = _bf16r(rope(rms(k, g["k_norm"])))
+        v = _bf16r(v)
+        k = np.repeat(k, group, axis=1)
+        v = np.repeat(v, group, axis=1)
+        s = np.einsum("thd,shd->hts", q, k) / math.sqrt(d)
+        s[:, causal] = -np.inf
+        p = np.exp(s - s.max(-1, keepdims=True))
+        p /= p.sum(-1, keepdims=True)
+        o = np.einsum("hts,shd->thd", p, v).reshape(T, -1)
+        x = x + o @ W["wo"].T
+        h = rms(x, g["ffn_norm"])
+        a = h @ W["w_gate"].T
+        x = x + (a / (1 + np.exp(-a)) * (h @ W["w_up"].T)) @ W["w_down"].T
+    U = w["embed"] if shape.tied else w["lm_head"]
+    return rms(x, w["final_norm"].double().numpy()) @ U.double().numpy().T
+
+
+def _nmse(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(((a - b) ** 2).sum() / (b ** 2).sum())
+
+
+@pytest.mark.parametrize("shape", [TINY, TINY_UNTIED], ids=lambda s: s.name)
+def test_brute_force_agrees(orc, shape):
+    m, w = _model(orc, shape)
+    toks = make_tokens(11, shape.vocab, seed=5)
+    got = m.session(max_ctx=64).eval(toks, all_rows=True)
+    ref = brute_force_logits(shape, w, toks)
+    for t in range(len(toks)):
+        assert _nmse(got[t], ref[t]) < 1e-10, t
+        assert int(np.argmax(got[t])) == int(np.argmax(ref[t]))
+
+
+def test_brute_force_agrees_q8_0(orc):
+    m, w = _model(orc, TINY_Q8)
+    toks = make_tokens(9, TINY_Q8.vocab, seed=6)
+    got = m.session(max_ctx=64).eval(toks, all_rows=True)
+    li = iter(range(10 ** 6))
+    deq = {}
+    for l, lw in enumerate(w["layers"]):
+        for name in orc.Model.PROJ:
+            deq[id(lw[name])] = orc.q8_0_unpack(m.q8_blocks[l][name], lw[name].shape[1]) \
+                .astype(np.float64)
+    ref = brute_force_logits(TINY_Q8, w, toks, weights64=lambda t: deq[id(t)])
+    del li
+    for t in range(len(toks)):
+        assert _nmse(got[t], ref[t]) < 1e-10
+
+
+def test_cached_decode_equals_recompute(orc):
+    tol = GOLD["nmse_cached_vs_recompute"]["value"]
+    m, _ = _model(orc, TINY)
+    toks = make_tokens(40, TINY.vocab, seed=8)
+    full = m.session(max_ctx=64).eval(toks, all_rows=True)      # one round, no reuse
+    s = m.session(max_ctx=64)
+    s.eval(toks[:8])
+    for t in range(8, 40):                                      # token by token from the cache
+        got = s.eval(toks[t:t + 1])
+        assert _nmse(got, full[t]) <= tol
+        np.testing.assert_array_equal(got, full[t])             # the oracle is exact here
+    assert s.pos == 40
+
+
+def test_paged_equals_contiguous_under_permuted_tables(orc):
+    m, _ = _model(orc, TINY)
+    toks = make_tokens(100, TINY.vocab, seed=9)
+    ref = m.session(max_ctx=128).eval(toks, all_rows=True)
+    for seed in (1, 2):
+        pool = m.pool(16)
+        s = m.session(pool=pool, max_ctx=128)
+        s.set_block_table(make_block_permutation(16, seed)[:4])
+        got = np.concatenate([s.eval(toks[:37], all_rows=True), s.eval(toks[37:38], all_rows=True),
+                              s.eval(toks[38:], all_rows=True)])
+        np.testing.assert_array_equal(got, ref)
+
+
+def test_batched_equals_isolated(orc):
+    m, _ = _model(orc, TINY)
+    pool = m.pool(32)
+    prompts = [make_tokens(n, TINY.vocab, seed=20 + n) for n in (5, 33, 12)]
+    iso = []
+    for p in prompts:
+        s = m.session(max_ctx=128)
+        iso.append([s.eval(p[:-1]), s.eval(p[-1:])])
+    sess = [m.session(pool=pool, max_ctx=128) for _ in prompts]
+    a = m.eval_batch(sess, [p[:-1] for p in prompts])
+    b = m.eval_batch(sess, [p[-1:] for p in prompts])
+    for i in range(3):
+        np.testing.assert_array_equal(a[i], iso[i][0])
+        np.testing.assert_array_equal(b[i], iso[i][1])
+
+
+def test_chunking_and_causality(orc):
+    m, _ = _model(orc, TINY)
+    toks = make_tokens(50, TINY.vocab, seed=10)
+    one = m.session(max_ctx=64).eval(toks, all_rows=True)
+    s = m.session(max_ctx=64)
+    parts = [s.eval(toks[a:b], all_rows=True) for a, b in ((0, 5), (5, 45), (45, 50))]
+    np.testing.assert_array_equal(np.concatenate(parts), one)
+    toks2 = toks.copy()
+    toks2[30:] = (toks2[30:] + 1) % TINY.vocab                  # change only later tokens
+    two = m.session(max_ctx=64).eval(toks2, all_rows=True)
+    np.testing.assert_array_equal(two[:30], one[:30])
+    assert not np.array_equal(two[30], one[30])
+
+
+def test_truncate_and_resume(orc):
+    m, _ = _model(orc, TINY)
+    toks = make_tokens(30, TINY.vocab, seed=11)
+    s = m.session(max_ctx=64)
+    ref = s.eval(toks, all_rows=True)
+    s.truncate(12)
+    assert s.pos == 12
+    np.testing.assert_array_equal(s.eval(toks[12:20], all_rows=True), ref[12:20])
+
+
+def test_capacity_errors(orc):
+    m, _ = _model(orc, TINY)
+    s = m.session(max_ctx=16)
+    with pytest.raises(RuntimeError):
+        s.eval(make_tokens(17, TINY.vocab, seed=1))
+    with pytest.raises(RuntimeError):
+        s.eval(np.array([TINY.vocab], np.int32))
+    pool = m.pool(1)
+    s = m.session(pool=pool, max_ctx=128)
+    s.eval(make_tokens(32, TINY.vocab, seed=2))
+    with pytest.raises(RuntimeError):
+        s.eval(make_tokens(1, TINY.vocab, seed=3))
+
+
+def test_shapes_follow_the_registry(orc):
+    import synthetic
+    for key in ("0.6b", "4b", "8b-q8_0", "14b"):
+        s = synthetic.SHAPES[key]
+        assert s.vocab == GOLD["vocab"]["value"]
+        assert s.n_kv_heads == GOLD["n_kv_heads"]["value"]
+        assert s.head_dim == GOLD["head_dim"]["value"]
+        assert s.rms_eps == GOLD["rms_eps"]["value"]
+    s = synthetic.SHAPES["0.6b"]
+    assert (s.q_width, s.hidden) == (GOLD["attn_width_0p6b"]["value"], GOLD["attn_width_0p6b"]["hidden"])
+    assert 34 * 8 / 32 == GOLD["q8_0"]["bits_per_weight"] and orc.Q8_0_BYTES == 34
+    assert orc.BLOCK == GOLD["kv_block_positions"]["value"]
+    assert BF16 == 0
