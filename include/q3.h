@@ -1,0 +1,212 @@
+/*
+ * q3.h -- C ABI of the GB300 (sm_103a) forward of a dense Qwen3-style decoder.
+ *
+ * The forward is the token round of the Kipp engine's dense Qwen3 path:
+ * RMSNorm (eps from the config, 1e-6 for the family), the seven per-layer
+ * projections over BF16 or Q8_0 weights with FP32 accumulation, per-head q/k
+ * RMSNorm and RoPE, GQA attention over a paged BF16 KV cache addressed through
+ * 32-position block tables, SwiGLU, and full-vocabulary FP32 lm_head logits
+ * with the greedy argmax.  It serves prefill rounds and batched decode.
+ *
+ * Sources on the Kipp pages:
+ *  - "Kipp Model Support", section "The registry": 8 KV heads, head width
+ *    128, vocabulary 151,936, RMS epsilon 1e-6, per-checkpoint dimensions,
+ *    RoPE theta and embedding tying (tied: lm_head is the token embedding).
+ *  - "Kipp Model Support", section "Quantization (Q8_0)": the seven
+ *    projections in 32-weight blocks (fp16 scale + int8 quants); embedding,
+ *    lm_head and norms stay BF16.
+ *  - "Kipp Model Support", section "qwen3-0.6b-base": K and V are stored as
+ *    BF16 (the KV storage contract).
+ *  - "Kipp Roadmap", status v0.0.2: multi-session evaluation (kipp_eval_batch),
+ *    paged KV through a per-session 32-position block table; status v0.0.3:
+ *    one model-owned pool of 32-token blocks shared by sessions; status
+ *    v0.0.4: activation scratch is one per model.
+ *  - "Kipp Model Support", section "What the gates check": truncate/resume,
+ *    batched evaluation; section "CUDA (NVIDIA H100 80GB ...)": weights are
+ *    resident in device memory, stateless prefill and reset/reuse; a backend
+ *    failure is fatal with no fallback ("Reproducing Kipp", section "Build";
+ *    "Kipp Model Support", section "Backends").
+ *
+ * Conventions
+ *  - Every pointer named *_dev is device memory on the model's device; every
+ *    other pointer is host memory.
+ *  - All calls are asynchronous on the model's CUDA stream except q3_sync,
+ *    the create/destroy calls and the error queries.  Outputs are valid after
+ *    q3_sync (or any later synchronisation of that stream).
+ *  - Return value: Q3_OK (0) or a negative Q3_ERR_* code; q3_last_error()
+ *    gives a message (thread-local).  A CUDA error or a failed device-side
+ *    check poisons the model: every later call on it returns Q3_ERR_POISONED.
+ *  - Calls on one model are not thread-safe; use one host thread per model.
+ */
+#ifndef Q3_H
+#define Q3_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q3_OK 0
+#define Q3_ERR_INVALID_ARG (-1)
+#define Q3_ERR_UNSUPPORTED_DEVICE (-2) /* not an sm_103 device */
+#define Q3_ERR_OOM (-3)                /* device allocation failed */
+#define Q3_ERR_POOL_EXHAUSTED (-4)     /* no free KV block */
+#define Q3_ERR_CTX_OVERFLOW (-5)       /* round would pass the model's max_ctx */
+#define Q3_ERR_CUDA (-6)               /* a CUDA call failed; model poisoned */
+#define Q3_ERR_DEVICE_CHECK (-7)       /* a kernel's own check failed; model poisoned */
+#define Q3_ERR_POISONED (-8)           /* an earlier error poisoned the model */
+
+#define Q3_BF16 0
+#define Q3_Q8_0 1
+#define Q3_KV_BLOCK 32       /* positions per KV block */
+#define Q3_Q8_0_BLOCK 32     /* weights per Q8_0 block */
+#define Q3_Q8_0_BYTES 34     /* bytes per canonical Q8_0 block */
+
+/* Device status-word bits (q3_sync reports them as Q3_ERR_DEVICE_CHECK). */
+#define Q3_STATUS_TOKEN_RANGE 0x1   /* a token id outside [0, vocab) */
+#define Q3_STATUS_BLOCK_RANGE 0x2   /* a block-table entry outside the pool */
+#define Q3_STATUS_TIMEOUT 0x4       /* a bounded device wait ran out */
+
+typedef struct q3_model q3_model;
+typedef struct q3_pool q3_pool;
+typedef struct q3_session q3_session;
+
+/* Shape of the decoder.  head_dim must be 128, n_q_heads a multiple of
+ * n_kv_heads (GQA group of at most 8), hidden, ffn, vocab and
+ * n_q_heads*head_dim multiples of 128.  max_ctx bounds a session's length
+ * (the RoPE table is built for it).  scheme: Q3_BF16 or Q3_Q8_0 (the seven
+ * projections only).  tied: 1 when lm_head is the token embedding. */
+typedef struct q3_config {
+    int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, max_ctx;
+    float rope_theta, rms_eps;
+    int tied;
+    int scheme;
+} q3_config;
+
+/* Device pointers of one layer.  Norm gains are bf16 [hidden] (attn_norm,
+ * ffn_norm) or [head_dim] (q_norm, k_norm).  Projections are row-major
+ * [out][in] (the nn.Linear layout): wq [n_q*d][hidden], wk and wv
+ * [n_kv*d][hidden], wo [hidden][n_q*d], w_gate and w_up [ffn][hidden],
+ * w_down [hidden][ffn].  With Q3_BF16 they are bf16; with Q3_Q8_0 they are
+ * canonical Q8_0 blocks [out][in/32] of 34 bytes (little-endian fp16 scale,
+ * then 32 int8 quants), as q3_quantize_q8_0 writes them. */
+typedef struct q3_layer_weights {
+    const void *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo,
+               *ffn_norm, *w_gate, *w_up, *w_down;
+} q3_layer_weights;
+
+/* embed: bf16 [vocab][hidden]; final_norm: bf16 [hidden]; lm_head: bf16
+ * [vocab][hidden], or NULL when tied; layers: host array of n_layers. */
+typedef struct q3_weights {
+    const void* embed;
+    const void* final_norm;
+    const void* lm_head;
+    const q3_layer_weights* layers;
+} q3_weights;
+
+/* Create a model on the current CUDA device.  The weights are borrowed: the
+ * caller keeps them alive and unchanged until q3_model_destroy.  With Q3_Q8_0
+ * the library derives its own device layout of the projections (an int8
+ * plane and an fp16 scale plane, bit-equal to the canonical blocks) once,
+ * here.  max_round_tokens bounds the rows of one round (the activation
+ * scratch, owned by the model, is sized for it; longer q3_session_eval rounds
+ * are split into chunks of this size).  stream: a cudaStream_t, or NULL for
+ * the legacy default stream.  Errors: Q3_ERR_INVALID_ARG (bad shape or NULL
+ * weight), Q3_ERR_UNSUPPORTED_DEVICE, Q3_ERR_OOM, Q3_ERR_CUDA. */
+int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tokens,
+                    void* stream, q3_model** out);
+void q3_model_destroy(q3_model* m);
+
+/* A pool of n_blocks KV blocks of 32 positions for all layers (BF16 K and
+ * V), owned by the library; up to max_sessions sessions draw from it.  One
+ * block holds n_layers * 2 * n_kv_heads * 32 * head_dim bf16 values.
+ * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_OOM. */
+int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out);
+void q3_pool_destroy(q3_pool* p);   /* after its sessions are destroyed */
+
+/* A session: a position counter and a block table in the pool.  Sessions of
+ * one pool may be evaluated together with q3_eval_batch.
+ * Errors: Q3_ERR_INVALID_ARG (pool full of sessions), Q3_ERR_OOM. */
+int q3_session_create(q3_pool* p, q3_session** out);
+void q3_session_destroy(q3_session* s);   /* returns its blocks to the pool */
+
+/* Fix which pool blocks back the session's first n*32 positions, in order
+ * (block i holds positions [32 i, 32 i + 32)); later positions draw free
+ * blocks as usual.  Only on an empty session (position 0); the ids must be
+ * free and in range.  Errors: Q3_ERR_INVALID_ARG. */
+int q3_session_set_block_table(q3_session* s, const int32_t* phys_ids, int n);
+
+/* One round of n tokens appended to the session at its current position
+ * (prefill when n > 1, a decode step when n == 1).  tokens_dev: int32 [n]
+ * device.  logits_dev: float [vocab] device, receives the FP32 logits of the
+ * round's last token.  argmax_dev: int32 [1] device or NULL, receives the
+ * greedy token (lowest index on ties).  Both may be the tokens_dev of a later
+ * call.  Token ids outside [0, vocab) are reported by q3_sync as
+ * Q3_ERR_DEVICE_CHECK.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CTX_OVERFLOW,
+ * Q3_ERR_POOL_EXHAUSTED, Q3_ERR_CUDA, Q3_ERR_POISONED. */
+int q3_session_eval(q3_session* s, const int32_t* tokens_dev, int n,
+                    float* logits_dev, int32_t* argmax_dev);
+
+/* One round over ns distinct sessions of one pool ("Kipp Roadmap", status
+ * v0.0.2, kipp_eval_batch): session i appends n[i] tokens.  tokens_dev:
+ * int32 device, the rounds concatenated in session order (sum n[i] tokens,
+ * at most max_round_tokens).  n: host int [ns].  logits_dev: float
+ * [ns][vocab] device, the last row of each session's round.  argmax_dev:
+ * int32 [ns] device or NULL.  Errors as q3_session_eval. */
+int q3_eval_batch(q3_session* const* sessions, int ns, const int32_t* tokens_dev,
+                  const int* n, float* logits_dev, int32_t* argmax_dev);
+
+/* Forget positions >= n_pos (truncate/resume); 0 <= n_pos <= position.
+ * Blocks past the new end return to the pool unless fixed by
+ * q3_session_set_block_table.  Errors: Q3_ERR_INVALID_ARG. */
+int q3_session_truncate(q3_session* s, int n_pos);
+/* Back to position 0 (reset/reuse). */
+int q3_session_reset(q3_session* s);
+int q3_session_pos(const q3_session* s);
+
+/* Wait for the model's stream; read and clear the device status word.
+ * Errors: Q3_ERR_CUDA, Q3_ERR_DEVICE_CHECK (both poison), Q3_ERR_POISONED. */
+int q3_sync(q3_model* m);
+
+/* Pack bf16 weights into canonical Q8_0 blocks on the device (the format of
+ * "Kipp Model Support", section "Quantization (Q8_0)"): per block of 32,
+ * d = absmax/127 in FP32, stored as fp16(d) round-to-nearest-even; quants
+ * are round-half-even(w/d) against the FP32 d, clamped to [-127, 127]; an
+ * all-zero block has scale 0 and zero quants.  w_dev: bf16 [n]; blocks_dev:
+ * [n/32][34] bytes; n a multiple of 32.  Asynchronous on stream (a
+ * cudaStream_t or NULL).  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+int q3_quantize_q8_0(const void* w_dev, int64_t n, void* blocks_dev, void* stream);
+
+/* Operator entry points, for per-kernel gates like the pages' operator tests
+ * ("Reproducing Kipp", section "Model-backed CPU and Metal gates":
+ * kipp_test_metal --metal-operators; "Kipp Roadmap", status v0.0.4: the
+ * first operator test of the flash prefill kernel).  They run one kernel of
+ * the forward on caller buffers, asynchronously on stream.
+ *
+ * q3_op_matmul: y[n][m] = sum_k w[m][k] * x[n][k] on the tcgen05 GEMM.
+ * w_dev: bf16 [M][K]; x_dev: bf16 [N][K] with at least round_up(N, 256)
+ * rows allocated (rows past N are read but their products discarded);
+ * y_dev: f32 [N][M].  M a multiple of 128, K a multiple of 64, 1 <= N.
+ * Pointers 16-byte aligned.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, float* y_dev,
+                 void* stream);
+
+/* q3_op_matvec: y[m] = sum_k w[m][k] * x[k] on the decode GEMV.  With
+ * scales_dev == NULL, w_dev is bf16 [M][K]; otherwise w_dev is the int8
+ * quant plane [M][K] and scales_dev the fp16 scale plane [M][K/32] of Q8_0
+ * weights.  x_dev: f32 [K]; y_dev: f32 [M].  M a multiple of 8, K of 32.
+ * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, int M, int K,
+                 float* y_dev, void* stream);
+
+/* Message of the last error on this host thread ("" if none). */
+const char* q3_last_error(void);
+
+/* Number of kernel launches this model has issued (for launch accounting). */
+int64_t q3_model_launch_count(const q3_model* m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,278 @@
+"""Python binding of libq3.so, the sm_103a forward of a dense Qwen3-style decoder.
+
+The binding only marshals arguments: every step of the forward runs in the
+library's CUDA kernels (include/q3.h documents each entry point).  PyTorch is
+used for device memory and streams.  There is no fallback: if the library is
+missing or the device is not an sm_103 GPU, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libq3.so")
+
+BF16, Q8_0 = 0, 1
+KV_BLOCK = 32
+Q8_0_BYTES = 34
+ERRORS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_DEVICE", -3: "OOM", -4: "POOL_EXHAUSTED",
+          -5: "CTX_OVERFLOW", -6: "CUDA", -7: "DEVICE_CHECK", -8: "POISONED"}
+
+PROJ = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+class Q3Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class _Config(C.Structure):
+    _fields_ = [("n_layers", C.c_int), ("hidden", C.c_int), ("n_q_heads", C.c_int),
+                ("n_kv_heads", C.c_int), ("head_dim", C.c_int), ("ffn", C.c_int),
+                ("vocab", C.c_int), ("max_ctx", C.c_int), ("rope_theta", C.c_float),
+                ("rms_eps", C.c_float), ("tied", C.c_int), ("scheme", C.c_int)]
+
+
+class _LayerW(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo",
+                                         "ffn_norm", "w_gate", "w_up", "w_down")]
+
+
+class _Weights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("final_norm", C.c_void_p), ("lm_head", C.c_void_p),
+                ("layers", C.POINTER(_LayerW))]
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def lib():
+    """The loaded libq3.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "qwen3_dense_decoder_gb300.build() (nvcc, sm_103a)")
+        L = C.CDLL(LIB_PATH)
+        vp, i, i64 = C.c_void_p, C.c_int, C.c_int64
+        L.q3_last_error.restype = C.c_char_p
+        L.q3_model_create.argtypes = [C.POINTER(_Config), C.POINTER(_Weights), i, vp, C.POINTER(vp)]
+        L.q3_model_destroy.argtypes = [vp]
+        L.q3_pool_create.argtypes = [vp, i, i, C.POINTER(vp)]
+        L.q3_pool_destroy.argtypes = [vp]
+        L.q3_session_create.argtypes = [vp, C.POINTER(vp)]
+        L.q3_session_destroy.argtypes = [vp]
+        L.q3_session_set_block_table.argtypes = [vp, vp, i]
+        L.q3_session_eval.argtypes = [vp, vp, i, vp, vp]
+        L.q3_eval_batch.argtypes = [vp, i, vp, vp, vp, vp]
+        L.q3_session_truncate.argtypes = [vp, i]
+        L.q3_session_reset.argtypes = [vp]
+        L.q3_session_pos.argtypes = [vp]
+        L.q3_sync.argtypes = [vp]
+        L.q3_quantize_q8_0.argtypes = [vp, i64, vp, vp]
+        L.q3_model_launch_count.argtypes = [vp]
+        L.q3_model_launch_count.restype = i64
+        L.q3_op_matmul.argtypes = [vp, vp, i, i, i, vp, vp]
+        L.q3_op_matvec.argtypes = [vp, vp, vp, i, i, vp, vp]
+        _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise Q3Error(rc, lib().q3_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def quantize_q8_0(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """Pack a bf16 CUDA tensor [..., n] into canonical Q8_0 blocks (uint8 [..., n/32*34])."""
+    assert w.is_cuda and w.dtype == torch.bfloat16 and w.is_contiguous()
+    assert w.shape[-1] % 32 == 0
+    out = torch.empty(w.shape[:-1] + (w.shape[-1] // 32 * Q8_0_BYTES,), dtype=torch.uint8,
+                      device=w.device)
+    _check(lib().q3_quantize_q8_0(_ptr(w), w.numel(), _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def op_matmul(w: torch.Tensor, x: torch.Tensor, n: int, stream=None) -> torch.Tensor:
+    """y[n][m] = sum_k w[m][k] x[n][k] on the tcgen05 GEMM (operator gate).
+    w: bf16 [M, K]; x: bf16 [>= round_up(n, 256), K]."""
+    M, K = w.shape
+    assert x.shape[0] >= (n + 255) // 256 * 256 and x.shape[1] == K
+    y = torch.empty(n, M, dtype=torch.float32, device=w.device)
+    _check(lib().q3_op_matmul(_ptr(w), _ptr(x), M, n, K, _ptr(y), _stream_handle(stream)))
+    return y
+
+
+def op_matvec(w: torch.Tensor, x: torch.Tensor, scales: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """y[m] = sum_k w[m][k] x[k] on the decode GEMV (operator gate).  w: bf16
+    [M, K], or the int8 quant plane with scales the fp16 [M, K/32] plane."""
+    M, K = w.shape
+    y = torch.empty(M, dtype=torch.float32, device=w.device)
+    _check(lib().q3_op_matvec(_ptr(w), _ptr(scales), _ptr(x), M, K, _ptr(y),
+                              _stream_handle(stream)))
+    return y
+
+
+class Model:
+    """A decoder over device weights (synthetic.make_weights() layout).
+
+    weights: {"embed", "final_norm", "lm_head" (None if tied), "layers": [...]};
+    for a Q8_0 shape the seven projections of each layer must be canonical
+    Q8_0 blocks (uint8), e.g. from quantize_q8_0.  The tensors are borrowed
+    and kept referenced by this object.
+    """
+
+    def __init__(self, shape, weights: dict, max_ctx: int, max_round_tokens: int = 2048,
+                 stream=None):
+        self.shape = shape
+        self.stream = stream or torch.cuda.current_stream()
+        self._keep = weights
+        cfg = _Config(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
+                      shape.head_dim, shape.ffn, shape.vocab, max_ctx, shape.rope_theta,
+                      shape.rms_eps, int(shape.tied), shape.scheme)
+        layers = (_LayerW * shape.n_layers)()
+        for li, lw in enumerate(weights["layers"]):
+            for name in ("attn_norm", "q_norm", "k_norm", "ffn_norm") + PROJ:
+                t = lw[name]
+                assert t.is_cuda and t.is_contiguous(), name
+                setattr(layers[li], name, t.data_ptr())
+        self._layers = layers
+        lm = weights.get("lm_head")
+        w = _Weights(weights["embed"].data_ptr(), weights["final_norm"].data_ptr(),
+                     lm.data_ptr() if lm is not None else None, layers)
+        h = C.c_void_p()
+        _check(lib().q3_model_create(C.byref(cfg), C.byref(w), max_round_tokens,
+                                     _stream_handle(self.stream), C.byref(h)))
+        self.h = h
+        self.max_ctx = max_ctx
+        self.max_round_tokens = max_round_tokens
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().q3_model_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def pool(self, n_blocks: int, max_sessions: int = 64) -> "Pool":
+        return Pool(self, n_blocks, max_sessions)
+
+    def sync(self) -> None:
+        _check(lib().q3_sync(self.h))
+
+    @property
+    def launch_count(self) -> int:
+        return lib().q3_model_launch_count(self.h)
+
+    def eval_batch(self, sessions, tokens: torch.Tensor, n, logits: torch.Tensor,
+                   argmax: torch.Tensor | None = None) -> None:
+        """One round over several sessions: tokens (int32, device) concatenated
+        in session order; logits [ns, vocab] f32 device; argmax [ns] int32."""
+        ns = len(sessions)
+        hs = (C.c_void_p * ns)(*[s.h.value for s in sessions])
+        nn = (C.c_int * ns)(*[int(k) for k in n])
+        _check(lib().q3_eval_batch(hs, ns, _ptr(tokens), nn, _ptr(logits), _ptr(argmax)))
+
+
+class Pool:
+    def __init__(self, model: Model, n_blocks: int, max_sessions: int):
+        self.model = model
+        h = C.c_void_p()
+        _check(lib().q3_pool_create(model.h, n_blocks, max_sessions, C.byref(h)))
+        self.h = h
+        self.n_blocks = n_blocks
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().q3_pool_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def session(self) -> "Session":
+        return Session(self)
+
+
+class Session:
+    def __init__(self, pool: Pool):
+        self.pool = pool
+        h = C.c_void_p()
+        _check(lib().q3_session_create(pool.h, C.byref(h)))
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().q3_session_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_block_table(self, ids) -> None:
+        import numpy as np
+        a = np.ascontiguousarray(ids, np.int32)
+        _check(lib().q3_session_set_block_table(self.h, a.ctypes.data_as(C.c_void_p), a.size))
+
+    def eval(self, tokens: torch.Tensor, logits: torch.Tensor,
+             argmax: torch.Tensor | None = None) -> None:
+        """Append a round of tokens (int32, device); logits [vocab] f32 device."""
+        assert tokens.is_cuda and tokens.dtype == torch.int32 and tokens.is_contiguous()
+        _check(lib().q3_session_eval(self.h, _ptr(tokens), tokens.numel(), _ptr(logits),
+                                     _ptr(argmax)))
+
+    def truncate(self, n_pos: int) -> None:
+        _check(lib().q3_session_truncate(self.h, n_pos))
+
+    def reset(self) -> None:
+        _check(lib().q3_session_reset(self.h))
+
+    @property
+    def pos(self) -> int:
+        return lib().q3_session_pos(self.h)
+
+
+def device_weights(shape, weights: dict) -> dict:
+    """The weight dict the library takes: bf16 tensors as given; for a Q8_0
+    shape the seven projections packed to canonical blocks by the library's
+    own quantizer (q3_quantize_q8_0)."""
+    if shape.scheme != Q8_0:
+        return weights
+    out = dict(weights)
+    out["layers"] = []
+    for lw in weights["layers"]:
+        d = dict(lw)
+        for name in PROJ:
+            d[name] = quantize_q8_0(lw[name])
+        out["layers"].append(d)
+    return out

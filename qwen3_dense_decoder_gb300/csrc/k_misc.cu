@@ -1,0 +1,336 @@
+// k_misc.cu -- the small kernels of the round: token embedding, RMSNorm to
+// bf16 rows, the fused per-head q/k RMSNorm + RoPE + paged KV append, the
+// vocabulary argmax, and the Q8_0 format kernels.
+//
+// Sources (Kipp pages): "Kipp Model Support", section "The registry" (RMS
+// epsilon, RoPE theta, embedding tying), section "qwen3-0.6b-base" (K/V
+// rounded to BF16 on store), section "Quantization (Q8_0)" (32-weight blocks
+// of fp16 scale + int8 quants); "Kipp Roadmap", status v0.0.2 (32-position
+// block tables).  Layer math not printed on the pages follows the standard
+// dense Qwen3 decoder: RMSNorm x / sqrt(mean(x^2) + eps) * g; q/k norm over
+// each 128-wide head with gains shared by the heads, before RoPE; RoPE in
+// rotate-half pairs (i, i + 64) with angle pos * theta^(-2i/128).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q3 {
+
+namespace {
+
+constexpr int D = 128;
+
+Q3_DEV float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <typename K, typename A>
+cudaError_t launch_ex(const Launch& L, K kern, dim3 grid, dim3 block, const A& args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (L.counter) ++*L.counter;
+    return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+// ---------------------------------------------------------------- embedding
+struct EmbedArgs {
+    const int32_t* tokens;
+    const __nv_bfloat16* E;
+    int H, vocab;
+    float* x;
+    int* status;
+};
+
+__global__ void __launch_bounds__(256) embed_kernel(const EmbedArgs a)
+{
+    grid_dep_wait();
+    const int t = blockIdx.x;
+    int tok = a.tokens[t];
+    if (tok < 0 || tok >= a.vocab) {
+        if (threadIdx.x == 0) set_status(a.status, Q3_STATUS_TOKEN_RANGE);
+        tok = 0;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(a.E + (size_t)tok * a.H);
+    float* dst = a.x + (size_t)t * a.H;
+    for (int c = threadIdx.x; c < a.H / 8; c += blockDim.x) {
+        const uint4 w = __ldg(src + c);
+        float4* o = reinterpret_cast<float4*>(dst + c * 8);
+        o[0] = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+        o[1] = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
+    }
+    grid_dep_launch();
+}
+
+// ---------------------------------------------------------------- RMSNorm -> bf16
+struct NormArgs {
+    const float* x;
+    const int* rows;
+    int H;
+    const __nv_bfloat16* g;
+    float eps;
+    __nv_bfloat16* h;
+};
+
+__global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const NormArgs a)
+{
+    __shared__ float red[8];
+    __shared__ float s_scale;
+    grid_dep_wait();
+    const int r = blockIdx.x;
+    const int src = a.rows ? a.rows[r] : r;
+    const float* x = a.x + (size_t)src * a.H;
+    float ss = 0.f;
+    for (int i = threadIdx.x * 4; i < a.H; i += blockDim.x * 4) {
+        const float4 v = *reinterpret_cast<const float4*>(x + i);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+        s_scale = 1.0f / sqrtf(t / (float)a.H + a.eps);
+    }
+    __syncthreads();
+    const float sc = s_scale;
+    __nv_bfloat16* h = a.h + (size_t)r * a.H;
+    for (int i = threadIdx.x * 2; i < a.H; i += blockDim.x * 2) {
+        const float2 v = *reinterpret_cast<const float2*>(x + i);
+        const float g0 = __bfloat162float(a.g[i]), g1 = __bfloat162float(a.g[i + 1]);
+        *reinterpret_cast<__nv_bfloat162*>(h + i) =
+            __floats2bfloat162_rn(v.x * sc * g0, v.y * sc * g1);
+    }
+    grid_dep_launch();
+}
+
+// ---------------------------------------------------------------- q/k norm + RoPE + KV append
+// One warp per head of one row; lane l holds elements [4l, 4l + 4).  The
+// rotate-half partner of element i < 64 is i + 64, held by lane l ^ 16.
+__global__ void __launch_bounds__(128) qk_norm_rope_append_kernel(const RopeArgs a)
+{
+    grid_dep_wait();
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hh = blockIdx.y * 4 + warp;                // q heads, then k heads, then v heads
+    const int n_heads = a.n_q + 2 * a.n_kv;
+    if (hh >= n_heads) return;
+    const int ld = n_heads * D;
+    const int pos = a.row_pos[t];
+    const float4 v = *reinterpret_cast<const float4*>(a.qkv + (size_t)t * ld + hh * D + lane * 4);
+    float y[4] = {v.x, v.y, v.z, v.w};
+
+    const bool is_q = hh < a.n_q, is_k = !is_q && hh < a.n_q + a.n_kv;
+    if (is_q || is_k) {
+        const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
+        const float r = 1.0f / sqrtf(ss / (float)D + a.eps);
+        const __nv_bfloat16* g = (is_q ? a.q_gain : a.k_gain) + lane * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = y[e] * r * __bfloat162float(g[e]);
+        const float2* cs = a.rope + (size_t)pos * (D / 2) + (lane & 15) * 4;
+        float out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float z = __shfl_xor_sync(0xffffffffu, y[e], 16);
+            const float2 c = cs[e];
+            out[e] = lane < 16 ? y[e] * c.x - z * c.y      // first half: x1 cos - x2 sin
+                               : y[e] * c.x + z * c.y;     // second half: x2 cos + x1 sin
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = out[e];
+    }
+    if (is_q) {
+        *reinterpret_cast<float4*>(a.q_out + ((size_t)t * a.n_q + hh) * D + lane * 4) =
+            make_float4(y[0], y[1], y[2], y[3]);
+        return;
+    }
+    const int slot = a.row_slot[t];
+    const int blk = a.tables[(size_t)slot * a.max_blocks + pos / 32];
+    if (blk < 0 || blk >= a.n_blocks) {
+        if (lane == 0) set_status(a.status, Q3_STATUS_BLOCK_RANGE);
+        return;
+    }
+    const int kvh = is_k ? hh - a.n_q : hh - a.n_q - a.n_kv;
+    __nv_bfloat16* dst = a.kv_layer +
+        (((size_t)blk * 2 + (is_k ? 0 : 1)) * a.n_kv + kvh) * (32 * D) + (size_t)(pos % 32) * D + lane * 4;
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = packed;
+}
+
+// ---------------------------------------------------------------- argmax
+struct ArgmaxArgs {
+    const float* logits;
+    int V;
+    int32_t* out;
+};
+
+// Greedy token: the largest logit, the lowest index on ties.
+__global__ void __launch_bounds__(1024) argmax_kernel(const ArgmaxArgs a)
+{
+    __shared__ float sv[32];
+    __shared__ int si[32];
+    grid_dep_wait();
+    const float* x = a.logits + (size_t)blockIdx.x * a.V;
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = threadIdx.x; i < a.V; i += blockDim.x) {
+        const float v = x[i];
+        if (v > best) { best = v; bi = i; }      // ascending i: first max kept
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+    }
+    if ((threadIdx.x & 31) == 0) { sv[threadIdx.x >> 5] = best; si[threadIdx.x >> 5] = bi; }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        best = sv[threadIdx.x];
+        bi = si[threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+        }
+        if (threadIdx.x == 0) a.out[blockIdx.x] = bi == 0x7fffffff ? 0 : bi;
+    }
+    grid_dep_launch();
+}
+
+// ---------------------------------------------------------------- Q8_0
+// canonical block: bytes 0-1 little-endian fp16 scale, bytes 2-33 int8 quants
+__global__ void q8_split_kernel(const uint8_t* blocks, int64_t nblocks, int8_t* qs, __half* scales)
+{
+    for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblocks;
+         b += (int64_t)gridDim.x * blockDim.x) {
+        const uint8_t* in = blocks + b * Q3_Q8_0_BYTES;
+        const uint16_t bits = (uint16_t)(in[0] | (in[1] << 8));
+        scales[b] = __ushort_as_half(bits);
+        int8_t* o = qs + b * 32;
+        for (int i = 0; i < 32; ++i) o[i] = (int8_t)in[2 + i];
+    }
+}
+
+struct Q8DeqArgs {
+    const int8_t* qs;
+    const __half* scales;
+    int64_t n;
+    __nv_bfloat16* w;
+};
+
+// bf16(fp16 scale * quant) for the tensor-core prefill path
+__global__ void q8_to_bf16_kernel(const Q8DeqArgs a)
+{
+    grid_dep_wait();
+    for (int64_t i = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 8; i < a.n;
+         i += (int64_t)gridDim.x * blockDim.x * 8) {
+        const float d = __half2float(a.scales[i / 32]);
+        const uint2 q = *reinterpret_cast<const uint2*>(a.qs + i);
+        __nv_bfloat16 out[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            out[e] = __float2bfloat16_rn(d * (float)(int8_t)((q.x >> (8 * e)) & 0xff));
+            out[4 + e] = __float2bfloat16_rn(d * (float)(int8_t)((q.y >> (8 * e)) & 0xff));
+        }
+        *reinterpret_cast<uint4*>(a.w + i) = *reinterpret_cast<const uint4*>(out);
+    }
+    grid_dep_launch();
+}
+
+// Per block of 32: d = absmax / 127 (FP32, correctly rounded), scale =
+// fp16(d) round-to-nearest-even, q = round-half-even(w / d) clamped to
+// [-127, 127]; an all-zero block gets scale 0 and zero quants.
+__global__ void quantize_q8_0_kernel(const __nv_bfloat16* w, int64_t nblocks, uint8_t* blocks)
+{
+    for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblocks;
+         b += (int64_t)gridDim.x * blockDim.x) {
+        float x[32];
+        float amax = 0.f;
+        for (int i = 0; i < 32; ++i) {
+            x[i] = __bfloat162float(w[b * 32 + i]);
+            amax = fmaxf(amax, fabsf(x[i]));
+        }
+        const float d = __fdiv_rn(amax, 127.0f);
+        const uint16_t dh = __half_as_ushort(__float2half_rn(d));
+        uint8_t* out = blocks + b * Q3_Q8_0_BYTES;
+        out[0] = (uint8_t)(dh & 0xff);
+        out[1] = (uint8_t)(dh >> 8);
+        for (int i = 0; i < 32; ++i) {
+            int q = 0;
+            if (d != 0.f) {
+                q = __float2int_rn(__fdiv_rn(x[i], d));
+                q = q > 127 ? 127 : (q < -127 ? -127 : q);
+            }
+            out[2 + i] = (uint8_t)(int8_t)q;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const Launch& L, const int32_t* tokens, int T, const __nv_bfloat16* E,
+                         int H, int vocab, float* x, int* status)
+{
+    return launch_ex(L, embed_kernel, dim3(T), dim3(256), EmbedArgs{tokens, E, H, vocab, x, status});
+}
+
+cudaError_t launch_rmsnorm_bf16(const Launch& L, const float* x, const int* rows, int n, int H,
+                                const __nv_bfloat16* g, float eps, __nv_bfloat16* h)
+{
+    return launch_ex(L, rmsnorm_bf16_kernel, dim3(n), dim3(256), NormArgs{x, rows, H, g, eps, h});
+}
+
+cudaError_t launch_qk_norm_rope_append(const Launch& L, const RopeArgs& a)
+{
+    const int heads = a.n_q + 2 * a.n_kv;
+    return launch_ex(L, qk_norm_rope_append_kernel, dim3(a.T, (heads + 3) / 4), dim3(128), a);
+}
+
+cudaError_t launch_argmax(const Launch& L, const float* logits, int rows, int V, int32_t* out)
+{
+    return launch_ex(L, argmax_kernel, dim3(rows), dim3(1024), ArgmaxArgs{logits, V, out});
+}
+
+cudaError_t launch_q8_split(cudaStream_t s, const uint8_t* blocks, int64_t nblocks, int8_t* qs,
+                            __half* scales)
+{
+    int grid = (int)((nblocks + 255) / 256);
+    if (grid > 152 * 32) grid = 152 * 32;
+    q8_split_kernel<<<grid, 256, 0, s>>>(blocks, nblocks, qs, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q8_to_bf16(const Launch& L, const int8_t* qs, const __half* scales, int64_t n,
+                              __nv_bfloat16* w)
+{
+    int64_t grid = (n / 8 + 255) / 256;
+    if (grid > 152 * 32) grid = 152 * 32;
+    return launch_ex(L, q8_to_bf16_kernel, dim3((unsigned)grid), dim3(256), Q8DeqArgs{qs, scales, n, w});
+}
+
+cudaError_t launch_quantize_q8_0(cudaStream_t s, const __nv_bfloat16* w, int64_t n, uint8_t* blocks)
+{
+    const int64_t nb = n / 32;
+    int grid = (int)((nb + 255) / 256);
+    if (grid > 152 * 32) grid = 152 * 32;
+    if (grid < 1) grid = 1;
+    quantize_q8_0_kernel<<<grid, 256, 0, s>>>(w, nb, blocks);
+    return cudaGetLastError();
+}
+
+}  // namespace q3

@@ -1,0 +1,131 @@
+// kernels.h -- host-side launch interface of the sm_103a kernels.
+// Every launcher is asynchronous on the given stream and returns the CUDA
+// launch status.  Shapes are validated by the runtime before these calls.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q3 {
+
+// ---------------------------------------------------------------- launch
+// How a kernel is launched: stream, and whether it may start early under
+// programmatic dependent launch.
+struct Launch {
+    cudaStream_t stream;
+    bool pdl;
+    int64_t* counter;   // incremented per launch
+};
+
+// ---------------------------------------------------------------- GEMM
+// D[M x N] = A[M x K] * B[N x K]^T on tcgen05 tensor cores.  A is the
+// weight matrix (row-major [out][in]); B holds N token rows (bf16
+// [rows][K]).  Output element (n, m) goes to out[n * ldo + m].
+enum Epi : int {
+    EPI_STORE_F32 = 0,   // out = acc (f32)
+    EPI_ADD_F32 = 1,     // out += acc (f32 residual)
+    EPI_STORE_BF16 = 2,  // out = bf16(acc)
+    EPI_SWIGLU_BF16 = 3, // paired gate/up tile: out[n][f] = bf16(silu(g) * u)
+    EPI_SWIGLU_F32 = 4,
+};
+
+struct GemmArgs {
+    int M, N, K;          // M multiple of 128; K multiple of 64
+    int a_tiles0, a_tiles1;  // plain mode: 128-row tiles [0,t0) from map a0, [t0,t1) from a1, rest a2
+    int pair;             // 1: tile t takes rows [64 t, 64 t + 64) of a0 (gate) then of a1 (up)
+    int k_splits;         // > 1: partial sums to ws, then gemm_splitk_reduce
+    int epi;
+    void* out;
+    int ldo;
+    float* ws;
+    int* status;
+};
+
+// Box shapes a tensor map must have for the GEMM: weights 64 (K) x 128
+// rows (64 rows in pair mode); activations 64 x BN.
+int gemm_block_n(int N);          // chosen BN for N token rows
+cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
+                        const CUtensorMap& a2, const CUtensorMap& b, int bn,
+                        const GemmArgs& g);
+cudaError_t launch_gemm_splitk_reduce(const Launch& L, const GemmArgs& g);
+
+// ---------------------------------------------------------------- GEMV
+// One token row: y[r] = sum_k W[r][k] * h[k], with h = x (or RMSNorm(x) * g
+// when norm_gain is set).  BF16 weights or Q8_0 planes (int8 quants +
+// fp16 scales per 32).
+struct GemvArgs {
+    const void* w[3];          // weight planes (bf16, or int8 quants for Q8_0)
+    const __half* scales[3];   // Q8_0 scale planes [rows][K/32] (else null)
+    int rows[3];               // rows per tensor (plain mode stacks them)
+    int n_tensors;
+    int pair;                  // w[0] = gate, w[1] = up, output F = rows[0] features
+    int K;
+    int warps_per_row;         // 1, 2, 4 or 8
+    const float* x;            // [K]
+    const __nv_bfloat16* norm_gain;  // null: no norm
+    float eps;
+    int epi;                   // EPI_STORE_F32, EPI_ADD_F32, EPI_SWIGLU_F32
+    float* out;
+    int* status;
+};
+cudaError_t launch_gemv(const Launch& L, int scheme, const GemvArgs& a);
+int gemv_warps_per_row(int rows, int K);
+
+// ---------------------------------------------------------------- elementwise
+cudaError_t launch_embed(const Launch& L, const int32_t* tokens, int T, const __nv_bfloat16* E,
+                         int H, int vocab, float* x, int* status);
+// h[r] = bf16(RMSNorm(x[rows[r]]) * g) for r < n (rows null: r itself)
+cudaError_t launch_rmsnorm_bf16(const Launch& L, const float* x, const int* rows, int n, int H,
+                                const __nv_bfloat16* g, float eps, __nv_bfloat16* h);
+
+struct RopeArgs {
+    const float* qkv;          // [T][n_q*128 + 2*n_kv*128]
+    int T, n_q, n_kv;
+    const __nv_bfloat16* q_gain;
+    const __nv_bfloat16* k_gain;
+    float eps;
+    const float2* rope;        // [max_ctx][64] (cos, sin)
+    const int* row_pos;        // [T]
+    const int* row_slot;       // [T] session slot
+    const int* tables;         // [slots][max_blocks]
+    int max_blocks;
+    __nv_bfloat16* kv_layer;   // pool base of this layer: [n_blocks][2][n_kv][32][128]
+    int64_t layer_stride;      // elements between layers (unused by the kernel)
+    int n_blocks;
+    float* q_out;              // [T][n_q*128]
+    int* status;
+};
+cudaError_t launch_qk_norm_rope_append(const Launch& L, const RopeArgs& a);
+
+struct AttnArgs {
+    const float* q;            // [T][n_q][128]
+    int T, n_q, n_kv;
+    const int* row_pos;
+    const int* row_slot;
+    const int* tables;
+    int max_blocks;
+    const __nv_bfloat16* kv_layer;
+    int n_blocks;
+    int n_splits;
+    float* part_ml;            // [T][n_q][n_splits][2]
+    float* part_o;             // [T][n_q][n_splits][128]
+    void* out;                 // [T][n_q*128], f32 or bf16
+    int out_bf16;
+    int* status;
+};
+cudaError_t launch_attention(const Launch& L, const AttnArgs& a);
+
+cudaError_t launch_argmax(const Launch& L, const float* logits, int rows, int V, int32_t* out);
+
+// Q8_0: canonical blocks -> (int8 plane, fp16 scale plane); planes -> bf16;
+// bf16 -> canonical blocks.
+cudaError_t launch_q8_split(cudaStream_t s, const uint8_t* blocks, int64_t nblocks, int8_t* qs,
+                            __half* scales);
+cudaError_t launch_q8_to_bf16(const Launch& L, const int8_t* qs, const __half* scales, int64_t n,
+                              __nv_bfloat16* w);
+cudaError_t launch_quantize_q8_0(cudaStream_t s, const __nv_bfloat16* w, int64_t n, uint8_t* blocks);
+
+}  // namespace q3

@@ -1,0 +1,977 @@
+// runtime.cu -- host runtime behind include/q3.h: model creation, the KV
+// block pool and sessions, round planning, and the per-round launch sequence.
+//
+// The round ("Kipp Roadmap", status v0.0.2 and v0.0.4; "Kipp Model Support",
+// section "The registry"):
+//   x = embed[tokens]
+//   per layer: QKV = W_qkv RMSNorm(x); q/k RMSNorm + RoPE, K/V -> paged pool;
+//              o = attention; x += W_o o; x += W_down SwiGLU(W_gate h, W_up h)
+//              with h = RMSNorm(x)
+//   logits = U RMSNorm(x_last) for the last row of each session; argmax.
+// One-token rounds stream weights through the GEMV kernel (FP32
+// activations); wider rounds use the tcgen05 GEMM with bf16 activations.
+// The host only plans: token positions, session slots and block tables are
+// uploaded to device memory and every kernel reads them there.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <set>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/q3.h"
+#include "kernels.h"
+
+using bf16 = __nv_bfloat16;
+using namespace q3;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows][cols] (row-major) read in boxes of 64 columns (one
+// 128-byte swizzle row) by box_rows rows.
+bool tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t elem[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+struct Q8Planes {
+    int8_t* qs = nullptr;
+    __half* sc = nullptr;
+};
+
+enum Proj { P_Q, P_K, P_V, P_O, P_G, P_U, P_D, N_PROJ };
+
+struct LayerMaps {
+    CUtensorMap m[N_PROJ];
+};
+
+}  // namespace
+
+struct q3_pool;
+
+struct q3_model {
+    q3_config c{};
+    int max_rows = 0, rows_alloc = 0;
+    int qw = 0, kvw = 0, qkvw = 0;
+    cudaStream_t stream = nullptr;
+    bool poisoned = false;
+    bool pdl = false;
+    int64_t launches = 0;
+
+    const bf16* embed = nullptr;
+    const bf16* final_norm = nullptr;
+    const bf16* lm_head = nullptr;
+    std::vector<q3_layer_weights> layers;
+    std::vector<std::vector<Q8Planes>> q8;   // [layer][proj]
+
+    // device memory owned by the model
+    std::vector<void*> allocs;
+    int* status = nullptr;
+    float2* rope = nullptr;
+    float* x = nullptr;       // [rows][H] residual
+    bf16* hb = nullptr;       // [rows_alloc][H] normed rows (GEMM path)
+    float* qkv = nullptr;     // [rows][qkvw]
+    float* q = nullptr;       // [rows][qw]
+    bf16* att = nullptr;      // [rows_alloc][qw]
+    float* attf = nullptr;    // [qw]
+    bf16* s = nullptr;        // [rows_alloc][F]
+    float* sf = nullptr;      // [F]
+    bf16* hfin = nullptr;     // [rows_alloc][H]
+    float* part_ml = nullptr;
+    float* part_o = nullptr;
+    size_t part_rows = 0;     // (row, split) pairs the partial buffers hold
+    float* ws = nullptr;
+    size_t ws_elems = 0;
+    bf16* deq = nullptr;      // Q8_0 prefill: dequantised projection(s)
+    int* meta = nullptr;      // [3][max_rows]: row_pos, row_slot, last_row
+
+    // pinned staging ring for host -> device metadata
+    uint8_t* stage = nullptr;
+    size_t stage_slot = 0;
+    int stage_n = 0, stage_next = 0;
+    std::vector<cudaEvent_t> stage_ev;
+    std::vector<char> stage_used;
+
+    std::vector<LayerMaps> maps;
+    LayerMaps maps_dummy{};
+    CUtensorMap lm_map{};
+    CUtensorMap deq_qkv{}, deq_o{}, deq_g{}, deq_u{}, deq_d{};
+    std::map<std::tuple<const void*, int, int>, CUtensorMap> act_maps;
+
+    int check(cudaError_t e, const char* what)
+    {
+        if (e == cudaSuccess) return Q3_OK;
+        poisoned = true;
+        return fail(Q3_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    }
+
+    void* dalloc(size_t bytes)
+    {
+        void* p = nullptr;
+        if (cudaMalloc(&p, bytes ? bytes : 16) != cudaSuccess) return nullptr;
+        allocs.push_back(p);
+        return p;
+    }
+
+    // a pinned staging slot; blocks only if the slot's previous copy is pending
+    uint8_t* stage_acquire(int* slot)
+    {
+        const int i = stage_next;
+        stage_next = (stage_next + 1) % stage_n;
+        if (stage_used[i]) cudaEventSynchronize(stage_ev[i]);
+        *slot = i;
+        return stage + (size_t)i * stage_slot;
+    }
+    cudaError_t stage_copy(int slot, void* dst, size_t bytes)
+    {
+        cudaError_t e = cudaMemcpyAsync(dst, stage + (size_t)slot * stage_slot, bytes,
+                                        cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaEventRecord(stage_ev[slot], stream);
+        stage_used[slot] = 1;
+        return e;
+    }
+
+    const CUtensorMap* act_map(const void* ptr, int K, int bn)
+    {
+        auto key = std::make_tuple(ptr, K, bn);
+        auto it = act_maps.find(key);
+        if (it != act_maps.end()) return &it->second;
+        CUtensorMap mp;
+        if (!tmap_bf16(&mp, ptr, rows_alloc, K, bn)) return nullptr;
+        return &(act_maps[key] = mp);
+    }
+};
+
+struct q3_session;
+
+struct q3_pool {
+    q3_model* m = nullptr;
+    int n_blocks = 0, max_sessions = 0, max_blocks = 0;
+    bf16* kv = nullptr;          // [L][n_blocks][2][n_kv][32][128]
+    int* tables = nullptr;       // [max_sessions][max_blocks]
+    std::set<int> free_blocks;
+    std::vector<char> slot_used;
+    int live = 0;
+};
+
+struct q3_session {
+    q3_pool* pool = nullptr;
+    int slot = 0;
+    int pos = 0;
+    std::vector<int> blocks;     // physical block of each 32 positions
+    int n_fixed = 0;             // leading blocks fixed by set_block_table
+    int uploaded = 0;            // table entries already on the device
+};
+
+namespace {
+
+int validate_config(const q3_config* c)
+{
+    if (!c) return fail(Q3_ERR_INVALID_ARG, "config is NULL");
+    if (c->n_layers < 1 || c->hidden < 128 || c->n_q_heads < 1 || c->n_kv_heads < 1 ||
+        c->ffn < 128 || c->vocab < 128 || c->max_ctx < 1)
+        return fail(Q3_ERR_INVALID_ARG, "config: non-positive dimension");
+    if (c->head_dim != 128) return fail(Q3_ERR_INVALID_ARG, "config: head_dim must be 128");
+    if (c->n_q_heads % c->n_kv_heads || c->n_q_heads / c->n_kv_heads > 8)
+        return fail(Q3_ERR_INVALID_ARG, "config: n_q_heads must be a multiple (<= 8x) of n_kv_heads");
+    if (c->hidden % 128 || c->ffn % 128 || c->vocab % 128)
+        return fail(Q3_ERR_INVALID_ARG, "config: hidden, ffn and vocab must be multiples of 128");
+    if (c->scheme != Q3_BF16 && c->scheme != Q3_Q8_0)
+        return fail(Q3_ERR_INVALID_ARG, "config: unknown weight scheme %d", c->scheme);
+    if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f))
+        return fail(Q3_ERR_INVALID_ARG, "config: rms_eps and rope_theta must be positive");
+    return Q3_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ---------------------------------------------------------------- the round
+
+struct Round {
+    int T = 0, ns = 0;
+    std::vector<int> n;              // tokens per session
+    const int32_t* tokens = nullptr;
+    float* logits = nullptr;
+    int32_t* argmax = nullptr;
+    q3_pool* pool = nullptr;
+    int last_row = 0;                // host copy when ns == 1
+    int max_ctx = 0;                 // largest context of the round
+};
+
+int attention_splits(const q3_model* m, int T, int max_ctx)
+{
+    const int nblk = (max_ctx + 31) / 32;
+    int s = (8 * 152 + T * m->c.n_kv_heads - 1) / (T * m->c.n_kv_heads);
+    s = std::max(1, std::min(s, nblk));
+    while (s > 1 && (size_t)T * s > m->part_rows) --s;
+    return s;
+}
+
+// Plan a tcgen05 GEMM: tile width and split-K count that keep the SMs busy.
+void plan_gemm(const q3_model* m, int M, int N, int K, int* bn, int* splits)
+{
+    const int kb = K / 64;
+    int best_bn = gemm_block_n(N), best_s = 1;
+    double best = 1e30;
+    const int bns[2] = {gemm_block_n(N), N > 128 ? 128 : gemm_block_n(N)};
+    for (int bi = 0; bi < 2; ++bi) {
+        const int b = bns[bi];
+        const int tiles = (M / 128) * ((N + b - 1) / b);
+        for (int s = 1; s <= 8; s *= 2) {
+            if (s > 1 && (kb / s < 4 || (size_t)s * N * M > m->ws_elems)) break;
+            const int ctas = tiles * s;
+            const int waves = (ctas + 151) / 152;
+            // per-CTA cost ~ MMA columns x k-blocks + a fixed prologue/epilogue
+            double cost = waves * ((double)b * kb / s + 8.0 * b + 400.0);
+            if (s > 1) cost += (double)s * N * M / (152.0 * 256.0);   // reduce pass
+            if (cost < best * 0.97) { best = cost; best_bn = b; best_s = s; }
+        }
+    }
+    *bn = best_bn;
+    *splits = best_s;
+}
+
+int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* a2,
+         int tiles0, int tiles1, int pair, int M, int N, int K, const void* act, int epi, void* out,
+         int ldo)
+{
+    int bn, splits;
+    plan_gemm(m, M, N, K, &bn, &splits);
+    const CUtensorMap* b = m->act_map(act, K, bn);
+    if (!b) return fail(Q3_ERR_CUDA, "tensor map encoding failed");
+    GemmArgs g{};
+    g.M = M; g.N = N; g.K = K;
+    g.a_tiles0 = tiles0; g.a_tiles1 = tiles1;
+    g.pair = pair;
+    g.k_splits = splits;
+    g.epi = epi;
+    g.out = out; g.ldo = ldo;
+    g.ws = m->ws;
+    g.status = m->status;
+    Launch L{m->stream, m->pdl, &m->launches};
+    int rc = m->check(launch_gemm(L, *a0, a1 ? *a1 : *a0, a2 ? *a2 : *a0, *b, bn, g), "gemm");
+    if (rc) return rc;
+    if (splits > 1) rc = m->check(launch_gemm_splitk_reduce(L, g), "gemm reduce");
+    return rc;
+}
+
+int gemv(q3_model* m, int n_tensors, const void* const* w, const __half* const* sc, const int* rows,
+         int pair, int K, const float* x, const bf16* gain, int epi, float* out)
+{
+    GemvArgs a{};
+    int total = 0;
+    for (int i = 0; i < n_tensors; ++i) {
+        a.w[i] = w[i];
+        a.scales[i] = sc ? sc[i] : nullptr;
+        a.rows[i] = rows[i];
+        total += rows[i];
+    }
+    a.n_tensors = n_tensors;
+    a.pair = pair;
+    a.K = K;
+    a.warps_per_row = gemv_warps_per_row(total, K);
+    if (pair && a.warps_per_row > 4) a.warps_per_row = 4;
+    a.x = x;
+    a.norm_gain = gain;
+    a.eps = m->c.rms_eps;
+    a.epi = epi;
+    a.out = out;
+    a.status = m->status;
+    Launch L{m->stream, m->pdl, &m->launches};
+    return m->check(launch_gemv(L, sc ? Q3_Q8_0 : Q3_BF16, a), "gemv");
+}
+
+int run_round(q3_model* m, const Round& r)
+{
+    const q3_config& c = m->c;
+    const int H = c.hidden, F = c.ffn, T = r.T;
+    const int* row_pos = m->meta;
+    const int* row_slot = m->meta + m->max_rows;
+    const int* last_rows = m->meta + 2 * m->max_rows;
+    const bool one = (T == 1);
+    const bool q8 = c.scheme == Q3_Q8_0;
+    Launch L{m->stream, m->pdl, &m->launches};
+    const size_t layer_kv = (size_t)r.pool->n_blocks * 2 * c.n_kv_heads * 32 * 128;
+    const int n_splits = attention_splits(m, T, r.max_ctx);
+    int rc;
+
+    if ((rc = m->check(launch_embed(L, r.tokens, T, m->embed, H, c.vocab, m->x, m->status), "embed")))
+        return rc;
+
+    for (int l = 0; l < c.n_layers; ++l) {
+        const q3_layer_weights& W = m->layers[l];
+        const LayerMaps& Mp = q8 ? m->maps_dummy : m->maps[l];
+        const bf16* attn_norm = static_cast<const bf16*>(W.attn_norm);
+        const bf16* ffn_norm = static_cast<const bf16*>(W.ffn_norm);
+
+        // ---- QKV projection
+        if (one) {
+            const void* w[3];
+            const __half* sc[3];
+            const int rows[3] = {m->qw, m->kvw, m->kvw};
+            if (q8) {
+                for (int i = 0; i < 3; ++i) { w[i] = m->q8[l][P_Q + i].qs; sc[i] = m->q8[l][P_Q + i].sc; }
+            } else {
+                w[0] = W.wq; w[1] = W.wk; w[2] = W.wv;
+            }
+            if ((rc = gemv(m, 3, w, q8 ? sc : nullptr, rows, 0, H, m->x, attn_norm, EPI_STORE_F32, m->qkv)))
+                return rc;
+        } else {
+            if ((rc = m->check(launch_rmsnorm_bf16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->hb),
+                               "rmsnorm")))
+                return rc;
+            if (q8) {
+                size_t off = 0;
+                for (int i = 0; i < 3; ++i) {
+                    const int rows = i == 0 ? m->qw : m->kvw;
+                    if ((rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_Q + i].qs, m->q8[l][P_Q + i].sc,
+                                                         (int64_t)rows * H, m->deq + off), "dequant")))
+                        return rc;
+                    off += (size_t)rows * H;
+                }
+                rc = gemm(m, &m->deq_qkv, nullptr, nullptr, m->qkvw / 128, m->qkvw / 128, 0, m->qkvw,
+                          T, H, m->hb, EPI_STORE_F32, m->qkv, m->qkvw);
+            } else {
+                rc = gemm(m, &Mp.m[P_Q], &Mp.m[P_K], &Mp.m[P_V], m->qw / 128, (m->qw + m->kvw) / 128, 0,
+                          m->qkvw, T, H, m->hb, EPI_STORE_F32, m->qkv, m->qkvw);
+            }
+            if (rc) return rc;
+        }
+
+        // ---- q/k norm, RoPE, KV append
+        RopeArgs ra{};
+        ra.qkv = m->qkv; ra.T = T; ra.n_q = c.n_q_heads; ra.n_kv = c.n_kv_heads;
+        ra.q_gain = static_cast<const bf16*>(W.q_norm);
+        ra.k_gain = static_cast<const bf16*>(W.k_norm);
+        ra.eps = c.rms_eps; ra.rope = m->rope;
+        ra.row_pos = row_pos; ra.row_slot = row_slot;
+        ra.tables = r.pool->tables; ra.max_blocks = r.pool->max_blocks;
+        ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
+        ra.n_blocks = r.pool->n_blocks;
+        ra.q_out = m->q; ra.status = m->status;
+        if ((rc = m->check(launch_qk_norm_rope_append(L, ra), "qk-norm/rope/append"))) return rc;
+
+        // ---- attention
+        AttnArgs aa{};
+        aa.q = m->q; aa.T = T; aa.n_q = c.n_q_heads; aa.n_kv = c.n_kv_heads;
+        aa.row_pos = row_pos; aa.row_slot = row_slot;
+        aa.tables = r.pool->tables; aa.max_blocks = r.pool->max_blocks;
+        aa.kv_layer = ra.kv_layer; aa.n_blocks = r.pool->n_blocks;
+        aa.n_splits = n_splits;
+        aa.part_ml = m->part_ml; aa.part_o = m->part_o;
+        aa.out = one ? (void*)m->attf : (void*)m->att;
+        aa.out_bf16 = one ? 0 : 1;
+        aa.status = m->status;
+        if ((rc = m->check(launch_attention(L, aa), "attention"))) return rc;
+
+        // ---- O projection + residual
+        if (one) {
+            const void* w[1] = {q8 ? (const void*)m->q8[l][P_O].qs : W.wo};
+            const __half* sc[1] = {q8 ? m->q8[l][P_O].sc : nullptr};
+            const int rows[1] = {H};
+            if ((rc = gemv(m, 1, w, q8 ? sc : nullptr, rows, 0, m->qw, m->attf, nullptr, EPI_ADD_F32, m->x)))
+                return rc;
+        } else {
+            if (q8) {
+                if ((rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_O].qs, m->q8[l][P_O].sc,
+                                                     (int64_t)H * m->qw, m->deq), "dequant")))
+                    return rc;
+                rc = gemm(m, &m->deq_o, nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
+                          EPI_ADD_F32, m->x, H);
+            } else {
+                rc = gemm(m, &Mp.m[P_O], nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
+                          EPI_ADD_F32, m->x, H);
+            }
+            if (rc) return rc;
+        }
+
+        // ---- FFN: gate/up + SwiGLU, down + residual
+        if (one) {
+            const void* w[2];
+            const __half* sc[2];
+            if (q8) {
+                w[0] = m->q8[l][P_G].qs; w[1] = m->q8[l][P_U].qs;
+                sc[0] = m->q8[l][P_G].sc; sc[1] = m->q8[l][P_U].sc;
+            } else {
+                w[0] = W.w_gate; w[1] = W.w_up;
+            }
+            const int rows[2] = {F, F};
+            if ((rc = gemv(m, 2, w, q8 ? sc : nullptr, rows, 1, H, m->x, ffn_norm, EPI_SWIGLU_F32, m->sf)))
+                return rc;
+            const void* wd[1] = {q8 ? (const void*)m->q8[l][P_D].qs : W.w_down};
+            const __half* scd[1] = {q8 ? m->q8[l][P_D].sc : nullptr};
+            const int rowsd[1] = {H};
+            if ((rc = gemv(m, 1, wd, q8 ? scd : nullptr, rowsd, 0, F, m->sf, nullptr, EPI_ADD_F32, m->x)))
+                return rc;
+        } else {
+            if ((rc = m->check(launch_rmsnorm_bf16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->hb),
+                               "rmsnorm")))
+                return rc;
+            if (q8) {
+                if ((rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_G].qs, m->q8[l][P_G].sc,
+                                                     (int64_t)F * H, m->deq), "dequant")) ||
+                    (rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_U].qs, m->q8[l][P_U].sc,
+                                                     (int64_t)F * H, m->deq + (size_t)F * H), "dequant")))
+                    return rc;
+                rc = gemm(m, &m->deq_g, &m->deq_u, nullptr, 0, 0, 1, 2 * F, T, H, m->hb, EPI_SWIGLU_BF16,
+                          m->s, F);
+            } else {
+                rc = gemm(m, &Mp.m[P_G], &Mp.m[P_U], nullptr, 0, 0, 1, 2 * F, T, H, m->hb,
+                          EPI_SWIGLU_BF16, m->s, F);
+            }
+            if (rc) return rc;
+            if (q8) {
+                if ((rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_D].qs, m->q8[l][P_D].sc,
+                                                     (int64_t)H * F, m->deq), "dequant")))
+                    return rc;
+                rc = gemm(m, &m->deq_d, nullptr, nullptr, H / 128, H / 128, 0, H, T, F, m->s, EPI_ADD_F32,
+                          m->x, H);
+            } else {
+                rc = gemm(m, &Mp.m[P_D], nullptr, nullptr, H / 128, H / 128, 0, H, T, F, m->s, EPI_ADD_F32,
+                          m->x, H);
+            }
+            if (rc) return rc;
+        }
+    }
+
+    // ---- final norm + lm_head (+ argmax), last row of each session
+    if (r.ns == 1) {
+        const void* w[1] = {m->lm_head};
+        const int rows[1] = {c.vocab};
+        if ((rc = gemv(m, 1, w, nullptr, rows, 0, H, m->x + (size_t)r.last_row * H, m->final_norm,
+                       EPI_STORE_F32, r.logits)))
+            return rc;
+    } else {
+        if ((rc = m->check(launch_rmsnorm_bf16(L, m->x, last_rows, r.ns, H, m->final_norm, c.rms_eps,
+                                               m->hfin), "final norm")))
+            return rc;
+        if ((rc = gemm(m, &m->lm_map, nullptr, nullptr, c.vocab / 128, c.vocab / 128, 0, c.vocab, r.ns, H,
+                       m->hfin, EPI_STORE_F32, r.logits, c.vocab)))
+            return rc;
+    }
+    if (r.argmax && (rc = m->check(launch_argmax(L, r.logits, r.ns, c.vocab, r.argmax), "argmax")))
+        return rc;
+    return Q3_OK;
+}
+
+// Reserve blocks for positions [0, end) of a session.
+int reserve(q3_session* s, int end, std::vector<std::pair<int, int>>* newly)
+{
+    q3_pool* p = s->pool;
+    const int need = (end + 31) / 32;
+    if (need > p->max_blocks) return fail(Q3_ERR_CTX_OVERFLOW, "context %d exceeds max_ctx", end);
+    while ((int)s->blocks.size() < need) {
+        if (p->free_blocks.empty()) return fail(Q3_ERR_POOL_EXHAUSTED, "KV pool exhausted");
+        const int b = *p->free_blocks.begin();
+        p->free_blocks.erase(p->free_blocks.begin());
+        s->blocks.push_back(b);
+    }
+    (void)newly;
+    return Q3_OK;
+}
+
+// Upload the table entries a session gained since the last upload.
+int upload_table(q3_session* s)
+{
+    q3_pool* p = s->pool;
+    q3_model* m = p->m;
+    const int n = (int)s->blocks.size();
+    if (s->uploaded >= n) return Q3_OK;
+    int slot;
+    int32_t* h = reinterpret_cast<int32_t*>(m->stage_acquire(&slot));
+    const int cnt = n - s->uploaded;
+    for (int i = 0; i < cnt; ++i) h[i] = s->blocks[s->uploaded + i];
+    int rc = m->check(m->stage_copy(slot, p->tables + (size_t)s->slot * p->max_blocks + s->uploaded,
+                                    sizeof(int32_t) * cnt), "table upload");
+    if (rc == Q3_OK) s->uploaded = n;
+    return rc;
+}
+
+int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n, float* logits,
+               int32_t* argmax)
+{
+    q3_pool* pool = S[0]->pool;
+    q3_model* m = pool->m;
+    if (m->poisoned) return fail(Q3_ERR_POISONED, "model poisoned by an earlier error");
+    Round r;
+    r.ns = ns;
+    r.pool = pool;
+    r.tokens = tokens;
+    r.logits = logits;
+    r.argmax = argmax;
+    for (int i = 0; i < ns; ++i) {
+        if (S[i]->pool != pool) return fail(Q3_ERR_INVALID_ARG, "sessions of different pools");
+        if (n[i] < 1) return fail(Q3_ERR_INVALID_ARG, "empty round for session %d", i);
+        for (int j = 0; j < i; ++j)
+            if (S[j] == S[i]) return fail(Q3_ERR_INVALID_ARG, "session listed twice");
+        if (S[i]->pos + n[i] > m->c.max_ctx)
+            return fail(Q3_ERR_CTX_OVERFLOW, "position %d + %d exceeds max_ctx %d", S[i]->pos, n[i],
+                        m->c.max_ctx);
+        r.T += n[i];
+        r.max_ctx = std::max(r.max_ctx, S[i]->pos + n[i]);
+    }
+    if (r.T > m->max_rows) return fail(Q3_ERR_INVALID_ARG, "round of %d tokens > max_round_tokens", r.T);
+    int rc;
+    for (int i = 0; i < ns; ++i) {
+        if ((rc = reserve(S[i], S[i]->pos + n[i], nullptr))) return rc;
+        if ((rc = upload_table(S[i]))) return rc;
+    }
+    // row metadata
+    int slot;
+    int32_t* h = reinterpret_cast<int32_t*>(m->stage_acquire(&slot));
+    int t = 0;
+    for (int i = 0; i < ns; ++i) {
+        for (int j = 0; j < n[i]; ++j, ++t) {
+            h[t] = S[i]->pos + j;
+            h[m->max_rows + t] = S[i]->slot;
+        }
+        h[2 * m->max_rows + i] = t - 1;
+    }
+    r.last_row = r.T - 1;
+    if ((rc = m->check(m->stage_copy(slot, m->meta, sizeof(int32_t) * 3 * m->max_rows), "meta upload")))
+        return rc;
+    if ((rc = run_round(m, r))) {
+        m->poisoned = true;
+        return rc;
+    }
+    for (int i = 0; i < ns; ++i) S[i]->pos += n[i];
+    return Q3_OK;
+}
+
+void free_model(q3_model* m)
+{
+    if (!m) return;
+    for (void* p : m->allocs) cudaFree(p);
+    for (auto& e : m->stage_ev) cudaEventDestroy(e);
+    if (m->stage) cudaFreeHost(m->stage);
+    delete m;
+}
+
+}  // namespace
+
+// =====================================================================
+// C ABI
+// =====================================================================
+
+extern "C" {
+
+const char* q3_last_error(void) { return g_err.c_str(); }
+
+int64_t q3_model_launch_count(const q3_model* m) { return m ? m->launches : 0; }
+
+int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tokens, void* stream,
+                    q3_model** out)
+{
+    if (!out) return fail(Q3_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    if (!w || !w->embed || !w->final_norm || !w->layers || (!cfg->tied && !w->lm_head))
+        return fail(Q3_ERR_INVALID_ARG, "weights: NULL pointer");
+    if (max_round_tokens < 1) return fail(Q3_ERR_INVALID_ARG, "max_round_tokens must be >= 1");
+    int dev;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return fail(Q3_ERR_UNSUPPORTED_DEVICE, "no CUDA device");
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(Q3_ERR_UNSUPPORTED_DEVICE, "device is sm_%d%d; this library is built for sm_103a",
+                    prop.major, prop.minor);
+    if (!encode_fn()) return fail(Q3_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+
+    q3_model* m = new q3_model();
+    m->c = *cfg;
+    const q3_config& c = m->c;
+    const int H = c.hidden, F = c.ffn;
+    m->qw = c.n_q_heads * 128;
+    m->kvw = c.n_kv_heads * 128;
+    m->qkvw = m->qw + 2 * m->kvw;
+    m->max_rows = max_round_tokens;
+    m->rows_alloc = (int)round_up(max_round_tokens, 256);
+    m->stream = static_cast<cudaStream_t>(stream);
+    m->embed = static_cast<const bf16*>(w->embed);
+    m->final_norm = static_cast<const bf16*>(w->final_norm);
+    m->lm_head = cfg->tied ? m->embed : static_cast<const bf16*>(w->lm_head);
+    m->layers.assign(w->layers, w->layers + c.n_layers);
+    m->pdl = true;
+
+    auto bad = [&](int code, const char* msg) {
+        free_model(m);
+        return fail(code, "%s", msg);
+    };
+    if (!aligned16(m->embed) || !aligned16(m->lm_head) || !aligned16(m->final_norm))
+        return bad(Q3_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+    for (auto& L : m->layers) {
+        const void* ps[11] = {L.attn_norm, L.wq, L.wk, L.wv, L.q_norm, L.k_norm, L.wo, L.ffn_norm,
+                              L.w_gate, L.w_up, L.w_down};
+        for (const void* p : ps)
+            if (!p) return bad(Q3_ERR_INVALID_ARG, "weights: NULL layer pointer");
+        if (c.scheme == Q3_BF16)
+            for (int i : {1, 2, 3, 6, 8, 9, 10})
+                if (!aligned16(ps[i])) return bad(Q3_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+    }
+
+    const size_t R = m->rows_alloc;
+    bool ok = true;
+    auto A = [&](size_t bytes) {
+        void* p = m->dalloc(bytes);
+        if (!p) ok = false;
+        return p;
+    };
+    m->status = static_cast<int*>(A(sizeof(int)));
+    m->rope = static_cast<float2*>(A(sizeof(float2) * (size_t)c.max_ctx * 64));
+    m->x = static_cast<float*>(A(sizeof(float) * R * H));
+    m->hb = static_cast<bf16*>(A(sizeof(bf16) * R * H));
+    m->qkv = static_cast<float*>(A(sizeof(float) * R * m->qkvw));
+    m->q = static_cast<float*>(A(sizeof(float) * R * m->qw));
+    m->att = static_cast<bf16*>(A(sizeof(bf16) * R * m->qw));
+    m->attf = static_cast<float*>(A(sizeof(float) * m->qw));
+    m->s = static_cast<bf16*>(A(sizeof(bf16) * R * F));
+    m->sf = static_cast<float*>(A(sizeof(float) * F));
+    m->hfin = static_cast<bf16*>(A(sizeof(bf16) * R * H));
+    m->part_rows = 2 * 8 * 152 + 64;
+    m->part_ml = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 2));
+    m->part_o = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 128));
+    m->ws_elems = (size_t)32 << 20;
+    m->ws = static_cast<float*>(A(sizeof(float) * m->ws_elems));
+    m->meta = static_cast<int*>(A(sizeof(int) * 3 * (size_t)m->max_rows));
+    if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
+    if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess)
+        return bad(Q3_ERR_CUDA, "cudaMemset failed");
+
+    // RoPE table: angle p * theta^(-2i/128) and its cos/sin in double, stored as f32
+    {
+        std::vector<float2> tab((size_t)c.max_ctx * 64);
+        for (int i = 0; i < 64; ++i) {
+            const double inv = std::pow((double)c.rope_theta, -(2.0 * i) / 128.0);
+            for (int p = 0; p < c.max_ctx; ++p) {
+                const double a = (double)p * inv;
+                tab[(size_t)p * 64 + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+            }
+        }
+        if (cudaMemcpy(m->rope, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+            return bad(Q3_ERR_CUDA, "rope table upload failed");
+    }
+
+    // pinned staging ring
+    m->stage_slot = round_up(std::max<size_t>(sizeof(int) * 3 * (size_t)m->max_rows,
+                                              sizeof(int) * ((size_t)c.max_ctx / 32 + 1)), 256);
+    m->stage_n = 64;
+    if (cudaMallocHost(&m->stage, m->stage_slot * m->stage_n) != cudaSuccess)
+        return bad(Q3_ERR_OOM, "pinned staging allocation failed");
+    m->stage_ev.resize(m->stage_n);
+    m->stage_used.assign(m->stage_n, 0);
+    for (auto& e : m->stage_ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+            return bad(Q3_ERR_CUDA, "event creation failed");
+
+    // Q8_0: derive the int8 / fp16 planes from the canonical blocks, once
+    const int proj_rows[N_PROJ] = {m->qw, m->kvw, m->kvw, H, F, F, H};
+    const int proj_cols[N_PROJ] = {H, H, H, m->qw, H, H, F};
+    if (c.scheme == Q3_Q8_0) {
+        m->q8.resize(c.n_layers);
+        for (int l = 0; l < c.n_layers && ok; ++l) {
+            const q3_layer_weights& L = m->layers[l];
+            const void* src[N_PROJ] = {L.wq, L.wk, L.wv, L.wo, L.w_gate, L.w_up, L.w_down};
+            m->q8[l].resize(N_PROJ);
+            for (int p = 0; p < N_PROJ; ++p) {
+                const size_t n = (size_t)proj_rows[p] * proj_cols[p];
+                m->q8[l][p].qs = static_cast<int8_t*>(A(n));
+                m->q8[l][p].sc = static_cast<__half*>(A(n / 32 * sizeof(__half)));
+                if (!ok) break;
+                if (launch_q8_split(m->stream, static_cast<const uint8_t*>(src[p]), (int64_t)(n / 32),
+                                    m->q8[l][p].qs, m->q8[l][p].sc) != cudaSuccess)
+                    return bad(Q3_ERR_CUDA, "Q8_0 plane derivation failed");
+            }
+        }
+        size_t deq = std::max({(size_t)m->qkvw * H, (size_t)H * m->qw, (size_t)2 * F * H, (size_t)H * F});
+        m->deq = static_cast<bf16*>(A(sizeof(bf16) * deq));
+        if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
+        if (!tmap_bf16(&m->deq_qkv, m->deq, m->qkvw, H, 128) || !tmap_bf16(&m->deq_o, m->deq, H, m->qw, 128) ||
+            !tmap_bf16(&m->deq_g, m->deq, F, H, 64) || !tmap_bf16(&m->deq_u, m->deq + (size_t)F * H, F, H, 64) ||
+            !tmap_bf16(&m->deq_d, m->deq, H, F, 128))
+            return bad(Q3_ERR_CUDA, "tensor map encoding failed");
+    } else {
+        m->maps.resize(c.n_layers);
+        for (int l = 0; l < c.n_layers; ++l) {
+            const q3_layer_weights& L = m->layers[l];
+            const void* src[N_PROJ] = {L.wq, L.wk, L.wv, L.wo, L.w_gate, L.w_up, L.w_down};
+            for (int p = 0; p < N_PROJ; ++p) {
+                const uint32_t box = (p == P_G || p == P_U) ? 64 : 128;
+                if (!tmap_bf16(&m->maps[l].m[p], src[p], proj_rows[p], proj_cols[p], box))
+                    return bad(Q3_ERR_CUDA, "tensor map encoding failed");
+            }
+        }
+    }
+    if (!tmap_bf16(&m->lm_map, m->lm_head, c.vocab, H, 128))
+        return bad(Q3_ERR_CUDA, "tensor map encoding failed");
+    if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
+    if (cudaStreamSynchronize(m->stream) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        return bad(Q3_ERR_CUDA, "model setup failed");
+    *out = m;
+    return Q3_OK;
+}
+
+void q3_model_destroy(q3_model* m)
+{
+    if (!m) return;
+    cudaStreamSynchronize(m->stream);
+    free_model(m);
+}
+
+int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
+{
+    if (!m || !out || n_blocks < 1 || max_sessions < 1)
+        return fail(Q3_ERR_INVALID_ARG, "pool: bad argument");
+    *out = nullptr;
+    q3_pool* p = new q3_pool();
+    p->m = m;
+    p->n_blocks = n_blocks;
+    p->max_sessions = max_sessions;
+    p->max_blocks = (m->c.max_ctx + 31) / 32;
+    const size_t kv = (size_t)m->c.n_layers * n_blocks * 2 * m->c.n_kv_heads * 32 * 128;
+    if (cudaMalloc(&p->kv, kv * sizeof(bf16)) != cudaSuccess) {
+        delete p;
+        return fail(Q3_ERR_OOM, "pool: cannot allocate %zu bytes of KV", kv * sizeof(bf16));
+    }
+    if (cudaMalloc(&p->tables, sizeof(int) * (size_t)max_sessions * p->max_blocks) != cudaSuccess) {
+        cudaFree(p->kv);
+        delete p;
+        return fail(Q3_ERR_OOM, "pool: cannot allocate block tables");
+    }
+    if (cudaMemsetAsync(p->tables, 0xff, sizeof(int) * (size_t)max_sessions * p->max_blocks,
+                        m->stream) != cudaSuccess) {
+        cudaFree(p->kv);
+        cudaFree(p->tables);
+        delete p;
+        return fail(Q3_ERR_CUDA, "pool: memset failed");
+    }
+    for (int b = 0; b < n_blocks; ++b) p->free_blocks.insert(p->free_blocks.end(), b);
+    p->slot_used.assign(max_sessions, 0);
+    *out = p;
+    return Q3_OK;
+}
+
+void q3_pool_destroy(q3_pool* p)
+{
+    if (!p) return;
+    cudaStreamSynchronize(p->m->stream);
+    cudaFree(p->kv);
+    cudaFree(p->tables);
+    delete p;
+}
+
+int q3_session_create(q3_pool* p, q3_session** out)
+{
+    if (!p || !out) return fail(Q3_ERR_INVALID_ARG, "session: bad argument");
+    *out = nullptr;
+    int slot = -1;
+    for (int i = 0; i < p->max_sessions; ++i)
+        if (!p->slot_used[i]) { slot = i; break; }
+    if (slot < 0) return fail(Q3_ERR_INVALID_ARG, "pool has no free session slot");
+    q3_session* s = new q3_session();
+    s->pool = p;
+    s->slot = slot;
+    p->slot_used[slot] = 1;
+    ++p->live;
+    *out = s;
+    return Q3_OK;
+}
+
+void q3_session_destroy(q3_session* s)
+{
+    if (!s) return;
+    for (int b : s->blocks) s->pool->free_blocks.insert(b);
+    s->pool->slot_used[s->slot] = 0;
+    --s->pool->live;
+    delete s;
+}
+
+int q3_session_set_block_table(q3_session* s, const int32_t* ids, int n)
+{
+    if (!s || (n > 0 && !ids) || n < 0) return fail(Q3_ERR_INVALID_ARG, "set_block_table: bad argument");
+    if (s->pos != 0) return fail(Q3_ERR_INVALID_ARG, "set_block_table: session is not empty");
+    q3_pool* p = s->pool;
+    if (n > p->max_blocks) return fail(Q3_ERR_INVALID_ARG, "set_block_table: more blocks than max_ctx");
+    for (int b : s->blocks) p->free_blocks.insert(b);
+    s->blocks.clear();
+    std::set<int> seen;
+    for (int i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= p->n_blocks || !p->free_blocks.count(ids[i]) || seen.count(ids[i])) {
+            for (int b : s->blocks) p->free_blocks.insert(b);
+            s->blocks.clear();
+            s->n_fixed = 0;
+            s->uploaded = 0;
+            return fail(Q3_ERR_INVALID_ARG, "set_block_table: block %d not free or out of range", ids[i]);
+        }
+        seen.insert(ids[i]);
+    }
+    for (int i = 0; i < n; ++i) {
+        p->free_blocks.erase(ids[i]);
+        s->blocks.push_back(ids[i]);
+    }
+    s->n_fixed = n;
+    s->uploaded = 0;
+    return Q3_OK;
+}
+
+int q3_session_eval(q3_session* s, const int32_t* tokens_dev, int n, float* logits_dev,
+                    int32_t* argmax_dev)
+{
+    if (!s || !tokens_dev || !logits_dev || n < 1) return fail(Q3_ERR_INVALID_ARG, "eval: bad argument");
+    q3_model* m = s->pool->m;
+    if (s->pos + n > m->c.max_ctx)
+        return fail(Q3_ERR_CTX_OVERFLOW, "position %d + %d exceeds max_ctx %d", s->pos, n, m->c.max_ctx);
+    for (int off = 0; off < n; off += m->max_rows) {
+        const int k = std::min(m->max_rows, n - off);
+        int rc = eval_round(&s, 1, tokens_dev + off, &k, logits_dev, argmax_dev);
+        if (rc) return rc;
+    }
+    return Q3_OK;
+}
+
+int q3_eval_batch(q3_session* const* sessions, int ns, const int32_t* tokens_dev, const int* n,
+                  float* logits_dev, int32_t* argmax_dev)
+{
+    if (!sessions || ns < 1 || !tokens_dev || !n || !logits_dev)
+        return fail(Q3_ERR_INVALID_ARG, "eval_batch: bad argument");
+    for (int i = 0; i < ns; ++i)
+        if (!sessions[i]) return fail(Q3_ERR_INVALID_ARG, "eval_batch: NULL session");
+    return eval_round(sessions, ns, tokens_dev, n, logits_dev, argmax_dev);
+}
+
+int q3_session_truncate(q3_session* s, int n_pos)
+{
+    if (!s || n_pos < 0 || n_pos > s->pos) return fail(Q3_ERR_INVALID_ARG, "truncate: bad position");
+    s->pos = n_pos;
+    const int keep = std::max((n_pos + 31) / 32, s->n_fixed);
+    while ((int)s->blocks.size() > keep) {
+        s->pool->free_blocks.insert(s->blocks.back());
+        s->blocks.pop_back();
+    }
+    s->uploaded = std::min(s->uploaded, (int)s->blocks.size());
+    return Q3_OK;
+}
+
+int q3_session_reset(q3_session* s) { return q3_session_truncate(s, 0); }
+
+int q3_session_pos(const q3_session* s) { return s ? s->pos : -1; }
+
+int q3_sync(q3_model* m)
+{
+    if (!m) return fail(Q3_ERR_INVALID_ARG, "sync: NULL model");
+    if (m->poisoned) return fail(Q3_ERR_POISONED, "model poisoned by an earlier error");
+    int rc = m->check(cudaStreamSynchronize(m->stream), "stream");
+    if (rc) return rc;
+    int st = 0;
+    if ((rc = m->check(cudaMemcpy(&st, m->status, sizeof(int), cudaMemcpyDeviceToHost), "status read")))
+        return rc;
+    if (st) {
+        cudaMemset(m->status, 0, sizeof(int));
+        m->poisoned = true;
+        return fail(Q3_ERR_DEVICE_CHECK, "device check failed (status 0x%x)", st);
+    }
+    return Q3_OK;
+}
+
+int q3_quantize_q8_0(const void* w_dev, int64_t n, void* blocks_dev, void* stream)
+{
+    if (!w_dev || !blocks_dev || n < 0 || n % 32) return fail(Q3_ERR_INVALID_ARG, "quantize: bad argument");
+    if (n == 0) return Q3_OK;
+    cudaError_t e = launch_quantize_q8_0(static_cast<cudaStream_t>(stream), static_cast<const bf16*>(w_dev),
+                                         n, static_cast<uint8_t*>(blocks_dev));
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "quantize: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, float* y_dev, void* stream)
+{
+    if (!w_dev || !x_dev || !y_dev || M < 128 || M % 128 || K < 64 || K % 64 || N < 1 ||
+        !aligned16(w_dev) || !aligned16(x_dev))
+        return fail(Q3_ERR_INVALID_ARG, "op_matmul: bad argument");
+    const int bn = gemm_block_n(N);
+    CUtensorMap a, b;
+    if (!tmap_bf16(&a, w_dev, M, K, 128) || !tmap_bf16(&b, x_dev, round_up(N, 256), K, bn))
+        return fail(Q3_ERR_CUDA, "op_matmul: tensor map encoding failed");
+    static int* status = nullptr;
+    if (!status && cudaMalloc(&status, sizeof(int)) != cudaSuccess)
+        return fail(Q3_ERR_OOM, "op_matmul: status allocation failed");
+    GemmArgs g{};
+    g.M = M; g.N = N; g.K = K;
+    g.a_tiles0 = g.a_tiles1 = M / 128;
+    g.k_splits = 1;
+    g.epi = EPI_STORE_F32;
+    g.out = y_dev; g.ldo = M;
+    g.status = status;
+    Launch L{static_cast<cudaStream_t>(stream), false, nullptr};
+    cudaError_t e = launch_gemm(L, a, a, a, b, bn, g);
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "op_matmul: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, int M, int K,
+                 float* y_dev, void* stream)
+{
+    if (!w_dev || !x_dev || !y_dev || M < 8 || M % 8 || K < 32 || K % 32 || !aligned16(w_dev) ||
+        !aligned16(x_dev))
+        return fail(Q3_ERR_INVALID_ARG, "op_matvec: bad argument");
+    GemvArgs a{};
+    a.w[0] = w_dev;
+    a.scales[0] = static_cast<const __half*>(scales_dev);
+    a.rows[0] = M;
+    a.n_tensors = 1;
+    a.K = K;
+    a.warps_per_row = gemv_warps_per_row(M, K);
+    a.x = x_dev;
+    a.epi = EPI_STORE_F32;
+    a.out = y_dev;
+    Launch L{static_cast<cudaStream_t>(stream), false, nullptr};
+    cudaError_t e = launch_gemv(L, scales_dev ? Q3_Q8_0 : Q3_BF16, a);
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "op_matvec: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, and exports every
+entry point include/q3.h declares (no compute calls are made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "q3.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(q3_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def libq3():
+    from qwen3_dense_decoder_gb300 import buildlib
+    path = buildlib.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("q3_model_create", "q3_model_destroy", "q3_pool_create", "q3_session_create",
+                     "q3_session_set_block_table", "q3_session_eval", "q3_eval_batch",
+                     "q3_session_truncate", "q3_session_reset", "q3_session_pos", "q3_sync",
+                     "q3_last_error", "q3_quantize_q8_0"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(libq3):
+    missing = [n for n in declared_functions() if not hasattr(libq3, n)]
+    assert not missing, missing
+
+
+def test_last_error_is_empty_string_initially(libq3):
+    libq3.q3_last_error.restype = ctypes.c_char_p
+    assert isinstance(libq3.q3_last_error(), bytes)
+
+
+def test_host_side_argument_checks_need_no_gpu(libq3):
+    # NULL arguments are rejected before any CUDA call
+    libq3.q3_last_error.restype = ctypes.c_char_p
+    assert libq3.q3_model_create(None, None, 16, None, None) == -1
+    assert libq3.q3_session_eval(None, None, 1, None, None) == -1
+    assert libq3.q3_quantize_q8_0(None, ctypes.c_int64(32), None, None) == -1
+    assert libq3.q3_op_matmul(None, None, 128, 1, 64, None, None) == -1
+    assert b"bad argument" in libq3.q3_last_error()
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "qwen3_dense_decoder_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "q3_oracle" not in text and "orc_" not in text, f

@@ -1,0 +1,91 @@
+"""Operator gates on the GPU: each kernel family against the oracle on the same
+seeded inputs (the pages' operator tests: "Reproducing Kipp", section
+"Model-backed CPU and Metal gates", --metal-operators).
+
+- Q8_0 packing: the library's CUDA quantizer and the oracle's packer agree
+  bit for bit ("Kipp Model Support", section "Quantization (Q8_0)").
+- tcgen05 GEMM: bf16 inputs, FP32 accumulation, against the oracle's FP64
+  matmul; shapes span several tiles and ragged token counts (1, 5, 40, 83,
+  200, 300) so every N tile width and the tile tail are exercised.
+- Decode GEMV, BF16 and Q8_0 planes, against the oracle.
+Tolerance: the products are exact in FP32 and only the K-term FP32
+accumulation differs from FP64, so per element |err| <= 1e-5 * sum_k |w x|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q3():
+    import qwen3_dense_decoder_gb300 as q3
+    q3.build()
+    return q3
+
+
+def _bf16(shape, seed, scale=1.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (torch.randn(shape, generator=g, device="cuda") * scale).to(torch.bfloat16)
+
+
+def _f32(t):
+    return t.float().cpu().numpy()
+
+
+def test_quantizer_matches_oracle_packer_bitwise(q3, orc):
+    w = _bf16((96, 4096), 1, 0.02)
+    w[3, :32] = 0                                             # all-zero block
+    w[4, 32:64] = torch.linspace(-1, 1, 32, device="cuda").to(torch.bfloat16)
+    got = q3.quantize_q8_0(w).cpu().numpy()
+    ref = orc.q8_0_pack(_f32(w))
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("n", [1, 5, 32, 40, 83, 200, 300])
+@pytest.mark.parametrize("M,K", [(256, 64), (384, 2560), (128, 9728)])
+def test_tcgen05_matmul_matches_oracle(q3, orc, n, M, K):
+    w = _bf16((M, K), 10 + n, 0.05)
+    rows = (n + 255) // 256 * 256
+    x = _bf16((rows, K), 20 + n)
+    y = q3.op_matmul(w, x, n)
+    torch.cuda.synchronize()
+    wb = w.view(torch.int16).cpu().numpy().view(np.uint16)
+    xf = _f32(x[:n])
+    ref = orc.matmul(wb, 0, M, K, xf, n_threads=8)
+    # tensor-core FP32 accumulation is not IEEE-ordered: allow 5e-5 of the magnitude sum
+    bound = 5e-5 * (np.abs(xf.astype(np.float64)) @ np.abs(_f32(w).astype(np.float64)).T) + 1e-30
+    err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), (err / bound).max()
+
+
+@pytest.mark.parametrize("M,K", [(128, 1024), (6144, 2560), (2560, 9728), (1024, 17408)])
+def test_gemv_bf16_matches_oracle(q3, orc, M, K):
+    w = _bf16((M, K), 30, 0.02)
+    x = torch.randn(K, generator=torch.Generator(device="cuda").manual_seed(31), device="cuda")
+    y = q3.op_matvec(w, x)
+    torch.cuda.synchronize()
+    ref = orc.matmul(w.view(torch.int16).cpu().numpy().view(np.uint16), 0, M, K, x.cpu().numpy(),
+                     n_threads=8)[0]
+    bound = 1e-5 * (np.abs(_f32(w).astype(np.float64)) @ np.abs(x.cpu().numpy().astype(np.float64)))
+    assert np.all(np.abs(y.cpu().numpy() - ref) <= bound)
+
+
+@pytest.mark.parametrize("M,K", [(128, 1024), (4096, 4096), (4096, 12288)])
+def test_gemv_q8_0_matches_oracle(q3, orc, M, K):
+    w = _bf16((M, K), 40, 0.02)
+    blocks = q3.quantize_q8_0(w)                              # canonical [M][K/32][34]
+    b3 = blocks.view(M, K // 32, 34)
+    scales = b3[:, :, 0:2].contiguous().view(torch.float16).view(M, K // 32)
+    quants = b3[:, :, 2:].contiguous().view(torch.int8).view(M, K)
+    x = torch.randn(K, generator=torch.Generator(device="cuda").manual_seed(41), device="cuda")
+    y = q3.op_matvec(quants, x, scales)
+    torch.cuda.synchronize()
+    bnp = blocks.cpu().numpy()
+    ref = orc.matmul(bnp, 1, M, K, x.cpu().numpy(), n_threads=8)[0]
+    deq = orc.q8_0_unpack(bnp, K).astype(np.float64)
+    bound = 1e-5 * (np.abs(deq) @ np.abs(x.cpu().numpy().astype(np.float64)))
+    assert np.all(np.abs(y.cpu().numpy() - ref) <= bound)
