@@ -37,6 +37,9 @@
  *    gives a message (thread-local).  A CUDA error or a failed device-side
  *    check poisons the model: every later call on it returns Q3_ERR_POISONED.
  *  - Calls on one model are not thread-safe; use one host thread per model.
+ *  - Handles may be destroyed in any order: a model's memory is released
+ *    when its handle and all its pools are destroyed, a pool's when its
+ *    handle and all its sessions are.  A destroyed handle must not be used.
  */
 #ifndef Q3_H
 #define Q3_H
@@ -67,6 +70,7 @@ extern "C" {
 #define Q3_STATUS_TOKEN_RANGE 0x1   /* a token id outside [0, vocab) */
 #define Q3_STATUS_BLOCK_RANGE 0x2   /* a block-table entry outside the pool */
 #define Q3_STATUS_TIMEOUT 0x4       /* a bounded device wait ran out */
+#define Q3_STATUS_F16_RANGE 0x8     /* a tensor-core activation beyond the fp16 range */
 
 typedef struct q3_model q3_model;
 typedef struct q3_pool q3_pool;
@@ -109,7 +113,14 @@ typedef struct q3_weights {
  * caller keeps them alive and unchanged until q3_model_destroy.  With Q3_Q8_0
  * the library derives its own device layout of the projections (an int8
  * plane and an fp16 scale plane, bit-equal to the canonical blocks) once,
- * here.  max_round_tokens bounds the rows of one round (the activation
+ * here.  Rounds of more than one token run their projections on tcgen05
+ * tensor cores with fp16 operands (kind::f16 takes A and B of one type and
+ * fp16 activations keep 3 more mantissa bits than bf16): the library keeps
+ * an fp16 copy of the BF16 projections and lm_head (exact except for
+ * |w| < 2^-17, whose rounding is below 2^-25), or dequantises Q8_0 blocks to
+ * fp16.  Weights beyond the fp16 range make creation fail with
+ * Q3_ERR_INVALID_ARG; an activation beyond it is reported by q3_sync as
+ * Q3_ERR_DEVICE_CHECK (Q3_STATUS_F16_RANGE).  max_round_tokens bounds the rows of one round (the activation
  * scratch, owned by the model, is sized for it; longer q3_session_eval rounds
  * are split into chunks of this size).  stream: a cudaStream_t, or NULL for
  * the legacy default stream.  Errors: Q3_ERR_INVALID_ARG (bad shape or NULL
@@ -123,7 +134,7 @@ void q3_model_destroy(q3_model* m);
  * block holds n_layers * 2 * n_kv_heads * 32 * head_dim bf16 values.
  * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_OOM. */
 int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out);
-void q3_pool_destroy(q3_pool* p);   /* after its sessions are destroyed */
+void q3_pool_destroy(q3_pool* p);
 
 /* A session: a position counter and a block table in the pool.  Sessions of
  * one pool may be evaluated together with q3_eval_batch.
@@ -184,8 +195,9 @@ int q3_quantize_q8_0(const void* w_dev, int64_t n, void* blocks_dev, void* strea
  * first operator test of the flash prefill kernel).  They run one kernel of
  * the forward on caller buffers, asynchronously on stream.
  *
- * q3_op_matmul: y[n][m] = sum_k w[m][k] * x[n][k] on the tcgen05 GEMM.
- * w_dev: bf16 [M][K]; x_dev: bf16 [N][K] with at least round_up(N, 256)
+ * q3_op_matmul: y[n][m] = sum_k w[m][k] * x[n][k] on the tcgen05 GEMM
+ * (the operand type of the prefill path, see q3_model_create).
+ * w_dev: fp16 [M][K]; x_dev: fp16 [N][K] with at least round_up(N, 256)
  * rows allocated (rows past N are read but their products discarded);
  * y_dev: f32 [N][M].  M a multiple of 128, K a multiple of 64, 1 <= N.
  * Pointers 16-byte aligned.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */

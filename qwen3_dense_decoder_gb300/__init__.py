@@ -114,8 +114,9 @@ def quantize_q8_0(w: torch.Tensor, stream=None) -> torch.Tensor:
 
 def op_matmul(w: torch.Tensor, x: torch.Tensor, n: int, stream=None) -> torch.Tensor:
     """y[n][m] = sum_k w[m][k] x[n][k] on the tcgen05 GEMM (operator gate).
-    w: bf16 [M, K]; x: bf16 [>= round_up(n, 256), K]."""
+    w: fp16 [M, K]; x: fp16 [>= round_up(n, 256), K]."""
     M, K = w.shape
+    assert w.dtype == x.dtype == torch.float16
     assert x.shape[0] >= (n + 255) // 256 * 256 and x.shape[1] == K
     y = torch.empty(n, M, dtype=torch.float32, device=w.device)
     _check(lib().q3_op_matmul(_ptr(w), _ptr(x), M, n, K, _ptr(y), _stream_handle(stream)))

@@ -124,7 +124,7 @@ Q3_DEV void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, f32 accumulate).
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (16-bit inputs, f32 accumulate).
 Q3_DEV void tc_mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                        uint32_t accumulate) {
     asm volatile("{\n\t.reg .pred p;\n\t"
@@ -159,7 +159,7 @@ Q3_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
 Q3_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major operand tile stored with the
-// 128-byte swizzle (rows of 64 bf16, 8-row groups 1024 bytes apart), as TMA
+// 128-byte swizzle (rows of 64 16-bit elements, 8-row groups 1024 bytes apart), as TMA
 // writes it with CU_TENSOR_MAP_SWIZZLE_128B.  Bits: start address >> 4
 // [0,14), leading offset >> 4 [16,30) (unused for this layout, 1), stride
 // offset >> 4 [32,46) = 1024 >> 4, version 1 [46,48), swizzle mode 2
@@ -174,12 +174,18 @@ Q3_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and
-// an f32 accumulator, for an M x N tile: D format f32 at [4,6), A and B
-// format bf16 at [7,10) and [10,13), N >> 3 at [17,23), M >> 4 at [24,29).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16 with fp16 A and B (both K-major, A/B
+// format field 0 at [7,10) and [10,13)) and an f32 accumulator (D format 1
+// at [4,6)), for an M x N tile: N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// fp16 of an activation; |v| beyond the fp16 range is reported (the caller
+// ORs the flag into the status word once) rather than silently saturated.
+Q3_DEV __half to_f16(float v, bool& out_of_range) {
+    out_of_range |= !(fabsf(v) <= 65504.0f);
+    return __float2half_rn(v);
 }
 
 }  // namespace q3

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_split_kernel(const AttnArgs 
 
     // merge the warps in order; thread d owns output dimension d
     const int d = threadIdx.x;
+    bool range_bad = false;
     for (int g = 0; g < G; ++g) {
         float M = -INFINITY;
         for (int w = 0; w < AWARPS; ++w) M = fmaxf(M, s_m[w][g]);
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_split_kernel(const AttnArgs 
         const size_t row = (size_t)t * p.n_q + hq;
         if (p.n_splits == 1) {
             const float v = O / L;
-            if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(v);
+            if (p.out_f16) reinterpret_cast<__half*>(p.out)[row * D + d] = to_f16(v, range_bad);
             else reinterpret_cast<float*>(p.out)[row * D + d] = v;
         } else {
             p.part_o[(row * p.n_splits + split) * D + d] = O;
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_split_kernel(const AttnArgs 
             }
         }
     }
+    if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
     grid_dep_launch();
 }
 
@@ -187,8 +189,10 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(const AttnArgs p)
         O = fmaf(p.part_o[(row * p.n_splits + s) * D + d], e, O);
     }
     const float v = O / L;
-    if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[row * D + d] = __float2bfloat16_rn(v);
+    bool range_bad = false;
+    if (p.out_f16) reinterpret_cast<__half*>(p.out)[row * D + d] = to_f16(v, range_bad);
     else reinterpret_cast<float*>(p.out)[row * D + d] = v;
+    if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
     grid_dep_launch();
 }
 

@@ -3,11 +3,15 @@
 // Computes the token-round projections of the decoder ("Kipp Model Support",
 // section "Quantization (Q8_0)": the seven per-layer projection tensors;
 // "Kipp Roadmap", status v0.0.6: BF16 layer projections of prefill on the
-// tensor units) as D = W * X^T with FP32 accumulation: the weight matrix W
-// [out][in] is the MMA's A operand (128 output features per tile, TMEM lanes)
-// and the round's token rows X [tokens][in] are the B operand (BN tokens per
-// tile, TMEM columns).  Both operands are K-major bf16 tiles of 64 elements
-// (one 128-byte swizzle row) staged by TMA into a STAGES-deep ring.
+// tensor units, with activations kept wider than BF16) as D = W * X^T with
+// FP32 accumulation: the weight matrix W [out][in] is the MMA's A operand
+// (128 output features per tile, TMEM lanes) and the round's token rows X
+// [tokens][in] are the B operand (BN tokens per tile, TMEM columns).  Both
+// operands are K-major fp16 tiles of 64 elements (one 128-byte swizzle row)
+// staged by TMA into a STAGES-deep ring: kind::f16 wants A and B of one
+// type, and fp16 activations carry 3 more mantissa bits than bf16 ones, so
+// the weights enter as an fp16 copy of the bf16 tensors (exact except for
+// |w| < 2^-17).
 //
 // Roles in a 128-thread CTA: warp 0 lane 0 issues TMA loads, warp 1 lane 0
 // issues tcgen05.mma and owns the TMEM allocation, and all four warps drain
@@ -116,7 +120,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
         for (int i = 0; i < nkb; ++i) {
             const int s = i % STAGES;
             const uint32_t use = i / STAGES;
@@ -146,7 +150,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
     const int row = warp * 32 + lane;                      // D row = TMEM lane
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     float* xch = reinterpret_cast<float*>(smem);           // SwiGLU exchange (ring is idle now)
-    const bool swiglu = (p.epi == EPI_SWIGLU_BF16 || p.epi == EPI_SWIGLU_F32) && p.k_splits == 1;
+    const bool swiglu = (p.epi == EPI_SWIGLU_F16 || p.epi == EPI_SWIGLU_F32) && p.k_splits == 1;
+    bool range_bad = false;
 
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -175,9 +180,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
                     if (n0 + j < p.N) {
                         const float g = __uint_as_float(r[j]);
                         const float v = silu(g) * xch[j * 64 + row];
-                        if (p.epi == EPI_SWIGLU_BF16)
-                            reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)(n0 + j) * p.ldo + f] =
-                                __float2bfloat16_rn(v);
+                        if (p.epi == EPI_SWIGLU_F16)
+                            reinterpret_cast<__half*>(p.out)[(size_t)(n0 + j) * p.ldo + f] =
+                                to_f16(v, range_bad);
                         else
                             reinterpret_cast<float*>(p.out)[(size_t)(n0 + j) * p.ldo + f] = v;
                     }
@@ -196,12 +201,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
                     else if (p.epi == EPI_ADD_F32)
                         reinterpret_cast<float*>(p.out)[o] += v;
                     else
-                        reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
+                        reinterpret_cast<__half*>(p.out)[o] = to_f16(v, range_bad);
                 }
             }
         }
     }
 
+    if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -217,6 +223,7 @@ __global__ void gemm_splitk_reduce_kernel(const GemmArgs p)
     const int m_out = p.pair ? p.M / 2 : p.M;
     const size_t total = (size_t)p.N * m_out;
     const size_t slab = (size_t)p.N * p.M;
+    bool range_bad = false;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
         const int n = (int)(i / m_out), f = (int)(i % m_out);
@@ -228,8 +235,8 @@ __global__ void gemm_splitk_reduce_kernel(const GemmArgs p)
                 u += p.ws[s * slab + (size_t)n * p.M + m_u];
             }
             const float v = silu(g) * u;
-            if (p.epi == EPI_SWIGLU_BF16)
-                reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)n * p.ldo + f] = __float2bfloat16_rn(v);
+            if (p.epi == EPI_SWIGLU_F16)
+                reinterpret_cast<__half*>(p.out)[(size_t)n * p.ldo + f] = to_f16(v, range_bad);
             else
                 reinterpret_cast<float*>(p.out)[(size_t)n * p.ldo + f] = v;
         } else {
@@ -241,9 +248,10 @@ __global__ void gemm_splitk_reduce_kernel(const GemmArgs p)
             else if (p.epi == EPI_ADD_F32)
                 reinterpret_cast<float*>(p.out)[o] += acc;
             else
-                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(acc);
+                reinterpret_cast<__half*>(p.out)[o] = to_f16(acc, range_bad);
         }
     }
+    if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
 }
 
 template <int BN>

@@ -70,17 +70,18 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedArgs a)
     grid_dep_launch();
 }
 
-// ---------------------------------------------------------------- RMSNorm -> bf16
+// ---------------------------------------------------------------- RMSNorm -> fp16
 struct NormArgs {
     const float* x;
     const int* rows;
     int H;
     const __nv_bfloat16* g;
     float eps;
-    __nv_bfloat16* h;
+    __half* h;
+    int* status;
 };
 
-__global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const NormArgs a)
+__global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const NormArgs a)
 {
     __shared__ float red[8];
     __shared__ float s_scale;
@@ -103,13 +104,17 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const NormArgs a)
     }
     __syncthreads();
     const float sc = s_scale;
-    __nv_bfloat16* h = a.h + (size_t)r * a.H;
+    __half* h = a.h + (size_t)r * a.H;
+    bool bad = false;
     for (int i = threadIdx.x * 2; i < a.H; i += blockDim.x * 2) {
         const float2 v = *reinterpret_cast<const float2*>(x + i);
         const float g0 = __bfloat162float(a.g[i]), g1 = __bfloat162float(a.g[i + 1]);
-        *reinterpret_cast<__nv_bfloat162*>(h + i) =
-            __floats2bfloat162_rn(v.x * sc * g0, v.y * sc * g1);
+        __half2 o;
+        o.x = to_f16(v.x * sc * g0, bad);
+        o.y = to_f16(v.y * sc * g1, bad);
+        *reinterpret_cast<__half2*>(h + i) = o;
     }
+    if (bad) set_status(a.status, Q3_STATUS_F16_RANGE);
     grid_dep_launch();
 }
 
@@ -230,26 +235,45 @@ struct Q8DeqArgs {
     const int8_t* qs;
     const __half* scales;
     int64_t n;
-    __nv_bfloat16* w;
+    __half* w;
 };
 
-// bf16(fp16 scale * quant) for the tensor-core prefill path
-__global__ void q8_to_bf16_kernel(const Q8DeqArgs a)
+// fp16(fp16 scale * quant) for the tensor-core prefill path (|d q| <= 127 d
+// never leaves the fp16 range; the product is rounded to 11 bits)
+__global__ void q8_to_f16_kernel(const Q8DeqArgs a)
 {
     grid_dep_wait();
     for (int64_t i = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 8; i < a.n;
          i += (int64_t)gridDim.x * blockDim.x * 8) {
         const float d = __half2float(a.scales[i / 32]);
         const uint2 q = *reinterpret_cast<const uint2*>(a.qs + i);
-        __nv_bfloat16 out[8];
+        __half out[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            out[e] = __float2bfloat16_rn(d * (float)(int8_t)((q.x >> (8 * e)) & 0xff));
-            out[4 + e] = __float2bfloat16_rn(d * (float)(int8_t)((q.y >> (8 * e)) & 0xff));
+            out[e] = __float2half_rn(d * (float)(int8_t)((q.x >> (8 * e)) & 0xff));
+            out[4 + e] = __float2half_rn(d * (float)(int8_t)((q.y >> (8 * e)) & 0xff));
         }
         *reinterpret_cast<uint4*>(a.w + i) = *reinterpret_cast<const uint4*>(out);
     }
     grid_dep_launch();
+}
+
+// fp16 copy of bf16 weights (exact for 2^-17 <= |w| <= 65504 and 0)
+__global__ void bf16_to_f16_kernel(const __nv_bfloat16* w, int64_t n, __half* out,
+                                   unsigned long long* inexact, unsigned long long* overflow)
+{
+    unsigned long long n_inexact = 0, n_over = 0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = __bfloat162float(w[i]);
+        const __half h = __float2half_rn(v);
+        out[i] = h;
+        const float back = __half2float(h);
+        if (!(fabsf(v) <= 65504.0f)) ++n_over;
+        else if (back != v) ++n_inexact;
+    }
+    if (n_inexact) atomicAdd(inexact, n_inexact);
+    if (n_over) atomicAdd(overflow, n_over);
 }
 
 // Per block of 32: d = absmax / 127 (FP32, correctly rounded), scale =
@@ -266,17 +290,18 @@ __global__ void quantize_q8_0_kernel(const __nv_bfloat16* w, int64_t nblocks, ui
             amax = fmaxf(amax, fabsf(x[i]));
         }
         const float d = __fdiv_rn(amax, 127.0f);
-        const uint16_t dh = __half_as_ushort(__float2half_rn(d));
-        uint8_t* out = blocks + b * Q3_Q8_0_BYTES;
-        out[0] = (uint8_t)(dh & 0xff);
-        out[1] = (uint8_t)(dh >> 8);
-        for (int i = 0; i < 32; ++i) {
-            int q = 0;
+        // the 34-byte record as 17 little-endian 16-bit words (2-byte aligned)
+        uint16_t* out = reinterpret_cast<uint16_t*>(blocks + b * Q3_Q8_0_BYTES);
+        out[0] = __half_as_ushort(__float2half_rn(d));
+        for (int i = 0; i < 32; i += 2) {
+            int q0 = 0, q1 = 0;
             if (d != 0.f) {
-                q = __float2int_rn(__fdiv_rn(x[i], d));
-                q = q > 127 ? 127 : (q < -127 ? -127 : q);
+                q0 = __float2int_rn(__fdiv_rn(x[i], d));
+                q1 = __float2int_rn(__fdiv_rn(x[i + 1], d));
+                q0 = q0 > 127 ? 127 : (q0 < -127 ? -127 : q0);
+                q1 = q1 > 127 ? 127 : (q1 < -127 ? -127 : q1);
             }
-            out[2 + i] = (uint8_t)(int8_t)q;
+            out[1 + i / 2] = (uint16_t)((uint8_t)(int8_t)q0 | ((uint16_t)(uint8_t)(int8_t)q1 << 8));
         }
     }
 }
@@ -289,10 +314,10 @@ cudaError_t launch_embed(const Launch& L, const int32_t* tokens, int T, const __
     return launch_ex(L, embed_kernel, dim3(T), dim3(256), EmbedArgs{tokens, E, H, vocab, x, status});
 }
 
-cudaError_t launch_rmsnorm_bf16(const Launch& L, const float* x, const int* rows, int n, int H,
-                                const __nv_bfloat16* g, float eps, __nv_bfloat16* h)
+cudaError_t launch_rmsnorm_f16(const Launch& L, const float* x, const int* rows, int n, int H,
+                               const __nv_bfloat16* g, float eps, __half* h, int* status)
 {
-    return launch_ex(L, rmsnorm_bf16_kernel, dim3(n), dim3(256), NormArgs{x, rows, H, g, eps, h});
+    return launch_ex(L, rmsnorm_f16_kernel, dim3(n), dim3(256), NormArgs{x, rows, H, g, eps, h, status});
 }
 
 cudaError_t launch_qk_norm_rope_append(const Launch& L, const RopeArgs& a)
@@ -315,12 +340,22 @@ cudaError_t launch_q8_split(cudaStream_t s, const uint8_t* blocks, int64_t nbloc
     return cudaGetLastError();
 }
 
-cudaError_t launch_q8_to_bf16(const Launch& L, const int8_t* qs, const __half* scales, int64_t n,
-                              __nv_bfloat16* w)
+cudaError_t launch_q8_to_f16(const Launch& L, const int8_t* qs, const __half* scales, int64_t n,
+                             __half* w)
 {
     int64_t grid = (n / 8 + 255) / 256;
     if (grid > 152 * 32) grid = 152 * 32;
-    return launch_ex(L, q8_to_bf16_kernel, dim3((unsigned)grid), dim3(256), Q8DeqArgs{qs, scales, n, w});
+    return launch_ex(L, q8_to_f16_kernel, dim3((unsigned)grid), dim3(256), Q8DeqArgs{qs, scales, n, w});
+}
+
+cudaError_t launch_bf16_to_f16(cudaStream_t s, const __nv_bfloat16* w, int64_t n, __half* out,
+                               unsigned long long* inexact, unsigned long long* overflow)
+{
+    int64_t grid = (n + 255) / 256;
+    if (grid > 152 * 32) grid = 152 * 32;
+    if (grid < 1) grid = 1;
+    bf16_to_f16_kernel<<<(unsigned)grid, 256, 0, s>>>(w, n, out, inexact, overflow);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_q8_0(cudaStream_t s, const __nv_bfloat16* w, int64_t n, uint8_t* blocks)

@@ -22,13 +22,13 @@ struct Launch {
 
 // ---------------------------------------------------------------- GEMM
 // D[M x N] = A[M x K] * B[N x K]^T on tcgen05 tensor cores.  A is the
-// weight matrix (row-major [out][in]); B holds N token rows (bf16
+// weight matrix (fp16, row-major [out][in]); B holds N token rows (fp16
 // [rows][K]).  Output element (n, m) goes to out[n * ldo + m].
 enum Epi : int {
     EPI_STORE_F32 = 0,   // out = acc (f32)
     EPI_ADD_F32 = 1,     // out += acc (f32 residual)
-    EPI_STORE_BF16 = 2,  // out = bf16(acc)
-    EPI_SWIGLU_BF16 = 3, // paired gate/up tile: out[n][f] = bf16(silu(g) * u)
+    EPI_STORE_F16 = 2,   // out = fp16(acc)
+    EPI_SWIGLU_F16 = 3,  // paired gate/up tile: out[n][f] = fp16(silu(g) * u)
     EPI_SWIGLU_F32 = 4,
 };
 
@@ -77,9 +77,9 @@ int gemv_warps_per_row(int rows, int K);
 // ---------------------------------------------------------------- elementwise
 cudaError_t launch_embed(const Launch& L, const int32_t* tokens, int T, const __nv_bfloat16* E,
                          int H, int vocab, float* x, int* status);
-// h[r] = bf16(RMSNorm(x[rows[r]]) * g) for r < n (rows null: r itself)
-cudaError_t launch_rmsnorm_bf16(const Launch& L, const float* x, const int* rows, int n, int H,
-                                const __nv_bfloat16* g, float eps, __nv_bfloat16* h);
+// h[r] = fp16(RMSNorm(x[rows[r]]) * g) for r < n (rows null: r itself)
+cudaError_t launch_rmsnorm_f16(const Launch& L, const float* x, const int* rows, int n, int H,
+                               const __nv_bfloat16* g, float eps, __half* h, int* status);
 
 struct RopeArgs {
     const float* qkv;          // [T][n_q*128 + 2*n_kv*128]
@@ -112,20 +112,25 @@ struct AttnArgs {
     int n_splits;
     float* part_ml;            // [T][n_q][n_splits][2]
     float* part_o;             // [T][n_q][n_splits][128]
-    void* out;                 // [T][n_q*128], f32 or bf16
-    int out_bf16;
+    void* out;                 // [T][n_q*128], f32 or fp16
+    int out_f16;
     int* status;
 };
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a);
 
 cudaError_t launch_argmax(const Launch& L, const float* logits, int rows, int V, int32_t* out);
 
-// Q8_0: canonical blocks -> (int8 plane, fp16 scale plane); planes -> bf16;
-// bf16 -> canonical blocks.
+// Q8_0: canonical blocks -> (int8 plane, fp16 scale plane); planes -> fp16
+// tensor-core operand; bf16 -> canonical blocks.
 cudaError_t launch_q8_split(cudaStream_t s, const uint8_t* blocks, int64_t nblocks, int8_t* qs,
                             __half* scales);
-cudaError_t launch_q8_to_bf16(const Launch& L, const int8_t* qs, const __half* scales, int64_t n,
-                              __nv_bfloat16* w);
+cudaError_t launch_q8_to_f16(const Launch& L, const int8_t* qs, const __half* scales, int64_t n,
+                             __half* w);
+// fp16 copy of bf16 weights for the tensor-core path; counts values that do
+// not convert exactly (|w| < 2^-17, rounded) in *inexact and values beyond
+// the fp16 range in *overflow.
+cudaError_t launch_bf16_to_f16(cudaStream_t s, const __nv_bfloat16* w, int64_t n, __half* out,
+                               unsigned long long* inexact, unsigned long long* overflow);
 cudaError_t launch_quantize_q8_0(cudaStream_t s, const __nv_bfloat16* w, int64_t n, uint8_t* blocks);
 
 }  // namespace q3

@@ -9,7 +9,8 @@
 //              with h = RMSNorm(x)
 //   logits = U RMSNorm(x_last) for the last row of each session; argmax.
 // One-token rounds stream weights through the GEMV kernel (FP32
-// activations); wider rounds use the tcgen05 GEMM with bf16 activations.
+// activations); wider rounds use the tcgen05 GEMM with fp16 operands (an fp16
+// copy of the bf16 projection weights, fp16 activations).
 // The host only plans: token positions, session slots and block tables are
 // uploaded to device memory and every kernel reads them there.
 #include <cudaTypedefs.h>
@@ -29,6 +30,7 @@
 #include "kernels.h"
 
 using bf16 = __nv_bfloat16;
+using f16 = __half;
 using namespace q3;
 
 namespace {
@@ -60,9 +62,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2-D bf16 tensor [rows][cols] (row-major) read in boxes of 64 columns (one
+// 2-D fp16 tensor [rows][cols] (row-major) read in boxes of 64 columns (one
 // 128-byte swizzle row) by box_rows rows.
-bool tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows)
+bool tmap_f16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows)
 {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -70,7 +72,7 @@ bool tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, ui
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t elem[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
               elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -100,6 +102,7 @@ struct q3_model {
     bool poisoned = false;
     bool pdl = false;
     int64_t launches = 0;
+    int refs = 1;             // the caller's handle + one per live pool
 
     const bf16* embed = nullptr;
     const bf16* final_norm = nullptr;
@@ -110,22 +113,26 @@ struct q3_model {
     // device memory owned by the model
     std::vector<void*> allocs;
     int* status = nullptr;
+    unsigned long long* conv_counts = nullptr;   // fp16 copy: inexact, overflow
+    int64_t inexact_f16 = 0;
     float2* rope = nullptr;
     float* x = nullptr;       // [rows][H] residual
-    bf16* hb = nullptr;       // [rows_alloc][H] normed rows (GEMM path)
+    f16* ha = nullptr;        // [rows_alloc][H] normed rows (GEMM path)
     float* qkv = nullptr;     // [rows][qkvw]
     float* q = nullptr;       // [rows][qw]
-    bf16* att = nullptr;      // [rows_alloc][qw]
+    f16* att = nullptr;       // [rows_alloc][qw]
     float* attf = nullptr;    // [qw]
-    bf16* s = nullptr;        // [rows_alloc][F]
+    f16* s = nullptr;         // [rows_alloc][F]
     float* sf = nullptr;      // [F]
-    bf16* hfin = nullptr;     // [rows_alloc][H]
+    f16* hfin = nullptr;      // [rows_alloc][H]
     float* part_ml = nullptr;
     float* part_o = nullptr;
     size_t part_rows = 0;     // (row, split) pairs the partial buffers hold
     float* ws = nullptr;
     size_t ws_elems = 0;
-    bf16* deq = nullptr;      // Q8_0 prefill: dequantised projection(s)
+    f16* deq = nullptr;       // Q8_0 prefill: dequantised projection(s)
+    std::vector<std::vector<f16*>> w16;   // [layer][proj] fp16 copies (BF16 scheme)
+    f16* lm16 = nullptr;      // fp16 copy of the lm_head for batched rows
     int* meta = nullptr;      // [3][max_rows]: row_pos, row_slot, last_row
 
     // pinned staging ring for host -> device metadata
@@ -180,7 +187,7 @@ struct q3_model {
         auto it = act_maps.find(key);
         if (it != act_maps.end()) return &it->second;
         CUtensorMap mp;
-        if (!tmap_bf16(&mp, ptr, rows_alloc, K, bn)) return nullptr;
+        if (!tmap_f16(&mp, ptr, rows_alloc, K, bn)) return nullptr;
         return &(act_maps[key] = mp);
     }
 };
@@ -194,7 +201,7 @@ struct q3_pool {
     int* tables = nullptr;       // [max_sessions][max_blocks]
     std::set<int> free_blocks;
     std::vector<char> slot_used;
-    int live = 0;
+    int refs = 1;                // the caller's handle + one per live session
 };
 
 struct q3_session {
@@ -360,23 +367,23 @@ int run_round(q3_model* m, const Round& r)
             if ((rc = gemv(m, 3, w, q8 ? sc : nullptr, rows, 0, H, m->x, attn_norm, EPI_STORE_F32, m->qkv)))
                 return rc;
         } else {
-            if ((rc = m->check(launch_rmsnorm_bf16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->hb),
+            if ((rc = m->check(launch_rmsnorm_f16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->ha, m->status),
                                "rmsnorm")))
                 return rc;
             if (q8) {
                 size_t off = 0;
                 for (int i = 0; i < 3; ++i) {
                     const int rows = i == 0 ? m->qw : m->kvw;
-                    if ((rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_Q + i].qs, m->q8[l][P_Q + i].sc,
+                    if ((rc = m->check(launch_q8_to_f16(L, m->q8[l][P_Q + i].qs, m->q8[l][P_Q + i].sc,
                                                          (int64_t)rows * H, m->deq + off), "dequant")))
                         return rc;
                     off += (size_t)rows * H;
                 }
                 rc = gemm(m, &m->deq_qkv, nullptr, nullptr, m->qkvw / 128, m->qkvw / 128, 0, m->qkvw,
-                          T, H, m->hb, EPI_STORE_F32, m->qkv, m->qkvw);
+                          T, H, m->ha, EPI_STORE_F32, m->qkv, m->qkvw);
             } else {
                 rc = gemm(m, &Mp.m[P_Q], &Mp.m[P_K], &Mp.m[P_V], m->qw / 128, (m->qw + m->kvw) / 128, 0,
-                          m->qkvw, T, H, m->hb, EPI_STORE_F32, m->qkv, m->qkvw);
+                          m->qkvw, T, H, m->ha, EPI_STORE_F32, m->qkv, m->qkvw);
             }
             if (rc) return rc;
         }
@@ -403,7 +410,7 @@ int run_round(q3_model* m, const Round& r)
         aa.n_splits = n_splits;
         aa.part_ml = m->part_ml; aa.part_o = m->part_o;
         aa.out = one ? (void*)m->attf : (void*)m->att;
-        aa.out_bf16 = one ? 0 : 1;
+        aa.out_f16 = one ? 0 : 1;
         aa.status = m->status;
         if ((rc = m->check(launch_attention(L, aa), "attention"))) return rc;
 
@@ -416,7 +423,7 @@ int run_round(q3_model* m, const Round& r)
                 return rc;
         } else {
             if (q8) {
-                if ((rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_O].qs, m->q8[l][P_O].sc,
+                if ((rc = m->check(launch_q8_to_f16(L, m->q8[l][P_O].qs, m->q8[l][P_O].sc,
                                                      (int64_t)H * m->qw, m->deq), "dequant")))
                     return rc;
                 rc = gemm(m, &m->deq_o, nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
@@ -447,24 +454,24 @@ int run_round(q3_model* m, const Round& r)
             if ((rc = gemv(m, 1, wd, q8 ? scd : nullptr, rowsd, 0, F, m->sf, nullptr, EPI_ADD_F32, m->x)))
                 return rc;
         } else {
-            if ((rc = m->check(launch_rmsnorm_bf16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->hb),
+            if ((rc = m->check(launch_rmsnorm_f16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->ha, m->status),
                                "rmsnorm")))
                 return rc;
             if (q8) {
-                if ((rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_G].qs, m->q8[l][P_G].sc,
+                if ((rc = m->check(launch_q8_to_f16(L, m->q8[l][P_G].qs, m->q8[l][P_G].sc,
                                                      (int64_t)F * H, m->deq), "dequant")) ||
-                    (rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_U].qs, m->q8[l][P_U].sc,
+                    (rc = m->check(launch_q8_to_f16(L, m->q8[l][P_U].qs, m->q8[l][P_U].sc,
                                                      (int64_t)F * H, m->deq + (size_t)F * H), "dequant")))
                     return rc;
-                rc = gemm(m, &m->deq_g, &m->deq_u, nullptr, 0, 0, 1, 2 * F, T, H, m->hb, EPI_SWIGLU_BF16,
+                rc = gemm(m, &m->deq_g, &m->deq_u, nullptr, 0, 0, 1, 2 * F, T, H, m->ha, EPI_SWIGLU_F16,
                           m->s, F);
             } else {
-                rc = gemm(m, &Mp.m[P_G], &Mp.m[P_U], nullptr, 0, 0, 1, 2 * F, T, H, m->hb,
-                          EPI_SWIGLU_BF16, m->s, F);
+                rc = gemm(m, &Mp.m[P_G], &Mp.m[P_U], nullptr, 0, 0, 1, 2 * F, T, H, m->ha,
+                          EPI_SWIGLU_F16, m->s, F);
             }
             if (rc) return rc;
             if (q8) {
-                if ((rc = m->check(launch_q8_to_bf16(L, m->q8[l][P_D].qs, m->q8[l][P_D].sc,
+                if ((rc = m->check(launch_q8_to_f16(L, m->q8[l][P_D].qs, m->q8[l][P_D].sc,
                                                      (int64_t)H * F, m->deq), "dequant")))
                     return rc;
                 rc = gemm(m, &m->deq_d, nullptr, nullptr, H / 128, H / 128, 0, H, T, F, m->s, EPI_ADD_F32,
@@ -485,8 +492,8 @@ int run_round(q3_model* m, const Round& r)
                        EPI_STORE_F32, r.logits)))
             return rc;
     } else {
-        if ((rc = m->check(launch_rmsnorm_bf16(L, m->x, last_rows, r.ns, H, m->final_norm, c.rms_eps,
-                                               m->hfin), "final norm")))
+        if ((rc = m->check(launch_rmsnorm_f16(L, m->x, last_rows, r.ns, H, m->final_norm, c.rms_eps,
+                                              m->hfin, m->status), "final norm")))
             return rc;
         if ((rc = gemm(m, &m->lm_map, nullptr, nullptr, c.vocab / 128, c.vocab / 128, 0, c.vocab, r.ns, H,
                        m->hfin, EPI_STORE_F32, r.logits, c.vocab)))
@@ -584,10 +591,30 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
 void free_model(q3_model* m)
 {
     if (!m) return;
+    if (m->stream || !m->allocs.empty()) cudaStreamSynchronize(m->stream);
     for (void* p : m->allocs) cudaFree(p);
     for (auto& e : m->stage_ev) cudaEventDestroy(e);
     if (m->stage) cudaFreeHost(m->stage);
     delete m;
+}
+
+// Handles are reference counted so that a model, its pools and their
+// sessions may be destroyed in any order: memory is freed when the last
+// dependent handle goes.
+void model_release(q3_model* m)
+{
+    if (--m->refs == 0) free_model(m);
+}
+
+void pool_release(q3_pool* p)
+{
+    if (--p->refs > 0) return;
+    cudaStreamSynchronize(p->m->stream);
+    cudaFree(p->kv);
+    cudaFree(p->tables);
+    q3_model* m = p->m;
+    delete p;
+    model_release(m);
 }
 
 }  // namespace
@@ -661,16 +688,17 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
         return p;
     };
     m->status = static_cast<int*>(A(sizeof(int)));
+    m->conv_counts = static_cast<unsigned long long*>(A(2 * sizeof(unsigned long long)));
     m->rope = static_cast<float2*>(A(sizeof(float2) * (size_t)c.max_ctx * 64));
     m->x = static_cast<float*>(A(sizeof(float) * R * H));
-    m->hb = static_cast<bf16*>(A(sizeof(bf16) * R * H));
+    m->ha = static_cast<f16*>(A(sizeof(f16) * R * H));
     m->qkv = static_cast<float*>(A(sizeof(float) * R * m->qkvw));
     m->q = static_cast<float*>(A(sizeof(float) * R * m->qw));
-    m->att = static_cast<bf16*>(A(sizeof(bf16) * R * m->qw));
+    m->att = static_cast<f16*>(A(sizeof(f16) * R * m->qw));
     m->attf = static_cast<float*>(A(sizeof(float) * m->qw));
-    m->s = static_cast<bf16*>(A(sizeof(bf16) * R * F));
+    m->s = static_cast<f16*>(A(sizeof(f16) * R * F));
     m->sf = static_cast<float*>(A(sizeof(float) * F));
-    m->hfin = static_cast<bf16*>(A(sizeof(bf16) * R * H));
+    m->hfin = static_cast<f16*>(A(sizeof(f16) * R * H));
     m->part_rows = 2 * 8 * 152 + 64;
     m->part_ml = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 2));
     m->part_o = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 128));
@@ -678,7 +706,8 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->ws = static_cast<float*>(A(sizeof(float) * m->ws_elems));
     m->meta = static_cast<int*>(A(sizeof(int) * 3 * (size_t)m->max_rows));
     if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
-    if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess)
+    if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(m->conv_counts, 0, 2 * sizeof(unsigned long long)) != cudaSuccess)
         return bad(Q3_ERR_CUDA, "cudaMemset failed");
 
     // RoPE table: angle p * theta^(-2i/128) and its cos/sin in double, stored as f32
@@ -728,26 +757,50 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
             }
         }
         size_t deq = std::max({(size_t)m->qkvw * H, (size_t)H * m->qw, (size_t)2 * F * H, (size_t)H * F});
-        m->deq = static_cast<bf16*>(A(sizeof(bf16) * deq));
+        m->deq = static_cast<f16*>(A(sizeof(f16) * deq));
         if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
-        if (!tmap_bf16(&m->deq_qkv, m->deq, m->qkvw, H, 128) || !tmap_bf16(&m->deq_o, m->deq, H, m->qw, 128) ||
-            !tmap_bf16(&m->deq_g, m->deq, F, H, 64) || !tmap_bf16(&m->deq_u, m->deq + (size_t)F * H, F, H, 64) ||
-            !tmap_bf16(&m->deq_d, m->deq, H, F, 128))
+        if (!tmap_f16(&m->deq_qkv, m->deq, m->qkvw, H, 128) || !tmap_f16(&m->deq_o, m->deq, H, m->qw, 128) ||
+            !tmap_f16(&m->deq_g, m->deq, F, H, 64) || !tmap_f16(&m->deq_u, m->deq + (size_t)F * H, F, H, 64) ||
+            !tmap_f16(&m->deq_d, m->deq, H, F, 128))
             return bad(Q3_ERR_CUDA, "tensor map encoding failed");
     } else {
+        // fp16 copies of the projections for the tensor-core path
         m->maps.resize(c.n_layers);
-        for (int l = 0; l < c.n_layers; ++l) {
+        m->w16.resize(c.n_layers);
+        for (int l = 0; l < c.n_layers && ok; ++l) {
             const q3_layer_weights& L = m->layers[l];
             const void* src[N_PROJ] = {L.wq, L.wk, L.wv, L.wo, L.w_gate, L.w_up, L.w_down};
+            m->w16[l].resize(N_PROJ);
             for (int p = 0; p < N_PROJ; ++p) {
+                const size_t n = (size_t)proj_rows[p] * proj_cols[p];
+                f16* d = static_cast<f16*>(A(n * sizeof(f16)));
+                if (!ok) break;
+                m->w16[l][p] = d;
+                if (launch_bf16_to_f16(m->stream, static_cast<const bf16*>(src[p]), (int64_t)n, d,
+                                       m->conv_counts, m->conv_counts + 1) != cudaSuccess)
+                    return bad(Q3_ERR_CUDA, "fp16 weight copy failed");
                 const uint32_t box = (p == P_G || p == P_U) ? 64 : 128;
-                if (!tmap_bf16(&m->maps[l].m[p], src[p], proj_rows[p], proj_cols[p], box))
+                if (!tmap_f16(&m->maps[l].m[p], d, proj_rows[p], proj_cols[p], box))
                     return bad(Q3_ERR_CUDA, "tensor map encoding failed");
             }
         }
     }
-    if (!tmap_bf16(&m->lm_map, m->lm_head, c.vocab, H, 128))
+    m->lm16 = static_cast<f16*>(A(sizeof(f16) * (size_t)c.vocab * H));
+    if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
+    if (launch_bf16_to_f16(m->stream, m->lm_head, (int64_t)c.vocab * H, m->lm16, m->conv_counts,
+                           m->conv_counts + 1) != cudaSuccess)
+        return bad(Q3_ERR_CUDA, "fp16 lm_head copy failed");
+    if (!tmap_f16(&m->lm_map, m->lm16, c.vocab, H, 128))
         return bad(Q3_ERR_CUDA, "tensor map encoding failed");
+    {
+        unsigned long long cnt[2] = {0, 0};
+        if (cudaMemcpyAsync(cnt, m->conv_counts, sizeof cnt, cudaMemcpyDeviceToHost, m->stream) !=
+                cudaSuccess || cudaStreamSynchronize(m->stream) != cudaSuccess)
+            return bad(Q3_ERR_CUDA, "fp16 weight copy failed");
+        if (cnt[1])
+            return bad(Q3_ERR_INVALID_ARG, "weights beyond the fp16 range of the tensor-core path");
+        m->inexact_f16 = (int64_t)cnt[0];
+    }
     if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
     if (cudaStreamSynchronize(m->stream) != cudaSuccess || cudaGetLastError() != cudaSuccess)
         return bad(Q3_ERR_CUDA, "model setup failed");
@@ -758,8 +811,7 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
 void q3_model_destroy(q3_model* m)
 {
     if (!m) return;
-    cudaStreamSynchronize(m->stream);
-    free_model(m);
+    model_release(m);
 }
 
 int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
@@ -791,6 +843,7 @@ int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
     }
     for (int b = 0; b < n_blocks; ++b) p->free_blocks.insert(p->free_blocks.end(), b);
     p->slot_used.assign(max_sessions, 0);
+    ++m->refs;
     *out = p;
     return Q3_OK;
 }
@@ -798,10 +851,7 @@ int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
 void q3_pool_destroy(q3_pool* p)
 {
     if (!p) return;
-    cudaStreamSynchronize(p->m->stream);
-    cudaFree(p->kv);
-    cudaFree(p->tables);
-    delete p;
+    pool_release(p);
 }
 
 int q3_session_create(q3_pool* p, q3_session** out)
@@ -816,7 +866,7 @@ int q3_session_create(q3_pool* p, q3_session** out)
     s->pool = p;
     s->slot = slot;
     p->slot_used[slot] = 1;
-    ++p->live;
+    ++p->refs;
     *out = s;
     return Q3_OK;
 }
@@ -824,10 +874,11 @@ int q3_session_create(q3_pool* p, q3_session** out)
 void q3_session_destroy(q3_session* s)
 {
     if (!s) return;
-    for (int b : s->blocks) s->pool->free_blocks.insert(b);
-    s->pool->slot_used[s->slot] = 0;
-    --s->pool->live;
+    q3_pool* p = s->pool;
+    for (int b : s->blocks) p->free_blocks.insert(b);
+    p->slot_used[s->slot] = 0;
     delete s;
+    pool_release(p);
 }
 
 int q3_session_set_block_table(q3_session* s, const int32_t* ids, int n)
@@ -934,7 +985,7 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
         return fail(Q3_ERR_INVALID_ARG, "op_matmul: bad argument");
     const int bn = gemm_block_n(N);
     CUtensorMap a, b;
-    if (!tmap_bf16(&a, w_dev, M, K, 128) || !tmap_bf16(&b, x_dev, round_up(N, 256), K, bn))
+    if (!tmap_f16(&a, w_dev, M, K, 128) || !tmap_f16(&b, x_dev, round_up(N, 256), K, bn))
         return fail(Q3_ERR_CUDA, "op_matmul: tensor map encoding failed");
     static int* status = nullptr;
     if (!status && cudaMalloc(&status, sizeof(int)) != cudaSuccess)

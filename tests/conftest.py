@@ -17,3 +17,19 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write every checked parity row to $Q3_PARITY_REPORT (JSON lines), if set."""
+    path = os.environ.get("Q3_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        import dataclasses
+        import json
+        from helpers import REPORT
+    except ImportError:
+        return
+    with open(path, "w") as f:
+        for tag, c in REPORT:
+            f.write(json.dumps({"tag": tag, **dataclasses.asdict(c), "ambiguous": c.ambiguous}) + "\n")

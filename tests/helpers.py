@@ -48,10 +48,16 @@ class RowCheck:
         return self.nmse <= NMSE_BOUND and (self.argmax_gpu == self.argmax_ref or self.ambiguous)
 
 
-def check_row(got: np.ndarray, ref: np.ndarray) -> RowCheck:
+REPORT: list = []      # (tag, RowCheck) of every checked row, for the parity report
+
+
+def check_row(got: np.ndarray, ref: np.ndarray, tag: str = "") -> RowCheck:
     top2 = np.partition(ref, -2)[-2:]
-    return RowCheck(nmse(got, ref), int(np.argmax(got)), int(np.argmax(ref)),
-                    float(top2[1] - top2[0]), float(np.abs(got.astype(np.float64) - ref).max()))
+    c = RowCheck(nmse(got, ref), int(np.argmax(got)), int(np.argmax(ref)),
+                 float(top2[1] - top2[0]), float(np.abs(got.astype(np.float64) - ref).max()))
+    if tag:
+        REPORT.append((tag, c))
+    return c
 
 
 class Pair:

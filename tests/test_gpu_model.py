@@ -28,14 +28,14 @@ def _run(pair, g, o, rounds, n_decode, tag=""):
     checks = []
     for r in rounds:
         got, ref, am = pair.eval(g, o, r)
-        c = check_row(got, ref)
+        c = check_row(got, ref, f"{tag}/prefill{len(r)}")
         assert am == c.argmax_gpu
         checks.append(c)
         assert c.ok, (tag, "prefill", len(r), c)
     tok = checks[-1].argmax_ref
     for step in range(n_decode):
         got, ref, am = pair.eval(g, o, [tok])
-        c = check_row(got, ref)
+        c = check_row(got, ref, f"{tag}/decode")
         assert am == c.argmax_gpu
         checks.append(c)
         assert c.ok, (tag, "decode", step, c)

@@ -4,8 +4,8 @@ seeded inputs (the pages' operator tests: "Reproducing Kipp", section
 
 - Q8_0 packing: the library's CUDA quantizer and the oracle's packer agree
   bit for bit ("Kipp Model Support", section "Quantization (Q8_0)").
-- tcgen05 GEMM: bf16 inputs, FP32 accumulation, against the oracle's FP64
-  matmul; shapes span several tiles and ragged token counts (1, 5, 40, 83,
+- tcgen05 GEMM: fp16 inputs (the prefill operand type), FP32 accumulation,
+  against an FP64 matmul of the same values; shapes span several tiles and ragged token counts (1, 5, 40, 83,
   200, 300) so every N tile width and the tile tail are exercised.
 - Decode GEMV, BF16 and Q8_0 planes, against the oracle.
 Tolerance: the products are exact in FP32 and only the K-term FP32
@@ -48,10 +48,12 @@ def test_quantizer_matches_oracle_packer_bitwise(q3, orc):
 @pytest.mark.parametrize("n", [1, 5, 32, 40, 83, 200, 300])
 @pytest.mark.parametrize("M,K", [(256, 64), (384, 2560), (128, 9728)])
 def test_tcgen05_matmul_matches_oracle(q3, orc, n, M, K):
+    # bf16-valued weights (exact in fp16) so the oracle's bf16 matmul applies
     w = _bf16((M, K), 10 + n, 0.05)
     rows = (n + 255) // 256 * 256
-    x = _bf16((rows, K), 20 + n)
-    y = q3.op_matmul(w, x, n)
+    x = torch.randn(rows, K, generator=torch.Generator(device="cuda").manual_seed(20 + n),
+                    device="cuda").to(torch.float16)
+    y = q3.op_matmul(w.to(torch.float16), x, n)
     torch.cuda.synchronize()
     wb = w.view(torch.int16).cpu().numpy().view(np.uint16)
     xf = _f32(x[:n])
