@@ -1,0 +1,491 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 forward on the Qwen3-4B shape.
+
+Workload (seeded, synthetic, random-init weights of the shape): 36 layers,
+hidden 2560, 32 query / 8 KV heads of width 128, FFN 9728, vocabulary
+151,936, tied embedding, BF16 weights ~N(0, 0.02), paged BF16 KV in
+32-position blocks.  A 2,048-token prompt is prefilled at batch 1, then the
+session decodes greedily (the argmax of each step is the next token, on the
+device).  Separately, 32 sessions with prompt lengths uniform in [64, 2048]
+decode together.
+
+A step is one decode token of the batch-1 session: one pass of every row of
+the forward (embedding, RMSNorm, QKV, q/k norm + RoPE + KV append, paged GQA
+attention, O, SwiGLU FFN, final norm, lm_head, argmax).  `value` is decode
+tokens/s at batch 1 with inputs resident on the device; the weights (8 GB)
+exceed L2, so no flush is needed between steps.  Prefill and batch-32 decode
+are reported beside it.
+
+Kernel rooflines come from a second, profiled pass of the same steps: the
+library brackets every launch with CUDA events on its own stream
+(q3_model_profile), and the dominant kernel's algorithmic bytes (or FLOPs)
+per launch are divided by its mean launch time.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the forward has no cross-GPU exchange); value = all ranks' tokens / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Qwen3-4B-shape decode tok/s (% HBM roofline); prefill tok/s (% BF16 TC peak)"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256, help="timed decode steps")
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--prompt", type=int, default=2048)
+    ap.add_argument("--sessions", type=int, default=32)
+    ap.add_argument("--no-b32", action="store_true", help="skip the batch-32 decode leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+def proj_params(s) -> int:
+    per_layer = (s.q_width + 2 * s.kv_width) * s.hidden + s.hidden * s.q_width + 3 * s.ffn * s.hidden
+    return per_layer * s.n_layers
+
+
+def decode_bytes(s, ctx: int, batch: int = 1, ctxs=None) -> float:
+    """HBM bytes one decode step must move: every weight once (bf16) plus the
+    K and V of every cached position of every session, per layer."""
+    w = 2.0 * proj_params(s) + 2.0 * s.vocab * s.hidden
+    kv_per_pos = s.n_layers * 2 * s.kv_width * 2
+    total_ctx = sum(ctxs) if ctxs is not None else ctx * batch
+    return w + kv_per_pos * total_ctx
+
+
+def prefill_flops(s, T: int) -> float:
+    """2 * params * tokens for the projections, causal attention (QK^T and PV
+    over T^2/2 pairs), and the lm_head of the last row."""
+    return (2.0 * proj_params(s) * T + 2.0 * s.n_layers * s.q_width * T * T
+            + 2.0 * s.vocab * s.hidden)
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while a timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        mhz, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class Timer:
+    """CUDA events on the library's stream."""
+
+    def __init__(self, stream):
+        import torch
+        self.stream = stream
+        self.a = torch.cuda.Event(enable_timing=True)
+        self.b = torch.cuda.Event(enable_timing=True)
+
+    def start(self):
+        self.a.record(self.stream)
+
+    def stop(self) -> float:
+        self.b.record(self.stream)
+        self.b.synchronize()
+        return self.a.elapsed_time(self.b)
+
+
+def barrier(dist_on: bool):
+    if dist_on:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, dist_on: bool) -> float:
+    if not dist_on:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def decode_loop(sess, tok, logits, steps: int):
+    """steps greedy decode steps at batch 1: each step's argmax is written over
+    its own input token, so the next step reads it on the device."""
+    for _ in range(steps):
+        sess.eval(tok, logits, tok)
+
+
+def run_gpu(args, dist_on: bool, rank: int, world: int):
+    import numpy as np
+    import torch
+
+    import qwen3_dense_decoder_gb300 as q3
+    import synthetic
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    q3.build()
+    shape = synthetic.SHAPES["4b"]
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    W, K, P = args.warmup, args.steps, args.prompt
+    max_ctx = P + W + 3 * K + 64      # value, profiled and e2e passes share the session
+    w = synthetic.make_weights(shape, seed=1234, device="cuda")
+    model = q3.Model(shape, w, max_ctx=max_ctx, max_round_tokens=P, stream=stream)
+    n_sess = 2 + (0 if args.no_b32 else args.sessions)     # decode + profiled-prefill sessions
+    blocks_per = (max_ctx + 31) // 32
+    pool = model.pool(n_blocks=blocks_per * n_sess + 8, max_sessions=n_sess + 2)
+    V = shape.vocab
+    logits = torch.empty(max(args.sessions, 1), V, dtype=torch.float32, device="cuda")
+    amax = torch.empty(max(args.sessions, 1), dtype=torch.int32, device="cuda")
+    timer = Timer(stream)
+    out = {}
+
+    # ---- prefill at batch 1: a 2,048-token prompt into an empty session
+    prompt = torch.tensor(synthetic.make_tokens(P, V, seed=7), device="cuda")
+    sess = pool.session()
+    pre_ms = []
+    for it in range(W + 3):
+        sess.reset()
+        torch.cuda.synchronize()
+        timer.start()
+        sess.eval(prompt, logits[0], amax[0:1])
+        ms = timer.stop()
+        if it >= W:
+            pre_ms.append(ms)
+    model.sync()
+    out["prefill_ms"] = statistics.median(pre_ms)
+
+    # ---- decode at batch 1 (the value): W warm-up steps, then K timed steps
+    tok = amax[0:1].clone()
+    decode_loop(sess, tok, logits[0], W)
+    model.sync()
+    ctx0 = sess.pos
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    l0 = model.launch_count
+    with ClockSampler(local) as clk:
+        timer.start()
+        decode_loop(sess, tok, logits[0], K)
+        dec_ms = timer.stop()
+    torch.cuda.synchronize()
+    barrier(dist_on)
+    model.sync()
+    out["launches"] = model.launch_count - l0
+    out["decode_ms"] = dec_ms
+    out["decode_ctx"] = (ctx0 + 1, ctx0 + K)
+    out["clocks"] = clk.summary()
+
+    # ---- profiled pass of the same decode steps (per-kernel CUDA events)
+    model.profile(True)
+    model.profile_reset()
+    decode_loop(sess, tok, logits[0], K)
+    out["decode_profile"] = model.profile_read()
+    model.profile(False)
+    # ---- profiled prefill
+    sess2 = pool.session()
+    model.profile(True)
+    model.profile_reset()
+    sess2.eval(prompt, logits[0], amax[0:1])
+    out["prefill_profile"] = model.profile_read()
+    model.profile(False)
+    sess2.close()
+
+    # ---- end to end through the C ABI with host buffers: per step the token
+    # goes host->device from pinned memory and the logits and argmax come back
+    h_tok = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    h_logits = torch.empty(V, dtype=torch.float32, pin_memory=True)
+    h_am = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    h_tok.copy_(tok.cpu())
+    d_tok = torch.empty(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        d_tok.copy_(h_tok, non_blocking=True)
+        sess.eval(d_tok, logits[0], amax[0:1])
+        h_logits.copy_(logits[0], non_blocking=True)
+        h_am.copy_(amax[0:1], non_blocking=True)
+        stream.synchronize()
+        h_tok.copy_(h_am)
+    e2e_s = time.perf_counter() - t0
+    model.sync()
+    out["e2e_s"] = e2e_s
+    out["e2e_bytes"] = (4, 4 * V + 4)
+    sess.close()
+
+    # ---- decode at 32 sessions, prompts uniform in [64, 2048]
+    if not args.no_b32:
+        B = args.sessions
+        lens = synthetic.make_prompt_lengths(B, 64, P, seed=11)
+        sessions = [pool.session() for _ in range(B)]
+        for i, s in enumerate(sessions):
+            s.eval(torch.tensor(synthetic.make_tokens(int(lens[i]), V, seed=100 + i), device="cuda"),
+                   logits[0], amax[i:i + 1])
+        model.sync()
+        toks = amax[:B].clone()
+        ones = [1] * B
+        for _ in range(W):
+            model.eval_batch(sessions, toks, ones, logits[:B], toks)
+        model.sync()
+        ctx_b = [s.pos for s in sessions]
+        barrier(dist_on)
+        torch.cuda.synchronize()
+        timer.start()
+        for _ in range(K):
+            model.eval_batch(sessions, toks, ones, logits[:B], toks)
+        b32_ms = timer.stop()
+        model.sync()
+        model.profile(True)
+        model.profile_reset()
+        for _ in range(min(K, 32)):
+            model.eval_batch(sessions, toks, ones, logits[:B], toks)
+        out["b32_profile"] = model.profile_read()
+        out["b32_profile_steps"] = min(K, 32)
+        model.profile(False)
+        out["b32_ms"] = b32_ms
+        out["b32_ctx"] = [c + K / 2 for c in ctx_b]
+        for s in sessions:
+            s.close()
+    out["shape"] = shape
+    out["weights"] = w
+    return out
+
+
+# ---------------------------------------------------------------- CPU baseline (the oracle)
+
+def oracle_decode_sample(shape, weights, budget_s: float, max_steps: int, warmup: int = 1):
+    """Time the oracle (plain C, FP64 accumulation) on greedy decode steps of
+    the same shape after a 16-token prompt, on this host's cores."""
+    import numpy as np
+
+    import oracle
+    import synthetic
+    oracle.build()
+    m = oracle.Model(shape, weights)
+    s = m.session(max_ctx=16 + warmup + max_steps + 1)
+    lg = s.eval(synthetic.make_tokens(16, shape.vocab, seed=7))
+    tok = int(np.argmax(lg))
+    for _ in range(warmup):
+        tok = int(np.argmax(s.eval([tok])))
+    t0 = time.perf_counter()
+    steps = 0
+    while steps < max_steps:
+        tok = int(np.argmax(s.eval([tok])))
+        steps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    ctx = 16 + warmup
+    return {"value": steps / dt, "unit": "tok/s", "cores": m.n_threads, "kind": "oracle",
+            "sample": (f"{steps} greedy decode steps of the full 36-layer Qwen3-4B shape at batch 1 "
+                       f"after a 16-token prompt (context {ctx + 1}..{ctx + steps} instead of "
+                       f"~{2048 + 128}: attention is under 8% of a step's work at that length)"),
+            "seconds": dt, "steps": steps}
+
+
+# ---------------------------------------------------------------- report
+
+def workload_config(args):
+    return {"workload": (f"qwen3-4b-shape (36 layers, hidden 2560, 32/8 heads x 128, FFN 9728, "
+                         f"vocab 151936, tied, bf16 N(0,0.02) random init); {args.prompt}-token "
+                         f"prefill at batch 1, then {args.steps} greedy decode steps at batch 1 "
+                         f"(value) and at {args.sessions} sessions with prompts U[64, {args.prompt}]"),
+            "l2": "inputs larger than L2: 8.0 GB of weights streamed per decode step",
+            "kv": "paged bf16, 32-position blocks", "parallelism": f"replicas x{args.gpus}"}
+
+
+def report(args, res, world, dist_on, pk, pk_kind):
+    s = res["shape"]
+    K = args.steps
+    dec_ms = max_over_ranks(res["decode_ms"], dist_on)
+    value = world * K / (dec_ms / 1e3)
+    c0, c1 = res["decode_ctx"]
+    mean_ctx = (c0 + c1) / 2
+    step_bytes = decode_bytes(s, mean_ctx)
+    w_bytes = 2.0 * proj_params(s) + 2.0 * s.vocab * s.hidden
+    gemv_ms, gemv_n = res["decode_profile"]["gemv"]
+    gemv_achieved = (w_bytes * K / gemv_n) / (gemv_ms / gemv_n / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(dec_ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights and tokens of the named shape)",
+        "config": workload_config(args),
+        "hbm_roofline": {"achieved_gbs": round(step_bytes * value / world / 1e9, 1),
+                         "bytes_per_step": step_bytes, "peak_gbs": pk["hbm_gbs"],
+                         "frac": round(step_bytes * value / world / 1e9 / pk["hbm_gbs"], 4),
+                         "peak_kind": pk_kind},
+        "roofline": {"kernel": "gemv (decode matvec, all projections + lm_head)", "bound": "hbm",
+                     "achieved": round(gemv_achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gemv_achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "bytes_per_launch": w_bytes * K / gemv_n, "launches": gemv_n,
+                     "mean_launch_us": round(gemv_ms / gemv_n * 1e3, 3), "peak_kind": pk_kind},
+        "clocks": res["clocks"],
+        "gpu_launches": res["launches"],
+        "decode_kernels_ms_per_step": {k: round(v[0] / K, 4) for k, v in res["decode_profile"].items()},
+    }
+    # prefill
+    P = args.prompt
+    pre_ms = max_over_ranks(res["prefill_ms"], dist_on)
+    fl = prefill_flops(s, P)
+    gemm_ms, gemm_n = res["prefill_profile"]["gemm"]
+    gemm_fl = 2.0 * proj_params(s) * P
+    line["prefill"] = {
+        "value": round(world * P / (pre_ms / 1e3), 1), "unit": "tok/s", "ms": round(pre_ms, 3),
+        "tc_roofline": {"achieved_tflops": round(fl / (pre_ms / 1e3) / 1e12, 1),
+                        "peak": pk["bf16_tflops"], "frac": round(fl / (pre_ms / 1e3) / 1e12 / pk["bf16_tflops"], 4),
+                        "flops": fl, "peak_kind": pk_kind},
+        "roofline": {"kernel": "gemm (tcgen05 projections)", "bound": "tensor",
+                     "achieved": round(gemm_fl / (gemm_ms / 1e3) / 1e12, 1), "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(gemm_fl / (gemm_ms / 1e3) / 1e12 / pk["bf16_tflops"], 4),
+                     "traffic": None, "launches": gemm_n, "peak_kind": pk_kind},
+        "kernels_ms": {k: round(v[0], 3) for k, v in res["prefill_profile"].items()},
+    }
+    if "b32_ms" in res:
+        B = args.sessions
+        b_ms = max_over_ranks(res["b32_ms"], dist_on)
+        b_val = world * B * K / (b_ms / 1e3)
+        b_bytes = decode_bytes(s, 0, ctxs=res["b32_ctx"])
+        line["decode_b32"] = {
+            "value": round(b_val, 1), "unit": "tok/s", "ms_per_step": round(b_ms / K, 4),
+            "hbm_roofline": {"achieved_gbs": round(b_bytes * K / (b_ms / 1e3) / 1e9, 1),
+                             "bytes_per_step": b_bytes,
+                             "frac": round(b_bytes * K / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)},
+            "kernels_ms_per_step": {k: round(v[0] / res["b32_profile_steps"], 4)
+                                    for k, v in res["b32_profile"].items()},
+        }
+    e_s = max_over_ranks(res["e2e_s"], dist_on)
+    line["e2e"] = {"value": round(world * K / e_s, 2), "unit": "tok/s",
+                   "h2d_bytes_per_step": res["e2e_bytes"][0], "d2h_bytes_per_step": res["e2e_bytes"][1]}
+    return line
+
+
+# ---------------------------------------------------------------- main
+
+def reference_arm(args, rank: int):
+    """The oracle timed on this host's cores, on the same metric and workload shape."""
+    if rank != 0:
+        return
+    import synthetic
+    shape = synthetic.SHAPES["4b"]
+    w = synthetic.make_weights(shape, seed=1234, device="cpu")
+    # every timed step is one full decode token; the count is capped so the
+    # run stays within a few minutes
+    cb = oracle_decode_sample(shape, w, budget_s=120.0, max_steps=args.steps, warmup=args.warmup)
+    line = {"metric": METRIC, "value": round(cb["value"], 4), "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 / cb["value"], 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded random-init weights and tokens of the named shape)",
+            "config": workload_config(args), "impl": "reference",
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": round(cb["value"], 4), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    line["cpu_baseline"]["sample"] += f"; {cb['steps']} of the {args.steps} requested steps timed"
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist_on = world > 1
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    if dist_on:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    pk, pk_kind = peaks()
+    res = run_gpu(args, dist_on, rank, world)
+    line = report(args, res, world, dist_on, pk, pk_kind)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = oracle_decode_sample(res["shape"], res["weights"], budget_s=20.0,
+                                                    max_steps=16)
+        for k in ("seconds", "steps"):
+            line["cpu_baseline"].pop(k, None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -218,6 +218,25 @@ const char* q3_last_error(void);
 /* Number of kernel launches this model has issued (for launch accounting). */
 int64_t q3_model_launch_count(const q3_model* m);
 
+/* Per-kernel timing for measurement (no counterpart on the pages beyond
+ * their isolated matmul instrument, "Kipp Roadmap", status v0.0.5).  While
+ * on, every kernel launch of the model's rounds is bracketed by CUDA events
+ * on the model's stream, which serialises the launches (no programmatic
+ * overlap), so a profiled round runs slower than an unprofiled one.
+ * q3_model_profile_read synchronises the stream and returns, for kernel
+ * class cls, the summed device time in ms and the launch count since the
+ * last reset.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+#define Q3_K_GEMV 0      /* decode matvec (projections, lm_head) */
+#define Q3_K_GEMM 1      /* tcgen05 GEMM and its split-K reduce */
+#define Q3_K_ATTN 2      /* attention and split combine */
+#define Q3_K_ROPE 3      /* q/k norm + RoPE + KV append */
+#define Q3_K_NORM 4      /* embedding and RMSNorm */
+#define Q3_K_OTHER 5     /* argmax, Q8_0 dequantisation */
+#define Q3_K_CLASSES 6
+int q3_model_profile(q3_model* m, int on);
+int q3_model_profile_reset(q3_model* m);
+int q3_model_profile_read(q3_model* m, int cls, double* total_ms, int64_t* launches);
+
 #ifdef __cplusplus
 }
 #endif

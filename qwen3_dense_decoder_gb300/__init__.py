@@ -82,6 +82,9 @@ def lib():
         L.q3_model_launch_count.argtypes = [vp]
         L.q3_model_launch_count.restype = i64
         L.q3_op_matmul.argtypes = [vp, vp, i, i, i, vp, vp]
+        L.q3_model_profile.argtypes = [vp, i]
+        L.q3_model_profile_reset.argtypes = [vp]
+        L.q3_model_profile_read.argtypes = [vp, i, C.POINTER(C.c_double), C.POINTER(C.c_int64)]
         L.q3_op_matvec.argtypes = [vp, vp, vp, i, i, vp, vp]
         _lib = L
     return _lib
@@ -188,6 +191,24 @@ class Model:
     @property
     def launch_count(self) -> int:
         return lib().q3_model_launch_count(self.h)
+
+    KERNEL_CLASSES = ("gemv", "gemm", "attention", "qk_norm_rope_append", "norm", "other")
+
+    def profile(self, on: bool) -> None:
+        """Per-launch CUDA-event timing by kernel class (serialises launches)."""
+        _check(lib().q3_model_profile(self.h, int(on)))
+
+    def profile_reset(self) -> None:
+        _check(lib().q3_model_profile_reset(self.h))
+
+    def profile_read(self) -> dict:
+        """{class: (total device ms, launches)} since the last reset."""
+        out = {}
+        for i, name in enumerate(self.KERNEL_CLASSES):
+            ms, n = C.c_double(), C.c_int64()
+            _check(lib().q3_model_profile_read(self.h, i, C.byref(ms), C.byref(n)))
+            out[name] = (ms.value, n.value)
+        return out
 
     def eval_batch(self, sessions, tokens: torch.Tensor, n, logits: torch.Tensor,
                    argmax: torch.Tensor | None = None) -> None:

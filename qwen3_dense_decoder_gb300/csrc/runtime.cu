@@ -148,6 +148,47 @@ struct q3_model {
     CUtensorMap deq_qkv{}, deq_o{}, deq_g{}, deq_u{}, deq_d{};
     std::map<std::tuple<const void*, int, int>, CUtensorMap> act_maps;
 
+    // per-launch event timing (q3_model_profile)
+    bool prof_on = false;
+    struct ProfRec { cudaEvent_t a, b; int cls; };
+    std::vector<ProfRec> prof_pending;
+    std::vector<cudaEvent_t> prof_free;
+    double prof_ms[Q3_K_CLASSES] = {};
+    int64_t prof_n[Q3_K_CLASSES] = {};
+    cudaEvent_t prof_event()
+    {
+        cudaEvent_t e = nullptr;
+        if (!prof_free.empty()) { e = prof_free.back(); prof_free.pop_back(); }
+        else cudaEventCreate(&e);
+        return e;
+    }
+    void prof_begin(int cls)
+    {
+        if (!prof_on) return;
+        ProfRec r{prof_event(), prof_event(), cls};
+        cudaEventRecord(r.a, stream);
+        prof_pending.push_back(r);
+    }
+    void prof_end()
+    {
+        if (prof_on && !prof_pending.empty()) cudaEventRecord(prof_pending.back().b, stream);
+    }
+    int prof_collect()
+    {
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return Q3_ERR_CUDA;
+        for (auto& r : prof_pending) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+                prof_ms[r.cls] += ms;
+                prof_n[r.cls] += 1;
+            }
+            prof_free.push_back(r.a);
+            prof_free.push_back(r.b);
+        }
+        prof_pending.clear();
+        return Q3_OK;
+    }
+
     int check(cudaError_t e, const char* what)
     {
         if (e == cudaSuccess) return Q3_OK;
@@ -298,10 +339,11 @@ int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtens
     g.out = out; g.ldo = ldo;
     g.ws = m->ws;
     g.status = m->status;
-    Launch L{m->stream, m->pdl, &m->launches};
+    Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
+    m->prof_begin(Q3_K_GEMM);
     int rc = m->check(launch_gemm(L, *a0, a1 ? *a1 : *a0, a2 ? *a2 : *a0, *b, bn, g), "gemm");
-    if (rc) return rc;
-    if (splits > 1) rc = m->check(launch_gemm_splitk_reduce(L, g), "gemm reduce");
+    if (rc == Q3_OK && splits > 1) rc = m->check(launch_gemm_splitk_reduce(L, g), "gemm reduce");
+    m->prof_end();
     return rc;
 }
 
@@ -327,8 +369,11 @@ int gemv(q3_model* m, int n_tensors, const void* const* w, const __half* const* 
     a.epi = epi;
     a.out = out;
     a.status = m->status;
-    Launch L{m->stream, m->pdl, &m->launches};
-    return m->check(launch_gemv(L, sc ? Q3_Q8_0 : Q3_BF16, a), "gemv");
+    Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
+    m->prof_begin(Q3_K_GEMV);
+    const int rc = m->check(launch_gemv(L, sc ? Q3_Q8_0 : Q3_BF16, a), "gemv");
+    m->prof_end();
+    return rc;
 }
 
 int run_round(q3_model* m, const Round& r)
@@ -340,12 +385,19 @@ int run_round(q3_model* m, const Round& r)
     const int* last_rows = m->meta + 2 * m->max_rows;
     const bool one = (T == 1);
     const bool q8 = c.scheme == Q3_Q8_0;
-    Launch L{m->stream, m->pdl, &m->launches};
+    Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
+    // one launcher call, bracketed by profiling events of kernel class cls
+    auto run = [m](int cls, auto&& launch) {
+        m->prof_begin(cls);
+        const cudaError_t e = launch();
+        m->prof_end();
+        return e;
+    };
     const size_t layer_kv = (size_t)r.pool->n_blocks * 2 * c.n_kv_heads * 32 * 128;
     const int n_splits = attention_splits(m, T, r.max_ctx);
     int rc;
 
-    if ((rc = m->check(launch_embed(L, r.tokens, T, m->embed, H, c.vocab, m->x, m->status), "embed")))
+    if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_embed(L, r.tokens, T, m->embed, H, c.vocab, m->x, m->status); }), "embed")))
         return rc;
 
     for (int l = 0; l < c.n_layers; ++l) {
@@ -367,15 +419,15 @@ int run_round(q3_model* m, const Round& r)
             if ((rc = gemv(m, 3, w, q8 ? sc : nullptr, rows, 0, H, m->x, attn_norm, EPI_STORE_F32, m->qkv)))
                 return rc;
         } else {
-            if ((rc = m->check(launch_rmsnorm_f16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->ha, m->status),
+            if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->ha, m->status); }),
                                "rmsnorm")))
                 return rc;
             if (q8) {
                 size_t off = 0;
                 for (int i = 0; i < 3; ++i) {
                     const int rows = i == 0 ? m->qw : m->kvw;
-                    if ((rc = m->check(launch_q8_to_f16(L, m->q8[l][P_Q + i].qs, m->q8[l][P_Q + i].sc,
-                                                         (int64_t)rows * H, m->deq + off), "dequant")))
+                    if ((rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_Q + i].qs, m->q8[l][P_Q + i].sc,
+                                                         (int64_t)rows * H, m->deq + off); }), "dequant")))
                         return rc;
                     off += (size_t)rows * H;
                 }
@@ -399,7 +451,7 @@ int run_round(q3_model* m, const Round& r)
         ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
         ra.n_blocks = r.pool->n_blocks;
         ra.q_out = m->q; ra.status = m->status;
-        if ((rc = m->check(launch_qk_norm_rope_append(L, ra), "qk-norm/rope/append"))) return rc;
+        if ((rc = m->check(run(Q3_K_ROPE, [&] { return launch_qk_norm_rope_append(L, ra); }), "qk-norm/rope/append"))) return rc;
 
         // ---- attention
         AttnArgs aa{};
@@ -412,7 +464,7 @@ int run_round(q3_model* m, const Round& r)
         aa.out = one ? (void*)m->attf : (void*)m->att;
         aa.out_f16 = one ? 0 : 1;
         aa.status = m->status;
-        if ((rc = m->check(launch_attention(L, aa), "attention"))) return rc;
+        if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_attention(L, aa); }), "attention"))) return rc;
 
         // ---- O projection + residual
         if (one) {
@@ -423,8 +475,8 @@ int run_round(q3_model* m, const Round& r)
                 return rc;
         } else {
             if (q8) {
-                if ((rc = m->check(launch_q8_to_f16(L, m->q8[l][P_O].qs, m->q8[l][P_O].sc,
-                                                     (int64_t)H * m->qw, m->deq), "dequant")))
+                if ((rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_O].qs, m->q8[l][P_O].sc,
+                                                     (int64_t)H * m->qw, m->deq); }), "dequant")))
                     return rc;
                 rc = gemm(m, &m->deq_o, nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
                           EPI_ADD_F32, m->x, H);
@@ -454,14 +506,14 @@ int run_round(q3_model* m, const Round& r)
             if ((rc = gemv(m, 1, wd, q8 ? scd : nullptr, rowsd, 0, F, m->sf, nullptr, EPI_ADD_F32, m->x)))
                 return rc;
         } else {
-            if ((rc = m->check(launch_rmsnorm_f16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->ha, m->status),
+            if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->ha, m->status); }),
                                "rmsnorm")))
                 return rc;
             if (q8) {
-                if ((rc = m->check(launch_q8_to_f16(L, m->q8[l][P_G].qs, m->q8[l][P_G].sc,
-                                                     (int64_t)F * H, m->deq), "dequant")) ||
-                    (rc = m->check(launch_q8_to_f16(L, m->q8[l][P_U].qs, m->q8[l][P_U].sc,
-                                                     (int64_t)F * H, m->deq + (size_t)F * H), "dequant")))
+                if ((rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_G].qs, m->q8[l][P_G].sc,
+                                                     (int64_t)F * H, m->deq); }), "dequant")) ||
+                    (rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_U].qs, m->q8[l][P_U].sc,
+                                                     (int64_t)F * H, m->deq + (size_t)F * H); }), "dequant")))
                     return rc;
                 rc = gemm(m, &m->deq_g, &m->deq_u, nullptr, 0, 0, 1, 2 * F, T, H, m->ha, EPI_SWIGLU_F16,
                           m->s, F);
@@ -471,8 +523,8 @@ int run_round(q3_model* m, const Round& r)
             }
             if (rc) return rc;
             if (q8) {
-                if ((rc = m->check(launch_q8_to_f16(L, m->q8[l][P_D].qs, m->q8[l][P_D].sc,
-                                                     (int64_t)H * F, m->deq), "dequant")))
+                if ((rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_D].qs, m->q8[l][P_D].sc,
+                                                     (int64_t)H * F, m->deq); }), "dequant")))
                     return rc;
                 rc = gemm(m, &m->deq_d, nullptr, nullptr, H / 128, H / 128, 0, H, T, F, m->s, EPI_ADD_F32,
                           m->x, H);
@@ -492,14 +544,14 @@ int run_round(q3_model* m, const Round& r)
                        EPI_STORE_F32, r.logits)))
             return rc;
     } else {
-        if ((rc = m->check(launch_rmsnorm_f16(L, m->x, last_rows, r.ns, H, m->final_norm, c.rms_eps,
-                                              m->hfin, m->status), "final norm")))
+        if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, last_rows, r.ns, H, m->final_norm, c.rms_eps,
+                                              m->hfin, m->status); }), "final norm")))
             return rc;
         if ((rc = gemm(m, &m->lm_map, nullptr, nullptr, c.vocab / 128, c.vocab / 128, 0, c.vocab, r.ns, H,
                        m->hfin, EPI_STORE_F32, r.logits, c.vocab)))
             return rc;
     }
-    if (r.argmax && (rc = m->check(launch_argmax(L, r.logits, r.ns, c.vocab, r.argmax), "argmax")))
+    if (r.argmax && (rc = m->check(run(Q3_K_OTHER, [&] { return launch_argmax(L, r.logits, r.ns, c.vocab, r.argmax); }), "argmax")))
         return rc;
     return Q3_OK;
 }
@@ -594,6 +646,8 @@ void free_model(q3_model* m)
     if (m->stream || !m->allocs.empty()) cudaStreamSynchronize(m->stream);
     for (void* p : m->allocs) cudaFree(p);
     for (auto& e : m->stage_ev) cudaEventDestroy(e);
+    for (auto& r : m->prof_pending) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+    for (auto& e : m->prof_free) cudaEventDestroy(e);
     if (m->stage) cudaFreeHost(m->stage);
     delete m;
 }
@@ -975,6 +1029,32 @@ int q3_quantize_q8_0(const void* w_dev, int64_t n, void* blocks_dev, void* strea
     cudaError_t e = launch_quantize_q8_0(static_cast<cudaStream_t>(stream), static_cast<const bf16*>(w_dev),
                                          n, static_cast<uint8_t*>(blocks_dev));
     if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "quantize: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+int q3_model_profile(q3_model* m, int on)
+{
+    if (!m) return fail(Q3_ERR_INVALID_ARG, "profile: NULL model");
+    if (m->prof_on && !on && m->prof_collect() != Q3_OK) return fail(Q3_ERR_CUDA, "profile: sync failed");
+    m->prof_on = on != 0;
+    return Q3_OK;
+}
+
+int q3_model_profile_reset(q3_model* m)
+{
+    if (!m) return fail(Q3_ERR_INVALID_ARG, "profile: NULL model");
+    if (m->prof_collect() != Q3_OK) return fail(Q3_ERR_CUDA, "profile: sync failed");
+    for (int i = 0; i < Q3_K_CLASSES; ++i) { m->prof_ms[i] = 0; m->prof_n[i] = 0; }
+    return Q3_OK;
+}
+
+int q3_model_profile_read(q3_model* m, int cls, double* total_ms, int64_t* launches)
+{
+    if (!m || cls < 0 || cls >= Q3_K_CLASSES || !total_ms || !launches)
+        return fail(Q3_ERR_INVALID_ARG, "profile_read: bad argument");
+    if (m->prof_collect() != Q3_OK) return fail(Q3_ERR_CUDA, "profile: sync failed");
+    *total_ms = m->prof_ms[cls];
+    *launches = m->prof_n[cls];
     return Q3_OK;
 }
 
