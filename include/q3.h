@@ -212,6 +212,30 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
 int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, int M, int K,
                  float* y_dev, void* stream);
 
+/* Split-K matmul that allocates nothing (the Kipp pages have no counterpart;
+ * this entry point serves callers that cannot call cudaMalloc where they need
+ * the product: a host framework that owns all device memory through its own
+ * allocator, a plug-in that may not grow its footprint, a latency-critical
+ * loop that cannot afford cudaMalloc's implicit synchronisation).
+ * y[n][m] = sum_k w[m][k] * x[n][k], the same tcgen05 GEMM as q3_op_matmul
+ * with K split over k_splits CTAs; the split partial sums live in a fixed
+ * scratch array of Q3_NOALLOC_SCRATCH_FLOATS floats (8 MiB) compiled into the
+ * library, which every GPU that loads the library holds until exit.
+ * w_dev: fp16 [M][K]; x_dev: fp16 [N][K] with at least round_up(N, 256)
+ * rows allocated; y_dev: f32 [N][M]; M a multiple of 128, K of 64, 1 <= N,
+ * 2 <= k_splits <= min(8, K/64), and k_splits * N * M must not exceed
+ * Q3_NOALLOC_SCRATCH_FLOATS (else Q3_ERR_INVALID_ARG, nothing launched).
+ * The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the scratch: calls whose
+ * kernels may overlap on the GPU race on it, so order them on one stream.
+ * Asynchronous on stream; allocates no device or host memory.  Errors (the
+ * message from q3_noalloc_last_error): Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+#define Q3_NOALLOC_SCRATCH_FLOATS (2 * 1024 * 1024)
+int q3_op_matmul_splitk_noalloc(const void* w_dev, const void* x_dev, int M, int N, int K,
+                                int k_splits, float* y_dev, void* stream);
+const char* q3_noalloc_last_error(void);
+
 /* Message of the last error on this host thread ("" if none). */
 const char* q3_last_error(void);
 

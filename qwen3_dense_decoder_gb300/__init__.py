@@ -82,6 +82,8 @@ def lib():
         L.q3_model_launch_count.argtypes = [vp]
         L.q3_model_launch_count.restype = i64
         L.q3_op_matmul.argtypes = [vp, vp, i, i, i, vp, vp]
+        L.q3_op_matmul_splitk_noalloc.argtypes = [vp, vp, i, i, i, i, vp, vp]
+        L.q3_noalloc_last_error.restype = C.c_char_p
         L.q3_model_profile.argtypes = [vp, i]
         L.q3_model_profile_reset.argtypes = [vp]
         L.q3_model_profile_read.argtypes = [vp, i, C.POINTER(C.c_double), C.POINTER(C.c_int64)]
@@ -124,6 +126,24 @@ def op_matmul(w: torch.Tensor, x: torch.Tensor, n: int, stream=None) -> torch.Te
     y = torch.empty(n, M, dtype=torch.float32, device=w.device)
     _check(lib().q3_op_matmul(_ptr(w), _ptr(x), M, n, K, _ptr(y), _stream_handle(stream)))
     return y
+
+
+NOALLOC_SCRATCH_FLOATS = 2 * 1024 * 1024
+
+
+def op_matmul_splitk_noalloc(w: torch.Tensor, x: torch.Tensor, n: int, k_splits: int,
+                             y: torch.Tensor, stream=None) -> None:
+    """Split-K matmul into the caller's y [n, M] f32 that allocates no device
+    memory: the partial sums use the library's fixed scratch array.  For
+    callers that cannot allocate at the call site (a framework-owned memory
+    pool, a plug-in, a latency-critical loop).  Calls that overlap on the GPU
+    race on the shared scratch."""
+    M, K = w.shape
+    assert w.dtype == x.dtype == torch.float16 and y.dtype == torch.float32
+    rc = lib().q3_op_matmul_splitk_noalloc(_ptr(w), _ptr(x), M, n, K, k_splits, _ptr(y),
+                                           _stream_handle(stream))
+    if rc != 0:
+        raise Q3Error(rc, lib().q3_noalloc_last_error().decode())
 
 
 def op_matvec(w: torch.Tensor, x: torch.Tensor, scales: torch.Tensor | None = None,
