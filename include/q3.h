@@ -207,7 +207,8 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
 /* q3_op_matvec: y[m] = sum_k w[m][k] * x[k] on the decode GEMV.  With
  * scales_dev == NULL, w_dev is bf16 [M][K]; otherwise w_dev is the int8
  * quant plane [M][K] and scales_dev the fp16 scale plane [M][K/32] of Q8_0
- * weights.  x_dev: f32 [K]; y_dev: f32 [M].  M a multiple of 8, K of 32.
+ * weights.  x_dev: f32 [K]; y_dev: f32 [M].  M a multiple of 8, K of 256;
+ * pointers 16-byte aligned.
  * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
 int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, int M, int K,
                  float* y_dev, void* stream);

@@ -20,6 +20,10 @@
 
 namespace q3 {
 
+Q3_DEV uint32_t smem_u32_early(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 Q3_DEV float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
 Q3_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 Q3_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -38,6 +42,44 @@ Q3_DEV uint64_t global_ns() {
 }
 
 Q3_DEV void set_status(int* status, int bits) { atomicOr(status, bits); }
+
+// ---------------------------------------------------------------- cp.async
+Q3_DEV void cp_async_16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"(smem_u32_early(smem_dst)), "l"(gmem_src) : "memory");
+}
+Q3_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+Q3_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// ---------------------------------------------------------------- per-head q/k norm + RoPE
+// One warp holds one 128-wide head, lane l elements [4l, 4l + 4).  RMSNorm
+// over the head with the shared gain, then rotate-half RoPE: element i < 64
+// pairs with i + 64 (lane l ^ 16); angle pos * theta^(-2i/128) from the
+// (cos, sin) table row of the position.
+Q3_DEV float warp_allsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+Q3_DEV void head_norm_rope(float (&y)[4], const __nv_bfloat16* gain, const float2* rope_row,
+                           float eps, int lane) {
+    const float ss = warp_allsum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
+    const float r = 1.0f / sqrtf(ss / 128.0f + eps);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = y[e] * r * __bfloat162float(gain[lane * 4 + e]);
+    const float2* cs = rope_row + (lane & 15) * 4;
+    float out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float z = __shfl_xor_sync(0xffffffffu, y[e], 16);
+        const float2 c = cs[e];
+        out[e] = lane < 16 ? y[e] * c.x - z * c.y      // first half: x1 cos - x2 sin
+                           : y[e] * c.x + z * c.y;     // second half: x2 cos + x1 sin
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = out[e];
+}
 
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch: a kernel may start while its predecessor
@@ -99,6 +141,30 @@ Q3_DEV void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int c0, int 
         " [%0], [%1, {%3, %4}], [%2];"
         :: "r"(smem_u32(dst)), "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
         : "memory");
+}
+
+// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned
+// addresses, size a multiple of 16)
+Q3_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// named barrier over a subset of the CTA's warps
+Q3_DEV void named_bar(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+// named barrier that also ANDs a predicate over the participating threads
+Q3_DEV bool named_bar_and(int id, int threads, bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "setp.ne.u32 p, %1, 0;\n\t"
+                 "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(threads) : "memory");
+    return r != 0;
 }
 
 Q3_DEV void prefetch_tmap(const void* tmap) {

@@ -9,13 +9,21 @@
 //
 // One CTA handles one (row, KV head, split): the G query heads that share the
 // KV head (contiguous GQA grouping, query head h reads KV head h / G) read
-// each K/V block once.  The split covers a contiguous range of logical
-// blocks whose bounds depend only on the context length, never on which
-// physical blocks back it, so paged and contiguous layouts give identical
-// bits.  Within a block, lane j scores position j; the values are then
-// accumulated with each lane owning 4 of the 128 output dimensions.  Warps
-// of the CTA take blocks round-robin and are merged in warp order; splits
-// are merged by attn_combine in split order.
+// each K/V block once.  A split is a contiguous range of logical blocks whose
+// bounds depend only on the context length, never on which physical blocks
+// back it, so paged and contiguous layouts give identical bits.  Each of the
+// four warps takes blocks round-robin and stages a block's K and V tiles in
+// shared memory with cp.async (one memory latency per block); lane j scores
+// position j, then each lane accumulates 4 of the 128 output dimensions.
+// Warps merge in warp order; splits merge in split order, done by whichever
+// split CTA of the (row, KV head) finishes last (an atomic ticket, no
+// waiting), so the result does not depend on scheduling.
+//
+// Decode rounds (each row the single new token of its session) fuse the
+// per-head q/k RMSNorm, RoPE and the K/V append of that token: the new K/V
+// row goes to the cache and straight into the staged tile, so tiles of
+// earlier positions can be fetched before the projections of this round
+// have landed (they are issued ahead of the programmatic-launch wait).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,41 +34,132 @@ namespace {
 constexpr int D = 128;
 constexpr int KV_BLOCK = 32;
 constexpr int AWARPS = 4;
+constexpr int K_STRIDE = D + 8;        // bf16 per staged K row: 272 bytes, conflict-free LDS.128
+constexpr int K_TILE = KV_BLOCK * K_STRIDE;
+constexpr int V_TILE = KV_BLOCK * D;
 
 Q3_DEV float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
-Q3_DEV float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 template <int G>
-__global__ void __launch_bounds__(AWARPS * 32) attn_split_kernel(const AttnArgs p)
+struct AttnSmem {
+    static constexpr size_t q_bytes = (size_t)G * D * sizeof(float);
+    static constexpr size_t k_bytes = (size_t)AWARPS * K_TILE * 2;
+    static constexpr size_t v_bytes = (size_t)AWARPS * V_TILE * 2;
+    static constexpr size_t new_bytes = 2 * D * 2;                  // new K and V row (bf16)
+    static constexpr size_t misc_bytes = 2 * AWARPS * G * sizeof(float) + 16;
+    static constexpr size_t total = q_bytes + k_bytes + v_bytes + new_bytes + misc_bytes;
+};
+
+// stage the K and V tiles of one 32-position block: 2 x 32 rows of 256 bytes,
+// 16-byte pieces, 16 per lane
+Q3_DEV void stage_block(__nv_bfloat16* kt, __nv_bfloat16* vt, const __nv_bfloat16* Kb,
+                        const __nv_bfloat16* Vb, int lane) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int piece = i * 32 + lane;          // 512 pieces: row = piece / 16, col16 = piece % 16
+        const int row = piece >> 4, c = piece & 15;
+        cp_async_16(kt + row * K_STRIDE + c * 8, Kb + row * D + c * 8);
+        cp_async_16(vt + row * D + c * 8, Vb + row * D + c * 8);
+    }
+    cp_async_commit();
+}
+
+template <int G, bool FUSED>
+__global__ void __launch_bounds__(AWARPS * 32) attn_kernel(const AttnArgs p)
 {
-    __shared__ __align__(16) float sq[G][D];
-    __shared__ float s_m[AWARPS][G], s_l[AWARPS][G];
-    __shared__ __align__(16) float s_o[AWARPS][G][D];
+    using S = AttnSmem<G>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float* sq = reinterpret_cast<float*>(smem);                                   // [G][D]
+    __nv_bfloat16* kt_all = reinterpret_cast<__nv_bfloat16*>(smem + S::q_bytes);
+    __nv_bfloat16* vt_all = reinterpret_cast<__nv_bfloat16*>(smem + S::q_bytes + S::k_bytes);
+    __nv_bfloat16* snew = reinterpret_cast<__nv_bfloat16*>(smem + S::q_bytes + S::k_bytes + S::v_bytes);
+    float* s_m = reinterpret_cast<float*>(smem + S::q_bytes + S::k_bytes + S::v_bytes + S::new_bytes);
+    float* s_l = s_m + AWARPS * G;
+    float* s_o = reinterpret_cast<float*>(kt_all);     // [AWARPS][G][D], reuses the K tiles at the end
+    __shared__ int s_ticket;
 
     const int split = blockIdx.x, kvh = blockIdx.y, t = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __nv_bfloat16* kt = kt_all + warp * K_TILE;
+    __nv_bfloat16* vt = vt_all + warp * V_TILE;
 
-    grid_dep_wait();
-
-    const int ctx = p.row_pos[t] + 1;
-    const int slot = p.row_slot[t];
+    // Row metadata and block tables were uploaded before the round began, so
+    // they may be read before the programmatic-launch wait.
+    const int pos = p.row_pos[t];
+    const int ctx = pos + 1;
+    const int* table = p.tables + (size_t)p.row_slot[t] * p.max_blocks;
     const int nblk = (ctx + KV_BLOCK - 1) / KV_BLOCK;
     const int bps = (nblk + p.n_splits - 1) / p.n_splits;
     const int b0 = split * bps;
     const int b1 = min(b0 + bps, nblk);
+    const size_t head_elems = (size_t)KV_BLOCK * D;
+    const int last_blk = nblk - 1;
 
-    // q of the G heads, scaled by log2(e) / sqrt(128)
-    const float qscale = 1.4426950408889634f * 0.08838834764831845f;
-    for (int i = threadIdx.x; i < G * D; i += AWARPS * 32)
-        sq[i / D][i % D] = p.q[((size_t)t * p.n_q + kvh * G + i / D) * D + i % D] * qscale;
+    auto block_ptr = [&](int b, const __nv_bfloat16*& Kb) -> bool {
+        const int phys = table[b];
+        if (phys < 0 || phys >= p.n_blocks) return false;
+        Kb = p.kv_layer + ((size_t)phys * 2 * p.n_kv + kvh) * head_elems;
+        return true;
+    };
+
+    int b = b0 + warp;
+    bool staged = false;
+    if (FUSED && b < b1) {
+        // K/V of earlier rounds do not depend on the kernels of this round
+        const __nv_bfloat16* Kb;
+        if (block_ptr(b, Kb)) {
+            stage_block(kt, vt, Kb, Kb + (size_t)p.n_kv * head_elems, lane);
+            staged = true;
+        }
+    }
+
+    // the next kernel may now be scheduled into the SM space this grid leaves
+    grid_dep_launch();
+    grid_dep_wait();
+
+    const float qscale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+    if (FUSED) {
+        const int n_heads = p.n_q + 2 * p.n_kv;
+        const float* row = p.qkv + (size_t)t * n_heads * D;
+        const float2* rope_row = p.rope + (size_t)pos * (D / 2);
+        for (int g = warp; g < G; g += AWARPS) {
+            const float4 v = *reinterpret_cast<const float4*>(row + (kvh * G + g) * D + lane * 4);
+            float y[4] = {v.x, v.y, v.z, v.w};
+            head_norm_rope(y, p.q_gain, rope_row, p.eps, lane);
+            *reinterpret_cast<float4*>(sq + g * D + lane * 4) =
+                make_float4(y[0] * qscale, y[1] * qscale, y[2] * qscale, y[3] * qscale);
+        }
+        const bool mine = b0 <= last_blk && last_blk < b1;   // this split holds the new position
+        if (mine && warp >= AWARPS - 2) {
+            const bool is_k = warp == AWARPS - 2;
+            const float4 v = *reinterpret_cast<const float4*>(
+                row + (p.n_q + (is_k ? 0 : p.n_kv) + kvh) * D + lane * 4);
+            float y[4] = {v.x, v.y, v.z, v.w};
+            if (is_k) head_norm_rope(y, p.k_gain, rope_row, p.eps, lane);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
+            uint2 packed;
+            packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(snew + (is_k ? 0 : D) + lane * 4) = packed;
+            const int phys = table[last_blk];
+            if (phys >= 0 && phys < p.n_blocks) {
+                __nv_bfloat16* dst = p.kv_layer +
+                    (((size_t)phys * 2 + (is_k ? 0 : 1)) * p.n_kv + kvh) * head_elems +
+                    (size_t)(pos % KV_BLOCK) * D + lane * 4;
+                *reinterpret_cast<uint2*>(dst) = packed;
+            } else if (lane == 0) {
+                set_status(p.status, Q3_STATUS_BLOCK_RANGE);
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < G * D; i += AWARPS * 32)
+            sq[i] = p.q[((size_t)t * p.n_q + kvh * G + i / D) * D + i % D] * qscale;
+    }
     __syncthreads();
 
     float m[G], l[G], o[G][4];
@@ -71,32 +170,43 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_split_kernel(const AttnArgs 
         o[g][0] = o[g][1] = o[g][2] = o[g][3] = 0.f;
     }
 
-    const int* table = p.tables + (size_t)slot * p.max_blocks;
-    const size_t head_elems = (size_t)KV_BLOCK * D;
-    for (int b = b0 + warp; b < b1; b += AWARPS) {
-        const int phys = table[b];
-        if (phys < 0 || phys >= p.n_blocks) {
-            if (lane == 0) set_status(p.status, Q3_STATUS_BLOCK_RANGE);
-            continue;
+    for (; b < b1; b += AWARPS) {
+        if (!staged) {
+            const __nv_bfloat16* Kb;
+            if (!block_ptr(b, Kb)) {
+                if (lane == 0) set_status(p.status, Q3_STATUS_BLOCK_RANGE);
+                continue;
+            }
+            stage_block(kt, vt, Kb, Kb + (size_t)p.n_kv * head_elems, lane);
         }
-        const __nv_bfloat16* Kb = p.kv_layer + ((size_t)phys * 2 * p.n_kv + kvh) * head_elems;
-        const __nv_bfloat16* Vb = Kb + (size_t)p.n_kv * head_elems;
+        staged = false;
+        cp_async_wait_all();
+        __syncwarp();
+        if (FUSED && b == last_blk) {
+            // the new position: its K/V were computed above, not read back
+            const int r = pos % KV_BLOCK;
+            *reinterpret_cast<uint2*>(kt + r * K_STRIDE + lane * 4) =
+                *reinterpret_cast<const uint2*>(snew + lane * 4);
+            *reinterpret_cast<uint2*>(vt + r * D + lane * 4) =
+                *reinterpret_cast<const uint2*>(snew + D + lane * 4);
+            __syncwarp();
+        }
         const bool valid = b * KV_BLOCK + lane < ctx;
 
-        // scores: lane j <- position b*32 + j
+        // scores: lane j <- position b * 32 + j
         float s[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) s[g] = 0.f;
-        const uint4* krow = reinterpret_cast<const uint4*>(Kb + (size_t)lane * D);
-#pragma unroll 4
+        const __nv_bfloat16* krow = kt + lane * K_STRIDE;
+#pragma unroll
         for (int c = 0; c < D / 8; ++c) {
-            const uint4 kw = __ldg(krow + c);
+            const uint4 kw = *reinterpret_cast<const uint4*>(krow + c * 8);
             const float k8[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
                                  bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float4 qa = *reinterpret_cast<const float4*>(&sq[g][c * 8]);
-                const float4 qb = *reinterpret_cast<const float4*>(&sq[g][c * 8 + 4]);
+                const float4 qa = *reinterpret_cast<const float4*>(sq + g * D + c * 8);
+                const float4 qb = *reinterpret_cast<const float4*>(sq + g * D + c * 8 + 4);
                 s[g] = fmaf(k8[0], qa.x, s[g]);
                 s[g] = fmaf(k8[1], qa.y, s[g]);
                 s[g] = fmaf(k8[2], qa.z, s[g]);
@@ -114,94 +224,137 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_split_kernel(const AttnArgs 
             const float m_new = fmaxf(m[g], warp_max(sg));
             const float alpha = exp2f(m[g] - m_new);      // 0 on the first block (m = -inf)
             pr[g] = valid ? exp2f(sg - m_new) : 0.f;
-            l[g] = l[g] * alpha + warp_sum(pr[g]);
+            l[g] = l[g] * alpha + warp_allsum(pr[g]);
             o[g][0] *= alpha; o[g][1] *= alpha; o[g][2] *= alpha; o[g][3] *= alpha;
             m[g] = m_new;
         }
-        // values: lane owns dims [4 lane, 4 lane + 4)
-        const int nvalid = min(KV_BLOCK, ctx - b * KV_BLOCK);
-        for (int j = 0; j < nvalid; ++j) {
-            const uint2 vw = __ldg(reinterpret_cast<const uint2*>(Vb + (size_t)j * D) + lane);
+        // values: lane owns dims [4 lane, 4 lane + 4); invalid positions have p = 0
+#pragma unroll 8
+        for (int j = 0; j < KV_BLOCK; ++j) {
+            const uint2 vw = *reinterpret_cast<const uint2*>(vt + j * D + lane * 4);
             const float v0 = bf16lo(vw.x), v1 = bf16hi(vw.x), v2 = bf16lo(vw.y), v3 = bf16hi(vw.y);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float pj = __shfl_sync(0xffffffffu, pr[g], j);
-                o[g][0] = fmaf(pj, v0, o[g][0]);
-                o[g][1] = fmaf(pj, v1, o[g][1]);
-                o[g][2] = fmaf(pj, v2, o[g][2]);
-                o[g][3] = fmaf(pj, v3, o[g][3]);
+                if (pj != 0.f) {
+                    o[g][0] = fmaf(pj, v0, o[g][0]);
+                    o[g][1] = fmaf(pj, v1, o[g][1]);
+                    o[g][2] = fmaf(pj, v2, o[g][2]);
+                    o[g][3] = fmaf(pj, v3, o[g][3]);
+                }
             }
         }
+        __syncwarp();      // the tile is rewritten by the next block's copies
     }
+    cp_async_wait_all();
+    __syncthreads();       // the K tiles become the warp-merge buffer
 
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        if (lane == 0) { s_m[warp][g] = m[g]; s_l[warp][g] = l[g]; }
-        *reinterpret_cast<float4*>(&s_o[warp][g][lane * 4]) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+        if (lane == 0) { s_m[warp * G + g] = m[g]; s_l[warp * G + g] = l[g]; }
+        *reinterpret_cast<float4*>(s_o + (warp * G + g) * D + lane * 4) =
+            make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
     }
     __syncthreads();
 
     // merge the warps in order; thread d owns output dimension d
     const int d = threadIdx.x;
     bool range_bad = false;
+    float Mg[G], Lg[G], Og[G];
+#pragma unroll
     for (int g = 0; g < G; ++g) {
         float M = -INFINITY;
-        for (int w = 0; w < AWARPS; ++w) M = fmaxf(M, s_m[w][g]);
+        for (int w = 0; w < AWARPS; ++w) M = fmaxf(M, s_m[w * G + g]);
         float L = 0.f, O = 0.f;
         if (M != -INFINITY) {
             for (int w = 0; w < AWARPS; ++w) {
-                const float e = exp2f(s_m[w][g] - M);   // 0 for a warp with no block
-                L = fmaf(s_l[w][g], e, L);
-                O = fmaf(s_o[w][g][d], e, O);
+                const float e = exp2f(s_m[w * G + g] - M);   // 0 for a warp with no block
+                L = fmaf(s_l[w * G + g], e, L);
+                O = fmaf(s_o[(w * G + g) * D + d], e, O);
             }
         }
-        const int hq = kvh * G + g;
-        const size_t row = (size_t)t * p.n_q + hq;
-        if (p.n_splits == 1) {
-            const float v = O / L;
-            if (p.out_f16) reinterpret_cast<__half*>(p.out)[row * D + d] = to_f16(v, range_bad);
-            else reinterpret_cast<float*>(p.out)[row * D + d] = v;
-        } else {
-            p.part_o[(row * p.n_splits + split) * D + d] = O;
+        Mg[g] = M; Lg[g] = L; Og[g] = O;
+    }
+    const size_t row0 = (size_t)t * p.n_q + kvh * G;
+    if (p.n_splits == 1) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float v = Og[g] / Lg[g];
+            if (p.out_f16) reinterpret_cast<__half*>(p.out)[(row0 + g) * D + d] = to_f16(v, range_bad);
+            else reinterpret_cast<float*>(p.out)[(row0 + g) * D + d] = v;
+        }
+    } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            p.part_o[((row0 + g) * p.n_splits + split) * D + d] = Og[g];
             if (d == 0) {
-                p.part_ml[(row * p.n_splits + split) * 2 + 0] = M;
-                p.part_ml[(row * p.n_splits + split) * 2 + 1] = L;
+                p.part_ml[((row0 + g) * p.n_splits + split) * 2 + 0] = Mg[g];
+                p.part_ml[((row0 + g) * p.n_splits + split) * 2 + 1] = Lg[g];
             }
+        }
+        // the last split CTA of this (row, KV head) merges every split in order
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) s_ticket = atomicAdd(p.counters + (size_t)t * p.n_kv + kvh, 1);
+        __syncthreads();
+        if (s_ticket == p.n_splits - 1) {
+            __threadfence();
+            // split maxima and sums of all G heads, fetched in parallel; the
+            // staging area is free (the warp merge above is done)
+            float* s_ml = s_o + AWARPS * G * D;              // [G][n_splits][2]
+            float* s_w = s_ml + 2 * G * p.n_splits;          // [G][n_splits]
+            for (int i = threadIdx.x; i < G * p.n_splits; i += AWARPS * 32) {
+                const int g = i / p.n_splits, sp = i % p.n_splits;
+                const float* ml = p.part_ml + ((row0 + g) * p.n_splits + sp) * 2;
+                s_ml[2 * i] = __ldcg(ml);
+                s_ml[2 * i + 1] = __ldcg(ml + 1);
+            }
+            __syncthreads();
+            if (threadIdx.x < G) {
+                const int g = threadIdx.x;
+                float M = -INFINITY;
+                for (int sp = 0; sp < p.n_splits; ++sp) M = fmaxf(M, s_ml[2 * (g * p.n_splits + sp)]);
+                float L = 0.f;
+                for (int sp = 0; sp < p.n_splits; ++sp) {
+                    const float ms = s_ml[2 * (g * p.n_splits + sp)];
+                    const float e = ms == -INFINITY ? 0.f : exp2f(ms - M);
+                    s_w[g * p.n_splits + sp] = e;
+                    L = fmaf(s_ml[2 * (g * p.n_splits + sp) + 1], e, L);
+                }
+                s_m[g] = L;                                  // reuse: the merged denominator
+            }
+            __syncthreads();
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float* po = p.part_o + (row0 + g) * p.n_splits * D + d;
+                float O = 0.f;
+#pragma unroll 8
+                for (int sp = 0; sp < p.n_splits; ++sp) O = fmaf(__ldcg(po + (size_t)sp * D), s_w[g * p.n_splits + sp], O);
+                const float v = O / s_m[g];
+                if (p.out_f16) reinterpret_cast<__half*>(p.out)[(row0 + g) * D + d] = to_f16(v, range_bad);
+                else reinterpret_cast<float*>(p.out)[(row0 + g) * D + d] = v;
+            }
+            if (threadIdx.x == 0) p.counters[(size_t)t * p.n_kv + kvh] = 0;
         }
     }
     if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
-    grid_dep_launch();
 }
 
-// Merge split partials in split order: o = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
-__global__ void __launch_bounds__(D) attn_combine_kernel(const AttnArgs p)
+template <int G, bool FUSED>
+cudaError_t launch_g(const Launch& L, const AttnArgs& a)
 {
-    grid_dep_wait();
-    const size_t row = blockIdx.x;        // t * n_q + head
-    const int d = threadIdx.x;
-    const float* ml = p.part_ml + row * p.n_splits * 2;
-    float M = -INFINITY;
-    for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, ml[2 * s]);
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < p.n_splits; ++s) {
-        const float e = ml[2 * s] == -INFINITY ? 0.f : exp2f(ml[2 * s] - M);
-        L = fmaf(ml[2 * s + 1], e, L);
-        O = fmaf(p.part_o[(row * p.n_splits + s) * D + d], e, O);
+    const size_t smem = AttnSmem<G>::total;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(attn_kernel<G, FUSED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
     }
-    const float v = O / L;
-    bool range_bad = false;
-    if (p.out_f16) reinterpret_cast<__half*>(p.out)[row * D + d] = to_f16(v, range_bad);
-    else reinterpret_cast<float*>(p.out)[row * D + d] = v;
-    if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
-    grid_dep_launch();
-}
-
-template <typename K, typename A>
-cudaError_t launch_ex(const Launch& L, K kern, dim3 grid, dim3 block, const A& args)
-{
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
+    cfg.gridDim = dim3(a.n_splits, a.n_kv, a.T);
+    cfg.blockDim = dim3(AWARPS * 32);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -209,29 +362,37 @@ cudaError_t launch_ex(const Launch& L, K kern, dim3 grid, dim3 block, const A& a
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (L.counter) ++*L.counter;
-    return cudaLaunchKernelEx(&cfg, kern, args);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<G, FUSED>, a);
+}
+
+template <bool FUSED>
+cudaError_t launch_fused(const Launch& L, const AttnArgs& a)
+{
+    switch (a.n_q / a.n_kv) {
+    case 1: return launch_g<1, FUSED>(L, a);
+    case 2: return launch_g<2, FUSED>(L, a);
+    case 3: return launch_g<3, FUSED>(L, a);
+    case 4: return launch_g<4, FUSED>(L, a);
+    case 5: return launch_g<5, FUSED>(L, a);
+    case 6: return launch_g<6, FUSED>(L, a);
+    case 7: return launch_g<7, FUSED>(L, a);
+    case 8: return launch_g<8, FUSED>(L, a);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const Launch& L, const AttnArgs& a)
+#ifndef Q3_ATTN_BLOCKS_PER_WARP
+#define Q3_ATTN_BLOCKS_PER_WARP 1
+#endif
+int attention_blocks_per_cta() { return Q3_ATTN_BLOCKS_PER_WARP * AWARPS; }
+
+int attention_max_splits() { return 128; }
+
+cudaError_t launch_attention(const Launch& L, const AttnArgs& a, bool fused)
 {
-    const int G = a.n_q / a.n_kv;
-    const dim3 grid(a.n_splits, a.n_kv, a.T), block(AWARPS * 32);
-    cudaError_t e;
-    switch (G) {
-    case 1: e = launch_ex(L, attn_split_kernel<1>, grid, block, a); break;
-    case 2: e = launch_ex(L, attn_split_kernel<2>, grid, block, a); break;
-    case 3: e = launch_ex(L, attn_split_kernel<3>, grid, block, a); break;
-    case 4: e = launch_ex(L, attn_split_kernel<4>, grid, block, a); break;
-    case 5: e = launch_ex(L, attn_split_kernel<5>, grid, block, a); break;
-    case 6: e = launch_ex(L, attn_split_kernel<6>, grid, block, a); break;
-    case 7: e = launch_ex(L, attn_split_kernel<7>, grid, block, a); break;
-    case 8: e = launch_ex(L, attn_split_kernel<8>, grid, block, a); break;
-    default: return cudaErrorInvalidValue;
-    }
-    if (e != cudaSuccess || a.n_splits == 1) return e;
-    return launch_ex(L, attn_combine_kernel, dim3(a.T * a.n_q), dim3(D), a);
+    return fused ? launch_fused<true>(L, a) : launch_fused<false>(L, a);
 }
 
 }  // namespace q3

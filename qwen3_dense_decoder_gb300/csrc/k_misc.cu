@@ -52,6 +52,7 @@ struct EmbedArgs {
 
 __global__ void __launch_bounds__(256) embed_kernel(const EmbedArgs a)
 {
+    grid_dep_launch();
     grid_dep_wait();
     const int t = blockIdx.x;
     int tok = a.tokens[t];
@@ -67,7 +68,6 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedArgs a)
         o[0] = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
         o[1] = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
     }
-    grid_dep_launch();
 }
 
 // ---------------------------------------------------------------- RMSNorm -> fp16
@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const NormArgs a)
         const float4 v = *reinterpret_cast<const float4*>(x + i);
         ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     }
+    grid_dep_launch();
     ss = warp_sum(ss);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
@@ -115,7 +116,6 @@ __global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const NormArgs a)
         *reinterpret_cast<__half2*>(h + i) = o;
     }
     if (bad) set_status(a.status, Q3_STATUS_F16_RANGE);
-    grid_dep_launch();
 }
 
 // ---------------------------------------------------------------- q/k norm + RoPE + KV append

@@ -70,9 +70,17 @@ struct GemvArgs {
     int epi;                   // EPI_STORE_F32, EPI_ADD_F32, EPI_SWIGLU_F32
     float* out;
     int* status;
+    // optional greedy argmax of the outputs (lowest index on ties): per-CTA
+    // partials, merged by the last CTA to finish (ticket counter kept at 0)
+    int32_t* argmax_out;
+    float* am_val;             // [grid]
+    int* am_idx;               // [grid]
+    int* am_counter;
 };
 cudaError_t launch_gemv(const Launch& L, int scheme, const GemvArgs& a);
-int gemv_warps_per_row(int rows, int K);
+// segments per row: a power of two, preferably with at most 8 loads per lane
+int gemv_warps_per_row(int rows, int K, int scheme, int pair);
+int gemv_max_grid();
 
 // ---------------------------------------------------------------- elementwise
 cudaError_t launch_embed(const Launch& L, const int32_t* tokens, int T, const __nv_bfloat16* E,
@@ -101,22 +109,33 @@ struct RopeArgs {
 cudaError_t launch_qk_norm_rope_append(const Launch& L, const RopeArgs& a);
 
 struct AttnArgs {
-    const float* q;            // [T][n_q][128]
+    const float* q;            // [T][n_q][128], normed and rotated (unfused rounds)
+    const float* qkv;          // [T][(n_q + 2 n_kv) 128] raw projections (fused decode rounds)
+    const __nv_bfloat16* q_gain;
+    const __nv_bfloat16* k_gain;
+    const float2* rope;        // [max_ctx][64] (cos, sin)
+    float eps;
     int T, n_q, n_kv;
     const int* row_pos;
     const int* row_slot;
     const int* tables;
     int max_blocks;
-    const __nv_bfloat16* kv_layer;
+    __nv_bfloat16* kv_layer;   // pool slab of this layer; written by the fused append
     int n_blocks;
     int n_splits;
     float* part_ml;            // [T][n_q][n_splits][2]
     float* part_o;             // [T][n_q][n_splits][128]
+    int* counters;             // [T][n_kv], zero between calls (the last split CTA resets it)
     void* out;                 // [T][n_q*128], f32 or fp16
     int out_f16;
     int* status;
 };
-cudaError_t launch_attention(const Launch& L, const AttnArgs& a);
+// fused: every row is the single new token of its session; q/k norm, RoPE
+// and the K/V append of that token happen inside the attention kernel.
+cudaError_t launch_attention(const Launch& L, const AttnArgs& a, bool fused);
+// blocks of context each split CTA should take, and the most splits a row may use
+int attention_blocks_per_cta();
+int attention_max_splits();
 
 cudaError_t launch_argmax(const Launch& L, const float* logits, int rows, int V, int32_t* out);
 

@@ -134,6 +134,10 @@ struct q3_model {
     std::vector<std::vector<f16*>> w16;   // [layer][proj] fp16 copies (BF16 scheme)
     f16* lm16 = nullptr;      // fp16 copy of the lm_head for batched rows
     int* meta = nullptr;      // [3][max_rows]: row_pos, row_slot, last_row
+    int* attn_counters = nullptr;   // [max_rows][n_kv] split tickets, zero between rounds
+    float* am_val = nullptr;        // lm_head argmax partials, one per GEMV CTA
+    int* am_idx = nullptr;
+    int* am_counter = nullptr;      // ticket of the argmax merge, zero between rounds
 
     // pinned staging ring for host -> device metadata
     uint8_t* stage = nullptr;
@@ -287,13 +291,18 @@ struct Round {
     q3_pool* pool = nullptr;
     int last_row = 0;                // host copy when ns == 1
     int max_ctx = 0;                 // largest context of the round
+    bool decode = false;             // every session appends exactly one token
 };
 
 int attention_splits(const q3_model* m, int T, int max_ctx)
 {
+    // about two 32-position blocks per warp of a split CTA; a round with many
+    // rows already fills the machine without splitting
     const int nblk = (max_ctx + 31) / 32;
-    int s = (8 * 152 + T * m->c.n_kv_heads - 1) / (T * m->c.n_kv_heads);
-    s = std::max(1, std::min(s, nblk));
+    const int rows = T * m->c.n_kv_heads;
+    if (rows >= 8 * 152) return 1;
+    int s = (nblk + attention_blocks_per_cta() - 1) / attention_blocks_per_cta();
+    s = std::max(1, std::min({s, nblk, attention_max_splits()}));
     while (s > 1 && (size_t)T * s > m->part_rows) --s;
     return s;
 }
@@ -348,7 +357,8 @@ int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtens
 }
 
 int gemv(q3_model* m, int n_tensors, const void* const* w, const __half* const* sc, const int* rows,
-         int pair, int K, const float* x, const bf16* gain, int epi, float* out)
+         int pair, int K, const float* x, const bf16* gain, int epi, float* out,
+         int32_t* argmax = nullptr)
 {
     GemvArgs a{};
     int total = 0;
@@ -361,8 +371,11 @@ int gemv(q3_model* m, int n_tensors, const void* const* w, const __half* const* 
     a.n_tensors = n_tensors;
     a.pair = pair;
     a.K = K;
-    a.warps_per_row = gemv_warps_per_row(total, K);
-    if (pair && a.warps_per_row > 4) a.warps_per_row = 4;
+    a.warps_per_row = gemv_warps_per_row(total, K, sc ? Q3_Q8_0 : Q3_BF16, pair);
+    a.argmax_out = argmax;
+    a.am_val = m->am_val;
+    a.am_idx = m->am_idx;
+    a.am_counter = m->am_counter;
     a.x = x;
     a.norm_gain = gain;
     a.eps = m->c.rms_eps;
@@ -440,31 +453,41 @@ int run_round(q3_model* m, const Round& r)
             if (rc) return rc;
         }
 
-        // ---- q/k norm, RoPE, KV append
-        RopeArgs ra{};
-        ra.qkv = m->qkv; ra.T = T; ra.n_q = c.n_q_heads; ra.n_kv = c.n_kv_heads;
-        ra.q_gain = static_cast<const bf16*>(W.q_norm);
-        ra.k_gain = static_cast<const bf16*>(W.k_norm);
-        ra.eps = c.rms_eps; ra.rope = m->rope;
-        ra.row_pos = row_pos; ra.row_slot = row_slot;
-        ra.tables = r.pool->tables; ra.max_blocks = r.pool->max_blocks;
-        ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
-        ra.n_blocks = r.pool->n_blocks;
-        ra.q_out = m->q; ra.status = m->status;
-        if ((rc = m->check(run(Q3_K_ROPE, [&] { return launch_qk_norm_rope_append(L, ra); }), "qk-norm/rope/append"))) return rc;
+        // ---- q/k norm, RoPE, KV append (fused into attention in decode rounds)
+        if (!r.decode) {
+            RopeArgs ra{};
+            ra.qkv = m->qkv; ra.T = T; ra.n_q = c.n_q_heads; ra.n_kv = c.n_kv_heads;
+            ra.q_gain = static_cast<const bf16*>(W.q_norm);
+            ra.k_gain = static_cast<const bf16*>(W.k_norm);
+            ra.eps = c.rms_eps; ra.rope = m->rope;
+            ra.row_pos = row_pos; ra.row_slot = row_slot;
+            ra.tables = r.pool->tables; ra.max_blocks = r.pool->max_blocks;
+            ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
+            ra.n_blocks = r.pool->n_blocks;
+            ra.q_out = m->q; ra.status = m->status;
+            if ((rc = m->check(run(Q3_K_ROPE, [&] { return launch_qk_norm_rope_append(L, ra); }),
+                               "qk-norm/rope/append")))
+                return rc;
+        }
 
         // ---- attention
         AttnArgs aa{};
-        aa.q = m->q; aa.T = T; aa.n_q = c.n_q_heads; aa.n_kv = c.n_kv_heads;
+        aa.q = m->q; aa.qkv = m->qkv;
+        aa.q_gain = static_cast<const bf16*>(W.q_norm);
+        aa.k_gain = static_cast<const bf16*>(W.k_norm);
+        aa.rope = m->rope; aa.eps = c.rms_eps;
+        aa.T = T; aa.n_q = c.n_q_heads; aa.n_kv = c.n_kv_heads;
         aa.row_pos = row_pos; aa.row_slot = row_slot;
         aa.tables = r.pool->tables; aa.max_blocks = r.pool->max_blocks;
-        aa.kv_layer = ra.kv_layer; aa.n_blocks = r.pool->n_blocks;
+        aa.kv_layer = r.pool->kv + (size_t)l * layer_kv; aa.n_blocks = r.pool->n_blocks;
         aa.n_splits = n_splits;
         aa.part_ml = m->part_ml; aa.part_o = m->part_o;
+        aa.counters = m->attn_counters;
         aa.out = one ? (void*)m->attf : (void*)m->att;
         aa.out_f16 = one ? 0 : 1;
         aa.status = m->status;
-        if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_attention(L, aa); }), "attention"))) return rc;
+        if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_attention(L, aa, r.decode); }), "attention")))
+            return rc;
 
         // ---- O projection + residual
         if (one) {
@@ -541,7 +564,7 @@ int run_round(q3_model* m, const Round& r)
         const void* w[1] = {m->lm_head};
         const int rows[1] = {c.vocab};
         if ((rc = gemv(m, 1, w, nullptr, rows, 0, H, m->x + (size_t)r.last_row * H, m->final_norm,
-                       EPI_STORE_F32, r.logits)))
+                       EPI_STORE_F32, r.logits, r.argmax)))
             return rc;
     } else {
         if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, last_rows, r.ns, H, m->final_norm, c.rms_eps,
@@ -551,7 +574,8 @@ int run_round(q3_model* m, const Round& r)
                        m->hfin, EPI_STORE_F32, r.logits, c.vocab)))
             return rc;
     }
-    if (r.argmax && (rc = m->check(run(Q3_K_OTHER, [&] { return launch_argmax(L, r.logits, r.ns, c.vocab, r.argmax); }), "argmax")))
+    if (r.ns > 1 && r.argmax &&
+        (rc = m->check(run(Q3_K_OTHER, [&] { return launch_argmax(L, r.logits, r.ns, c.vocab, r.argmax); }), "argmax")))
         return rc;
     return Q3_OK;
 }
@@ -630,6 +654,7 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
         h[2 * m->max_rows + i] = t - 1;
     }
     r.last_row = r.T - 1;
+    r.decode = (r.T == ns);
     if ((rc = m->check(m->stage_copy(slot, m->meta, sizeof(int32_t) * 3 * m->max_rows), "meta upload")))
         return rc;
     if ((rc = run_round(m, r))) {
@@ -759,8 +784,14 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->ws_elems = (size_t)32 << 20;
     m->ws = static_cast<float*>(A(sizeof(float) * m->ws_elems));
     m->meta = static_cast<int*>(A(sizeof(int) * 3 * (size_t)m->max_rows));
+    m->attn_counters = static_cast<int*>(A(sizeof(int) * (size_t)m->max_rows * c.n_kv_heads));
+    m->am_val = static_cast<float*>(A(sizeof(float) * gemv_max_grid()));
+    m->am_idx = static_cast<int*>(A(sizeof(int) * gemv_max_grid()));
+    m->am_counter = static_cast<int*>(A(sizeof(int)));
     if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
     if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(m->attn_counters, 0, sizeof(int) * (size_t)m->max_rows * c.n_kv_heads) != cudaSuccess ||
+        cudaMemset(m->am_counter, 0, sizeof(int)) != cudaSuccess ||
         cudaMemset(m->conv_counts, 0, 2 * sizeof(unsigned long long)) != cudaSuccess)
         return bad(Q3_ERR_CUDA, "cudaMemset failed");
 
@@ -1086,8 +1117,8 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
 int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, int M, int K,
                  float* y_dev, void* stream)
 {
-    if (!w_dev || !x_dev || !y_dev || M < 8 || M % 8 || K < 32 || K % 32 || !aligned16(w_dev) ||
-        !aligned16(x_dev))
+    if (!w_dev || !x_dev || !y_dev || M < 8 || M % 8 || K < 256 || K % 256 || !aligned16(w_dev) ||
+        !aligned16(x_dev) || (scales_dev && !aligned16(scales_dev)))
         return fail(Q3_ERR_INVALID_ARG, "op_matvec: bad argument");
     GemvArgs a{};
     a.w[0] = w_dev;
@@ -1095,7 +1126,7 @@ int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, 
     a.rows[0] = M;
     a.n_tensors = 1;
     a.K = K;
-    a.warps_per_row = gemv_warps_per_row(M, K);
+    a.warps_per_row = gemv_warps_per_row(M, K, scales_dev ? Q3_Q8_0 : Q3_BF16, 0);
     a.x = x_dev;
     a.epi = EPI_STORE_F32;
     a.out = y_dev;
