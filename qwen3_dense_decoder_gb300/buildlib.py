@@ -19,7 +19,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libq3.so")
 
-SOURCES = ["runtime.cu", "k_gemm.cu", "k_gemv.cu", "k_attn.cu", "k_misc.cu", "noalloc.cu"]
+SOURCES = ["runtime.cu", "k_gemm.cu", "k_gemv.cu", "k_attn.cu", "k_attn_prefill.cu", "k_misc.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

@@ -50,6 +50,8 @@ Q3_DEV void cp_async_16(void* smem_dst, const void* gmem_src) {
 }
 Q3_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 Q3_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// wait until at most one committed group is still in flight
+Q3_DEV void cp_async_wait_all_but(int) { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // ---------------------------------------------------------------- per-head q/k norm + RoPE
 // One warp holds one 128-wide head, lane l elements [4l, 4l + 4).  RMSNorm

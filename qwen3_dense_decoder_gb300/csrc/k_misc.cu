@@ -154,8 +154,20 @@ __global__ void __launch_bounds__(128) qk_norm_rope_append_kernel(const RopeArgs
         for (int e = 0; e < 4; ++e) y[e] = out[e];
     }
     if (is_q) {
-        *reinterpret_cast<float4*>(a.q_out + ((size_t)t * a.n_q + hh) * D + lane * 4) =
-            make_float4(y[0], y[1], y[2], y[3]);
+        const size_t o = ((size_t)t * a.n_q + hh) * D + lane * 4;
+        if (a.q_out)
+            *reinterpret_cast<float4*>(a.q_out + o) = make_float4(y[0], y[1], y[2], y[3]);
+        if (a.q_out16) {
+            bool bad = false;
+            __half2 lo, hi;
+            lo.x = to_f16(y[0], bad); lo.y = to_f16(y[1], bad);
+            hi.x = to_f16(y[2], bad); hi.y = to_f16(y[3], bad);
+            uint2 packed;
+            packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(a.q_out16 + o) = packed;
+            if (bad) set_status(a.status, Q3_STATUS_F16_RANGE);
+        }
         return;
     }
     const int slot = a.row_slot[t];

@@ -103,7 +103,8 @@ struct RopeArgs {
     __nv_bfloat16* kv_layer;   // pool base of this layer: [n_blocks][2][n_kv][32][128]
     int64_t layer_stride;      // elements between layers (unused by the kernel)
     int n_blocks;
-    float* q_out;              // [T][n_q*128]
+    float* q_out;              // [T][n_q*128] f32, or null
+    __half* q_out16;           // [T][n_q*128] fp16, or null
     int* status;
 };
 cudaError_t launch_qk_norm_rope_append(const Launch& L, const RopeArgs& a);
@@ -130,6 +131,25 @@ struct AttnArgs {
     int out_f16;
     int* status;
 };
+// Prefill attention on tensor cores (mma.sync, fp16): query tiles of 64 rows
+// of one session, one query head per CTA, 64-position K/V tiles.
+struct PrefillAttnArgs {
+    const __half* q;           // [T][n_q][128] normed, rotated (fp16)
+    int T, n_q, n_kv;
+    const int* row_pos;
+    const int* row_slot;
+    const int* tile_row0;      // [n_tiles] first row of each 64-row query tile
+    const int* tile_rows;      // [n_tiles] rows in the tile (<= 64)
+    int n_tiles;
+    const int* tables;
+    int max_blocks;
+    const __nv_bfloat16* kv_layer;
+    int n_blocks;
+    __half* out;               // [T][n_q * 128] fp16
+    int* status;
+};
+cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a);
+
 // fused: every row is the single new token of its session; q/k norm, RoPE
 // and the K/V append of that token happen inside the attention kernel.
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, bool fused);

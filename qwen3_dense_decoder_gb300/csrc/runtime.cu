@@ -133,7 +133,8 @@ struct q3_model {
     f16* deq = nullptr;       // Q8_0 prefill: dequantised projection(s)
     std::vector<std::vector<f16*>> w16;   // [layer][proj] fp16 copies (BF16 scheme)
     f16* lm16 = nullptr;      // fp16 copy of the lm_head for batched rows
-    int* meta = nullptr;      // [3][max_rows]: row_pos, row_slot, last_row
+    int* meta = nullptr;      // [5][max_rows]: row_pos, row_slot, last_row, tile_row0, tile_rows
+    f16* q16 = nullptr;       // [rows_alloc][qw] fp16 q of prefill rounds
     int* attn_counters = nullptr;   // [max_rows][n_kv] split tickets, zero between rounds
     float* am_val = nullptr;        // lm_head argmax partials, one per GEMV CTA
     int* am_idx = nullptr;
@@ -292,6 +293,7 @@ struct Round {
     int last_row = 0;                // host copy when ns == 1
     int max_ctx = 0;                 // largest context of the round
     bool decode = false;             // every session appends exactly one token
+    int n_tiles = 0;                 // 64-row query tiles (prefill attention)
 };
 
 int attention_splits(const q3_model* m, int T, int max_ctx)
@@ -464,30 +466,46 @@ int run_round(q3_model* m, const Round& r)
             ra.tables = r.pool->tables; ra.max_blocks = r.pool->max_blocks;
             ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
             ra.n_blocks = r.pool->n_blocks;
-            ra.q_out = m->q; ra.status = m->status;
+            ra.q_out = nullptr; ra.q_out16 = m->q16; ra.status = m->status;
             if ((rc = m->check(run(Q3_K_ROPE, [&] { return launch_qk_norm_rope_append(L, ra); }),
                                "qk-norm/rope/append")))
                 return rc;
         }
 
         // ---- attention
-        AttnArgs aa{};
-        aa.q = m->q; aa.qkv = m->qkv;
-        aa.q_gain = static_cast<const bf16*>(W.q_norm);
-        aa.k_gain = static_cast<const bf16*>(W.k_norm);
-        aa.rope = m->rope; aa.eps = c.rms_eps;
-        aa.T = T; aa.n_q = c.n_q_heads; aa.n_kv = c.n_kv_heads;
-        aa.row_pos = row_pos; aa.row_slot = row_slot;
-        aa.tables = r.pool->tables; aa.max_blocks = r.pool->max_blocks;
-        aa.kv_layer = r.pool->kv + (size_t)l * layer_kv; aa.n_blocks = r.pool->n_blocks;
-        aa.n_splits = n_splits;
-        aa.part_ml = m->part_ml; aa.part_o = m->part_o;
-        aa.counters = m->attn_counters;
-        aa.out = one ? (void*)m->attf : (void*)m->att;
-        aa.out_f16 = one ? 0 : 1;
-        aa.status = m->status;
-        if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_attention(L, aa, r.decode); }), "attention")))
-            return rc;
+        if (r.decode) {
+            AttnArgs aa{};
+            aa.q = m->q; aa.qkv = m->qkv;
+            aa.q_gain = static_cast<const bf16*>(W.q_norm);
+            aa.k_gain = static_cast<const bf16*>(W.k_norm);
+            aa.rope = m->rope; aa.eps = c.rms_eps;
+            aa.T = T; aa.n_q = c.n_q_heads; aa.n_kv = c.n_kv_heads;
+            aa.row_pos = row_pos; aa.row_slot = row_slot;
+            aa.tables = r.pool->tables; aa.max_blocks = r.pool->max_blocks;
+            aa.kv_layer = r.pool->kv + (size_t)l * layer_kv; aa.n_blocks = r.pool->n_blocks;
+            aa.n_splits = n_splits;
+            aa.part_ml = m->part_ml; aa.part_o = m->part_o;
+            aa.counters = m->attn_counters;
+            aa.out = one ? (void*)m->attf : (void*)m->att;
+            aa.out_f16 = one ? 0 : 1;
+            aa.status = m->status;
+            if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_attention(L, aa, true); }), "attention")))
+                return rc;
+        } else {
+            PrefillAttnArgs pa{};
+            pa.q = m->q16; pa.T = T; pa.n_q = c.n_q_heads; pa.n_kv = c.n_kv_heads;
+            pa.row_pos = row_pos; pa.row_slot = row_slot;
+            pa.tile_row0 = m->meta + 3 * m->max_rows;
+            pa.tile_rows = m->meta + 4 * m->max_rows;
+            pa.n_tiles = r.n_tiles;
+            pa.tables = r.pool->tables; pa.max_blocks = r.pool->max_blocks;
+            pa.kv_layer = r.pool->kv + (size_t)l * layer_kv; pa.n_blocks = r.pool->n_blocks;
+            pa.out = m->att;
+            pa.status = m->status;
+            if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_prefill_attention(L, pa); }),
+                               "prefill attention")))
+                return rc;
+        }
 
         // ---- O projection + residual
         if (one) {
@@ -653,9 +671,17 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
         }
         h[2 * m->max_rows + i] = t - 1;
     }
+    // 64-row query tiles of the prefill attention, never spanning two sessions
+    int n_tiles = 0;
+    for (int i = 0, row = 0; i < ns; row += n[i], ++i)
+        for (int k = 0; k < n[i]; k += 64, ++n_tiles) {
+            h[3 * m->max_rows + n_tiles] = row + k;
+            h[4 * m->max_rows + n_tiles] = std::min(64, n[i] - k);
+        }
+    r.n_tiles = n_tiles;
     r.last_row = r.T - 1;
     r.decode = (r.T == ns);
-    if ((rc = m->check(m->stage_copy(slot, m->meta, sizeof(int32_t) * 3 * m->max_rows), "meta upload")))
+    if ((rc = m->check(m->stage_copy(slot, m->meta, sizeof(int32_t) * 5 * m->max_rows), "meta upload")))
         return rc;
     if ((rc = run_round(m, r))) {
         m->poisoned = true;
@@ -783,7 +809,8 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->part_o = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 128));
     m->ws_elems = (size_t)32 << 20;
     m->ws = static_cast<float*>(A(sizeof(float) * m->ws_elems));
-    m->meta = static_cast<int*>(A(sizeof(int) * 3 * (size_t)m->max_rows));
+    m->meta = static_cast<int*>(A(sizeof(int) * 5 * (size_t)m->max_rows));
+    m->q16 = static_cast<f16*>(A(sizeof(f16) * R * m->qw));
     m->attn_counters = static_cast<int*>(A(sizeof(int) * (size_t)m->max_rows * c.n_kv_heads));
     m->am_val = static_cast<float*>(A(sizeof(float) * gemv_max_grid()));
     m->am_idx = static_cast<int*>(A(sizeof(int) * gemv_max_grid()));
@@ -811,7 +838,7 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     }
 
     // pinned staging ring
-    m->stage_slot = round_up(std::max<size_t>(sizeof(int) * 3 * (size_t)m->max_rows,
+    m->stage_slot = round_up(std::max<size_t>(sizeof(int) * 5 * (size_t)m->max_rows,
                                               sizeof(int) * ((size_t)c.max_ctx / 32 + 1)), 256);
     m->stage_n = 64;
     if (cudaMallocHost(&m->stage, m->stage_slot * m->stage_n) != cudaSuccess)
@@ -913,6 +940,12 @@ int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
     if (cudaMalloc(&p->kv, kv * sizeof(bf16)) != cudaSuccess) {
         delete p;
         return fail(Q3_ERR_OOM, "pool: cannot allocate %zu bytes of KV", kv * sizeof(bf16));
+    }
+    // zeroed once so positions a block has not been written hold finite values
+    if (cudaMemsetAsync(p->kv, 0, kv * sizeof(bf16), m->stream) != cudaSuccess) {
+        cudaFree(p->kv);
+        delete p;
+        return fail(Q3_ERR_CUDA, "pool: memset failed");
     }
     if (cudaMalloc(&p->tables, sizeof(int) * (size_t)max_sessions * p->max_blocks) != cudaSuccess) {
         cudaFree(p->kv);
