@@ -200,9 +200,11 @@ int q3_quantize_q8_0(const void* w_dev, int64_t n, void* blocks_dev, void* strea
  * w_dev: fp16 [M][K]; x_dev: fp16 [N][K] with at least round_up(N, 256)
  * rows allocated (rows past N are read but their products discarded);
  * y_dev: f32 [N][M].  M a multiple of 128, K a multiple of 64, 1 <= N.
- * Pointers 16-byte aligned.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+ * block_n: token-tile width (32, 64, 96, 128, 192 or 256), or 0 for the
+ * width the prefill planner would pick.  Pointers 16-byte aligned.
+ * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
 int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, float* y_dev,
-                 void* stream);
+                 int block_n, void* stream);
 
 /* q3_op_matvec: y[m] = sum_k w[m][k] * x[k] on the decode GEMV.  With
  * scales_dev == NULL, w_dev is bf16 [M][K]; otherwise w_dev is the int8

@@ -81,7 +81,7 @@ def lib():
         L.q3_quantize_q8_0.argtypes = [vp, i64, vp, vp]
         L.q3_model_launch_count.argtypes = [vp]
         L.q3_model_launch_count.restype = i64
-        L.q3_op_matmul.argtypes = [vp, vp, i, i, i, vp, vp]
+        L.q3_op_matmul.argtypes = [vp, vp, i, i, i, vp, i, vp]
         L.q3_op_matmul_splitk_noalloc.argtypes = [vp, vp, i, i, i, i, vp, vp]
         L.q3_noalloc_last_error.restype = C.c_char_p
         L.q3_model_profile.argtypes = [vp, i]
@@ -117,14 +117,16 @@ def quantize_q8_0(w: torch.Tensor, stream=None) -> torch.Tensor:
     return out
 
 
-def op_matmul(w: torch.Tensor, x: torch.Tensor, n: int, stream=None) -> torch.Tensor:
+def op_matmul(w: torch.Tensor, x: torch.Tensor, n: int, block_n: int = 0,
+              stream=None) -> torch.Tensor:
     """y[n][m] = sum_k w[m][k] x[n][k] on the tcgen05 GEMM (operator gate).
-    w: fp16 [M, K]; x: fp16 [>= round_up(n, 256), K]."""
+    w: fp16 [M, K]; x: fp16 [>= round_up(n, 256), K]; block_n: token-tile
+    width, 0 for the planner's choice."""
     M, K = w.shape
     assert w.dtype == x.dtype == torch.float16
     assert x.shape[0] >= (n + 255) // 256 * 256 and x.shape[1] == K
     y = torch.empty(n, M, dtype=torch.float32, device=w.device)
-    _check(lib().q3_op_matmul(_ptr(w), _ptr(x), M, n, K, _ptr(y), _stream_handle(stream)))
+    _check(lib().q3_op_matmul(_ptr(w), _ptr(x), M, n, K, _ptr(y), block_n, _stream_handle(stream)))
     return y
 
 

@@ -9,6 +9,7 @@
 #include <stdint.h>
 
 #include "../../include/q3.h"
+#include "kernels.h"
 
 #define Q3_DEV __device__ __forceinline__
 
@@ -151,6 +152,26 @@ Q3_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// asynchronous prefetch of a contiguous global range into L2 (16-byte
+// aligned, size a multiple of 16)
+Q3_DEV void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+
+// This CTA's share of an L2 prefetch: each range is cut into n_ctas equal
+// 16-byte-aligned slices.
+Q3_DEV void issue_l2_prefetch(const L2Prefetch& pf, int cta, int n_ctas) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        if (!pf.bytes[i]) continue;
+        const uint64_t slice = ((pf.bytes[i] + n_ctas - 1) / n_ctas + 15) & ~uint64_t(15);
+        const uint64_t off = slice * cta;
+        if (off >= pf.bytes[i]) continue;
+        const uint64_t n = min(slice, pf.bytes[i] - off) & ~uint64_t(15);
+        if (n) prefetch_l2(static_cast<const uint8_t*>(pf.ptr[i]) + off, (uint32_t)n);
+    }
 }
 
 // named barrier over a subset of the CTA's warps

@@ -117,6 +117,9 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_kernel(const AttnArgs p)
         }
     }
 
+    if (threadIdx.x == 0)
+        issue_l2_prefetch(p.next, blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z),
+                          gridDim.x * gridDim.y * gridDim.z);
     // the next kernel may now be scheduled into the SM space this grid leaves
     grid_dep_launch();
     grid_dep_wait();

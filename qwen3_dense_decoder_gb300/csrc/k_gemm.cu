@@ -13,11 +13,16 @@
 // the weights enter as an fp16 copy of the bf16 tensors (exact except for
 // |w| < 2^-17).
 //
-// Roles in a 128-thread CTA: warp 0 lane 0 issues TMA loads, warp 1 lane 0
-// issues tcgen05.mma and owns the TMEM allocation, and all four warps drain
-// the accumulator (warp w reads TMEM lanes 32w..32w+31) through the fused
-// epilogue: plain store, residual add, or SwiGLU of a paired gate/up tile.
-// Split-K writes FP32 partials that gemm_splitk_reduce sums in split order.
+// Persistent and warp-specialised: one CTA per SM walks its share of the
+// (token tile, weight tile, K split) units.  Warp 0 lane 0 issues TMA loads
+// into a STAGES-deep ring, warp 1 lane 0 issues tcgen05.mma into one of two
+// TMEM accumulators and owns the TMEM allocation, and warps 2..5 drain the
+// other accumulator (warp w reads TMEM lanes 32 (w % 4)..+31) through the
+// fused epilogue: plain store, residual add, or SwiGLU of a paired gate/up
+// tile.  The epilogue of one unit therefore overlaps the main loop of the
+// next.  Consecutive units of a CTA share the weight tile, which is read
+// from HBM once and then hit in L2.  Split-K writes FP32 partials that
+// gemm_splitk_reduce sums in split order.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -35,17 +40,43 @@ template <int BN>
 struct GemmCfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    // as many stages as fit in ~200 KB, at most 8
-    static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
+    // as many stages as fit beside the SwiGLU exchange buffer, at most 8
+    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-    static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t ACC_COLS = BN < 32 ? 32 : BN;     // one accumulator
+    // two accumulators, allocated as a power of two of at least 32 columns
+    static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS <= 64 ? 64 : 2 * ACC_COLS <= 128 ? 128
+                                        : 2 * ACC_COLS <= 256 ? 256 : 512;
+    static constexpr int XCH_BYTES = 32 * 128 * 4;                // SwiGLU exchange, 32 columns
+    static constexpr int SMEM = STAGES * STAGE_BYTES + XCH_BYTES + 1024 /*align*/ + 512 /*barriers*/;
 };
 
+constexpr int GEMM_THREADS = 192;     // producer, MMA issuer, 4 epilogue warps
+constexpr int BAR_EPI = 1;            // named barrier of the epilogue warps
+
 Q3_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+Q3_DEV float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+struct Unit {
+    int nt, mt, split, kb0, kb1;
+};
+
+Q3_DEV Unit decode_unit(const GemmArgs& p, int u, int n_tiles)
+{
+    Unit w;
+    const int m_tiles = p.M / BM;
+    w.nt = u % n_tiles;
+    const int rest = u / n_tiles;
+    w.mt = rest % m_tiles;
+    w.split = rest / m_tiles;
+    const int kb_total = p.K / BK;
+    w.kb0 = w.split * kb_total / p.k_splits;
+    w.kb1 = (w.split + 1) * kb_total / p.k_splits;
+    return w;
+}
 
 template <int BN>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
                const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tb,
                const GemmArgs p)
@@ -57,30 +88,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
                                                ~uintptr_t(1023));
     uint8_t* sa = smem;
     uint8_t* sb = smem + STAGES * A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sb + STAGES * C::B_BYTES);
+    float* xch = reinterpret_cast<float*>(sb + STAGES * C::B_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xch) + C::XCH_BYTES);
     uint64_t* empty = full + STAGES;
-    uint64_t* accum = empty + STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+    uint64_t* tfull = empty + STAGES;       // accumulator ready, one per TMEM buffer
+    uint64_t* tempty = tfull + 2;           // accumulator drained
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = (p.N + BN - 1) / BN;
-    const int m_tiles = p.M / BM;
-    int bid = blockIdx.x;
-    const int nt = bid % n_tiles;
-    bid /= n_tiles;
-    const int mt = bid % m_tiles;
-    const int split = bid / m_tiles;
-    const int kb_total = p.K / BK;
-    const int kb0 = split * kb_total / p.k_splits;
-    const int kb1 = (split + 1) * kb_total / p.k_splits;
-    const int nkb = kb1 - kb0;
+    const int units = n_tiles * (p.M / BM) * p.k_splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accum, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);       // one arrival per epilogue warp
+        }
         fence_barrier_init();
         prefetch_tmap(&ta0);
         prefetch_tmap(&tb);
@@ -94,120 +121,153 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // The token rows (B) are written by the previous kernel.
+    // the token rows (B) are written by the previous kernel
     grid_dep_wait();
 
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
         // ---------------- TMA producer
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % STAGES;
-            const uint32_t use = i / STAGES;
-            if (i >= STAGES && !mbar_wait(&empty[s], (use & 1) ^ 1, p.status)) break;
-            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-            const int kc = (kb0 + i) * BK;
-            uint8_t* a_dst = sa + s * A_BYTES;
-            if (p.pair) {
-                tma_load_2d(a_dst, &ta0, &full[s], kc, mt * 64);
-                tma_load_2d(a_dst + A_BYTES / 2, &ta1, &full[s], kc, mt * 64);
-            } else if (mt < p.a_tiles0) {
-                tma_load_2d(a_dst, &ta0, &full[s], kc, mt * BM);
-            } else if (mt < p.a_tiles1) {
-                tma_load_2d(a_dst, &ta1, &full[s], kc, (mt - p.a_tiles0) * BM);
-            } else {
-                tma_load_2d(a_dst, &ta2, &full[s], kc, (mt - p.a_tiles1) * BM);
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit w = decode_unit(p, u, n_tiles);
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t use = it / STAGES;
+                    if (it >= STAGES && !mbar_wait(&empty[s], (use & 1) ^ 1, p.status)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+                    const int kc = kb * BK;
+                    uint8_t* a_dst = sa + s * A_BYTES;
+                    if (p.pair) {
+                        tma_load_2d(a_dst, &ta0, &full[s], kc, w.mt * 64);
+                        tma_load_2d(a_dst + A_BYTES / 2, &ta1, &full[s], kc, w.mt * 64);
+                    } else if (w.mt < p.a_tiles0) {
+                        tma_load_2d(a_dst, &ta0, &full[s], kc, w.mt * BM);
+                    } else if (w.mt < p.a_tiles1) {
+                        tma_load_2d(a_dst, &ta1, &full[s], kc, (w.mt - p.a_tiles0) * BM);
+                    } else {
+                        tma_load_2d(a_dst, &ta2, &full[s], kc, (w.mt - p.a_tiles1) * BM);
+                    }
+                    tma_load_2d(sb + s * C::B_BYTES, &tb, &full[s], kc, w.nt * BN);
+                }
             }
-            tma_load_2d(sb + s * C::B_BYTES, &tb, &full[s], kc, nt * BN);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
         // ---------------- MMA issuer
-        constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % STAGES;
-            const uint32_t use = i / STAGES;
-            if (!mbar_wait(&full[s], use & 1, p.status)) break;
-            tc_fence_after();
-            const uint32_t a_base = smem_u32(sa + s * A_BYTES);
-            const uint32_t b_base = smem_u32(sb + s * C::B_BYTES);
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+            int it = 0, local = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+                const Unit w = decode_unit(p, u, n_tiles);
+                const int ab = local & 1;
+                const uint32_t use_ab = local >> 1;
+                if (local >= 2 && !mbar_wait(&tempty[ab], (use_ab - 1) & 1, p.status)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + ab * C::ACC_COLS;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t use = it / STAGES;
+                    if (!mbar_wait(&full[s], use & 1, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sa + s * A_BYTES);
+                    const uint32_t b_base = smem_u32(sb + s * C::B_BYTES);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-                // advancing 16 elements (32 bytes) along K inside the swizzle row
-                tc_mma_f16(tmem, smem_desc_sw128(a_base + k * 32), smem_desc_sw128(b_base + k * 32),
-                           idesc, (i > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < BK / 16; ++k) {
+                        // advancing 16 elements (32 bytes) along K inside the swizzle row
+                        tc_mma_f16(d, smem_desc_sw128(a_base + k * 32), smem_desc_sw128(b_base + k * 32),
+                                   idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[s]);
+                }
+                tc_commit(&tfull[ab]);
             }
-            tc_commit(&empty[s]);
         }
-        tc_commit(accum);
-    }
-    __syncwarp();
-
-    // The next kernel may start its prologue while this epilogue drains.
-    grid_dep_launch();
-
-    // ---------------- epilogue: all four warps
-    // CTA-uniform: a failed (timed-out) wait anywhere skips every TMEM read
-    const bool have = __syncthreads_and(mbar_wait(accum, 0, p.status)) != 0;
-    tc_fence_after();
-    const int row = warp * 32 + lane;                      // D row = TMEM lane
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-    float* xch = reinterpret_cast<float*>(smem);           // SwiGLU exchange (ring is idle now)
-    const bool swiglu = (p.epi == EPI_SWIGLU_F16 || p.epi == EPI_SWIGLU_F32) && p.k_splits == 1;
-    bool range_bad = false;
-
+    } else {
+        // ---------------- epilogue: TMEM -> registers -> global, warps 2..5
+        const int q = warp & 3;                         // TMEM lane quadrant of this warp
+        const int row = q * 32 + lane;                  // D row = TMEM lane
+        const bool swiglu = (p.epi == EPI_SWIGLU_F16 || p.epi == EPI_SWIGLU_F32) && p.k_splits == 1;
+        bool range_bad = false;
+        int local = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+            const Unit w = decode_unit(p, u, n_tiles);
+            const int ab = local & 1;
+            const uint32_t use_ab = local >> 1;
+            if (!named_bar_and(BAR_EPI, 128, mbar_wait(&tfull[ab], use_ab & 1, p.status))) break;
+            tc_fence_after();
+            const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + ab * C::ACC_COLS;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-        if (!have) break;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
-        tmem_ld_wait();
-        const int n0 = nt * BN + c * 32;
-        if (p.k_splits > 1) {
-            float* ws = p.ws + (size_t)split * p.N * p.M;
-            const int m = mt * BM + row;
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + c * 32, r);
+                tmem_ld_wait();
+                const int n0 = w.nt * BN + c * 32;
+                if (p.k_splits > 1) {
+                    float* ws = p.ws + (size_t)w.split * p.N * p.M;
+                    const int m = w.mt * BM + row;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (n0 + j < p.N) ws[(size_t)(n0 + j) * p.M + m] = __uint_as_float(r[j]);
-        } else if (swiglu) {
-            // rows 64..127 hold the up projection of the features of rows 0..63
-            if (warp >= 2) {
+                    for (int j = 0; j < 32; ++j)
+                        if (n0 + j < p.N) ws[(size_t)(n0 + j) * p.M + m] = __uint_as_float(r[j]);
+                } else if (swiglu) {
+                    // rows 0..63 hold the gate and rows 64..127 the up projection of
+                    // the same 64 features: every thread posts its 32 columns, then
+                    // computes 16 columns of one feature (all four warps share the work)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) xch[j * 64 + (row - 64)] = __uint_as_float(r[j]);
-            }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (warp < 2) {
-                const int f = mt * 64 + row;
+                    for (int j = 0; j < 32; ++j) xch[j * 128 + row] = __uint_as_float(r[j]);
+                    named_bar(BAR_EPI, 128);
+                    const int fr = row & 63;                    // feature row
+                    const int jh = (row >> 6) * 16;             // column half
+                    const int f = w.mt * 64 + fr;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (n0 + j < p.N) {
-                        const float g = __uint_as_float(r[j]);
-                        const float v = silu(g) * xch[j * 64 + row];
-                        if (p.epi == EPI_SWIGLU_F16)
-                            reinterpret_cast<__half*>(p.out)[(size_t)(n0 + j) * p.ldo + f] =
-                                to_f16(v, range_bad);
-                        else
-                            reinterpret_cast<float*>(p.out)[(size_t)(n0 + j) * p.ldo + f] = v;
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = jh + jj;
+                        if (n0 + j < p.N) {
+                            const float v = silu_fast(xch[j * 128 + fr]) * xch[j * 128 + 64 + fr];
+                            if (p.epi == EPI_SWIGLU_F16)
+                                reinterpret_cast<__half*>(p.out)[(size_t)(n0 + j) * p.ldo + f] =
+                                    to_f16(v, range_bad);
+                            else
+                                reinterpret_cast<float*>(p.out)[(size_t)(n0 + j) * p.ldo + f] = v;
+                        }
+                    }
+                    named_bar(BAR_EPI, 128);
+                } else if (p.epi == EPI_ADD_F32) {
+                    // residual add: all 32 loads are issued before any store
+                    const int m = w.mt * BM + row;
+                    float* out = reinterpret_cast<float*>(p.out);
+                    float old[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        old[j] = n0 + j < p.N ? out[(size_t)(n0 + j) * p.ldo + m] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (n0 + j < p.N) out[(size_t)(n0 + j) * p.ldo + m] = old[j] + __uint_as_float(r[j]);
+                } else {
+                    const int m = w.mt * BM + row;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (n0 + j < p.N) {
+                            const size_t o = (size_t)(n0 + j) * p.ldo + m;
+                            const float v = __uint_as_float(r[j]);
+                            if (p.epi == EPI_STORE_F32)
+                                reinterpret_cast<float*>(p.out)[o] = v;
+                            else
+                                reinterpret_cast<__half*>(p.out)[o] = to_f16(v, range_bad);
+                        }
                     }
                 }
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-        } else {
-            const int m = mt * BM + row;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (n0 + j < p.N) {
-                    const size_t o = (size_t)(n0 + j) * p.ldo + m;
-                    const float v = __uint_as_float(r[j]);
-                    if (p.epi == EPI_STORE_F32)
-                        reinterpret_cast<float*>(p.out)[o] = v;
-                    else if (p.epi == EPI_ADD_F32)
-                        reinterpret_cast<float*>(p.out)[o] += v;
-                    else
-                        reinterpret_cast<__half*>(p.out)[o] = to_f16(v, range_bad);
-                }
-            }
+            // this accumulator may be overwritten by the unit after next
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
         }
+        if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
     }
 
-    if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
+    // the next kernel may start its prologue while this grid drains
+    grid_dep_launch();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -253,7 +313,6 @@ __global__ void gemm_splitk_reduce_kernel(const GemmArgs p)
     }
     if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
 }
-
 template <int BN>
 cudaError_t launch_bn(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
                       const CUtensorMap& a2, const CUtensorMap& b, const GemmArgs& g)
@@ -267,10 +326,11 @@ cudaError_t launch_bn(const Launch& L, const CUtensorMap& a0, const CUtensorMap&
         attr_done = true;
     }
     const int n_tiles = (g.N + BN - 1) / BN;
-    const int grid = n_tiles * (g.M / BM) * g.k_splits;
+    const int units = n_tiles * (g.M / BM) * g.k_splits;
+    const int grid = units < 152 ? units : 152;          // persistent: one CTA per SM
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(GEMM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
@@ -292,13 +352,20 @@ int gemm_block_n(int N)
     return 256;
 }
 
+bool gemm_block_n_supported(int bn)
+{
+    return bn == 32 || bn == 64 || bn == 96 || bn == 128 || bn == 192 || bn == 256;
+}
+
 cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& a2, const CUtensorMap& b, int bn, const GemmArgs& g)
 {
     switch (bn) {
     case 32: return launch_bn<32>(L, a0, a1, a2, b, g);
     case 64: return launch_bn<64>(L, a0, a1, a2, b, g);
+    case 96: return launch_bn<96>(L, a0, a1, a2, b, g);
     case 128: return launch_bn<128>(L, a0, a1, a2, b, g);
+    case 192: return launch_bn<192>(L, a0, a1, a2, b, g);
     case 256: return launch_bn<256>(L, a0, a1, a2, b, g);
     default: return cudaErrorInvalidValue;
     }

@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_kernel(const GemvAr
         cur = locate<SCHEME>(p, grp, slot, seg, S, R);
         issue<SCHEME>(cur, lane, v, sc);
     }
+    if (threadIdx.x == 0) issue_l2_prefetch(p.next, blockIdx.x, gridDim.x);
     grid_dep_wait();
 
     // stage the activation row, RMS-normalised when a gain is given

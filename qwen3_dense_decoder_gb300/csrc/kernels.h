@@ -46,11 +46,20 @@ struct GemmArgs {
 
 // Box shapes a tensor map must have for the GEMM: weights 64 (K) x 128
 // rows (64 rows in pair mode); activations 64 x BN.
-int gemm_block_n(int N);          // chosen BN for N token rows
+int gemm_block_n(int N);          // smallest tile width covering N token rows
+bool gemm_block_n_supported(int bn);   // 32, 64, 96, 128, 192 or 256
 cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& a2, const CUtensorMap& b, int bn,
                         const GemmArgs& g);
 cudaError_t launch_gemm_splitk_reduce(const Launch& L, const GemmArgs& g);
+
+// Weights the next launch will stream: up to three contiguous ranges that a
+// kernel prefetches into L2 (a capped prefix, split over its CTAs) so HBM
+// stays busy across the kernel boundary.
+struct L2Prefetch {
+    const void* ptr[3];
+    uint64_t bytes[3];
+};
 
 // ---------------------------------------------------------------- GEMV
 // One token row: y[r] = sum_k W[r][k] * h[k], with h = x (or RMSNorm(x) * g
@@ -76,6 +85,7 @@ struct GemvArgs {
     float* am_val;             // [grid]
     int* am_idx;               // [grid]
     int* am_counter;
+    L2Prefetch next;           // weights of the next launch (bytes 0: none)
 };
 cudaError_t launch_gemv(const Launch& L, int scheme, const GemvArgs& a);
 // segments per row: a power of two, preferably with at most 8 loads per lane
@@ -127,6 +137,7 @@ struct AttnArgs {
     float* part_ml;            // [T][n_q][n_splits][2]
     float* part_o;             // [T][n_q][n_splits][128]
     int* counters;             // [T][n_kv], zero between calls (the last split CTA resets it)
+    L2Prefetch next;           // weights of the next launch
     void* out;                 // [T][n_q*128], f32 or fp16
     int out_f16;
     int* status;

@@ -309,28 +309,44 @@ int attention_splits(const q3_model* m, int T, int max_ctx)
     return s;
 }
 
-// Plan a tcgen05 GEMM: tile width and split-K count that keep the SMs busy.
-void plan_gemm(const q3_model* m, int M, int N, int K, int* bn, int* splits)
+// Plan a tcgen05 GEMM: tile width and split-K count.  Per 64-deep k-block a
+// 128 x BN tile costs the largest of 2 BN SM cycles (MMA issue), 128 + BN
+// (shared-memory reads of the A and B tiles at 128 bytes per cycle), the L2
+// time of those tiles and the HBM time of the weight tile (one read shared
+// by the n tiles); units run in rounds of 152 (one persistent CTA per SM);
+// split-K adds a reduction.
+void plan_gemm_impl(int M, int N, int K, size_t ws_elems, int* bn, int* splits)
 {
     const int kb = K / 64;
+    const int cand[6] = {32, 64, 96, 128, 192, 256};
     int best_bn = gemm_block_n(N), best_s = 1;
     double best = 1e30;
-    const int bns[2] = {gemm_block_n(N), N > 128 ? 128 : gemm_block_n(N)};
-    for (int bi = 0; bi < 2; ++bi) {
-        const int b = bns[bi];
+    for (int b : cand) {
+        if (b > gemm_block_n(N)) break;                  // wider than the rows need
         const int tiles = (M / 128) * ((N + b - 1) / b);
-        for (int s = 1; s <= 8; s *= 2) {
-            if (s > 1 && (kb / s < 4 || (size_t)s * N * M > m->ws_elems)) break;
-            const int ctas = tiles * s;
-            const int waves = (ctas + 151) / 152;
-            // per-CTA cost ~ MMA columns x k-blocks + a fixed prologue/epilogue
-            double cost = waves * ((double)b * kb / s + 8.0 * b + 400.0);
-            if (s > 1) cost += (double)s * N * M / (152.0 * 256.0);   // reduce pass
-            if (cost < best * 0.97) { best = cost; best_bn = b; best_s = s; }
+        for (int s = 1; s <= 4; s *= 2) {
+            if (s > 1 && (kb / s < 4 || (size_t)s * N * M > ws_elems)) break;
+            const int rounds = (tiles * s + 151) / 152;
+            // weight tile bytes from HBM per k-block, shared by the n tiles that
+            // read it at about the same time, at ~22 bytes per SM cycle
+            const int n_t = (N + b - 1) / b;
+            const double hbm = 16384.0 / n_t / 22.0;
+            // A and B tiles from L2 at ~58 bytes per SM cycle (measured on 2048-token tiles)
+            const double l2 = (16384.0 + 128.0 * b) / 58.0;
+            const double per_kb = std::max({(double)(2 * b), (double)(128 + b), hbm, l2});
+            double cost = (double)rounds * ((double)kb / s * per_kb + 600.0);
+            // partials written and read back plus the output pass, at ~3 TB/s (cycles at 2 GHz)
+            if (s > 1) cost += ((double)s * N * M * 8.0 + (double)N * M * 8.0) / 1500.0;
+            if (cost < best * 0.98) { best = cost; best_bn = b; best_s = s; }
         }
     }
     *bn = best_bn;
     *splits = best_s;
+}
+
+void plan_gemm(const q3_model* m, int M, int N, int K, int* bn, int* splits)
+{
+    plan_gemm_impl(M, N, K, m->ws_elems, bn, splits);
 }
 
 int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* a2,
@@ -360,9 +376,10 @@ int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtens
 
 int gemv(q3_model* m, int n_tensors, const void* const* w, const __half* const* sc, const int* rows,
          int pair, int K, const float* x, const bf16* gain, int epi, float* out,
-         int32_t* argmax = nullptr)
+         int32_t* argmax = nullptr, const L2Prefetch* next = nullptr)
 {
     GemvArgs a{};
+    if (next) a.next = *next;
     int total = 0;
     for (int i = 0; i < n_tensors; ++i) {
         a.w[i] = w[i];
@@ -389,6 +406,48 @@ int gemv(q3_model* m, int n_tensors, const void* const* w, const __half* const* 
     const int rc = m->check(launch_gemv(L, sc ? Q3_Q8_0 : Q3_BF16, a), "gemv");
     m->prof_end();
     return rc;
+}
+
+#ifndef Q3_L2_PREFETCH_MB
+#define Q3_L2_PREFETCH_MB 32
+#endif
+
+// The weight ranges of decode GEMV g of layer l (g: 0 QKV, 1 O, 2 gate/up,
+// 3 down; layer n_layers: the lm_head), capped to a prefix for L2 prefetch.
+L2Prefetch decode_weights(const q3_model* m, int l, int g)
+{
+    L2Prefetch pf{};
+    const q3_config& c = m->c;
+    const bool q8 = c.scheme == Q3_Q8_0;
+    const uint64_t cap = (uint64_t)Q3_L2_PREFETCH_MB << 20;
+    const uint64_t es = q8 ? 1 : 2;
+    const int H = c.hidden, F = c.ffn;
+    auto put = [&](int i, const void* p, uint64_t bytes) { pf.ptr[i] = p; pf.bytes[i] = bytes & ~uint64_t(15); };
+    if (l >= c.n_layers) {
+        put(0, m->lm_head, (uint64_t)c.vocab * H * 2);
+    } else {
+        const q3_layer_weights& W = m->layers[l];
+        auto wp = [&](int proj, const void* bf) -> const void* { return q8 ? (const void*)m->q8[l][proj].qs : bf; };
+        switch (g) {
+        case 0:
+            put(0, wp(P_Q, W.wq), (uint64_t)m->qw * H * es);
+            put(1, wp(P_K, W.wk), (uint64_t)m->kvw * H * es);
+            put(2, wp(P_V, W.wv), (uint64_t)m->kvw * H * es);
+            break;
+        case 1: put(0, wp(P_O, W.wo), (uint64_t)H * m->qw * es); break;
+        case 2:
+            put(0, wp(P_G, W.w_gate), (uint64_t)F * H * es);
+            put(1, wp(P_U, W.w_up), (uint64_t)F * H * es);
+            break;
+        default: put(0, wp(P_D, W.w_down), (uint64_t)H * F * es); break;
+        }
+    }
+    // cap the total to a prefix of each range, in proportion
+    uint64_t total = pf.bytes[0] + pf.bytes[1] + pf.bytes[2];
+    if (total > cap)
+        for (int i = 0; i < 3; ++i) pf.bytes[i] = (pf.bytes[i] * cap / total) & ~uint64_t(15);
+    if (cap == 0) pf = L2Prefetch{};
+    return pf;
 }
 
 int run_round(q3_model* m, const Round& r)
@@ -431,7 +490,9 @@ int run_round(q3_model* m, const Round& r)
             } else {
                 w[0] = W.wq; w[1] = W.wk; w[2] = W.wv;
             }
-            if ((rc = gemv(m, 3, w, q8 ? sc : nullptr, rows, 0, H, m->x, attn_norm, EPI_STORE_F32, m->qkv)))
+            const L2Prefetch nx = decode_weights(m, l, 1);
+            if ((rc = gemv(m, 3, w, q8 ? sc : nullptr, rows, 0, H, m->x, attn_norm, EPI_STORE_F32, m->qkv,
+                           nullptr, &nx)))
                 return rc;
         } else {
             if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->ha, m->status); }),
@@ -489,6 +550,7 @@ int run_round(q3_model* m, const Round& r)
             aa.out = one ? (void*)m->attf : (void*)m->att;
             aa.out_f16 = one ? 0 : 1;
             aa.status = m->status;
+            if (one) aa.next = decode_weights(m, l, 1);
             if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_attention(L, aa, true); }), "attention")))
                 return rc;
         } else {
@@ -512,7 +574,9 @@ int run_round(q3_model* m, const Round& r)
             const void* w[1] = {q8 ? (const void*)m->q8[l][P_O].qs : W.wo};
             const __half* sc[1] = {q8 ? m->q8[l][P_O].sc : nullptr};
             const int rows[1] = {H};
-            if ((rc = gemv(m, 1, w, q8 ? sc : nullptr, rows, 0, m->qw, m->attf, nullptr, EPI_ADD_F32, m->x)))
+            const L2Prefetch nx = decode_weights(m, l, 2);
+            if ((rc = gemv(m, 1, w, q8 ? sc : nullptr, rows, 0, m->qw, m->attf, nullptr, EPI_ADD_F32, m->x,
+                           nullptr, &nx)))
                 return rc;
         } else {
             if (q8) {
@@ -539,12 +603,16 @@ int run_round(q3_model* m, const Round& r)
                 w[0] = W.w_gate; w[1] = W.w_up;
             }
             const int rows[2] = {F, F};
-            if ((rc = gemv(m, 2, w, q8 ? sc : nullptr, rows, 1, H, m->x, ffn_norm, EPI_SWIGLU_F32, m->sf)))
+            const L2Prefetch nx2 = decode_weights(m, l, 3);
+            if ((rc = gemv(m, 2, w, q8 ? sc : nullptr, rows, 1, H, m->x, ffn_norm, EPI_SWIGLU_F32, m->sf,
+                           nullptr, &nx2)))
                 return rc;
             const void* wd[1] = {q8 ? (const void*)m->q8[l][P_D].qs : W.w_down};
             const __half* scd[1] = {q8 ? m->q8[l][P_D].sc : nullptr};
             const int rowsd[1] = {H};
-            if ((rc = gemv(m, 1, wd, q8 ? scd : nullptr, rowsd, 0, F, m->sf, nullptr, EPI_ADD_F32, m->x)))
+            const L2Prefetch nx3 = decode_weights(m, l + 1, 0);
+            if ((rc = gemv(m, 1, wd, q8 ? scd : nullptr, rowsd, 0, F, m->sf, nullptr, EPI_ADD_F32, m->x,
+                           nullptr, &nx3)))
                 return rc;
         } else {
             if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->ha, m->status); }),
@@ -1122,12 +1190,15 @@ int q3_model_profile_read(q3_model* m, int cls, double* total_ms, int64_t* launc
     return Q3_OK;
 }
 
-int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, float* y_dev, void* stream)
+int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, float* y_dev, int block_n,
+                 void* stream)
 {
     if (!w_dev || !x_dev || !y_dev || M < 128 || M % 128 || K < 64 || K % 64 || N < 1 ||
         !aligned16(w_dev) || !aligned16(x_dev))
         return fail(Q3_ERR_INVALID_ARG, "op_matmul: bad argument");
-    const int bn = gemm_block_n(N);
+    int bn = block_n, unused;
+    if (bn == 0) plan_gemm_impl(M, N, K, 0, &bn, &unused);   // no workspace: no split-K
+    if (!gemm_block_n_supported(bn)) return fail(Q3_ERR_INVALID_ARG, "op_matmul: unsupported block_n");
     CUtensorMap a, b;
     if (!tmap_f16(&a, w_dev, M, K, 128) || !tmap_f16(&b, x_dev, round_up(N, 256), K, bn))
         return fail(Q3_ERR_CUDA, "op_matmul: tensor map encoding failed");

@@ -47,7 +47,7 @@ def test_host_side_argument_checks_need_no_gpu(libq3):
     assert libq3.q3_model_create(None, None, 16, None, None) == -1
     assert libq3.q3_session_eval(None, None, 1, None, None) == -1
     assert libq3.q3_quantize_q8_0(None, ctypes.c_int64(32), None, None) == -1
-    assert libq3.q3_op_matmul(None, None, 128, 1, 64, None, None) == -1
+    assert libq3.q3_op_matmul(None, None, 128, 1, 64, None, 0, None) == -1
     assert b"bad argument" in libq3.q3_last_error()
 
 

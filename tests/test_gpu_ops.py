@@ -45,15 +45,16 @@ def test_quantizer_matches_oracle_packer_bitwise(q3, orc):
     np.testing.assert_array_equal(got, ref)
 
 
-@pytest.mark.parametrize("n", [1, 5, 32, 40, 83, 200, 300])
+@pytest.mark.parametrize("bn", [0, 32, 64, 96, 128, 192, 256])
+@pytest.mark.parametrize("n", [1, 5, 40, 83, 200, 300])
 @pytest.mark.parametrize("M,K", [(256, 64), (384, 2560), (128, 9728)])
-def test_tcgen05_matmul_matches_oracle(q3, orc, n, M, K):
+def test_tcgen05_matmul_matches_oracle(q3, orc, n, M, K, bn):
     # bf16-valued weights (exact in fp16) so the oracle's bf16 matmul applies
     w = _bf16((M, K), 10 + n, 0.05)
     rows = (n + 255) // 256 * 256
     x = torch.randn(rows, K, generator=torch.Generator(device="cuda").manual_seed(20 + n),
                     device="cuda").to(torch.float16)
-    y = q3.op_matmul(w.to(torch.float16), x, n)
+    y = q3.op_matmul(w.to(torch.float16), x, n, block_n=bn)
     torch.cuda.synchronize()
     wb = w.view(torch.int16).cpu().numpy().view(np.uint16)
     xf = _f32(x[:n])
