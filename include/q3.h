@@ -239,6 +239,20 @@ int q3_op_matmul_splitk_noalloc(const void* w_dev, const void* x_dev, int M, int
                                 int k_splits, float* y_dev, void* stream);
 const char* q3_noalloc_last_error(void);
 
+/* Fused decode step.  A one-session decode round (q3_session_eval with
+ * n == 1) runs as ONE persistent kernel -- embedding, every layer's
+ * projections, q/k norm + RoPE + KV append, attention, SwiGLU, final norm,
+ * lm_head and argmax -- instead of one launch per operation.  It computes
+ * what the per-operation path computes ("Kipp Model Support", section
+ * "qwen3-0.6b-base"; "Kipp Roadmap", status v0.0.4) with the same FP32
+ * accumulation; only summation order differs.  On by default wherever the
+ * shapes allow it.  q3_model_set_fused_decode(m, 0) selects the
+ * per-operation path (for comparison); on = 1 where the shapes do not
+ * allow it returns Q3_ERR_INVALID_ARG.  q3_model_fused_decode returns 1 when
+ * the fused step is in use, 0 otherwise. */
+int q3_model_set_fused_decode(q3_model* m, int on);
+int q3_model_fused_decode(const q3_model* m);
+
 /* Message of the last error on this host thread ("" if none). */
 const char* q3_last_error(void);
 
@@ -259,7 +273,8 @@ int64_t q3_model_launch_count(const q3_model* m);
 #define Q3_K_ROPE 3      /* q/k norm + RoPE + KV append */
 #define Q3_K_NORM 4      /* embedding and RMSNorm */
 #define Q3_K_OTHER 5     /* argmax, Q8_0 dequantisation */
-#define Q3_K_CLASSES 6
+#define Q3_K_STEP 6      /* fused one-kernel decode step */
+#define Q3_K_CLASSES 7
 int q3_model_profile(q3_model* m, int on);
 int q3_model_profile_reset(q3_model* m);
 int q3_model_profile_read(q3_model* m, int cls, double* total_ms, int64_t* launches);

@@ -88,6 +88,8 @@ def lib():
         L.q3_model_profile_reset.argtypes = [vp]
         L.q3_model_profile_read.argtypes = [vp, i, C.POINTER(C.c_double), C.POINTER(C.c_int64)]
         L.q3_op_matvec.argtypes = [vp, vp, vp, i, i, vp, vp]
+        L.q3_model_set_fused_decode.argtypes = [vp, i]
+        L.q3_model_fused_decode.argtypes = [vp]
         _lib = L
     return _lib
 
@@ -214,7 +216,17 @@ class Model:
     def launch_count(self) -> int:
         return lib().q3_model_launch_count(self.h)
 
-    KERNEL_CLASSES = ("gemv", "gemm", "attention", "qk_norm_rope_append", "norm", "other")
+    KERNEL_CLASSES = ("gemv", "gemm", "attention", "qk_norm_rope_append", "norm", "other",
+                      "decode_step")
+
+    @property
+    def fused_decode(self) -> bool:
+        """Whether one-session decode rounds run as the one-kernel fused step."""
+        return bool(lib().q3_model_fused_decode(self.h))
+
+    def set_fused_decode(self, on: bool) -> None:
+        """Select the fused decode step (default where supported) or the per-operation path."""
+        _check(lib().q3_model_set_fused_decode(self.h, 1 if on else 0))
 
     def profile(self, on: bool) -> None:
         """Per-launch CUDA-event timing by kernel class (serialises launches)."""

@@ -168,6 +168,65 @@ cudaError_t launch_attention(const Launch& L, const AttnArgs& a, bool fused);
 int attention_blocks_per_cta();
 int attention_max_splits();
 
+// ---------------------------------------------------------------- fused decode step
+// The whole one-token round of one session in one persistent kernel: one CTA
+// per SM, a producer warp streaming weight and KV tiles into a shared-memory
+// ring with bulk copies, and consumer warps computing every stage (QKV, q/k
+// norm + RoPE + KV append + attention, O, gate/up + SwiGLU, down, lm_head +
+// argmax), separated by grid-wide barriers.
+struct DecodeLayer {
+    const __nv_bfloat16* attn_norm;
+    const __nv_bfloat16* q_norm;
+    const __nv_bfloat16* k_norm;
+    const __nv_bfloat16* ffn_norm;
+    const void* w[7];          // wq, wk, wv, wo, w_gate, w_up, w_down: bf16, or Q8_0 int8 quants
+    const __half* sc[7];       // Q8_0 fp16 scale planes [rows][K/32] (null for bf16)
+};
+
+struct DecodeArgs {
+    int n_layers, H, F, V, n_q, n_kv;
+    float eps;
+    int q8;                    // projections are Q8_0 planes (the lm_head is bf16 either way)
+    const DecodeLayer* layers; // device [n_layers]
+    const __nv_bfloat16* embed;
+    const __nv_bfloat16* final_norm;
+    const __nv_bfloat16* lm_head;
+    const float2* rope;        // [max_ctx][64] (cos, sin)
+    const int32_t* token;      // [1]
+    const int* row_pos;        // [1] position of the new token
+    const int* row_slot;       // [1] session slot
+    const int* tables;
+    int max_blocks;
+    __nv_bfloat16* kv;         // pool base: [n_layers][n_blocks][2][n_kv][32][128]
+    int64_t layer_kv;          // elements per layer
+    int n_blocks;
+    int n_splits;              // attention splits per KV head (n_kv * n_splits <= grid)
+    float* x;                  // [H] residual
+    float* qkv;                // [(n_q + 2 n_kv) 128]
+    float* att;                // [n_q 128]
+    float* ffn;                // [F]
+    float* part_ml;            // [n_q][n_splits][2]
+    float* part_o;             // [n_q][n_splits][128]
+    int* counters;             // [n_kv], zero between calls
+    float* logits;             // [V]
+    int32_t* argmax_out;       // [1] or null
+    float* am_val;             // [grid]
+    int* am_idx;               // [grid]
+    int* am_counter;           // zero between calls
+    unsigned long long* bar;   // grid barrier counter (monotonic across launches)
+    unsigned long long bar_base;   // its value when this launch starts
+    int n_slots;               // ring depth
+    int* status;
+};
+// Shared memory of the fused step for these dimensions and ring depth; 0 if
+// the shapes are outside what the kernel handles.
+size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, int n_splits);
+int decode_step_slot_bytes();
+// Grid barriers one launch performs (each adds grid to *bar).
+int decode_step_barriers(int n_layers);
+cudaError_t decode_step_prepare(size_t smem);
+cudaError_t launch_decode_step(const Launch& L, const DecodeArgs& a, int grid, size_t smem);
+
 cudaError_t launch_argmax(const Launch& L, const float* logits, int rows, int V, int32_t* out);
 
 // Q8_0: canonical blocks -> (int8 plane, fp16 scale plane); planes -> fp16

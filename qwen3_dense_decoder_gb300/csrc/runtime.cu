@@ -140,6 +140,17 @@ struct q3_model {
     int* am_idx = nullptr;
     int* am_counter = nullptr;      // ticket of the argmax merge, zero between rounds
 
+    // fused one-kernel decode step (one-session decode rounds)
+    bool step_ok = false;           // shapes and device support it
+    bool fused_decode = true;       // use it when step_ok
+    int step_grid = 0, step_slots = 0, step_splits = 0;
+    size_t step_smem = 0;
+    DecodeLayer* step_layers = nullptr;       // device [n_layers]
+    unsigned long long* step_bar = nullptr;   // grid barrier counter
+    unsigned long long step_epoch = 0;        // its value before the next launch
+    float* step_am_val = nullptr;
+    int* step_am_idx = nullptr;
+
     // pinned staging ring for host -> device metadata
     uint8_t* stage = nullptr;
     size_t stage_slot = 0;
@@ -450,6 +461,102 @@ L2Prefetch decode_weights(const q3_model* m, int l, int g)
     return pf;
 }
 
+// The fused decode step: one CTA per SM, a cooperative launch.  Chooses the
+// ring depth that fits the shared memory, the attention splits per KV head,
+// and uploads the per-layer weight pointers.  Shapes the kernel does not
+// handle leave it off (the per-operation path runs instead).
+int setup_decode_step(q3_model* m, int n_sm)
+{
+    const q3_config& c = m->c;
+    const bool q8 = c.scheme == Q3_Q8_0;
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return fail(Q3_ERR_CUDA, "device query failed");
+    const int grid = n_sm;
+    int splits = grid / c.n_kv_heads;
+    splits = std::min<int>(splits, (int)m->part_rows);
+    if (splits < 1) return Q3_OK;
+    int slots = 0;
+    size_t smem = 0;
+    for (int n = 8; n >= 3; --n) {
+        const size_t b = decode_step_smem(c.hidden, c.ffn, c.n_q_heads, c.n_kv_heads, q8, n, splits);
+        if (b && b <= (size_t)optin) { slots = n; smem = b; break; }
+    }
+    if (!slots) return Q3_OK;
+    if (decode_step_prepare(smem) != cudaSuccess) {
+        cudaGetLastError();
+        return Q3_OK;
+    }
+    std::vector<DecodeLayer> h(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        const q3_layer_weights& W = m->layers[l];
+        DecodeLayer& d = h[l];
+        d.attn_norm = static_cast<const bf16*>(W.attn_norm);
+        d.q_norm = static_cast<const bf16*>(W.q_norm);
+        d.k_norm = static_cast<const bf16*>(W.k_norm);
+        d.ffn_norm = static_cast<const bf16*>(W.ffn_norm);
+        const void* src[N_PROJ] = {W.wq, W.wk, W.wv, W.wo, W.w_gate, W.w_up, W.w_down};
+        for (int p = 0; p < N_PROJ; ++p) {
+            d.w[p] = q8 ? static_cast<const void*>(m->q8[l][p].qs) : src[p];
+            d.sc[p] = q8 ? m->q8[l][p].sc : nullptr;
+        }
+    }
+    m->step_layers = static_cast<DecodeLayer*>(m->dalloc(sizeof(DecodeLayer) * c.n_layers));
+    m->step_bar = static_cast<unsigned long long*>(m->dalloc(sizeof(unsigned long long)));
+    m->step_am_val = static_cast<float*>(m->dalloc(sizeof(float) * grid));
+    m->step_am_idx = static_cast<int*>(m->dalloc(sizeof(int) * grid));
+    if (!m->step_layers || !m->step_bar || !m->step_am_val || !m->step_am_idx)
+        return fail(Q3_ERR_OOM, "device allocation failed");
+    if (cudaMemcpy(m->step_layers, h.data(), sizeof(DecodeLayer) * c.n_layers, cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemset(m->step_bar, 0, sizeof(unsigned long long)) != cudaSuccess)
+        return fail(Q3_ERR_CUDA, "fused decode setup failed");
+    m->step_grid = grid;
+    m->step_slots = slots;
+    m->step_splits = splits;
+    m->step_smem = smem;
+    m->step_epoch = 0;
+    m->step_ok = true;
+    return Q3_OK;
+}
+
+// One-session decode round as one fused kernel.
+int run_decode_step(q3_model* m, const Round& r)
+{
+    const q3_config& c = m->c;
+    DecodeArgs a{};
+    a.n_layers = c.n_layers; a.H = c.hidden; a.F = c.ffn; a.V = c.vocab;
+    a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.eps = c.rms_eps;
+    a.q8 = c.scheme == Q3_Q8_0;
+    a.layers = m->step_layers;
+    a.embed = m->embed; a.final_norm = m->final_norm; a.lm_head = m->lm_head;
+    a.rope = m->rope;
+    a.token = r.tokens;
+    a.row_pos = m->meta;
+    a.row_slot = m->meta + m->max_rows;
+    a.tables = r.pool->tables; a.max_blocks = r.pool->max_blocks;
+    a.kv = r.pool->kv;
+    a.layer_kv = (int64_t)r.pool->n_blocks * 2 * c.n_kv_heads * 32 * 128;
+    a.n_blocks = r.pool->n_blocks;
+    a.n_splits = m->step_splits;
+    a.x = m->x; a.qkv = m->qkv; a.att = m->attf; a.ffn = m->sf;
+    a.part_ml = m->part_ml; a.part_o = m->part_o;
+    a.counters = m->attn_counters;
+    a.logits = r.logits; a.argmax_out = r.argmax;
+    a.am_val = m->step_am_val; a.am_idx = m->step_am_idx; a.am_counter = m->am_counter;
+    a.bar = m->step_bar; a.bar_base = m->step_epoch;
+    a.n_slots = m->step_slots;
+    a.status = m->status;
+    Launch L{m->stream, false, &m->launches};
+    m->prof_begin(Q3_K_STEP);
+    const int rc = m->check(launch_decode_step(L, a, m->step_grid, m->step_smem), "fused decode step");
+    m->prof_end();
+    if (rc == Q3_OK)
+        m->step_epoch += (unsigned long long)decode_step_barriers(c.n_layers) * m->step_grid;
+    return rc;
+}
+
 int run_round(q3_model* m, const Round& r)
 {
     const q3_config& c = m->c;
@@ -467,6 +574,7 @@ int run_round(q3_model* m, const Round& r)
         m->prof_end();
         return e;
     };
+    if (one && r.ns == 1 && m->step_ok && m->fused_decode) return run_decode_step(m, r);
     const size_t layer_kv = (size_t)r.pool->n_blocks * 2 * c.n_kv_heads * 32 * 128;
     const int n_splits = attention_splits(m, T, r.max_ctx);
     int rc;
@@ -802,6 +910,16 @@ const char* q3_last_error(void) { return g_err.c_str(); }
 
 int64_t q3_model_launch_count(const q3_model* m) { return m ? m->launches : 0; }
 
+int q3_model_set_fused_decode(q3_model* m, int on)
+{
+    if (!m) return fail(Q3_ERR_INVALID_ARG, "model is NULL");
+    if (on && !m->step_ok) return fail(Q3_ERR_INVALID_ARG, "fused decode step unsupported for these shapes");
+    m->fused_decode = on != 0;
+    return Q3_OK;
+}
+
+int q3_model_fused_decode(const q3_model* m) { return m && m->step_ok && m->fused_decode ? 1 : 0; }
+
 int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tokens, void* stream,
                     q3_model** out)
 {
@@ -982,6 +1100,10 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
         m->inexact_f16 = (int64_t)cnt[0];
     }
     if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
+    if ((rc = setup_decode_step(m, prop.multiProcessorCount))) {
+        free_model(m);
+        return rc;
+    }
     if (cudaStreamSynchronize(m->stream) != cudaSuccess || cudaGetLastError() != cudaSuccess)
         return bad(Q3_ERR_CUDA, "model setup failed");
     *out = m;
