@@ -203,7 +203,7 @@ def run_gpu(args, dist_on: bool, rank: int, world: int):
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     W, K, P = args.warmup, args.steps, args.prompt
-    max_ctx = P + W + 3 * K + 64      # value, profiled and e2e passes share the session
+    max_ctx = P + W + 4 * K + 64      # value, profiled, per-operation and e2e passes share the session
     w = synthetic.make_weights(shape, seed=1234, device="cuda")
     model = q3.Model(shape, w, max_ctx=max_ctx, max_round_tokens=P, stream=stream)
     n_sess = 2 + (0 if args.no_b32 else args.sessions)     # decode + profiled-prefill sessions
@@ -251,11 +251,27 @@ def run_gpu(args, dist_on: bool, rank: int, world: int):
     out["clocks"] = clk.summary()
 
     # ---- profiled pass of the same decode steps (per-kernel CUDA events)
+    p0 = sess.pos
     model.profile(True)
     model.profile_reset()
     decode_loop(sess, tok, logits[0], K)
     out["decode_profile"] = model.profile_read()
+    out["decode_profile_ctx"] = (p0 + 1, p0 + K)
     model.profile(False)
+    # ---- the same decode steps on the per-operation path (one launch per
+    # operation), for comparison with the fused step
+    out["fused"] = model.fused_decode
+    if model.fused_decode:
+        model.set_fused_decode(False)
+        decode_loop(sess, tok, logits[0], 2)
+        model.sync()
+        q0 = sess.pos
+        timer.start()
+        decode_loop(sess, tok, logits[0], K)
+        out["per_op_ms"] = timer.stop()
+        out["per_op_ctx"] = (q0 + 1, q0 + K)
+        model.set_fused_decode(True)
+        model.sync()
     # ---- profiled prefill
     sess2 = pool.session()
     model.profile(True)
@@ -377,8 +393,18 @@ def report(args, res, world, dist_on, pk, pk_kind):
     mean_ctx = (c0 + c1) / 2
     step_bytes = decode_bytes(s, mean_ctx)
     w_bytes = 2.0 * proj_params(s) + 2.0 * s.vocab * s.hidden
-    gemv_ms, gemv_n = res["decode_profile"]["gemv"]
-    gemv_achieved = (w_bytes * K / gemv_n) / (gemv_ms / gemv_n / 1e3) / 1e9
+    prof = res["decode_profile"]
+    if prof.get("decode_step", (0, 0))[1]:
+        # the fused step: one launch streams every weight and the KV context
+        k_ms, k_n = prof["decode_step"]
+        pc0, pc1 = res["decode_profile_ctx"]
+        k_bytes = decode_bytes(s, (pc0 + pc1) / 2)
+        k_name = "decode_step (fused one-kernel decode step: all projections, attention, lm_head)"
+    else:
+        k_ms, k_n = prof["gemv"]
+        k_bytes = w_bytes * K / k_n
+        k_name = "gemv (decode matvec, all projections + lm_head)"
+    k_achieved = k_bytes / (k_ms / k_n / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(dec_ms / K, 4),
@@ -389,15 +415,22 @@ def report(args, res, world, dist_on, pk, pk_kind):
                          "bytes_per_step": step_bytes, "peak_gbs": pk["hbm_gbs"],
                          "frac": round(step_bytes * value / world / 1e9 / pk["hbm_gbs"], 4),
                          "peak_kind": pk_kind},
-        "roofline": {"kernel": "gemv (decode matvec, all projections + lm_head)", "bound": "hbm",
-                     "achieved": round(gemv_achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gemv_achieved / pk["hbm_gbs"], 4), "traffic": None,
-                     "bytes_per_launch": w_bytes * K / gemv_n, "launches": gemv_n,
-                     "mean_launch_us": round(gemv_ms / gemv_n * 1e3, 3), "peak_kind": pk_kind},
+        "roofline": {"kernel": k_name, "bound": "hbm",
+                     "achieved": round(k_achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(k_achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "bytes_per_launch": k_bytes, "launches": k_n,
+                     "mean_launch_us": round(k_ms / k_n * 1e3, 3), "peak_kind": pk_kind},
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
         "decode_kernels_ms_per_step": {k: round(v[0] / K, 4) for k, v in res["decode_profile"].items()},
     }
+    if "per_op_ms" in res:
+        q0, q1 = res["per_op_ctx"]
+        po_ms = max_over_ranks(res["per_op_ms"], dist_on)
+        line["decode_per_op_path"] = {
+            "value": round(world * K / (po_ms / 1e3), 2), "unit": "tok/s", "ms_per_step": round(po_ms / K, 4),
+            "hbm_frac": round(decode_bytes(s, (q0 + q1) / 2) * K / (po_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+            "note": "same steps, one launch per operation (q3_model_set_fused_decode(m, 0))"}
     # prefill
     P = args.prompt
     pre_ms = max_over_ranks(res["prefill_ms"], dist_on)

@@ -46,14 +46,15 @@ constexpr int THREADS = NCT + 64;          // + producer and epilogue warps
 constexpr int SLOT = 40 * 1024;            // bytes per ring slot
 constexpr int RED = 64;                    // row partials per slot (rows x warp segments)
 constexpr int D = 128, KVB = 32;
-constexpr int KSTR = D + 8;                // staged K row stride (bf16): 272 bytes, conflict-free
+constexpr int KSTR = D + 8;                // staged K/V/q row stride (bf16): 272 bytes, conflict-free ldmatrix
 constexpr int KT_BYTES = KVB * KSTR * 2;
-constexpr int VT_BYTES = KVB * D * 2;
+constexpr int VT_BYTES = KVB * KSTR * 2;
 constexpr int BLK_BYTES = KT_BYTES + VT_BYTES;
 constexpr int BLKS_PER_SLOT = 2;
 constexpr int CONS_BAR = 1;                // named barrier of the consumer warps
 constexpr int MIN_SLOTS = 3, MAX_SLOTS = 8;
-constexpr int XCPL = 5;                    // activation chunks a lane keeps in registers (bf16 tiles)
+constexpr int XCPL = 5;
+constexpr int MAX_OWN = 64;                // residual rows a CTA owns (H / grid, rounded up)                    // activation chunks a lane keeps in registers (bf16 tiles)
 
 static_assert(BLKS_PER_SLOT * BLK_BYTES <= SLOT, "two KV blocks per slot");
 
@@ -79,7 +80,7 @@ struct AttScratch {
 __host__ __device__ inline AttScratch att_scratch(int G, int ns) {
     AttScratch a;
     int o = 0;
-    a.sq = o; o += G * D;
+    a.sq = o; o += 16 * KSTR / 2;                 // bf16 [16][KSTR]: q hi / lo rows
     a.snew = o; o += D;
     a.pm = o; o += 4 * G;
     a.pl = o; o += 4 * G;
@@ -110,7 +111,7 @@ __host__ __device__ inline Layout make_layout(int n_slots, int sxf) {
     L.red = L.sx + (size_t)sxf * 4;
     L.bars = L.red + (size_t)n_slots * RED * 4;
     L.misc = L.bars + (size_t)(3 * n_slots + 1) * 8;
-    L.total = L.misc + (size_t)(3 * NCW + 4) * 4;
+    L.total = L.misc + (size_t)(3 * NCW + 4 + MAX_OWN) * 4;
     return L;
 }
 
@@ -127,6 +128,7 @@ struct Smem {
     int* bi;            // [NCW]
     volatile int* abort;
     int* ticket;
+    float* xres;        // [MAX_OWN] the CTA's residual rows (epilogue warp only)
     int n_slots;
 };
 
@@ -134,12 +136,6 @@ struct Smem {
 Q3_DEV float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-Q3_DEV float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 
@@ -346,8 +342,8 @@ Q3_DEV bool produce_weights(const WStage& s, const Smem& sm, uint32_t& it, int l
     return true;
 }
 
-// KV blocks of the attention unit, two per slot: K rows padded to KSTR (one
-// 256-byte copy per row, one per lane), V as one 8 KB copy.
+// KV blocks of the attention unit, two per slot: K and V rows padded to KSTR
+// (one 256-byte copy per row; lane l copies row l of both).
 Q3_DEV bool produce_attention(const DecodeArgs& p, int l, const Unit& u, const int* table,
                               const Smem& sm, uint32_t& it, int lane) {
     for (int b = u.b0; b < u.b1; b += BLKS_PER_SLOT) {
@@ -360,7 +356,7 @@ Q3_DEV bool produce_attention(const DecodeArgs& p, int l, const Unit& u, const i
         for (int j = 0; j < BLKS_PER_SLOT; ++j) {
             phys[j] = j < nb ? table[b + j] : -1;
             if (phys[j] >= p.n_blocks) phys[j] = -1;
-            if (phys[j] >= 0) bytes += 2 * KVB * D * 2;
+            if (phys[j] >= 0) bytes += 2 * KVB * D * 2;   // 64 rows of 256 bytes
         }
         if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], bytes);
         __syncwarp();
@@ -371,7 +367,7 @@ Q3_DEV bool produce_attention(const DecodeArgs& p, int l, const Unit& u, const i
             const bf16* Kb = kv_block(p, l, phys[j], u.kvh);
             const bf16* Vb = Kb + (size_t)p.n_kv * KVB * D;
             bulk_load(dst + j * BLK_BYTES + lane * KSTR * 2, Kb + lane * D, D * 2, &sm.full[slot]);
-            if (lane == 0) bulk_load(dst + j * BLK_BYTES + KT_BYTES, Vb, VT_BYTES, &sm.full[slot]);
+            bulk_load(dst + j * BLK_BYTES + KT_BYTES + lane * KSTR * 2, Vb + lane * D, D * 2, &sm.full[slot]);
         }
         __syncwarp();
         ++it;
@@ -436,7 +432,7 @@ Q3_DEV void stage_x(const Smem& sm, const float* src, const bf16* src16, int K, 
 // their S segment sums in segment order; store, residual add, SwiGLU of a
 // gate/up pair, or store plus greedy-argmax tracking.
 Q3_DEV void tile_epilogue(const WStage& s, int kind, const float* red, int S, int a, int nvalid, int lane,
-                          float* out, float& best, int& best_i) {
+                          float* out, float* xres, float& best, int& best_i) {
     for (int rho = lane; rho < nvalid; rho += 32) {
         const int row = a + rho;
         float v = 0.f;
@@ -446,7 +442,10 @@ Q3_DEV void tile_epilogue(const WStage& s, int kind, const float* red, int S, in
             for (int q = 0; q < S; ++q) u += red[(rho + s.per) * S + q];
             __stcg(out + row, silu(v) * u);
         } else if (kind == ST_O || kind == ST_DOWN) {
-            __stcg(out + row, __ldcg(out + row) + v);
+            // the residual row lives in shared memory; global memory gets a copy
+            const float x = xres[row - s.r0] + v;
+            xres[row - s.r0] = x;
+            __stcg(out + row, x);
         } else {
             __stcg(out + row, v);
             if (kind == ST_LM && better(v, row, best, best_i)) { best = v; best_i = row; }
@@ -564,62 +563,147 @@ Q3_DEV void consume_weights(const WStage& s, const Smem& sm, uint32_t& it, int w
     else consume_bf16(s, sm, it, warp, lane, p);
 }
 
-// One 32-position block for one query head: lane j scores position j, then
-// lane l accumulates output dimensions [4 l, 4 l + 4).  The new position's
-// K/V rows come from knew/vnew (this step's append), not from the tile.
-Q3_DEV void attend_block(const bf16* kt, const bf16* vt, const float* q, const bf16* knew,
-                         const bf16* vnew, int new_r, int n_pos, int lane, float& m, float& l,
-                         float (&o)[4]) {
-    const bf16* krow = (knew && lane == new_r) ? knew : kt + lane * KSTR;
-    float s = 0.f;
+// ---------------------------------------------------------------- attention on tensor cores
+Q3_DEV void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+Q3_DEV void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+// D = A (16 x 16, row) * B (16 x 8, col) + D, bf16 inputs, fp32 accumulate
+Q3_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                     uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                 "{%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+Q3_DEV uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Online-softmax state of one warp over its blocks: the warp holds S and O
+// rows g = lane / 4 and g + 8 of the 16-row operands, row r standing for
+// query head r / 2 (even r: the bf16 high part of q or p, odd r: the
+// remainder), so q . k and p . v are exact to about 16 bits while K and V
+// stay the stored BF16.
+constexpr int ATT_DQ = 4;                  // warps per block: each takes 128 / ATT_DQ output dims
+constexpr int ATT_DT = D / 8 / ATT_DQ;     // dimension tiles of 8 per warp
+
+struct AttWarp {
+    float m[2], l[2];
+    float o[ATT_DT][4];       // this warp's dimension tiles
+};
+
+// Address of 16-byte chunk c (0..15, 8 dims each) of row r of a staged K/V tile.
+Q3_DEV const uint8_t* tile_chunk(const uint8_t* t, int r, int c) {
+    return t + r * (KSTR * 2) + c * 16;
+}
+
+// One 32-position block for the G query heads of the KV head (rows 2h, 2h+1
+// of sqa), output dimensions [32 dq, 32 dq + 32): S = q K^T on 4 x 8 mma
+// (positions x dims), masked to n_pos, online softmax, O += P V on 4 x 2.
+Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const bf16* sqa, int n_pos, int dq, int lane,
+                            AttWarp& w) {
+    const int g = lane >> 2, tig = lane & 3;
+    float sacc[4][4];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-        const uint4 kw = *reinterpret_cast<const uint4*>(krow + c * 8);
-        const float4 qa = *reinterpret_cast<const float4*>(q + c * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(q + c * 8 + 4);
-        s = fmaf(bf16lo(kw.x), qa.x, s);
-        s = fmaf(bf16hi(kw.x), qa.y, s);
-        s = fmaf(bf16lo(kw.y), qa.z, s);
-        s = fmaf(bf16hi(kw.y), qa.w, s);
-        s = fmaf(bf16lo(kw.z), qb.x, s);
-        s = fmaf(bf16hi(kw.z), qb.y, s);
-        s = fmaf(bf16lo(kw.w), qb.z, s);
-        s = fmaf(bf16hi(kw.w), qb.w, s);
-    }
-    const bool valid = lane < n_pos;
-    const float sv = valid ? s : -INFINITY;
-    const float m_new = fmaxf(m, warp_max(sv));
-    const float alpha = exp2f(m - m_new);           // 0 on the first block (m = -inf)
-    const float pr = valid ? exp2f(sv - m_new) : 0.f;
-    l = l * alpha + warp_sum(pr);
-    o[0] *= alpha; o[1] *= alpha; o[2] *= alpha; o[3] *= alpha;
-    m = m_new;
-#pragma unroll 8
-    for (int j = 0; j < KVB; ++j) {
-        const float pj = __shfl_sync(0xffffffffu, pr, j);
-        if (pj != 0.f) {
-            const bf16* vrow = (vnew && j == new_r) ? vnew : vt + j * D;
-            const uint2 vw = *reinterpret_cast<const uint2*>(vrow + lane * 4);
-            o[0] = fmaf(pj, bf16lo(vw.x), o[0]);
-            o[1] = fmaf(pj, bf16hi(vw.x), o[1]);
-            o[2] = fmaf(pj, bf16lo(vw.y), o[2]);
-            o[3] = fmaf(pj, bf16hi(vw.y), o[3]);
+    for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t a[4];
+        // A: matrices (rows 0-7, k 0-7), (rows 8-15, k 0-7), (rows 0-7, k 8-15), (rows 8-15, k 8-15)
+        ldsm_x4(a, sqa + ((mi & 1) * 8 + r8) * KSTR + kk * 16 + (mi >> 1) * 8);
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+            uint32_t b[4];
+            // B: positions 16 nh + (0-7 | 8-15) x dims (0-7 | 8-15) of this k step
+            ldsm_x4(b, tile_chunk(kt, nh * 16 + (mi >> 1) * 8 + r8, kk * 2 + (mi & 1)));
+            mma_bf16(sacc[2 * nh], a[0], a[1], a[2], a[3], b[0], b[1]);
+            mma_bf16(sacc[2 * nh + 1], a[0], a[1], a[2], a[3], b[2], b[3]);
         }
+    }
+    // rows 2h and 2h + 1 hold the two parts of head h: add them (lanes g ^ 1)
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float v = sacc[nt][e] + __shfl_xor_sync(0xffffffffu, sacc[nt][e], 4);
+            const int pos = nt * 8 + 2 * tig + (e & 1);
+            v = pos < n_pos ? v : -INFINITY;
+            sacc[nt][e] = v;
+            mx[e >> 1] = fmaxf(mx[e >> 1], v);
+        }
+    }
+    float alpha[2], sum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        const float m_new = fmaxf(w.m[h], mx[h]);
+        alpha[h] = exp2f(w.m[h] - m_new);          // 0 on the first block (m = -inf)
+        w.m[h] = m_new;
+    }
+    // P and its bf16 split: even rows take the high part, odd rows the rest
+    const bool hi_row = (g & 1) == 0;
+    uint32_t pa[4][2];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            pv[e] = exp2f(sacc[nt][e] - w.m[e >> 1]);
+            sum[e >> 1] += pv[e];
+        }
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+            const float x0 = pv[2 * hp], x1 = pv[2 * hp + 1];
+            const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+            const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+            pa[nt][hp] = hi_row ? pack_bf16(h0, h1) : pack_bf16(x0 - h0, x1 - h1);
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
+        sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
+        w.l[h] = w.l[h] * alpha[h] + sum[h];
+    }
+#pragma unroll
+    for (int dt = 0; dt < ATT_DT; ++dt) {
+        w.o[dt][0] *= alpha[0]; w.o[dt][1] *= alpha[0];
+        w.o[dt][2] *= alpha[1]; w.o[dt][3] *= alpha[1];
+    }
+    // O += P V: k = positions (2 steps of 16), n = this warp's dimension tiles
+#pragma unroll
+    for (int dt = 0; dt < ATT_DT; ++dt) {
+        uint32_t b[4];
+        // V^T: matrices of positions (0-7 | 8-15 | 16-23 | 24-31) x dims 8 dt of this quarter
+        ldsm_x4_t(b, tile_chunk(vt, mi * 8 + r8, (dq * (D / ATT_DQ) + dt * 8) / 8));
+        mma_bf16(w.o[dt], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b[0], b[1]);
+        mma_bf16(w.o[dt], pa[2][0], pa[2][1], pa[3][0], pa[3][1], b[2], b[3]);
     }
 }
 
-// The attention unit of this CTA: q heads of its KV head normed and rotated,
-// the new K/V appended (by the unit holding the last block), its blocks
-// attended by BR x G warps (BR blocks in flight per round of BR / 2 slots,
-// warp (j, g) takes block j of each round for query head g), then merged:
-// block lanes in order, then splits in order by the last split CTA of the
-// KV head, which first stages every split's partials in shared memory.
+// The attention unit of this CTA: q heads of its KV head normed, rotated and
+// split into bf16 high/low rows; the new K/V appended (by the unit holding
+// the last block) and patched into its staged tile; blocks attended on
+// tensor cores by groups of ATT_DQ warps (block j of each round of 4, one
+// quarter of the output dimensions each);
+// then merged: block lanes in order, then splits in order by the last split
+// CTA of the KV head, which first stages every split's partials in shared
+// memory.
 Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const int* table, const Smem& sm,
                               uint32_t& it, int warp, int lane) {
     const int G = p.n_q / p.n_kv, ns = p.n_splits, tid = threadIdx.x;
-    const int BR = 2 * BLKS_PER_SLOT * G <= NCW ? 2 * BLKS_PER_SLOT : BLKS_PER_SLOT;
+    constexpr int BR = 2 * BLKS_PER_SLOT;                      // blocks per round (2 slots)
     const AttScratch A = att_scratch(G, ns);
-    float* sq = sm.sx + A.sq;                                  // [G][D]
+    bf16* sqa = reinterpret_cast<bf16*>(sm.sx + A.sq);         // [16][KSTR]
     bf16* snew = reinterpret_cast<bf16*>(sm.sx + A.snew);      // [2][D]
     float* pm = sm.sx + A.pm;                                  // [BR][G]
     float* pl = sm.sx + A.pl;                                  // [BR][G]
@@ -636,19 +720,24 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
             const float4 v = __ldcg(reinterpret_cast<const float4*>(p.qkv + (u.kvh * G + warp) * D + lane * 4));
             float y[4] = {v.x, v.y, v.z, v.w};
             head_norm_rope(y, L.q_norm, rope_row, p.eps, lane);
-            *reinterpret_cast<float4*>(sq + warp * D + lane * 4) =
-                make_float4(y[0] * qscale, y[1] * qscale, y[2] * qscale, y[3] * qscale);
+            float hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float q = y[e] * qscale;
+                hi[e] = __bfloat162float(__float2bfloat16_rn(q));
+                lo[e] = q - hi[e];
+            }
+            *reinterpret_cast<uint2*>(sqa + (2 * warp) * KSTR + lane * 4) =
+                make_uint2(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]));
+            *reinterpret_cast<uint2*>(sqa + (2 * warp + 1) * KSTR + lane * 4) =
+                make_uint2(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]));
         } else if (mine && warp < G + 2) {
             const bool is_k = warp == G;
             const float4 v = __ldcg(reinterpret_cast<const float4*>(
                 p.qkv + (p.n_q + (is_k ? 0 : p.n_kv) + u.kvh) * D + lane * 4));
             float y[4] = {v.x, v.y, v.z, v.w};
             if (is_k) head_norm_rope(y, L.k_norm, rope_row, p.eps, lane);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
-            uint2 packed;
-            packed.x = *reinterpret_cast<const uint32_t*>(&lo);
-            packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+            const uint2 packed = make_uint2(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]));
             *reinterpret_cast<uint2*>(snew + (is_k ? 0 : D) + lane * 4) = packed;
             const int phys = table[last_blk];
             if (phys >= 0 && phys < p.n_blocks) {
@@ -658,31 +747,48 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
             } else if (lane == 0) {
                 set_status(p.status, Q3_STATUS_BLOCK_RANGE);
             }
+        } else if (warp >= G + 2) {
+            // rows of the 16-row q operand past the G heads are zero
+            for (int i = (warp - G - 2) * 32 + lane; i < (16 - 2 * G) * (D / 8); i += (NCW - G - 2) * 32)
+                *reinterpret_cast<uint4*>(sqa + (2 * G + i / (D / 8)) * KSTR + (i % (D / 8)) * 8) =
+                    make_uint4(0u, 0u, 0u, 0u);
         }
     }
     consumer_sync();
 
-    const int j = warp / G, g = warp % G;
+    // warp w: block j = w / ATT_DQ of each round, dimension quarter dq = w % ATT_DQ
+    const int j = warp / ATT_DQ, dq = warp % ATT_DQ;
     const bool worker = j < BR;
-    float m = -INFINITY, lsum = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+    AttWarp st;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+    for (int dt = 0; dt < ATT_DT; ++dt) st.o[dt][0] = st.o[dt][1] = st.o[dt][2] = st.o[dt][3] = 0.f;
     const int new_r = u.pos % KVB;
     for (int b = u.b0, k = 0; b < u.b1; b += BLKS_PER_SLOT, ++k) {
         const int slot = it % sm.n_slots;
         const uint32_t use = it / sm.n_slots;
         ++it;
         if (!wait_bar(&sm.full[slot], use & 1, sm, p.status)) break;
-        // slot k of the unit holds blocks b, b + 1; in a round of BR blocks
-        // it is slot k % (BR / 2), served by warps j = 2 (k % (BR / 2)) + {0, 1}
+        // slot k of the unit holds blocks b, b + 1: in a round of BR blocks it
+        // is slot k % (BR / 2), served by block lanes j = 2 (k % (BR / 2)) + {0, 1}
         const int blk = b + (j % BLKS_PER_SLOT);
         if (worker && j / BLKS_PER_SLOT == k % (BR / BLKS_PER_SLOT) && blk < u.b1) {
             const int phys = table[blk];
             if (phys >= 0 && phys < p.n_blocks) {
-                const uint8_t* base = sm.ring + (size_t)slot * SLOT + (j % BLKS_PER_SLOT) * BLK_BYTES;
-                const bool has_new = blk == last_blk;
-                attend_block(reinterpret_cast<const bf16*>(base), reinterpret_cast<const bf16*>(base + KT_BYTES),
-                             sq + g * D, has_new ? snew : nullptr, has_new ? snew + D : nullptr, new_r,
-                             min(KVB, u.ctx - blk * KVB), lane, m, lsum, o);
-            } else if (lane == 0 && g == 0) {
+                uint8_t* kt = sm.ring + (size_t)slot * SLOT + (j % BLKS_PER_SLOT) * BLK_BYTES;
+                uint8_t* vt = kt + KT_BYTES;
+                if (blk == last_blk) {
+                    // this step's K/V row replaces the stale one in the tile
+                    if (dq == 0) {
+                        const int kv = lane >> 4, c = lane & 15;
+                        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(tile_chunk(kv ? vt : kt, new_r, c))) =
+                            *reinterpret_cast<const uint4*>(snew + kv * D + c * 8);
+                    }
+                    named_bar(2 + j, ATT_DQ * 32);
+                }
+                attend_block_tc(kt, vt, sqa, min(KVB, u.ctx - blk * KVB), dq, lane, st);
+            } else if (lane == 0 && dq == 0) {
                 set_status(p.status, Q3_STATUS_BLOCK_RANGE);
             }
         }
@@ -692,9 +798,27 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
             mbar_arrive(&sm.empty[slot]);
         }
     }
+    // per-warp partials: rows g (head g / 2) and g + 8 (head 4 + g / 2); the
+    // two parts of a head are summed across lanes g, g ^ 1
     if (worker && u.active) {
-        if (lane == 0) { pm[warp] = m; pl[warp] = lsum; }
-        *reinterpret_cast<float4*>(po + warp * D + lane * 4) = make_float4(o[0], o[1], o[2], o[3]);
+        const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int dt = 0; dt < ATT_DT; ++dt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st.o[dt][e] += __shfl_xor_sync(0xffffffffu, st.o[dt][e], 4);
+        if ((g & 1) == 0) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int h = hr * 4 + g / 2;
+                if (h < G) {
+                    if (dq == 0 && tig == 0) { pm[j * G + h] = st.m[hr]; pl[j * G + h] = st.l[hr]; }
+#pragma unroll
+                    for (int dt = 0; dt < ATT_DT; ++dt)
+                        *reinterpret_cast<float2*>(po + (j * G + h) * D + dq * (D / ATT_DQ) + dt * 8 + 2 * tig) =
+                            make_float2(st.o[dt][2 * hr], st.o[dt][2 * hr + 1]);
+                }
+            }
+        }
     }
     consumer_sync();
 
@@ -726,13 +850,18 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
         }
     }
     if (ns == 1) return;
-    // the last split CTA of this KV head merges every split in order
-    __threadfence();
+    // the last split CTA of this KV head merges every split in order: one
+    // acquire-release ticket per CTA publishes its partials and, for the last,
+    // makes every other split's visible
     consumer_sync();
-    if (tid == 0) *sm.ticket = u.active ? atomicAdd(p.counters + u.kvh, 1) : -1;
+    if (tid == 0) {
+        int t = -1;
+        if (u.active)
+            asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(t) : "l"(p.counters + u.kvh) : "memory");
+        *sm.ticket = t;
+    }
     consumer_sync();
     if (*sm.ticket != ns - 1) return;
-    __threadfence();
     // the G heads of this KV head hold contiguous partials: [G][ns][2] and
     // [G][ns][D] from head kvh * G; fetch them all at once
     {
@@ -816,7 +945,7 @@ Q3_DEV bool epilogue_stage(const DecodeArgs& p, const WStage& s, int kind, const
         const uint32_t use = it / sm.n_slots;
         ++it;
         if (!wait_bar(&sm.redf[slot], use & 1, sm, p.status)) return false;
-        tile_epilogue(s, kind, sm.red + slot * RED, S, a, nvalid, lane, out, best, best_i);
+        tile_epilogue(s, kind, sm.red + slot * RED, S, a, nvalid, lane, out, sm.xres, best, best_i);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
@@ -827,7 +956,11 @@ Q3_DEV void epilogue(const DecodeArgs& p, const Unit& u, const Smem& sm, int lan
     const bf16* erow = p.embed + (size_t)checked_token(p) * p.H;
     {
         const WStage so = weight_stage(p, 0, ST_O);
-        for (int r = so.r0 + lane; r < so.r1; r += 32) __stcg(p.x + r, __bfloat162float(erow[r]));
+        for (int r = so.r0 + lane; r < so.r1; r += 32) {
+            const float x = __bfloat162float(erow[r]);
+            sm.xres[r - so.r0] = x;
+            __stcg(p.x + r, x);
+        }
     }
     uint32_t it = 0;
     float best = -INFINITY;
@@ -919,6 +1052,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
     sm.bi = reinterpret_cast<int*>(sm.bv + NCW);
     sm.abort = reinterpret_cast<volatile int*>(sm.bi + NCW);
     sm.ticket = const_cast<int*>(sm.abort) + 1;
+    sm.xres = reinterpret_cast<float*>(sm.ticket + 3);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.n_slots; ++s) {
@@ -946,9 +1080,10 @@ int decode_step_slot_bytes() { return SLOT; }
 
 int decode_step_barriers(int n_layers) { return 5 * n_layers; }
 
-size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, int n_splits)
+size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, int n_splits, int grid)
 {
     if (n_kv < 1 || n_q % n_kv || n_q / n_kv > NCW / BLKS_PER_SLOT) return 0;
+    if (grid < 1 || (H + grid - 1) / grid > MAX_OWN) return 0;
     if (n_slots < MIN_SLOTS || n_slots > MAX_SLOTS || n_splits < 1) return 0;
     const int qw = n_q * D;
     const int align = q8 ? 256 : 8;
