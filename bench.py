@@ -62,7 +62,46 @@ def parse():
     ap.add_argument("--sessions", type=int, default=32)
     ap.add_argument("--no-b32", action="store_true", help="skip the batch-32 decode leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup"), default=None,
+                    help="run only a small case sized for an ncu capture (a few GB on the device) and exit")
     return ap.parse_args()
+
+
+def ncu_case(name: str):
+    """Small cases for full ncu captures of the top kernels (the full-size
+    workload holds ~20 GB and runs hundreds of launches)."""
+    import torch
+
+    import qwen3_dense_decoder_gb300 as q3
+    import synthetic
+    q3.build()
+    if name == "decode-4layer":
+        # the Qwen3-4B shape cut to 4 layers: a 2,048-token prefill, then fused
+        # decode steps at context ~2,050 (about 1.6 GB streamed per step)
+        s = synthetic.SHAPES["4b"].replace(n_layers=4)
+        st = torch.cuda.Stream()
+        torch.cuda.set_stream(st)
+        w = synthetic.make_weights(s, seed=1234, device="cuda")
+        m = q3.Model(s, w, max_ctx=2400, max_round_tokens=2048, stream=st)
+        pool = m.pool(80, 2)
+        ses = pool.session()
+        lg = torch.empty(s.vocab, device="cuda")
+        tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ses.eval(torch.tensor(synthetic.make_tokens(2048, s.vocab, 7), device="cuda"), lg, tok)
+        for _ in range(6):
+            ses.eval(tok, lg, tok)
+        m.sync()
+    else:
+        # the gate/up projection of a 2,048-token prefill of the Qwen3-4B shape
+        M, N, K = 19456, 2048, 2560
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5)
+        w = (torch.randn(M, K, device="cuda", generator=g) * 0.02).to(torch.float16)
+        x = torch.randn((N + 255) // 256 * 256, K, device="cuda", generator=g).to(torch.float16)
+        for _ in range(6):
+            q3.op_matmul(w, x, N)
+        torch.cuda.synchronize()
+    print("ok", name, flush=True)
 
 
 # ---------------------------------------------------------------- algorithmic work
@@ -493,6 +532,9 @@ def reference_arm(args, rank: int):
 
 def main():
     args = parse()
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist_on = world > 1

@@ -102,16 +102,18 @@ __host__ __device__ inline int sx_floats(int H, int F, int n_q, int n_kv, int n_
 }
 
 struct Layout {
-    size_t sx, red, bars, misc, total;
+    size_t sx, red, bars, misc, ptrs, total;
 };
 
-__host__ __device__ inline Layout make_layout(int n_slots, int sxf) {
+__host__ __device__ inline Layout make_layout(int n_slots, int sxf, int n_layers) {
     Layout L;
     L.sx = (size_t)n_slots * SLOT;
     L.red = L.sx + (size_t)sxf * 4;
     L.bars = L.red + (size_t)n_slots * RED * 4;
     L.misc = L.bars + (size_t)(3 * n_slots + 1) * 8;
-    L.total = L.misc + (size_t)(3 * NCW + 4 + MAX_OWN) * 4;
+    L.ptrs = L.misc + (size_t)(3 * NCW + 4 + MAX_OWN) * 4;
+    L.ptrs = (L.ptrs + 15) & ~(size_t)15;
+    L.total = L.ptrs + (size_t)n_layers * 14 * 8;     // per layer: 7 weight planes, 7 scale planes
     return L;
 }
 
@@ -129,6 +131,7 @@ struct Smem {
     volatile int* abort;
     int* ticket;
     float* xres;        // [MAX_OWN] the CTA's residual rows (epilogue warp only)
+    const void** wp;    // [n_layers][14]: the layer's 7 weight planes, then their 7 scale planes
     int n_slots;
 };
 
@@ -212,8 +215,8 @@ Q3_DEV bool grid_sync(const DecodeArgs& p, const Smem& sm, unsigned long long ta
     if (threadIdx.x == 0 && !*sm.abort) {
         asm volatile("red.release.gpu.global.add.u64 [%0], 1;" :: "l"(p.bar) : "memory");
         const uint64_t t0 = global_ns();
-        while (ld_acquire_u64(p.bar) < target) {
-            if (global_ns() - t0 > Q3_WAIT_LIMIT_NS) {
+        for (uint32_t n = 1; ld_acquire_u64(p.bar) < target; ++n) {
+            if ((n & 63) == 0 && global_ns() - t0 > Q3_WAIT_LIMIT_NS) {
                 set_status(p.status, Q3_STATUS_TIMEOUT);
                 *sm.abort = 1;
                 break;
@@ -233,7 +236,7 @@ struct WStage {
     int K, pair, q8, nr, per, r0, r1;
 };
 
-Q3_DEV WStage weight_stage(const DecodeArgs& p, int l, int kind) {
+Q3_DEV WStage weight_stage(const DecodeArgs& p, const Smem& sm, int l, int kind) {
     WStage s{};
     const int qw = p.n_q * D, kvw = p.n_kv * D;
     int M;
@@ -243,11 +246,11 @@ Q3_DEV WStage weight_stage(const DecodeArgs& p, int l, int kind) {
         s.K = p.H;
         M = p.V;
     } else {
-        const DecodeLayer& L = p.layers[l];
+        const void* const* lp = sm.wp + (size_t)l * 14;
         s.q8 = p.q8;
         auto set = [&](int i, int proj, int rows) {
-            s.w[i] = static_cast<const uint8_t*>(L.w[proj]);
-            s.sc[i] = L.sc[proj];
+            s.w[i] = static_cast<const uint8_t*>(lp[proj]);
+            s.sc[i] = static_cast<const __half*>(lp[7 + proj]);
             s.rows[i] = rows;
         };
         switch (kind) {
@@ -381,13 +384,13 @@ Q3_DEV void producer(const DecodeArgs& p, const Unit& u, const int* table, const
     uint32_t it = 0;
     bool ok = true;
     for (int l = 0; l < p.n_layers && ok; ++l) {
-        ok = produce_weights<Q8>(weight_stage(p, l, ST_QKV), sm, it, lane, p.status, pol) &&
+        ok = produce_weights<Q8>(weight_stage(p, sm, l, ST_QKV), sm, it, lane, p.status, pol) &&
              produce_attention(p, l, u, table, sm, it, lane) &&
-             produce_weights<Q8>(weight_stage(p, l, ST_O), sm, it, lane, p.status, pol) &&
-             produce_weights<Q8>(weight_stage(p, l, ST_GU), sm, it, lane, p.status, pol) &&
-             produce_weights<Q8>(weight_stage(p, l, ST_DOWN), sm, it, lane, p.status, pol);
+             produce_weights<Q8>(weight_stage(p, sm, l, ST_O), sm, it, lane, p.status, pol) &&
+             produce_weights<Q8>(weight_stage(p, sm, l, ST_GU), sm, it, lane, p.status, pol) &&
+             produce_weights<Q8>(weight_stage(p, sm, l, ST_DOWN), sm, it, lane, p.status, pol);
     }
-    if (ok) produce_weights<false>(weight_stage(p, 0, ST_LM), sm, it, lane, p.status, pol);
+    if (ok) produce_weights<false>(weight_stage(p, sm, 0, ST_LM), sm, it, lane, p.status, pol);
     // copies still in flight must land before the CTA may exit
     if (lane == 0) {
         for (int s = 0; s < sm.n_slots; ++s)
@@ -914,22 +917,22 @@ Q3_DEV void consumer(const DecodeArgs& p, const Unit& u, const int* table, const
     for (int l = 0; l < p.n_layers; ++l) {
         const DecodeLayer& L = p.layers[l];
         stage_x(sm, p.x, l == 0 ? erow : nullptr, p.H, L.attn_norm, p.eps);
-        consume_weights<Q8>(weight_stage(p, l, ST_QKV), sm, it, warp, lane, p);
+        consume_weights<Q8>(weight_stage(p, sm, l, ST_QKV), sm, it, warp, lane, p);
         if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
         consume_attention(p, l, u, table, sm, it, warp, lane);
         if (!grid_sync(p, sm, target += gridDim.x, -1)) return;
         stage_x(sm, p.att, nullptr, qw, nullptr, p.eps);
-        consume_weights<Q8>(weight_stage(p, l, ST_O), sm, it, warp, lane, p);
+        consume_weights<Q8>(weight_stage(p, sm, l, ST_O), sm, it, warp, lane, p);
         if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
         stage_x(sm, p.x, nullptr, p.H, L.ffn_norm, p.eps);
-        consume_weights<Q8>(weight_stage(p, l, ST_GU), sm, it, warp, lane, p);
+        consume_weights<Q8>(weight_stage(p, sm, l, ST_GU), sm, it, warp, lane, p);
         if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
         stage_x(sm, p.ffn, nullptr, p.F, nullptr, p.eps);
-        consume_weights<Q8>(weight_stage(p, l, ST_DOWN), sm, it, warp, lane, p);
+        consume_weights<Q8>(weight_stage(p, sm, l, ST_DOWN), sm, it, warp, lane, p);
         if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
     }
     stage_x(sm, p.x, nullptr, p.H, p.final_norm, p.eps);
-    consume_weights<false>(weight_stage(p, 0, ST_LM), sm, it, warp, lane, p);
+    consume_weights<false>(weight_stage(p, sm, 0, ST_LM), sm, it, warp, lane, p);
 }
 
 // The epilogue warp: for every matvec tile, once the consumer warps' segment
@@ -955,7 +958,7 @@ Q3_DEV bool epilogue_stage(const DecodeArgs& p, const WStage& s, int kind, const
 Q3_DEV void epilogue(const DecodeArgs& p, const Unit& u, const Smem& sm, int lane) {
     const bf16* erow = p.embed + (size_t)checked_token(p) * p.H;
     {
-        const WStage so = weight_stage(p, 0, ST_O);
+        const WStage so = weight_stage(p, sm, 0, ST_O);
         for (int r = so.r0 + lane; r < so.r1; r += 32) {
             const float x = __bfloat162float(erow[r]);
             sm.xres[r - so.r0] = x;
@@ -971,7 +974,7 @@ Q3_DEV void epilogue(const DecodeArgs& p, const Unit& u, const Smem& sm, int lan
         if (lane == 0) mbar_arrive(sm.epi_done);
     };
     for (int l = 0; l < p.n_layers && ok; ++l) {
-        ok = epilogue_stage(p, weight_stage(p, l, ST_QKV), ST_QKV, sm, it, lane, p.qkv, best, best_i);
+        ok = epilogue_stage(p, weight_stage(p, sm, l, ST_QKV), ST_QKV, sm, it, lane, p.qkv, best, best_i);
         if (!ok) break;
         closed();
         // attention slots: nothing to finish, only the slot release
@@ -983,18 +986,18 @@ Q3_DEV void epilogue(const DecodeArgs& p, const Unit& u, const Smem& sm, int lan
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(&sm.empty[slot]);
         }
-        ok = ok && epilogue_stage(p, weight_stage(p, l, ST_O), ST_O, sm, it, lane, p.x, best, best_i);
+        ok = ok && epilogue_stage(p, weight_stage(p, sm, l, ST_O), ST_O, sm, it, lane, p.x, best, best_i);
         if (!ok) break;
         closed();
-        ok = epilogue_stage(p, weight_stage(p, l, ST_GU), ST_GU, sm, it, lane, p.ffn, best, best_i);
+        ok = epilogue_stage(p, weight_stage(p, sm, l, ST_GU), ST_GU, sm, it, lane, p.ffn, best, best_i);
         if (!ok) break;
         closed();
-        ok = epilogue_stage(p, weight_stage(p, l, ST_DOWN), ST_DOWN, sm, it, lane, p.x, best, best_i);
+        ok = epilogue_stage(p, weight_stage(p, sm, l, ST_DOWN), ST_DOWN, sm, it, lane, p.x, best, best_i);
         if (!ok) break;
         closed();
     }
     if (!ok) return;
-    if (!epilogue_stage(p, weight_stage(p, 0, ST_LM), ST_LM, sm, it, lane, p.logits, best, best_i)) return;
+    if (!epilogue_stage(p, weight_stage(p, sm, 0, ST_LM), ST_LM, sm, it, lane, p.logits, best, best_i)) return;
     if (!p.argmax_out) return;
 
     // this CTA's argmax partial, then the last CTA to finish merges them all
@@ -1037,7 +1040,7 @@ template <bool Q8>
 __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArgs p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const Layout lay = make_layout(p.n_slots, sx_floats(p.H, p.F, p.n_q, p.n_kv, p.n_splits));
+    const Layout lay = make_layout(p.n_slots, sx_floats(p.H, p.F, p.n_q, p.n_kv, p.n_splits), p.n_layers);
     Smem sm;
     sm.n_slots = p.n_slots;
     sm.ring = smem;
@@ -1053,6 +1056,13 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
     sm.abort = reinterpret_cast<volatile int*>(sm.bi + NCW);
     sm.ticket = const_cast<int*>(sm.abort) + 1;
     sm.xres = reinterpret_cast<float*>(sm.ticket + 3);
+    sm.wp = reinterpret_cast<const void**>(smem + lay.ptrs);
+    // the per-layer weight pointers, read on every stage by producer, consumers and epilogue
+    for (int i = threadIdx.x; i < p.n_layers * 14; i += blockDim.x) {
+        const DecodeLayer& L = p.layers[i / 14];
+        const int k = i % 14;
+        sm.wp[i] = k < 7 ? L.w[k] : static_cast<const void*>(L.sc[k - 7]);
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.n_slots; ++s) {
@@ -1080,7 +1090,8 @@ int decode_step_slot_bytes() { return SLOT; }
 
 int decode_step_barriers(int n_layers) { return 5 * n_layers; }
 
-size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, int n_splits, int grid)
+size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, int n_splits, int grid,
+                        int n_layers)
 {
     if (n_kv < 1 || n_q % n_kv || n_q / n_kv > NCW / BLKS_PER_SLOT) return 0;
     if (grid < 1 || (H + grid - 1) / grid > MAX_OWN) return 0;
@@ -1098,7 +1109,7 @@ size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, in
         const int S = NCW / tile_rows(K, false);
         if ((K / 8 + S - 1) / S > 32 * XCPL) return 0;
     }
-    return make_layout(n_slots, sx_floats(H, F, n_q, n_kv, n_splits)).total;
+    return make_layout(n_slots, sx_floats(H, F, n_q, n_kv, n_splits), n_layers).total;
 }
 
 cudaError_t decode_step_prepare(size_t smem)

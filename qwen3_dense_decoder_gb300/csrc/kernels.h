@@ -220,7 +220,8 @@ struct DecodeArgs {
 };
 // Shared memory of the fused step for these dimensions and ring depth; 0 if
 // the shapes are outside what the kernel handles.
-size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, int n_splits, int grid);
+size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, int n_splits, int grid,
+                        int n_layers);
 int decode_step_slot_bytes();
 // Grid barriers one launch performs (each adds grid to *bar).
 int decode_step_barriers(int n_layers);

@@ -480,7 +480,8 @@ int setup_decode_step(q3_model* m, int n_sm)
     int slots = 0;
     size_t smem = 0;
     for (int n = 8; n >= 3; --n) {
-        const size_t b = decode_step_smem(c.hidden, c.ffn, c.n_q_heads, c.n_kv_heads, q8, n, splits, grid);
+        const size_t b = decode_step_smem(c.hidden, c.ffn, c.n_q_heads, c.n_kv_heads, q8, n, splits, grid,
+                                          c.n_layers);
         if (b && b <= (size_t)optin) { slots = n; smem = b; break; }
     }
     if (!slots) return Q3_OK;
