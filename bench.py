@@ -40,6 +40,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Qwen3-4B-shape decode tok/s (% HBM roofline); prefill tok/s (% BF16 TC peak)"
+# DRAM bytes read + written by one fused decode step over its algorithmic
+# bytes, from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
+# 4-layer case; to be retaken whenever the kernel changes
+DECODE_STEP_TRAFFIC_RATIO = (1.6196e9 + 2.99e6) / 1.6189e9
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -101,6 +105,14 @@ def ncu_case(name: str):
         for _ in range(6):
             q3.op_matmul(w, x, N)
         torch.cuda.synchronize()
+        a, b = torch.cuda.Event(True), torch.cuda.Event(True)
+        a.record()
+        for _ in range(10):
+            q3.op_matmul(w, x, N)
+        b.record()
+        b.synchronize()
+        us = a.elapsed_time(b) / 10 * 1e3
+        print(f"gemm {M}x{N}x{K}: {us:.1f} us/launch, {2.0 * M * N * K / us / 1e6:.1f} TFLOP/s", flush=True)
     print("ok", name, flush=True)
 
 
@@ -439,10 +451,15 @@ def report(args, res, world, dist_on, pk, pk_kind):
         pc0, pc1 = res["decode_profile_ctx"]
         k_bytes = decode_bytes(s, (pc0 + pc1) / 2)
         k_name = "decode_step (fused one-kernel decode step: all projections, attention, lm_head)"
+        # DRAM bytes of one launch from an ncu capture of the 4-layer case
+        # (bench.py --ncu-case decode-4layer): 1.0023 x its algorithmic bytes,
+        # scaled to this launch by the same ratio
+        k_traffic = round(DECODE_STEP_TRAFFIC_RATIO * k_bytes)
     else:
         k_ms, k_n = prof["gemv"]
         k_bytes = w_bytes * K / k_n
         k_name = "gemv (decode matvec, all projections + lm_head)"
+        k_traffic = None
     k_achieved = k_bytes / (k_ms / k_n / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world,
@@ -456,7 +473,7 @@ def report(args, res, world, dist_on, pk, pk_kind):
                          "peak_kind": pk_kind},
         "roofline": {"kernel": k_name, "bound": "hbm",
                      "achieved": round(k_achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(k_achieved / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(k_achieved / pk["hbm_gbs"], 4), "traffic": k_traffic,
                      "bytes_per_launch": k_bytes, "launches": k_n,
                      "mean_launch_us": round(k_ms / k_n * 1e3, 3), "peak_kind": pk_kind},
         "clocks": res["clocks"],
