@@ -4,11 +4,12 @@
 // and to the rows before them in the round ("Kipp Roadmap", status v0.0.3:
 // flash-attention prefill kernel; status v0.0.6: long-context prefill
 // attention is the next lever; "Kipp Model Support", section
-// "qwen3-0.6b-base": K/V stored as BF16).  Flash-style tiling: a CTA of four
-// warps owns 64 query rows of one session and one query head (each warp 16
-// rows) and walks the session's paged K/V in tiles of 64 positions (two
-// 32-position blocks through the block table), keeping the online-softmax
-// row maximum and sum and the 16 x 128 output accumulator in registers.
+// "qwen3-0.6b-base": K/V stored as BF16).  Flash-style tiling: a CTA owns 64
+// query rows of one session for up to four query heads of one KV head (four
+// warps of 16 rows per head) and walks the session's paged K/V in tiles of
+// 64 positions (two 32-position blocks through the block table), keeping the
+// online-softmax row maximum and sum and the 16 x 128 output accumulator in
+// registers; the heads of the group share each staged K/V tile.
 //
 // Products run on mma.sync m16n8k16 with fp16 operands and FP32
 // accumulation: Q arrives in fp16; K/V tiles are copied as stored (BF16)
@@ -19,6 +20,8 @@
 // conflict-free.  Scores are scaled by log2(e)/sqrt(128) and exponentiated
 // in base 2; positions after a query's own position are masked.  Positions a
 // block does not hold read zeros, never stale shared memory.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,7 +32,6 @@ namespace {
 constexpr int D = 128;
 constexpr int BM = 64;                 // query rows per CTA
 constexpr int BN = 64;                 // key positions per tile
-constexpr int PWARPS = 4;
 constexpr int TILE_BYTES = BM * D * 2; // 16 KB (64 rows x 256 bytes)
 
 // byte offset of 16-byte chunk c of row r in a swizzled 64 x 128 fp16 tile
@@ -64,22 +66,48 @@ Q3_DEV uint4 bf16x8_to_f16x8(uint4 w) {
     return o;
 }
 
-__global__ void __launch_bounds__(PWARPS * 32) prefill_attn_kernel(const PrefillAttnArgs p)
+// One CTA per (64-row query tile of one session, KV head, group of HPC query
+// heads of that KV head): the heads of a group share each K/V tile, fetched
+// and converted once for all of them.  Warp w takes query head w / 4 of the
+// group and rows 16 (w % 4) .. + 16 of the tile.
+template <int HPC>
+__global__ void __launch_bounds__(HPC * 4 * 32, 1) prefill_attn_kernel(const PrefillAttnArgs p)
 {
+    constexpr int NT = HPC * 4 * 32;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* sQ = smem;                                   // fp16, swizzled
-    uint8_t* sK = smem + TILE_BYTES;
-    uint8_t* sV = smem + 2 * TILE_BYTES;
-    uint8_t* bKV = smem + 3 * TILE_BYTES;                 // [2 buffers][K, V] bf16, linear
+    uint8_t* sQ = smem;                                   // [HPC] fp16 swizzled 64 x 128 tiles
+    uint8_t* sK = smem + HPC * TILE_BYTES;
+    uint8_t* sV = sK + TILE_BYTES;
+    uint8_t* bKV = sV + TILE_BYTES;                       // [2 buffers][K, V] bf16, linear
 
-    const int tile = p.n_tiles - 1 - (int)blockIdx.x;     // longest tiles first
-    const int h = blockIdx.y;
+    __shared__ int s_item;
     const int G = p.n_q / p.n_kv;
-    const int kvh = h / G;
+    const int Z = G / HPC;                                // head groups per KV head
+    const int n_items = p.n_tiles * p.n_kv * Z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hg = warp >> 2, rg = warp & 3;
     const int g = lane >> 2, tq = lane & 3;
 
     grid_dep_wait();
+
+    // Persistent CTAs take (tile, KV head, head group) items from a queue in
+    // order: tiles come longest context first, so the longest items start
+    // first.  Each CTA's final draw lands past the end; the last of those
+    // resets the queue for the next launch.
+    for (;;) {
+    __syncthreads();
+    if (tid == 0) {
+        const int it = atomicAdd(p.work_counter, 1);
+        if (it == n_items + (int)gridDim.x - 1) *p.work_counter = 0;
+        s_item = it;
+    }
+    __syncthreads();
+    const int item = s_item;
+    if (item >= n_items) break;
+    const int tile = item / (p.n_kv * Z);
+    const int kvh = (item / Z) % p.n_kv;
+    const int head0 = kvh * G + (item % Z) * HPC;         // first query head of the group
+    const int h = head0 + hg;
 
     const int row0 = p.tile_row0[tile];
     const int nrows = p.tile_rows[tile];
@@ -90,11 +118,11 @@ __global__ void __launch_bounds__(PWARPS * 32) prefill_attn_kernel(const Prefill
     const int n_kt = (pos_last + BN) / BN;
     const int qw = p.n_q * D;
 
-    // ---- Q tile (rows past the round repeat its last row)
-    for (int i = tid; i < BM * 16; i += PWARPS * 32) {
-        const int r = i >> 4, c = i & 15;
+    // ---- Q tiles of the G heads (rows past the round repeat its last row)
+    for (int i = tid; i < HPC * BM * 16; i += NT) {
+        const int hh = i / (BM * 16), r = (i >> 4) % BM, c = i & 15;
         const int src_row = row0 + min(r, nrows - 1);
-        cp_async_16(sQ + swz(r, c), p.q + (size_t)src_row * qw + h * D + c * 8);
+        cp_async_16(sQ + hh * TILE_BYTES + swz(r, c), p.q + (size_t)src_row * qw + (head0 + hh) * D + c * 8);
     }
     cp_async_commit();
 
@@ -102,45 +130,33 @@ __global__ void __launch_bounds__(PWARPS * 32) prefill_attn_kernel(const Prefill
     auto issue_kv = [&](int kt, int buf) {
         uint8_t* dstK = bKV + (size_t)buf * 2 * TILE_BYTES;
         uint8_t* dstV = dstK + TILE_BYTES;
-        for (int half = 0; half < 2; ++half) {
-            const int b = 2 * kt + half;
+        for (int i = tid; i < BN * 16; i += NT) {
+            const int r = i >> 4, c = i & 15;
+            const int b = 2 * kt + (r >> 5);
             if (b >= nblk) continue;
             const int phys = table[b];
             if (phys < 0 || phys >= p.n_blocks) {
-                if (tid == 0) set_status(p.status, Q3_STATUS_BLOCK_RANGE);
+                if (c == 0 && (r & 31) == 0) set_status(p.status, Q3_STATUS_BLOCK_RANGE);
                 continue;
             }
             const __nv_bfloat16* Kb = p.kv_layer + ((size_t)phys * 2 * p.n_kv + kvh) * (32 * D);
             const __nv_bfloat16* Vb = Kb + (size_t)p.n_kv * (32 * D);
-            for (int i = tid; i < 32 * 16; i += PWARPS * 32) {
-                const int r = i >> 4, c = i & 15;
-                cp_async_16(dstK + (half * 32 + r) * 256 + c * 16, Kb + r * D + c * 8);
-                cp_async_16(dstV + (half * 32 + r) * 256 + c * 16, Vb + r * D + c * 8);
-            }
+            cp_async_16(dstK + r * 256 + c * 16, Kb + (r & 31) * D + c * 8);
+            cp_async_16(dstV + r * 256 + c * 16, Vb + (r & 31) * D + c * 8);
         }
         cp_async_commit();
     };
     issue_kv(0, 0);
 
-    // Q fragments of this warp's 16 rows, all 8 k-steps
-    cp_async_wait_all_but(1);
-    __syncthreads();
-    uint32_t qa[8][4];
-    {
-        const uint32_t base = smem_u32(sQ);
-        const int r = warp * 16 + (lane & 15);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            ldsm_x4(base + swz(r, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-    }
-
     float o[16][4];
 #pragma unroll
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-    const int qr0 = warp * 16 + g;                        // this thread's two query rows
+    const int qr0 = rg * 16 + g;                          // this thread's two query rows
     const int qp[2] = {pos0 + min(qr0, nrows - 1), pos0 + min(qr0 + 8, nrows - 1)};
+    const int qp_min = pos0 + min(rg * 16, nrows - 1);    // the warp's first query position
     const float scale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+    const uint32_t qbase = smem_u32(sQ + hg * TILE_BYTES);
 
     for (int kt = 0; kt < n_kt; ++kt) {
         if (kt + 1 < n_kt) {
@@ -154,7 +170,7 @@ __global__ void __launch_bounds__(PWARPS * 32) prefill_attn_kernel(const Prefill
         {
             const uint8_t* srcK = bKV + (size_t)(kt & 1) * 2 * TILE_BYTES;
             const uint8_t* srcV = srcK + TILE_BYTES;
-            for (int i = tid; i < BM * 16; i += PWARPS * 32) {
+            for (int i = tid; i < BN * 16; i += NT) {
                 const int r = i >> 4, c = i & 15;
                 const bool present = 2 * kt + (r >> 5) < nblk;
                 uint4 k = make_uint4(0, 0, 0, 0), v = make_uint4(0, 0, 0, 0);
@@ -174,18 +190,21 @@ __global__ void __launch_bounds__(PWARPS * 32) prefill_attn_kernel(const Prefill
         for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
         const uint32_t kbase = smem_u32(sK);
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
-            const int r = 16 * np + (lane & 7) + ((lane >> 4) & 1) * 8;
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(qbase + swz(rg * 16 + (lane & 15), 2 * kk + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int np = 0; np < 4; ++np) {
+                const int r = 16 * np + (lane & 7) + ((lane >> 4) & 1) * 8;
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(kbase + swz(r, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
-                mma16816(s[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                mma16816(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                mma16816(s[2 * np], a0, a1, a2, a3, b0, b1);
+                mma16816(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
             }
         }
 
-        // ---- causal mask and online softmax (rows g and g + 8 of the warp)
+        // ---- causal mask (only tiles reaching past the warp's first row) and online softmax
+        const bool masked = kt * BN + BN - 1 > qp_min;
         float mx[2] = {m_r[0], m_r[1]};
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
@@ -193,7 +212,7 @@ __global__ void __launch_bounds__(PWARPS * 32) prefill_attn_kernel(const Prefill
             for (int e = 0; e < 4; ++e) {
                 const int kp = kt * BN + n * 8 + 2 * tq + (e & 1);
                 const int ri = e >> 1;
-                const float v = kp <= qp[ri] ? s[n][e] * scale : -INFINITY;
+                const float v = (!masked || kp <= qp[ri]) ? s[n][e] * scale : -INFINITY;
                 s[n][e] = v;
                 mx[ri] = fmaxf(mx[ri], v);
             }
@@ -245,6 +264,7 @@ __global__ void __launch_bounds__(PWARPS * 32) prefill_attn_kernel(const Prefill
                 mma16816(o[2 * dp + 1], a0, a1, a2, a3, b2, b3);
             }
         }
+        __syncthreads();       // sK / sV are rewritten by the next tile's conversion
     }
 
     // ---- normalise and store fp16
@@ -264,24 +284,35 @@ __global__ void __launch_bounds__(PWARPS * 32) prefill_attn_kernel(const Prefill
         }
     }
     if (bad) set_status(p.status, Q3_STATUS_F16_RANGE);
+    }   // items
     grid_dep_launch();
 }
 
-}  // namespace
-
-cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a)
+template <int HPC>
+cudaError_t launch_prefill_g(const Launch& L, const PrefillAttnArgs& a)
 {
-    const size_t smem = 3 * TILE_BYTES + 2 * 2 * TILE_BYTES;   // Q, K, V fp16 + 2 staged K/V bf16
+    const size_t smem = (size_t)(HPC + 2) * TILE_BYTES + 2 * 2 * TILE_BYTES;   // Q x HPC, K, V fp16 + staged K/V
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel,
+        cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<HPC>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
+    static int per_sm = 0, n_sm = 0;
+    if (!per_sm) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_attn_kernel<HPC>, HPC * 4 * 32, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    }
+    const int items = a.n_tiles * a.n_q / HPC;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.n_tiles, a.n_q);
-    cfg.blockDim = dim3(PWARPS * 32);
+    cfg.gridDim = dim3(std::min(items, per_sm * n_sm));
+    cfg.blockDim = dim3(HPC * 4 * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
@@ -290,7 +321,21 @@ cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (L.counter) ++*L.counter;
-    return cudaLaunchKernelEx(&cfg, prefill_attn_kernel, a);
+    return cudaLaunchKernelEx(&cfg, prefill_attn_kernel<HPC>, a);
+}
+
+}  // namespace
+
+// Heads per CTA: the largest of 4, 3, 2, 1 dividing the group size (16
+// warps at most, for the registers the accumulators need).
+cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a)
+{
+    const int G = a.n_q / a.n_kv;
+    if (G < 1 || a.n_q % a.n_kv) return cudaErrorInvalidValue;
+    if (G % 4 == 0) return launch_prefill_g<4>(L, a);
+    if (G % 3 == 0) return launch_prefill_g<3>(L, a);
+    if (G % 2 == 0) return launch_prefill_g<2>(L, a);
+    return launch_prefill_g<1>(L, a);
 }
 
 }  // namespace q3

@@ -149,9 +149,10 @@ struct PrefillAttnArgs {
     int T, n_q, n_kv;
     const int* row_pos;
     const int* row_slot;
-    const int* tile_row0;      // [n_tiles] first row of each 64-row query tile
+    const int* tile_row0;      // [n_tiles] first row of each 64-row query tile, longest context first
     const int* tile_rows;      // [n_tiles] rows in the tile (<= 64)
     int n_tiles;
+    int* work_counter;         // work queue position, zero between launches (the kernel resets it)
     const int* tables;
     int max_blocks;
     const __nv_bfloat16* kv_layer;

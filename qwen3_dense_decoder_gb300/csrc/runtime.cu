@@ -139,6 +139,7 @@ struct q3_model {
     float* am_val = nullptr;        // lm_head argmax partials, one per GEMV CTA
     int* am_idx = nullptr;
     int* am_counter = nullptr;      // ticket of the argmax merge, zero between rounds
+    int* pre_counter = nullptr;     // work queue of the prefill attention, zero between launches
 
     // fused one-kernel decode step (one-session decode rounds)
     bool step_ok = false;           // shapes and device support it
@@ -672,6 +673,7 @@ int run_round(q3_model* m, const Round& r)
             pa.tables = r.pool->tables; pa.max_blocks = r.pool->max_blocks;
             pa.kv_layer = r.pool->kv + (size_t)l * layer_kv; pa.n_blocks = r.pool->n_blocks;
             pa.out = m->att;
+            pa.work_counter = m->pre_counter;
             pa.status = m->status;
             if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_prefill_attention(L, pa); }),
                                "prefill attention")))
@@ -848,14 +850,24 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
         }
         h[2 * m->max_rows + i] = t - 1;
     }
-    // 64-row query tiles of the prefill attention, never spanning two sessions
-    int n_tiles = 0;
-    for (int i = 0, row = 0; i < ns; row += n[i], ++i)
-        for (int k = 0; k < n[i]; k += 64, ++n_tiles) {
-            h[3 * m->max_rows + n_tiles] = row + k;
-            h[4 * m->max_rows + n_tiles] = std::min(64, n[i] - k);
+    // 64-row query tiles of the prefill attention, never spanning two
+    // sessions, longest context first (the kernel takes them in this order)
+    {
+        struct Tile { int row0, rows, last_pos; };
+        std::vector<Tile> tiles;
+        for (int i = 0, row = 0; i < ns; row += n[i], ++i)
+            for (int k = 0; k < n[i]; k += 64) {
+                const int rows = std::min(64, n[i] - k);
+                tiles.push_back({row + k, rows, S[i]->pos + k + rows - 1});
+            }
+        std::stable_sort(tiles.begin(), tiles.end(),
+                         [](const Tile& a, const Tile& b) { return a.last_pos > b.last_pos; });
+        for (size_t t = 0; t < tiles.size(); ++t) {
+            h[3 * m->max_rows + t] = tiles[t].row0;
+            h[4 * m->max_rows + t] = tiles[t].rows;
         }
-    r.n_tiles = n_tiles;
+        r.n_tiles = (int)tiles.size();
+    }
     r.last_row = r.T - 1;
     r.decode = (r.T == ns);
     if ((rc = m->check(m->stage_copy(slot, m->meta, sizeof(int32_t) * 5 * m->max_rows), "meta upload")))
@@ -1002,10 +1014,12 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->am_val = static_cast<float*>(A(sizeof(float) * gemv_max_grid()));
     m->am_idx = static_cast<int*>(A(sizeof(int) * gemv_max_grid()));
     m->am_counter = static_cast<int*>(A(sizeof(int)));
+    m->pre_counter = static_cast<int*>(A(sizeof(int)));
     if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
     if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess ||
         cudaMemset(m->attn_counters, 0, sizeof(int) * (size_t)m->max_rows * c.n_kv_heads) != cudaSuccess ||
         cudaMemset(m->am_counter, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(m->pre_counter, 0, sizeof(int)) != cudaSuccess ||
         cudaMemset(m->conv_counts, 0, 2 * sizeof(unsigned long long)) != cudaSuccess)
         return bad(Q3_ERR_CUDA, "cudaMemset failed");
 
