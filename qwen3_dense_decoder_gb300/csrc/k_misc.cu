@@ -81,18 +81,35 @@ struct NormArgs {
     int* status;
 };
 
-__global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const NormArgs a)
+// The row stays in registers between the two passes (rows up to NORM_MAX
+// floats; wider rows re-read it); gains and outputs move 4 values at a time.
+constexpr int NORM_THREADS = 256;
+constexpr int NORM_VEC = 8;                          // float4 per thread held in registers
+constexpr int NORM_MAX = NORM_THREADS * 4 * NORM_VEC;
+
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_f16_kernel(const NormArgs a)
 {
-    __shared__ float red[8];
+    __shared__ float red[NORM_THREADS / 32];
     __shared__ float s_scale;
     grid_dep_wait();
     const int r = blockIdx.x;
     const int src = a.rows ? a.rows[r] : r;
     const float* x = a.x + (size_t)src * a.H;
+    const bool held = a.H <= NORM_MAX;
+    float4 v[NORM_VEC];
     float ss = 0.f;
-    for (int i = threadIdx.x * 4; i < a.H; i += blockDim.x * 4) {
-        const float4 v = *reinterpret_cast<const float4*>(x + i);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    if (held) {
+#pragma unroll
+        for (int k = 0; k < NORM_VEC; ++k) {
+            const int i = (threadIdx.x + k * NORM_THREADS) * 4;
+            v[k] = i < a.H ? *reinterpret_cast<const float4*>(x + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+        }
+    } else {
+        for (int i = threadIdx.x * 4; i < a.H; i += NORM_THREADS * 4) {
+            const float4 w = *reinterpret_cast<const float4*>(x + i);
+            ss += w.x * w.x + w.y * w.y + w.z * w.z + w.w * w.w;
+        }
     }
     grid_dep_launch();
     ss = warp_sum(ss);
@@ -100,20 +117,34 @@ __global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const NormArgs a)
     __syncthreads();
     if (threadIdx.x == 0) {
         float t = 0.f;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+        for (int w = 0; w < NORM_THREADS / 32; ++w) t += red[w];
         s_scale = 1.0f / sqrtf(t / (float)a.H + a.eps);
     }
     __syncthreads();
     const float sc = s_scale;
     __half* h = a.h + (size_t)r * a.H;
     bool bad = false;
-    for (int i = threadIdx.x * 2; i < a.H; i += blockDim.x * 2) {
-        const float2 v = *reinterpret_cast<const float2*>(x + i);
-        const float g0 = __bfloat162float(a.g[i]), g1 = __bfloat162float(a.g[i + 1]);
-        __half2 o;
-        o.x = to_f16(v.x * sc * g0, bad);
-        o.y = to_f16(v.y * sc * g1, bad);
-        *reinterpret_cast<__half2*>(h + i) = o;
+    auto put = [&](int i, float4 w) {
+        const uint2 gg = *reinterpret_cast<const uint2*>(a.g + i);
+        __half2 lo, hi;
+        lo.x = to_f16(w.x * sc * bf16lo(gg.x), bad);
+        lo.y = to_f16(w.y * sc * bf16hi(gg.x), bad);
+        hi.x = to_f16(w.z * sc * bf16lo(gg.y), bad);
+        hi.y = to_f16(w.w * sc * bf16hi(gg.y), bad);
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(h + i) = o;
+    };
+    if (held) {
+#pragma unroll
+        for (int k = 0; k < NORM_VEC; ++k) {
+            const int i = (threadIdx.x + k * NORM_THREADS) * 4;
+            if (i < a.H) put(i, v[k]);
+        }
+    } else {
+        for (int i = threadIdx.x * 4; i < a.H; i += NORM_THREADS * 4)
+            put(i, *reinterpret_cast<const float4*>(x + i));
     }
     if (bad) set_status(a.status, Q3_STATUS_F16_RANGE);
 }
@@ -136,12 +167,17 @@ __global__ void __launch_bounds__(128) qk_norm_rope_append_kernel(const RopeArgs
 
     const bool is_q = hh < a.n_q, is_k = !is_q && hh < a.n_q + a.n_kv;
     if (is_q || is_k) {
+        // gain (4 bf16) and the (cos, sin) pairs of the lane's 4 frequencies, as vector loads
+        const uint2 gg = *reinterpret_cast<const uint2*>((is_q ? a.q_gain : a.k_gain) + lane * 4);
+        const float4* csv = reinterpret_cast<const float4*>(a.rope + (size_t)pos * (D / 2) + (lane & 15) * 4);
+        const float4 c01 = csv[0], c23 = csv[1];
+        const float2 cs[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
+                              make_float2(c23.z, c23.w)};
+        const float gf[4] = {bf16lo(gg.x), bf16hi(gg.x), bf16lo(gg.y), bf16hi(gg.y)};
         const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
         const float r = 1.0f / sqrtf(ss / (float)D + a.eps);
-        const __nv_bfloat16* g = (is_q ? a.q_gain : a.k_gain) + lane * 4;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[e] = y[e] * r * __bfloat162float(g[e]);
-        const float2* cs = a.rope + (size_t)pos * (D / 2) + (lane & 15) * 4;
+        for (int e = 0; e < 4; ++e) y[e] = y[e] * r * gf[e];
         float out[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
