@@ -401,31 +401,54 @@ Q3_DEV void producer(const DecodeArgs& p, const Unit& u, const int* table, const
 // ---------------------------------------------------------------- consumers
 // Stage the activation row (f32, or the bf16 embedding row) into shared
 // memory, RMS-normalised with `gain` when given.
+// Rows with a gain (the hidden width, at most 4 NCT GAIN_IT) fetch the gain in
+// the same pass as the row, held in registers until the scale is known.
+constexpr int GAIN_IT = 3;
+
 Q3_DEV void stage_x(const Smem& sm, const float* src, const bf16* src16, int K, const bf16* gain,
                     float eps) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float ss = 0.f;
-    for (int i = tid * 4; i < K; i += NCT * 4) {
-        float4 v;
-        if (src16) {
-            const uint2 w = *reinterpret_cast<const uint2*>(src16 + i);
-            v = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
-        } else {
-            v = __ldcg(reinterpret_cast<const float4*>(src + i));
-        }
-        *reinterpret_cast<float4*>(sm.sx + i) = v;
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
     if (gain) {
+        uint2 gr[GAIN_IT];
+#pragma unroll
+        for (int k = 0; k < GAIN_IT; ++k) {
+            const int i = (tid + k * NCT) * 4;
+            if (i < K) {
+                float4 v;
+                if (src16) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(src16 + i);
+                    v = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+                } else {
+                    v = __ldcg(reinterpret_cast<const float4*>(src + i));
+                }
+                gr[k] = *reinterpret_cast<const uint2*>(gain + i);
+                *reinterpret_cast<float4*>(sm.sx + i) = v;
+                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            }
+        }
         ss = warp_sum(ss);
         if (lane == 0) sm.ss[warp] = ss;
         consumer_sync();
         float t = 0.f;
         for (int w = 0; w < NCW; ++w) t += sm.ss[w];
         const float scl = 1.0f / sqrtf(t / (float)K + eps);
-        for (int i = tid * 4; i < K; i += NCT * 4) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sm.sx[i + e] = sm.sx[i + e] * scl * __bfloat162float(gain[i + e]);
+        for (int k = 0; k < GAIN_IT; ++k) {
+            const int i = (tid + k * NCT) * 4;
+            if (i < K) {
+                float4 v = *reinterpret_cast<const float4*>(sm.sx + i);
+                v.x = v.x * scl * bf16lo(gr[k].x);
+                v.y = v.y * scl * bf16hi(gr[k].x);
+                v.z = v.z * scl * bf16lo(gr[k].y);
+                v.w = v.w * scl * bf16hi(gr[k].y);
+                *reinterpret_cast<float4*>(sm.sx + i) = v;
+            }
+        }
+    } else {
+        for (int i = tid * 4; i < K; i += NCT * 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + i));
+            *reinterpret_cast<float4*>(sm.sx + i) = v;
         }
     }
     consumer_sync();
@@ -1099,6 +1122,7 @@ size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, in
     const int qw = n_q * D;
     const int align = q8 ? 256 : 8;
     if (H % align || qw % align || F % align || H % 8) return 0;
+    if (H > 4 * NCT * GAIN_IT) return 0;                         // the normalised row's gain in registers
     // one row of every matvec (and a gate/up pair of rows) must fit a slot
     if (tile_rows(H, q8) < 2 || row_bytes(H, false) > SLOT || row_bytes(qw, q8) > SLOT ||
         row_bytes(F, q8) > SLOT)
