@@ -215,6 +215,26 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
 int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, int M, int K,
                  float* y_dev, void* stream);
 
+/* q3_op_prefill_attention: the causal GQA attention of one session's
+ * prefill round over its paged K/V ("Kipp Roadmap", status v0.0.3:
+ * flash-attention prefill kernel; "Kipp Model Support", section
+ * "qwen3-0.6b-base": BF16 K/V in 32-position blocks).  Row t (position
+ * pos0 + t) of head h: out[t][h] = sum_j softmax_j(q[t][h] . K[j][h / G] /
+ * sqrt(128)) V[j][h / G] over positions j <= pos0 + t, G = n_q / n_kv.
+ * q_dev: fp16 [T][n_q][128] (normed, rotated); kv_dev: bf16
+ * [n_blocks][2][n_kv][32][128] (K then V of each block, the layout of one
+ * layer of a pool); table_dev: int32 [n_table] physical block of each 32
+ * positions, n_table >= ceil((pos0 + T) / 32); out_dev: fp16 [T][n_q * 128].
+ * use_tc selects the tcgen05 kernel (1) or the mma.sync kernel (0).
+ * Pointers 16-byte aligned.  Synchronous: returns once the kernel has
+ * finished on stream (it allocates and frees a small metadata buffer).
+ * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_OOM, Q3_ERR_CUDA, Q3_ERR_DEVICE_CHECK (a
+ * table entry outside [0, n_blocks) or a bounded wait that ran out; the
+ * message gives the status bits). */
+int q3_op_prefill_attention(const void* q_dev, const void* kv_dev, const int32_t* table_dev, int n_table,
+                            int n_blocks, int pos0, int T, int n_q, int n_kv, void* out_dev, int use_tc,
+                            void* stream);
+
 /* Split-K matmul that allocates nothing (the Kipp pages have no counterpart;
  * this entry point serves callers that cannot call cudaMalloc where they need
  * the product: a host framework that owns all device memory through its own
@@ -252,6 +272,19 @@ const char* q3_noalloc_last_error(void);
  * the fused step is in use, 0 otherwise. */
 int q3_model_set_fused_decode(q3_model* m, int on);
 int q3_model_fused_decode(const q3_model* m);
+
+/* Prefill attention on the tcgen05 tensor cores.  Rounds with more than one
+ * row per session (prefill, chunked prefill, mixed rounds) run their causal
+ * GQA attention ("Kipp Roadmap", status v0.0.3: flash-attention prefill
+ * kernel) with scores and outputs accumulated in tensor memory; the result
+ * equals the mma.sync kernel's up to summation order.  On by default where
+ * the shapes allow it (query heads a multiple of KV heads, at most 128 query
+ * heads per KV head).  q3_model_set_prefill_tc(m, 0) selects the mma.sync
+ * kernel (for comparison); on = 1 where unsupported returns
+ * Q3_ERR_INVALID_ARG.  q3_model_prefill_tc returns 1 when the tcgen05
+ * kernel is in use, 0 otherwise. */
+int q3_model_set_prefill_tc(q3_model* m, int on);
+int q3_model_prefill_tc(const q3_model* m);
 
 /* Message of the last error on this host thread ("" if none). */
 const char* q3_last_error(void);

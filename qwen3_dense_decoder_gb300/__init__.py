@@ -88,8 +88,11 @@ def lib():
         L.q3_model_profile_reset.argtypes = [vp]
         L.q3_model_profile_read.argtypes = [vp, i, C.POINTER(C.c_double), C.POINTER(C.c_int64)]
         L.q3_op_matvec.argtypes = [vp, vp, vp, i, i, vp, vp]
+        L.q3_op_prefill_attention.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp, i, vp]
         L.q3_model_set_fused_decode.argtypes = [vp, i]
         L.q3_model_fused_decode.argtypes = [vp]
+        L.q3_model_set_prefill_tc.argtypes = [vp, i]
+        L.q3_model_prefill_tc.argtypes = [vp]
         _lib = L
     return _lib
 
@@ -161,6 +164,22 @@ def op_matvec(w: torch.Tensor, x: torch.Tensor, scales: torch.Tensor | None = No
     return y
 
 
+def op_prefill_attention(q: torch.Tensor, kv: torch.Tensor, table: torch.Tensor, pos0: int,
+                         n_kv: int, use_tc: bool = True, stream=None) -> torch.Tensor:
+    """Causal GQA attention of one session's prefill round over its paged K/V
+    (operator gate of the prefill attention).  q: fp16 [T, n_q, 128]; kv:
+    bf16 [n_blocks, 2, n_kv, 32, 128]; table: int32 physical block of each 32
+    positions.  Returns fp16 [T, n_q * 128].  Synchronous."""
+    T, n_q, d = q.shape
+    assert d == 128 and q.dtype == torch.float16 and kv.dtype == torch.bfloat16
+    assert table.dtype == torch.int32
+    out = torch.empty(T, n_q * 128, dtype=torch.float16, device=q.device)
+    _check(lib().q3_op_prefill_attention(_ptr(q), _ptr(kv), _ptr(table), table.numel(), kv.shape[0],
+                                         pos0, T, n_q, n_kv, _ptr(out), 1 if use_tc else 0,
+                                         _stream_handle(stream)))
+    return out
+
+
 class Model:
     """A decoder over device weights (synthetic.make_weights() layout).
 
@@ -227,6 +246,15 @@ class Model:
     def set_fused_decode(self, on: bool) -> None:
         """Select the fused decode step (default where supported) or the per-operation path."""
         _check(lib().q3_model_set_fused_decode(self.h, 1 if on else 0))
+
+    @property
+    def prefill_tc(self) -> bool:
+        """True when prefill attention runs on the tcgen05 kernel."""
+        return bool(lib().q3_model_prefill_tc(self.h))
+
+    def set_prefill_tc(self, on: bool) -> None:
+        """Choose the tcgen05 (True) or mma.sync (False) prefill attention."""
+        _check(lib().q3_model_set_prefill_tc(self.h, 1 if on else 0))
 
     def profile(self, on: bool) -> None:
         """Per-launch CUDA-event timing by kernel class (serialises launches)."""

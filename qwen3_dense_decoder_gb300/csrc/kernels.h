@@ -153,6 +153,10 @@ struct PrefillAttnArgs {
     const int* tile_rows;      // [n_tiles] rows in the tile (<= 64)
     int n_tiles;
     int* work_counter;         // work queue position, zero between launches (the kernel resets it)
+    const int* sched_start;    // tcgen05 kernel: [grid + 1] first item of each CTA
+    const int* sched_items;    // tcgen05 kernel: items (tile * n_kv + KV head), per CTA in order
+    int kv_row0;               // tcgen05 kernel: row of this layer's first K row in the pool's
+                               // tensor map (rows of 128 bf16: [layer][block][K/V][n_kv][32])
     const int* tables;
     int max_blocks;
     const __nv_bfloat16* kv_layer;
@@ -161,6 +165,11 @@ struct PrefillAttnArgs {
     int* status;
 };
 cudaError_t launch_prefill_attention(const Launch& L, const PrefillAttnArgs& a);
+// tcgen05 variant: query tiles of prefill_tc_rows() positions carry all query
+// heads of a KV head; CTA c takes items sched_start[c] .. sched_start[c + 1].
+int prefill_tc_rows(int n_q, int n_kv);
+size_t prefill_tc_smem();
+cudaError_t launch_prefill_attention_tc(const Launch& L, const CUtensorMap& tkv, const PrefillAttnArgs& a, int grid);
 
 // fused: every row is the single new token of its session; q/k norm, RoPE
 // and the K/V append of that token happen inside the attention kernel.

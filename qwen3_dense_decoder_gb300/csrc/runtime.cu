@@ -21,6 +21,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <queue>
 #include <set>
 #include <string>
 #include <tuple>
@@ -75,6 +76,21 @@ bool tmap_f16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
               elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A K/V pool (or one layer of it) as rows of 128 bf16, read in boxes of 32
+// positions x 64 dimensions with the 128-byte swizzle (prefill attention).
+bool tmap_kv(CUtensorMap* m, const void* ptr, uint64_t rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t elem[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, elem,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
@@ -133,13 +149,17 @@ struct q3_model {
     f16* deq = nullptr;       // Q8_0 prefill: dequantised projection(s)
     std::vector<std::vector<f16*>> w16;   // [layer][proj] fp16 copies (BF16 scheme)
     f16* lm16 = nullptr;      // fp16 copy of the lm_head for batched rows
-    int* meta = nullptr;      // [5][max_rows]: row_pos, row_slot, last_row, tile_row0, tile_rows
+    int* meta = nullptr;      // [5][max_rows]: row_pos, row_slot, last_row, tile_row0, tile_rows,
+                              // then the tcgen05 attention schedule: [SCHED_GRID + 1] starts, items
     f16* q16 = nullptr;       // [rows_alloc][qw] fp16 q of prefill rounds
     int* attn_counters = nullptr;   // [max_rows][n_kv] split tickets, zero between rounds
     float* am_val = nullptr;        // lm_head argmax partials, one per GEMV CTA
     int* am_idx = nullptr;
     int* am_counter = nullptr;      // ticket of the argmax merge, zero between rounds
     int* pre_counter = nullptr;     // work queue of the prefill attention, zero between launches
+    int n_sm = 0;
+    bool prefill_tc_ok = false;     // the tcgen05 prefill attention supports these shapes
+    bool prefill_tc = true;         // use it when prefill_tc_ok
 
     // fused one-kernel decode step (one-session decode rounds)
     bool step_ok = false;           // shapes and device support it
@@ -256,11 +276,24 @@ struct q3_pool {
     q3_model* m = nullptr;
     int n_blocks = 0, max_sessions = 0, max_blocks = 0;
     bf16* kv = nullptr;          // [L][n_blocks][2][n_kv][32][128]
+    CUtensorMap kv_map;          // kv as rows of 128 (tcgen05 prefill attention)
     int* tables = nullptr;       // [max_sessions][max_blocks]
     std::set<int> free_blocks;
     std::vector<char> slot_used;
     int refs = 1;                // the caller's handle + one per live session
 };
+
+namespace {
+// most CTAs of the tcgen05 prefill attention (one per SM); sizes its schedule area
+constexpr int SCHED_GRID = 1024;
+
+// ints of the per-round metadata: rows, tiles and the attention schedule
+// (tiles <= max_rows, so items <= max_rows * n_kv)
+size_t meta_capacity(const q3_model* m)
+{
+    return 5 * (size_t)m->max_rows + SCHED_GRID + 1 + (size_t)m->max_rows * m->c.n_kv_heads;
+}
+}  // namespace
 
 struct q3_session {
     q3_pool* pool = nullptr;
@@ -305,7 +338,9 @@ struct Round {
     int last_row = 0;                // host copy when ns == 1
     int max_ctx = 0;                 // largest context of the round
     bool decode = false;             // every session appends exactly one token
-    int n_tiles = 0;                 // 64-row query tiles (prefill attention)
+    int n_tiles = 0;                 // query tiles (prefill attention)
+    bool attn_tc = false;            // the tiles and schedule are the tcgen05 kernel's
+    int attn_grid = 0;               // its CTAs
 };
 
 int attention_splits(const q3_model* m, int T, int max_ctx)
@@ -674,9 +709,14 @@ int run_round(q3_model* m, const Round& r)
             pa.kv_layer = r.pool->kv + (size_t)l * layer_kv; pa.n_blocks = r.pool->n_blocks;
             pa.out = m->att;
             pa.work_counter = m->pre_counter;
+            pa.sched_start = m->meta + 5 * m->max_rows;
+            pa.sched_items = pa.sched_start + SCHED_GRID + 1;
+            pa.kv_row0 = (int)((size_t)l * layer_kv / 128);
             pa.status = m->status;
-            if ((rc = m->check(run(Q3_K_ATTN, [&] { return launch_prefill_attention(L, pa); }),
-                               "prefill attention")))
+            if ((rc = m->check(run(Q3_K_ATTN, [&] {
+                     return r.attn_tc ? launch_prefill_attention_tc(L, r.pool->kv_map, pa, r.attn_grid)
+                                      : launch_prefill_attention(L, pa);
+                 }), "prefill attention")))
                 return rc;
         }
 
@@ -850,14 +890,20 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
         }
         h[2 * m->max_rows + i] = t - 1;
     }
-    // 64-row query tiles of the prefill attention, never spanning two
-    // sessions, longest context first (the kernel takes them in this order)
+    // Query tiles of the prefill attention, never spanning two sessions,
+    // longest context first: 64 rows for the mma.sync kernel, 128 / G for the
+    // tcgen05 kernel, which also takes a per-CTA item list built here by
+    // longest-processing-time-first assignment (an item is one tile for one
+    // KV head; its cost is the number of 128-position K/V tiles it walks).
+    size_t meta_ints = 5 * (size_t)m->max_rows;
+    r.attn_tc = m->prefill_tc && m->prefill_tc_ok;
     {
+        const int R = r.attn_tc ? prefill_tc_rows(m->c.n_q_heads, m->c.n_kv_heads) : 64;
         struct Tile { int row0, rows, last_pos; };
         std::vector<Tile> tiles;
         for (int i = 0, row = 0; i < ns; row += n[i], ++i)
-            for (int k = 0; k < n[i]; k += 64) {
-                const int rows = std::min(64, n[i] - k);
+            for (int k = 0; k < n[i]; k += R) {
+                const int rows = std::min(R, n[i] - k);
                 tiles.push_back({row + k, rows, S[i]->pos + k + rows - 1});
             }
         std::stable_sort(tiles.begin(), tiles.end(),
@@ -867,10 +913,40 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
             h[4 * m->max_rows + t] = tiles[t].rows;
         }
         r.n_tiles = (int)tiles.size();
+        if (r.attn_tc) {
+            const int n_kv = m->c.n_kv_heads;
+            const int n_items = r.n_tiles * n_kv;
+            const int grid = std::max(1, std::min({m->n_sm, n_items, SCHED_GRID}));
+            // items come longest first (tiles are sorted); each goes to the
+            // least-loaded CTA (ties: lowest index)
+            std::vector<std::vector<int>> lists(grid);
+            std::priority_queue<std::pair<long long, int>, std::vector<std::pair<long long, int>>,
+                                std::greater<std::pair<long long, int>>> load;
+            for (int c = 0; c < grid; ++c) load.push({0, c});
+            for (int t = 0; t < r.n_tiles; ++t) {
+                const long long cost = tiles[t].last_pos / 128 + 2;
+                for (int kvh = 0; kvh < n_kv; ++kvh) {
+                    auto top = load.top();
+                    load.pop();
+                    lists[top.second].push_back(t * n_kv + kvh);
+                    load.push({top.first + cost, top.second});
+                }
+            }
+            int* start = h + 5 * m->max_rows;
+            int* items = start + SCHED_GRID + 1;
+            int at = 0;
+            for (int c = 0; c < grid; ++c) {
+                start[c] = at;
+                for (int v : lists[c]) items[at++] = v;
+            }
+            start[grid] = at;
+            r.attn_grid = grid;
+            meta_ints += SCHED_GRID + 1 + (size_t)at;
+        }
     }
     r.last_row = r.T - 1;
     r.decode = (r.T == ns);
-    if ((rc = m->check(m->stage_copy(slot, m->meta, sizeof(int32_t) * 5 * m->max_rows), "meta upload")))
+    if ((rc = m->check(m->stage_copy(slot, m->meta, sizeof(int32_t) * meta_ints), "meta upload")))
         return rc;
     if ((rc = run_round(m, r))) {
         m->poisoned = true;
@@ -933,6 +1009,16 @@ int q3_model_set_fused_decode(q3_model* m, int on)
 
 int q3_model_fused_decode(const q3_model* m) { return m && m->step_ok && m->fused_decode ? 1 : 0; }
 
+int q3_model_set_prefill_tc(q3_model* m, int on)
+{
+    if (!m) return fail(Q3_ERR_INVALID_ARG, "model is NULL");
+    if (on && !m->prefill_tc_ok) return fail(Q3_ERR_INVALID_ARG, "tcgen05 prefill attention unsupported here");
+    m->prefill_tc = on != 0;
+    return Q3_OK;
+}
+
+int q3_model_prefill_tc(const q3_model* m) { return m && m->prefill_tc_ok && m->prefill_tc ? 1 : 0; }
+
 int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tokens, void* stream,
                     q3_model** out)
 {
@@ -967,6 +1053,9 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->lm_head = cfg->tied ? m->embed : static_cast<const bf16*>(w->lm_head);
     m->layers.assign(w->layers, w->layers + c.n_layers);
     m->pdl = true;
+    m->n_sm = std::min(prop.multiProcessorCount, SCHED_GRID);
+    m->prefill_tc_ok = prefill_tc_rows(c.n_q_heads, c.n_kv_heads) > 0 &&
+                       prefill_tc_smem() <= (size_t)prop.sharedMemPerBlockOptin;
 
     auto bad = [&](int code, const char* msg) {
         free_model(m);
@@ -1008,7 +1097,7 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->part_o = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 128));
     m->ws_elems = (size_t)32 << 20;
     m->ws = static_cast<float*>(A(sizeof(float) * m->ws_elems));
-    m->meta = static_cast<int*>(A(sizeof(int) * 5 * (size_t)m->max_rows));
+    m->meta = static_cast<int*>(A(sizeof(int) * meta_capacity(m)));
     m->q16 = static_cast<f16*>(A(sizeof(f16) * R * m->qw));
     m->attn_counters = static_cast<int*>(A(sizeof(int) * (size_t)m->max_rows * c.n_kv_heads));
     m->am_val = static_cast<float*>(A(sizeof(float) * gemv_max_grid()));
@@ -1039,7 +1128,7 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     }
 
     // pinned staging ring
-    m->stage_slot = round_up(std::max<size_t>(sizeof(int) * 5 * (size_t)m->max_rows,
+    m->stage_slot = round_up(std::max<size_t>(sizeof(int) * meta_capacity(m),
                                               sizeof(int) * ((size_t)c.max_ctx / 32 + 1)), 256);
     m->stage_n = 64;
     if (cudaMallocHost(&m->stage, m->stage_slot * m->stage_n) != cudaSuccess)
@@ -1145,6 +1234,11 @@ int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
     if (cudaMalloc(&p->kv, kv * sizeof(bf16)) != cudaSuccess) {
         delete p;
         return fail(Q3_ERR_OOM, "pool: cannot allocate %zu bytes of KV", kv * sizeof(bf16));
+    }
+    if (!tmap_kv(&p->kv_map, p->kv, kv / 128)) {
+        cudaFree(p->kv);
+        delete p;
+        return fail(Q3_ERR_CUDA, "pool: tensor map encoding failed");
     }
     // zeroed once so positions a block has not been written hold finite values
     if (cudaMemsetAsync(p->kv, 0, kv * sizeof(bf16), m->stream) != cudaSuccess) {
@@ -1374,6 +1468,91 @@ int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, 
     Launch L{static_cast<cudaStream_t>(stream), false, nullptr};
     cudaError_t e = launch_gemv(L, scales_dev ? Q3_Q8_0 : Q3_BF16, a);
     if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "op_matvec: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+int q3_op_prefill_attention(const void* q_dev, const void* kv_dev, const int32_t* table_dev, int n_table,
+                            int n_blocks, int pos0, int T, int n_q, int n_kv, void* out_dev, int use_tc,
+                            void* stream)
+{
+    if (!q_dev || !kv_dev || !table_dev || !out_dev || T < 1 || pos0 < 0 || n_kv < 1 || n_q < 1 ||
+        n_q % n_kv || n_blocks < 1 || n_table < (pos0 + T + 31) / 32 || !aligned16(q_dev) ||
+        !aligned16(kv_dev) || !aligned16(out_dev))
+        return fail(Q3_ERR_INVALID_ARG, "op_prefill_attention: bad argument");
+    if (use_tc && prefill_tc_rows(n_q, n_kv) < 1)
+        return fail(Q3_ERR_INVALID_ARG, "op_prefill_attention: tcgen05 kernel unsupported for these heads");
+    int dev = 0, n_sm = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return fail(Q3_ERR_CUDA, "op_prefill_attention: no CUDA device");
+    if (use_tc && prefill_tc_smem() > (size_t)optin)
+        return fail(Q3_ERR_INVALID_ARG, "op_prefill_attention: not enough shared memory");
+    // host-built metadata, as a round builds it: rows, tiles (longest
+    // context first), schedule, then the work counter and the status word
+    const int R = use_tc ? prefill_tc_rows(n_q, n_kv) : 64;
+    std::vector<int> row_pos(T), row_slot(T, 0), t_row0, t_rows;
+    for (int t = 0; t < T; ++t) row_pos[t] = pos0 + t;
+    for (int k = ((T - 1) / R) * R; k >= 0; k -= R) {
+        t_row0.push_back(k);
+        t_rows.push_back(std::min(R, T - k));
+    }
+    const int n_tiles = (int)t_row0.size();
+    std::vector<int> start, items;
+    int grid = 0;
+    if (use_tc) {
+        const int n_items = n_tiles * n_kv;
+        grid = std::max(1, std::min({n_sm, n_items, SCHED_GRID}));
+        std::vector<std::vector<int>> lists(grid);
+        std::vector<long long> load(grid, 0);
+        for (int t = 0; t < n_tiles; ++t) {
+            const long long cost = (pos0 + t_row0[t] + t_rows[t] - 1) / 128 + 2;
+            for (int h = 0; h < n_kv; ++h) {
+                const int c = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+                lists[c].push_back(t * n_kv + h);
+                load[c] += cost;
+            }
+        }
+        for (int c = 0; c < grid; ++c) {
+            start.push_back((int)items.size());
+            items.insert(items.end(), lists[c].begin(), lists[c].end());
+        }
+        start.push_back((int)items.size());
+    }
+    std::vector<int> meta;
+    auto put = [&](const std::vector<int>& v) { size_t at = meta.size(); meta.insert(meta.end(), v.begin(), v.end()); return at; };
+    const size_t o_pos = put(row_pos), o_slot = put(row_slot), o_r0 = put(t_row0), o_rows = put(t_rows);
+    const size_t o_start = put(start), o_items = put(items), o_ctr = put({0, 0});
+    int* dmeta = nullptr;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMalloc(&dmeta, sizeof(int) * meta.size()) != cudaSuccess)
+        return fail(Q3_ERR_OOM, "op_prefill_attention: metadata allocation failed");
+    PrefillAttnArgs pa{};
+    pa.q = static_cast<const __half*>(q_dev);
+    pa.T = T; pa.n_q = n_q; pa.n_kv = n_kv;
+    pa.row_pos = dmeta + o_pos; pa.row_slot = dmeta + o_slot;
+    pa.tile_row0 = dmeta + o_r0; pa.tile_rows = dmeta + o_rows; pa.n_tiles = n_tiles;
+    pa.work_counter = dmeta + o_ctr;
+    pa.sched_start = dmeta + o_start; pa.sched_items = dmeta + o_items;
+    pa.tables = table_dev; pa.max_blocks = n_table;
+    pa.kv_layer = static_cast<const bf16*>(kv_dev); pa.n_blocks = n_blocks;
+    pa.out = static_cast<__half*>(out_dev);
+    pa.status = dmeta + o_ctr + 1;
+    pa.kv_row0 = 0;
+    CUtensorMap tkv;
+    if (use_tc && !tmap_kv(&tkv, kv_dev, (uint64_t)n_blocks * 2 * n_kv * 32)) {
+        cudaFree(dmeta);
+        return fail(Q3_ERR_CUDA, "op_prefill_attention: tensor map encoding failed");
+    }
+    Launch L{st, false, nullptr};
+    cudaError_t e = cudaMemcpyAsync(dmeta, meta.data(), sizeof(int) * meta.size(), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = use_tc ? launch_prefill_attention_tc(L, tkv, pa, grid) : launch_prefill_attention(L, pa);
+    int status = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&status, pa.status, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    cudaFree(dmeta);
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "op_prefill_attention: %s", cudaGetErrorString(e));
+    if (status) return fail(Q3_ERR_DEVICE_CHECK, "op_prefill_attention: device status 0x%x", status);
     return Q3_OK;
 }
 
