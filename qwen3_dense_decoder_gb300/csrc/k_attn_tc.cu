@@ -26,13 +26,14 @@
 //
 // Roles (one CTA per SM, items from a host-built per-CTA list):
 //   warp 0       lane 0 issues every MMA and owns the tensor-memory columns
+//   warp 1       lane 0 fetches the K/V blocks of each tile with TMA
 //   warps 4..11  softmax and output: warp w reads TMEM lanes 32 (w % 4) ..
 //                + 32 and columns 64 ((w - 4) / 4) .. + 64 of its row, so two
 //                warps share each row (maxima exchanged through shared memory)
 //   warps 12..19 converters: the Q tile (cp.async); each K/V block of a tile
-//                lands as stored (BF16) by TMA in its 128-byte-swizzled place,
-//                and is converted to fp16 in place (positions past the tile's
-//                last query position, and blocks not fetched, become zeros)
+//                lands as stored (BF16) in its 128-byte-swizzled place and is
+//                converted to fp16 in place (positions past the tile's last
+//                query position, and blocks not fetched, become zeros)
 // Tensor memory (512 columns): S[2] at 0 / 128, O at 256, P[2] at 384 / 448.
 // Every wait is bounded; a timeout sets the status word and the CTA winds
 // down without touching its remaining items.
@@ -58,13 +59,16 @@ constexpr int TMEM_COLS = 512;
 constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;
 constexpr float LAZY = 8.0f;                 // log2 growth of a row maximum tolerated before rescaling
 
+constexpr int NST = 3;                       // K/V ring stages
+
 struct alignas(1024) TcSmem {
-    uint8_t q[2][TILE];
-    uint8_t k[2][TILE];
-    uint8_t v[2][TILE];
-    uint64_t q_full[2], q_free[2], kv_load[2], kv_full[2], s_full[2], p_full[2], pv_done[2], o_free, drain;
-    int blk_ok[2][BN / 32];                  // blocks of the tile the loader fetched
-    float xch[2][2][128];                    // [tile parity][column half][row] maxima, then row sums
+    uint8_t q[TILE];                         // the item's Q tile, released after its last S
+    uint8_t k[NST][TILE];
+    uint8_t v[NST][TILE];
+    uint64_t q_full, q_free, kv_load[NST], kv_full[NST], kv_free[NST], s_full[2], p_full[2], pv_done[2];
+    uint64_t o_free, drain, pair[4];
+    int blk_ok[NST][BN / 32];                // blocks of the tile the loader fetched
+    float xch[2][128];                       // [column half][row] maxima, then row sums
     uint32_t tmem;
     int abort;
 };
@@ -178,11 +182,11 @@ Q3_DEV Item item_of(const PrefillAttnArgs& p, int k) {
 // ---------------------------------------------------------------- MMA issuer
 Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0, int i1) {
     uint32_t g = 0;                                  // K/V tiles issued so far by this CTA
-    auto issue_s = [&](int qb, uint32_t gt) -> bool {
-        const int b = gt & 1;
-        if (!wait_bar(&sm.kv_full[b], (gt >> 1) & 1, sm, p.status)) return false;
+    auto issue_s = [&](uint32_t gt) -> bool {
+        const int b = gt & 1, st = gt % NST;
+        if (!wait_bar(&sm.kv_full[st], (gt / NST) & 1, sm, p.status)) return false;
         tc_fence_after();
-        const uint32_t qa = smem_u32(sm.q[qb]), ka = smem_u32(sm.k[b]);
+        const uint32_t qa = smem_u32(sm.q), ka = smem_u32(sm.k[st]);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
             const uint32_t off = (s >> 2) * ATOM + (s & 3) * 32;
@@ -193,31 +197,40 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
         return true;
     };
     bool ok = true;
-    if (i0 < i1) ok = wait_bar(&sm.q_full[0], 0, sm, p.status) && issue_s(0, 0);
+    if (i0 < i1) {
+        const Item it0 = item_of(p, i0);
+        ok = wait_bar(&sm.q_full, 0, sm, p.status) && issue_s(0);
+        if (ok && it0.n_kt == 1) tc_commit(&sm.q_free);
+    }
     for (int k = i0, local = 0; k < i1 && ok; ++k, ++local) {
         const Item it = item_of(p, k);
-        const int qb = local & 1;
         for (int t = 0; t < it.n_kt; ++t, ++g) {
-            // scores of the item's next tile run while the softmax works on this one
-            if (t + 1 < it.n_kt && !(ok = issue_s(qb, g + 1))) break;
+            // scores of the item's next tile run while the softmax works on this one;
+            // after the item's last scores its Q buffer is free for the next item
+            if (t + 1 < it.n_kt) {
+                if (!(ok = issue_s(g + 1))) break;
+                if (t + 2 == it.n_kt) tc_commit(&sm.q_free);
+            }
             // O of the previous item read out before this item's first PV overwrites it
             if (t == 0 && local > 0 && !(ok = wait_bar(&sm.o_free, (local - 1) & 1, sm, p.status))) break;
-            const int b = g & 1;
+            const int b = g & 1, st = g % NST;
             if (!(ok = wait_bar(&sm.p_full[b], (g >> 1) & 1, sm, p.status))) break;
             tc_fence_after();
-            const uint32_t va = smem_u32(sm.v[b]);
+            const uint32_t va = smem_u32(sm.v[st]);
 #pragma unroll
             for (int s = 0; s < BN / 16; ++s)          // 16 positions per step
                 tc_mma_f16_ts(tmem + T_O, tmem + T_P + b * 64 + s * 8, smem_desc_sw128_mn(va + s * 2048, ATOM),
                               IDESC_PV, (t > 0 || s > 0) ? 1u : 0u);
             tc_commit(&sm.pv_done[b]);
+            tc_commit(&sm.kv_free[st]);
         }
         if (!ok) break;
-        tc_commit(&sm.q_free[qb]);
         // the next item's first scores (g is its first tile)
         if (k + 1 < i1) {
             const int nl = local + 1;
-            ok = wait_bar(&sm.q_full[nl & 1], (nl >> 1) & 1, sm, p.status) && issue_s(nl & 1, g);
+            const Item nx = item_of(p, k + 1);
+            ok = wait_bar(&sm.q_full, nl & 1, sm, p.status) && issue_s(g);
+            if (ok && nx.n_kt == 1) tc_commit(&sm.q_free);
         }
     }
     // nothing of this CTA's may still run on the tensor cores at deallocation
@@ -225,67 +238,74 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
     mbar_wait(&sm.drain, 0, p.status);
 }
 
+// ---------------------------------------------------------------- K/V loader
+// One thread fetches each tile's blocks once the PV NST tiles back has
+// released the stage, up to NST tiles ahead of the converters: per block, K
+// and V as two 64-column boxes of 32 positions each.
+Q3_DEV void load_role(const PrefillAttnArgs& p, const CUtensorMap* tkv, TcSmem& sm, int i0, int i1) {
+    uint32_t g = 0;
+    for (int k = i0; k < i1; ++k) {
+        const Item it = item_of(p, k);
+        for (int t = 0; t < it.n_kt; ++t, ++g) {
+            const int b = g % NST;
+            if (g >= NST && !wait_bar(&sm.kv_free[b], (g / NST - 1) & 1, sm, p.status)) return;
+            int phys[BN / 32];
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int j = 0; j < BN / 32; ++j) {
+                const int kp = t * BN + 32 * j;
+                phys[j] = -1;
+                if (kp <= it.pos_last) {
+                    const int ph = it.table[kp >> 5];
+                    if (ph >= 0 && ph < p.n_blocks) {
+                        phys[j] = ph;
+                        bytes += 4 * 32 * 64 * 2;
+                    } else {
+                        set_status(p.status, Q3_STATUS_BLOCK_RANGE);
+                    }
+                }
+                sm.blk_ok[b][j] = phys[j] >= 0;
+            }
+            mbar_arrive_expect_tx(&sm.kv_load[b], bytes);
+#pragma unroll
+            for (int j = 0; j < BN / 32; ++j) {
+                if (phys[j] < 0) continue;
+                const int rk = p.kv_row0 + ((phys[j] * 2) * p.n_kv + it.kvh) * 32;
+                const int rv = rk + p.n_kv * 32;
+                tma_load_2d(sm.k[b] + j * 32 * 128, tkv, &sm.kv_load[b], 0, rk);
+                tma_load_2d(sm.k[b] + ATOM + j * 32 * 128, tkv, &sm.kv_load[b], 64, rk);
+                tma_load_2d(sm.v[b] + j * 32 * 128, tkv, &sm.kv_load[b], 0, rv);
+                tma_load_2d(sm.v[b] + ATOM + j * 32 * 128, tkv, &sm.kv_load[b], 64, rv);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- converters
-Q3_DEV void convert_role(const PrefillAttnArgs& p, const CUtensorMap* tkv, TcSmem& sm, int i0, int i1) {
+Q3_DEV void convert_role(const PrefillAttnArgs& p, TcSmem& sm, int i0, int i1) {
     const int ct = threadIdx.x - CONV0 * 32;
     const int G = p.n_q / p.n_kv, R = 128 / G;
     const int qw = p.n_q * D;
     uint32_t g = 0;
     for (int k = i0, local = 0; k < i1; ++k, ++local) {
         const Item it = item_of(p, k);
-        const int qb = local & 1;
-        if (local >= 2 && !wait_bar(&sm.q_free[qb], ((local >> 1) - 1) & 1, sm, p.status)) return;
+        if (local >= 1 && !wait_bar(&sm.q_free, (local - 1) & 1, sm, p.status)) return;
         // Q tile: row r = position index r / G, head r % G (padding rows repeat row 0)
         for (int i = ct; i < 128 * 16; i += NCT) {
             const int r = i >> 4, c = i & 15;
             int ir = r / G, hh = r % G;
             if (ir >= R) ir = hh = 0;
             const int src_row = it.row0 + min(ir, it.nrows - 1);
-            cp_async_16(sm.q[qb] + sw_off(r, c), p.q + (size_t)src_row * qw + (it.kvh * G + hh) * D + c * 8);
+            cp_async_16(sm.q + sw_off(r, c), p.q + (size_t)src_row * qw + (it.kvh * G + hh) * D + c * 8);
         }
         cp_async_commit();
         cp_async_wait_all();
         fence_proxy_async_smem();
-        mbar_arrive(&sm.q_full[qb]);
+        mbar_arrive(&sm.q_full);
 
         for (int t = 0; t < it.n_kt; ++t, ++g) {
-            const int b = g & 1;
-            // one thread fetches the tile's blocks once the PV two tiles back
-            // has released the buffer: per block, K and V as two 64-column
-            // boxes of 32 positions each
-            if (ct == 0) {
-                bool ok = g < 2 || wait_bar(&sm.pv_done[b], ((g >> 1) - 1) & 1, sm, p.status);
-                int phys[BN / 32];
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int j = 0; j < BN / 32; ++j) {
-                    const int kp = t * BN + 32 * j;
-                    phys[j] = -1;
-                    if (ok && kp <= it.pos_last) {
-                        const int ph = it.table[kp >> 5];
-                        if (ph >= 0 && ph < p.n_blocks) {
-                            phys[j] = ph;
-                            bytes += 4 * 32 * 64 * 2;
-                        } else {
-                            set_status(p.status, Q3_STATUS_BLOCK_RANGE);
-                        }
-                    }
-                    sm.blk_ok[b][j] = phys[j] >= 0;
-                }
-                mbar_arrive_expect_tx(&sm.kv_load[b], bytes);
-#pragma unroll
-                for (int j = 0; j < BN / 32; ++j) {
-                    if (phys[j] < 0) continue;
-                    const int rk = p.kv_row0 + ((phys[j] * 2) * p.n_kv + it.kvh) * 32;
-                    const int rv = rk + p.n_kv * 32;
-                    tma_load_2d(sm.k[b] + j * 32 * 128, tkv, &sm.kv_load[b], 0, rk);
-                    tma_load_2d(sm.k[b] + ATOM + j * 32 * 128, tkv, &sm.kv_load[b], 64, rk);
-                    tma_load_2d(sm.v[b] + j * 32 * 128, tkv, &sm.kv_load[b], 0, rv);
-                    tma_load_2d(sm.v[b] + ATOM + j * 32 * 128, tkv, &sm.kv_load[b], 64, rv);
-                }
-                if (!ok) return;
-            }
-            if (!wait_bar(&sm.kv_load[b], (g >> 1) & 1, sm, p.status)) return;
+            const int b = g % NST;
+            if (!wait_bar(&sm.kv_load[b], (g / NST) & 1, sm, p.status)) return;
             // each thread converts its chunks in place (zeros where nothing valid was fetched)
             constexpr int PER = BN * 16 / NCT;
 #pragma unroll
@@ -317,8 +337,16 @@ Q3_DEV float ex2(float x) {
     return y;
 }
 
-// the two warps of a TMEM lane quadrant meet on named barrier 1 + quadrant
-Q3_DEV void pair_sync(int quad) { named_bar(1 + quad, 64); }
+
+// the two warps of a TMEM lane quadrant meet on the quadrant's mbarrier
+// (bounded, so a partner that gave up cannot leave this warp waiting); n
+// counts the meetings so far
+Q3_DEV bool pair_sync(TcSmem& sm, int quad, uint32_t& n, int* status) {
+    mbar_arrive(&sm.pair[quad]);
+    const bool ok = wait_bar(&sm.pair[quad], n & 1, sm, status);
+    ++n;
+    return ok;
+}
 
 Q3_DEV void softmax_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0, int i1) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -329,7 +357,7 @@ Q3_DEV void softmax_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, in
     const int qw = p.n_q * D;
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);     // this warp's TMEM lanes
     const float scale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
-    uint32_t g = 0;
+    uint32_t g = 0, npair = 0;
     for (int k = i0, local = 0; k < i1; ++k, ++local) {
         const Item it = item_of(p, k);
         const int ir = row / G, hh = row % G;
@@ -355,9 +383,10 @@ Q3_DEV void softmax_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, in
             }
 #pragma unroll
             for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(v[e >> 5][e & 31]));
-            sm.xch[b][half][row] = mx * scale;
-            pair_sync(quad);
-            const float m_new = fmaxf(m_used, fmaxf(sm.xch[b][0][row], sm.xch[b][1][row]));
+            if (!pair_sync(sm, quad, npair, p.status)) return;   // the partner has read the last exchange
+            sm.xch[half][row] = mx * scale;
+            if (!pair_sync(sm, quad, npair, p.status)) return;
+            const float m_new = fmaxf(m_used, fmaxf(sm.xch[0][row], sm.xch[1][row]));
             if (t == 0) {
                 m_used = m_new;
             } else if (__any_sync(0xffffffffu, m_new > m_used + LAZY)) {
@@ -404,16 +433,16 @@ Q3_DEV void softmax_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, in
             mbar_arrive(&sm.p_full[b]);
         }
         // the item's O is complete once the PV of its last tile is; the row
-        // sum is the two halves' (the slot of the last tile's parity was
-        // last read before that tile's pair barrier)
-        sm.xch[g & 1][half][row] = l;
+        // sum is the two halves'
+        if (!pair_sync(sm, quad, npair, p.status)) return;
+        sm.xch[half][row] = l;
         {
             const uint32_t gl = g - 1;
             if (!wait_bar(&sm.pv_done[gl & 1], (gl >> 1) & 1, sm, p.status)) return;
             tc_fence_after();
         }
-        pair_sync(quad);
-        const float inv = 1.0f / (sm.xch[g & 1][0][row] + sm.xch[g & 1][1][row]);
+        if (!pair_sync(sm, quad, npair, p.status)) return;
+        const float inv = 1.0f / (sm.xch[0][row] + sm.xch[1][row]);
         bool bad = false;
         __half* dst = p.out + (size_t)(it.row0 + min(ir, it.nrows - 1)) * qw + (it.kvh * G + hh) * D + c0;
 #pragma unroll 1
@@ -450,16 +479,20 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_attn_tc_kernel(const __gri
     TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm.q_full[b], NCT);
-            mbar_init(&sm.q_free[b], 1);
+        mbar_init(&sm.q_full, NCT);
+        mbar_init(&sm.q_free, 1);
+        for (int b = 0; b < NST; ++b) {
             mbar_init(&sm.kv_load[b], 1);
             mbar_init(&sm.kv_full[b], NCT);
+            mbar_init(&sm.kv_free[b], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.s_full[b], 1);
             mbar_init(&sm.p_full[b], NSOFT * 32);
             mbar_init(&sm.pv_done[b], 1);
         }
         mbar_init(&sm.o_free, NSOFT * 32);
+        for (int i = 0; i < 4; ++i) mbar_init(&sm.pair[i], 64);
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
         fence_barrier_init();
@@ -479,10 +512,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_attn_tc_kernel(const __gri
     if (warp == 0) {
         if ((threadIdx.x & 31) == 0) mma_role(p, sm, tmem, i0, i1);
         __syncwarp();
+    } else if (warp == 1) {
+        if ((threadIdx.x & 31) == 0) load_role(p, &tkv, sm, i0, i1);
+        __syncwarp();
     } else if (warp >= SOFT0 && warp < SOFT0 + NSOFT) {
         softmax_role(p, sm, tmem, i0, i1);
     } else if (warp >= CONV0) {
-        convert_role(p, &tkv, sm, i0, i1);
+        convert_role(p, sm, i0, i1);
     }
     tc_fence_before();
     __syncthreads();
