@@ -66,7 +66,7 @@ def parse():
     ap.add_argument("--sessions", type=int, default=32)
     ap.add_argument("--no-b32", action="store_true", help="skip the batch-32 decode leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
-    ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup"), default=None,
+    ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill"), default=None,
                     help="run only a small case sized for an ncu capture (a few GB on the device) and exit")
     return ap.parse_args()
 
@@ -95,6 +95,29 @@ def ncu_case(name: str):
         for _ in range(6):
             ses.eval(tok, lg, tok)
         m.sync()
+    elif name == "attn-prefill":
+        # one layer's prefill attention of a 2,048-token round of the Qwen3-4B
+        # shape (32 query / 8 KV heads) over a permuted block table
+        T, n_q, n_kv = 2048, 32, 8
+        nblk = T // 32
+        g = torch.Generator(device="cuda")
+        g.manual_seed(6)
+        q = torch.randn(T, n_q, 128, device="cuda", generator=g).to(torch.float16)
+        kv = torch.randn(nblk + 8, 2, n_kv, 32, 128, device="cuda", generator=g).to(torch.bfloat16)
+        table = torch.from_numpy(synthetic.make_block_permutation(nblk + 8, seed=7)[:nblk]).cuda()
+        for _ in range(6):
+            q3.op_prefill_attention(q, kv, table, 0, n_kv)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(True), torch.cuda.Event(True)
+        a.record()
+        for _ in range(10):
+            q3.op_prefill_attention(q, kv, table, 0, n_kv)
+        b.record()
+        b.synchronize()
+        us = a.elapsed_time(b) / 10 * 1e3
+        fl = 4.0 * 128 * n_q * T * (T + 1) / 2
+        print(f"prefill attention T={T}: {us:.1f} us/call (with its metadata upload and sync), "
+              f"{fl / us / 1e6:.1f} TFLOP/s", flush=True)
     else:
         # the gate/up projection of a 2,048-token prefill of the Qwen3-4B shape
         M, N, K = 19456, 2048, 2560

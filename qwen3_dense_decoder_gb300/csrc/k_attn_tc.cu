@@ -30,7 +30,7 @@
 //   warps 4..11  softmax and output: warp w reads TMEM lanes 32 (w % 4) ..
 //                + 32 and columns 64 ((w - 4) / 4) .. + 64 of its row, so two
 //                warps share each row (maxima exchanged through shared memory)
-//   warps 12..19 converters: the Q tile (cp.async); each K/V block of a tile
+//   warps 2, 3, 12..19 converters: the Q tile (cp.async); each K/V block of a tile
 //                lands as stored (BF16) in its 128-byte-swizzled place and is
 //                converted to fp16 in place (positions past the tile's last
 //                query position, and blocks not fetched, become zeros)
@@ -50,10 +50,10 @@ constexpr int D = 128;
 constexpr int BN = 128;                      // key positions per K/V tile
 constexpr int ATOM = 128 * 128;              // one 128-row x 64-column fp16 swizzle atom (bytes)
 constexpr int TILE = 2 * ATOM;               // 128 rows x 128 fp16 (32 KB)
-constexpr int NCONV = 8;                     // converter warps
 constexpr int NSOFT = 8;                     // softmax warps (two per TMEM lane quadrant)
 constexpr int SOFT0 = 4, CONV0 = SOFT0 + NSOFT;
-constexpr int THREADS = (CONV0 + NCONV) * 32;
+constexpr int NCONV = 10;                    // converter warps: 2, 3 and CONV0 .. CONV0 + 7
+constexpr int THREADS = (CONV0 + NCONV - 2) * 32;
 constexpr int NCT = NCONV * 32;              // converter threads
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;
@@ -283,7 +283,7 @@ Q3_DEV void load_role(const PrefillAttnArgs& p, const CUtensorMap* tkv, TcSmem& 
 
 // ---------------------------------------------------------------- converters
 Q3_DEV void convert_role(const PrefillAttnArgs& p, TcSmem& sm, int i0, int i1) {
-    const int ct = threadIdx.x - CONV0 * 32;
+    const int ct = threadIdx.x < CONV0 * 32 ? threadIdx.x - 64 : threadIdx.x - CONV0 * 32 + 64;
     const int G = p.n_q / p.n_kv, R = 128 / G;
     const int qw = p.n_q * D;
     uint32_t g = 0;
@@ -307,10 +307,8 @@ Q3_DEV void convert_role(const PrefillAttnArgs& p, TcSmem& sm, int i0, int i1) {
             const int b = g % NST;
             if (!wait_bar(&sm.kv_load[b], (g / NST) & 1, sm, p.status)) return;
             // each thread converts its chunks in place (zeros where nothing valid was fetched)
-            constexpr int PER = BN * 16 / NCT;
-#pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                const int i = ct + j * NCT;
+#pragma unroll 2
+            for (int i = ct; i < BN * 16; i += NCT) {
                 const int key = i >> 4;
                 const uint32_t off = sw_off(key, i & 15);
                 uint4* pk_ = reinterpret_cast<uint4*>(sm.k[b] + off);
@@ -517,7 +515,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_attn_tc_kernel(const __gri
         __syncwarp();
     } else if (warp >= SOFT0 && warp < SOFT0 + NSOFT) {
         softmax_role(p, sm, tmem, i0, i1);
-    } else if (warp >= CONV0) {
+    } else if (warp >= CONV0 || warp == 2 || warp == 3) {
         convert_role(p, sm, i0, i1);
     }
     tc_fence_before();
