@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--sessions", type=int, default=32)
     ap.add_argument("--no-b32", action="store_true", help="skip the batch-32 decode leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
+    ap.add_argument("--shapes", nargs="*", default=None,
+                    choices=("0.6b", "8b-q8_0", "14b"),
+                    help="measure the other named shapes instead (one JSON line each; all three if none given)")
     ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill"), default=None,
                     help="run only a small case sized for an ncu capture (a few GB on the device) and exit")
     return ap.parse_args()
@@ -441,10 +444,185 @@ def oracle_decode_sample(shape, weights, budget_s: float, max_steps: int, warmup
     dt = time.perf_counter() - t0
     ctx = 16 + warmup
     return {"value": steps / dt, "unit": "tok/s", "cores": m.n_threads, "kind": "oracle",
-            "sample": (f"{steps} greedy decode steps of the full 36-layer Qwen3-4B shape at batch 1 "
-                       f"after a 16-token prompt (context {ctx + 1}..{ctx + steps} instead of "
-                       f"~{2048 + 128}: attention is under 8% of a step's work at that length)"),
+            "sample": (f"{steps} greedy decode steps of the full {shape.n_layers}-layer {shape.name} shape "
+                       f"at batch 1 after a 16-token prompt (context {ctx + 1}..{ctx + steps}; at that "
+                       f"length attention is a few percent of a step's work)"),
             "seconds": dt, "steps": steps}
+
+
+# ---------------------------------------------------------------- other named shapes
+
+def q8_bytes(params: int) -> float:
+    """Q8_0 bytes of `params` weights: 34-byte blocks of 32."""
+    return params * 34.0 / 32.0
+
+
+def step_bytes(s, ctxs) -> float:
+    """HBM bytes of one decode step: every projection once (bf16, or Q8_0
+    blocks), the lm_head once (bf16), and the K/V of every cached position of
+    every session."""
+    w = (q8_bytes(proj_params(s)) if s.scheme == 1 else 2.0 * proj_params(s)) + 2.0 * s.vocab * s.hidden
+    return w + s.n_layers * 2 * s.kv_width * 2 * float(sum(ctxs))
+
+
+def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
+    """The named workload of one shape ("Kipp Model Support", section "The
+    registry"): 0.6B -- a 128-token prompt, 64 greedy decode steps, and a ragged
+    3-round prefill (5, 40, 83); 8B Q8_0 -- a 2,048-token prefill, then decode at
+    batch 1 and at 32 sessions with prompts U[64, 2048]; 14B -- a 12,800-token
+    prefill in 2,048-token chunks, then 8 sessions decoding 128 tokens at a
+    16,384-token context over one shared block pool with permuted tables."""
+    import numpy as np
+    import torch
+
+    import qwen3_dense_decoder_gb300 as q3
+    import synthetic
+    s = synthetic.SHAPES[name]
+    st = torch.cuda.Stream()
+    torch.cuda.set_stream(st)
+    w = synthetic.make_weights(s, seed=1234, device="cuda")     # bf16 source (the oracle packs its own)
+    wg = w
+    if s.scheme == synthetic.Q8_0:
+        wg = dict(w, layers=[dict(lw) for lw in w["layers"]])
+        for lw in wg["layers"]:
+            for nm in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
+                lw[nm] = q3.quantize_q8_0(lw[nm])
+    V = s.vocab
+
+    def timed(fn):
+        a, b = torch.cuda.Event(True), torch.cuda.Event(True)
+        torch.cuda.synchronize()
+        a.record(st)
+        fn()
+        b.record(st)
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    out = {"shape": s.name, "n_gpus": 1, "dtype": "bf16" if s.scheme == synthetic.BF16 else "q8_0 weights, fp16/bf16 compute",
+           "data": "synthetic (seeded random-init weights and tokens)", "peak_kind": pk_kind}
+    lg = torch.empty(max(32, 8), V, dtype=torch.float32, device="cuda")
+    am = torch.zeros(max(32, 8), dtype=torch.int32, device="cuda")
+    peak_tf, peak_gb = pk["bf16_tflops"], pk["hbm_gbs"]
+
+    def prefill_entry(T, ms, flops=None):
+        fl = flops if flops is not None else prefill_flops(s, T)
+        return {"tokens": T, "ms": round(ms, 3), "tok_s": round(T / ms * 1e3, 1),
+                "tflops": round(fl / ms / 1e9, 1), "tc_frac": round(fl / ms / 1e9 / peak_tf, 4)}
+
+    def decode_entry(sessions, steps, ms, ctxs):
+        by = step_bytes(s, ctxs)
+        return {"sessions": sessions, "steps": steps, "ms_per_step": round(ms / steps, 4),
+                "tok_s": round(sessions * steps / ms * 1e3, 1), "bytes_per_step": by,
+                "hbm_frac": round(by / (ms / steps) / 1e6 / peak_gb, 4)}
+
+    if name == "0.6b":
+        m = q3.Model(s, wg, max_ctx=512, max_round_tokens=2048, stream=st)
+        pool = m.pool(16, 2)
+        ses = pool.session()
+        toks = torch.tensor(synthetic.make_tokens(128, V, seed=7), device="cuda")
+        pre = []
+        for i in range(4):
+            ses.reset()
+            t = timed(lambda: ses.eval(toks, lg[0], am[0:1]))
+            if i:
+                pre.append(t)
+        out["prefill_128"] = prefill_entry(128, statistics.median(pre))
+        tok = am[0:1].clone()
+        for _ in range(3):
+            ses.eval(tok, lg[0], tok)
+        c0 = ses.pos
+        ms = timed(lambda: [ses.eval(tok, lg[0], tok) for _ in range(64)])
+        out["decode_b1"] = decode_entry(1, 64, ms, [c0 + 32])
+        ses.reset()
+        rounds = [5, 40, 83]
+        rt = torch.tensor(synthetic.make_tokens(sum(rounds), V, seed=8), device="cuda")
+
+        def ragged():
+            a = 0
+            for n in rounds:
+                ses.eval(rt[a:a + n], lg[0], am[0:1])
+                a += n
+        ragged()
+        ses.reset()
+        ms = timed(ragged)
+        out["prefill_ragged_5_40_83"] = prefill_entry(sum(rounds), ms)
+        ses.close()
+    elif name == "8b-q8_0":
+        m = q3.Model(s, wg, max_ctx=2400, max_round_tokens=2048, stream=st)
+        pool = m.pool(34 * 75 + 8, 36)
+        ses = pool.session()
+        toks = torch.tensor(synthetic.make_tokens(2048, V, seed=7), device="cuda")
+        pre = []
+        for i in range(3):
+            ses.reset()
+            t = timed(lambda: ses.eval(toks, lg[0], am[0:1]))
+            if i:
+                pre.append(t)
+        out["prefill_2048"] = prefill_entry(2048, statistics.median(pre))
+        tok = am[0:1].clone()
+        for _ in range(3):
+            ses.eval(tok, lg[0], tok)
+        c0 = ses.pos
+        ms = timed(lambda: [ses.eval(tok, lg[0], tok) for _ in range(64)])
+        out["decode_b1"] = decode_entry(1, 64, ms, [c0 + 32])
+        ses.close()
+        B = 32
+        lens = synthetic.make_prompt_lengths(B, 64, 2048, seed=11)
+        ss = [pool.session() for _ in range(B)]
+        for i, x in enumerate(ss):
+            x.eval(torch.tensor(synthetic.make_tokens(int(lens[i]), V, seed=100 + i), device="cuda"),
+                   lg[0], am[i:i + 1])
+        bt = am[:B].clone()
+        for _ in range(3):
+            m.eval_batch(ss, bt, [1] * B, lg[:B], bt)
+        ctxs = [x.pos + 8 for x in ss]
+        ms = timed(lambda: [m.eval_batch(ss, bt, [1] * B, lg[:B], bt) for _ in range(16)])
+        out["decode_b32"] = decode_entry(B, 16, ms, ctxs)
+        for x in ss:
+            x.close()
+    else:
+        B, CTX, STEPS, CHUNK = 8, 16384, 128, 2048
+        nblk = (CTX + STEPS + 31) // 32
+        m = q3.Model(s, wg, max_ctx=CTX + STEPS + 64, max_round_tokens=CHUNK, stream=st)
+        pool = m.pool(B * nblk + 16, B + 1)
+        perm = synthetic.make_block_permutation(B * nblk + 16, seed=21)
+        ss = []
+        for i in range(B):
+            x = pool.session()
+            x.set_block_table(perm[i * nblk:(i + 1) * nblk])
+            ss.append(x)
+        toks = torch.tensor(synthetic.make_tokens(CTX, V, seed=9), device="cuda")
+
+        def chunks(x, lo, hi):
+            for a in range(lo, hi, CHUNK):
+                x.eval(toks[a:min(hi, a + CHUNK)], lg[0], am[0:1])
+        ms = timed(lambda: chunks(ss[0], 0, 12800))
+        fl = 2.0 * proj_params(s) * 12800 + 2.0 * s.n_layers * s.q_width * 12800 * 12800 \
+            + 2.0 * V * s.hidden * ((12800 + CHUNK - 1) // CHUNK)
+        out["prefill_12800_chunked"] = prefill_entry(12800, ms, fl)
+        chunks(ss[0], 12800, CTX)
+        for x in ss[1:]:
+            chunks(x, 0, CTX)
+        bt = am[:B].clone()
+        for _ in range(2):
+            m.eval_batch(ss, bt, [1] * B, lg[:B], bt)
+        ctxs = [x.pos + STEPS // 2 for x in ss]
+        ms = timed(lambda: [m.eval_batch(ss, bt, [1] * B, lg[:B], bt) for _ in range(STEPS)])
+        out["decode_8x16k"] = decode_entry(B, STEPS, ms, ctxs)
+        for x in ss:
+            x.close()
+    m.sync()
+    out["gpu_launches_total"] = m.launch_count
+    del m
+    torch.cuda.synchronize()
+    if with_oracle:
+        cb = oracle_decode_sample(s, w, budget_s=8.0, max_steps=8)
+        cb.pop("steps", None)
+        cb.pop("seconds", None)
+        out["cpu_baseline"] = cb
+    del w, wg
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- report
@@ -587,6 +765,11 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
     pk, pk_kind = peaks()
+    if args.shapes is not None:
+        for name in args.shapes or ["0.6b", "8b-q8_0", "14b"]:
+            if rank == 0:
+                print(json.dumps(run_shape(name, pk, pk_kind, with_oracle=not args.no_cpu)), flush=True)
+        return
     res = run_gpu(args, dist_on, rank, world)
     line = report(args, res, world, dist_on, pk, pk_kind)
     if rank == 0 and not args.no_cpu:
