@@ -28,6 +28,13 @@ Q3_DEV uint32_t smem_u32_early(const void* p) {
 Q3_DEV float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
 Q3_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 Q3_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// The four signed bytes of q as exact floats without the int-to-float unit:
+// with the sign bit flipped a byte b becomes b + 128 in [0, 255], and the
+// word 0x4B000000 | (b + 128) is the float 2^23 + 128 + b exactly, so one
+// byte permute and one subtraction give b (the same value as a conversion).
+Q3_DEV float i8_byte(uint32_t flipped, uint32_t sel) {
+    return __uint_as_float(__byte_perm(flipped, 0x4B000000u, sel)) - 8388736.0f;
+}
 
 Q3_DEV uint4 ldg_nc_v4(const void* p) {
     uint4 r;

@@ -159,10 +159,11 @@ Q3_DEV float dot8(uint4 w, float4 a, float4 b) {
 }
 
 Q3_DEV float dot4_i8(uint32_t q, float4 a) {
-    float s = (float)(int8_t)(q & 0xff) * a.x;
-    s = fmaf((float)(int8_t)((q >> 8) & 0xff), a.y, s);
-    s = fmaf((float)(int8_t)((q >> 16) & 0xff), a.z, s);
-    s = fmaf((float)(int8_t)(q >> 24), a.w, s);
+    const uint32_t f = q ^ 0x80808080u;
+    float s = i8_byte(f, 0x7650) * a.x;
+    s = fmaf(i8_byte(f, 0x7651), a.y, s);
+    s = fmaf(i8_byte(f, 0x7652), a.z, s);
+    s = fmaf(i8_byte(f, 0x7653), a.w, s);
     return s;
 }
 
