@@ -13,8 +13,9 @@
 // bounds depend only on the context length, never on which physical blocks
 // back it, so paged and contiguous layouts give identical bits.  Each of the
 // four warps takes blocks round-robin and stages a block's K and V tiles in
-// shared memory with cp.async (one memory latency per block); lane j scores
-// position j, then each lane accumulates 4 of the 128 output dimensions.
+// shared memory with cp.async (one memory latency per block), then attends
+// the block on mma.sync tensor cores (q and P as BF16 high/low pairs, K and V
+// as stored; the routine the fused decode step uses).
 // Warps merge in warp order; splits merge in split order, done by whichever
 // split CTA of the (row, KV head) finishes last (an atomic ticket, no
 // waiting), so the result does not depend on scheduling.
@@ -24,6 +25,7 @@
 // row goes to the cache and straight into the staged tile, so tiles of
 // earlier positions can be fetched before the projections of this round
 // have landed (they are issued ahead of the programmatic-launch wait).
+#include "attn_block.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -34,19 +36,14 @@ namespace {
 constexpr int D = 128;
 constexpr int KV_BLOCK = 32;
 constexpr int AWARPS = 4;
-constexpr int K_STRIDE = D + 8;        // bf16 per staged K row: 272 bytes, conflict-free LDS.128
+constexpr int K_STRIDE = ATT_KSTR;     // bf16 per staged K/V row: 272 bytes, conflict-free ldmatrix
 constexpr int K_TILE = KV_BLOCK * K_STRIDE;
-constexpr int V_TILE = KV_BLOCK * D;
-
-Q3_DEV float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
+constexpr int V_TILE = KV_BLOCK * K_STRIDE;
+constexpr int NDT = D / 8;             // a warp attends all 16 dimension tiles of its blocks
 
 template <int G>
 struct AttnSmem {
-    static constexpr size_t q_bytes = (size_t)G * D * sizeof(float);
+    static constexpr size_t q_bytes = (size_t)16 * K_STRIDE * 2;     // q high/low rows (bf16)
     static constexpr size_t k_bytes = (size_t)AWARPS * K_TILE * 2;
     static constexpr size_t v_bytes = (size_t)AWARPS * V_TILE * 2;
     static constexpr size_t new_bytes = 2 * D * 2;                  // new K and V row (bf16)
@@ -63,17 +60,33 @@ Q3_DEV void stage_block(__nv_bfloat16* kt, __nv_bfloat16* vt, const __nv_bfloat1
         const int piece = i * 32 + lane;          // 512 pieces: row = piece / 16, col16 = piece % 16
         const int row = piece >> 4, c = piece & 15;
         cp_async_16(kt + row * K_STRIDE + c * 8, Kb + row * D + c * 8);
-        cp_async_16(vt + row * D + c * 8, Vb + row * D + c * 8);
+        cp_async_16(vt + row * K_STRIDE + c * 8, Vb + row * D + c * 8);
     }
     cp_async_commit();
 }
 
+// head g's q (lane: dims [4 lane, 4 lane + 4)), scaled, as BF16 rows 2g
+// (high part) and 2g + 1 (remainder) of the 16-row tensor-core operand
+Q3_DEV void store_q_split(__nv_bfloat16* sqa, int g, const float (&y)[4], float scale, int lane) {
+    float hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float q = y[e] * scale;
+        hi[e] = __bfloat162float(__float2bfloat16_rn(q));
+        lo[e] = q - hi[e];
+    }
+    *reinterpret_cast<uint2*>(sqa + (2 * g) * K_STRIDE + lane * 4) =
+        make_uint2(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]));
+    *reinterpret_cast<uint2*>(sqa + (2 * g + 1) * K_STRIDE + lane * 4) =
+        make_uint2(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]));
+}
+
 template <int G, bool FUSED>
-__global__ void __launch_bounds__(AWARPS * 32) attn_kernel(const AttnArgs p)
+__global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
 {
     using S = AttnSmem<G>;
     extern __shared__ __align__(16) uint8_t smem[];
-    float* sq = reinterpret_cast<float*>(smem);                                   // [G][D]
+    __nv_bfloat16* sqa = reinterpret_cast<__nv_bfloat16*>(smem);                  // [16][K_STRIDE]
     __nv_bfloat16* kt_all = reinterpret_cast<__nv_bfloat16*>(smem + S::q_bytes);
     __nv_bfloat16* vt_all = reinterpret_cast<__nv_bfloat16*>(smem + S::q_bytes + S::k_bytes);
     __nv_bfloat16* snew = reinterpret_cast<__nv_bfloat16*>(smem + S::q_bytes + S::k_bytes + S::v_bytes);
@@ -133,8 +146,7 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_kernel(const AttnArgs p)
             const float4 v = *reinterpret_cast<const float4*>(row + (kvh * G + g) * D + lane * 4);
             float y[4] = {v.x, v.y, v.z, v.w};
             head_norm_rope(y, p.q_gain, rope_row, p.eps, lane);
-            *reinterpret_cast<float4*>(sq + g * D + lane * 4) =
-                make_float4(y[0] * qscale, y[1] * qscale, y[2] * qscale, y[3] * qscale);
+            store_q_split(sqa, g, y, qscale, lane);
         }
         const bool mine = b0 <= last_blk && last_blk < b1;   // this split holds the new position
         if (mine && warp >= AWARPS - 2) {
@@ -160,18 +172,22 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_kernel(const AttnArgs p)
             }
         }
     } else {
-        for (int i = threadIdx.x; i < G * D; i += AWARPS * 32)
-            sq[i] = p.q[((size_t)t * p.n_q + kvh * G + i / D) * D + i % D] * qscale;
+        for (int g = warp; g < G; g += AWARPS) {
+            const float4 v = *reinterpret_cast<const float4*>(p.q + ((size_t)t * p.n_q + kvh * G + g) * D + lane * 4);
+            float y[4] = {v.x, v.y, v.z, v.w};
+            store_q_split(sqa, g, y, qscale, lane);
+        }
     }
+    // rows of the 16-row q operand past the G heads are zero
+    for (int i = threadIdx.x; i < (16 - 2 * G) * (D / 8); i += AWARPS * 32)
+        *reinterpret_cast<uint4*>(sqa + (2 * G + i / (D / 8)) * K_STRIDE + (i % (D / 8)) * 8) = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
-    float m[G], l[G], o[G][4];
+    AttAcc<NDT> st;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
-        o[g][0] = o[g][1] = o[g][2] = o[g][3] = 0.f;
-    }
+    for (int dt = 0; dt < NDT; ++dt) st.o[dt][0] = st.o[dt][1] = st.o[dt][2] = st.o[dt][3] = 0.f;
 
     for (; b < b1; b += AWARPS) {
         if (!staged) {
@@ -190,73 +206,37 @@ __global__ void __launch_bounds__(AWARPS * 32) attn_kernel(const AttnArgs p)
             const int r = pos % KV_BLOCK;
             *reinterpret_cast<uint2*>(kt + r * K_STRIDE + lane * 4) =
                 *reinterpret_cast<const uint2*>(snew + lane * 4);
-            *reinterpret_cast<uint2*>(vt + r * D + lane * 4) =
+            *reinterpret_cast<uint2*>(vt + r * K_STRIDE + lane * 4) =
                 *reinterpret_cast<const uint2*>(snew + D + lane * 4);
             __syncwarp();
         }
-        const bool valid = b * KV_BLOCK + lane < ctx;
-
-        // scores: lane j <- position b * 32 + j
-        float s[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) s[g] = 0.f;
-        const __nv_bfloat16* krow = kt + lane * K_STRIDE;
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 kw = *reinterpret_cast<const uint4*>(krow + c * 8);
-            const float k8[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
-                                 bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float4 qa = *reinterpret_cast<const float4*>(sq + g * D + c * 8);
-                const float4 qb = *reinterpret_cast<const float4*>(sq + g * D + c * 8 + 4);
-                s[g] = fmaf(k8[0], qa.x, s[g]);
-                s[g] = fmaf(k8[1], qa.y, s[g]);
-                s[g] = fmaf(k8[2], qa.z, s[g]);
-                s[g] = fmaf(k8[3], qa.w, s[g]);
-                s[g] = fmaf(k8[4], qb.x, s[g]);
-                s[g] = fmaf(k8[5], qb.y, s[g]);
-                s[g] = fmaf(k8[6], qb.z, s[g]);
-                s[g] = fmaf(k8[7], qb.w, s[g]);
-            }
-        }
-        float pr[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float sg = valid ? s[g] : -INFINITY;
-            const float m_new = fmaxf(m[g], warp_max(sg));
-            const float alpha = exp2f(m[g] - m_new);      // 0 on the first block (m = -inf)
-            pr[g] = valid ? exp2f(sg - m_new) : 0.f;
-            l[g] = l[g] * alpha + warp_allsum(pr[g]);
-            o[g][0] *= alpha; o[g][1] *= alpha; o[g][2] *= alpha; o[g][3] *= alpha;
-            m[g] = m_new;
-        }
-        // values: lane owns dims [4 lane, 4 lane + 4); invalid positions have p = 0
-#pragma unroll 8
-        for (int j = 0; j < KV_BLOCK; ++j) {
-            const uint2 vw = *reinterpret_cast<const uint2*>(vt + j * D + lane * 4);
-            const float v0 = bf16lo(vw.x), v1 = bf16hi(vw.x), v2 = bf16lo(vw.y), v3 = bf16hi(vw.y);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float pj = __shfl_sync(0xffffffffu, pr[g], j);
-                if (pj != 0.f) {
-                    o[g][0] = fmaf(pj, v0, o[g][0]);
-                    o[g][1] = fmaf(pj, v1, o[g][1]);
-                    o[g][2] = fmaf(pj, v2, o[g][2]);
-                    o[g][3] = fmaf(pj, v3, o[g][3]);
-                }
-            }
-        }
+        attend_block_tc<NDT>(reinterpret_cast<const uint8_t*>(kt), reinterpret_cast<const uint8_t*>(vt), sqa,
+                             min(KV_BLOCK, ctx - b * KV_BLOCK), 0, lane, st);
         __syncwarp();      // the tile is rewritten by the next block's copies
     }
     cp_async_wait_all();
     __syncthreads();       // the K tiles become the warp-merge buffer
 
+    // rows 2h and 2h + 1 of the accumulator hold the high and low parts of
+    // head h (rows g and g + 8 of lane g = lane / 4): head h of this warp is
+    // their sum, kept by the lanes of even g
+    {
+        const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if (lane == 0) { s_m[warp * G + g] = m[g]; s_l[warp * G + g] = l[g]; }
-        *reinterpret_cast<float4*>(s_o + (warp * G + g) * D + lane * 4) =
-            make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+        for (int dt = 0; dt < NDT; ++dt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st.o[dt][e] += __shfl_xor_sync(0xffffffffu, st.o[dt][e], 4);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int h = half * 4 + (g >> 1);
+            if ((g & 1) == 0 && h < G) {
+                if (tig == 0) { s_m[warp * G + h] = st.m[half]; s_l[warp * G + h] = st.l[half]; }
+#pragma unroll
+                for (int dt = 0; dt < NDT; ++dt)
+                    *reinterpret_cast<float2*>(s_o + (warp * G + h) * D + dt * 8 + 2 * tig) =
+                        make_float2(st.o[dt][2 * half], st.o[dt][2 * half + 1]);
+            }
+        }
     }
     __syncthreads();
 

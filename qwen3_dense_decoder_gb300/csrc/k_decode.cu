@@ -31,6 +31,7 @@
 // Q3_STATUS_TIMEOUT, unwinds, and waits (bounded) for its copies in flight.
 #include "common.cuh"
 #include "kernels.h"
+#include "attn_block.cuh"
 
 namespace q3 {
 
@@ -591,131 +592,10 @@ Q3_DEV void consume_weights(const WStage& s, const Smem& sm, uint32_t& it, int w
 }
 
 // ---------------------------------------------------------------- attention on tensor cores
-Q3_DEV void ldsm_x4(uint32_t (&r)[4], const void* p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
-}
-Q3_DEV void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
-}
-// D = A (16 x 16, row) * B (16 x 8, col) + D, bf16 inputs, fp32 accumulate
-Q3_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                     uint32_t b1) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-                 "{%8,%9}, {%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-Q3_DEV uint32_t pack_bf16(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// Online-softmax state of one warp over its blocks: the warp holds S and O
-// rows g = lane / 4 and g + 8 of the 16-row operands, row r standing for
-// query head r / 2 (even r: the bf16 high part of q or p, odd r: the
-// remainder), so q . k and p . v are exact to about 16 bits while K and V
-// stay the stored BF16.
 constexpr int ATT_DQ = 4;                  // warps per block: each takes 128 / ATT_DQ output dims
 constexpr int ATT_DT = D / 8 / ATT_DQ;     // dimension tiles of 8 per warp
-
-struct AttWarp {
-    float m[2], l[2];
-    float o[ATT_DT][4];       // this warp's dimension tiles
-};
-
-// Address of 16-byte chunk c (0..15, 8 dims each) of row r of a staged K/V tile.
-Q3_DEV const uint8_t* tile_chunk(const uint8_t* t, int r, int c) {
-    return t + r * (KSTR * 2) + c * 16;
-}
-
-// One 32-position block for the G query heads of the KV head (rows 2h, 2h+1
-// of sqa), output dimensions [32 dq, 32 dq + 32): S = q K^T on 4 x 8 mma
-// (positions x dims), masked to n_pos, online softmax, O += P V on 4 x 2.
-Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const bf16* sqa, int n_pos, int dq, int lane,
-                            AttWarp& w) {
-    const int g = lane >> 2, tig = lane & 3;
-    float sacc[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-    const int mi = lane >> 3, r8 = lane & 7;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t a[4];
-        // A: matrices (rows 0-7, k 0-7), (rows 8-15, k 0-7), (rows 0-7, k 8-15), (rows 8-15, k 8-15)
-        ldsm_x4(a, sqa + ((mi & 1) * 8 + r8) * KSTR + kk * 16 + (mi >> 1) * 8);
-#pragma unroll
-        for (int nh = 0; nh < 2; ++nh) {
-            uint32_t b[4];
-            // B: positions 16 nh + (0-7 | 8-15) x dims (0-7 | 8-15) of this k step
-            ldsm_x4(b, tile_chunk(kt, nh * 16 + (mi >> 1) * 8 + r8, kk * 2 + (mi & 1)));
-            mma_bf16(sacc[2 * nh], a[0], a[1], a[2], a[3], b[0], b[1]);
-            mma_bf16(sacc[2 * nh + 1], a[0], a[1], a[2], a[3], b[2], b[3]);
-        }
-    }
-    // rows 2h and 2h + 1 hold the two parts of head h: add them (lanes g ^ 1)
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float v = sacc[nt][e] + __shfl_xor_sync(0xffffffffu, sacc[nt][e], 4);
-            const int pos = nt * 8 + 2 * tig + (e & 1);
-            v = pos < n_pos ? v : -INFINITY;
-            sacc[nt][e] = v;
-            mx[e >> 1] = fmaxf(mx[e >> 1], v);
-        }
-    }
-    float alpha[2], sum[2] = {0.f, 0.f};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-        const float m_new = fmaxf(w.m[h], mx[h]);
-        alpha[h] = exp2f(w.m[h] - m_new);          // 0 on the first block (m = -inf)
-        w.m[h] = m_new;
-    }
-    // P and its bf16 split: even rows take the high part, odd rows the rest
-    const bool hi_row = (g & 1) == 0;
-    uint32_t pa[4][2];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-        float pv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            pv[e] = exp2f(sacc[nt][e] - w.m[e >> 1]);
-            sum[e >> 1] += pv[e];
-        }
-#pragma unroll
-        for (int hp = 0; hp < 2; ++hp) {
-            const float x0 = pv[2 * hp], x1 = pv[2 * hp + 1];
-            const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-            const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-            pa[nt][hp] = hi_row ? pack_bf16(h0, h1) : pack_bf16(x0 - h0, x1 - h1);
-        }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 1);
-        sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], 2);
-        w.l[h] = w.l[h] * alpha[h] + sum[h];
-    }
-#pragma unroll
-    for (int dt = 0; dt < ATT_DT; ++dt) {
-        w.o[dt][0] *= alpha[0]; w.o[dt][1] *= alpha[0];
-        w.o[dt][2] *= alpha[1]; w.o[dt][3] *= alpha[1];
-    }
-    // O += P V: k = positions (2 steps of 16), n = this warp's dimension tiles
-#pragma unroll
-    for (int dt = 0; dt < ATT_DT; ++dt) {
-        uint32_t b[4];
-        // V^T: matrices of positions (0-7 | 8-15 | 16-23 | 24-31) x dims 8 dt of this quarter
-        ldsm_x4_t(b, tile_chunk(vt, mi * 8 + r8, (dq * (D / ATT_DQ) + dt * 8) / 8));
-        mma_bf16(w.o[dt], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b[0], b[1]);
-        mma_bf16(w.o[dt], pa[2][0], pa[2][1], pa[3][0], pa[3][1], b[2], b[3]);
-    }
-}
+static_assert(KSTR == ATT_KSTR, "staged rows of the shared block routine");
+using AttWarp = AttAcc<ATT_DT>;
 
 // The attention unit of this CTA: q heads of its KV head normed, rotated and
 // split into bf16 high/low rows; the new K/V appended (by the unit holding
@@ -814,7 +694,7 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
                     }
                     named_bar(2 + j, ATT_DQ * 32);
                 }
-                attend_block_tc(kt, vt, sqa, min(KVB, u.ctx - blk * KVB), dq, lane, st);
+                attend_block_tc<ATT_DT>(kt, vt, sqa, min(KVB, u.ctx - blk * KVB), dq * ATT_DT, lane, st);
             } else if (lane == 0 && dq == 0) {
                 set_status(p.status, Q3_STATUS_BLOCK_RANGE);
             }

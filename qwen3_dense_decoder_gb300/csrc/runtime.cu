@@ -345,12 +345,15 @@ struct Round {
 
 int attention_splits(const q3_model* m, int T, int max_ctx)
 {
-    // about two 32-position blocks per warp of a split CTA; a round with many
-    // rows already fills the machine without splitting
+    // one 32-position block per warp of a split CTA when the round has few
+    // (row, KV head) units; four when the units alone fill the SMs (fewer,
+    // longer CTAs: their fixed costs -- q prologue, warp merge, split
+    // ticket -- then weigh less); a round with many rows needs no splitting
     const int nblk = (max_ctx + 31) / 32;
     const int rows = T * m->c.n_kv_heads;
     if (rows >= 8 * 152) return 1;
-    int s = (nblk + attention_blocks_per_cta() - 1) / attention_blocks_per_cta();
+    const int per_cta = attention_blocks_per_cta() * (rows >= 152 ? 4 : 1);
+    int s = (nblk + per_cta - 1) / per_cta;
     s = std::max(1, std::min({s, nblk, attention_max_splits()}));
     while (s > 1 && (size_t)T * s > m->part_rows) --s;
     return s;
