@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     const int* table = p.tables + (size_t)p.row_slot[t] * p.max_blocks;
     const int nblk = (ctx + KV_BLOCK - 1) / KV_BLOCK;
     const int bps = (nblk + p.n_splits - 1) / p.n_splits;
+    const int ns = (nblk + bps - 1) / bps;              // splits of this row that hold blocks
     const int b0 = split * bps;
     const int b1 = min(b0 + bps, nblk);
     const size_t head_elems = (size_t)KV_BLOCK * D;
@@ -133,6 +134,9 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     if (threadIdx.x == 0)
         issue_l2_prefetch(p.next, blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z),
                           gridDim.x * gridDim.y * gridDim.z);
+    // the grid is sized for the round's longest context: splits past a
+    // shorter row's blocks have nothing to do
+    if (split >= ns) return;
     // the next kernel may now be scheduled into the SM space this grid leaves
     grid_dep_launch();
     grid_dep_wait();
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
         Mg[g] = M; Lg[g] = L; Og[g] = O;
     }
     const size_t row0 = (size_t)t * p.n_q + kvh * G;
-    if (p.n_splits == 1) {
+    if (ns == 1) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const float v = Og[g] / Lg[g];
@@ -275,30 +279,30 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
                 p.part_ml[((row0 + g) * p.n_splits + split) * 2 + 1] = Lg[g];
             }
         }
-        // the last split CTA of this (row, KV head) merges every split in order
+        // the last split CTA of this (row, KV head) merges its ns splits in order
         __threadfence();
         __syncthreads();
         if (threadIdx.x == 0) s_ticket = atomicAdd(p.counters + (size_t)t * p.n_kv + kvh, 1);
         __syncthreads();
-        if (s_ticket == p.n_splits - 1) {
+        if (s_ticket == ns - 1) {
             __threadfence();
             // split maxima and sums of all G heads, fetched in parallel; the
             // staging area is free (the warp merge above is done)
             float* s_ml = s_o + AWARPS * G * D;              // [G][n_splits][2]
             float* s_w = s_ml + 2 * G * p.n_splits;          // [G][n_splits]
-            for (int i = threadIdx.x; i < G * p.n_splits; i += AWARPS * 32) {
-                const int g = i / p.n_splits, sp = i % p.n_splits;
+            for (int i = threadIdx.x; i < G * ns; i += AWARPS * 32) {
+                const int g = i / ns, sp = i % ns;
                 const float* ml = p.part_ml + ((row0 + g) * p.n_splits + sp) * 2;
-                s_ml[2 * i] = __ldcg(ml);
-                s_ml[2 * i + 1] = __ldcg(ml + 1);
+                s_ml[2 * (g * p.n_splits + sp)] = __ldcg(ml);
+                s_ml[2 * (g * p.n_splits + sp) + 1] = __ldcg(ml + 1);
             }
             __syncthreads();
             if (threadIdx.x < G) {
                 const int g = threadIdx.x;
                 float M = -INFINITY;
-                for (int sp = 0; sp < p.n_splits; ++sp) M = fmaxf(M, s_ml[2 * (g * p.n_splits + sp)]);
+                for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, s_ml[2 * (g * p.n_splits + sp)]);
                 float L = 0.f;
-                for (int sp = 0; sp < p.n_splits; ++sp) {
+                for (int sp = 0; sp < ns; ++sp) {
                     const float ms = s_ml[2 * (g * p.n_splits + sp)];
                     const float e = ms == -INFINITY ? 0.f : exp2f(ms - M);
                     s_w[g * p.n_splits + sp] = e;
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
                 const float* po = p.part_o + (row0 + g) * p.n_splits * D + d;
                 float O = 0.f;
 #pragma unroll 8
-                for (int sp = 0; sp < p.n_splits; ++sp) O = fmaf(__ldcg(po + (size_t)sp * D), s_w[g * p.n_splits + sp], O);
+                for (int sp = 0; sp < ns; ++sp) O = fmaf(__ldcg(po + (size_t)sp * D), s_w[g * p.n_splits + sp], O);
                 const float v = O / s_m[g];
                 if (p.out_f16) reinterpret_cast<__half*>(p.out)[(row0 + g) * D + d] = to_f16(v, range_bad);
                 else reinterpret_cast<float*>(p.out)[(row0 + g) * D + d] = v;

@@ -343,16 +343,21 @@ struct Round {
     int attn_grid = 0;               // its CTAs
 };
 
+#ifndef Q3_ATTN_BATCH_BPW
+#define Q3_ATTN_BATCH_BPW 8
+#endif
+
 int attention_splits(const q3_model* m, int T, int max_ctx)
 {
     // one 32-position block per warp of a split CTA when the round has few
-    // (row, KV head) units; four when the units alone fill the SMs (fewer,
-    // longer CTAs: their fixed costs -- q prologue, warp merge, split
-    // ticket -- then weigh less); a round with many rows needs no splitting
+    // (row, KV head) units; Q3_ATTN_BATCH_BPW when the units alone fill the
+    // SMs (fewer, longer CTAs: their fixed costs -- q prologue, warp merge,
+    // split ticket -- then weigh less); a round with many rows needs no
+    // splitting
     const int nblk = (max_ctx + 31) / 32;
     const int rows = T * m->c.n_kv_heads;
     if (rows >= 8 * 152) return 1;
-    const int per_cta = attention_blocks_per_cta() * (rows >= 152 ? 4 : 1);
+    const int per_cta = attention_blocks_per_cta() * (rows >= 152 ? Q3_ATTN_BATCH_BPW : 1);
     int s = (nblk + per_cta - 1) / per_cta;
     s = std::max(1, std::min({s, nblk, attention_max_splits()}));
     while (s > 1 && (size_t)T * s > m->part_rows) --s;
