@@ -159,6 +159,18 @@ int q3_session_set_block_table(q3_session* s, const int32_t* phys_ids, int n);
 int q3_session_eval(q3_session* s, const int32_t* tokens_dev, int n,
                     float* logits_dev, int32_t* argmax_dev);
 
+/* One round of n tokens for one session, returning the logits of its last
+ * n_logits rows (1 <= n_logits <= n; n_logits == n scores every prompt row)
+ * ("Kipp Roadmap", status v0.0.2: multi-logit evaluation, kipp_session_eval_n).
+ * logits_dev: f32 [n_logits][vocab], row i the logits after token
+ * n - n_logits + i; argmax_dev: int32 [n_logits] or NULL.  Rounds longer
+ * than max_round_tokens are split as in q3_session_eval; the result does not
+ * depend on the split.  n_logits == 1 is q3_session_eval.  Asynchronous on
+ * the model's stream.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CTX_OVERFLOW,
+ * Q3_ERR_POOL_EXHAUSTED, Q3_ERR_CUDA, Q3_ERR_POISONED. */
+int q3_session_eval_n(q3_session* s, const int32_t* tokens_dev, int n, int n_logits, float* logits_dev,
+                      int32_t* argmax_dev);
+
 /* One round over ns distinct sessions of one pool ("Kipp Roadmap", status
  * v0.0.2, kipp_eval_batch): session i appends n[i] tokens.  tokens_dev:
  * int32 device, the rounds concatenated in session order (sum n[i] tokens,

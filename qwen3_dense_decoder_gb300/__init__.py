@@ -88,6 +88,7 @@ def lib():
         L.q3_model_profile_reset.argtypes = [vp]
         L.q3_model_profile_read.argtypes = [vp, i, C.POINTER(C.c_double), C.POINTER(C.c_int64)]
         L.q3_op_matvec.argtypes = [vp, vp, vp, i, i, vp, vp]
+        L.q3_session_eval_n.argtypes = [vp, vp, i, i, vp, vp]
         L.q3_op_prefill_attention.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp, i, vp]
         L.q3_model_set_fused_decode.argtypes = [vp, i]
         L.q3_model_fused_decode.argtypes = [vp]
@@ -327,6 +328,15 @@ class Session:
         import numpy as np
         a = np.ascontiguousarray(ids, np.int32)
         _check(lib().q3_session_set_block_table(self.h, a.ctypes.data_as(C.c_void_p), a.size))
+
+    def eval_n(self, tokens: torch.Tensor, n_logits: int, logits: torch.Tensor,
+               argmax: torch.Tensor | None = None) -> None:
+        """Append a round of tokens and write the logits of its last n_logits
+        rows: logits [n_logits, vocab] f32 device, argmax [n_logits] int32."""
+        assert tokens.is_cuda and tokens.dtype == torch.int32 and tokens.is_contiguous()
+        assert logits.is_contiguous() and logits.numel() >= n_logits * logits.shape[-1]
+        _check(lib().q3_session_eval_n(self.h, _ptr(tokens), tokens.numel(), n_logits, _ptr(logits),
+                                       _ptr(argmax)))
 
     def eval(self, tokens: torch.Tensor, logits: torch.Tensor,
              argmax: torch.Tensor | None = None) -> None:

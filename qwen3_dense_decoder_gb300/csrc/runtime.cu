@@ -336,6 +336,7 @@ struct Round {
     int32_t* argmax = nullptr;
     q3_pool* pool = nullptr;
     int last_row = 0;                // host copy when ns == 1
+    int n_out = 1;                   // rows with logits: one per session, or (ns == 1) the last n_out
     int max_ctx = 0;                 // largest context of the round
     bool decode = false;             // every session appends exactly one token
     int n_tiles = 0;                 // query tiles (prefill attention)
@@ -804,23 +805,25 @@ int run_round(q3_model* m, const Round& r)
         }
     }
 
-    // ---- final norm + lm_head (+ argmax), last row of each session
-    if (r.ns == 1) {
+    // ---- final norm + lm_head (+ argmax): the last row of each session, or
+    // the last n_out rows of a one-session round
+    const int n_out = r.ns == 1 ? r.n_out : r.ns;
+    if (n_out == 1) {
         const void* w[1] = {m->lm_head};
         const int rows[1] = {c.vocab};
         if ((rc = gemv(m, 1, w, nullptr, rows, 0, H, m->x + (size_t)r.last_row * H, m->final_norm,
                        EPI_STORE_F32, r.logits, r.argmax)))
             return rc;
     } else {
-        if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, last_rows, r.ns, H, m->final_norm, c.rms_eps,
+        if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, last_rows, n_out, H, m->final_norm, c.rms_eps,
                                               m->hfin, m->status); }), "final norm")))
             return rc;
-        if ((rc = gemm(m, &m->lm_map, nullptr, nullptr, c.vocab / 128, c.vocab / 128, 0, c.vocab, r.ns, H,
+        if ((rc = gemm(m, &m->lm_map, nullptr, nullptr, c.vocab / 128, c.vocab / 128, 0, c.vocab, n_out, H,
                        m->hfin, EPI_STORE_F32, r.logits, c.vocab)))
             return rc;
     }
-    if (r.ns > 1 && r.argmax &&
-        (rc = m->check(run(Q3_K_OTHER, [&] { return launch_argmax(L, r.logits, r.ns, c.vocab, r.argmax); }), "argmax")))
+    if (n_out > 1 && r.argmax &&
+        (rc = m->check(run(Q3_K_OTHER, [&] { return launch_argmax(L, r.logits, n_out, c.vocab, r.argmax); }), "argmax")))
         return rc;
     return Q3_OK;
 }
@@ -859,7 +862,7 @@ int upload_table(q3_session* s)
 }
 
 int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n, float* logits,
-               int32_t* argmax)
+               int32_t* argmax, int n_out = 1)
 {
     q3_pool* pool = S[0]->pool;
     q3_model* m = pool->m;
@@ -870,6 +873,9 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
     r.tokens = tokens;
     r.logits = logits;
     r.argmax = argmax;
+    r.n_out = n_out;
+    if (n_out < 1 || (ns > 1 && n_out != 1) || (ns == 1 && n_out > n[0]))
+        return fail(Q3_ERR_INVALID_ARG, "logit rows %d outside [1, round rows]", n_out);
     for (int i = 0; i < ns; ++i) {
         if (S[i]->pool != pool) return fail(Q3_ERR_INVALID_ARG, "sessions of different pools");
         if (n[i] < 1) return fail(Q3_ERR_INVALID_ARG, "empty round for session %d", i);
@@ -898,6 +904,9 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
         }
         h[2 * m->max_rows + i] = t - 1;
     }
+    // a one-session round with n_out logit rows: its last n_out rows, in order
+    if (ns == 1 && n_out > 1)
+        for (int j = 0; j < n_out; ++j) h[2 * m->max_rows + j] = n[0] - n_out + j;
     // Query tiles of the prefill attention, never spanning two sessions,
     // longest context first: 64 rows for the mma.sync kernel, 128 / G for the
     // tcgen05 kernel, which also takes a per-CTA item list built here by
@@ -1344,6 +1353,32 @@ int q3_session_eval(q3_session* s, const int32_t* tokens_dev, int n, float* logi
     for (int off = 0; off < n; off += m->max_rows) {
         const int k = std::min(m->max_rows, n - off);
         int rc = eval_round(&s, 1, tokens_dev + off, &k, logits_dev, argmax_dev);
+        if (rc) return rc;
+    }
+    return Q3_OK;
+}
+
+int q3_session_eval_n(q3_session* s, const int32_t* tokens_dev, int n, int n_logits, float* logits_dev,
+                      int32_t* argmax_dev)
+{
+    if (!s || !tokens_dev || !logits_dev || n < 1 || n_logits < 1 || n_logits > n)
+        return fail(Q3_ERR_INVALID_ARG, "eval_n: bad argument");
+    q3_model* m = s->pool->m;
+    if (s->pos + n > m->c.max_ctx)
+        return fail(Q3_ERR_CTX_OVERFLOW, "position %d + %d exceeds max_ctx %d", s->pos, n, m->c.max_ctx);
+    // rounds of at most max_round_tokens rows; the last n_logits rows of the
+    // call are a suffix of its last rounds
+    const int first = n - n_logits;
+    for (int off = 0; off < n; off += m->max_rows) {
+        const int k = std::min(m->max_rows, n - off);
+        const int lo = std::max(off, first);
+        const int rows = off + k - lo;                          // this round's logit rows (a suffix)
+        int rc;
+        if (rows >= 1)
+            rc = eval_round(&s, 1, tokens_dev + off, &k, logits_dev + (size_t)(lo - first) * m->c.vocab,
+                            argmax_dev ? argmax_dev + (lo - first) : nullptr, rows);
+        else
+            rc = eval_round(&s, 1, tokens_dev + off, &k, logits_dev, nullptr, 1);   // overwritten later
         if (rc) return rc;
     }
     return Q3_OK;
