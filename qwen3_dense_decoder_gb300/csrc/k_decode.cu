@@ -102,6 +102,10 @@ __host__ __device__ inline int sx_floats(int H, int F, int n_q, int n_kv, int n_
     return (k + 3) & ~3;
 }
 
+// per-layer pointer table in shared memory: 7 weight planes, 7 Q8_0 scale
+// planes, then the attention, q, k and FFN norm gains
+constexpr int WP_N = 18, WP_ATTN_NORM = 14, WP_Q_NORM = 15, WP_K_NORM = 16, WP_FFN_NORM = 17;
+
 struct Layout {
     size_t sx, red, bars, misc, ptrs, total;
 };
@@ -114,7 +118,7 @@ __host__ __device__ inline Layout make_layout(int n_slots, int sxf, int n_layers
     L.misc = L.bars + (size_t)(3 * n_slots + 1) * 8;
     L.ptrs = L.misc + (size_t)(3 * NCW + 4 + MAX_OWN) * 4;
     L.ptrs = (L.ptrs + 15) & ~(size_t)15;
-    L.total = L.ptrs + (size_t)n_layers * 14 * 8;     // per layer: 7 weight planes, 7 scale planes
+    L.total = L.ptrs + (size_t)n_layers * WP_N * 8;   // per layer: weight planes, scale planes, norm gains
     return L;
 }
 
@@ -248,7 +252,7 @@ Q3_DEV WStage weight_stage(const DecodeArgs& p, const Smem& sm, int l, int kind)
         s.K = p.H;
         M = p.V;
     } else {
-        const void* const* lp = sm.wp + (size_t)l * 14;
+        const void* const* lp = sm.wp + (size_t)l * WP_N;
         s.q8 = p.q8;
         auto set = [&](int i, int proj, int rows) {
             s.w[i] = static_cast<const uint8_t*>(lp[proj]);
@@ -620,13 +624,15 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
     const int last_blk = u.nblk - 1;
     const bool mine = u.active && u.b0 <= last_blk && last_blk < u.b1;
     const float2* rope_row = p.rope + (size_t)u.pos * (D / 2);
-    const DecodeLayer& L = p.layers[l];
+    const void* const* lp = sm.wp + (size_t)l * WP_N;
+    const bf16* q_gain = static_cast<const bf16*>(lp[WP_Q_NORM]);
+    const bf16* k_gain = static_cast<const bf16*>(lp[WP_K_NORM]);
     const float qscale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
     if (u.active) {
         if (warp < G) {
             const float4 v = __ldcg(reinterpret_cast<const float4*>(p.qkv + (u.kvh * G + warp) * D + lane * 4));
             float y[4] = {v.x, v.y, v.z, v.w};
-            head_norm_rope(y, L.q_norm, rope_row, p.eps, lane);
+            head_norm_rope(y, q_gain, rope_row, p.eps, lane);
             float hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -643,7 +649,7 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
             const float4 v = __ldcg(reinterpret_cast<const float4*>(
                 p.qkv + (p.n_q + (is_k ? 0 : p.n_kv) + u.kvh) * D + lane * 4));
             float y[4] = {v.x, v.y, v.z, v.w};
-            if (is_k) head_norm_rope(y, L.k_norm, rope_row, p.eps, lane);
+            if (is_k) head_norm_rope(y, k_gain, rope_row, p.eps, lane);
             const uint2 packed = make_uint2(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]));
             *reinterpret_cast<uint2*>(snew + (is_k ? 0 : D) + lane * 4) = packed;
             const int phys = table[last_blk];
@@ -819,8 +825,8 @@ Q3_DEV void consumer(const DecodeArgs& p, const Unit& u, const int* table, const
     int epi = 0;                                   // matvec stages the epilogue warp has closed
     const int qw = p.n_q * D;
     for (int l = 0; l < p.n_layers; ++l) {
-        const DecodeLayer& L = p.layers[l];
-        stage_x(sm, p.x, l == 0 ? erow : nullptr, p.H, L.attn_norm, p.eps);
+        const void* const* lp = sm.wp + (size_t)l * WP_N;
+        stage_x(sm, p.x, l == 0 ? erow : nullptr, p.H, static_cast<const bf16*>(lp[WP_ATTN_NORM]), p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_QKV), sm, it, warp, lane, p);
         if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
         consume_attention(p, l, u, table, sm, it, warp, lane);
@@ -828,7 +834,7 @@ Q3_DEV void consumer(const DecodeArgs& p, const Unit& u, const int* table, const
         stage_x(sm, p.att, nullptr, qw, nullptr, p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_O), sm, it, warp, lane, p);
         if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
-        stage_x(sm, p.x, nullptr, p.H, L.ffn_norm, p.eps);
+        stage_x(sm, p.x, nullptr, p.H, static_cast<const bf16*>(lp[WP_FFN_NORM]), p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_GU), sm, it, warp, lane, p);
         if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
         stage_x(sm, p.ffn, nullptr, p.F, nullptr, p.eps);
@@ -961,11 +967,16 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
     sm.ticket = const_cast<int*>(sm.abort) + 1;
     sm.xres = reinterpret_cast<float*>(sm.ticket + 3);
     sm.wp = reinterpret_cast<const void**>(smem + lay.ptrs);
-    // the per-layer weight pointers, read on every stage by producer, consumers and epilogue
-    for (int i = threadIdx.x; i < p.n_layers * 14; i += blockDim.x) {
-        const DecodeLayer& L = p.layers[i / 14];
-        const int k = i % 14;
-        sm.wp[i] = k < 7 ? L.w[k] : static_cast<const void*>(L.sc[k - 7]);
+    // the per-layer weight and gain pointers, read on every stage by producer, consumers and epilogue
+    for (int i = threadIdx.x; i < p.n_layers * WP_N; i += blockDim.x) {
+        const DecodeLayer& L = p.layers[i / WP_N];
+        const int k = i % WP_N;
+        const void* v = k < 7 ? L.w[k] : k < 14 ? static_cast<const void*>(L.sc[k - 7])
+                      : k == WP_ATTN_NORM ? static_cast<const void*>(L.attn_norm)
+                      : k == WP_Q_NORM ? static_cast<const void*>(L.q_norm)
+                      : k == WP_K_NORM ? static_cast<const void*>(L.k_norm)
+                      : static_cast<const void*>(L.ffn_norm);
+        sm.wp[i] = v;
     }
 
     if (threadIdx.x == 0) {
