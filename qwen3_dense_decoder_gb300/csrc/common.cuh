@@ -74,16 +74,22 @@ Q3_DEV float warp_allsum(float v) {
 
 Q3_DEV void head_norm_rope(float (&y)[4], const __nv_bfloat16* gain, const float2* rope_row,
                            float eps, int lane) {
+    // gain and cos/sin loads go out before the reduction that precedes their use
+    const uint2 g4 = *reinterpret_cast<const uint2*>(gain + lane * 4);
+    const float4* cs = reinterpret_cast<const float4*>(rope_row + (lane & 15) * 4);
+    const float4 c01 = cs[0], c23 = cs[1];
+    const float gv[4] = {bf16lo(g4.x), bf16hi(g4.x), bf16lo(g4.y), bf16hi(g4.y)};
+    const float2 cv[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
+                          make_float2(c23.z, c23.w)};
     const float ss = warp_allsum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
     const float r = 1.0f / sqrtf(ss / 128.0f + eps);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) y[e] = y[e] * r * __bfloat162float(gain[lane * 4 + e]);
-    const float2* cs = rope_row + (lane & 15) * 4;
+    for (int e = 0; e < 4; ++e) y[e] = y[e] * r * gv[e];
     float out[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const float z = __shfl_xor_sync(0xffffffffu, y[e], 16);
-        const float2 c = cs[e];
+        const float2 c = cv[e];
         out[e] = lane < 16 ? y[e] * c.x - z * c.y      // first half: x1 cos - x2 sin
                            : y[e] * c.x + z * c.y;     // second half: x2 cos + x1 sin
     }
