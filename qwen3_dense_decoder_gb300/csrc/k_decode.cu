@@ -115,7 +115,7 @@ __host__ __device__ inline Layout make_layout(int n_slots, int sxf, int n_layers
     L.sx = (size_t)n_slots * SLOT;
     L.red = L.sx + (size_t)sxf * 4;
     L.bars = L.red + (size_t)n_slots * RED * 4;
-    L.misc = L.bars + (size_t)(3 * n_slots + 1) * 8;
+    L.misc = L.bars + (size_t)(3 * n_slots) * 8;
     L.ptrs = L.misc + (size_t)(3 * NCW + 4 + MAX_OWN) * 4;
     L.ptrs = (L.ptrs + 15) & ~(size_t)15;
     L.total = L.ptrs + (size_t)n_layers * WP_N * 8;   // per layer: weight planes, scale planes, norm gains
@@ -129,7 +129,6 @@ struct Smem {
     uint64_t* full;     // [n_slots] tile landed (tx bytes)
     uint64_t* empty;    // [n_slots] tile consumed: NCW readers + the epilogue warp
     uint64_t* redf;     // [n_slots] all NCW row partials written
-    uint64_t* epi_done; // the epilogue warp finished a matvec stage
     float* ss;          // [NCW]
     float* bv;          // [NCW]
     int* bi;            // [NCW]
@@ -211,15 +210,15 @@ Q3_DEV bool wait_bar(uint64_t* bar, uint32_t parity, const Smem& sm, int* status
     }
 }
 
-// Grid barrier among the consumer warps of all CTAs; after a matvec stage
-// (epi_phase >= 0) it first waits for this CTA's epilogue warp to finish the
-// stage, whose outputs the release then publishes.  Returns false, the same
-// on every consumer thread, when the step is aborting.
-Q3_DEV bool grid_sync(const DecodeArgs& p, const Smem& sm, unsigned long long target, int epi_phase) {
+// Grid barrier among the consumer warps of all CTAs.  After a matvec stage
+// (by_epilogue) this CTA's arrival is the epilogue warp's: it releases the
+// stage's outputs as soon as it has written them; after the attention stage
+// the consumers' thread 0 releases theirs.  Returns false, the same on every
+// consumer thread, when the step is aborting.
+Q3_DEV bool grid_sync(const DecodeArgs& p, const Smem& sm, unsigned long long target, bool by_epilogue) {
     consumer_sync();
-    if (threadIdx.x == 0 && epi_phase >= 0 && !*sm.abort) wait_bar(sm.epi_done, epi_phase & 1, sm, p.status);
     if (threadIdx.x == 0 && !*sm.abort) {
-        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" :: "l"(p.bar) : "memory");
+        if (!by_epilogue) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" :: "l"(p.bar) : "memory");
         const uint64_t t0 = global_ns();
         for (uint32_t n = 1; ld_acquire_u64(p.bar) < target; ++n) {
             if ((n & 63) == 0 && global_ns() - t0 > Q3_WAIT_LIMIT_NS) {
@@ -822,24 +821,23 @@ Q3_DEV void consumer(const DecodeArgs& p, const Unit& u, const int* table, const
     const bf16* erow = p.embed + (size_t)checked_token(p) * p.H;
     uint32_t it = 0;
     unsigned long long target = p.bar_base;
-    int epi = 0;                                   // matvec stages the epilogue warp has closed
     const int qw = p.n_q * D;
     for (int l = 0; l < p.n_layers; ++l) {
         const void* const* lp = sm.wp + (size_t)l * WP_N;
         stage_x(sm, p.x, l == 0 ? erow : nullptr, p.H, static_cast<const bf16*>(lp[WP_ATTN_NORM]), p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_QKV), sm, it, warp, lane, p);
-        if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
+        if (!grid_sync(p, sm, target += gridDim.x, true)) return;
         consume_attention(p, l, u, table, sm, it, warp, lane);
-        if (!grid_sync(p, sm, target += gridDim.x, -1)) return;
+        if (!grid_sync(p, sm, target += gridDim.x, false)) return;
         stage_x(sm, p.att, nullptr, qw, nullptr, p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_O), sm, it, warp, lane, p);
-        if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
+        if (!grid_sync(p, sm, target += gridDim.x, true)) return;
         stage_x(sm, p.x, nullptr, p.H, static_cast<const bf16*>(lp[WP_FFN_NORM]), p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_GU), sm, it, warp, lane, p);
-        if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
+        if (!grid_sync(p, sm, target += gridDim.x, true)) return;
         stage_x(sm, p.ffn, nullptr, p.F, nullptr, p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_DOWN), sm, it, warp, lane, p);
-        if (!grid_sync(p, sm, target += gridDim.x, epi++)) return;
+        if (!grid_sync(p, sm, target += gridDim.x, true)) return;
     }
     stage_x(sm, p.x, nullptr, p.H, p.final_norm, p.eps);
     consume_weights<false>(weight_stage(p, sm, 0, ST_LM), sm, it, warp, lane, p);
@@ -879,9 +877,10 @@ Q3_DEV void epilogue(const DecodeArgs& p, const Unit& u, const Smem& sm, int lan
     float best = -INFINITY;
     int best_i = 0x7fffffff;
     bool ok = true;
+    // a matvec stage's outputs are written: this CTA's grid-barrier arrival
     auto closed = [&]() {
         __syncwarp();
-        if (lane == 0) mbar_arrive(sm.epi_done);
+        if (lane == 0) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" :: "l"(p.bar) : "memory");
     };
     for (int l = 0; l < p.n_layers && ok; ++l) {
         ok = epilogue_stage(p, weight_stage(p, sm, l, ST_QKV), ST_QKV, sm, it, lane, p.qkv, best, best_i);
@@ -959,7 +958,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
     sm.full = reinterpret_cast<uint64_t*>(smem + lay.bars);
     sm.empty = sm.full + p.n_slots;
     sm.redf = sm.empty + p.n_slots;
-    sm.epi_done = sm.redf + p.n_slots;
     sm.ss = reinterpret_cast<float*>(smem + lay.misc);
     sm.bv = sm.ss + NCW;
     sm.bi = reinterpret_cast<int*>(sm.bv + NCW);
@@ -985,7 +983,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
             mbar_init(&sm.empty[s], NCW + 1);
             mbar_init(&sm.redf[s], NCW);
         }
-        mbar_init(sm.epi_done, 1);
         *sm.abort = 0;
         fence_barrier_init();
     }
