@@ -43,7 +43,7 @@ METRIC = "Qwen3-4B-shape decode tok/s (% HBM roofline); prefill tok/s (% BF16 TC
 # DRAM bytes read + written by one fused decode step over its algorithmic
 # bytes, from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
 # 4-layer case; to be retaken whenever the kernel changes
-DECODE_STEP_TRAFFIC_RATIO = (1.6196e9 + 2.99e6) / 1.6189e9
+DECODE_STEP_TRAFFIC_RATIO = (1.619629056e9 + 3.240704e6) / 1.6189e9
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
