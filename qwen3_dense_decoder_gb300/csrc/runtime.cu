@@ -350,15 +350,21 @@ struct Round {
 
 int attention_splits(const q3_model* m, int T, int max_ctx)
 {
-    // one 32-position block per warp of a split CTA when the round has few
-    // (row, KV head) units; Q3_ATTN_BATCH_BPW when the units alone fill the
-    // SMs (fewer, longer CTAs: their fixed costs -- q prologue, warp merge,
-    // split ticket -- then weigh less); a round with many rows needs no
-    // splitting
+    // Blocks per split CTA from the round's work: one block per warp while
+    // the (row, KV head) units' split CTAs (the longest context bounds every
+    // row) fit in about one wave of three CTAs per SM, doubling up to
+    // Q3_ATTN_BATCH_BPW per warp until they do (fewer, longer CTAs, whose
+    // fixed costs -- q prologue, warp merge, split ticket -- then weigh
+    // less).  A round with many rows needs no splitting.
     const int nblk = (max_ctx + 31) / 32;
     const int rows = T * m->c.n_kv_heads;
     if (rows >= 8 * 152) return 1;
-    const int per_cta = attention_blocks_per_cta() * (rows >= 152 ? Q3_ATTN_BATCH_BPW : 1);
+    int bpw = 1;
+    while (bpw < Q3_ATTN_BATCH_BPW &&
+           (long long)rows * ((nblk + attention_blocks_per_cta() * bpw - 1) / (attention_blocks_per_cta() * bpw)) >
+               3LL * 152)
+        bpw *= 2;
+    const int per_cta = attention_blocks_per_cta() * bpw;
     int s = (nblk + per_cta - 1) / per_cta;
     s = std::max(1, std::min({s, nblk, attention_max_splits()}));
     while (s > 1 && (size_t)T * s > m->part_rows) --s;
