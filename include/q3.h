@@ -117,8 +117,9 @@ typedef struct q3_weights {
  * tensor cores with fp16 operands (kind::f16 takes A and B of one type and
  * fp16 activations keep 3 more mantissa bits than bf16): the library keeps
  * an fp16 copy of the BF16 projections and lm_head (exact except for
- * |w| < 2^-17, whose rounding is below 2^-25), or dequantises Q8_0 blocks to
- * fp16.  Weights beyond the fp16 range make creation fail with
+ * |w| < 2^-17, whose rounding is below 2^-25), or of the Q8_0 projections
+ * dequantised once (d * q rounded to fp16; 2 bytes per weight of device
+ * memory beside the 1.0625 of the planes).  Weights beyond the fp16 range make creation fail with
  * Q3_ERR_INVALID_ARG; an activation beyond it is reported by q3_sync as
  * Q3_ERR_DEVICE_CHECK (Q3_STATUS_F16_RANGE).  max_round_tokens bounds the rows of one round (the activation
  * scratch, owned by the model, is sized for it; longer q3_session_eval rounds

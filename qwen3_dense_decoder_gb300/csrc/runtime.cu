@@ -146,8 +146,8 @@ struct q3_model {
     size_t part_rows = 0;     // (row, split) pairs the partial buffers hold
     float* ws = nullptr;
     size_t ws_elems = 0;
-    f16* deq = nullptr;       // Q8_0 prefill: dequantised projection(s)
-    std::vector<std::vector<f16*>> w16;   // [layer][proj] fp16 copies (BF16 scheme)
+    std::vector<std::vector<f16*>> w16;   // [layer][proj] fp16 copies for the tensor cores
+                                          // (of the BF16 weights, or the dequantised Q8_0 planes)
     f16* lm16 = nullptr;      // fp16 copy of the lm_head for batched rows
     int* meta = nullptr;      // [5][max_rows]: row_pos, row_slot, last_row, tile_row0, tile_rows,
                               // then the tcgen05 attention schedule: [SCHED_GRID + 1] starts, items
@@ -180,9 +180,7 @@ struct q3_model {
     std::vector<char> stage_used;
 
     std::vector<LayerMaps> maps;
-    LayerMaps maps_dummy{};
     CUtensorMap lm_map{};
-    CUtensorMap deq_qkv{}, deq_o{}, deq_g{}, deq_u{}, deq_d{};
     std::map<std::tuple<const void*, int, int>, CUtensorMap> act_maps;
 
     // per-launch event timing (q3_model_profile)
@@ -636,7 +634,7 @@ int run_round(q3_model* m, const Round& r)
 
     for (int l = 0; l < c.n_layers; ++l) {
         const q3_layer_weights& W = m->layers[l];
-        const LayerMaps& Mp = q8 ? m->maps_dummy : m->maps[l];
+        const LayerMaps& Mp = m->maps[l];
         const bf16* attn_norm = static_cast<const bf16*>(W.attn_norm);
         const bf16* ffn_norm = static_cast<const bf16*>(W.ffn_norm);
 
@@ -658,21 +656,8 @@ int run_round(q3_model* m, const Round& r)
             if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->ha, m->status); }),
                                "rmsnorm")))
                 return rc;
-            if (q8) {
-                size_t off = 0;
-                for (int i = 0; i < 3; ++i) {
-                    const int rows = i == 0 ? m->qw : m->kvw;
-                    if ((rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_Q + i].qs, m->q8[l][P_Q + i].sc,
-                                                         (int64_t)rows * H, m->deq + off); }), "dequant")))
-                        return rc;
-                    off += (size_t)rows * H;
-                }
-                rc = gemm(m, &m->deq_qkv, nullptr, nullptr, m->qkvw / 128, m->qkvw / 128, 0, m->qkvw,
-                          T, H, m->ha, EPI_STORE_F32, m->qkv, m->qkvw);
-            } else {
-                rc = gemm(m, &Mp.m[P_Q], &Mp.m[P_K], &Mp.m[P_V], m->qw / 128, (m->qw + m->kvw) / 128, 0,
-                          m->qkvw, T, H, m->ha, EPI_STORE_F32, m->qkv, m->qkvw);
-            }
+            rc = gemm(m, &Mp.m[P_Q], &Mp.m[P_K], &Mp.m[P_V], m->qw / 128, (m->qw + m->kvw) / 128, 0,
+                      m->qkvw, T, H, m->ha, EPI_STORE_F32, m->qkv, m->qkvw);
             if (rc) return rc;
         }
 
@@ -745,16 +730,8 @@ int run_round(q3_model* m, const Round& r)
                            nullptr, &nx)))
                 return rc;
         } else {
-            if (q8) {
-                if ((rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_O].qs, m->q8[l][P_O].sc,
-                                                     (int64_t)H * m->qw, m->deq); }), "dequant")))
-                    return rc;
-                rc = gemm(m, &m->deq_o, nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
-                          EPI_ADD_F32, m->x, H);
-            } else {
-                rc = gemm(m, &Mp.m[P_O], nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
-                          EPI_ADD_F32, m->x, H);
-            }
+            rc = gemm(m, &Mp.m[P_O], nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
+                      EPI_ADD_F32, m->x, H);
             if (rc) return rc;
         }
 
@@ -784,29 +761,11 @@ int run_round(q3_model* m, const Round& r)
             if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->ha, m->status); }),
                                "rmsnorm")))
                 return rc;
-            if (q8) {
-                if ((rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_G].qs, m->q8[l][P_G].sc,
-                                                     (int64_t)F * H, m->deq); }), "dequant")) ||
-                    (rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_U].qs, m->q8[l][P_U].sc,
-                                                     (int64_t)F * H, m->deq + (size_t)F * H); }), "dequant")))
-                    return rc;
-                rc = gemm(m, &m->deq_g, &m->deq_u, nullptr, 0, 0, 1, 2 * F, T, H, m->ha, EPI_SWIGLU_F16,
-                          m->s, F);
-            } else {
-                rc = gemm(m, &Mp.m[P_G], &Mp.m[P_U], nullptr, 0, 0, 1, 2 * F, T, H, m->ha,
-                          EPI_SWIGLU_F16, m->s, F);
-            }
+            rc = gemm(m, &Mp.m[P_G], &Mp.m[P_U], nullptr, 0, 0, 1, 2 * F, T, H, m->ha,
+                      EPI_SWIGLU_F16, m->s, F);
             if (rc) return rc;
-            if (q8) {
-                if ((rc = m->check(run(Q3_K_OTHER, [&] { return launch_q8_to_f16(L, m->q8[l][P_D].qs, m->q8[l][P_D].sc,
-                                                     (int64_t)H * F, m->deq); }), "dequant")))
-                    return rc;
-                rc = gemm(m, &m->deq_d, nullptr, nullptr, H / 128, H / 128, 0, H, T, F, m->s, EPI_ADD_F32,
-                          m->x, H);
-            } else {
-                rc = gemm(m, &Mp.m[P_D], nullptr, nullptr, H / 128, H / 128, 0, H, T, F, m->s, EPI_ADD_F32,
-                          m->x, H);
-            }
+            rc = gemm(m, &Mp.m[P_D], nullptr, nullptr, H / 128, H / 128, 0, H, T, F, m->s, EPI_ADD_F32,
+                      m->x, H);
             if (rc) return rc;
         }
     }
@@ -1181,13 +1140,25 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
                     return bad(Q3_ERR_CUDA, "Q8_0 plane derivation failed");
             }
         }
-        size_t deq = std::max({(size_t)m->qkvw * H, (size_t)H * m->qw, (size_t)2 * F * H, (size_t)H * F});
-        m->deq = static_cast<f16*>(A(sizeof(f16) * deq));
-        if (!ok) return bad(Q3_ERR_OOM, "device allocation failed");
-        if (!tmap_f16(&m->deq_qkv, m->deq, m->qkvw, H, 128) || !tmap_f16(&m->deq_o, m->deq, H, m->qw, 128) ||
-            !tmap_f16(&m->deq_g, m->deq, F, H, 64) || !tmap_f16(&m->deq_u, m->deq + (size_t)F * H, F, H, 64) ||
-            !tmap_f16(&m->deq_d, m->deq, H, F, 128))
-            return bad(Q3_ERR_CUDA, "tensor map encoding failed");
+        // fp16 copies of the dequantised projections for the tensor-core path
+        // (prefill and batched rounds), made once: d * q rounded to fp16
+        m->maps.resize(c.n_layers);
+        m->w16.resize(c.n_layers);
+        const Launch L0{m->stream, false, nullptr};
+        for (int l = 0; l < c.n_layers && ok; ++l) {
+            m->w16[l].resize(N_PROJ);
+            for (int p = 0; p < N_PROJ; ++p) {
+                const size_t n = (size_t)proj_rows[p] * proj_cols[p];
+                f16* d = static_cast<f16*>(A(n * sizeof(f16)));
+                if (!ok) break;
+                m->w16[l][p] = d;
+                if (launch_q8_to_f16(L0, m->q8[l][p].qs, m->q8[l][p].sc, (int64_t)n, d) != cudaSuccess)
+                    return bad(Q3_ERR_CUDA, "Q8_0 dequantisation failed");
+                const uint32_t box = (p == P_G || p == P_U) ? 64 : 128;
+                if (!tmap_f16(&m->maps[l].m[p], d, proj_rows[p], proj_cols[p], box))
+                    return bad(Q3_ERR_CUDA, "tensor map encoding failed");
+            }
+        }
     } else {
         // fp16 copies of the projections for the tensor-core path
         m->maps.resize(c.n_layers);
