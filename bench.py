@@ -69,7 +69,8 @@ def parse():
     ap.add_argument("--shapes", nargs="*", default=None,
                     choices=("0.6b", "8b-q8_0", "14b"),
                     help="measure the other named shapes instead (one JSON line each; all three if none given)")
-    ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill"), default=None,
+    ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill", "attn-decode-b32"),
+                    default=None,
                     help="run only a small case sized for an ncu capture (a few GB on the device) and exit")
     return ap.parse_args()
 
@@ -97,6 +98,27 @@ def ncu_case(name: str):
         ses.eval(torch.tensor(synthetic.make_tokens(2048, s.vocab, 7), device="cuda"), lg, tok)
         for _ in range(6):
             ses.eval(tok, lg, tok)
+        m.sync()
+    elif name == "attn-decode-b32":
+        # batch-32 decode of the Qwen3-4B shape cut to 2 layers: 32 sessions
+        # with prompts U[64, 2048] (the bench's lengths), then 4 decode rounds
+        s = synthetic.SHAPES["4b"].replace(n_layers=2)
+        st = torch.cuda.Stream()
+        torch.cuda.set_stream(st)
+        w = synthetic.make_weights(s, seed=1234, device="cuda")
+        B = 32
+        m = q3.Model(s, w, max_ctx=2400, max_round_tokens=2048, stream=st)
+        pool = m.pool(B * 75 + 8, B + 2)
+        lg = torch.empty(B, s.vocab, device="cuda")
+        am = torch.zeros(B, dtype=torch.int32, device="cuda")
+        lens = synthetic.make_prompt_lengths(B, 64, 2048, seed=11)
+        ss = [pool.session() for _ in range(B)]
+        for i, x in enumerate(ss):
+            x.eval(torch.tensor(synthetic.make_tokens(int(lens[i]), s.vocab, seed=100 + i), device="cuda"),
+                   lg[0], am[i:i + 1])
+        toks = am.clone()
+        for _ in range(4):
+            m.eval_batch(ss, toks, [1] * B, lg, toks)
         m.sync()
     elif name == "attn-prefill":
         # one layer's prefill attention of a 2,048-token round of the Qwen3-4B
