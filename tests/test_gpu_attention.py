@@ -65,6 +65,7 @@ CASES = [
     (40, 8, 0, 260), (40, 8, 77, 50),      # G = 5
     (16, 8, 0, 300), (16, 8, 31, 97),      # G = 2
     (8, 8, 0, 200),                        # G = 1
+    (40, 8, 10000, 64),                    # a late chunk of a long prefill (the 14B shape's heads)
 ]
 
 

@@ -106,6 +106,35 @@ def test_batched_equals_isolated(tiny_pair):
         g.close()
 
 
+def test_batched_decode_over_long_unequal_contexts():
+    # three sessions of 300, 1,700 and 3,100 positions decode together: the
+    # attention's split count follows the longest row, shorter rows leave
+    # splits empty, and each row's splits merge in order
+    pair = Pair(TINY, seed=131, max_ctx=3200, max_round_tokens=256, n_blocks=220, max_sessions=4)
+    lens = [300, 1700, 3100]
+    perm = synthetic.make_block_permutation(220, seed=140)
+    tables = [perm[0:60], perm[60:120], None]                 # disjoint; the third from the allocator
+    gs, os_, nxt = [], [], []
+    for i, n in enumerate(lens):
+        g, o = pair.sessions(table=tables[i])
+        toks = synthetic.make_tokens(n, TINY.vocab, seed=150 + i)
+        for a in range(0, n, 256):
+            got, ref, _ = pair.eval(g, o, toks[a:a + 256])
+        assert check_row(got, ref).ok, i
+        gs.append(g)
+        os_.append(o)
+        nxt.append(int(np.argmax(ref)))
+    for step in range(4):
+        got, ref, am = pair.eval_batch(gs, os_, [[t] for t in nxt])
+        for i in range(3):
+            c = check_row(got[i], ref[i], f"long-batched/{lens[i]}")
+            assert c.ok, (step, i, c)
+            assert am[i] == c.argmax_gpu
+        nxt = [int(np.argmax(r)) for r in ref]
+    for g in gs:
+        g.close()
+
+
 def test_truncate_resume_and_reset_reuse(tiny_pair):
     prompt = synthetic.make_tokens(40, TINY.vocab, seed=14)
     g, o = tiny_pair.sessions()
