@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     float* s_o = reinterpret_cast<float*>(kt_all);     // [AWARPS][G][D], reuses the K tiles at the end
     __shared__ int s_ticket;
 
-    const int split = blockIdx.x, kvh = blockIdx.y, t = blockIdx.z;
+    const int split = blockIdx.x, kvh = blockIdx.y;
+    const int t = p.row_order ? p.row_order[blockIdx.z] : (int)blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __nv_bfloat16* kt = kt_all + warp * K_TILE;
     __nv_bfloat16* vt = vt_all + warp * V_TILE;

@@ -129,6 +129,7 @@ struct AttnArgs {
     int T, n_q, n_kv;
     const int* row_pos;
     const int* row_slot;
+    const int* row_order;      // [T] row of grid z-index z (longest context first), or null: row z
     const int* tables;
     int max_blocks;
     __nv_bfloat16* kv_layer;   // pool slab of this layer; written by the fused append

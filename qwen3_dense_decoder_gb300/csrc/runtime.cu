@@ -149,7 +149,7 @@ struct q3_model {
     std::vector<std::vector<f16*>> w16;   // [layer][proj] fp16 copies for the tensor cores
                                           // (of the BF16 weights, or the dequantised Q8_0 planes)
     f16* lm16 = nullptr;      // fp16 copy of the lm_head for batched rows
-    int* meta = nullptr;      // [5][max_rows]: row_pos, row_slot, last_row, tile_row0, tile_rows,
+    int* meta = nullptr;      // [6][max_rows]: row_pos, row_slot, last_row, tile_row0, tile_rows, row_order,
                               // then the tcgen05 attention schedule: [SCHED_GRID + 1] starts, items
     f16* q16 = nullptr;       // [rows_alloc][qw] fp16 q of prefill rounds
     int* attn_counters = nullptr;   // [max_rows][n_kv] split tickets, zero between rounds
@@ -289,7 +289,7 @@ constexpr int SCHED_GRID = 1024;
 // (tiles <= max_rows, so items <= max_rows * n_kv)
 size_t meta_capacity(const q3_model* m)
 {
-    return 5 * (size_t)m->max_rows + SCHED_GRID + 1 + (size_t)m->max_rows * m->c.n_kv_heads;
+    return 6 * (size_t)m->max_rows + SCHED_GRID + 1 + (size_t)m->max_rows * m->c.n_kv_heads;
 }
 }  // namespace
 
@@ -692,6 +692,7 @@ int run_round(q3_model* m, const Round& r)
             aa.n_splits = n_splits;
             aa.part_ml = m->part_ml; aa.part_o = m->part_o;
             aa.counters = m->attn_counters;
+            aa.row_order = m->meta + 5 * m->max_rows;
             aa.out = one ? (void*)m->attf : (void*)m->att;
             aa.out_f16 = one ? 0 : 1;
             aa.status = m->status;
@@ -709,7 +710,7 @@ int run_round(q3_model* m, const Round& r)
             pa.kv_layer = r.pool->kv + (size_t)l * layer_kv; pa.n_blocks = r.pool->n_blocks;
             pa.out = m->att;
             pa.work_counter = m->pre_counter;
-            pa.sched_start = m->meta + 5 * m->max_rows;
+            pa.sched_start = m->meta + 6 * m->max_rows;
             pa.sched_items = pa.sched_start + SCHED_GRID + 1;
             pa.kv_row0 = (int)((size_t)l * layer_kv / 128);
             pa.status = m->status;
@@ -869,6 +870,13 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
         }
         h[2 * m->max_rows + i] = t - 1;
     }
+    // rows by position, latest first: the decode attention launches the rows
+    // with the most blocks first, so the longest split CTAs start in the first wave
+    {
+        int* order = h + 5 * m->max_rows;
+        for (int i = 0; i < t; ++i) order[i] = i;
+        std::stable_sort(order, order + t, [&](int a, int b) { return h[a] > h[b]; });
+    }
     // a one-session round with n_out logit rows: its last n_out rows, in order
     if (ns == 1 && n_out > 1)
         for (int j = 0; j < n_out; ++j) h[2 * m->max_rows + j] = n[0] - n_out + j;
@@ -877,7 +885,7 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
     // tcgen05 kernel, which also takes a per-CTA item list built here by
     // longest-processing-time-first assignment (an item is one tile for one
     // KV head; its cost is the number of 128-position K/V tiles it walks).
-    size_t meta_ints = 5 * (size_t)m->max_rows;
+    size_t meta_ints = 6 * (size_t)m->max_rows;
     r.attn_tc = m->prefill_tc && m->prefill_tc_ok;
     {
         const int R = r.attn_tc ? prefill_tc_rows(m->c.n_q_heads, m->c.n_kv_heads) : 64;
@@ -914,7 +922,7 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
                     load.push({top.first + cost, top.second});
                 }
             }
-            int* start = h + 5 * m->max_rows;
+            int* start = h + 6 * m->max_rows;
             int* items = start + SCHED_GRID + 1;
             int at = 0;
             for (int c = 0; c < grid; ++c) {
