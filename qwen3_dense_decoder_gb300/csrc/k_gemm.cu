@@ -121,6 +121,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // the weight tile (A) of stage s for k-block kb of unit w
+    auto load_a = [&](int s, const Unit& w, int kb) {
+        const int kc = kb * BK;
+        uint8_t* a_dst = sa + s * A_BYTES;
+        if (p.pair) {
+            tma_load_2d(a_dst, &ta0, &full[s], kc, w.mt * 64);
+            tma_load_2d(a_dst + A_BYTES / 2, &ta1, &full[s], kc, w.mt * 64);
+        } else if (w.mt < p.a_tiles0) {
+            tma_load_2d(a_dst, &ta0, &full[s], kc, w.mt * BM);
+        } else if (w.mt < p.a_tiles1) {
+            tma_load_2d(a_dst, &ta1, &full[s], kc, (w.mt - p.a_tiles0) * BM);
+        } else {
+            tma_load_2d(a_dst, &ta2, &full[s], kc, (w.mt - p.a_tiles1) * BM);
+        }
+    };
+    // Weights do not depend on the previous kernel: with early_a the first
+    // ring stages' weight tiles are requested before the dependency wait
+    // (their stage barriers expect the token tiles' bytes too, requested
+    // after it).
+    int pre = 0;
+    if (p.early_a && warp == 0 && lane == 0) {
+        for (int u = blockIdx.x; u < units && pre < STAGES; u += gridDim.x) {
+            const Unit w = decode_unit(p, u, n_tiles);
+            for (int kb = w.kb0; kb < w.kb1 && pre < STAGES; ++kb, ++pre) {
+                mbar_arrive_expect_tx(&full[pre], C::STAGE_BYTES);
+                load_a(pre, w, kb);
+            }
+        }
+    }
+
     // the token rows (B) are written by the previous kernel
     grid_dep_wait();
 
@@ -134,6 +164,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
                 for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t use = it / STAGES;
+                    if (it < pre) {                        // weights already requested
+                        tma_load_2d(sb + s * C::B_BYTES, &tb, &full[s], kb * BK, w.nt * BN);
+                        continue;
+                    }
                     if (it >= STAGES && !mbar_wait(&empty[s], (use & 1) ^ 1, p.status)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
                     const int kc = kb * BK;

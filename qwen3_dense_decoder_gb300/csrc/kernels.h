@@ -41,6 +41,8 @@ struct GemmArgs {
     void* out;
     int ldo;
     float* ws;
+    int early_a;          // request the first stages' weight tiles before the dependency wait
+                          // (helps short GEMMs, whose ring ramp is a large part of the launch)
     int* status;
 };
 

@@ -425,6 +425,7 @@ int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtens
     g.epi = epi;
     g.out = out; g.ldo = ldo;
     g.ws = m->ws;
+    g.early_a = N <= 256;                    // batched decode rounds: the ring ramp overlaps the previous kernel
     g.status = m->status;
     Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
     m->prof_begin(Q3_K_GEMM);
