@@ -675,7 +675,7 @@ def report(args, res, world, dist_on, pk, pk_kind):
         k_bytes = decode_bytes(s, (pc0 + pc1) / 2)
         k_name = "decode_step (fused one-kernel decode step: all projections, attention, lm_head)"
         # DRAM bytes of one launch from an ncu capture of the 4-layer case
-        # (bench.py --ncu-case decode-4layer): 1.0023 x its algorithmic bytes,
+        # (bench.py --ncu-case decode-4layer): 1.0025 x its algorithmic bytes,
         # scaled to this launch by the same ratio
         k_traffic = round(DECODE_STEP_TRAFFIC_RATIO * k_bytes)
     else:
