@@ -50,6 +50,15 @@ def test_host_side_argument_checks_need_no_gpu(libq3):
     assert libq3.q3_op_matmul(None, None, 128, 1, 64, None, 0, None) == -1
     assert b"bad argument" in libq3.q3_last_error()
 
+    # the multi-logit round, the prefill attention operator and the path
+    # selectors reject bad arguments the same way
+    assert libq3.q3_session_eval_n(None, None, 4, 2, None, None) == -1
+    assert libq3.q3_op_prefill_attention(None, None, None, 1, 1, 0, 1, 32, 8, None, 1, None) == -1
+    assert libq3.q3_model_set_prefill_tc(None, 1) == -1
+    assert libq3.q3_model_set_fused_decode(None, 1) == -1
+    assert libq3.q3_model_prefill_tc(None) == 0
+    assert libq3.q3_model_fused_decode(None) == 0
+
 
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "qwen3_dense_decoder_gb300")
