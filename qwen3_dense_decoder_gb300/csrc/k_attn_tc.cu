@@ -14,8 +14,8 @@
 // (four blocks through the block table) with an online softmax:
 //   S  = Q K^T        tcgen05.mma, A = Q (shared memory), B = K tile (shared
 //                     memory), FP32 accumulator in tensor memory
-//   P  = exp2(S - m)  softmax warps, one thread per row, P written back to
-//                     tensor memory as fp16 pairs
+//   P  = exp2(S - m)  softmax warps, two threads per row (64 columns each),
+//                     P written back to tensor memory as fp16 pairs
 //   O += P V          tcgen05.mma, A = P (tensor memory), B = V tile read
 //                     MN-major from shared memory, FP32 accumulator in TMEM
 // Operands are fp16 (3 more mantissa bits than bf16 for Q and P); the BF16
@@ -23,6 +23,9 @@
 // The running maximum is raised lazily: O and the row sum are rescaled only
 // when a row maximum grows by more than 2^8, so P <= 256 always fits fp16,
 // and the final O / l is the same quantity.
+//
+// K/V pass through a three-stage ring; the Q tile has one buffer, released
+// for the next item once the item's last scores have been computed.
 //
 // Roles (one CTA per SM, items from a host-built per-CTA list):
 //   warp 0       lane 0 issues every MMA and owns the tensor-memory columns
