@@ -20,9 +20,10 @@ _SRC = os.path.join(_HERE, "q3_oracle.c")
 _HDR = os.path.join(_HERE, "q3_oracle.h")
 _LIB = os.path.join(_HERE, "libq3_oracle.so")
 
-BF16, Q8_0 = 0, 1
+BF16, Q8_0, AFFINE4 = 0, 1, 2
 BLOCK = 32
 Q8_0_BYTES = 34
+AFFINE4_BYTES = 20
 
 
 def build(force: bool = False) -> str:
@@ -63,6 +64,8 @@ def lib():
         L.orc_f32_to_f16.argtypes, L.orc_f32_to_f16.restype = [f], C.c_uint16
         L.orc_q8_0_pack.argtypes = [vp, C.c_long, vp]
         L.orc_q8_0_unpack.argtypes = [vp, C.c_long, vp]
+        L.orc_affine4_pack.argtypes = [vp, C.c_long, vp]
+        L.orc_affine4_unpack.argtypes = [vp, C.c_long, vp]
         L.orc_rmsnorm.argtypes = [vp, vp, i, d, vp]
         L.orc_rope.argtypes = [vp, i, i, d]
         L.orc_silu.argtypes, L.orc_silu.restype = [f], f
@@ -138,6 +141,22 @@ def q8_0_unpack(blocks: np.ndarray, n: int) -> np.ndarray:
     return out
 
 
+def affine4_pack(w: np.ndarray) -> np.ndarray:
+    """float32 weights [..., n] (n % 32 == 0) -> 20-byte AFFINE4_GS32 groups (uint8)."""
+    w = np.ascontiguousarray(w, np.float32)
+    assert w.shape[-1] % BLOCK == 0
+    out = np.empty(w.shape[:-1] + (w.shape[-1] // BLOCK * AFFINE4_BYTES,), np.uint8)
+    lib().orc_affine4_pack(_ptr(w), w.size, _ptr(out))
+    return out
+
+
+def affine4_unpack(groups: np.ndarray, n: int) -> np.ndarray:
+    groups = np.ascontiguousarray(groups, np.uint8)
+    out = np.empty(groups.shape[:-1] + (n,), np.float32)
+    lib().orc_affine4_unpack(_ptr(groups), out.size, _ptr(out))
+    return out
+
+
 def rmsnorm(x: np.ndarray, gain_bits: np.ndarray, eps: float) -> np.ndarray:
     x = np.ascontiguousarray(x, np.float32)
     g = np.ascontiguousarray(gain_bits, np.uint16)
@@ -187,8 +206,8 @@ class Model:
     """Oracle model over host copies of the synthetic weights.
 
     ``weights`` is synthetic.make_weights()'s dict (torch bf16 tensors, any
-    device).  For a Q8_0 shape the oracle packs the seven projections itself
-    with its own packer.
+    device).  For a Q8_0 or AFFINE4 shape the oracle packs the seven
+    projections itself with its own packer (``packed`` keeps them per layer).
     """
 
     PROJ = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
@@ -206,7 +225,7 @@ class Model:
         emb = keep(self.embed)
         fnorm = keep(bf16_bits(weights["final_norm"]))
         lm = keep(bf16_bits(weights["lm_head"])) if not shape.tied else None
-        self.q8_blocks = []   # per layer {name: blocks} when Q8_0
+        self.packed = []      # per layer {name: blocks or groups} when quantized
         layers = (_Layer * shape.n_layers)()
         for li, lw in enumerate(weights["layers"]):
             ptrs = {}
@@ -215,13 +234,14 @@ class Model:
             packed = {}
             for name in self.PROJ:
                 bits = bf16_bits(lw[name])
-                if shape.scheme == Q8_0:
-                    blk = q8_0_pack(bf16_to_f32_fast(bits).reshape(bits.shape))
+                if shape.scheme in (Q8_0, AFFINE4):
+                    pack = q8_0_pack if shape.scheme == Q8_0 else affine4_pack
+                    blk = pack(bf16_to_f32_fast(bits).reshape(bits.shape))
                     packed[name] = blk
                     ptrs[name] = keep(blk)
                 else:
                     ptrs[name] = keep(bits)
-            self.q8_blocks.append(packed)
+            self.packed.append(packed)
             L = layers[li]
             L.attn_norm, L.q_norm, L.k_norm, L.ffn_norm = (
                 ptrs["attn_norm"], ptrs["q_norm"], ptrs["k_norm"], ptrs["ffn_norm"])

@@ -4,7 +4,8 @@
  * and the bench's CPU-baseline leg call it; the CUDA path never does.
  *
  * Sources (Kipp pages): "Kipp Model Support" (sections "The registry",
- * "What the gates check", "qwen3-0.6b-base", "Quantization (Q8_0)"),
+ * "What the gates check", "qwen3-0.6b-base", "Quantization (Q8_0)",
+ * "Quantization (AFFINE4_GS32)"),
  * "Kipp Roadmap" (status v0.0.2: paged KV and batched evaluation), and
  * "Reproducing Kipp" (section "Model-backed CPU and Metal gates").  Where the
  * pages leave the layer math open, the oracle takes the plain reading of a
@@ -138,6 +139,74 @@ void orc_q8_0_unpack(const uint8_t* blocks, long n, float* w)
 }
 
 /* ------------------------------------------------------------------ */
+/* AFFINE4_GS32 ("Kipp Model Support", section                         */
+/* "Quantization (AFFINE4_GS32)")                                       */
+/* ------------------------------------------------------------------ */
+
+/* The pages fix the group (32 weights), the parts (4-bit codes, an fp16 scale
+ * and an fp16 bias) and the size (5.0 bits per weight, so 20 bytes a group).
+ * Readings for the rest:
+ *  - a weight is scale * q + bias with the code q in [0, 15] (affine: the
+ *    bias is the value of code 0);
+ *  - record layout: the 16 code bytes, weight 2i in the low nibble of byte i
+ *    and weight 2i + 1 in its high nibble, then the scale, then the bias,
+ *    each fp16 little-endian;
+ *  - quantizer: bias = fp16(min), scale = fp16((max - min) / 15) with the
+ *    subtraction and the division in FP32; each code rounds
+ *    (w - bias) / scale, computed in FP32 against the stored (fp16) scale
+ *    and bias, to the nearest integer, ties to even, clamped to [0, 15]; a
+ *    stored scale of zero (a constant group, or a range below half the
+ *    smallest fp16 step) gives all codes zero. */
+void orc_affine4_pack(const float* w, long n, uint8_t* groups)
+{
+    for (long g = 0; g < n / ORC_BLOCK; g++) {
+        const float* x = w + g * ORC_BLOCK;
+        uint8_t* out = groups + g * ORC_AFFINE4_BYTES;
+        float lo = x[0], hi = x[0];
+        for (int i = 1; i < ORC_BLOCK; i++) {
+            if (x[i] < lo) lo = x[i];
+            if (x[i] > hi) hi = x[i];
+        }
+        float range = hi - lo;
+        uint16_t sh = orc_f32_to_f16(range / 15.0f);
+        uint16_t bh = orc_f32_to_f16(lo);
+        float scale = orc_f16_to_f32(sh), bias = orc_f16_to_f32(bh);
+        memset(out, 0, 16);
+        for (int i = 0; i < ORC_BLOCK; i++) {
+            int q = 0;
+            if (scale != 0.0f) {
+                float diff = x[i] - bias;
+                float r = nearbyintf(diff / scale);
+                if (r < 0.0f) r = 0.0f;
+                if (r > 15.0f) r = 15.0f;
+                q = (int)r;
+            }
+            out[i / 2] |= (uint8_t)(i % 2 ? q << 4 : q);
+        }
+        out[16] = (uint8_t)(sh & 0xff);
+        out[17] = (uint8_t)(sh >> 8);
+        out[18] = (uint8_t)(bh & 0xff);
+        out[19] = (uint8_t)(bh >> 8);
+    }
+}
+
+/* w = scale * q + bias rounded once to FP32.  In FP64 the product of an fp16
+ * scale and a 4-bit code and its sum with an fp16 bias are exact (they span
+ * at most 2^-24 .. 2^21, 45 bits), so one rounding follows. */
+void orc_affine4_unpack(const uint8_t* groups, long n, float* w)
+{
+    for (long g = 0; g < n / ORC_BLOCK; g++) {
+        const uint8_t* in = groups + g * ORC_AFFINE4_BYTES;
+        double scale = orc_f16_to_f32((uint16_t)(in[16] | (in[17] << 8)));
+        double bias = orc_f16_to_f32((uint16_t)(in[18] | (in[19] << 8)));
+        for (int i = 0; i < ORC_BLOCK; i++) {
+            int q = i % 2 ? in[i / 2] >> 4 : in[i / 2] & 0xf;
+            w[g * ORC_BLOCK + i] = (float)(scale * q + bias);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* threads: split [0, n) into contiguous ranges, one per thread         */
 /* ------------------------------------------------------------------ */
 
@@ -222,10 +291,15 @@ static void matmul_rows(void* a, long o0, long o1)
         if (j->scheme == ORC_BF16) {
             const uint16_t* row = (const uint16_t*)j->W + o * (long)j->n_in;
             for (int i = 0; i < j->n_in; i++) w[i] = orc_bf16_to_f32(row[i]);
-        } else {
+        } else if (j->scheme == ORC_Q8_0) {
             const uint8_t* row = (const uint8_t*)j->W
                                + o * (long)(j->n_in / ORC_BLOCK) * ORC_Q8_0_BYTES;
             orc_q8_0_unpack(row, j->n_in, wq);
+            for (int i = 0; i < j->n_in; i++) w[i] = wq[i];
+        } else {
+            const uint8_t* row = (const uint8_t*)j->W
+                               + o * (long)(j->n_in / ORC_BLOCK) * ORC_AFFINE4_BYTES;
+            orc_affine4_unpack(row, j->n_in, wq);
             for (int i = 0; i < j->n_in; i++) w[i] = wq[i];
         }
         for (int t = 0; t < j->n_tok; t++) {
@@ -311,7 +385,8 @@ orc_model* orc_model_create(const orc_cfg* cfg, const uint16_t* embed,
                             const orc_layer* layers, int n_threads)
 {
     if (cfg->n_q_heads % cfg->n_kv_heads || cfg->head_dim % 2 ||
-        (cfg->scheme == ORC_Q8_0 && (cfg->hidden % ORC_BLOCK || cfg->ffn % ORC_BLOCK ||
+        (cfg->scheme != ORC_BF16 && cfg->scheme != ORC_Q8_0 && cfg->scheme != ORC_AFFINE4) ||
+        (cfg->scheme != ORC_BF16 && (cfg->hidden % ORC_BLOCK || cfg->ffn % ORC_BLOCK ||
                                      (cfg->n_q_heads * cfg->head_dim) % ORC_BLOCK)))
         return NULL;
     orc_model* m = (orc_model*)calloc(1, sizeof(orc_model));

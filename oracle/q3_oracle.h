@@ -15,6 +15,9 @@
  *  - "Kipp Model Support", section "Quantization (Q8_0)": the seven per-layer
  *    projections in 32-weight blocks of fp16 scale + int8 quants; embedding,
  *    lm_head and all norms stay BF16.
+ *  - "Kipp Model Support", section "Quantization (AFFINE4_GS32)": 32-weight
+ *    groups of 4-bit codes with an fp16 scale and an fp16 bias, 5.0 bits per
+ *    weight (the same seven projections; the rest stays BF16).
  *  - "Kipp Roadmap", status v0.0.2: paged KV through a per-session
  *    32-position block table, bitwise equal to the contiguous layout;
  *    batched evaluation equal to isolated evaluation.
@@ -38,21 +41,23 @@
 extern "C" {
 #endif
 
-enum { ORC_BF16 = 0, ORC_Q8_0 = 1 };
-enum { ORC_BLOCK = 32 };          /* KV positions per block, Q8_0 weights per block */
+enum { ORC_BF16 = 0, ORC_Q8_0 = 1, ORC_AFFINE4 = 2 };
+enum { ORC_BLOCK = 32 };          /* KV positions per block; weights per Q8_0 block / AFFINE4 group */
 enum { ORC_Q8_0_BYTES = 34 };     /* fp16 scale + 32 int8 quants */
+enum { ORC_AFFINE4_BYTES = 20 };  /* 16 bytes of 4-bit codes + fp16 scale + fp16 bias */
 
 typedef struct orc_cfg {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
     int tied;     /* 1: lm_head is the token embedding */
-    int scheme;   /* ORC_BF16 or ORC_Q8_0 (the seven projections only) */
+    int scheme;   /* ORC_BF16, ORC_Q8_0 or ORC_AFFINE4 (the seven projections only) */
     double rope_theta, rms_eps;
 } orc_cfg;
 
 /* Per-layer weights, host memory, row-major [out][in].  BF16 tensors are
  * uint16 bit patterns.  With ORC_Q8_0 the seven projections point at
  * canonical blocks: [out][in/32] records of 34 bytes (little-endian fp16
- * scale, then 32 int8 quants). */
+ * scale, then 32 int8 quants).  With ORC_AFFINE4 they point at [out][in/32]
+ * groups of 20 bytes (16 code bytes, then little-endian fp16 scale and bias). */
 typedef struct orc_layer {
     const uint16_t *attn_norm, *q_norm, *k_norm, *ffn_norm;
     const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
@@ -73,11 +78,17 @@ uint16_t orc_f32_to_f16(float f);               /* round to nearest even */
 void orc_q8_0_pack(const float* w, long n, uint8_t* blocks);
 void orc_q8_0_unpack(const uint8_t* blocks, long n, float* w);
 
+/* ---- AFFINE4_GS32 ---- */
+/* w: n floats (n % 32 == 0) -> n/32 groups of 20 bytes. */
+void orc_affine4_pack(const float* w, long n, uint8_t* groups);
+void orc_affine4_unpack(const uint8_t* groups, long n, float* w);
+
 /* ---- components (exported so the tests can pin each one) ---- */
 void  orc_rmsnorm(const float* x, const uint16_t* gain, int n, double eps, float* y);
 void  orc_rope(float* v, int head_dim, int pos, double theta);       /* in place */
 float orc_silu(float z);
-/* y[t][o] = sum_i W[o][i] * x[t][i]; W bf16 (scheme 0) or Q8_0 blocks (1). */
+/* y[t][o] = sum_i W[o][i] * x[t][i]; W bf16 (scheme 0), Q8_0 blocks (1) or
+ * AFFINE4 groups (2). */
 void  orc_matmul(const void* W, int scheme, int n_out, int n_in,
                  const float* x, int n_tok, float* y, int n_threads);
 /* One query row of GQA attention over ctx cached positions.

@@ -18,7 +18,7 @@ import dataclasses
 import numpy as np
 import torch
 
-BF16, Q8_0 = 0, 1
+BF16, Q8_0, AFFINE4 = 0, 1, 2
 
 
 @dataclasses.dataclass(frozen=True)
@@ -84,8 +84,8 @@ def _draw(shape, seed: int, device, gain: bool) -> torch.Tensor:
 
 def make_weights(s: Shape, seed: int = 1234, device="cpu") -> dict:
     """bf16 weights for shape s: {"embed", "final_norm", "lm_head" (None if tied),
-    "layers": [{name: tensor}]}.  For a Q8_0 shape these are the bf16 source
-    weights that the quantizers of either side pack."""
+    "layers": [{name: tensor}]}.  For a Q8_0 or AFFINE4 shape these are the
+    bf16 source weights that the quantizers of either side pack."""
     k = seed
     out = {"embed": _draw((s.vocab, s.hidden), k, device, False)}
     k += 1

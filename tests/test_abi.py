@@ -60,6 +60,22 @@ def test_host_side_argument_checks_need_no_gpu(libq3):
     assert libq3.q3_model_fused_decode(None) == 0
 
 
+def test_config_checks_need_no_gpu(libq3):
+    # a config is checked before any CUDA call: a weight scheme the CUDA path
+    # does not implement (AFFINE4_GS32 is oracle-only so far) fails loudly
+    from qwen3_dense_decoder_gb300 import _Config
+    libq3.q3_last_error.restype = ctypes.c_char_p
+    out = ctypes.c_void_p()
+    for scheme, msg in ((2, b"unknown weight scheme 2"), (-1, b"unknown weight scheme -1")):
+        cfg = _Config(2, 1024, 16, 8, 128, 3072, 4096, 64, 1e6, 1e-6, 1, scheme)
+        assert libq3.q3_model_create(ctypes.byref(cfg), None, 16, None, ctypes.byref(out)) == -1
+        assert msg in libq3.q3_last_error()
+        assert out.value is None
+    cfg = _Config(2, 1024, 16, 8, 64, 3072, 4096, 64, 1e6, 1e-6, 1, 0)
+    assert libq3.q3_model_create(ctypes.byref(cfg), None, 16, None, ctypes.byref(out)) == -1
+    assert b"head_dim must be 128" in libq3.q3_last_error()
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "qwen3_dense_decoder_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -100,6 +100,17 @@ def test_matmul_orientation_and_values(orc):
     deq = orc.q8_0_unpack(packed, n_in).astype(np.float64)
     yq = orc.matmul(packed, 1, n_out, n_in, x, n_threads=2)
     np.testing.assert_allclose(yq, x.astype(np.float64) @ deq.T, rtol=1e-6, atol=1e-6)
+    # AFFINE4_GS32 weights: the same, with 20-byte groups along each row
+    groups = orc.affine4_pack(Wf.astype(np.float32))
+    assert groups.shape == (n_out, n_in // 32 * 20)
+    deq4 = orc.affine4_unpack(groups, n_in).astype(np.float64)
+    for i in (0, 17, 95):
+        e = np.zeros(n_in, np.float32)
+        e[i] = 1.0
+        np.testing.assert_array_equal(orc.matmul(groups, 2, n_out, n_in, e)[0],
+                                      deq4[:, i].astype(np.float32))
+    y4 = orc.matmul(groups, 2, n_out, n_in, x, n_threads=2)
+    np.testing.assert_allclose(y4, x.astype(np.float64) @ deq4.T, rtol=1e-6, atol=1e-6)
 
 
 def _kv(a):

@@ -19,13 +19,14 @@ import numpy as np
 import pytest
 import torch
 
-from synthetic import BF16, Q8_0, Shape, make_block_permutation, make_tokens, make_weights
+from synthetic import AFFINE4, BF16, Q8_0, Shape, make_block_permutation, make_tokens, make_weights
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_facts.json")))
 
 TINY = Shape("oracle-tiny", 2, 64, 4, 2, 16, 96, 128, True, rope_theta=1e4)
 TINY_UNTIED = TINY.replace(name="oracle-tiny-untied", tied=False, n_layers=1)
 TINY_Q8 = TINY.replace(name="oracle-tiny-q8", scheme=Q8_0, tied=False)
+TINY_A4 = TINY.replace(name="oracle-tiny-affine4", scheme=AFFINE4, tied=False)
 
 
 def _model(orc, shape, seed=7, threads=2):
@@ -98,20 +99,31 @@ def test_brute_force_agrees(orc, shape):
         assert int(np.argmax(got[t])) == int(np.argmax(ref[t]))
 
 
-def test_brute_force_agrees_q8_0(orc):
-    m, w = _model(orc, TINY_Q8)
-    toks = make_tokens(9, TINY_Q8.vocab, seed=6)
+@pytest.mark.parametrize("shape", [TINY_Q8, TINY_A4], ids=lambda s: s.name)
+def test_brute_force_agrees_quantized(orc, shape):
+    """The quantized forward is the BF16 forward over the dequantised projections."""
+    m, w = _model(orc, shape)
+    toks = make_tokens(9, shape.vocab, seed=6)
     got = m.session(max_ctx=64).eval(toks, all_rows=True)
-    li = iter(range(10 ** 6))
+    unpack = orc.q8_0_unpack if shape.scheme == Q8_0 else orc.affine4_unpack
     deq = {}
     for l, lw in enumerate(w["layers"]):
         for name in orc.Model.PROJ:
-            deq[id(lw[name])] = orc.q8_0_unpack(m.q8_blocks[l][name], lw[name].shape[1]) \
-                .astype(np.float64)
-    ref = brute_force_logits(TINY_Q8, w, toks, weights64=lambda t: deq[id(t)])
-    del li
+            deq[id(lw[name])] = unpack(m.packed[l][name], lw[name].shape[1]).astype(np.float64)
+    ref = brute_force_logits(shape, w, toks, weights64=lambda t: deq[id(t)])
     for t in range(len(toks)):
         assert _nmse(got[t], ref[t]) < 1e-10
+
+
+def test_affine4_forward_stays_near_bf16(orc):
+    """4-bit codes are lossy: the AFFINE4 forward is near the BF16 one, not equal."""
+    a4, w = _model(orc, TINY_A4)
+    bf = orc.Model(TINY_A4.replace(scheme=BF16), w, n_threads=2)
+    toks = make_tokens(9, TINY_A4.vocab, seed=6)
+    got = a4.session(max_ctx=64).eval(toks, all_rows=True)
+    ref = bf.session(max_ctx=64).eval(toks, all_rows=True)
+    e = _nmse(got, ref)
+    assert 1e-6 < e < 1e-1, e
 
 
 def test_cached_decode_equals_recompute(orc):
@@ -206,5 +218,8 @@ def test_shapes_follow_the_registry(orc):
     s = synthetic.SHAPES["0.6b"]
     assert (s.q_width, s.hidden) == (GOLD["attn_width_0p6b"]["value"], GOLD["attn_width_0p6b"]["hidden"])
     assert 34 * 8 / 32 == GOLD["q8_0"]["bits_per_weight"] and orc.Q8_0_BYTES == 34
+    a4 = GOLD["affine4_gs32"]
+    assert orc.AFFINE4_BYTES * 8 / a4["weights_per_group"] == a4["bits_per_weight"]
+    assert orc.AFFINE4_BYTES == (a4["weights_per_group"] * a4["code_bits"] + 2 * 16) // 8
     assert orc.BLOCK == GOLD["kv_block_positions"]["value"]
     assert BF16 == 0

@@ -1,10 +1,13 @@
-"""Pins of the oracle's scalar conversions and of its Q8_0 packer.
+"""Pins of the oracle's scalar conversions and of its Q8_0 and AFFINE4_GS32 packers.
 
 bf16 and fp16 rounding are checked against library conversions that
 implement the same IEEE rules (torch's bf16 cast, numpy's float16 cast);
 Q8_0 against blocks worked by hand (tests/golden/q8_0_worked_example.json)
 and against closed-form error bounds of the format ("Kipp Model Support",
-section "Quantization (Q8_0)").
+section "Quantization (Q8_0)"); AFFINE4_GS32 against groups worked by hand
+(tests/golden/affine4_gs32_worked_example.json) and against the closed forms
+of rounding to a 16-point grid ("Kipp Model Support", section
+"Quantization (AFFINE4_GS32)").
 """
 import json
 import os
@@ -110,6 +113,82 @@ def test_q8_0_multiples_of_scale_round_trip(orc):
         w = (k * 2.0 ** e).astype(np.float32)
         back = orc.q8_0_unpack(orc.q8_0_pack(w), 32)
         np.testing.assert_array_equal(back, w)
+
+
+def test_affine4_hand_worked_groups(orc):
+    spec = json.load(open(os.path.join(GOLDEN, "affine4_gs32_worked_example.json")))
+    for grp in spec["groups"]:
+        k = np.array(grp["k"], np.float64)
+        assert k.shape == (32,)
+        w = np.ldexp(k, grp["unit_log2"]).astype(np.float32)
+        assert np.all(w.astype(np.float64) == np.ldexp(k, grp["unit_log2"]))
+        packed = orc.affine4_pack(w)
+        assert packed.shape == (20,), grp["name"]
+        np.testing.assert_array_equal(packed[:16], np.array(grp["code_bytes"], np.uint8),
+                                      err_msg=grp["name"])
+        assert int(packed[16]) | (int(packed[17]) << 8) == grp["scale_bits"], grp["name"]
+        assert int(packed[18]) | (int(packed[19]) << 8) == grp["bias_bits"], grp["name"]
+        back = orc.affine4_unpack(packed, 32)
+        for i, v in grp["dequant"]:
+            assert back[i] == np.float32(v), (grp["name"], i)
+
+
+def _affine4_fields(packed, rows, groups):
+    g = packed.reshape(rows, groups, 20)
+    codes = np.empty((rows, groups, 32), np.int64)
+    codes[..., 0::2] = g[..., :16] & 0xF
+    codes[..., 1::2] = g[..., :16] >> 4
+    sh = (g[..., 16].astype(np.uint16) | (g[..., 17].astype(np.uint16) << 8))
+    bh = (g[..., 18].astype(np.uint16) | (g[..., 19].astype(np.uint16) << 8))
+    return codes, sh.view(np.float16).astype(np.float64), bh.view(np.float16).astype(np.float64)
+
+
+def test_affine4_grid_rounding_bounds(orc):
+    rng = np.random.default_rng(4)
+    rows, n = 64, 256
+    w = (rng.standard_normal((rows, n)) * 0.02).astype(np.float32)
+    w[2, :32] = 0.01                                   # a constant group
+    w[7, 64:96] = np.linspace(-3, 5, 32)               # a wide group
+    packed = orc.affine4_pack(w)
+    assert packed.shape == (rows, n // 32 * 20)        # 5.0 bits per weight
+    back = orc.affine4_unpack(packed, n).reshape(rows, n // 32, 32).astype(np.float64)
+    codes, s16, b16 = _affine4_fields(packed, rows, n // 32)
+    wb = w.reshape(rows, n // 32, 32).astype(np.float64)
+    lo, hi = wb.min(-1), wb.max(-1)
+    # the stored bias and scale are the fp16 roundings of the group minimum and range / 15
+    np.testing.assert_array_equal(b16, lo.astype(np.float16).astype(np.float64))
+    d32 = ((hi - lo).astype(np.float32) / np.float32(15)).astype(np.float32)
+    np.testing.assert_array_equal(s16, d32.astype(np.float16).astype(np.float64))
+    # dequant is scale * code + bias, rounded once to FP32
+    np.testing.assert_array_equal(back, (s16[..., None] * codes + b16[..., None])
+                                  .astype(np.float32).astype(np.float64))
+    # codes span the grid: the minimum gets 0 and the maximum 15 wherever the range is non-zero
+    wide = s16 > 0
+    assert np.all(codes.min(-1)[wide] == 0) and np.all(codes.max(-1)[wide] == 15)
+    assert np.all(codes[~wide] == 0) and not wide[2, 0]
+    # codes are monotone in the weight within a group
+    order = np.argsort(wb, axis=-1, kind="stable")
+    assert np.all(np.diff(np.take_along_axis(codes, order, -1), axis=-1) >= 0)
+    # nearest grid point: |w - (scale * code + bias)| <= scale / 2 (plus FP32 rounding of the
+    # quotient and of the dequantised value)
+    grid = s16[..., None] * codes + b16[..., None]
+    err = np.abs(wb - grid)
+    assert np.all(err[wide] <= s16[wide][:, None] * (0.5 + 2.0 ** -18) + 1e-12)
+    # a zero scale leaves every weight at the bias: off by the fp16 rounding of the minimum
+    assert np.all(err[~wide] == np.abs(lo - b16)[~wide][:, None])
+    assert np.all(np.abs(back - grid) <= np.abs(grid) * 2.0 ** -24)
+    # the constant group comes back exactly when its value is an fp16 number
+    assert np.all(back[2, 0] == np.float32(np.float16(0.01)))
+
+
+def test_affine4_quantizer_keeps_its_own_output(orc):
+    """A group already on an fp16 grid (minimum 0 code, maximum 15) packs to the same bytes."""
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((16, 512)) * 0.02).astype(np.float32)
+    once = orc.affine4_pack(w)
+    back = orc.affine4_unpack(once, 512)
+    np.testing.assert_array_equal(orc.affine4_pack(back), once)
+    np.testing.assert_array_equal(orc.affine4_unpack(orc.affine4_pack(back), 512), back)
 
 
 def test_argmax_lowest_index_on_ties(orc):
