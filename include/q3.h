@@ -62,9 +62,12 @@ extern "C" {
 
 #define Q3_BF16 0
 #define Q3_Q8_0 1
+#define Q3_AFFINE4 2
 #define Q3_KV_BLOCK 32       /* positions per KV block */
 #define Q3_Q8_0_BLOCK 32     /* weights per Q8_0 block */
 #define Q3_Q8_0_BYTES 34     /* bytes per canonical Q8_0 block */
+#define Q3_AFFINE4_GROUP 32  /* weights per AFFINE4_GS32 group */
+#define Q3_AFFINE4_BYTES 20  /* bytes per AFFINE4_GS32 group */
 
 /* Device status-word bits (q3_sync reports them as Q3_ERR_DEVICE_CHECK). */
 #define Q3_STATUS_TOKEN_RANGE 0x1   /* a token id outside [0, vocab) */
@@ -79,8 +82,8 @@ typedef struct q3_session q3_session;
 /* Shape of the decoder.  head_dim must be 128, n_q_heads a multiple of
  * n_kv_heads (GQA group of at most 8), hidden, ffn, vocab and
  * n_q_heads*head_dim multiples of 128.  max_ctx bounds a session's length
- * (the RoPE table is built for it).  scheme: Q3_BF16 or Q3_Q8_0 (the seven
- * projections only).  tied: 1 when lm_head is the token embedding. */
+ * (the RoPE table is built for it).  scheme: Q3_BF16, Q3_Q8_0 or Q3_AFFINE4
+ * (the seven projections only).  tied: 1 when lm_head is the token embedding. */
 typedef struct q3_config {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, max_ctx;
     float rope_theta, rms_eps;
@@ -94,7 +97,9 @@ typedef struct q3_config {
  * [n_kv*d][hidden], wo [hidden][n_q*d], w_gate and w_up [ffn][hidden],
  * w_down [hidden][ffn].  With Q3_BF16 they are bf16; with Q3_Q8_0 they are
  * canonical Q8_0 blocks [out][in/32] of 34 bytes (little-endian fp16 scale,
- * then 32 int8 quants), as q3_quantize_q8_0 writes them. */
+ * then 32 int8 quants), as q3_quantize_q8_0 writes them; with Q3_AFFINE4
+ * they are AFFINE4_GS32 groups [out][in/32] of 20 bytes, 4-byte aligned, as
+ * q3_quantize_affine4 writes them. */
 typedef struct q3_layer_weights {
     const void *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo,
                *ffn_norm, *w_gate, *w_up, *w_down;
@@ -119,7 +124,11 @@ typedef struct q3_weights {
  * an fp16 copy of the BF16 projections and lm_head (exact except for
  * |w| < 2^-17, whose rounding is below 2^-25), or of the Q8_0 projections
  * dequantised once (d * q rounded to fp16; 2 bytes per weight of device
- * memory beside the 1.0625 of the planes).  Weights beyond the fp16 range make creation fail with
+ * memory beside the 1.0625 of the planes).  With Q3_AFFINE4 every round,
+ * batch-1 decode included, runs its projections on the tensor cores over an
+ * fp16 copy of the dequantised groups (scale * code + bias rounded to FP32,
+ * then to fp16, as q3_affine4_to_f16 writes it); the fused decode step and
+ * the batch-1 GEMV take BF16 and Q8_0 only.  Weights beyond the fp16 range make creation fail with
  * Q3_ERR_INVALID_ARG; an activation beyond it is reported by q3_sync as
  * Q3_ERR_DEVICE_CHECK (Q3_STATUS_F16_RANGE).  max_round_tokens bounds the rows of one round (the activation
  * scratch, owned by the model, is sized for it; longer q3_session_eval rounds
@@ -201,6 +210,28 @@ int q3_sync(q3_model* m);
  * [n/32][34] bytes; n a multiple of 32.  Asynchronous on stream (a
  * cudaStream_t or NULL).  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
 int q3_quantize_q8_0(const void* w_dev, int64_t n, void* blocks_dev, void* stream);
+
+/* Pack bf16 weights into AFFINE4_GS32 groups on the device ("Kipp Model
+ * Support", section "Quantization (AFFINE4_GS32)": 32 weights, 4-bit codes,
+ * an fp16 scale and an fp16 bias, 5.0 bits per weight).  A weight is
+ * scale * code + bias, code in [0, 15].  Per group: bias = fp16(min),
+ * scale = fp16((max - min) / 15) with the FP32 subtraction and division
+ * correctly rounded; code = round-half-even((w - bias) / scale) in FP32
+ * against the stored scale and bias, clamped to [0, 15]; a zero scale gives
+ * zero codes.  Record: 16 code bytes (weight 2i in the low nibble of byte i,
+ * weight 2i + 1 in the high nibble), then the scale, then the bias, fp16
+ * little-endian.  w_dev: bf16 [n], 16-byte aligned; groups_dev: [n/32][20]
+ * bytes, 4-byte aligned; n a multiple of 32.  Asynchronous on stream.
+ * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+int q3_quantize_affine4(const void* w_dev, int64_t n, void* groups_dev, void* stream);
+
+/* The fp16 copy the model keeps of AFFINE4_GS32 projections: out[i] =
+ * fp16_rne(fp32_rne(scale * code + bias)) (one fused multiply-add, then the
+ * fp16 rounding), with scale, bias and code those of weight i's group.
+ * groups_dev: [n/32][20] bytes, 4-byte aligned; out_dev: fp16 [n], 16-byte
+ * aligned; n a multiple of 32.  Asynchronous on stream.
+ * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+int q3_affine4_to_f16(const void* groups_dev, int64_t n, void* out_dev, void* stream);
 
 /* Operator entry points, for per-kernel gates like the pages' operator tests
  * ("Reproducing Kipp", section "Model-backed CPU and Metal gates":

@@ -15,9 +15,10 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libq3.so")
 
-BF16, Q8_0 = 0, 1
+BF16, Q8_0, AFFINE4 = 0, 1, 2
 KV_BLOCK = 32
 Q8_0_BYTES = 34
+AFFINE4_BYTES = 20
 ERRORS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_DEVICE", -3: "OOM", -4: "POOL_EXHAUSTED",
           -5: "CTX_OVERFLOW", -6: "CUDA", -7: "DEVICE_CHECK", -8: "POISONED"}
 
@@ -79,6 +80,8 @@ def lib():
         L.q3_session_pos.argtypes = [vp]
         L.q3_sync.argtypes = [vp]
         L.q3_quantize_q8_0.argtypes = [vp, i64, vp, vp]
+        L.q3_quantize_affine4.argtypes = [vp, i64, vp, vp]
+        L.q3_affine4_to_f16.argtypes = [vp, i64, vp, vp]
         L.q3_model_launch_count.argtypes = [vp]
         L.q3_model_launch_count.restype = i64
         L.q3_op_matmul.argtypes = [vp, vp, i, i, i, vp, i, vp]
@@ -120,6 +123,25 @@ def quantize_q8_0(w: torch.Tensor, stream=None) -> torch.Tensor:
     out = torch.empty(w.shape[:-1] + (w.shape[-1] // 32 * Q8_0_BYTES,), dtype=torch.uint8,
                       device=w.device)
     _check(lib().q3_quantize_q8_0(_ptr(w), w.numel(), _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def quantize_affine4(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """Pack a bf16 CUDA tensor [..., n] into AFFINE4_GS32 groups (uint8 [..., n/32*20])."""
+    assert w.is_cuda and w.dtype == torch.bfloat16 and w.is_contiguous()
+    assert w.shape[-1] % 32 == 0
+    out = torch.empty(w.shape[:-1] + (w.shape[-1] // 32 * AFFINE4_BYTES,), dtype=torch.uint8,
+                      device=w.device)
+    _check(lib().q3_quantize_affine4(_ptr(w), w.numel(), _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def affine4_to_f16(groups: torch.Tensor, n: int, stream=None) -> torch.Tensor:
+    """The fp16 copy [..., n] the model keeps of AFFINE4_GS32 groups [..., n/32*20]."""
+    assert groups.is_cuda and groups.dtype == torch.uint8 and groups.is_contiguous()
+    assert n % 32 == 0 and groups.shape[-1] == n // 32 * AFFINE4_BYTES
+    out = torch.empty(groups.shape[:-1] + (n,), dtype=torch.float16, device=groups.device)
+    _check(lib().q3_affine4_to_f16(_ptr(groups), out.numel(), _ptr(out), _stream_handle(stream)))
     return out
 
 
@@ -186,8 +208,9 @@ class Model:
 
     weights: {"embed", "final_norm", "lm_head" (None if tied), "layers": [...]};
     for a Q8_0 shape the seven projections of each layer must be canonical
-    Q8_0 blocks (uint8), e.g. from quantize_q8_0.  The tensors are borrowed
-    and kept referenced by this object.
+    Q8_0 blocks (uint8), e.g. from quantize_q8_0, and for an AFFINE4 shape
+    AFFINE4_GS32 groups (uint8), e.g. from quantize_affine4.  The tensors are
+    borrowed and kept referenced by this object.
     """
 
     def __init__(self, shape, weights: dict, max_ctx: int, max_round_tokens: int = 2048,
@@ -358,15 +381,16 @@ class Session:
 
 def device_weights(shape, weights: dict) -> dict:
     """The weight dict the library takes: bf16 tensors as given; for a Q8_0
-    shape the seven projections packed to canonical blocks by the library's
-    own quantizer (q3_quantize_q8_0)."""
-    if shape.scheme != Q8_0:
+    or AFFINE4 shape the seven projections packed by the library's own
+    quantizer (q3_quantize_q8_0, q3_quantize_affine4)."""
+    if shape.scheme not in (Q8_0, AFFINE4):
         return weights
+    pack = quantize_q8_0 if shape.scheme == Q8_0 else quantize_affine4
     out = dict(weights)
     out["layers"] = []
     for lw in weights["layers"]:
         d = dict(lw)
         for name in PROJ:
-            d[name] = quantize_q8_0(lw[name])
+            d[name] = pack(lw[name])
         out["layers"].append(d)
     return out

@@ -354,6 +354,88 @@ __global__ void quantize_q8_0_kernel(const __nv_bfloat16* w, int64_t nblocks, ui
     }
 }
 
+// ---------------------------------------------------------------- AFFINE4_GS32
+// 20-byte group: 16 code bytes (weight 2i in the low nibble of byte i, weight
+// 2i + 1 in the high nibble), then fp16 scale and fp16 bias, little-endian;
+// a weight is scale * code + bias.  As five little-endian words, weight i's
+// code sits in word i / 8 at bit 4 (i % 8), and word 4 holds scale | bias << 16.
+
+// Per group of 32: bias = fp16(min), scale = fp16((max - min) / 15) (FP32,
+// correctly rounded), code = round-half-even((w - bias) / scale) in FP32
+// against the stored scale and bias, clamped to [0, 15]; a zero scale gives
+// zero codes.  One thread per group.
+__global__ void quantize_affine4_kernel(const __nv_bfloat16* w, int64_t ngroups, uint8_t* groups)
+{
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ngroups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        float x[32];
+        const uint4* src = reinterpret_cast<const uint4*>(w + g * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 u = src[v];
+            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[8 * v + 2 * e] = __uint_as_float(wd[e] << 16);
+                x[8 * v + 2 * e + 1] = __uint_as_float(wd[e] & 0xffff0000u);
+            }
+        }
+        float lo = x[0], hi = x[0];
+#pragma unroll
+        for (int i = 1; i < 32; ++i) {
+            if (x[i] < lo) lo = x[i];
+            if (x[i] > hi) hi = x[i];
+        }
+        const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
+        const __half bh = __float2half_rn(lo);
+        const float scale = __half2float(sh), bias = __half2float(bh);
+        uint32_t out[5] = {0u, 0u, 0u, 0u,
+                           (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(bh) << 16)};
+        if (scale != 0.f) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                int q = __float2int_rn(__fdiv_rn(__fsub_rn(x[i], bias), scale));
+                q = q < 0 ? 0 : (q > 15 ? 15 : q);
+                out[i / 8] |= (uint32_t)q << (4 * (i % 8));
+            }
+        }
+        uint32_t* dst = reinterpret_cast<uint32_t*>(groups + g * Q3_AFFINE4_BYTES);
+#pragma unroll
+        for (int k = 0; k < 5; ++k) dst[k] = out[k];
+    }
+}
+
+// fp16(fma(scale, code, bias)) for the tensor-core path; one thread per group.
+__global__ void affine4_to_f16_kernel(const uint8_t* groups, int64_t ngroups, __half* w,
+                                      unsigned long long* overflow)
+{
+    unsigned long long n_over = 0;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < ngroups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t* in = reinterpret_cast<const uint32_t*>(groups + g * Q3_AFFINE4_BYTES);
+        const uint32_t sb = in[4];
+        const float scale = __half2float(__ushort_as_half((unsigned short)(sb & 0xffffu)));
+        const float bias = __half2float(__ushort_as_half((unsigned short)(sb >> 16)));
+        uint4* dst = reinterpret_cast<uint4*>(w + g * 32);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t c = in[k];
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float v0 = __fmaf_rn(scale, (float)((c >> (8 * e)) & 0xfu), bias);
+                const float v1 = __fmaf_rn(scale, (float)((c >> (8 * e + 4)) & 0xfu), bias);
+                if (!(fabsf(v0) <= 65504.0f)) ++n_over;
+                if (!(fabsf(v1) <= 65504.0f)) ++n_over;
+                h[e] = (uint32_t)__half_as_ushort(__float2half_rn(v0)) |
+                       ((uint32_t)__half_as_ushort(__float2half_rn(v1)) << 16);
+            }
+            dst[k] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+    }
+    if (n_over && overflow) atomicAdd(overflow, n_over);
+}
+
 }  // namespace
 
 cudaError_t launch_embed(const Launch& L, const int32_t* tokens, int T, const __nv_bfloat16* E,
@@ -403,6 +485,27 @@ cudaError_t launch_bf16_to_f16(cudaStream_t s, const __nv_bfloat16* w, int64_t n
     if (grid > 152 * 32) grid = 152 * 32;
     if (grid < 1) grid = 1;
     bf16_to_f16_kernel<<<(unsigned)grid, 256, 0, s>>>(w, n, out, inexact, overflow);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_affine4(cudaStream_t s, const __nv_bfloat16* w, int64_t n, uint8_t* groups)
+{
+    const int64_t ng = n / 32;
+    int grid = (int)((ng + 255) / 256);
+    if (grid > 152 * 32) grid = 152 * 32;
+    if (grid < 1) grid = 1;
+    quantize_affine4_kernel<<<grid, 256, 0, s>>>(w, ng, groups);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_affine4_to_f16(cudaStream_t s, const uint8_t* groups, int64_t n, __half* w,
+                                  unsigned long long* overflow)
+{
+    const int64_t ng = n / 32;
+    int grid = (int)((ng + 255) / 256);
+    if (grid > 152 * 32) grid = 152 * 32;
+    if (grid < 1) grid = 1;
+    affine4_to_f16_kernel<<<grid, 256, 0, s>>>(groups, ng, w, overflow);
     return cudaGetLastError();
 }
 

@@ -255,5 +255,10 @@ cudaError_t launch_q8_to_f16(const Launch& L, const int8_t* qs, const __half* sc
 cudaError_t launch_bf16_to_f16(cudaStream_t s, const __nv_bfloat16* w, int64_t n, __half* out,
                                unsigned long long* inexact, unsigned long long* overflow);
 cudaError_t launch_quantize_q8_0(cudaStream_t s, const __nv_bfloat16* w, int64_t n, uint8_t* blocks);
+// AFFINE4_GS32: bf16 -> 20-byte groups; groups -> fp16 tensor-core operand,
+// counting values beyond the fp16 range in *overflow (may be NULL).
+cudaError_t launch_quantize_affine4(cudaStream_t s, const __nv_bfloat16* w, int64_t n, uint8_t* groups);
+cudaError_t launch_affine4_to_f16(cudaStream_t s, const uint8_t* groups, int64_t n, __half* w,
+                                  unsigned long long* overflow);
 
 }  // namespace q3

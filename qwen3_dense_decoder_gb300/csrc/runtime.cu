@@ -315,7 +315,7 @@ int validate_config(const q3_config* c)
         return fail(Q3_ERR_INVALID_ARG, "config: n_q_heads must be a multiple (<= 8x) of n_kv_heads");
     if (c->hidden % 128 || c->ffn % 128 || c->vocab % 128)
         return fail(Q3_ERR_INVALID_ARG, "config: hidden, ffn and vocab must be multiples of 128");
-    if (c->scheme != Q3_BF16 && c->scheme != Q3_Q8_0)
+    if (c->scheme != Q3_BF16 && c->scheme != Q3_Q8_0 && c->scheme != Q3_AFFINE4)
         return fail(Q3_ERR_INVALID_ARG, "config: unknown weight scheme %d", c->scheme);
     if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f))
         return fail(Q3_ERR_INVALID_ARG, "config: rms_eps and rope_theta must be positive");
@@ -518,6 +518,7 @@ L2Prefetch decode_weights(const q3_model* m, int l, int g)
 int setup_decode_step(q3_model* m, int n_sm)
 {
     const q3_config& c = m->c;
+    if (c.scheme == Q3_AFFINE4) return Q3_OK;   // no AFFINE4 consumer in the step
     const bool q8 = c.scheme == Q3_Q8_0;
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -615,7 +616,9 @@ int run_round(q3_model* m, const Round& r)
     const int* row_pos = m->meta;
     const int* row_slot = m->meta + m->max_rows;
     const int* last_rows = m->meta + 2 * m->max_rows;
-    const bool one = (T == 1);
+    // one-row rounds take the GEMV path, which reads BF16 or Q8_0 weights;
+    // AFFINE4 rounds of any size take the tensor-core path over the fp16 copy
+    const bool one = (T == 1) && c.scheme != Q3_AFFINE4;
     const bool q8 = c.scheme == Q3_Q8_0;
     Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
     // one launcher call, bracketed by profiling events of kernel class cls
@@ -1062,6 +1065,10 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
         if (c.scheme == Q3_BF16)
             for (int i : {1, 2, 3, 6, 8, 9, 10})
                 if (!aligned16(ps[i])) return bad(Q3_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+        if (c.scheme == Q3_AFFINE4)
+            for (int i : {1, 2, 3, 6, 8, 9, 10})
+                if (reinterpret_cast<uintptr_t>(ps[i]) & 3)
+                    return bad(Q3_ERR_INVALID_ARG, "AFFINE4 groups must be 4-byte aligned");
     }
 
     const size_t R = m->rows_alloc;
@@ -1163,6 +1170,28 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
                 m->w16[l][p] = d;
                 if (launch_q8_to_f16(L0, m->q8[l][p].qs, m->q8[l][p].sc, (int64_t)n, d) != cudaSuccess)
                     return bad(Q3_ERR_CUDA, "Q8_0 dequantisation failed");
+                const uint32_t box = (p == P_G || p == P_U) ? 64 : 128;
+                if (!tmap_f16(&m->maps[l].m[p], d, proj_rows[p], proj_cols[p], box))
+                    return bad(Q3_ERR_CUDA, "tensor map encoding failed");
+            }
+        }
+    } else if (c.scheme == Q3_AFFINE4) {
+        // fp16 copies of the dequantised groups for the tensor-core path, which
+        // runs every AFFINE4 round: fp16(fma(scale, code, bias))
+        m->maps.resize(c.n_layers);
+        m->w16.resize(c.n_layers);
+        for (int l = 0; l < c.n_layers && ok; ++l) {
+            const q3_layer_weights& L = m->layers[l];
+            const void* src[N_PROJ] = {L.wq, L.wk, L.wv, L.wo, L.w_gate, L.w_up, L.w_down};
+            m->w16[l].resize(N_PROJ);
+            for (int p = 0; p < N_PROJ; ++p) {
+                const size_t n = (size_t)proj_rows[p] * proj_cols[p];
+                f16* d = static_cast<f16*>(A(n * sizeof(f16)));
+                if (!ok) break;
+                m->w16[l][p] = d;
+                if (launch_affine4_to_f16(m->stream, static_cast<const uint8_t*>(src[p]), (int64_t)n, d,
+                                          m->conv_counts + 1) != cudaSuccess)
+                    return bad(Q3_ERR_CUDA, "AFFINE4 dequantisation failed");
                 const uint32_t box = (p == P_G || p == P_U) ? 64 : 128;
                 if (!tmap_f16(&m->maps[l].m[p], d, proj_rows[p], proj_cols[p], box))
                     return bad(Q3_ERR_CUDA, "tensor map encoding failed");
@@ -1421,6 +1450,30 @@ int q3_quantize_q8_0(const void* w_dev, int64_t n, void* blocks_dev, void* strea
     cudaError_t e = launch_quantize_q8_0(static_cast<cudaStream_t>(stream), static_cast<const bf16*>(w_dev),
                                          n, static_cast<uint8_t*>(blocks_dev));
     if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "quantize: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+int q3_quantize_affine4(const void* w_dev, int64_t n, void* groups_dev, void* stream)
+{
+    if (!w_dev || !groups_dev || n < 0 || n % 32 || !aligned16(w_dev) ||
+        (reinterpret_cast<uintptr_t>(groups_dev) & 3))
+        return fail(Q3_ERR_INVALID_ARG, "quantize: bad argument");
+    if (n == 0) return Q3_OK;
+    cudaError_t e = launch_quantize_affine4(static_cast<cudaStream_t>(stream), static_cast<const bf16*>(w_dev),
+                                            n, static_cast<uint8_t*>(groups_dev));
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "quantize: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+int q3_affine4_to_f16(const void* groups_dev, int64_t n, void* out_dev, void* stream)
+{
+    if (!groups_dev || !out_dev || n < 0 || n % 32 || !aligned16(out_dev) ||
+        (reinterpret_cast<uintptr_t>(groups_dev) & 3))
+        return fail(Q3_ERR_INVALID_ARG, "dequantize: bad argument");
+    if (n == 0) return Q3_OK;
+    cudaError_t e = launch_affine4_to_f16(static_cast<cudaStream_t>(stream), static_cast<const uint8_t*>(groups_dev),
+                                          n, static_cast<f16*>(out_dev), nullptr);
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "dequantize: %s", cudaGetErrorString(e));
     return Q3_OK;
 }
 

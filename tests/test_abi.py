@@ -27,7 +27,7 @@ def test_header_declares_the_boundary():
     for required in ("q3_model_create", "q3_model_destroy", "q3_pool_create", "q3_session_create",
                      "q3_session_set_block_table", "q3_session_eval", "q3_eval_batch",
                      "q3_session_truncate", "q3_session_reset", "q3_session_pos", "q3_sync",
-                     "q3_last_error", "q3_quantize_q8_0"):
+                     "q3_last_error", "q3_quantize_q8_0", "q3_quantize_affine4", "q3_affine4_to_f16"):
         assert required in names
 
 
@@ -47,6 +47,15 @@ def test_host_side_argument_checks_need_no_gpu(libq3):
     assert libq3.q3_model_create(None, None, 16, None, None) == -1
     assert libq3.q3_session_eval(None, None, 1, None, None) == -1
     assert libq3.q3_quantize_q8_0(None, ctypes.c_int64(32), None, None) == -1
+    assert libq3.q3_quantize_affine4(None, ctypes.c_int64(32), None, None) == -1
+    assert libq3.q3_affine4_to_f16(None, ctypes.c_int64(32), None, None) == -1
+    # misaligned pointers and ragged lengths are rejected before any memory access
+    p16, p1 = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 1)
+    assert libq3.q3_quantize_affine4(p1, ctypes.c_int64(32), p16, None) == -1
+    assert libq3.q3_quantize_affine4(p16, ctypes.c_int64(32), p1, None) == -1
+    assert libq3.q3_quantize_affine4(p16, ctypes.c_int64(33), p16, None) == -1
+    assert libq3.q3_affine4_to_f16(p1, ctypes.c_int64(32), p16, None) == -1
+    assert libq3.q3_affine4_to_f16(p16, ctypes.c_int64(32), ctypes.c_void_p((1 << 20) + 8), None) == -1
     assert libq3.q3_op_matmul(None, None, 128, 1, 64, None, 0, None) == -1
     assert b"bad argument" in libq3.q3_last_error()
 
@@ -61,12 +70,11 @@ def test_host_side_argument_checks_need_no_gpu(libq3):
 
 
 def test_config_checks_need_no_gpu(libq3):
-    # a config is checked before any CUDA call: a weight scheme the CUDA path
-    # does not implement (AFFINE4_GS32 is oracle-only so far) fails loudly
+    # a config is checked before any CUDA call: an unknown weight scheme fails loudly
     from qwen3_dense_decoder_gb300 import _Config
     libq3.q3_last_error.restype = ctypes.c_char_p
     out = ctypes.c_void_p()
-    for scheme, msg in ((2, b"unknown weight scheme 2"), (-1, b"unknown weight scheme -1")):
+    for scheme, msg in ((3, b"unknown weight scheme 3"), (-1, b"unknown weight scheme -1")):
         cfg = _Config(2, 1024, 16, 8, 128, 3072, 4096, 64, 1e6, 1e-6, 1, scheme)
         assert libq3.q3_model_create(ctypes.byref(cfg), None, 16, None, ctypes.byref(out)) == -1
         assert msg in libq3.q3_last_error()

@@ -200,6 +200,18 @@ def test_qwen3_8b_q8_0_shape_two_layers():
     _run(pair, g, o, [prompt], 4, "8b-q8_0")
 
 
+def test_qwen3_4b_affine4_shape_two_layers():
+    """AFFINE4_GS32 projections: both sides quantize the same bf16 weights
+    (bit-equal packers), so the gate is the usual one against the oracle's
+    AFFINE4 forward; one-token decode rounds take the tensor-core path."""
+    shape = make_shape("4b", n_layers=2, scheme=synthetic.AFFINE4, name="qwen3-4b-affine4")
+    pair = Pair(shape, seed=505, max_ctx=128, max_round_tokens=64, n_blocks=8)
+    g, o = pair.sessions(table=synthetic.make_block_permutation(8, seed=6)[:3])
+    prompt = synthetic.make_tokens(40, shape.vocab, seed=24)
+    _run(pair, g, o, [prompt[:7], prompt[7:40]], 4, "4b-affine4")
+    assert not pair.model.fused_decode
+
+
 def test_qwen3_4b_shape_full_depth():
     shape = make_shape("4b")
     pair = Pair(shape, seed=404, max_ctx=128, max_round_tokens=64, n_blocks=8)

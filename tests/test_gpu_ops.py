@@ -4,6 +4,10 @@ seeded inputs (the pages' operator tests: "Reproducing Kipp", section
 
 - Q8_0 packing: the library's CUDA quantizer and the oracle's packer agree
   bit for bit ("Kipp Model Support", section "Quantization (Q8_0)").
+- AFFINE4_GS32 packing and the fp16 copy of its groups: the CUDA quantizer
+  and the oracle's packer agree bit for bit, and the fp16 copy is the fp16
+  rounding of the oracle's dequantised values, bit for bit ("Kipp Model
+  Support", section "Quantization (AFFINE4_GS32)").
 - tcgen05 GEMM: fp16 inputs (the prefill operand type), FP32 accumulation,
   against an FP64 matmul of the same values; shapes span several tiles and ragged token counts (1, 5, 40, 83,
   200, 300) so every N tile width and the tile tail are exercised.
@@ -43,6 +47,45 @@ def test_quantizer_matches_oracle_packer_bitwise(q3, orc):
     got = q3.quantize_q8_0(w).cpu().numpy()
     ref = orc.q8_0_pack(_f32(w))
     np.testing.assert_array_equal(got, ref)
+
+
+def _affine4_edge_rows(w):
+    """Edge groups: all zero, signed zeros, constant, a linear ramp, a range
+    whose scale is an fp16 subnormal (codes clamp at 15), mixed signs."""
+    dev = w.device
+    w[3, :32] = 0
+    w[4, :32] = 0
+    w[4, 1:32:3] = -0.0
+    w[4, 0] = -0.0
+    w[5, 32:64] = 0.75
+    w[6, 64:96] = torch.linspace(-1, 1, 32, device=dev).to(torch.bfloat16)
+    k = torch.tensor(list(range(19)) + list(range(13)), dtype=torch.float32, device=dev)
+    w[7, 96:128] = (k * 2.0 ** -24).to(torch.bfloat16)
+    w[8, :32] = torch.tensor([(-1) ** i * (i + 1) for i in range(32)], dtype=torch.float32,
+                             device=dev).to(torch.bfloat16)
+    return w
+
+
+@pytest.mark.parametrize("rows,n", [(96, 4096), (3, 7 * 32), (1, 32)])
+def test_affine4_quantizer_matches_oracle_packer_bitwise(q3, orc, rows, n):
+    w = _bf16((rows, n), 7, 0.02)
+    if rows >= 9 and n >= 128:
+        w = _affine4_edge_rows(w)
+    got = q3.quantize_affine4(w).cpu().numpy()
+    assert got.shape == (rows, n // 32 * 20)
+    ref = orc.affine4_pack(_f32(w))
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("rows,n", [(96, 4096), (5, 9 * 32)])
+def test_affine4_f16_copy_matches_oracle_dequant_bitwise(q3, orc, rows, n):
+    w = _bf16((rows, n), 8, 0.02)
+    if rows >= 9:
+        w = _affine4_edge_rows(w)
+    groups = q3.quantize_affine4(w)
+    got = q3.affine4_to_f16(groups, n).cpu().numpy()
+    ref = orc.affine4_unpack(groups.cpu().numpy(), n).astype(np.float16)
+    np.testing.assert_array_equal(got.view(np.uint16), ref.view(np.uint16))
 
 
 @pytest.mark.parametrize("bn", [0, 32, 64, 96, 128, 192, 256])
