@@ -67,8 +67,9 @@ def parse():
     ap.add_argument("--no-b32", action="store_true", help="skip the batch-32 decode leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
     ap.add_argument("--shapes", nargs="*", default=None,
-                    choices=("0.6b", "8b-q8_0", "14b"),
-                    help="measure the other named shapes instead (one JSON line each; all three if none given)")
+                    choices=("0.6b", "8b-q8_0", "14b", "4b-affine4"),
+                    help="measure the other named shapes instead (one JSON line each; 0.6b, 8b-q8_0 "
+                         "and 14b if none given)")
     ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill", "attn-decode-b32"),
                     default=None,
                     help="run only a small case sized for an ncu capture (a few GB on the device) and exit")
@@ -481,11 +482,18 @@ def q8_bytes(params: int) -> float:
     return params * 34.0 / 32.0
 
 
+def affine4_bytes(params: int) -> float:
+    """AFFINE4_GS32 bytes of `params` weights: 20-byte groups of 32 (5.0 bits a weight)."""
+    return params * 20.0 / 32.0
+
+
 def step_bytes(s, ctxs) -> float:
-    """HBM bytes of one decode step: every projection once (bf16, or Q8_0
-    blocks), the lm_head once (bf16), and the K/V of every cached position of
-    every session."""
-    w = (q8_bytes(proj_params(s)) if s.scheme == 1 else 2.0 * proj_params(s)) + 2.0 * s.vocab * s.hidden
+    """HBM bytes of one decode step: every projection once (bf16, Q8_0 blocks
+    or AFFINE4 groups: the format's bytes, whatever copy the kernels read), the
+    lm_head once (bf16), and the K/V of every cached position of every session."""
+    p = proj_params(s)
+    pw = {1: q8_bytes(p), 2: affine4_bytes(p)}.get(s.scheme, 2.0 * p)
+    w = pw + 2.0 * s.vocab * s.hidden
     return w + s.n_layers * 2 * s.kv_width * 2 * float(sum(ctxs))
 
 
@@ -493,7 +501,9 @@ def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
     """The named workload of one shape ("Kipp Model Support", section "The
     registry"): 0.6B -- a 128-token prompt, 64 greedy decode steps, and a ragged
     3-round prefill (5, 40, 83); 8B Q8_0 -- a 2,048-token prefill, then decode at
-    batch 1 and at 32 sessions with prompts U[64, 2048]; 14B -- a 12,800-token
+    batch 1 and at 32 sessions with prompts U[64, 2048] (the same for 4B
+    AFFINE4_GS32, the scheme of "Kipp Roadmap", status v0.0.4's 2,048-token
+    prefill figures); 14B -- a 12,800-token
     prefill in 2,048-token chunks, then 8 sessions decoding 128 tokens at a
     16,384-token context over one shared block pool with permuted tables."""
     import numpy as np
@@ -506,11 +516,12 @@ def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
     torch.cuda.set_stream(st)
     w = synthetic.make_weights(s, seed=1234, device="cuda")     # bf16 source (the oracle packs its own)
     wg = w
-    if s.scheme == synthetic.Q8_0:
+    if s.scheme in (synthetic.Q8_0, synthetic.AFFINE4):
+        pack = q3.quantize_q8_0 if s.scheme == synthetic.Q8_0 else q3.quantize_affine4
         wg = dict(w, layers=[dict(lw) for lw in w["layers"]])
         for lw in wg["layers"]:
             for nm in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
-                lw[nm] = q3.quantize_q8_0(lw[nm])
+                lw[nm] = pack(lw[nm])
     V = s.vocab
 
     def timed(fn):
@@ -522,7 +533,9 @@ def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
         b.synchronize()
         return a.elapsed_time(b)
 
-    out = {"shape": s.name, "n_gpus": 1, "dtype": "bf16" if s.scheme == synthetic.BF16 else "q8_0 weights, fp16/bf16 compute",
+    dtype = {synthetic.BF16: "bf16", synthetic.Q8_0: "q8_0 weights, fp16/bf16 compute",
+             synthetic.AFFINE4: "affine4_gs32 weights, fp16/bf16 compute"}[s.scheme]
+    out = {"shape": s.name, "n_gpus": 1, "dtype": dtype,
            "data": "synthetic (seeded random-init weights and tokens)", "peak_kind": pk_kind}
     lg = torch.empty(max(32, 8), V, dtype=torch.float32, device="cuda")
     am = torch.zeros(max(32, 8), dtype=torch.int32, device="cuda")
@@ -571,7 +584,7 @@ def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
         ms = timed(ragged)
         out["prefill_ragged_5_40_83"] = prefill_entry(sum(rounds), ms)
         ses.close()
-    elif name == "8b-q8_0":
+    elif name in ("8b-q8_0", "4b-affine4"):
         m = q3.Model(s, wg, max_ctx=2400, max_round_tokens=2048, stream=st)
         pool = m.pool(34 * 75 + 8, 36)
         ses = pool.session()

@@ -54,6 +54,7 @@ SHAPES = {
     "0.6b": Shape("qwen3-0.6b", 28, 1024, 16, 8, 128, 3072, 151936, True),
     "4b": Shape("qwen3-4b", 36, 2560, 32, 8, 128, 9728, 151936, True),
     "8b-q8_0": Shape("qwen3-8b-q8_0", 36, 4096, 32, 8, 128, 12288, 151936, False, Q8_0),
+    "4b-affine4": Shape("qwen3-4b-affine4", 36, 2560, 32, 8, 128, 9728, 151936, True, AFFINE4),
     "14b": Shape("qwen3-14b", 40, 5120, 40, 8, 128, 17408, 151936, False),
 }
 

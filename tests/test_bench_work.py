@@ -36,6 +36,10 @@ def test_decode_step_bytes():
     s8 = S["8b-q8_0"]
     w8 = 6_945_767_424 * 34 / 32 + 2 * 151_936 * 4096
     assert abs(bench.step_bytes(s8, [0]) - w8) < 1 and 8.61e9 < w8 < 8.63e9
+    # AFFINE4_GS32 projections at 20 B per 32 weights, tied BF16 lm_head: 3.05 GB
+    sa = S["4b-affine4"]
+    wa = 3_633_315_840 * 20 / 32 + 2 * 151_936 * 2560
+    assert abs(bench.step_bytes(sa, [0]) - wa) < 1 and 3.04e9 < wa < 3.05e9
     # 14B: 27.98 GB of weights, 163,840 B of K/V per position (40 layers)
     s14 = S["14b"]
     w14 = 2 * 13_212_057_600 + 2 * 151_936 * 5120
