@@ -41,7 +41,7 @@ class _Cfg(C.Structure):
     _fields_ = [("n_layers", C.c_int), ("hidden", C.c_int), ("n_q_heads", C.c_int),
                 ("n_kv_heads", C.c_int), ("head_dim", C.c_int), ("ffn", C.c_int),
                 ("vocab", C.c_int), ("tied", C.c_int), ("scheme", C.c_int),
-                ("rope_theta", C.c_double), ("rms_eps", C.c_double)]
+                ("rope_theta", C.c_double), ("rms_eps", C.c_double), ("kv_quant", C.c_int)]
 
 
 class _Layer(C.Structure):
@@ -84,6 +84,8 @@ def lib():
         L.orc_eval.argtypes = [vp, vp, i, vp, vp]
         L.orc_eval_batch.argtypes = [vp, vp, vp, i, vp]
         L.orc_argmax.argtypes = [vp, i]
+        L.orc_kv_bytes_per_position.argtypes = [C.POINTER(_Cfg)]
+        L.orc_kv_bytes_per_position.restype = C.c_long
         _lib = L
     return _lib
 
@@ -202,6 +204,18 @@ def argmax(v: np.ndarray) -> int:
 
 # ---------------------------------------------------------------- model
 
+def _cfg(shape) -> _Cfg:
+    return _Cfg(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
+                shape.head_dim, shape.ffn, shape.vocab, int(shape.tied), shape.scheme,
+                shape.rope_theta, shape.rms_eps, getattr(shape, "kv_quant", BF16))
+
+
+def kv_bytes_per_position(shape) -> int:
+    """Bytes one position's K and V take in one layer's cache (bf16 or Q8_0)."""
+    cfg = _cfg(shape)
+    return lib().orc_kv_bytes_per_position(C.byref(cfg))
+
+
 class Model:
     """Oracle model over host copies of the synthetic weights.
 
@@ -247,9 +261,7 @@ class Model:
                 ptrs["attn_norm"], ptrs["q_norm"], ptrs["k_norm"], ptrs["ffn_norm"])
             L.wq, L.wk, L.wv, L.wo = ptrs["wq"], ptrs["wk"], ptrs["wv"], ptrs["wo"]
             L.wg, L.wu, L.wd = ptrs["w_gate"], ptrs["w_up"], ptrs["w_down"]
-        cfg = _Cfg(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
-                   shape.head_dim, shape.ffn, shape.vocab, int(shape.tied), shape.scheme,
-                   shape.rope_theta, shape.rms_eps)
+        cfg = _cfg(shape)
         self._layers = layers
         self.h = lib().orc_model_create(C.byref(cfg), emb, fnorm, lm, layers, self.n_threads)
         if not self.h:

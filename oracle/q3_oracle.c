@@ -6,7 +6,8 @@
  * Sources (Kipp pages): "Kipp Model Support" (sections "The registry",
  * "What the gates check", "qwen3-0.6b-base", "Quantization (Q8_0)",
  * "Quantization (AFFINE4_GS32)"),
- * "Kipp Roadmap" (status v0.0.2: paged KV and batched evaluation), and
+ * "Kipp Roadmap" (status v0.0.2: paged KV and batched evaluation; status
+ * v0.0.4: the Q8_0 KV cache), and
  * "Reproducing Kipp" (section "Model-backed CPU and Metal gates").  Where the
  * pages leave the layer math open, the oracle takes the plain reading of a
  * standard dense Qwen3 decoder; each such reading is marked "reading".
@@ -324,8 +325,27 @@ void orc_matmul(const void* W, int scheme, int n_out, int n_in,
 /* Causal softmax attention of one query row over ctx cached positions
  * (reading: scale 1/sqrt(d), the max subtracted before exp, contiguous GQA
  * grouping: query head h reads KV head h / (n_q / n_kv)). */
+static void gqa_attend_f32(const float* q, const float* K, const float* V,
+                           int ctx, int n_q, int n_kv, int d, float* o);
+
 void orc_gqa_attend(const float* q, const uint16_t* K, const uint16_t* V,
                     int ctx, int n_q, int n_kv, int d, float* o)
+{
+    long n = (long)ctx * n_kv * d;
+    float* Kf = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
+    float* Vf = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
+    for (long i = 0; i < n; i++) {
+        Kf[i] = orc_bf16_to_f32(K[i]);
+        Vf[i] = orc_bf16_to_f32(V[i]);
+    }
+    gqa_attend_f32(q, Kf, Vf, ctx, n_q, n_kv, d, o);
+    free(Kf);
+    free(Vf);
+}
+
+/* The same over K and V already in FP32 (exact bf16 or Q8_0 values). */
+static void gqa_attend_f32(const float* q, const float* K, const float* V,
+                           int ctx, int n_q, int n_kv, int d, float* o)
 {
     int group = n_q / n_kv;
     double scale = 1.0 / sqrt((double)d);
@@ -335,9 +355,9 @@ void orc_gqa_attend(const float* q, const uint16_t* K, const uint16_t* V,
         const float* qh = q + (long)h * d;
         double mx = -INFINITY;
         for (int j = 0; j < ctx; j++) {
-            const uint16_t* kj = K + ((long)j * n_kv + kvh) * d;
+            const float* kj = K + ((long)j * n_kv + kvh) * d;
             double dot = 0.0;
-            for (int i = 0; i < d; i++) dot += (double)qh[i] * orc_bf16_to_f32(kj[i]);
+            for (int i = 0; i < d; i++) dot += (double)qh[i] * kj[i];
             s[j] = dot * scale;
             if (s[j] > mx) mx = s[j];
         }
@@ -346,7 +366,7 @@ void orc_gqa_attend(const float* q, const uint16_t* K, const uint16_t* V,
         for (int i = 0; i < d; i++) {
             double acc = 0.0;
             for (int j = 0; j < ctx; j++)
-                acc += s[j] * orc_bf16_to_f32(V[((long)j * n_kv + kvh) * d + i]);
+                acc += s[j] * V[((long)j * n_kv + kvh) * d + i];
             o[(long)h * d + i] = (float)(acc / z);
         }
     }
@@ -367,7 +387,7 @@ struct orc_model {
 struct orc_pool {
     orc_model* m;
     int n_blocks;
-    uint16_t *k, *v;        /* [L][n_blocks][32][n_kv][d] bf16 */
+    uint8_t *k, *v;         /* [L][n_blocks][32] K (V) rows of kv_row_bytes */
     unsigned char* used;
 };
 
@@ -375,7 +395,7 @@ struct orc_session {
     orc_model* m;
     orc_pool* pool;         /* NULL: contiguous */
     int max_ctx, pos;
-    uint16_t *k, *v;        /* contiguous: [L][max_ctx][n_kv][d] bf16 */
+    uint8_t *k, *v;         /* contiguous: [L][max_ctx] K (V) rows of kv_row_bytes */
     int32_t* table;         /* paged: block id per 32 positions */
     int n_table, n_given;   /* blocks taken; entries given by the caller */
 };
@@ -385,6 +405,8 @@ orc_model* orc_model_create(const orc_cfg* cfg, const uint16_t* embed,
                             const orc_layer* layers, int n_threads)
 {
     if (cfg->n_q_heads % cfg->n_kv_heads || cfg->head_dim % 2 ||
+        (cfg->kv_quant != ORC_BF16 && cfg->kv_quant != ORC_Q8_0) ||
+        (cfg->kv_quant == ORC_Q8_0 && cfg->head_dim % ORC_BLOCK) ||
         (cfg->scheme != ORC_BF16 && cfg->scheme != ORC_Q8_0 && cfg->scheme != ORC_AFFINE4) ||
         (cfg->scheme != ORC_BF16 && (cfg->hidden % ORC_BLOCK || cfg->ffn % ORC_BLOCK ||
                                      (cfg->n_q_heads * cfg->head_dim) % ORC_BLOCK)))
@@ -409,14 +431,23 @@ void orc_model_free(orc_model* m)
 
 static long kv_row(const orc_cfg* c) { return (long)c->n_kv_heads * c->head_dim; }
 
+/* Bytes of one position's K (or V) row: bf16 values, or Q8_0 blocks of 32
+ * consecutive values (a head row of d values is d/32 whole blocks). */
+static long kv_row_bytes(const orc_cfg* c)
+{
+    return c->kv_quant == ORC_Q8_0 ? kv_row(c) / ORC_BLOCK * ORC_Q8_0_BYTES : kv_row(c) * 2;
+}
+
+long orc_kv_bytes_per_position(const orc_cfg* c) { return 2 * kv_row_bytes(c); }
+
 orc_pool* orc_pool_create(orc_model* m, int n_blocks)
 {
     orc_pool* p = (orc_pool*)calloc(1, sizeof(orc_pool));
-    long n = (long)m->c.n_layers * n_blocks * ORC_BLOCK * kv_row(&m->c);
+    long n = (long)m->c.n_layers * n_blocks * ORC_BLOCK * kv_row_bytes(&m->c);
     p->m = m;
     p->n_blocks = n_blocks;
-    p->k = (uint16_t*)calloc(n, 2);
-    p->v = (uint16_t*)calloc(n, 2);
+    p->k = (uint8_t*)calloc(n, 1);
+    p->v = (uint8_t*)calloc(n, 1);
     p->used = (unsigned char*)calloc(n_blocks, 1);
     if (!p->k || !p->v || !p->used) { orc_pool_free(p); return NULL; }
     return p;
@@ -435,9 +466,9 @@ orc_session* orc_session_create(orc_model* m, orc_pool* pool, int max_ctx)
     s->pool = pool;
     s->max_ctx = max_ctx;
     if (!pool) {
-        long n = (long)m->c.n_layers * max_ctx * kv_row(&m->c);
-        s->k = (uint16_t*)calloc(n, 2);
-        s->v = (uint16_t*)calloc(n, 2);
+        long n = (long)m->c.n_layers * max_ctx * kv_row_bytes(&m->c);
+        s->k = (uint8_t*)calloc(n, 1);
+        s->v = (uint8_t*)calloc(n, 1);
         if (!s->k || !s->v) { orc_session_free(s); return NULL; }
     } else {
         s->table = (int32_t*)calloc((max_ctx + ORC_BLOCK - 1) / ORC_BLOCK, sizeof(int32_t));
@@ -495,16 +526,42 @@ static int reserve(orc_session* s, int end)
 }
 
 /* address of the K (or V) row of position p in layer l */
-static uint16_t* kv_slot(orc_session* s, int l, int p, int is_v)
+static uint8_t* kv_slot(orc_session* s, int l, int p, int is_v)
 {
     const orc_cfg* c = &s->m->c;
     if (!s->pool) {
-        uint16_t* base = is_v ? s->v : s->k;
-        return base + ((long)l * s->max_ctx + p) * kv_row(c);
+        uint8_t* base = is_v ? s->v : s->k;
+        return base + ((long)l * s->max_ctx + p) * kv_row_bytes(c);
     }
-    uint16_t* base = is_v ? s->pool->v : s->pool->k;
+    uint8_t* base = is_v ? s->pool->v : s->pool->k;
     long blk = s->table[p / ORC_BLOCK];
-    return base + (((long)l * s->pool->n_blocks + blk) * ORC_BLOCK + p % ORC_BLOCK) * kv_row(c);
+    return base + (((long)l * s->pool->n_blocks + blk) * ORC_BLOCK + p % ORC_BLOCK) * kv_row_bytes(c);
+}
+
+/* store one position's K (or V) row: rounded to bf16, or packed to Q8_0
+ * blocks straight from FP32 (reading: the quantizer of the weights) */
+static void kv_store(const orc_cfg* c, const float* row, uint8_t* slot)
+{
+    if (c->kv_quant == ORC_Q8_0) {
+        orc_q8_0_pack(row, kv_row(c), slot);
+        return;
+    }
+    for (long i = 0; i < kv_row(c); i++) {
+        uint16_t b = orc_f32_to_bf16(row[i]);
+        slot[2 * i] = (uint8_t)(b & 0xff);
+        slot[2 * i + 1] = (uint8_t)(b >> 8);
+    }
+}
+
+/* read it back as FP32 values (exact: bf16 widening, or fp16 scale times quant) */
+static void kv_load(const orc_cfg* c, const uint8_t* slot, float* row)
+{
+    if (c->kv_quant == ORC_Q8_0) {
+        orc_q8_0_unpack(slot, kv_row(c), row);
+        return;
+    }
+    for (long i = 0; i < kv_row(c); i++)
+        row[i] = orc_bf16_to_f32((uint16_t)(slot[2 * i] | (slot[2 * i + 1] << 8)));
 }
 
 /* ---- one round over a set of rows (one or more sessions) ---- */
@@ -526,14 +583,14 @@ static void attn_rows(void* a, long t0, long t1)
         const orc_cfg* c = &s->m->c;
         int ctx = j->row_pos[t] + 1;               /* causal: positions 0..pos */
         long kvr = kv_row(c);
-        uint16_t* K = (uint16_t*)malloc(sizeof(uint16_t) * ctx * kvr);
-        uint16_t* V = (uint16_t*)malloc(sizeof(uint16_t) * ctx * kvr);
+        float* K = (float*)malloc(sizeof(float) * ctx * kvr);
+        float* V = (float*)malloc(sizeof(float) * ctx * kvr);
         for (int p = 0; p < ctx; p++) {            /* gather through the layout */
-            memcpy(K + p * kvr, kv_slot(s, j->layer, p, 0), sizeof(uint16_t) * kvr);
-            memcpy(V + p * kvr, kv_slot(s, j->layer, p, 1), sizeof(uint16_t) * kvr);
+            kv_load(c, kv_slot(s, j->layer, p, 0), K + p * kvr);
+            kv_load(c, kv_slot(s, j->layer, p, 1), V + p * kvr);
         }
         long qw = (long)c->n_q_heads * c->head_dim;
-        orc_gqa_attend(j->q + t * qw, K, V, ctx, c->n_q_heads, c->n_kv_heads,
+        gqa_attend_f32(j->q + t * qw, K, V, ctx, c->n_q_heads, c->n_kv_heads,
                        c->head_dim, j->att + t * qw);
         free(K);
         free(V);
@@ -599,13 +656,10 @@ static int eval_rows(orc_session* const* S, const int32_t* const* toks, const in
                 orc_rmsnorm(kh, W->k_norm, d, c->rms_eps, kh);
                 orc_rope(kh, d, row_pos[t], c->rope_theta);
             }
-            /* store K and V rounded to bf16 (the KV storage contract) */
-            uint16_t* ks = kv_slot(S[row_sess[t]], l, row_pos[t], 0);
-            uint16_t* vs = kv_slot(S[row_sess[t]], l, row_pos[t], 1);
-            for (int i = 0; i < KW; i++) {
-                ks[i] = orc_f32_to_bf16(k[(long)t * KW + i]);
-                vs[i] = orc_f32_to_bf16(v[(long)t * KW + i]);
-            }
+            /* store K and V: rounded to bf16 (the KV storage contract) or
+             * packed to Q8_0 (the opt-in quantized cache) */
+            kv_store(c, k + (long)t * KW, kv_slot(S[row_sess[t]], l, row_pos[t], 0));
+            kv_store(c, v + (long)t * KW, kv_slot(S[row_sess[t]], l, row_pos[t], 1));
         }
         attn_job aj = { S, row_sess, row_pos, q, att, l };
         parallel_for(T, m->n_threads, attn_rows, &aj);

@@ -21,6 +21,8 @@
  *  - "Kipp Roadmap", status v0.0.2: paged KV through a per-session
  *    32-position block table, bitwise equal to the contiguous layout;
  *    batched evaluation equal to isolated evaluation.
+ *  - "Kipp Roadmap", status v0.0.4: an opt-in Q8_0 KV cache, about 1.9x
+ *    smaller than BF16, gated for tolerance and placement invariance.
  *  - "Reproducing Kipp", section "Model-backed CPU and Metal gates": cached
  *    decode must equal recomputation; the CPU oracle is FP32.
  * The layer math itself is not printed on the pages; the oracle takes the
@@ -51,6 +53,7 @@ typedef struct orc_cfg {
     int tied;     /* 1: lm_head is the token embedding */
     int scheme;   /* ORC_BF16, ORC_Q8_0 or ORC_AFFINE4 (the seven projections only) */
     double rope_theta, rms_eps;
+    int kv_quant; /* ORC_BF16: K/V stored as bf16; ORC_Q8_0: as Q8_0 blocks */
 } orc_cfg;
 
 /* Per-layer weights, host memory, row-major [out][in].  BF16 tensors are
@@ -95,6 +98,10 @@ void  orc_matmul(const void* W, int scheme, int n_out, int n_in,
  * q: [n_q][d] f32; K, V: [ctx][n_kv][d] bf16; o: [n_q][d]. */
 void  orc_gqa_attend(const float* q, const uint16_t* K, const uint16_t* V,
                      int ctx, int n_q, int n_kv, int d, float* o);
+
+/* Bytes one position's K and V take in one layer's cache: 2 n_kv d (bf16)
+ * or 2 n_kv (d/32) 34 (Q8_0 blocks). */
+long  orc_kv_bytes_per_position(const orc_cfg* c);
 
 /* ---- model / KV / sessions ---- */
 orc_model* orc_model_create(const orc_cfg* cfg, const uint16_t* embed,

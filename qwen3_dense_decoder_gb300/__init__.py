@@ -215,6 +215,8 @@ class Model:
 
     def __init__(self, shape, weights: dict, max_ctx: int, max_round_tokens: int = 2048,
                  stream=None):
+        if getattr(shape, "kv_quant", BF16) != BF16:
+            raise ValueError("the CUDA path keeps K/V in bf16; a Q8_0 KV cache is not built on it")
         self.shape = shape
         self.stream = stream or torch.cuda.current_stream()
         self._keep = weights

@@ -35,6 +35,7 @@ class Shape:
     scheme: int = BF16
     rope_theta: float = 1e6
     rms_eps: float = 1e-6
+    kv_quant: int = BF16      # K/V cache: BF16, or Q8_0 blocks (the opt-in quantized cache)
 
     @property
     def q_width(self) -> int:

@@ -84,6 +84,15 @@ def test_config_checks_need_no_gpu(libq3):
     assert b"head_dim must be 128" in libq3.q3_last_error()
 
 
+def test_cuda_model_refuses_a_quantized_kv_cache():
+    # the Q8_0 KV cache exists in the oracle only: the binding says so before any CUDA call
+    import synthetic
+    import qwen3_dense_decoder_gb300 as q3
+    shape = synthetic.SHAPES["tiny"].replace(kv_quant=synthetic.Q8_0)
+    with pytest.raises(ValueError, match="Q8_0 KV cache"):
+        q3.Model(shape, {}, max_ctx=64)
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "qwen3_dense_decoder_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -27,6 +27,9 @@ TINY = Shape("oracle-tiny", 2, 64, 4, 2, 16, 96, 128, True, rope_theta=1e4)
 TINY_UNTIED = TINY.replace(name="oracle-tiny-untied", tied=False, n_layers=1)
 TINY_Q8 = TINY.replace(name="oracle-tiny-q8", scheme=Q8_0, tied=False)
 TINY_A4 = TINY.replace(name="oracle-tiny-affine4", scheme=AFFINE4, tied=False)
+# Q8_0 blocks run along a head row, so the head width is a multiple of 32
+TINY_KVQ8 = TINY.replace(name="oracle-tiny-kv-q8_0", head_dim=32, kv_quant=Q8_0)
+KV_SHAPES = [TINY, TINY_KVQ8]            # the placement gates hold for either K/V storage
 
 
 def _model(orc, shape, seed=7, threads=2):
@@ -38,9 +41,11 @@ def _bf16r(a):
     return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def brute_force_logits(shape, w, tokens, weights64=None):
-    """float64 statement of the forward with no cache: every row's logits."""
+def brute_force_logits(shape, w, tokens, weights64=None, kv_round=None):
+    """float64 statement of the forward with no cache: every row's logits.
+    kv_round maps K or V [T, n_kv, d] to its stored values (default: bf16)."""
     f = (lambda t: t.double().numpy()) if weights64 is None else weights64
+    kv_round = _bf16r if kv_round is None else kv_round
     eps, d = shape.rms_eps, shape.head_dim
     T = len(tokens)
     x = w["embed"].double().numpy()[np.asarray(tokens)]
@@ -66,8 +71,8 @@ def brute_force_logits(shape, w, tokens, weights64=None):
         k = (h @ W["wk"].T).reshape(T, shape.n_kv_heads, d)
         v = (h @ W["wv"].T).reshape(T, shape.n_kv_heads, d)
         q = rope(rms(q, g["q_norm"]))
-        k = _bf16r(rope(rms(k, g["k_norm"])))
-        v = _bf16r(v)
+        k = kv_round(rope(rms(k, g["k_norm"])))
+        v = kv_round(v)
         k = np.repeat(k, group, axis=1)
         v = np.repeat(v, group, axis=1)
         s = np.einsum("thd,shd->hts", q, k) / math.sqrt(d)
@@ -115,6 +120,47 @@ def test_brute_force_agrees_quantized(orc, shape):
         assert _nmse(got[t], ref[t]) < 1e-10
 
 
+def _q8_0_round(orc):
+    """K or V [T, n_kv, d] as the Q8_0 cache stores it: FP32 rows packed in
+    blocks of 32 by the oracle's (separately pinned) packer, then unpacked."""
+    def rnd(a):
+        a = np.asarray(a)
+        f = np.ascontiguousarray(a.reshape(a.shape[0], -1), np.float32)
+        return orc.q8_0_unpack(orc.q8_0_pack(f), f.shape[1]).astype(np.float64).reshape(a.shape)
+    return rnd
+
+
+def test_brute_force_agrees_q8_0_kv(orc):
+    m, w = _model(orc, TINY_KVQ8)
+    toks = make_tokens(11, TINY_KVQ8.vocab, seed=5)
+    got = m.session(max_ctx=64).eval(toks, all_rows=True)
+    ref = brute_force_logits(TINY_KVQ8, w, toks, kv_round=_q8_0_round(orc))
+    for t in range(len(toks)):
+        # a K/V value within FP32-vs-FP64 rounding of a quantization boundary may
+        # take the neighbouring code on one side: 1e-8 leaves room for a few
+        assert _nmse(got[t], ref[t]) < 1e-8, t
+        assert int(np.argmax(got[t])) == int(np.argmax(ref[t]))
+
+
+def test_q8_0_kv_cache_size_and_tolerance(orc):
+    """About 1.9x smaller than bf16, and near the bf16-cache forward without equalling it."""
+    kv = GOLD["q8_0_kv"]
+    for key in ("4b", "14b"):
+        s = __import__("synthetic").SHAPES[key]
+        b16 = orc.kv_bytes_per_position(s)
+        q8 = orc.kv_bytes_per_position(s.replace(kv_quant=Q8_0))
+        assert b16 == 2 * s.n_kv_heads * s.head_dim * 2
+        assert q8 == 2 * s.n_kv_heads * (s.head_dim // 32) * 34
+        assert round(b16 / q8, 1) == kv["ratio_vs_bf16"]
+    q, w = _model(orc, TINY_KVQ8)
+    bf = orc.Model(TINY_KVQ8.replace(kv_quant=BF16), w, n_threads=2)
+    toks = make_tokens(40, TINY.vocab, seed=12)
+    got = q.session(max_ctx=64).eval(toks, all_rows=True)
+    ref = bf.session(max_ctx=64).eval(toks, all_rows=True)
+    e = _nmse(got, ref)
+    assert 0 < e < kv["nmse_vs_bf16_cache"], e
+
+
 def test_affine4_forward_stays_near_bf16(orc):
     """4-bit codes are lossy: the AFFINE4 forward is near the BF16 one, not equal."""
     a4, w = _model(orc, TINY_A4)
@@ -126,10 +172,13 @@ def test_affine4_forward_stays_near_bf16(orc):
     assert 1e-6 < e < 1e-1, e
 
 
-def test_cached_decode_equals_recompute(orc):
+@pytest.mark.parametrize("shape", KV_SHAPES, ids=lambda s: s.name)
+def test_cached_decode_equals_recompute(orc, shape):
+    """Each position's K/V (bf16 or Q8_0) depends on that position only, so the
+    cache a decode reads equals the one a full recompute builds."""
     tol = GOLD["nmse_cached_vs_recompute"]["value"]
-    m, _ = _model(orc, TINY)
-    toks = make_tokens(40, TINY.vocab, seed=8)
+    m, _ = _model(orc, shape)
+    toks = make_tokens(40, shape.vocab, seed=8)
     full = m.session(max_ctx=64).eval(toks, all_rows=True)      # one round, no reuse
     s = m.session(max_ctx=64)
     s.eval(toks[:8])
@@ -140,9 +189,10 @@ def test_cached_decode_equals_recompute(orc):
     assert s.pos == 40
 
 
-def test_paged_equals_contiguous_under_permuted_tables(orc):
-    m, _ = _model(orc, TINY)
-    toks = make_tokens(100, TINY.vocab, seed=9)
+@pytest.mark.parametrize("shape", KV_SHAPES, ids=lambda s: s.name)
+def test_paged_equals_contiguous_under_permuted_tables(orc, shape):
+    m, _ = _model(orc, shape)
+    toks = make_tokens(100, shape.vocab, seed=9)
     ref = m.session(max_ctx=128).eval(toks, all_rows=True)
     for seed in (1, 2):
         pool = m.pool(16)
@@ -153,10 +203,11 @@ def test_paged_equals_contiguous_under_permuted_tables(orc):
         np.testing.assert_array_equal(got, ref)
 
 
-def test_batched_equals_isolated(orc):
-    m, _ = _model(orc, TINY)
+@pytest.mark.parametrize("shape", KV_SHAPES, ids=lambda s: s.name)
+def test_batched_equals_isolated(orc, shape):
+    m, _ = _model(orc, shape)
     pool = m.pool(32)
-    prompts = [make_tokens(n, TINY.vocab, seed=20 + n) for n in (5, 33, 12)]
+    prompts = [make_tokens(n, shape.vocab, seed=20 + n) for n in (5, 33, 12)]
     iso = []
     for p in prompts:
         s = m.session(max_ctx=128)
@@ -169,23 +220,25 @@ def test_batched_equals_isolated(orc):
         np.testing.assert_array_equal(b[i], iso[i][1])
 
 
-def test_chunking_and_causality(orc):
-    m, _ = _model(orc, TINY)
-    toks = make_tokens(50, TINY.vocab, seed=10)
+@pytest.mark.parametrize("shape", KV_SHAPES, ids=lambda s: s.name)
+def test_chunking_and_causality(orc, shape):
+    m, _ = _model(orc, shape)
+    toks = make_tokens(50, shape.vocab, seed=10)
     one = m.session(max_ctx=64).eval(toks, all_rows=True)
     s = m.session(max_ctx=64)
     parts = [s.eval(toks[a:b], all_rows=True) for a, b in ((0, 5), (5, 45), (45, 50))]
     np.testing.assert_array_equal(np.concatenate(parts), one)
     toks2 = toks.copy()
-    toks2[30:] = (toks2[30:] + 1) % TINY.vocab                  # change only later tokens
+    toks2[30:] = (toks2[30:] + 1) % shape.vocab                  # change only later tokens
     two = m.session(max_ctx=64).eval(toks2, all_rows=True)
     np.testing.assert_array_equal(two[:30], one[:30])
     assert not np.array_equal(two[30], one[30])
 
 
-def test_truncate_and_resume(orc):
-    m, _ = _model(orc, TINY)
-    toks = make_tokens(30, TINY.vocab, seed=11)
+@pytest.mark.parametrize("shape", KV_SHAPES, ids=lambda s: s.name)
+def test_truncate_and_resume(orc, shape):
+    m, _ = _model(orc, shape)
+    toks = make_tokens(30, shape.vocab, seed=11)
     s = m.session(max_ctx=64)
     ref = s.eval(toks, all_rows=True)
     s.truncate(12)
@@ -198,6 +251,9 @@ def test_capacity_errors(orc):
     s = m.session(max_ctx=16)
     with pytest.raises(RuntimeError):
         s.eval(make_tokens(17, TINY.vocab, seed=1))
+    # a Q8_0 cache needs whole 32-value blocks per head row
+    with pytest.raises(ValueError):
+        orc.Model(TINY.replace(kv_quant=Q8_0), make_weights(TINY, seed=7), n_threads=1)
     with pytest.raises(RuntimeError):
         s.eval(np.array([TINY.vocab], np.int32))
     pool = m.pool(1)
