@@ -84,6 +84,10 @@ def lib():
         L.orc_eval.argtypes = [vp, vp, i, vp, vp]
         L.orc_eval_batch.argtypes = [vp, vp, vp, i, vp]
         L.orc_argmax.argtypes = [vp, i]
+        L.orc_pool_enable_prefix.argtypes = [vp, i]
+        L.orc_session_publish.argtypes = [vp]
+        L.orc_pool_free_blocks.argtypes = [vp]
+        L.orc_session_attach_prefix.argtypes = [vp, vp, i]
         L.orc_kv_bytes_per_position.argtypes = [C.POINTER(_Cfg)]
         L.orc_kv_bytes_per_position.restype = C.c_long
         _lib = L
@@ -307,6 +311,15 @@ class Pool:
             lib().orc_pool_free(self.h)
             self.h = None
 
+    @property
+    def free_blocks(self) -> int:
+        return lib().orc_pool_free_blocks(self.h)
+
+    def enable_prefix(self, hash_bits: int = 16) -> None:
+        """Content-addressed prefix sharing over this pool (2^hash_bits buckets)."""
+        if lib().orc_pool_enable_prefix(self.h, hash_bits):
+            raise ValueError("oracle: enable_prefix")
+
 
 class Session:
     def __init__(self, model: Model, pool: Pool | None, max_ctx: int):
@@ -324,6 +337,22 @@ class Session:
         ids = np.ascontiguousarray(ids, np.int32)
         if lib().orc_session_set_block_table(self.h, _ptr(ids), ids.size):
             raise ValueError("oracle: bad block table")
+
+    def publish(self) -> int:
+        """Make the session's full blocks shareable; returns how many were newly published."""
+        n = lib().orc_session_publish(self.h)
+        if n < 0:
+            raise ValueError("oracle: publish")
+        return n
+
+    def attach_prefix(self, tokens) -> int:
+        """At position 0: attach the longest published chain matching the prompt's
+        leading full blocks (at least one token left); returns the positions attached."""
+        t = np.ascontiguousarray(tokens, np.int32)
+        n = lib().orc_session_attach_prefix(self.h, _ptr(t), t.size)
+        if n < 0:
+            raise ValueError("oracle: attach_prefix")
+        return n
 
     @property
     def pos(self) -> int:

@@ -388,7 +388,18 @@ struct orc_pool {
     orc_model* m;
     int n_blocks;
     uint8_t *k, *v;         /* [L][n_blocks][32] K (V) rows of kv_row_bytes */
-    unsigned char* used;
+    int* ref;               /* holders of each block: sessions, +1 while published */
+    /* content-addressed prefix index (orc_pool_enable_prefix) */
+    int prefix_on;
+    unsigned hash_mask;     /* buckets - 1 */
+    int* bucket;            /* [buckets] first published block of the bucket, or -1 */
+    int* next;              /* [n_blocks] next published block in the same bucket */
+    int* parent;            /* [n_blocks] the published block before it (-1: first) */
+    int* children;          /* [n_blocks] published blocks whose parent it is */
+    long* stamp;            /* [n_blocks] last publish or attach, for eviction */
+    int32_t* btok;          /* [n_blocks][32] the tokens of a published block */
+    unsigned char* published;
+    long clock;
 };
 
 struct orc_session {
@@ -398,6 +409,7 @@ struct orc_session {
     uint8_t *k, *v;         /* contiguous: [L][max_ctx] K (V) rows of kv_row_bytes */
     int32_t* table;         /* paged: block id per 32 positions */
     int n_table, n_given;   /* blocks taken; entries given by the caller */
+    int32_t* toks;          /* [max_ctx] the token at each position */
 };
 
 orc_model* orc_model_create(const orc_cfg* cfg, const uint16_t* embed,
@@ -448,15 +460,135 @@ orc_pool* orc_pool_create(orc_model* m, int n_blocks)
     p->n_blocks = n_blocks;
     p->k = (uint8_t*)calloc(n, 1);
     p->v = (uint8_t*)calloc(n, 1);
-    p->used = (unsigned char*)calloc(n_blocks, 1);
-    if (!p->k || !p->v || !p->used) { orc_pool_free(p); return NULL; }
+    p->ref = (int*)calloc(n_blocks, sizeof(int));
+    if (!p->k || !p->v || !p->ref) { orc_pool_free(p); return NULL; }
     return p;
 }
 
 void orc_pool_free(orc_pool* p)
 {
     if (!p) return;
-    free(p->k); free(p->v); free(p->used); free(p);
+    free(p->k); free(p->v); free(p->ref);
+    free(p->bucket); free(p->next); free(p->parent); free(p->children); free(p->stamp);
+    free(p->btok); free(p->published);
+    free(p);
+}
+
+/* ---- content-addressed prefix sharing ("Kipp Roadmap", status v0.0.3) ---- */
+
+/* Readings (the pages name the parts, not the rules):
+ *  - a published block is addressed by its content: the block before it in
+ *    the chain (its parent, -1 for a prompt's first block) and its 32
+ *    tokens; a lookup hashes that key (64-bit FNV-1a over the parent id and
+ *    the tokens, little-endian) to a bucket and accepts a candidate only if
+ *    its parent is equal and its tokens compare equal (memcmp), so a hash
+ *    collision never shares a block;
+ *  - only full blocks are published, when a session says it is finished
+ *    with them (orc_session_publish); an equal block published earlier is
+ *    shared in place of the session's own copy;
+ *  - the index holds one reference to each published block, so it outlives
+ *    its session; when the pool has no free block, the published block held
+ *    by the index alone, with no published successor, that was published or
+ *    attached longest ago is evicted;
+ *  - a session writes only blocks that it alone holds: attaching stops on a
+ *    block boundary, and a truncation into a shared block copies it first. */
+int orc_pool_enable_prefix(orc_pool* p, int hash_bits)
+{
+    if (!p || hash_bits < 0 || hash_bits > 24 || p->prefix_on) return -1;
+    int nb = 1 << hash_bits, n = p->n_blocks;
+    p->bucket = (int*)malloc(sizeof(int) * nb);
+    p->next = (int*)malloc(sizeof(int) * n);
+    p->parent = (int*)malloc(sizeof(int) * n);
+    p->children = (int*)calloc(n, sizeof(int));
+    p->stamp = (long*)calloc(n, sizeof(long));
+    p->btok = (int32_t*)calloc((size_t)n * ORC_BLOCK, sizeof(int32_t));
+    p->published = (unsigned char*)calloc(n, 1);
+    if (!p->bucket || !p->next || !p->parent || !p->children || !p->stamp || !p->btok ||
+        !p->published)
+        return -1;
+    for (int i = 0; i < nb; i++) p->bucket[i] = -1;
+    for (int i = 0; i < n; i++) p->next[i] = p->parent[i] = -1;
+    p->hash_mask = (unsigned)nb - 1;
+    p->prefix_on = 1;
+    return 0;
+}
+
+int orc_pool_free_blocks(const orc_pool* p)
+{
+    int n = 0;
+    for (int b = 0; b < p->n_blocks; b++) n += p->ref[b] == 0;
+    return n;
+}
+
+static uint64_t block_hash(int parent, const int32_t* t)
+{
+    uint64_t h = 14695981039346656037ull;              /* FNV-1a offset basis */
+    uint32_t words[1 + ORC_BLOCK];
+    words[0] = (uint32_t)parent;
+    for (int i = 0; i < ORC_BLOCK; i++) words[1 + i] = (uint32_t)t[i];
+    for (int w = 0; w < 1 + ORC_BLOCK; w++)
+        for (int b = 0; b < 4; b++) {
+            h ^= (words[w] >> (8 * b)) & 0xffu;
+            h *= 1099511628211ull;                     /* FNV-1a 64-bit prime */
+        }
+    return h;
+}
+
+static int find_published(orc_pool* p, int parent, const int32_t* t)
+{
+    for (int b = p->bucket[block_hash(parent, t) & p->hash_mask]; b >= 0; b = p->next[b])
+        if (p->parent[b] == parent && memcmp(p->btok + (long)b * ORC_BLOCK, t,
+                                             sizeof(int32_t) * ORC_BLOCK) == 0)
+            return b;
+    return -1;
+}
+
+static void index_insert(orc_pool* p, int b, int parent, const int32_t* t)
+{
+    unsigned h = (unsigned)(block_hash(parent, t) & p->hash_mask);
+    memcpy(p->btok + (long)b * ORC_BLOCK, t, sizeof(int32_t) * ORC_BLOCK);
+    p->parent[b] = parent;
+    p->next[b] = p->bucket[h];
+    p->bucket[h] = b;
+    p->published[b] = 1;
+    p->stamp[b] = ++p->clock;
+    p->ref[b]++;
+    if (parent >= 0) p->children[parent]++;
+}
+
+static void index_remove(orc_pool* p, int b)
+{
+    unsigned h = (unsigned)(block_hash(p->parent[b], p->btok + (long)b * ORC_BLOCK) & p->hash_mask);
+    int* link = &p->bucket[h];
+    while (*link != b) link = &p->next[*link];
+    *link = p->next[b];
+    if (p->parent[b] >= 0) p->children[p->parent[b]]--;
+    p->next[b] = p->parent[b] = -1;
+    p->published[b] = 0;
+    p->ref[b]--;
+}
+
+/* a block someone else may read: published, or held by more than one */
+static int shared_block(const orc_pool* p, int b)
+{
+    return p->ref[b] > 1 || (p->prefix_on && p->published[b]);
+}
+
+/* the lowest free block, evicting a published block when none is free */
+static int take_block(orc_pool* p)
+{
+    for (int b = 0; b < p->n_blocks; b++)
+        if (p->ref[b] == 0) { p->ref[b] = 1; return b; }
+    if (!p->prefix_on) return -1;
+    int best = -1;
+    for (int b = 0; b < p->n_blocks; b++)
+        if (p->published[b] && p->ref[b] == 1 && p->children[b] == 0 &&
+            (best < 0 || p->stamp[b] < p->stamp[best]))
+            best = b;
+    if (best < 0) return -1;
+    index_remove(p, best);
+    p->ref[best] = 1;
+    return best;
 }
 
 orc_session* orc_session_create(orc_model* m, orc_pool* pool, int max_ctx)
@@ -473,26 +605,38 @@ orc_session* orc_session_create(orc_model* m, orc_pool* pool, int max_ctx)
     } else {
         s->table = (int32_t*)calloc((max_ctx + ORC_BLOCK - 1) / ORC_BLOCK, sizeof(int32_t));
     }
+    s->toks = (int32_t*)calloc(max_ctx > 0 ? max_ctx : 1, sizeof(int32_t));
+    if (!s->toks || (pool && !s->table)) { orc_session_free(s); return NULL; }
     return s;
+}
+
+static void release_blocks(orc_session* s, int from)
+{
+    for (int b = from; b < s->n_table; b++) s->pool->ref[s->table[b]]--;
+    s->n_table = from;
+    if (s->n_given > from) s->n_given = from;
 }
 
 void orc_session_free(orc_session* s)
 {
     if (!s) return;
-    if (s->pool)
-        for (int b = 0; b < s->n_table; b++) s->pool->used[s->table[b]] = 0;
-    free(s->k); free(s->v); free(s->table); free(s);
+    if (s->pool && s->table) release_blocks(s, 0);
+    free(s->k); free(s->v); free(s->table); free(s->toks); free(s);
 }
 
 /* The caller fixes which pool blocks back the session's positions, in
  * order: block i holds positions [32 i, 32 i + 32). */
 int orc_session_set_block_table(orc_session* s, const int32_t* ids, int n)
 {
-    if (!s->pool || s->pos != 0 || n > (s->max_ctx + ORC_BLOCK - 1) / ORC_BLOCK) return -1;
-    for (int b = 0; b < s->n_table; b++) s->pool->used[s->table[b]] = 0;
+    if (!s->pool || s->pos != 0 || n < 0 || n > (s->max_ctx + ORC_BLOCK - 1) / ORC_BLOCK) return -1;
+    release_blocks(s, 0);
     for (int i = 0; i < n; i++) {
-        if (ids[i] < 0 || ids[i] >= s->pool->n_blocks || s->pool->used[ids[i]]) return -1;
-        s->pool->used[ids[i]] = 1;
+        int dup = 0;
+        for (int j = 0; j < i; j++) dup |= ids[j] == ids[i];
+        if (ids[i] < 0 || ids[i] >= s->pool->n_blocks || s->pool->ref[ids[i]] || dup) return -1;
+    }
+    for (int i = 0; i < n; i++) {
+        s->pool->ref[ids[i]] = 1;
         s->table[i] = ids[i];
     }
     s->n_table = n;
@@ -502,9 +646,32 @@ int orc_session_set_block_table(orc_session* s, const int32_t* ids, int n)
 
 int orc_session_pos(const orc_session* s) { return s->pos; }
 
+/* Forget positions >= n_pos.  Paged: blocks wholly past the new end go back
+ * to the pool (those the caller fixed stay); a shared block that still holds
+ * kept positions and would be written next is first copied to a block of the
+ * session's own. */
 int orc_session_truncate(orc_session* s, int n_pos)
 {
     if (n_pos < 0 || n_pos > s->pos) return -1;
+    if (s->pool) {
+        orc_pool* p = s->pool;
+        int keep = (n_pos + ORC_BLOCK - 1) / ORC_BLOCK;
+        if (keep < s->n_given) keep = s->n_given < s->n_table ? s->n_given : s->n_table;
+        if (keep < s->n_table) release_blocks(s, keep);
+        int last = n_pos / ORC_BLOCK;                  /* the block position n_pos falls in */
+        if (n_pos % ORC_BLOCK && last < s->n_table && shared_block(p, s->table[last])) {
+            int b = s->table[last], nb = take_block(p);
+            if (nb < 0) return -1;
+            const orc_cfg* c = &s->m->c;
+            long blk = ORC_BLOCK * kv_row_bytes(c);
+            for (int l = 0; l < c->n_layers; l++) {
+                memcpy(p->k + ((long)l * p->n_blocks + nb) * blk, p->k + ((long)l * p->n_blocks + b) * blk, blk);
+                memcpy(p->v + ((long)l * p->n_blocks + nb) * blk, p->v + ((long)l * p->n_blocks + b) * blk, blk);
+            }
+            p->ref[b]--;
+            s->table[last] = nb;
+        }
+    }
     s->pos = n_pos;
     return 0;
 }
@@ -516,13 +683,63 @@ static int reserve(orc_session* s, int end)
     if (!s->pool) return 0;
     int need = (end + ORC_BLOCK - 1) / ORC_BLOCK;
     while (s->n_table < need) {
-        int b = 0;
-        while (b < s->pool->n_blocks && s->pool->used[b]) b++;
-        if (b == s->pool->n_blocks) return -1;
-        s->pool->used[b] = 1;
+        int b = take_block(s->pool);
+        if (b < 0) return -1;
         s->table[s->n_table++] = b;
     }
     return 0;
+}
+
+/* Publish the session's full blocks: each becomes content-addressed, or is
+ * swapped for an equal block published earlier (same chain, same tokens,
+ * so the same K/V bits).  Returns the number of blocks newly published. */
+int orc_session_publish(orc_session* s)
+{
+    orc_pool* p = s->pool;
+    if (!p || !p->prefix_on || s->n_given) return -1;
+    int parent = -1, count = 0;
+    for (int i = 0; i < s->pos / ORC_BLOCK; i++) {
+        int b = s->table[i];
+        const int32_t* t = s->toks + (long)i * ORC_BLOCK;
+        if (!p->published[b]) {
+            int e = find_published(p, parent, t);
+            if (e >= 0) {
+                p->ref[e]++;
+                p->ref[b]--;
+                s->table[i] = e;
+                b = e;
+            } else {
+                index_insert(p, b, parent, t);
+                count++;
+            }
+        }
+        parent = b;
+    }
+    return count;
+}
+
+/* Before a session's first round: attach the longest chain of published
+ * blocks that matches the prompt's leading full blocks, keeping at least one
+ * token of the prompt to evaluate.  Returns the positions attached (a
+ * multiple of 32, and the session's new position). */
+int orc_session_attach_prefix(orc_session* s, const int32_t* tokens, int n)
+{
+    orc_pool* p = s->pool;
+    if (!p || !p->prefix_on || s->pos != 0 || s->n_given || n < 1 || n > s->max_ctx) return -1;
+    release_blocks(s, 0);
+    int parent = -1, i = 0;
+    for (; i < (n - 1) / ORC_BLOCK; i++) {
+        int e = find_published(p, parent, tokens + (long)i * ORC_BLOCK);
+        if (e < 0) break;
+        p->ref[e]++;
+        p->stamp[e] = ++p->clock;
+        s->table[i] = e;
+        parent = e;
+    }
+    s->n_table = i;
+    s->pos = i * ORC_BLOCK;
+    memcpy(s->toks, tokens, sizeof(int32_t) * (size_t)s->pos);
+    return s->pos;
 }
 
 /* address of the K (or V) row of position p in layer l */
@@ -610,6 +827,9 @@ static int eval_rows(orc_session* const* S, const int32_t* const* toks, const in
         for (int i = 0; i < n[b]; i++)
             if (toks[b][i] < 0 || toks[b][i] >= c->vocab) return -1;
         if (reserve(S[b], S[b]->pos + n[b])) return -1;
+        if (S[b]->pool)
+            for (int i = S[b]->pos / ORC_BLOCK; i <= (S[b]->pos + n[b] - 1) / ORC_BLOCK; i++)
+                if (shared_block(S[b]->pool, S[b]->table[i])) return -1;
         T += n[b];
     }
     int* row_sess = (int*)malloc(sizeof(int) * T);
@@ -692,7 +912,10 @@ static int eval_rows(orc_session* const* S, const int32_t* const* toks, const in
                    sizeof(float) * c->vocab);
         free(out);
     }
-    for (int b = 0; b < ns; b++) S[b]->pos += n[b];
+    for (int b = 0; b < ns; b++) {
+        memcpy(S[b]->toks + S[b]->pos, toks[b], sizeof(int32_t) * (size_t)n[b]);
+        S[b]->pos += n[b];
+    }
 
     free(x); free(h); free(y); free(q); free(k); free(v); free(att); free(g); free(u);
     free(row_sess); free(row_pos); free(row_tok);

@@ -122,6 +122,20 @@ int  orc_session_set_block_table(orc_session* s, const int32_t* ids, int n);
 int  orc_session_pos(const orc_session* s);
 int  orc_session_truncate(orc_session* s, int n_pos);
 
+/* Content-addressed prefix sharing over a pool ("Kipp Roadmap", status
+ * v0.0.3: a content-addressed 32-token block pool, publish-at-finish,
+ * memcmp-verified).  enable: an index of 2^hash_bits buckets (0..24; few
+ * buckets force hash collisions, which the token comparison resolves).
+ * publish: the session's full blocks become shareable; returns how many
+ * were newly published.  attach_prefix: at position 0, take the longest
+ * published chain matching the prompt's leading full blocks, leaving at
+ * least one token to evaluate; returns the positions attached. */
+int  orc_pool_enable_prefix(orc_pool* p, int hash_bits);
+/* blocks no session holds and the index does not keep */
+int  orc_pool_free_blocks(const orc_pool* p);
+int  orc_session_publish(orc_session* s);
+int  orc_session_attach_prefix(orc_session* s, const int32_t* tokens, int n);
+
 /* One round of n tokens appended at the session's position.  logits_last:
  * [vocab] logits of the round's last token (may be NULL).  logits_all:
  * [n][vocab] logits of every row (may be NULL).  Returns 0 or -1. */
