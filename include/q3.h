@@ -245,10 +245,37 @@ int q3_affine4_to_f16(const void* groups_dev, int64_t n, void* out_dev, void* st
  * rows allocated (rows past N are read but their products discarded);
  * y_dev: f32 [N][M].  M a multiple of 128, K a multiple of 64, 1 <= N.
  * block_n: token-tile width (32, 64, 96, 128, 192 or 256), or 0 for the
- * width the prefill planner would pick.  Pointers 16-byte aligned.
- * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+ * width the prefill planner would pick; no split-K.  Pointers 16-byte
+ * aligned.  Synchronous: returns once the kernel has finished on stream (it
+ * allocates and frees a status word).  Errors: Q3_ERR_INVALID_ARG,
+ * Q3_ERR_OOM, Q3_ERR_CUDA, Q3_ERR_DEVICE_CHECK (a bounded device wait ran
+ * out; the message gives the status bits). */
 int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, float* y_dev,
                  int block_n, void* stream);
+
+/* q3_op_gemm: one projection GEMM of a prefill round with the round's
+ * epilogue and split-K ("Kipp Roadmap", status v0.0.6: layer projections of
+ * prefill on the tensor units), on caller buffers.  With d[n][m] =
+ * sum_k w[m][k] * x[n][k]:
+ *   Q3_OP_STORE:  out f32 [N][M] = d                   (QKV, lm_head rows)
+ *   Q3_OP_ADD:    out f32 [N][M] += d                  (O and down: the residual)
+ *   Q3_OP_SWIGLU: out fp16 [N][M] = fp16(silu(g) * u), g = the product with
+ *                 w (gate), u = the product with w2 (up), silu(z) = z / (1 + e^-z)
+ * w_dev, w2_dev: fp16 [M][K] (w2_dev only for Q3_OP_SWIGLU); x_dev: fp16
+ * [N][K] with at least round_up(N, 256) rows allocated.  M a multiple of 128
+ * (of 64 for Q3_OP_SWIGLU), K of 64, 1 <= N.  block_n as q3_op_matmul (0:
+ * the planner's width); k_splits: 1..8 K splits (at most K/64; > 1 sums FP32
+ * partials in split order in a second kernel, as a round does), or 0 for the
+ * planner's choice.  Pointers 16-byte aligned.  Synchronous: allocates a
+ * status word and the split workspace for the call and returns once the
+ * kernels have finished.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_OOM,
+ * Q3_ERR_CUDA, Q3_ERR_DEVICE_CHECK (a bounded wait ran out, or an fp16
+ * SwiGLU output beyond the fp16 range). */
+#define Q3_OP_STORE 0
+#define Q3_OP_ADD 1
+#define Q3_OP_SWIGLU 2
+int q3_op_gemm(const void* w_dev, const void* w2_dev, const void* x_dev, int M, int N, int K, int epi,
+               void* out_dev, int block_n, int k_splits, void* stream);
 
 /* q3_op_matvec: y[m] = sum_k w[m][k] * x[k] on the decode GEMV.  With
  * scales_dev == NULL, w_dev is bf16 [M][K]; otherwise w_dev is the int8
@@ -293,11 +320,20 @@ int q3_op_prefill_attention(const void* q_dev, const void* kv_dev, const int32_t
  * 2 <= k_splits <= min(8, K/64), and k_splits * N * M must not exceed
  * Q3_NOALLOC_SCRATCH_FLOATS (else Q3_ERR_INVALID_ARG, nothing launched).
  * The first call on a device looks up the scratch's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the scratch: calls whose
- * kernels may overlap on the GPU race on it, so order them on one stream.
- * Asynchronous on stream; allocates no device or host memory.  Errors (the
- * message from q3_noalloc_last_error): Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+ * (cudaGetSymbolAddress) with that device current; that lookup loads the
+ * library's device code for this entry point, which is when the driver
+ * commits the scratch's memory on the device, so make the first call (a
+ * warm-up) outside any latency-critical region and before any stream
+ * capture.  All calls share the scratch: calls whose kernels may overlap on
+ * the GPU race on it, so order them on one stream.  The caller must pass
+ * buffers of the stated sizes: the library cannot check an allocation's
+ * extent, and a short x_dev or y_dev is read or written past its end.
+ * Synchronous: the call reads its device status word back into a host
+ * variable and waits for the stream, so it returns once the kernels have
+ * finished.  Allocates no device or host memory.  Errors (the message from
+ * q3_noalloc_last_error): Q3_ERR_INVALID_ARG, Q3_ERR_CUDA,
+ * Q3_ERR_DEVICE_CHECK (a bounded device wait ran out; the output is then
+ * not valid). */
 #define Q3_NOALLOC_SCRATCH_FLOATS (2 * 1024 * 1024)
 int q3_op_matmul_splitk_noalloc(const void* w_dev, const void* x_dev, int M, int N, int K,
                                 int k_splits, float* y_dev, void* stream);

@@ -83,6 +83,7 @@ def lib():
         L.orc_session_truncate.argtypes = [vp, i]
         L.orc_eval.argtypes = [vp, vp, i, vp, vp]
         L.orc_eval_batch.argtypes = [vp, vp, vp, i, vp]
+        L.orc_eval_rows.argtypes = [vp, vp, i, vp, i, vp]
         L.orc_argmax.argtypes = [vp, i]
         L.orc_pool_enable_prefix.argtypes = [vp, i]
         L.orc_session_publish.argtypes = [vp]
@@ -373,6 +374,23 @@ class Session:
         if rc:
             raise RuntimeError("oracle: eval failed (capacity or token range)")
         return allr if all_rows else last
+
+    def eval_rows(self, tokens, rows) -> np.ndarray:
+        """Logits [len(rows), vocab] of the listed rows of the round (indices
+        into tokens, increasing); an empty list appends the positions and
+        computes no logits."""
+        t = np.ascontiguousarray(tokens, np.int32)
+        r = np.ascontiguousarray(rows, np.int32)
+        out = np.empty((r.size, self.model.shape.vocab), np.float32)
+        rc = lib().orc_eval_rows(self.h, _ptr(t), t.size, _ptr(r) if r.size else None, r.size,
+                                 _ptr(out) if r.size else None)
+        if rc:
+            raise RuntimeError("oracle: eval_rows failed (capacity, token range or row list)")
+        return out
+
+    def append(self, tokens) -> None:
+        """Append a round's positions (K/V stored) without computing logits."""
+        self.eval_rows(tokens, [])
 
 
 def nmse(got: np.ndarray, ref: np.ndarray) -> float:

@@ -814,8 +814,13 @@ static void attn_rows(void* a, long t0, long t1)
     }
 }
 
+/* One round over the sessions' rows (row t of the round: session row_sess[t],
+ * rows of a session consecutive and in order).  sel: the rows whose logits
+ * are wanted, increasing, n_sel of them; out: [n_sel][vocab].  With no row
+ * wanted (n_sel == 0) nothing reads the last layer past its K/V store, so
+ * the round stops there: the positions are appended with the same K/V. */
 static int eval_rows(orc_session* const* S, const int32_t* const* toks, const int* n,
-                     int ns, float* logits_last, float* logits_all)
+                     int ns, const int* sel, int n_sel, float* out)
 {
     orc_model* m = S[0]->m;
     const orc_cfg* c = &m->c;
@@ -881,6 +886,7 @@ static int eval_rows(orc_session* const* S, const int32_t* const* toks, const in
             kv_store(c, k + (long)t * KW, kv_slot(S[row_sess[t]], l, row_pos[t], 0));
             kv_store(c, v + (long)t * KW, kv_slot(S[row_sess[t]], l, row_pos[t], 1));
         }
+        if (n_sel == 0 && l == c->n_layers - 1) break;   /* no logits: nothing reads on */
         attn_job aj = { S, row_sess, row_pos, q, att, l };
         parallel_for(T, m->n_threads, attn_rows, &aj);
         orc_matmul(W->wo, c->scheme, H, QW, att, T, y, m->n_threads);
@@ -898,19 +904,10 @@ static int eval_rows(orc_session* const* S, const int32_t* const* toks, const in
     }
 
     /* final norm and lm_head on the requested rows */
-    for (int b = 0, t0 = 0; b < ns; t0 += n[b], b++) {
-        int r0 = logits_all ? t0 : t0 + n[b] - 1;
-        int nr = t0 + n[b] - r0;
-        for (int t = r0; t < r0 + nr; t++)
-            orc_rmsnorm(x + (long)t * H, m->final_norm, H, c->rms_eps, h + (long)(t - r0) * H);
-        float* out = (float*)malloc(sizeof(float) * (long)nr * c->vocab);
-        orc_matmul(m->lm_head, ORC_BF16, c->vocab, H, h, nr, out, m->n_threads);
-        if (logits_all)
-            memcpy(logits_all + (long)t0 * c->vocab, out, sizeof(float) * (long)nr * c->vocab);
-        if (logits_last)
-            memcpy(logits_last + (long)b * c->vocab, out + (long)(nr - 1) * c->vocab,
-                   sizeof(float) * c->vocab);
-        free(out);
+    if (n_sel > 0) {
+        for (int i = 0; i < n_sel; i++)
+            orc_rmsnorm(x + (long)sel[i] * H, m->final_norm, H, c->rms_eps, h + (long)i * H);
+        orc_matmul(m->lm_head, ORC_BF16, c->vocab, H, h, n_sel, out, m->n_threads);
     }
     for (int b = 0; b < ns; b++) {
         memcpy(S[b]->toks + S[b]->pos, toks[b], sizeof(int32_t) * (size_t)n[b]);
@@ -925,14 +922,46 @@ static int eval_rows(orc_session* const* S, const int32_t* const* toks, const in
 int orc_eval(orc_session* s, const int32_t* tokens, int n, float* logits_last,
              float* logits_all)
 {
-    return eval_rows(&s, &tokens, &n, 1, logits_last, logits_all);
+    if (n < 1) return -1;
+    int* sel = (int*)malloc(sizeof(int) * (size_t)n);
+    int n_sel = 0;
+    if (logits_all)
+        for (int t = 0; t < n; t++) sel[n_sel++] = t;
+    else if (logits_last)
+        sel[n_sel++] = n - 1;
+    float* out = logits_all ? logits_all : logits_last;
+    int rc = eval_rows(&s, &tokens, &n, 1, sel, n_sel, out);
+    if (rc == 0 && logits_all && logits_last)
+        memcpy(logits_last, logits_all + (long)(n - 1) * s->m->c.vocab,
+               sizeof(float) * s->m->c.vocab);
+    free(sel);
+    return rc;
+}
+
+int orc_eval_rows(orc_session* s, const int32_t* tokens, int n, const int* rows,
+                  int n_rows, float* logits)
+{
+    if (n < 1 || n_rows < 0 || (n_rows > 0 && !logits)) return -1;
+    for (int i = 0; i < n_rows; i++)
+        if (rows[i] < 0 || rows[i] >= n || (i > 0 && rows[i] <= rows[i - 1])) return -1;
+    return eval_rows(&s, &tokens, &n, 1, rows, n_rows, logits);
 }
 
 int orc_eval_batch(orc_session* const* s, const int32_t* const* tokens,
                    const int* n, int ns, float* logits)
 {
-    for (int a = 0; a < ns; a++)
+    if (ns < 1) return -1;
+    for (int a = 0; a < ns; a++) {
+        if (n[a] < 1) return -1;
         for (int b = 0; b < a; b++)
             if (s[a] == s[b]) return -1;
-    return eval_rows(s, tokens, n, ns, logits, NULL);
+    }
+    int* sel = (int*)malloc(sizeof(int) * (size_t)ns);
+    for (int b = 0, t = 0; b < ns; b++) {
+        t += n[b];
+        sel[b] = t - 1;                 /* the last row of each session's round */
+    }
+    int rc = eval_rows(s, tokens, n, ns, logits ? sel : NULL, logits ? ns : 0, logits);
+    free(sel);
+    return rc;
 }

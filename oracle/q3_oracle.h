@@ -142,6 +142,13 @@ int  orc_session_attach_prefix(orc_session* s, const int32_t* tokens, int n);
 int orc_eval(orc_session* s, const int32_t* tokens, int n,
              float* logits_last, float* logits_all);
 
+/* The same round, returning the logits of the listed rows only: rows are
+ * indices into the round, increasing; logits: [n_rows][vocab].  n_rows == 0
+ * appends the positions (their K/V stored) and computes no logits.
+ * Returns 0 or -1. */
+int orc_eval_rows(orc_session* s, const int32_t* tokens, int n, const int* rows,
+                  int n_rows, float* logits);
+
 /* One round over several sessions, processed layer by layer over all rows
  * at once.  logits: [ns][vocab], the last row of each session's round. */
 int orc_eval_batch(orc_session* const* s, const int32_t* const* tokens,

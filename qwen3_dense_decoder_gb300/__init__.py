@@ -86,6 +86,7 @@ def lib():
         L.q3_model_launch_count.restype = i64
         L.q3_op_matmul.argtypes = [vp, vp, i, i, i, vp, i, vp]
         L.q3_op_matmul_splitk_noalloc.argtypes = [vp, vp, i, i, i, i, vp, vp]
+        L.q3_op_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp, i, i, vp]
         L.q3_noalloc_last_error.restype = C.c_char_p
         L.q3_model_profile.argtypes = [vp, i]
         L.q3_model_profile_reset.argtypes = [vp]
@@ -161,15 +162,57 @@ def op_matmul(w: torch.Tensor, x: torch.Tensor, n: int, block_n: int = 0,
 NOALLOC_SCRATCH_FLOATS = 2 * 1024 * 1024
 
 
+OP_STORE, OP_ADD, OP_SWIGLU = 0, 1, 2
+
+
+def op_gemm(w: torch.Tensor, x: torch.Tensor, n: int, epi: int, out: torch.Tensor,
+            w2: torch.Tensor | None = None, block_n: int = 0, k_splits: int = 0,
+            stream=None) -> None:
+    """One prefill-round projection GEMM with its epilogue and split-K
+    (operator gate): OP_STORE out f32 [n, M] = W x; OP_ADD out f32 += W x;
+    OP_SWIGLU out fp16 [n, M] = silu(W x) * (W2 x).  w, w2: fp16 [M, K]; x:
+    fp16 [>= round_up(n, 256), K].  block_n / k_splits 0: the planner's.
+    Synchronous."""
+    M, K = w.shape
+    if w.dtype != torch.float16 or x.dtype != torch.float16:
+        raise ValueError("op_gemm: w and x must be fp16")
+    if x.dim() != 2 or x.shape[1] != K or x.shape[0] < (n + 255) // 256 * 256:
+        raise ValueError("op_gemm: x must be [>= round_up(n, 256), K]")
+    if (epi == OP_SWIGLU) != (w2 is not None) or (w2 is not None and w2.shape != w.shape):
+        raise ValueError("op_gemm: OP_SWIGLU takes w2 of w's shape, other epilogues none")
+    want = torch.float16 if epi == OP_SWIGLU else torch.float32
+    if out.dtype != want or tuple(out.shape) != (n, M):
+        raise ValueError(f"op_gemm: out must be {want} [{n}, {M}]")
+    ts = [w, x, out] + ([w2] if w2 is not None else [])
+    if not all(t.is_contiguous() for t in ts) or len({t.device for t in ts}) != 1:
+        raise ValueError("op_gemm: tensors must be contiguous and on one device")
+    _check(lib().q3_op_gemm(_ptr(w), _ptr(w2), _ptr(x), M, n, K, epi, _ptr(out), block_n, k_splits,
+                            _stream_handle(stream)))
+
+
 def op_matmul_splitk_noalloc(w: torch.Tensor, x: torch.Tensor, n: int, k_splits: int,
                              y: torch.Tensor, stream=None) -> None:
     """Split-K matmul into the caller's y [n, M] f32 that allocates no device
     memory: the partial sums use the library's fixed scratch array.  For
     callers that cannot allocate at the call site (a framework-owned memory
     pool, a plug-in, a latency-critical loop).  Calls that overlap on the GPU
-    race on the shared scratch."""
+    race on the shared scratch.  The library cannot see a buffer's extent, so
+    the shapes are checked here, before anything is launched: w fp16 [M, K],
+    x fp16 [>= round_up(n, 256), K], y f32 [n, M], all contiguous on one
+    device.  Returns once the kernels have finished."""
+    if w.dim() != 2 or x.dim() != 2 or y.dim() != 2:
+        raise ValueError("op_matmul_splitk_noalloc: w, x and y must be 2-D")
     M, K = w.shape
-    assert w.dtype == x.dtype == torch.float16 and y.dtype == torch.float32
+    if w.dtype != torch.float16 or x.dtype != torch.float16 or y.dtype != torch.float32:
+        raise ValueError("op_matmul_splitk_noalloc: w and x fp16, y float32")
+    if x.shape[1] != K or x.shape[0] < (n + 255) // 256 * 256:
+        raise ValueError(f"op_matmul_splitk_noalloc: x must be [>= {(n + 255) // 256 * 256}, {K}]")
+    if tuple(y.shape) != (n, M):
+        raise ValueError(f"op_matmul_splitk_noalloc: y must be [{n}, {M}]")
+    if not (w.is_contiguous() and x.is_contiguous() and y.is_contiguous()):
+        raise ValueError("op_matmul_splitk_noalloc: tensors must be contiguous")
+    if not (w.device == x.device == y.device) or w.device.type != "cuda":
+        raise ValueError("op_matmul_splitk_noalloc: tensors must be on one CUDA device")
     rc = lib().q3_op_matmul_splitk_noalloc(_ptr(w), _ptr(x), M, n, K, k_splits, _ptr(y),
                                            _stream_handle(stream))
     if rc != 0:

@@ -332,13 +332,8 @@ template <int G, bool FUSED>
 cudaError_t launch_g(const Launch& L, const AttnArgs& a)
 {
     const size_t smem = AttnSmem<G>::total;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<G, FUSED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<unsigned long long> attr_done{0};
+    if (cudaError_t e = allow_smem_per_device(attn_kernel<G, FUSED>, (int)smem, attr_done)) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.n_splits, a.n_kv, a.T);
     cfg.blockDim = dim3(AWARPS * 32);

@@ -292,23 +292,17 @@ template <int HPC>
 cudaError_t launch_prefill_g(const Launch& L, const PrefillAttnArgs& a)
 {
     const size_t smem = (size_t)(HPC + 2) * TILE_BYTES + 2 * 2 * TILE_BYTES;   // Q x HPC, K, V fp16 + staged K/V
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<HPC>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
-    static int per_sm = 0, n_sm = 0;
-    if (!per_sm) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_attn_kernel<HPC>, HPC * 4 * 32, smem);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    }
+    static std::atomic<unsigned long long> attr_done{0};
+    if (cudaError_t e = allow_smem_per_device(prefill_attn_kernel<HPC>, (int)smem, attr_done)) return e;
+    // resident CTAs per SM and SMs of the current device (asked on every launch:
+    // cheap beside the kernel, and right on any device)
+    int dev = 0, per_sm = 0, n_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_attn_kernel<HPC>, HPC * 4 * 32, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int items = a.n_tiles * a.n_q / HPC;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(items, per_sm * n_sm));

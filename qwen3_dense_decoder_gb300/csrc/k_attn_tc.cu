@@ -544,13 +544,8 @@ size_t prefill_tc_smem() { return SMEM_BYTES; }
 cudaError_t launch_prefill_attention_tc(const Launch& L, const CUtensorMap& tkv, const PrefillAttnArgs& a, int grid)
 {
     if (prefill_tc_rows(a.n_q, a.n_kv) < 1 || grid < 1) return cudaErrorInvalidValue;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<unsigned long long> attr_done{0};
+    if (cudaError_t e = allow_smem_per_device(prefill_attn_tc_kernel, (int)SMEM_BYTES, attr_done)) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);

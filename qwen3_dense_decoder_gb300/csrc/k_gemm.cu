@@ -352,13 +352,8 @@ cudaError_t launch_bn(const Launch& L, const CUtensorMap& a0, const CUtensorMap&
                       const CUtensorMap& a2, const CUtensorMap& b, const GemmArgs& g)
 {
     using C = GemmCfg<BN>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static std::atomic<unsigned long long> attr_done{0};
+    if (cudaError_t e = allow_smem_per_device(gemm_tc_kernel<BN>, C::SMEM, attr_done)) return e;
     const int n_tiles = (g.N + BN - 1) / BN;
     const int units = n_tiles * (g.M / BM) * g.k_splits;
     const int grid = units < 152 ? units : 152;          // persistent: one CTA per SM

@@ -20,6 +20,8 @@
 // SwiGLU of a gate/up row pair, and the greedy argmax of the lm_head.  Q8_0
 // dequantisation happens in registers: fp16 scale times the block's int8
 // dot product.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -321,12 +323,20 @@ cudaError_t launch_gemv(const Launch& L, int scheme, const GemvArgs& a)
     const int iters = (n_groups + C - 1) / C;
     const int grid = (n_groups + iters - 1) / iters;
     auto kern = scheme == Q3_Q8_0 ? gemv_kernel<Q3_Q8_0> : gemv_kernel<Q3_BF16>;
-    static size_t attr_set[2] = {0, 0};
-    if (smem > 48 * 1024 && attr_set[scheme] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set[scheme] = smem;
+    // the largest dynamic shared memory allowed so far, per device and scheme
+    static std::mutex attr_mu;
+    static size_t attr_set[64][2] = {};
+    if (smem > 48 * 1024) {
+        int dev = 0;
+        if (cudaError_t e = cudaGetDevice(&dev)) return e;
+        std::lock_guard<std::mutex> lock(attr_mu);
+        size_t* have = (dev >= 0 && dev < 64) ? &attr_set[dev][scheme == Q3_Q8_0] : nullptr;
+        if (!have || *have < smem) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            if (have) *have = smem;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

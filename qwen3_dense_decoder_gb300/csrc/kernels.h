@@ -9,7 +9,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace q3 {
+
+// ---------------------------------------------------------------- kernel attributes
+// A kernel that takes more than 48 KB of dynamic shared memory must be
+// allowed it on every device it launches on.  `done` keeps one bit per
+// device id (ids 0..63) so the attribute is set once per device; devices
+// past 63 set it on every launch.
+template <typename Kernel>
+cudaError_t allow_smem_per_device(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // ---------------------------------------------------------------- launch
 // How a kernel is launched: stream, and whether it may start early under

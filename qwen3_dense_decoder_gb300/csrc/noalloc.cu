@@ -15,8 +15,13 @@
 // process exits.  Host code cannot use the array's name as a device address
 // (it is a host-side stand-in), so the first call on each device looks the
 // address up with cudaGetSymbolAddress while that device is current and
-// caches it.  All calls share the one array: two calls whose kernels overlap
-// on the GPU (different streams, no ordering between them) race on it.
+// caches it.  That first call also loads this file's device code, which is
+// when the driver commits the array's memory on that device: make it outside
+// any latency-critical region.  All calls share the one array: two calls
+// whose kernels overlap on the GPU (different streams, no ordering between
+// them) race on it.  Each call reads the status word of its bounded waits
+// back into a host variable and waits for the stream, so it returns only
+// once its kernels have finished and reports a wait that ran out.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -74,16 +79,17 @@ bool device_scratch(DeviceScratch* out)
 
 bool tmap_f16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows)
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    // the driver's encoder, resolved once and thread-safely (a function-local static)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         cudaDriverEntryPointQueryResult q;
         void* p = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &q) != cudaSuccess ||
             q != cudaDriverEntryPointSuccess)
-            return false;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    if (!fn) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {64, box_rows};
@@ -135,7 +141,17 @@ int q3_op_matmul_splitk_noalloc(const void* w_dev, const void* x_dev, int M, int
     Launch L{s, false, nullptr};
     cudaError_t e = launch_gemm(L, a, a, a, b, bn, g);
     if (e == cudaSuccess) e = launch_gemm_splitk_reduce(L, g);
+    // the status word comes back to a host int on this stack (no allocation):
+    // a bounded wait that ran out leaves partial sums behind, so it is an error
+    int word = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&word, d.status, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return noalloc_fail(Q3_ERR_CUDA, cudaGetErrorString(e));
+    if (word) {
+        snprintf(g_msg, sizeof g_msg, "matmul_splitk_noalloc: device status 0x%x (a bounded wait ran out)",
+                 word);
+        return Q3_ERR_DEVICE_CHECK;
+    }
     return Q3_OK;
 }
 

@@ -51,15 +51,16 @@ int fail(int code, const char* fmt, ...)
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    // resolved once, thread-safely (a function-local static)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         cudaDriverEntryPointQueryResult q;
         void* p = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -1503,32 +1504,89 @@ int q3_model_profile_read(q3_model* m, int cls, double* total_ms, int64_t* launc
     return Q3_OK;
 }
 
+// One GEMM of the operator gates on caller buffers: planned (block_n 0) or
+// forced tile width and split-K, with the prefill path's epilogues.  Owns a
+// status word and, for split-K, a partial-sum workspace for the call, and
+// returns once the kernels have finished: a bounded device wait that ran out
+// (or an fp16 output beyond range) is reported, never hidden.
+int op_gemm_sync(const char* name, const void* w_dev, const void* w2_dev, const void* x_dev, int M, int N,
+                 int K, int epi, void* out_dev, int block_n, int k_splits, void* stream)
+{
+    const bool pair = epi == EPI_SWIGLU_F16;
+    const int MA = pair ? 2 * M : M;          // GEMM rows: gate and up rows interleaved by 64-row tiles
+    int bn = block_n, splits = k_splits;
+    if (bn == 0 || splits == 0) {
+        int pbn, ps;
+        plan_gemm_impl(MA, N, K, k_splits == 0 ? (size_t)8 * N * MA : 0, &pbn, &ps);
+        if (bn == 0) bn = pbn;
+        if (splits == 0) splits = ps;
+    }
+    if (!gemm_block_n_supported(bn)) return fail(Q3_ERR_INVALID_ARG, "%s: unsupported block_n", name);
+    if (splits < 1 || splits > 8 || K / 64 < splits)
+        return fail(Q3_ERR_INVALID_ARG, "%s: k_splits must be in [1, 8] and at most K/64", name);
+    CUtensorMap a0, a1, b;
+    if (!tmap_f16(&a0, w_dev, M, K, pair ? 64 : 128) || (pair && !tmap_f16(&a1, w2_dev, M, K, 64)) ||
+        !tmap_f16(&b, x_dev, round_up(N, 256), K, bn))
+        return fail(Q3_ERR_CUDA, "%s: tensor map encoding failed", name);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* status = nullptr;
+    float* ws = nullptr;
+    auto release = [&]() {
+        if (status) cudaFree(status);
+        if (ws) cudaFree(ws);
+    };
+    if (cudaMalloc(&status, sizeof(int)) != cudaSuccess ||
+        (splits > 1 && cudaMalloc(&ws, sizeof(float) * (size_t)splits * N * MA) != cudaSuccess)) {
+        release();
+        return fail(Q3_ERR_OOM, "%s: workspace allocation failed", name);
+    }
+    GemmArgs g{};
+    g.M = MA; g.N = N; g.K = K;
+    g.a_tiles0 = g.a_tiles1 = MA / 128;
+    g.pair = pair ? 1 : 0;
+    g.k_splits = splits;
+    g.epi = epi;
+    g.out = out_dev; g.ldo = M;
+    g.ws = ws;
+    g.status = status;
+    Launch L{st, false, nullptr};
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = launch_gemm(L, a0, pair ? a1 : a0, a0, b, bn, g);
+    if (e == cudaSuccess && splits > 1) e = launch_gemm_splitk_reduce(L, g);
+    int word = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&word, status, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    release();
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
+    if (word) return fail(Q3_ERR_DEVICE_CHECK, "%s: device status 0x%x", name, word);
+    return Q3_OK;
+}
+
 int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, float* y_dev, int block_n,
                  void* stream)
 {
     if (!w_dev || !x_dev || !y_dev || M < 128 || M % 128 || K < 64 || K % 64 || N < 1 ||
         !aligned16(w_dev) || !aligned16(x_dev))
         return fail(Q3_ERR_INVALID_ARG, "op_matmul: bad argument");
-    int bn = block_n, unused;
-    if (bn == 0) plan_gemm_impl(M, N, K, 0, &bn, &unused);   // no workspace: no split-K
-    if (!gemm_block_n_supported(bn)) return fail(Q3_ERR_INVALID_ARG, "op_matmul: unsupported block_n");
-    CUtensorMap a, b;
-    if (!tmap_f16(&a, w_dev, M, K, 128) || !tmap_f16(&b, x_dev, round_up(N, 256), K, bn))
-        return fail(Q3_ERR_CUDA, "op_matmul: tensor map encoding failed");
-    static int* status = nullptr;
-    if (!status && cudaMalloc(&status, sizeof(int)) != cudaSuccess)
-        return fail(Q3_ERR_OOM, "op_matmul: status allocation failed");
-    GemmArgs g{};
-    g.M = M; g.N = N; g.K = K;
-    g.a_tiles0 = g.a_tiles1 = M / 128;
-    g.k_splits = 1;
-    g.epi = EPI_STORE_F32;
-    g.out = y_dev; g.ldo = M;
-    g.status = status;
-    Launch L{static_cast<cudaStream_t>(stream), false, nullptr};
-    cudaError_t e = launch_gemm(L, a, a, a, b, bn, g);
-    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "op_matmul: %s", cudaGetErrorString(e));
-    return Q3_OK;
+    return op_gemm_sync("op_matmul", w_dev, nullptr, x_dev, M, N, K, EPI_STORE_F32, y_dev, block_n, 1, stream);
+}
+
+int q3_op_gemm(const void* w_dev, const void* w2_dev, const void* x_dev, int M, int N, int K, int epi,
+               void* out_dev, int block_n, int k_splits, void* stream)
+{
+    const bool pair = epi == Q3_OP_SWIGLU;
+    if (!w_dev || !x_dev || !out_dev || (pair && !w2_dev) || N < 1 || K < 64 || K % 64 ||
+        M < (pair ? 64 : 128) || M % (pair ? 64 : 128) || !aligned16(w_dev) || !aligned16(x_dev) ||
+        (pair && !aligned16(w2_dev)) || k_splits < 0 || block_n < 0)
+        return fail(Q3_ERR_INVALID_ARG, "op_gemm: bad argument");
+    int kepi;
+    switch (epi) {
+    case Q3_OP_STORE: kepi = EPI_STORE_F32; break;
+    case Q3_OP_ADD: kepi = EPI_ADD_F32; break;
+    case Q3_OP_SWIGLU: kepi = EPI_SWIGLU_F16; break;
+    default: return fail(Q3_ERR_INVALID_ARG, "op_gemm: unknown epilogue %d", epi);
+    }
+    return op_gemm_sync("op_gemm", w_dev, w2_dev, x_dev, M, N, K, kepi, out_dev, block_n, k_splits, stream);
 }
 
 int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, int M, int K,

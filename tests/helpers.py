@@ -5,10 +5,11 @@ the oracle, and compare.
 Comparison rule (Kipp pages: "Reproducing Kipp", section "Model-backed CPU
 and Metal gates"; "Kipp Model Support", section "What the gates check"): the
 full-vocabulary NMSE of the GPU logits against the oracle's is at most 1e-4
-and the argmax is identical.  An argmax is only called ambiguous, and not
-counted as a mismatch, when the oracle's own top-1/top-2 margin is below four
-times the largest absolute logit error measured on that row: then the
-decision is not fixed at the precision the GPU demonstrably has.
+and the argmax is identical.  Every argmax mismatch fails the row.  A row
+whose oracle top-1/top-2 margin is below the fixed AMBIGUOUS_MARGIN is
+flagged "ambiguous" in the parity report (the decision there rests on less
+than ten times the GPU's expected logit error), but the flag excuses
+nothing: it only says which rows came close.
 """
 from __future__ import annotations
 
@@ -23,6 +24,8 @@ import synthetic
 
 GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_facts.json")))
 NMSE_BOUND = GOLD["nmse_gpu_vs_cpu"]["value"]
+# oracle top-1/top-2 margins below this are flagged (reported, never excused)
+AMBIGUOUS_MARGIN = 1e-3
 
 
 def nmse(got, ref) -> float:
@@ -41,11 +44,11 @@ class RowCheck:
 
     @property
     def ambiguous(self) -> bool:
-        return self.margin < 4 * self.max_abs_err
+        return self.margin < AMBIGUOUS_MARGIN
 
     @property
     def ok(self) -> bool:
-        return self.nmse <= NMSE_BOUND and (self.argmax_gpu == self.argmax_ref or self.ambiguous)
+        return self.nmse <= NMSE_BOUND and self.argmax_gpu == self.argmax_ref
 
 
 REPORT: list = []      # (tag, RowCheck) of every checked row, for the parity report

@@ -101,3 +101,24 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "q3_oracle" not in text and "orc_" not in text, f
+
+
+def test_noalloc_binding_checks_shapes_before_any_launch():
+    """The library cannot see a buffer's extent, so the binding refuses a short
+    x or y (which the kernels would read or write past its end) before it
+    touches the library: CPU tensors never reach a launch."""
+    import torch
+    import qwen3_dense_decoder_gb300 as q3
+    w = torch.zeros(256, 128, dtype=torch.float16)
+    y = torch.zeros(40, 256, dtype=torch.float32)
+    bad = [
+        (w, torch.zeros(40, 128, dtype=torch.float16), y),          # x has n rows, not round_up(n, 256)
+        (w, torch.zeros(256, 64, dtype=torch.float16), y),          # x's K differs from w's
+        (w, torch.zeros(256, 128, dtype=torch.float16), torch.zeros(39, 256)),   # y too short
+        (w, torch.zeros(256, 128, dtype=torch.float16), torch.zeros(40, 256, dtype=torch.float16)),
+        (w, torch.zeros(256, 128, dtype=torch.float16).t().contiguous().t(), y),  # not contiguous
+        (w, torch.zeros(256, 128, dtype=torch.float16), y),          # CPU tensors
+    ]
+    for wi, xi, yi in bad:
+        with pytest.raises(ValueError):
+            q3.op_matmul_splitk_noalloc(wi, xi, 40, 2, yi)

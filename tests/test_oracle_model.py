@@ -279,3 +279,25 @@ def test_shapes_follow_the_registry(orc):
     assert orc.AFFINE4_BYTES == (a4["weights_per_group"] * a4["code_bits"] + 2 * 16) // 8
     assert orc.BLOCK == GOLD["kv_block_positions"]["value"]
     assert BF16 == 0
+
+
+@pytest.mark.parametrize("shape", KV_SHAPES, ids=lambda s: s.name)
+def test_selected_rows_and_append_only(orc, shape):
+    """eval_rows returns exactly the listed rows of the every-row logits, and a
+    round appended without logits leaves the same cache as one that computed
+    them (the full-size GPU gates lean on both: they score a sample of the
+    rows of a long round, and prefill long prior contexts with append)."""
+    m, _ = _model(orc, shape)
+    toks = make_tokens(70, shape.vocab, seed=12)
+    full = m.session(max_ctx=128).eval(toks, all_rows=True)
+    rows = [0, 5, 31, 32, 63, 69]
+    got = m.session(max_ctx=128).eval_rows(toks, rows)
+    np.testing.assert_array_equal(got, full[rows])
+    s = m.session(max_ctx=128)
+    s.append(toks[:64])
+    assert s.pos == 64
+    np.testing.assert_array_equal(s.eval(toks[64:], all_rows=True), full[64:])
+    with pytest.raises(RuntimeError):
+        m.session(max_ctx=128).eval_rows(toks[:10], [3, 3])        # rows must increase
+    with pytest.raises(RuntimeError):
+        m.session(max_ctx=128).eval_rows(toks[:10], [10])          # and lie in the round
