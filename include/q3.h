@@ -192,11 +192,42 @@ int q3_eval_batch(q3_session* const* sessions, int ns, const int32_t* tokens_dev
 
 /* Forget positions >= n_pos (truncate/resume); 0 <= n_pos <= position.
  * Blocks past the new end return to the pool unless fixed by
- * q3_session_set_block_table.  Errors: Q3_ERR_INVALID_ARG. */
+ * q3_session_set_block_table.  If the block holding position n_pos is
+ * shared (published, or attached by other sessions), it is first copied to
+ * a block of the session's own, asynchronously on the model's stream.
+ * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_POOL_EXHAUSTED (no block for that
+ * copy), Q3_ERR_CUDA. */
 int q3_session_truncate(q3_session* s, int n_pos);
 /* Back to position 0 (reset/reuse). */
 int q3_session_reset(q3_session* s);
 int q3_session_pos(const q3_session* s);
+
+/* Content-addressed prefix sharing over a pool ("Kipp Roadmap", status
+ * v0.0.3: a content-addressed 32-token block pool, publish-at-finish,
+ * memcmp-verified).  A published block is addressed by the block before it
+ * in its chain and its 32 tokens; a lookup hashes that key (64-bit FNV-1a)
+ * into one of 2^hash_bits buckets and accepts a candidate only if the
+ * previous block and the tokens compare equal, so a collision never shares
+ * a block.  The pool keeps each published block until it needs the room:
+ * with no free block, the least recently published or attached block that
+ * no session holds and no published block follows is reused.
+ *
+ * q3_pool_enable_prefix: once per pool; hash_bits in [0, 24].
+ * q3_session_publish: tokens (host, int32 [n], n == the session's position)
+ *   are the tokens the session evaluated; its full blocks become shared,
+ *   and where an equal chain is already published the session switches to
+ *   it and frees its own blocks.  *n_published: blocks newly published.
+ *   Not for sessions with a table fixed by q3_session_set_block_table.
+ * q3_session_attach_prefix: on an empty session, attach the longest
+ *   published chain matching the leading full blocks of tokens (host, int32
+ *   [n]), leaving at least one token to evaluate; the session's position
+ *   becomes *n_attached (a multiple of 32) and the caller evaluates
+ *   tokens[*n_attached .. n).
+ * A round never writes a shared block (Q3_ERR_INVALID_ARG if it would).
+ * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CTX_OVERFLOW. */
+int q3_pool_enable_prefix(q3_pool* p, int hash_bits);
+int q3_session_publish(q3_session* s, const int32_t* tokens, int n, int* n_published);
+int q3_session_attach_prefix(q3_session* s, const int32_t* tokens, int n, int* n_attached);
 
 /* Wait for the model's stream; read and clear the device status word.
  * Errors: Q3_ERR_CUDA, Q3_ERR_DEVICE_CHECK (both poison), Q3_ERR_POISONED. */

@@ -76,6 +76,9 @@ def lib():
         L.q3_session_eval.argtypes = [vp, vp, i, vp, vp]
         L.q3_eval_batch.argtypes = [vp, i, vp, vp, vp, vp]
         L.q3_session_truncate.argtypes = [vp, i]
+        L.q3_pool_enable_prefix.argtypes = [vp, i]
+        L.q3_session_publish.argtypes = [vp, vp, i, vp]
+        L.q3_session_attach_prefix.argtypes = [vp, vp, i, vp]
         L.q3_session_reset.argtypes = [vp]
         L.q3_session_pos.argtypes = [vp]
         L.q3_sync.argtypes = [vp]
@@ -373,6 +376,10 @@ class Pool:
     def session(self) -> "Session":
         return Session(self)
 
+    def enable_prefix(self, hash_bits: int = 16) -> None:
+        """Content-addressed prefix sharing over this pool (2^hash_bits buckets)."""
+        _check(lib().q3_pool_enable_prefix(self.h, hash_bits))
+
 
 class Session:
     def __init__(self, pool: Pool):
@@ -396,6 +403,24 @@ class Session:
         import numpy as np
         a = np.ascontiguousarray(ids, np.int32)
         _check(lib().q3_session_set_block_table(self.h, a.ctypes.data_as(C.c_void_p), a.size))
+
+    def publish(self, tokens) -> int:
+        """Share the session's full blocks; tokens (host) are those it evaluated.
+        Returns how many blocks were newly published."""
+        import numpy as np
+        a = np.ascontiguousarray(tokens, np.int32)
+        out = C.c_int(0)
+        _check(lib().q3_session_publish(self.h, a.ctypes.data_as(C.c_void_p), a.size, C.byref(out)))
+        return out.value
+
+    def attach_prefix(self, tokens) -> int:
+        """On an empty session: attach the longest published chain matching the
+        prompt's leading full blocks; returns the positions attached."""
+        import numpy as np
+        a = np.ascontiguousarray(tokens, np.int32)
+        out = C.c_int(0)
+        _check(lib().q3_session_attach_prefix(self.h, a.ctypes.data_as(C.c_void_p), a.size, C.byref(out)))
+        return out.value
 
     def eval_n(self, tokens: torch.Tensor, n_logits: int, logits: torch.Tensor,
                argmax: torch.Tensor | None = None) -> None:

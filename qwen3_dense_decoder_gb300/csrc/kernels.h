@@ -249,6 +249,7 @@ struct DecodeArgs {
     unsigned long long* bar;   // grid barrier counter (monotonic across launches)
     unsigned long long bar_base;   // its value when this launch starts
     int n_slots;               // ring depth
+    int pf_tiles;              // L2 prefetch window: tiles ahead of the producer (0: none)
     int* status;
 };
 // Shared memory of the fused step for these dimensions and ring depth; 0 if

@@ -23,6 +23,7 @@
 #include <map>
 #include <queue>
 #include <set>
+#include <unordered_map>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -166,6 +167,7 @@ struct q3_model {
     bool step_ok = false;           // shapes and device support it
     bool fused_decode = true;       // use it when step_ok
     int step_grid = 0, step_slots = 0, step_splits = 0;
+    int step_pf_tiles = 0;      // the fused step's L2 prefetch window (tiles ahead of its producer)
     size_t step_smem = 0;
     DecodeLayer* step_layers = nullptr;       // device [n_layers]
     unsigned long long* step_bar = nullptr;   // grid barrier counter
@@ -277,9 +279,22 @@ struct q3_pool {
     bf16* kv = nullptr;          // [L][n_blocks][2][n_kv][32][128]
     CUtensorMap kv_map;          // kv as rows of 128 (tcgen05 prefill attention)
     int* tables = nullptr;       // [max_sessions][max_blocks]
-    std::set<int> free_blocks;
+    std::set<int> free_blocks;   // blocks nobody holds
+    std::vector<int> holders;    // per block: sessions holding it, +1 while published
     std::vector<char> slot_used;
     int refs = 1;                // the caller's handle + one per live session
+
+    // content-addressed prefix index ("Kipp Roadmap", status v0.0.3): a
+    // published block is found by (parent block, 32 tokens); the hash picks
+    // a bucket and a candidate counts only if parent and tokens compare equal
+    bool prefix_on = false;
+    uint64_t bucket_mask = 0;
+    std::unordered_map<uint64_t, std::vector<int>> buckets;
+    std::vector<int> parent_of, successors;   // per published block
+    std::vector<int64_t> last_use;            // publish or attach order, for eviction
+    std::vector<int32_t> block_tokens;        // [n_blocks][32]
+    std::vector<char> published;
+    int64_t use_clock = 0;
 };
 
 namespace {
@@ -304,6 +319,72 @@ struct q3_session {
 };
 
 namespace {
+
+// ---------------------------------------------------------------- block ownership
+
+uint64_t prefix_key(int parent, const int32_t* t)
+{
+    // 64-bit FNV-1a over the parent id and the 32 tokens, little-endian bytes
+    uint64_t h = 0xcbf29ce484222325ull;
+    auto mix = [&h](uint32_t w) {
+        for (int b = 0; b < 4; ++b) { h ^= (w >> (8 * b)) & 0xffu; h *= 0x100000001b3ull; }
+    };
+    mix((uint32_t)parent);
+    for (int i = 0; i < 32; ++i) mix((uint32_t)t[i]);
+    return h;
+}
+
+int find_published(const q3_pool* p, int parent, const int32_t* t)
+{
+    auto it = p->buckets.find(prefix_key(parent, t) & p->bucket_mask);
+    if (it == p->buckets.end()) return -1;
+    for (int b : it->second)
+        if (p->parent_of[b] == parent &&
+            std::memcmp(&p->block_tokens[(size_t)b * 32], t, 32 * sizeof(int32_t)) == 0)
+            return b;
+    return -1;
+}
+
+void unpublish(q3_pool* p, int b)
+{
+    auto& v = p->buckets[prefix_key(p->parent_of[b], &p->block_tokens[(size_t)b * 32]) & p->bucket_mask];
+    v.erase(std::find(v.begin(), v.end(), b));
+    if (p->parent_of[b] >= 0) --p->successors[p->parent_of[b]];
+    p->parent_of[b] = -1;
+    p->published[b] = 0;
+    if (--p->holders[b] == 0) p->free_blocks.insert(b);
+}
+
+// The lowest free block; with the prefix index on and none free, the
+// published block held by the index alone, with no published successor,
+// used longest ago is evicted.  -1: none.
+int take_block(q3_pool* p)
+{
+    if (p->free_blocks.empty() && p->prefix_on) {
+        int best = -1;
+        for (int b = 0; b < p->n_blocks; ++b)
+            if (p->published[b] && p->holders[b] == 1 && p->successors[b] == 0 &&
+                (best < 0 || p->last_use[b] < p->last_use[best]))
+                best = b;
+        if (best >= 0) unpublish(p, best);
+    }
+    if (p->free_blocks.empty()) return -1;
+    const int b = *p->free_blocks.begin();
+    p->free_blocks.erase(p->free_blocks.begin());
+    p->holders[b] = 1;
+    return b;
+}
+
+void drop_block(q3_pool* p, int b)
+{
+    if (--p->holders[b] == 0) p->free_blocks.insert(b);
+}
+
+// a block another session may read: held twice or published
+bool shared_block(const q3_pool* p, int b)
+{
+    return p->holders[b] > 1 || (p->prefix_on && p->published[b]);
+}
 
 int validate_config(const q3_config* c)
 {
@@ -567,6 +648,10 @@ int setup_decode_step(q3_model* m, int n_sm)
         return fail(Q3_ERR_CUDA, "fused decode setup failed");
     m->step_grid = grid;
     m->step_slots = slots;
+    {
+        const char* e = getenv("Q3_DECODE_PF_TILES");
+        m->step_pf_tiles = e ? atoi(e) : 8;
+    }
     m->step_splits = splits;
     m->step_smem = smem;
     m->step_epoch = 0;
@@ -600,6 +685,7 @@ int run_decode_step(q3_model* m, const Round& r)
     a.am_val = m->step_am_val; a.am_idx = m->step_am_idx; a.am_counter = m->am_counter;
     a.bar = m->step_bar; a.bar_base = m->step_epoch;
     a.n_slots = m->step_slots;
+    a.pf_tiles = m->step_pf_tiles;
     a.status = m->status;
     Launch L{m->stream, false, &m->launches};
     m->prof_begin(Q3_K_STEP);
@@ -806,11 +892,14 @@ int reserve(q3_session* s, int end, std::vector<std::pair<int, int>>* newly)
     const int need = (end + 31) / 32;
     if (need > p->max_blocks) return fail(Q3_ERR_CTX_OVERFLOW, "context %d exceeds max_ctx", end);
     while ((int)s->blocks.size() < need) {
-        if (p->free_blocks.empty()) return fail(Q3_ERR_POOL_EXHAUSTED, "KV pool exhausted");
-        const int b = *p->free_blocks.begin();
-        p->free_blocks.erase(p->free_blocks.begin());
+        const int b = take_block(p);
+        if (b < 0) return fail(Q3_ERR_POOL_EXHAUSTED, "KV pool exhausted");
         s->blocks.push_back(b);
     }
+    // a round writes positions [pos, end): their blocks must be the session's own
+    for (int i = s->pos / 32; i < need; ++i)
+        if (shared_block(p, s->blocks[i]))
+            return fail(Q3_ERR_INVALID_ARG, "round would write shared KV block %d", s->blocks[i]);
     (void)newly;
     return Q3_OK;
 }
@@ -1292,6 +1381,7 @@ int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
         return fail(Q3_ERR_CUDA, "pool: memset failed");
     }
     for (int b = 0; b < n_blocks; ++b) p->free_blocks.insert(p->free_blocks.end(), b);
+    p->holders.assign(n_blocks, 0);
     p->slot_used.assign(max_sessions, 0);
     ++m->refs;
     *out = p;
@@ -1325,7 +1415,7 @@ void q3_session_destroy(q3_session* s)
 {
     if (!s) return;
     q3_pool* p = s->pool;
-    for (int b : s->blocks) p->free_blocks.insert(b);
+    for (int b : s->blocks) drop_block(p, b);
     p->slot_used[s->slot] = 0;
     delete s;
     pool_release(p);
@@ -1337,13 +1427,11 @@ int q3_session_set_block_table(q3_session* s, const int32_t* ids, int n)
     if (s->pos != 0) return fail(Q3_ERR_INVALID_ARG, "set_block_table: session is not empty");
     q3_pool* p = s->pool;
     if (n > p->max_blocks) return fail(Q3_ERR_INVALID_ARG, "set_block_table: more blocks than max_ctx");
-    for (int b : s->blocks) p->free_blocks.insert(b);
+    for (int b : s->blocks) drop_block(p, b);
     s->blocks.clear();
     std::set<int> seen;
     for (int i = 0; i < n; ++i) {
         if (ids[i] < 0 || ids[i] >= p->n_blocks || !p->free_blocks.count(ids[i]) || seen.count(ids[i])) {
-            for (int b : s->blocks) p->free_blocks.insert(b);
-            s->blocks.clear();
             s->n_fixed = 0;
             s->uploaded = 0;
             return fail(Q3_ERR_INVALID_ARG, "set_block_table: block %d not free or out of range", ids[i]);
@@ -1352,6 +1440,7 @@ int q3_session_set_block_table(q3_session* s, const int32_t* ids, int n)
     }
     for (int i = 0; i < n; ++i) {
         p->free_blocks.erase(ids[i]);
+        p->holders[ids[i]] = 1;
         s->blocks.push_back(ids[i]);
     }
     s->n_fixed = n;
@@ -1413,17 +1502,111 @@ int q3_eval_batch(q3_session* const* sessions, int ns, const int32_t* tokens_dev
 int q3_session_truncate(q3_session* s, int n_pos)
 {
     if (!s || n_pos < 0 || n_pos > s->pos) return fail(Q3_ERR_INVALID_ARG, "truncate: bad position");
-    s->pos = n_pos;
+    q3_pool* p = s->pool;
     const int keep = std::max((n_pos + 31) / 32, s->n_fixed);
     while ((int)s->blocks.size() > keep) {
-        s->pool->free_blocks.insert(s->blocks.back());
+        drop_block(p, s->blocks.back());
         s->blocks.pop_back();
     }
+    // the block position n_pos falls in is written next: a shared one is
+    // copied to a block of the session's own first (all layers, K and V)
+    const int last = n_pos / 32;
+    if (n_pos % 32 && last < (int)s->blocks.size() && shared_block(p, s->blocks[last])) {
+        q3_model* m = p->m;
+        const int b = s->blocks[last], nb = take_block(p);
+        if (nb < 0) return fail(Q3_ERR_POOL_EXHAUSTED, "truncate: no block for the copy of a shared block");
+        const size_t blk = (size_t)2 * m->c.n_kv_heads * 32 * 128;      // bf16 values per block and layer
+        for (int l = 0; l < m->c.n_layers; ++l) {
+            const int rc = m->check(cudaMemcpyAsync(p->kv + ((size_t)l * p->n_blocks + nb) * blk,
+                                                    p->kv + ((size_t)l * p->n_blocks + b) * blk,
+                                                    blk * sizeof(bf16), cudaMemcpyDeviceToDevice, m->stream),
+                                    "shared block copy");
+            if (rc) return rc;
+        }
+        drop_block(p, b);
+        s->blocks[last] = nb;
+        s->uploaded = std::min(s->uploaded, last);
+    }
+    s->pos = n_pos;
     s->uploaded = std::min(s->uploaded, (int)s->blocks.size());
     return Q3_OK;
 }
 
 int q3_session_reset(q3_session* s) { return q3_session_truncate(s, 0); }
+
+int q3_pool_enable_prefix(q3_pool* p, int hash_bits)
+{
+    if (!p || hash_bits < 0 || hash_bits > 24) return fail(Q3_ERR_INVALID_ARG, "enable_prefix: bad argument");
+    if (p->prefix_on) return fail(Q3_ERR_INVALID_ARG, "enable_prefix: already enabled");
+    const size_t n = (size_t)p->n_blocks;
+    p->bucket_mask = ((uint64_t)1 << hash_bits) - 1;
+    p->parent_of.assign(n, -1);
+    p->successors.assign(n, 0);
+    p->last_use.assign(n, 0);
+    p->block_tokens.assign(n * 32, 0);
+    p->published.assign(n, 0);
+    p->prefix_on = true;
+    return Q3_OK;
+}
+
+int q3_session_publish(q3_session* s, const int32_t* tokens, int n, int* n_published)
+{
+    if (!s || (n > 0 && !tokens) || n != (s ? s->pos : 0))
+        return fail(Q3_ERR_INVALID_ARG, "publish: tokens must cover the session's positions");
+    q3_pool* p = s->pool;
+    if (!p->prefix_on || s->n_fixed) return fail(Q3_ERR_INVALID_ARG, "publish: no prefix index, or a fixed table");
+    int parent = -1, count = 0;
+    for (int i = 0; i < s->pos / 32; ++i) {
+        int b = s->blocks[i];
+        const int32_t* t = tokens + (size_t)i * 32;
+        if (!p->published[b]) {
+            const int e = find_published(p, parent, t);
+            if (e >= 0) {                      // an equal block: share it, free ours
+                ++p->holders[e];
+                drop_block(p, b);
+                s->blocks[i] = e;
+                s->uploaded = std::min(s->uploaded, i);
+                b = e;
+            } else {
+                std::memcpy(&p->block_tokens[(size_t)b * 32], t, 32 * sizeof(int32_t));
+                p->parent_of[b] = parent;
+                p->buckets[prefix_key(parent, t) & p->bucket_mask].push_back(b);
+                p->published[b] = 1;
+                p->last_use[b] = ++p->use_clock;
+                ++p->holders[b];
+                if (parent >= 0) ++p->successors[parent];
+                ++count;
+            }
+        }
+        parent = b;
+    }
+    if (n_published) *n_published = count;
+    return Q3_OK;
+}
+
+int q3_session_attach_prefix(q3_session* s, const int32_t* tokens, int n, int* n_attached)
+{
+    if (!s || !tokens || n < 1) return fail(Q3_ERR_INVALID_ARG, "attach_prefix: bad argument");
+    q3_pool* p = s->pool;
+    if (!p->prefix_on || s->pos != 0 || s->n_fixed)
+        return fail(Q3_ERR_INVALID_ARG, "attach_prefix: no prefix index, a non-empty session or a fixed table");
+    if (n > p->m->c.max_ctx) return fail(Q3_ERR_CTX_OVERFLOW, "attach_prefix: prompt exceeds max_ctx");
+    for (int b : s->blocks) drop_block(p, b);
+    s->blocks.clear();
+    int parent = -1;
+    for (int i = 0; i < (n - 1) / 32; ++i) {          // at least one token stays to evaluate
+        const int e = find_published(p, parent, tokens + (size_t)i * 32);
+        if (e < 0) break;
+        ++p->holders[e];
+        p->last_use[e] = ++p->use_clock;
+        s->blocks.push_back(e);
+        parent = e;
+    }
+    s->pos = 32 * (int)s->blocks.size();
+    s->uploaded = 0;
+    if (n_attached) *n_attached = s->pos;
+    return Q3_OK;
+}
 
 int q3_session_pos(const q3_session* s) { return s ? s->pos : -1; }
 
