@@ -83,12 +83,22 @@ typedef struct q3_session q3_session;
  * n_kv_heads (GQA group of at most 8), hidden, ffn, vocab and
  * n_q_heads*head_dim multiples of 128.  max_ctx bounds a session's length
  * (the RoPE table is built for it).  scheme: Q3_BF16, Q3_Q8_0 or Q3_AFFINE4
- * (the seven projections only).  tied: 1 when lm_head is the token embedding. */
+ * (the seven projections only).  tied: 1 when lm_head is the token embedding.
+ * kv_scheme: Q3_BF16 (the K/V storage contract of "Kipp Model Support",
+ * section "qwen3-0.6b-base") or Q3_Q8_0, the opt-in quantized cache of "Kipp
+ * Roadmap", status v0.0.4: every position's K and V head rows (after the q/k
+ * norm and RoPE) packed by the weights' Q8_0 rule -- blocks of 32 values,
+ * d = absmax / 127 in FP32, stored as fp16(d), codes round-half-even(x / d)
+ * clamped to [-127, 127] -- 136 bytes per head row against 256, about 1.9x
+ * smaller.  Attention reads fp16(fp16 d * code) (each product rounded once);
+ * a Q8_0-cache model runs prefill attention on the mma.sync kernel and
+ * one-session decode on the per-operation path. */
 typedef struct q3_config {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, max_ctx;
     float rope_theta, rms_eps;
     int tied;
     int scheme;
+    int kv_scheme;
 } q3_config;
 
 /* Device pointers of one layer.  Norm gains are bf16 [hidden] (attn_norm,
@@ -139,10 +149,12 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
                     void* stream, q3_model** out);
 void q3_model_destroy(q3_model* m);
 
-/* A pool of n_blocks KV blocks of 32 positions for all layers (BF16 K and
- * V), owned by the library; up to max_sessions sessions draw from it.  One
- * block holds n_layers * 2 * n_kv_heads * 32 * head_dim bf16 values.
- * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_OOM. */
+/* A pool of n_blocks KV blocks of 32 positions for all layers, owned by the
+ * library; up to max_sessions sessions draw from it.  One block holds, per
+ * layer, K and V of every KV head: 32 * head_dim bf16 values each, or with
+ * the Q8_0 cache a tile of 4,096 int8 codes ([32 positions][128]) followed
+ * by 128 fp16 scales ([32 positions][4]).  Errors: Q3_ERR_INVALID_ARG,
+ * Q3_ERR_OOM. */
 int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out);
 void q3_pool_destroy(q3_pool* p);
 
@@ -396,6 +408,18 @@ int q3_model_fused_decode(const q3_model* m);
  * kernel is in use, 0 otherwise. */
 int q3_model_set_prefill_tc(q3_model* m, int on);
 int q3_model_prefill_tc(const q3_model* m);
+
+/* Bytes one position's K and V take in one layer of the cache: 2 * n_kv *
+ * 256 (BF16) or 2 * n_kv * 136 (Q8_0); -1 for a NULL model. */
+int q3_model_kv_bytes_per_position(const q3_model* m);
+
+/* q3_op_kv_pack_q8_0: the Q8_0 cache writers' packing on caller rows
+ * (operator gate of the cache writers, "Kipp Roadmap", status v0.0.4).
+ * rows_dev: f32 [n_rows][128], 16-byte aligned; out_dev: [n_rows][136]
+ * bytes, each row four canonical Q8_0 blocks of 34 bytes (little-endian
+ * fp16 scale, then 32 int8 codes), by the rule q3_config's kv_scheme states.
+ * Asynchronous on stream.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
+int q3_op_kv_pack_q8_0(const float* rows_dev, int n_rows, void* out_dev, void* stream);
 
 /* Message of the last error on this host thread ("" if none). */
 const char* q3_last_error(void);

@@ -35,7 +35,8 @@ class _Config(C.Structure):
     _fields_ = [("n_layers", C.c_int), ("hidden", C.c_int), ("n_q_heads", C.c_int),
                 ("n_kv_heads", C.c_int), ("head_dim", C.c_int), ("ffn", C.c_int),
                 ("vocab", C.c_int), ("max_ctx", C.c_int), ("rope_theta", C.c_float),
-                ("rms_eps", C.c_float), ("tied", C.c_int), ("scheme", C.c_int)]
+                ("rms_eps", C.c_float), ("tied", C.c_int), ("scheme", C.c_int),
+                ("kv_scheme", C.c_int)]
 
 
 class _LayerW(C.Structure):
@@ -100,6 +101,8 @@ def lib():
         L.q3_model_set_fused_decode.argtypes = [vp, i]
         L.q3_model_fused_decode.argtypes = [vp]
         L.q3_model_set_prefill_tc.argtypes = [vp, i]
+        L.q3_model_kv_bytes_per_position.argtypes = [vp]
+        L.q3_op_kv_pack_q8_0.argtypes = [vp, i, vp, vp]
         L.q3_model_prefill_tc.argtypes = [vp]
         _lib = L
     return _lib
@@ -222,6 +225,16 @@ def op_matmul_splitk_noalloc(w: torch.Tensor, x: torch.Tensor, n: int, k_splits:
         raise Q3Error(rc, lib().q3_noalloc_last_error().decode())
 
 
+def op_kv_pack_q8_0(rows: torch.Tensor, stream=None) -> torch.Tensor:
+    """The Q8_0 cache writers' packing of f32 rows [n, 128] into canonical
+    Q8_0 blocks (uint8 [n, 136]) (operator gate)."""
+    if rows.dtype != torch.float32 or rows.dim() != 2 or rows.shape[1] != 128 or not rows.is_contiguous():
+        raise ValueError("op_kv_pack_q8_0: rows must be contiguous float32 [n, 128]")
+    out = torch.empty(rows.shape[0], 136, dtype=torch.uint8, device=rows.device)
+    _check(lib().q3_op_kv_pack_q8_0(_ptr(rows), rows.shape[0], _ptr(out), _stream_handle(stream)))
+    return out
+
+
 def op_matvec(w: torch.Tensor, x: torch.Tensor, scales: torch.Tensor | None = None,
               stream=None) -> torch.Tensor:
     """y[m] = sum_k w[m][k] x[k] on the decode GEMV (operator gate).  w: bf16
@@ -261,14 +274,15 @@ class Model:
 
     def __init__(self, shape, weights: dict, max_ctx: int, max_round_tokens: int = 2048,
                  stream=None):
-        if getattr(shape, "kv_quant", BF16) != BF16:
-            raise ValueError("the CUDA path keeps K/V in bf16; a Q8_0 KV cache is not built on it")
+        kv_scheme = getattr(shape, "kv_quant", BF16)
+        if kv_scheme not in (BF16, Q8_0):
+            raise ValueError(f"unknown K/V cache scheme {kv_scheme}")
         self.shape = shape
         self.stream = stream or torch.cuda.current_stream()
         self._keep = weights
         cfg = _Config(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
                       shape.head_dim, shape.ffn, shape.vocab, max_ctx, shape.rope_theta,
-                      shape.rms_eps, int(shape.tied), shape.scheme)
+                      shape.rms_eps, int(shape.tied), shape.scheme, kv_scheme)
         layers = (_LayerW * shape.n_layers)()
         for li, lw in enumerate(weights["layers"]):
             for name in ("attn_norm", "q_norm", "k_norm", "ffn_norm") + PROJ:
@@ -302,6 +316,11 @@ class Model:
 
     def sync(self) -> None:
         _check(lib().q3_sync(self.h))
+
+    @property
+    def kv_bytes_per_position(self) -> int:
+        """Bytes one position's K and V take in one layer of the cache."""
+        return lib().q3_model_kv_bytes_per_position(self.h)
 
     @property
     def launch_count(self) -> int:

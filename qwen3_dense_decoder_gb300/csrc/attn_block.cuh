@@ -7,7 +7,9 @@
 // in base 2 (log2(e) folded into q), O += P V.  q and P enter the BF16
 // products as high/low BF16 pairs (row 2h the high part of head h, row
 // 2h + 1 the remainder), so both products keep about 16 bits while K and V
-// are used exactly as stored.
+// are used exactly as stored.  With the opt-in Q8_0 cache the staged tiles
+// hold fp16(scale * code) and the products run in fp16, q and P as fp16
+// high/low pairs (about 22 bits).
 #pragma once
 
 #include "common.cuh"
@@ -36,6 +38,32 @@ Q3_DEV uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
+// the same with fp16 inputs
+Q3_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                    uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                 "{%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+Q3_DEV uint32_t pack_h2(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+// operand type of the block products: bf16 (the BF16 cache) or fp16 (Q8_0 cache)
+template <bool F16>
+Q3_DEV void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    if (F16) mma_f16(d, a0, a1, a2, a3, b0, b1);
+    else mma_bf16(d, a0, a1, a2, a3, b0, b1);
+}
+template <bool F16>
+Q3_DEV float round_op(float x) {
+    return F16 ? __half2float(__float2half_rn(x)) : __bfloat162float(__float2bfloat16_rn(x));
+}
+template <bool F16>
+Q3_DEV uint32_t pack_op(float lo, float hi) {
+    return F16 ? pack_h2(lo, hi) : pack_bf16(lo, hi);
+}
 
 // Online-softmax state of one warp over its blocks: the warp holds S and O
 // rows g = lane / 4 and g + 8 of the 16-row operands, row r standing for
@@ -58,9 +86,10 @@ Q3_DEV const uint8_t* tile_chunk(const uint8_t* t, int r, int c) {
 // of sqa, rows of ATT_KSTR bf16), output dimensions [8 dt0, 8 (dt0 + NDT)):
 // S = q K^T on 4 x 8 mma (positions x dims), masked to n_pos, online
 // softmax, O += P V on NDT x 2.
-template <int NDT>
-Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const __nv_bfloat16* sqa, int n_pos, int dt0,
+template <int NDT, bool F16 = false>
+Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const void* sqa_, int n_pos, int dt0,
                             int lane, AttAcc<NDT>& w) {
+    const uint16_t* sqa = static_cast<const uint16_t*>(sqa_);
     const int g = lane >> 2, tig = lane & 3;
     float sacc[4][4];
 #pragma unroll
@@ -76,8 +105,8 @@ Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const __nv_bfl
             uint32_t b[4];
             // B: positions 16 nh + (0-7 | 8-15) x dims (0-7 | 8-15) of this k step
             ldsm_x4(b, tile_chunk(kt, nh * 16 + (mi >> 1) * 8 + r8, kk * 2 + (mi & 1)));
-            mma_bf16(sacc[2 * nh], a[0], a[1], a[2], a[3], b[0], b[1]);
-            mma_bf16(sacc[2 * nh + 1], a[0], a[1], a[2], a[3], b[2], b[3]);
+            mma_kv<F16>(sacc[2 * nh], a[0], a[1], a[2], a[3], b[0], b[1]);
+            mma_kv<F16>(sacc[2 * nh + 1], a[0], a[1], a[2], a[3], b[2], b[3]);
         }
     }
     // rows 2h and 2h + 1 hold the two parts of head h: add them (lanes g ^ 1)
@@ -116,9 +145,9 @@ Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const __nv_bfl
 #pragma unroll
         for (int hp = 0; hp < 2; ++hp) {
             const float x0 = pv[2 * hp], x1 = pv[2 * hp + 1];
-            const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-            const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-            pa[nt][hp] = hi_row ? pack_bf16(h0, h1) : pack_bf16(x0 - h0, x1 - h1);
+            const float h0 = round_op<F16>(x0);
+            const float h1 = round_op<F16>(x1);
+            pa[nt][hp] = hi_row ? pack_op<F16>(h0, h1) : pack_op<F16>(x0 - h0, x1 - h1);
         }
     }
 #pragma unroll
@@ -138,8 +167,8 @@ Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const __nv_bfl
         uint32_t b[4];
         // V^T: matrices of positions (0-7 | 8-15 | 16-23 | 24-31) x dims 8 (dt0 + dt)
         ldsm_x4_t(b, tile_chunk(vt, mi * 8 + r8, dt0 + dt));
-        mma_bf16(w.o[dt], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b[0], b[1]);
-        mma_bf16(w.o[dt], pa[2][0], pa[2][1], pa[3][0], pa[3][1], b[2], b[3]);
+        mma_kv<F16>(w.o[dt], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b[0], b[1]);
+        mma_kv<F16>(w.o[dt], pa[2][0], pa[2][1], pa[3][0], pa[3][1], b[2], b[3]);
     }
 }
 

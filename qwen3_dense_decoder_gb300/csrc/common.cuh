@@ -97,6 +97,59 @@ Q3_DEV void head_norm_rope(float (&y)[4], const __nv_bfloat16* gain, const float
     for (int e = 0; e < 4; ++e) y[e] = out[e];
 }
 
+// ---------------------------------------------------------------- Q8_0 K/V rows
+// The opt-in Q8_0 K/V cache ("Kipp Roadmap", status v0.0.4: an opt-in Q8_0 KV
+// cache, about 1.9x smaller than BF16) packs each position's 128-wide head
+// row with the weights' Q8_0 rule ("Kipp Model Support", section
+// "Quantization (Q8_0)"): blocks of 32 consecutive values, d = absmax / 127
+// in FP32 (correctly rounded), stored as fp16(d); codes round-half-even(x / d)
+// against the FP32 d, clamped to [-127, 127]; an all-zero block has d = 0.
+// The pool's tile layout (KVQ_CODES, KVQ_TILE) is in kernels.h.
+
+// One head row held by a warp, lane l values [4l, 4l + 4): block b is lanes
+// 8b .. 8b + 7.  Returns the lane's four codes (bytes, value 4l + i in byte
+// i), its block's fp16 scale, and the values the cache then holds (fp16
+// scale times code, exact in FP32).
+Q3_DEV void kvq_pack(const float (&y)[4], uint32_t& codes, __half& scale, float (&deq)[4]) {
+    float am = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    const float d = __fdiv_rn(am, 127.0f);
+    scale = __float2half_rn(d);
+    const float ds = __half2float(scale);
+    codes = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        int q = 0;
+        if (d != 0.0f) q = (int)fminf(fmaxf(rintf(__fdiv_rn(y[e], d)), -127.0f), 127.0f);
+        codes |= (uint32_t)(q & 0xff) << (8 * e);
+        deq[e] = ds * (float)q;
+    }
+}
+
+// Store a packed row at position r of a pool tile (lane l: codes of values
+// [4l, 4l + 4); lane 8b: the scale of block b).
+Q3_DEV void kvq_store(uint8_t* tile, int r, uint32_t codes, __half scale, int lane) {
+    *reinterpret_cast<uint32_t*>(tile + r * 128 + lane * 4) = codes;
+    if ((lane & 7) == 0) *reinterpret_cast<__half*>(tile + KVQ_CODES + (r * 4 + (lane >> 3)) * 2) = scale;
+}
+
+// Four codes (bytes of w) times the fp16 scale d, each product rounded once to
+// fp16 (the tensor-core operand type): two fp16 pairs.  A byte b becomes
+// 1024 + (b ^ 0x80) as the fp16 0x64 << 8 | (b ^ 0x80), exactly; subtracting
+// 1152 leaves the signed code, and the multiply rounds the exact product.
+Q3_DEV uint2 kvq_dequant4(uint32_t w, __half d) {
+    const uint32_t f = w ^ 0x80808080u;
+    const uint32_t lo = __byte_perm(f, 0x64646464u, 0x5140);      // bytes 0, 1
+    const uint32_t hi = __byte_perm(f, 0x64646464u, 0x5342);      // bytes 2, 3
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));   // 1152
+    const __half2 dd = __half2half2(d);
+    __half2 a = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), bias), dd);
+    __half2 b = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), bias), dd);
+    return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+}
+
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch: a kernel may start while its predecessor
 // drains; it must call grid_dep_wait() before touching what the predecessor

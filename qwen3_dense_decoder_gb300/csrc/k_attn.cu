@@ -20,6 +20,12 @@
 // split CTA of the (row, KV head) finishes last (an atomic ticket, no
 // waiting), so the result does not depend on scheduling.
 //
+// With the opt-in Q8_0 cache ("Kipp Roadmap", status v0.0.4) a warp copies
+// the block's raw Q8_0 tiles (codes and fp16 scales, 4,352 bytes each for K
+// and V) and expands them in shared memory into fp16 tiles of scale * code
+// (each product rounded once to fp16), then attends them with fp16 products;
+// the new position's K/V are packed by the same rule as every other row.
+//
 // Decode rounds (each row the single new token of its session) fuse the
 // per-head q/k RMSNorm, RoPE and the K/V append of that token: the new K/V
 // row goes to the cache and straight into the staged tile, so tiles of
@@ -41,14 +47,15 @@ constexpr int K_TILE = KV_BLOCK * K_STRIDE;
 constexpr int V_TILE = KV_BLOCK * K_STRIDE;
 constexpr int NDT = D / 8;             // a warp attends all 16 dimension tiles of its blocks
 
-template <int G>
+template <int G, bool KQ>
 struct AttnSmem {
-    static constexpr size_t q_bytes = (size_t)16 * K_STRIDE * 2;     // q high/low rows (bf16)
+    static constexpr size_t q_bytes = (size_t)16 * K_STRIDE * 2;     // q high/low rows (bf16 or fp16)
     static constexpr size_t k_bytes = (size_t)AWARPS * K_TILE * 2;
     static constexpr size_t v_bytes = (size_t)AWARPS * V_TILE * 2;
-    static constexpr size_t new_bytes = 2 * D * 2;                  // new K and V row (bf16)
+    static constexpr size_t new_bytes = 2 * D * 2;                  // new K and V row (bf16 or fp16)
     static constexpr size_t misc_bytes = 2 * AWARPS * G * sizeof(float) + 16;
-    static constexpr size_t total = q_bytes + k_bytes + v_bytes + new_bytes + misc_bytes;
+    static constexpr size_t raw_bytes = KQ ? (size_t)AWARPS * 2 * KVQ_TILE : 0;   // Q8_0 K and V tiles
+    static constexpr size_t total = q_bytes + k_bytes + v_bytes + new_bytes + misc_bytes + raw_bytes;
 };
 
 // stage the K and V tiles of one 32-position block: 2 x 32 rows of 256 bytes,
@@ -65,26 +72,48 @@ Q3_DEV void stage_block(__nv_bfloat16* kt, __nv_bfloat16* vt, const __nv_bfloat1
     cp_async_commit();
 }
 
-// head g's q (lane: dims [4 lane, 4 lane + 4)), scaled, as BF16 rows 2g
-// (high part) and 2g + 1 (remainder) of the 16-row tensor-core operand
+// stage the raw Q8_0 K and V tiles of one block: 2 x 272 16-byte pieces
+Q3_DEV void stage_block_q8(uint8_t* raw, const uint8_t* Kq, const uint8_t* Vq, int lane) {
+    for (int i = lane; i < KVQ_TILE / 16; i += 32) {
+        cp_async_16(raw + i * 16, Kq + i * 16);
+        cp_async_16(raw + KVQ_TILE + i * 16, Vq + i * 16);
+    }
+    cp_async_commit();
+}
+
+// expand one staged Q8_0 tile into an fp16 tile of scale * code (rows of
+// K_STRIDE halves); lane l takes values [4l, 4l + 4) of every row
+Q3_DEV void expand_q8(__nv_bfloat16* tile, const uint8_t* raw, int lane) {
+#pragma unroll 4
+    for (int r = 0; r < 32; ++r) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + r * 128 + lane * 4);
+        const __half d = *reinterpret_cast<const __half*>(raw + KVQ_CODES + (r * 4 + (lane >> 3)) * 2);
+        *reinterpret_cast<uint2*>(tile + r * K_STRIDE + lane * 4) = kvq_dequant4(w, d);
+    }
+}
+
+// head g's q (lane: dims [4 lane, 4 lane + 4)), scaled, as rows 2g (high
+// part) and 2g + 1 (remainder) of the 16-row tensor-core operand, in the
+// operand type of the block products (bf16, or fp16 for the Q8_0 cache)
+template <bool F16>
 Q3_DEV void store_q_split(__nv_bfloat16* sqa, int g, const float (&y)[4], float scale, int lane) {
     float hi[4], lo[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const float q = y[e] * scale;
-        hi[e] = __bfloat162float(__float2bfloat16_rn(q));
+        hi[e] = round_op<F16>(q);
         lo[e] = q - hi[e];
     }
     *reinterpret_cast<uint2*>(sqa + (2 * g) * K_STRIDE + lane * 4) =
-        make_uint2(pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]));
+        make_uint2(pack_op<F16>(hi[0], hi[1]), pack_op<F16>(hi[2], hi[3]));
     *reinterpret_cast<uint2*>(sqa + (2 * g + 1) * K_STRIDE + lane * 4) =
-        make_uint2(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]));
+        make_uint2(pack_op<F16>(lo[0], lo[1]), pack_op<F16>(lo[2], lo[3]));
 }
 
-template <int G, bool FUSED>
-__global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
+template <int G, bool FUSED, bool KQ>
+__global__ void __launch_bounds__(AWARPS * 32, KQ ? 2 : 3) attn_kernel(const AttnArgs p)
 {
-    using S = AttnSmem<G>;
+    using S = AttnSmem<G, KQ>;
     extern __shared__ __align__(16) uint8_t smem[];
     __nv_bfloat16* sqa = reinterpret_cast<__nv_bfloat16*>(smem);                  // [16][K_STRIDE]
     __nv_bfloat16* kt_all = reinterpret_cast<__nv_bfloat16*>(smem + S::q_bytes);
@@ -93,6 +122,7 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     float* s_m = reinterpret_cast<float*>(smem + S::q_bytes + S::k_bytes + S::v_bytes + S::new_bytes);
     float* s_l = s_m + AWARPS * G;
     float* s_o = reinterpret_cast<float*>(kt_all);     // [AWARPS][G][D], reuses the K tiles at the end
+    uint8_t* raw_all = smem + S::q_bytes + S::k_bytes + S::v_bytes + S::new_bytes + S::misc_bytes;
     __shared__ int s_ticket;
 
     const int split = blockIdx.x, kvh = blockIdx.y;
@@ -100,6 +130,7 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __nv_bfloat16* kt = kt_all + warp * K_TILE;
     __nv_bfloat16* vt = vt_all + warp * V_TILE;
+    uint8_t* raw = raw_all + (size_t)warp * 2 * KVQ_TILE;     // (Q8_0 cache only)
 
     // Row metadata and block tables were uploaded before the round began, so
     // they may be read before the programmatic-launch wait.
@@ -114,23 +145,23 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     const size_t head_elems = (size_t)KV_BLOCK * D;
     const int last_blk = nblk - 1;
 
-    auto block_ptr = [&](int b, const __nv_bfloat16*& Kb) -> bool {
+    // issue the copies of block b's K/V (bf16 tiles, or raw Q8_0 tiles)
+    auto stage = [&](int b) -> bool {
         const int phys = table[b];
         if (phys < 0 || phys >= p.n_blocks) return false;
-        Kb = p.kv_layer + ((size_t)phys * 2 * p.n_kv + kvh) * head_elems;
+        if (KQ) {
+            const uint8_t* Kq = p.kvq_layer + ((size_t)phys * 2 * p.n_kv + kvh) * KVQ_TILE;
+            stage_block_q8(raw, Kq, Kq + (size_t)p.n_kv * KVQ_TILE, lane);
+        } else {
+            const __nv_bfloat16* Kb = p.kv_layer + ((size_t)phys * 2 * p.n_kv + kvh) * head_elems;
+            stage_block(kt, vt, Kb, Kb + (size_t)p.n_kv * head_elems, lane);
+        }
         return true;
     };
 
     int b = b0 + warp;
     bool staged = false;
-    if (FUSED && b < b1) {
-        // K/V of earlier rounds do not depend on the kernels of this round
-        const __nv_bfloat16* Kb;
-        if (block_ptr(b, Kb)) {
-            stage_block(kt, vt, Kb, Kb + (size_t)p.n_kv * head_elems, lane);
-            staged = true;
-        }
-    }
+    if (FUSED && b < b1) staged = stage(b);   // K/V of earlier rounds do not depend on this round's kernels
 
     if (threadIdx.x == 0)
         issue_l2_prefetch(p.next, blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z),
@@ -151,7 +182,7 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
             const float4 v = *reinterpret_cast<const float4*>(row + (kvh * G + g) * D + lane * 4);
             float y[4] = {v.x, v.y, v.z, v.w};
             head_norm_rope(y, p.q_gain, rope_row, p.eps, lane);
-            store_q_split(sqa, g, y, qscale, lane);
+            store_q_split<KQ>(sqa, g, y, qscale, lane);
         }
         const bool mine = b0 <= last_blk && last_blk < b1;   // this split holds the new position
         if (mine && warp >= AWARPS - 2) {
@@ -160,27 +191,40 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
                 row + (p.n_q + (is_k ? 0 : p.n_kv) + kvh) * D + lane * 4);
             float y[4] = {v.x, v.y, v.z, v.w};
             if (is_k) head_norm_rope(y, p.k_gain, rope_row, p.eps, lane);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
-            uint2 packed;
-            packed.x = *reinterpret_cast<const uint32_t*>(&lo);
-            packed.y = *reinterpret_cast<const uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(snew + (is_k ? 0 : D) + lane * 4) = packed;
             const int phys = table[last_blk];
-            if (phys >= 0 && phys < p.n_blocks) {
-                __nv_bfloat16* dst = p.kv_layer +
-                    (((size_t)phys * 2 + (is_k ? 0 : 1)) * p.n_kv + kvh) * head_elems +
-                    (size_t)(pos % KV_BLOCK) * D + lane * 4;
-                *reinterpret_cast<uint2*>(dst) = packed;
-            } else if (lane == 0) {
-                set_status(p.status, Q3_STATUS_BLOCK_RANGE);
+            const bool in_pool = phys >= 0 && phys < p.n_blocks;
+            if (KQ) {
+                // packed by the cache's Q8_0 rule; the tile gets the values the cache holds
+                uint32_t codes;
+                __half scale;
+                float deq[4];
+                kvq_pack(y, codes, scale, deq);
+                *reinterpret_cast<uint2*>(snew + (is_k ? 0 : D) + lane * 4) =
+                    make_uint2(pack_h2(deq[0], deq[1]), pack_h2(deq[2], deq[3]));
+                if (in_pool)
+                    kvq_store(p.kvq_layer + (((size_t)phys * 2 + (is_k ? 0 : 1)) * p.n_kv + kvh) * KVQ_TILE,
+                              pos % KV_BLOCK, codes, scale, lane);
+            } else {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
+                uint2 packed;
+                packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+                packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(snew + (is_k ? 0 : D) + lane * 4) = packed;
+                if (in_pool) {
+                    __nv_bfloat16* dst = p.kv_layer +
+                        (((size_t)phys * 2 + (is_k ? 0 : 1)) * p.n_kv + kvh) * head_elems +
+                        (size_t)(pos % KV_BLOCK) * D + lane * 4;
+                    *reinterpret_cast<uint2*>(dst) = packed;
+                }
             }
+            if (!in_pool && lane == 0) set_status(p.status, Q3_STATUS_BLOCK_RANGE);
         }
     } else {
         for (int g = warp; g < G; g += AWARPS) {
             const float4 v = *reinterpret_cast<const float4*>(p.q + ((size_t)t * p.n_q + kvh * G + g) * D + lane * 4);
             float y[4] = {v.x, v.y, v.z, v.w};
-            store_q_split(sqa, g, y, qscale, lane);
+            store_q_split<KQ>(sqa, g, y, qscale, lane);
         }
     }
     // rows of the 16-row q operand past the G heads are zero
@@ -195,17 +239,18 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     for (int dt = 0; dt < NDT; ++dt) st.o[dt][0] = st.o[dt][1] = st.o[dt][2] = st.o[dt][3] = 0.f;
 
     for (; b < b1; b += AWARPS) {
-        if (!staged) {
-            const __nv_bfloat16* Kb;
-            if (!block_ptr(b, Kb)) {
-                if (lane == 0) set_status(p.status, Q3_STATUS_BLOCK_RANGE);
-                continue;
-            }
-            stage_block(kt, vt, Kb, Kb + (size_t)p.n_kv * head_elems, lane);
+        if (!staged && !stage(b)) {
+            if (lane == 0) set_status(p.status, Q3_STATUS_BLOCK_RANGE);
+            continue;
         }
         staged = false;
         cp_async_wait_all();
         __syncwarp();
+        if (KQ) {
+            expand_q8(kt, raw, lane);
+            expand_q8(vt, raw + KVQ_TILE, lane);
+            __syncwarp();
+        }
         if (FUSED && b == last_blk) {
             // the new position: its K/V were computed above, not read back
             const int r = pos % KV_BLOCK;
@@ -215,8 +260,8 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
                 *reinterpret_cast<const uint2*>(snew + D + lane * 4);
             __syncwarp();
         }
-        attend_block_tc<NDT>(reinterpret_cast<const uint8_t*>(kt), reinterpret_cast<const uint8_t*>(vt), sqa,
-                             min(KV_BLOCK, ctx - b * KV_BLOCK), 0, lane, st);
+        attend_block_tc<NDT, KQ>(reinterpret_cast<const uint8_t*>(kt), reinterpret_cast<const uint8_t*>(vt), sqa,
+                                 min(KV_BLOCK, ctx - b * KV_BLOCK), 0, lane, st);
         __syncwarp();      // the tile is rewritten by the next block's copies
     }
     cp_async_wait_all();
@@ -328,12 +373,12 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
 }
 
-template <int G, bool FUSED>
+template <int G, bool FUSED, bool KQ>
 cudaError_t launch_g(const Launch& L, const AttnArgs& a)
 {
-    const size_t smem = AttnSmem<G>::total;
+    const size_t smem = AttnSmem<G, KQ>::total;
     static std::atomic<unsigned long long> attr_done{0};
-    if (cudaError_t e = allow_smem_per_device(attn_kernel<G, FUSED>, (int)smem, attr_done)) return e;
+    if (cudaError_t e = allow_smem_per_device(attn_kernel<G, FUSED, KQ>, (int)smem, attr_done)) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.n_splits, a.n_kv, a.T);
     cfg.blockDim = dim3(AWARPS * 32);
@@ -345,21 +390,21 @@ cudaError_t launch_g(const Launch& L, const AttnArgs& a)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (L.counter) ++*L.counter;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<G, FUSED>, a);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<G, FUSED, KQ>, a);
 }
 
-template <bool FUSED>
+template <bool FUSED, bool KQ>
 cudaError_t launch_fused(const Launch& L, const AttnArgs& a)
 {
     switch (a.n_q / a.n_kv) {
-    case 1: return launch_g<1, FUSED>(L, a);
-    case 2: return launch_g<2, FUSED>(L, a);
-    case 3: return launch_g<3, FUSED>(L, a);
-    case 4: return launch_g<4, FUSED>(L, a);
-    case 5: return launch_g<5, FUSED>(L, a);
-    case 6: return launch_g<6, FUSED>(L, a);
-    case 7: return launch_g<7, FUSED>(L, a);
-    case 8: return launch_g<8, FUSED>(L, a);
+    case 1: return launch_g<1, FUSED, KQ>(L, a);
+    case 2: return launch_g<2, FUSED, KQ>(L, a);
+    case 3: return launch_g<3, FUSED, KQ>(L, a);
+    case 4: return launch_g<4, FUSED, KQ>(L, a);
+    case 5: return launch_g<5, FUSED, KQ>(L, a);
+    case 6: return launch_g<6, FUSED, KQ>(L, a);
+    case 7: return launch_g<7, FUSED, KQ>(L, a);
+    case 8: return launch_g<8, FUSED, KQ>(L, a);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -375,7 +420,9 @@ int attention_max_splits() { return 128; }
 
 cudaError_t launch_attention(const Launch& L, const AttnArgs& a, bool fused)
 {
-    return fused ? launch_fused<true>(L, a) : launch_fused<false>(L, a);
+    if (a.kvq_layer)
+        return fused ? launch_fused<true, true>(L, a) : launch_fused<false, true>(L, a);
+    return fused ? launch_fused<true, false>(L, a) : launch_fused<false, false>(L, a);
 }
 
 }  // namespace q3

@@ -17,7 +17,10 @@
 // shared-memory tiles (exact for the ranges of normed, rotated K and of V;
 // fp16 keeps 3 more mantissa bits than bf16 for Q and P).  Shared-memory
 // tiles use an XOR swizzle of 16-byte chunks so ldmatrix reads are
-// conflict-free.  Scores are scaled by log2(e)/sqrt(128) and exponentiated
+// conflict-free.  With the opt-in Q8_0 cache ("Kipp Roadmap", status v0.0.4)
+// the raw Q8_0 tiles (codes and fp16 scales) are copied instead and the
+// conversion writes fp16(scale * code), each product rounded once.
+// Scores are scaled by log2(e)/sqrt(128) and exponentiated
 // in base 2; positions after a query's own position are masked.  Positions a
 // block does not hold read zeros, never stale shared memory.
 #include <algorithm>
@@ -130,6 +133,25 @@ __global__ void __launch_bounds__(HPC * 4 * 32, 1) prefill_attn_kernel(const Pre
     auto issue_kv = [&](int kt, int buf) {
         uint8_t* dstK = bKV + (size_t)buf * 2 * TILE_BYTES;
         uint8_t* dstV = dstK + TILE_BYTES;
+        if (p.kvq_layer) {
+            // raw Q8_0 tiles of the two blocks: block j at j * KVQ_TILE
+            for (int i = tid; i < 2 * (KVQ_TILE / 16); i += NT) {
+                const int j = i / (KVQ_TILE / 16), piece = i % (KVQ_TILE / 16);
+                const int b = 2 * kt + j;
+                if (b >= nblk) continue;
+                const int phys = table[b];
+                if (phys < 0 || phys >= p.n_blocks) {
+                    if (piece == 0) set_status(p.status, Q3_STATUS_BLOCK_RANGE);
+                    continue;
+                }
+                const uint8_t* Kq = p.kvq_layer + ((size_t)phys * 2 * p.n_kv + kvh) * KVQ_TILE;
+                const uint8_t* Vq = Kq + (size_t)p.n_kv * KVQ_TILE;
+                cp_async_16(dstK + j * KVQ_TILE + piece * 16, Kq + piece * 16);
+                cp_async_16(dstV + j * KVQ_TILE + piece * 16, Vq + piece * 16);
+            }
+            cp_async_commit();
+            return;
+        }
         for (int i = tid; i < BN * 16; i += NT) {
             const int r = i >> 4, c = i & 15;
             const int b = 2 * kt + (r >> 5);
@@ -174,7 +196,18 @@ __global__ void __launch_bounds__(HPC * 4 * 32, 1) prefill_attn_kernel(const Pre
                 const int r = i >> 4, c = i & 15;
                 const bool present = 2 * kt + (r >> 5) < nblk;
                 uint4 k = make_uint4(0, 0, 0, 0), v = make_uint4(0, 0, 0, 0);
-                if (present) {
+                if (present && p.kvq_layer) {
+                    // 8 codes of row r at dims 8c.., scale of their 32-dim block c / 4
+                    const int off = (r >> 5) * KVQ_TILE, rr = r & 31;
+                    const uint2 ck = *reinterpret_cast<const uint2*>(srcK + off + rr * 128 + c * 8);
+                    const uint2 cv = *reinterpret_cast<const uint2*>(srcV + off + rr * 128 + c * 8);
+                    const __half dk = *reinterpret_cast<const __half*>(srcK + off + KVQ_CODES + (rr * 4 + c / 4) * 2);
+                    const __half dv = *reinterpret_cast<const __half*>(srcV + off + KVQ_CODES + (rr * 4 + c / 4) * 2);
+                    const uint2 k0 = kvq_dequant4(ck.x, dk), k1 = kvq_dequant4(ck.y, dk);
+                    const uint2 v0 = kvq_dequant4(cv.x, dv), v1 = kvq_dequant4(cv.y, dv);
+                    k = make_uint4(k0.x, k0.y, k1.x, k1.y);
+                    v = make_uint4(v0.x, v0.y, v1.x, v1.y);
+                } else if (present) {
                     k = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(srcK + r * 256 + c * 16));
                     v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(srcV + r * 256 + c * 16));
                 }

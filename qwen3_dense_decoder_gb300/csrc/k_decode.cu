@@ -43,8 +43,7 @@ constexpr int NCW = 16;                    // consumer warps
 constexpr int NCT = NCW * 32;              // consumer threads
 constexpr int PRODUCER = NCW;              // warp index of the producer
 constexpr int EPILOGUE = NCW + 1;          // warp index of the epilogue warp
-constexpr int PREFETCHER = NCW + 2;        // warp index of the L2 prefetch warp
-constexpr int THREADS = NCT + 96;          // + producer, epilogue and prefetch warps
+constexpr int THREADS = NCT + 64;          // + producer and epilogue warps
 constexpr int SLOT = 40 * 1024;            // bytes per ring slot
 constexpr int RED = 64;                    // row partials per slot (rows x warp segments)
 constexpr int D = 128, KVB = 32;
@@ -135,7 +134,6 @@ struct Smem {
     int* bi;            // [NCW]
     volatile int* abort;
     int* ticket;
-    volatile int* prod_it;  // ring tiles the producer has issued (read by the prefetch warp)
     float* xres;        // [MAX_OWN] the CTA's residual rows (epilogue warp only)
     const void** wp;    // [n_layers][14]: the layer's 7 weight planes, then their 7 scale planes
     int n_slots;
@@ -348,7 +346,6 @@ Q3_DEV bool produce_weights(const WStage& s, const Smem& sm, uint32_t& it, int l
         }
         __syncwarp();
         ++it;
-        if (lane == 0) *sm.prod_it = (int)it;
     }
     return true;
 }
@@ -382,7 +379,6 @@ Q3_DEV bool produce_attention(const DecodeArgs& p, int l, const Unit& u, const i
         }
         __syncwarp();
         ++it;
-        if (lane == 0) *sm.prod_it = (int)it;
     }
     return true;
 }
@@ -405,107 +401,6 @@ Q3_DEV void producer(const DecodeArgs& p, const Unit& u, const int* table, const
         for (int s = 0; s < sm.n_slots; ++s)
             if (it > (uint32_t)s) mbar_wait(&sm.full[s], ((it - 1 - s) / sm.n_slots) & 1, p.status);
     }
-}
-
-// ---------------------------------------------------------------- L2 prefetch warp
-// The ring holds a few tiles per SM (about 3.6 us of this SM's share of HBM
-// time).  Consumers stall at every grid barrier and for the whole attention
-// chain, and once the ring is full the producer stalls with them, leaving HBM
-// idle.  This warp walks the same tile sequence as the producer but runs up
-// to pf_tiles tiles ahead of the producer's issue point, asking L2 for each
-// tile's lines (plain per-line prefetches on the load/store path, so the
-// producer's bulk copies never queue behind them).  It does not wait for the
-// consumers, so while they stall HBM keeps filling L2 with the weights they
-// will read next, and the producer's copies of those tiles then come from L2.
-Q3_DEV void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" :: "l"(p)); }
-
-// every 128-byte line of [src, src + bytes), one line per lane
-Q3_DEV void prefetch_range(const void* src, size_t bytes, int lane) {
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~(uintptr_t)127;
-    const uintptr_t a1 = reinterpret_cast<uintptr_t>(src) + bytes;
-    for (uintptr_t a = a0 + (uintptr_t)lane * 128; a < a1; a += 32 * 128)
-        prefetch_l2(reinterpret_cast<const void*>(a));
-}
-
-// Wait until tile i is within the window ahead of the producer; false when
-// the step is aborting or the wait ran out.
-Q3_DEV bool prefetch_window(const Smem& sm, uint32_t i, int window, int lane, int* status) {
-    bool ok = true;
-    if (lane == 0) {
-        const uint64_t t0 = global_ns();
-        while ((int)i >= *sm.prod_it + window) {
-            if (*sm.abort) { ok = false; break; }
-            if (global_ns() - t0 > Q3_WAIT_LIMIT_NS) {
-                set_status(status, Q3_STATUS_TIMEOUT);
-                *sm.abort = 1;
-                ok = false;
-                break;
-            }
-            __nanosleep(128);
-        }
-    }
-    return __shfl_sync(0xffffffffu, ok, 0);
-}
-
-Q3_DEV bool prefetch_weights(const WStage& s, const Smem& sm, uint32_t& it, int window, int lane, int* status) {
-    const size_t qb = s.q8 ? (size_t)s.K : (size_t)s.K * 2;
-    const size_t sb = s.q8 ? (size_t)s.K / 16 : 0;
-    for (int a = s.r0; a < s.r1; a += s.per) {
-        const int b = min(a + s.per, s.r1), n = b - a;
-        if (!prefetch_window(sm, it, window, lane, status)) return false;
-        if (s.pair) {
-            for (int t = 0; t < 2; ++t) {
-                prefetch_range(s.w[t] + (size_t)a * qb, (size_t)n * qb, lane);
-                if (sb) prefetch_range(reinterpret_cast<const uint8_t*>(s.sc[t]) + (size_t)a * sb, (size_t)n * sb, lane);
-            }
-        } else {
-            int r = a, base = 0;
-            for (int t = 0; t < 3 && r < b; ++t) {
-                const int e = min(b, base + s.rows[t]);
-                if (r < e) {
-                    prefetch_range(s.w[t] + (size_t)(r - base) * qb, (size_t)(e - r) * qb, lane);
-                    if (sb)
-                        prefetch_range(reinterpret_cast<const uint8_t*>(s.sc[t]) + (size_t)(r - base) * sb,
-                                       (size_t)(e - r) * sb, lane);
-                    r = e;
-                }
-                base += s.rows[t];
-            }
-        }
-        ++it;
-    }
-    return true;
-}
-
-Q3_DEV bool prefetch_attention(const DecodeArgs& p, int l, const Unit& u, const int* table, const Smem& sm,
-                               uint32_t& it, int window, int lane) {
-    for (int b = u.b0; b < u.b1; b += BLKS_PER_SLOT) {
-        if (!prefetch_window(sm, it, window, lane, p.status)) return false;
-        for (int j = 0; j < BLKS_PER_SLOT && b + j < u.b1; ++j) {
-            const int phys = table[b + j];
-            if (phys < 0 || phys >= p.n_blocks) continue;
-            const bf16* Kb = kv_block(p, l, phys, u.kvh);
-            prefetch_range(Kb, KVB * D * 2, lane);
-            prefetch_range(Kb + (size_t)p.n_kv * KVB * D, KVB * D * 2, lane);
-        }
-        ++it;
-    }
-    return true;
-}
-
-Q3_DEV void prefetcher(const DecodeArgs& p, const Unit& u, const int* table, const Smem& sm, int lane) {
-    const int window = p.pf_tiles;
-    if (window <= 0) return;
-    uint32_t it = 0;
-    bool ok = true;
-    for (int l = 0; l < p.n_layers && ok; ++l) {
-        ok = prefetch_weights(weight_stage(p, sm, l, ST_QKV), sm, it, window, lane, p.status) &&
-             prefetch_attention(p, l, u, table, sm, it, window, lane) &&
-             prefetch_weights(weight_stage(p, sm, l, ST_O), sm, it, window, lane, p.status) &&
-             prefetch_weights(weight_stage(p, sm, l, ST_GU), sm, it, window, lane, p.status) &&
-             prefetch_weights(weight_stage(p, sm, l, ST_DOWN), sm, it, window, lane, p.status);
-    }
-    if (ok) prefetch_weights(weight_stage(p, sm, 0, ST_LM), sm, it, window, lane, p.status);
 }
 
 // ---------------------------------------------------------------- consumers
@@ -1068,7 +963,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
     sm.bi = reinterpret_cast<int*>(sm.bv + NCW);
     sm.abort = reinterpret_cast<volatile int*>(sm.bi + NCW);
     sm.ticket = const_cast<int*>(sm.abort) + 1;
-    sm.prod_it = sm.abort + 2;
     sm.xres = reinterpret_cast<float*>(sm.ticket + 3);
     sm.wp = reinterpret_cast<const void**>(smem + lay.ptrs);
     // the per-layer weight and gain pointers, read on every stage by producer, consumers and epilogue
@@ -1090,7 +984,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
             mbar_init(&sm.redf[s], NCW);
         }
         *sm.abort = 0;
-        *sm.prod_it = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -1100,7 +993,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
     const int* table = p.tables + (size_t)p.row_slot[0] * p.max_blocks;
     if (warp == PRODUCER) producer<Q8>(p, u, table, sm, lane);
     else if (warp == EPILOGUE) epilogue(p, u, sm, lane);
-    else if (warp == PREFETCHER) prefetcher(p, u, table, sm, lane);
     else consumer<Q8>(p, u, table, sm, warp, lane);
 }
 

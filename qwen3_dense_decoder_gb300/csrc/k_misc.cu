@@ -213,6 +213,15 @@ __global__ void __launch_bounds__(128) qk_norm_rope_append_kernel(const RopeArgs
         return;
     }
     const int kvh = is_k ? hh - a.n_q : hh - a.n_q - a.n_kv;
+    if (a.kvq_layer) {
+        uint32_t codes;
+        __half scale;
+        float deq[4];
+        kvq_pack(y, codes, scale, deq);
+        kvq_store(a.kvq_layer + (((size_t)blk * 2 + (is_k ? 0 : 1)) * a.n_kv + kvh) * KVQ_TILE, pos % 32,
+                  codes, scale, lane);
+        return;
+    }
     __nv_bfloat16* dst = a.kv_layer +
         (((size_t)blk * 2 + (is_k ? 0 : 1)) * a.n_kv + kvh) * (32 * D) + (size_t)(pos % 32) * D + lane * 4;
     const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
@@ -454,6 +463,34 @@ cudaError_t launch_qk_norm_rope_append(const Launch& L, const RopeArgs& a)
 {
     const int heads = a.n_q + 2 * a.n_kv;
     return launch_ex(L, qk_norm_rope_append_kernel, dim3(a.T, (heads + 3) / 4), dim3(128), a);
+}
+
+// Q8_0 K/V packing of caller rows (operator gate of the cache writers): one
+// warp per 128-value row, written as 4 canonical blocks of 34 bytes.
+__global__ void __launch_bounds__(128) kv_pack_q8_kernel(const float* rows, int n, uint8_t* out)
+{
+    const int r = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (r >= n) return;
+    const float4 v = *reinterpret_cast<const float4*>(rows + (size_t)r * 128 + lane * 4);
+    const float y[4] = {v.x, v.y, v.z, v.w};
+    uint32_t codes;
+    __half scale;
+    float deq[4];
+    kvq_pack(y, codes, scale, deq);
+    uint8_t* blk = out + (size_t)r * 136 + (lane >> 3) * 34;
+    if ((lane & 7) == 0) {
+        const unsigned short sb = __half_as_ushort(scale);
+        blk[0] = (uint8_t)(sb & 0xff);
+        blk[1] = (uint8_t)(sb >> 8);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) blk[2 + (lane & 7) * 4 + e] = (uint8_t)(codes >> (8 * e));
+}
+
+cudaError_t launch_kv_pack_q8(cudaStream_t s, const float* rows, int n, uint8_t* out)
+{
+    kv_pack_q8_kernel<<<(n + 3) / 4, 128, 0, s>>>(rows, n, out);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_argmax(const Launch& L, const float* logits, int rows, int V, int32_t* out)

@@ -13,6 +13,14 @@
 
 namespace q3 {
 
+// ---------------------------------------------------------------- Q8_0 K/V cache layout
+// With the opt-in Q8_0 cache a (block, K or V, KV head) tile of the pool is
+// KVQ_TILE bytes: the codes [32 positions][128] int8, then the scales
+// [32 positions][4] fp16 (one per 32 values of a head row) -- 136 bytes per
+// position and head against 256 in BF16.
+constexpr int KVQ_CODES = 32 * 128;
+constexpr int KVQ_TILE = KVQ_CODES + 32 * 4 * 2;
+
 // ---------------------------------------------------------------- kernel attributes
 // A kernel that takes more than 48 KB of dynamic shared memory must be
 // allowed it on every device it launches on.  `done` keeps one bit per
@@ -133,6 +141,8 @@ struct RopeArgs {
     const int* tables;         // [slots][max_blocks]
     int max_blocks;
     __nv_bfloat16* kv_layer;   // pool base of this layer: [n_blocks][2][n_kv][32][128]
+    uint8_t* kvq_layer;        // Q8_0 cache: pool base of this layer, [n_blocks][2][n_kv] tiles of
+                               // KVQ_TILE bytes (null: the BF16 cache at kv_layer)
     int64_t layer_stride;      // elements between layers (unused by the kernel)
     int n_blocks;
     float* q_out;              // [T][n_q*128] f32, or null
@@ -155,6 +165,7 @@ struct AttnArgs {
     const int* tables;
     int max_blocks;
     __nv_bfloat16* kv_layer;   // pool slab of this layer; written by the fused append
+    uint8_t* kvq_layer;        // Q8_0 cache: the layer's tiles instead (null: BF16 cache)
     int n_blocks;
     int n_splits;
     float* part_ml;            // [T][n_q][n_splits][2]
@@ -183,6 +194,7 @@ struct PrefillAttnArgs {
     const int* tables;
     int max_blocks;
     const __nv_bfloat16* kv_layer;
+    const uint8_t* kvq_layer;  // Q8_0 cache (mma.sync kernel only): the layer's tiles (null: BF16)
     int n_blocks;
     __half* out;               // [T][n_q * 128] fp16
     int* status;
@@ -249,7 +261,6 @@ struct DecodeArgs {
     unsigned long long* bar;   // grid barrier counter (monotonic across launches)
     unsigned long long bar_base;   // its value when this launch starts
     int n_slots;               // ring depth
-    int pf_tiles;              // L2 prefetch window: tiles ahead of the producer (0: none)
     int* status;
 };
 // Shared memory of the fused step for these dimensions and ring depth; 0 if
@@ -263,6 +274,10 @@ cudaError_t decode_step_prepare(size_t smem);
 cudaError_t launch_decode_step(const Launch& L, const DecodeArgs& a, int grid, size_t smem);
 
 cudaError_t launch_argmax(const Launch& L, const float* logits, int rows, int V, int32_t* out);
+
+// Q8_0 K/V rows: n rows of 128 floats packed into canonical Q8_0 blocks (4 x
+// 34 bytes a row: fp16 scale, then 32 codes), by the cache writers' rule.
+cudaError_t launch_kv_pack_q8(cudaStream_t s, const float* rows, int n, uint8_t* out);
 
 // Q8_0: canonical blocks -> (int8 plane, fp16 scale plane); planes -> fp16
 // tensor-core operand; bf16 -> canonical blocks.

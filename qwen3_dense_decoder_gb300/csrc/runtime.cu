@@ -160,6 +160,7 @@ struct q3_model {
     int* am_counter = nullptr;      // ticket of the argmax merge, zero between rounds
     int* pre_counter = nullptr;     // work queue of the prefill attention, zero between launches
     int n_sm = 0;
+    bool kv_q8 = false;             // the opt-in Q8_0 K/V cache
     bool prefill_tc_ok = false;     // the tcgen05 prefill attention supports these shapes
     bool prefill_tc = true;         // use it when prefill_tc_ok
 
@@ -167,7 +168,6 @@ struct q3_model {
     bool step_ok = false;           // shapes and device support it
     bool fused_decode = true;       // use it when step_ok
     int step_grid = 0, step_slots = 0, step_splits = 0;
-    int step_pf_tiles = 0;      // the fused step's L2 prefetch window (tiles ahead of its producer)
     size_t step_smem = 0;
     DecodeLayer* step_layers = nullptr;       // device [n_layers]
     unsigned long long* step_bar = nullptr;   // grid barrier counter
@@ -276,7 +276,8 @@ struct q3_session;
 struct q3_pool {
     q3_model* m = nullptr;
     int n_blocks = 0, max_sessions = 0, max_blocks = 0;
-    bf16* kv = nullptr;          // [L][n_blocks][2][n_kv][32][128]
+    bf16* kv = nullptr;          // [L][n_blocks][2][n_kv][32][128] bf16, or [L][n_blocks][2][n_kv] Q8_0 tiles
+    size_t block_bytes = 0;      // one block of one layer: K and V of every KV head
     CUtensorMap kv_map;          // kv as rows of 128 (tcgen05 prefill attention)
     int* tables = nullptr;       // [max_sessions][max_blocks]
     std::set<int> free_blocks;   // blocks nobody holds
@@ -399,12 +400,20 @@ int validate_config(const q3_config* c)
         return fail(Q3_ERR_INVALID_ARG, "config: hidden, ffn and vocab must be multiples of 128");
     if (c->scheme != Q3_BF16 && c->scheme != Q3_Q8_0 && c->scheme != Q3_AFFINE4)
         return fail(Q3_ERR_INVALID_ARG, "config: unknown weight scheme %d", c->scheme);
+    if (c->kv_scheme != Q3_BF16 && c->kv_scheme != Q3_Q8_0)
+        return fail(Q3_ERR_INVALID_ARG, "config: unknown K/V cache scheme %d", c->kv_scheme);
     if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f))
         return fail(Q3_ERR_INVALID_ARG, "config: rms_eps and rope_theta must be positive");
     return Q3_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// bytes of one 32-position block of one layer: K and V of every KV head
+size_t kv_block_bytes(const q3_model* m)
+{
+    return (size_t)2 * m->c.n_kv_heads * (m->kv_q8 ? KVQ_TILE : 32 * 128 * 2);
+}
 
 // ---------------------------------------------------------------- the round
 
@@ -601,6 +610,7 @@ int setup_decode_step(q3_model* m, int n_sm)
 {
     const q3_config& c = m->c;
     if (c.scheme == Q3_AFFINE4) return Q3_OK;   // no AFFINE4 consumer in the step
+    if (m->kv_q8) return Q3_OK;                 // the step reads the BF16 cache only
     const bool q8 = c.scheme == Q3_Q8_0;
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -648,10 +658,6 @@ int setup_decode_step(q3_model* m, int n_sm)
         return fail(Q3_ERR_CUDA, "fused decode setup failed");
     m->step_grid = grid;
     m->step_slots = slots;
-    {
-        const char* e = getenv("Q3_DECODE_PF_TILES");
-        m->step_pf_tiles = e ? atoi(e) : 8;
-    }
     m->step_splits = splits;
     m->step_smem = smem;
     m->step_epoch = 0;
@@ -685,7 +691,6 @@ int run_decode_step(q3_model* m, const Round& r)
     a.am_val = m->step_am_val; a.am_idx = m->step_am_idx; a.am_counter = m->am_counter;
     a.bar = m->step_bar; a.bar_base = m->step_epoch;
     a.n_slots = m->step_slots;
-    a.pf_tiles = m->step_pf_tiles;
     a.status = m->status;
     Launch L{m->stream, false, &m->launches};
     m->prof_begin(Q3_K_STEP);
@@ -716,7 +721,8 @@ int run_round(q3_model* m, const Round& r)
         return e;
     };
     if (one && r.ns == 1 && m->step_ok && m->fused_decode) return run_decode_step(m, r);
-    const size_t layer_kv = (size_t)r.pool->n_blocks * 2 * c.n_kv_heads * 32 * 128;
+    const size_t layer_kv = (size_t)r.pool->n_blocks * 2 * c.n_kv_heads * 32 * 128;   // bf16 cache
+    const size_t layer_bytes = (size_t)r.pool->n_blocks * r.pool->block_bytes;
     const int n_splits = attention_splits(m, T, r.max_ctx);
     int rc;
 
@@ -762,6 +768,7 @@ int run_round(q3_model* m, const Round& r)
             ra.row_pos = row_pos; ra.row_slot = row_slot;
             ra.tables = r.pool->tables; ra.max_blocks = r.pool->max_blocks;
             ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
+            ra.kvq_layer = m->kv_q8 ? reinterpret_cast<uint8_t*>(r.pool->kv) + (size_t)l * layer_bytes : nullptr;
             ra.n_blocks = r.pool->n_blocks;
             ra.q_out = nullptr; ra.q_out16 = m->q16; ra.status = m->status;
             if ((rc = m->check(run(Q3_K_ROPE, [&] { return launch_qk_norm_rope_append(L, ra); }),
@@ -780,6 +787,7 @@ int run_round(q3_model* m, const Round& r)
             aa.row_pos = row_pos; aa.row_slot = row_slot;
             aa.tables = r.pool->tables; aa.max_blocks = r.pool->max_blocks;
             aa.kv_layer = r.pool->kv + (size_t)l * layer_kv; aa.n_blocks = r.pool->n_blocks;
+            aa.kvq_layer = m->kv_q8 ? reinterpret_cast<uint8_t*>(r.pool->kv) + (size_t)l * layer_bytes : nullptr;
             aa.n_splits = n_splits;
             aa.part_ml = m->part_ml; aa.part_o = m->part_o;
             aa.counters = m->attn_counters;
@@ -799,6 +807,7 @@ int run_round(q3_model* m, const Round& r)
             pa.n_tiles = r.n_tiles;
             pa.tables = r.pool->tables; pa.max_blocks = r.pool->max_blocks;
             pa.kv_layer = r.pool->kv + (size_t)l * layer_kv; pa.n_blocks = r.pool->n_blocks;
+            pa.kvq_layer = m->kv_q8 ? reinterpret_cast<uint8_t*>(r.pool->kv) + (size_t)l * layer_bytes : nullptr;
             pa.out = m->att;
             pa.work_counter = m->pre_counter;
             pa.sched_start = m->meta + 6 * m->max_rows;
@@ -1138,7 +1147,10 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->layers.assign(w->layers, w->layers + c.n_layers);
     m->pdl = true;
     m->n_sm = std::min(prop.multiProcessorCount, SCHED_GRID);
-    m->prefill_tc_ok = prefill_tc_rows(c.n_q_heads, c.n_kv_heads) > 0 &&
+    m->kv_q8 = c.kv_scheme == Q3_Q8_0;
+    // the tcgen05 prefill attention reads the BF16 cache through a tensor map;
+    // the Q8_0 cache takes the mma.sync kernel
+    m->prefill_tc_ok = !m->kv_q8 && prefill_tc_rows(c.n_q_heads, c.n_kv_heads) > 0 &&
                        prefill_tc_smem() <= (size_t)prop.sharedMemPerBlockOptin;
 
     auto bad = [&](int code, const char* msg) {
@@ -1352,18 +1364,20 @@ int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
     p->n_blocks = n_blocks;
     p->max_sessions = max_sessions;
     p->max_blocks = (m->c.max_ctx + 31) / 32;
-    const size_t kv = (size_t)m->c.n_layers * n_blocks * 2 * m->c.n_kv_heads * 32 * 128;
-    if (cudaMalloc(&p->kv, kv * sizeof(bf16)) != cudaSuccess) {
+    p->block_bytes = kv_block_bytes(m);
+    const size_t kv_bytes = (size_t)m->c.n_layers * n_blocks * p->block_bytes;
+    if (cudaMalloc(&p->kv, kv_bytes) != cudaSuccess) {
         delete p;
-        return fail(Q3_ERR_OOM, "pool: cannot allocate %zu bytes of KV", kv * sizeof(bf16));
+        return fail(Q3_ERR_OOM, "pool: cannot allocate %zu bytes of KV", kv_bytes);
     }
-    if (!tmap_kv(&p->kv_map, p->kv, kv / 128)) {
+    if (!m->kv_q8 && !tmap_kv(&p->kv_map, p->kv, kv_bytes / 256)) {
         cudaFree(p->kv);
         delete p;
         return fail(Q3_ERR_CUDA, "pool: tensor map encoding failed");
     }
     // zeroed once so positions a block has not been written hold finite values
-    if (cudaMemsetAsync(p->kv, 0, kv * sizeof(bf16), m->stream) != cudaSuccess) {
+    // (zero codes and zero scales for the Q8_0 cache)
+    if (cudaMemsetAsync(p->kv, 0, kv_bytes, m->stream) != cudaSuccess) {
         cudaFree(p->kv);
         delete p;
         return fail(Q3_ERR_CUDA, "pool: memset failed");
@@ -1515,11 +1529,12 @@ int q3_session_truncate(q3_session* s, int n_pos)
         q3_model* m = p->m;
         const int b = s->blocks[last], nb = take_block(p);
         if (nb < 0) return fail(Q3_ERR_POOL_EXHAUSTED, "truncate: no block for the copy of a shared block");
-        const size_t blk = (size_t)2 * m->c.n_kv_heads * 32 * 128;      // bf16 values per block and layer
+        const size_t blk = p->block_bytes;
+        uint8_t* base = reinterpret_cast<uint8_t*>(p->kv);
         for (int l = 0; l < m->c.n_layers; ++l) {
-            const int rc = m->check(cudaMemcpyAsync(p->kv + ((size_t)l * p->n_blocks + nb) * blk,
-                                                    p->kv + ((size_t)l * p->n_blocks + b) * blk,
-                                                    blk * sizeof(bf16), cudaMemcpyDeviceToDevice, m->stream),
+            const int rc = m->check(cudaMemcpyAsync(base + ((size_t)l * p->n_blocks + nb) * blk,
+                                                    base + ((size_t)l * p->n_blocks + b) * blk,
+                                                    blk, cudaMemcpyDeviceToDevice, m->stream),
                                     "shared block copy");
             if (rc) return rc;
         }
@@ -1684,6 +1699,21 @@ int q3_model_profile_read(q3_model* m, int cls, double* total_ms, int64_t* launc
     if (m->prof_collect() != Q3_OK) return fail(Q3_ERR_CUDA, "profile: sync failed");
     *total_ms = m->prof_ms[cls];
     *launches = m->prof_n[cls];
+    return Q3_OK;
+}
+
+int q3_model_kv_bytes_per_position(const q3_model* m)
+{
+    return m ? (int)(kv_block_bytes(m) / 32) : -1;
+}
+
+int q3_op_kv_pack_q8_0(const float* rows_dev, int n_rows, void* out_dev, void* stream)
+{
+    if (!rows_dev || !out_dev || n_rows < 1 || !aligned16(rows_dev))
+        return fail(Q3_ERR_INVALID_ARG, "op_kv_pack_q8_0: bad argument");
+    const cudaError_t e = launch_kv_pack_q8(static_cast<cudaStream_t>(stream), rows_dev, n_rows,
+                                            static_cast<uint8_t*>(out_dev));
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "op_kv_pack_q8_0: %s", cudaGetErrorString(e));
     return Q3_OK;
 }
 

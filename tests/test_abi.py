@@ -79,18 +79,19 @@ def test_config_checks_need_no_gpu(libq3):
         assert libq3.q3_model_create(ctypes.byref(cfg), None, 16, None, ctypes.byref(out)) == -1
         assert msg in libq3.q3_last_error()
         assert out.value is None
-    cfg = _Config(2, 1024, 16, 8, 64, 3072, 4096, 64, 1e6, 1e-6, 1, 0)
+    cfg = _Config(2, 1024, 16, 8, 64, 3072, 4096, 64, 1e6, 1e-6, 1, 0, 0)
     assert libq3.q3_model_create(ctypes.byref(cfg), None, 16, None, ctypes.byref(out)) == -1
     assert b"head_dim must be 128" in libq3.q3_last_error()
 
 
-def test_cuda_model_refuses_a_quantized_kv_cache():
-    # the Q8_0 KV cache exists in the oracle only: the binding says so before any CUDA call
-    import synthetic
-    import qwen3_dense_decoder_gb300 as q3
-    shape = synthetic.SHAPES["tiny"].replace(kv_quant=synthetic.Q8_0)
-    with pytest.raises(ValueError, match="Q8_0 KV cache"):
-        q3.Model(shape, {}, max_ctx=64)
+def test_unknown_kv_cache_scheme_is_refused(libq3):
+    # a K/V cache scheme other than BF16 and Q8_0 is refused before any CUDA call
+    libq3.q3_last_error.restype = ctypes.c_char_p
+    from qwen3_dense_decoder_gb300 import _Config
+    out = ctypes.c_void_p()
+    cfg = _Config(2, 1024, 16, 8, 128, 3072, 4096, 64, 1e6, 1e-6, 1, 0, 7)
+    assert libq3.q3_model_create(ctypes.byref(cfg), None, 16, None, ctypes.byref(out)) == -1
+    assert b"K/V cache scheme" in libq3.q3_last_error()
 
 
 def test_product_path_does_not_import_the_oracle():
