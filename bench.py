@@ -67,9 +67,9 @@ def parse():
     ap.add_argument("--no-b32", action="store_true", help="skip the batch-32 decode leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline leg")
     ap.add_argument("--shapes", nargs="*", default=None,
-                    choices=("0.6b", "8b-q8_0", "14b", "4b-affine4"),
+                    choices=("0.6b", "8b-q8_0", "14b", "4b-affine4", "14b-kvq8"),
                     help="measure the other named shapes instead (one JSON line each; 0.6b, 8b-q8_0 "
-                         "and 14b if none given)")
+                         "and 14b if none given; 14b-kvq8 is the 14B workload over the Q8_0 K/V cache)")
     ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill", "attn-decode-b32"),
                     default=None,
                     help="run only a small case sized for an ncu capture (a few GB on the device) and exit")
@@ -226,9 +226,16 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self) -> dict:
+        return clock_summary(getattr(self, "lines", []))
+
+
+def clock_summary(lines) -> dict:
+    """Median SM clock, the largest max clock and the throttle reasons seen
+    in nvidia-smi sample lines (the CLOCK_FIELDS columns)."""
+    if True:
         mhz, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for l in getattr(self, "lines", []):
+        for l in lines:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -490,11 +497,13 @@ def affine4_bytes(params: int) -> float:
 def step_bytes(s, ctxs) -> float:
     """HBM bytes of one decode step: every projection once (bf16, Q8_0 blocks
     or AFFINE4 groups: the format's bytes, whatever copy the kernels read), the
-    lm_head once (bf16), and the K/V of every cached position of every session."""
+    lm_head once (bf16), and the K/V of every cached position of every session
+    (2 bytes a value in BF16, 34 bytes per 32 values with the Q8_0 cache)."""
     p = proj_params(s)
     pw = {1: q8_bytes(p), 2: affine4_bytes(p)}.get(s.scheme, 2.0 * p)
     w = pw + 2.0 * s.vocab * s.hidden
-    return w + s.n_layers * 2 * s.kv_width * 2 * float(sum(ctxs))
+    kv_b = 34.0 / 32.0 if getattr(s, "kv_quant", 0) == 1 else 2.0
+    return w + s.n_layers * 2 * s.kv_width * kv_b * float(sum(ctxs))
 
 
 def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
@@ -505,13 +514,15 @@ def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
     AFFINE4_GS32, the scheme of "Kipp Roadmap", status v0.0.4's 2,048-token
     prefill figures); 14B -- a 12,800-token
     prefill in 2,048-token chunks, then 8 sessions decoding 128 tokens at a
-    16,384-token context over one shared block pool with permuted tables."""
+    16,384-token context over one shared block pool with permuted tables
+    (14b-kvq8: the same over the opt-in Q8_0 K/V cache)."""
     import numpy as np
     import torch
 
     import qwen3_dense_decoder_gb300 as q3
     import synthetic
-    s = synthetic.SHAPES[name]
+    s = synthetic.SHAPES["14b"].replace(kv_quant=synthetic.Q8_0, name="qwen3-14b-kv-q8_0") \
+        if name == "14b-kvq8" else synthetic.SHAPES[name]
     st = torch.cuda.Stream()
     torch.cuda.set_stream(st)
     w = synthetic.make_weights(s, seed=1234, device="cuda")     # bf16 source (the oracle packs its own)
@@ -524,17 +535,23 @@ def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
                 lw[nm] = pack(lw[nm])
     V = s.vocab
 
+    clock_lines = []      # nvidia-smi samples taken during every timed region of the shape
+
     def timed(fn):
         a, b = torch.cuda.Event(True), torch.cuda.Event(True)
         torch.cuda.synchronize()
-        a.record(st)
-        fn()
-        b.record(st)
-        b.synchronize()
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            a.record(st)
+            fn()
+            b.record(st)
+            b.synchronize()
+        clock_lines.extend(clk.lines)
         return a.elapsed_time(b)
 
     dtype = {synthetic.BF16: "bf16", synthetic.Q8_0: "q8_0 weights, fp16/bf16 compute",
              synthetic.AFFINE4: "affine4_gs32 weights, fp16/bf16 compute"}[s.scheme]
+    if getattr(s, "kv_quant", synthetic.BF16) == synthetic.Q8_0:
+        dtype += "; q8_0 K/V cache"
     out = {"shape": s.name, "n_gpus": 1, "dtype": dtype,
            "data": "synthetic (seeded random-init weights and tokens)", "peak_kind": pk_kind}
     lg = torch.empty(max(32, 8), V, dtype=torch.float32, device="cuda")
@@ -649,6 +666,7 @@ def run_shape(name: str, pk: dict, pk_kind: str, with_oracle: bool) -> dict:
         for x in ss:
             x.close()
     m.sync()
+    out["clocks"] = clock_summary(clock_lines)
     out["gpu_launches_total"] = m.launch_count
     del m
     torch.cuda.synchronize()
