@@ -67,6 +67,34 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     return LIB
 
 
+FAULT_LIB = os.path.join(BUILD, "faults", "libq3_faults.so")
+
+
+def build_fault_variant(force: bool = False) -> str:
+    """The test build of the mutation gate: runtime.cu compiled with
+    -DQ3_TEST_FAULTS (the host then plants the addressing fault named by the
+    Q3_FAULT environment variable in what it uploads) and linked with the
+    product's kernel objects into a separate library.  Never the product."""
+    build()
+    out_dir = os.path.dirname(FAULT_LIB)
+    obj = os.path.join(out_dir, "runtime.o")
+    src = os.path.join(CSRC, "runtime.cu")
+    if not force and os.path.exists(FAULT_LIB) and os.path.getmtime(FAULT_LIB) >= os.path.getmtime(LIB):
+        return FAULT_LIB
+    os.makedirs(out_dir, exist_ok=True)
+    cc = nvcc()
+    r = subprocess.run([cc, *ARCH, *FLAGS, "-DQ3_TEST_FAULTS", "-c", src, "-o", obj], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on runtime.cu (fault build):\n{r.stdout}\n{r.stderr}")
+    objs = [obj] + [os.path.join(BUILD, f.replace(".cu", ".o")) for f in SOURCES if f != "runtime.cu"]
+    tmp = FAULT_LIB + f".tmp{os.getpid()}"
+    r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed (fault build):\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, FAULT_LIB)
+    return FAULT_LIB
+
+
 if __name__ == "__main__":
     v = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas" in sys.argv else None

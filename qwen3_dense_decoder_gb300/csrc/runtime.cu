@@ -18,6 +18,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -151,6 +152,10 @@ struct q3_model {
     std::vector<std::vector<f16*>> w16;   // [layer][proj] fp16 copies for the tensor cores
                                           // (of the BF16 weights, or the dequantised Q8_0 planes)
     f16* lm16 = nullptr;      // fp16 copy of the lm_head for batched rows
+#ifdef Q3_TEST_FAULTS
+    int fault = 0;            // the planted addressing fault of a test build (Q3_FAULT)
+    int* fault_pos = nullptr; // fault 2: the writers' row positions
+#endif
     int* meta = nullptr;      // [6][max_rows]: row_pos, row_slot, last_row, tile_row0, tile_rows, row_order,
                               // then the tcgen05 attention schedule: [SCHED_GRID + 1] starts, items
     f16* q16 = nullptr;       // [rows_alloc][qw] fp16 q of prefill rounds
@@ -280,6 +285,9 @@ struct q3_pool {
     size_t block_bytes = 0;      // one block of one layer: K and V of every KV head
     CUtensorMap kv_map;          // kv as rows of 128 (tcgen05 prefill attention)
     int* tables = nullptr;       // [max_sessions][max_blocks]
+#ifdef Q3_TEST_FAULTS
+    int* fault_tables = nullptr; // faults 1, 3 (readers) and 4 (writers): the perturbed tables
+#endif
     std::set<int> free_blocks;   // blocks nobody holds
     std::vector<int> holders;    // per block: sessions holding it, +1 while published
     std::vector<char> slot_used;
@@ -611,6 +619,9 @@ int setup_decode_step(q3_model* m, int n_sm)
     const q3_config& c = m->c;
     if (c.scheme == Q3_AFFINE4) return Q3_OK;   // no AFFINE4 consumer in the step
     if (m->kv_q8) return Q3_OK;                 // the step reads the BF16 cache only
+#ifdef Q3_TEST_FAULTS
+    if (m->fault) return Q3_OK;                 // planted faults reach the per-operation kernels only
+#endif
     const bool q8 = c.scheme == Q3_Q8_0;
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -767,6 +778,10 @@ int run_round(q3_model* m, const Round& r)
             ra.eps = c.rms_eps; ra.rope = m->rope;
             ra.row_pos = row_pos; ra.row_slot = row_slot;
             ra.tables = r.pool->tables; ra.max_blocks = r.pool->max_blocks;
+#ifdef Q3_TEST_FAULTS
+            if (m->fault_pos) ra.row_pos = m->fault_pos;
+            if (m->fault == 4) ra.tables = r.pool->fault_tables;
+#endif
             ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
             ra.kvq_layer = m->kv_q8 ? reinterpret_cast<uint8_t*>(r.pool->kv) + (size_t)l * layer_bytes : nullptr;
             ra.n_blocks = r.pool->n_blocks;
@@ -806,6 +821,9 @@ int run_round(q3_model* m, const Round& r)
             pa.tile_rows = m->meta + 4 * m->max_rows;
             pa.n_tiles = r.n_tiles;
             pa.tables = r.pool->tables; pa.max_blocks = r.pool->max_blocks;
+#ifdef Q3_TEST_FAULTS
+            if (m->fault == 1 || m->fault == 3) pa.tables = r.pool->fault_tables;
+#endif
             pa.kv_layer = r.pool->kv + (size_t)l * layer_kv; pa.n_blocks = r.pool->n_blocks;
             pa.kvq_layer = m->kv_q8 ? reinterpret_cast<uint8_t*>(r.pool->kv) + (size_t)l * layer_bytes : nullptr;
             pa.out = m->att;
@@ -926,6 +944,21 @@ int upload_table(q3_session* s)
     for (int i = 0; i < cnt; ++i) h[i] = s->blocks[s->uploaded + i];
     int rc = m->check(m->stage_copy(slot, p->tables + (size_t)s->slot * p->max_blocks + s->uploaded,
                                     sizeof(int32_t) * cnt), "table upload");
+#ifdef Q3_TEST_FAULTS
+    // the whole perturbed table of the session; every id stays inside the pool
+    if (rc == Q3_OK && p->fault_tables) {
+        int fslot;
+        int32_t* f = reinterpret_cast<int32_t*>(m->stage_acquire(&fslot));
+        for (int i = 0; i < n; ++i) {
+            const int b = s->blocks[i];
+            f[i] = m->fault == 1 ? i % p->n_blocks                                  // readers ignore the table
+                 : m->fault == 3 ? ((b ^ 1) < p->n_blocks ? (b ^ 1) : b)           // readers: a wrong id
+                 : (i > 0 ? s->blocks[i - 1] : b);                                 // writers roll back one block
+        }
+        rc = m->check(m->stage_copy(fslot, p->fault_tables + (size_t)s->slot * p->max_blocks,
+                                    sizeof(int32_t) * n), "fault table upload");
+    }
+#endif
     if (rc == Q3_OK) s->uploaded = n;
     return rc;
 }
@@ -1041,6 +1074,15 @@ int eval_round(q3_session* const* S, int ns, const int32_t* tokens, const int* n
     r.decode = (r.T == ns);
     if ((rc = m->check(m->stage_copy(slot, m->meta, sizeof(int32_t) * meta_ints), "meta upload")))
         return rc;
+#ifdef Q3_TEST_FAULTS
+    if (m->fault_pos) {                  // the writers see every row one position later
+        int fslot;
+        int32_t* f = reinterpret_cast<int32_t*>(m->stage_acquire(&fslot));
+        for (int i = 0; i < t; ++i) f[i] = h[i] + 1;
+        if ((rc = m->check(m->stage_copy(fslot, m->fault_pos, sizeof(int32_t) * t), "fault meta upload")))
+            return rc;
+    }
+#endif
     if ((rc = run_round(m, r))) {
         m->poisoned = true;
         return rc;
@@ -1075,6 +1117,9 @@ void pool_release(q3_pool* p)
     cudaStreamSynchronize(p->m->stream);
     cudaFree(p->kv);
     cudaFree(p->tables);
+#ifdef Q3_TEST_FAULTS
+    cudaFree(p->fault_tables);
+#endif
     q3_model* m = p->m;
     delete p;
     model_release(m);
@@ -1198,6 +1243,14 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->ws_elems = (size_t)32 << 20;
     m->ws = static_cast<float*>(A(sizeof(float) * m->ws_elems));
     m->meta = static_cast<int*>(A(sizeof(int) * meta_capacity(m)));
+#ifdef Q3_TEST_FAULTS
+    // a test build plants one addressing fault in what the host uploads
+    // (prefill rounds only: the writer is the q/k-norm/RoPE/append kernel and
+    // the reader the prefill attention); one-session decode keeps the fused
+    // step off so that no kernel outside those two sees the fault
+    if (const char* f = getenv("Q3_FAULT")) m->fault = atoi(f);
+    if (m->fault == 2) m->fault_pos = static_cast<int*>(A(sizeof(int) * (size_t)m->max_rows));
+#endif
     m->q16 = static_cast<f16*>(A(sizeof(f16) * R * m->qw));
     m->attn_counters = static_cast<int*>(A(sizeof(int) * (size_t)m->max_rows * c.n_kv_heads));
     m->am_val = static_cast<float*>(A(sizeof(float) * gemv_max_grid()));
@@ -1394,6 +1447,19 @@ int q3_pool_create(q3_model* m, int n_blocks, int max_sessions, q3_pool** out)
         delete p;
         return fail(Q3_ERR_CUDA, "pool: memset failed");
     }
+#ifdef Q3_TEST_FAULTS
+    if (m->fault == 1 || m->fault == 3 || m->fault == 4) {
+        const size_t tb = sizeof(int) * (size_t)max_sessions * p->max_blocks;
+        if (cudaMalloc(&p->fault_tables, tb) != cudaSuccess ||
+            cudaMemsetAsync(p->fault_tables, 0xff, tb, m->stream) != cudaSuccess) {
+            cudaFree(p->fault_tables);
+            cudaFree(p->kv);
+            cudaFree(p->tables);
+            delete p;
+            return fail(Q3_ERR_OOM, "pool: fault tables");
+        }
+    }
+#endif
     for (int b = 0; b < n_blocks; ++b) p->free_blocks.insert(p->free_blocks.end(), b);
     p->holders.assign(n_blocks, 0);
     p->slot_used.assign(max_sessions, 0);
