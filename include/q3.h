@@ -134,11 +134,13 @@ typedef struct q3_weights {
  * an fp16 copy of the BF16 projections and lm_head (exact except for
  * |w| < 2^-17, whose rounding is below 2^-25), or of the Q8_0 projections
  * dequantised once (d * q rounded to fp16; 2 bytes per weight of device
- * memory beside the 1.0625 of the planes).  With Q3_AFFINE4 every round,
- * batch-1 decode included, runs its projections on the tensor cores over an
- * fp16 copy of the dequantised groups (scale * code + bias rounded to FP32,
- * then to fp16, as q3_affine4_to_f16 writes it); the fused decode step and
- * the batch-1 GEMV take BF16 and Q8_0 only.  Weights beyond the fp16 range make creation fail with
+ * memory beside the 1.0625 of the planes).  With Q3_AFFINE4, rounds of more
+ * than one token run their projections on the tensor cores over an fp16 copy
+ * of the dequantised groups (scale * code + bias rounded to FP32, then to
+ * fp16, as q3_affine4_to_f16 writes it), and one-token rounds on a 5.0-bit
+ * matvec over lane-major planes derived here from the groups (the format's
+ * bytes rearranged; see q3_op_matvec_affine4); the fused decode step takes
+ * BF16 and Q8_0 only.  Weights beyond the fp16 range make creation fail with
  * Q3_ERR_INVALID_ARG; an activation beyond it is reported by q3_sync as
  * Q3_ERR_DEVICE_CHECK (Q3_STATUS_F16_RANGE).  max_round_tokens bounds the rows of one round (the activation
  * scratch, owned by the model, is sized for it; longer q3_session_eval rounds
@@ -328,6 +330,18 @@ int q3_op_gemm(const void* w_dev, const void* w2_dev, const void* x_dev, int M, 
  * Errors: Q3_ERR_INVALID_ARG, Q3_ERR_CUDA. */
 int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, int M, int K,
                  float* y_dev, void* stream);
+
+/* q3_op_matvec_affine4: y[m] = sum_k w[m][k] * x[k] on the 5.0-bit matvec
+ * of one-token rounds over AFFINE4_GS32 weights ("Kipp Model Support",
+ * section "Quantization (AFFINE4_GS32)"), with w[m][k] = scale * code + bias
+ * of its group.  groups_dev: canonical 20-byte groups [M][K/32], 4-byte
+ * aligned (as q3_quantize_affine4 writes them); x_dev: f32 [K]; y_dev: f32
+ * [M].  M a multiple of 8, K of 128 (at most 32,768).  The call derives the
+ * matvec's lane-major planes (allocated and freed here) and returns once the
+ * kernel has finished.  Errors: Q3_ERR_INVALID_ARG, Q3_ERR_OOM, Q3_ERR_CUDA,
+ * Q3_ERR_DEVICE_CHECK (an activation beyond the fp16 range). */
+int q3_op_matvec_affine4(const void* groups_dev, const float* x_dev, int M, int K, float* y_dev,
+                         void* stream);
 
 /* q3_op_prefill_attention: the causal GQA attention of one session's
  * prefill round over its paged K/V ("Kipp Roadmap", status v0.0.3:

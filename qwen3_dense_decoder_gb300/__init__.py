@@ -103,6 +103,7 @@ def lib():
         L.q3_model_set_prefill_tc.argtypes = [vp, i]
         L.q3_model_kv_bytes_per_position.argtypes = [vp]
         L.q3_op_kv_pack_q8_0.argtypes = [vp, i, vp, vp]
+        L.q3_op_matvec_affine4.argtypes = [vp, vp, i, i, vp, vp]
         L.q3_model_prefill_tc.argtypes = [vp]
         _lib = L
     return _lib
@@ -243,6 +244,19 @@ def op_matvec(w: torch.Tensor, x: torch.Tensor, scales: torch.Tensor | None = No
     y = torch.empty(M, dtype=torch.float32, device=w.device)
     _check(lib().q3_op_matvec(_ptr(w), _ptr(scales), _ptr(x), M, K, _ptr(y),
                               _stream_handle(stream)))
+    return y
+
+
+def op_matvec_affine4(groups: torch.Tensor, x: torch.Tensor, M: int, K: int, stream=None) -> torch.Tensor:
+    """y[m] = sum_k w[m][k] x[k] on the 5.0-bit AFFINE4 matvec (operator gate):
+    groups uint8 [M, K/32*20] (q3_quantize_affine4's format), x f32 [K].
+    Synchronous."""
+    if groups.dtype != torch.uint8 or groups.numel() != M * K // 32 * AFFINE4_BYTES or not groups.is_contiguous():
+        raise ValueError("op_matvec_affine4: groups must be contiguous uint8 [M, K/32*20]")
+    if x.dtype != torch.float32 or x.numel() != K or not x.is_contiguous():
+        raise ValueError("op_matvec_affine4: x must be contiguous float32 [K]")
+    y = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(lib().q3_op_matvec_affine4(_ptr(groups), _ptr(x), M, K, _ptr(y), _stream_handle(stream)))
     return y
 
 

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libq3.so")
 
 SOURCES = ["runtime.cu", "k_gemm.cu", "k_gemv.cu", "k_attn.cu", "k_attn_prefill.cu", "k_misc.cu",
-           "noalloc.cu", "k_decode.cu", "k_attn_tc.cu"]
+           "noalloc.cu", "k_decode.cu", "k_attn_tc.cu", "k_gemv_a4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

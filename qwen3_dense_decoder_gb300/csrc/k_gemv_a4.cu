@@ -1,0 +1,367 @@
+// k_gemv_a4.cu -- one-token matvec over AFFINE4_GS32 weights at 5.0 bits a
+// weight ("Kipp Model Support", section "Quantization (AFFINE4_GS32)": 32
+// weights a group, 4-bit codes, an fp16 scale and an fp16 bias; "Kipp
+// Roadmap", "Delivered since": dedicated affine4 decode paths).
+//
+// A decode step streams every weight once, so the kernel reads the format's
+// bytes and nothing more: 16 bytes of codes and 4 bytes of (scale, bias) per
+// group.  The work per weight must stay below the SM's issue budget (about
+// 34 weights per SM cycle at the HBM rate), which CUDA-core FMAs with a
+// per-nibble conversion do not (about 4 instructions a weight).  So the
+// products run on mma.sync m16n8k16 (fp16 in, FP32 accumulate):
+//  - B (16 x 8) is eight weight rows by 16 codes: a lane's four fp16 pairs
+//    come from one 32-bit word of the derived code plane, two nibbles a pair
+//    ((w >> 4j) & 0x000F000F | 0x64006400 is the fp16 pair 1024 + q, and one
+//    HSUB2 leaves q exactly);
+//  - A (16 x 16) holds the activation's fp16 high part in row 0 and its
+//    remainder in row 1 (rows 2..15 zero), so the two rows of D add up to
+//    sum q x to about 22 bits;
+//  - each group's D is taken alone and scaled: y += s * sum(q x) + b * sum(x),
+//    with sum(x) over the group formed once per CTA.
+// The derived planes (built once at model creation from the 20-byte groups)
+// are lane-major so every load is a coalesced 16-byte vector:
+//  - codes: [rows / 8][K / 128][32 lanes][4 groups] 32-bit words; lane
+//    (n = lane / 4, t = lane % 4) holds row n's codes at k = 2t, 2t + 1,
+//    2t + 8, 2t + 9, 16 + 2t, 17 + 2t, 24 + 2t, 25 + 2t of the group: fp16
+//    pair j low halves in bits 4j .. 4j + 3, high halves in bits 16 + 4j ..;
+//  - (scale, bias): [rows / 8][K / 128][4 lanes t][4 groups][rows 2t, 2t + 1]
+//    fp16 pairs, the rows whose outputs lane t of the D fragment holds; a
+//    block's 32 words are loaded one per lane and passed to lanes 0..3 by
+//    shuffles when their group is reduced.
+// Rows of one output are split over S warps of a CTA and summed in warp
+// order; epilogues as the BF16 matvec (store, residual add, SwiGLU pairs).
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q3 {
+
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
+constexpr int CTAS_PER_SM = 3;      // 85 registers a thread: the two block buffers without spills
+constexpr int BPL = 4;              // 4-group blocks a warp keeps in flight
+
+Q3_DEV float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+Q3_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+
+Q3_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    // rows 8..15 of A are zero (a1 = a3 = 0)
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                 "{%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// fp16 pair j of a code word: (q_lo, q_hi) exactly
+Q3_DEV uint32_t code_pair(uint32_t w, int j) {
+    const uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), __half2half2(__ushort_as_half(0x6400)));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// A unit is one 8-row tile of one tensor; tile index -> (tensor, row tile)
+struct A4Tile {
+    const uint4* codes;     // the tile's code blocks [K/128][32 lanes] uint4
+    const uint32_t* sb;     // the tile's (scale, bias) blocks [K/128][32 words]
+};
+
+Q3_DEV A4Tile locate_a4(const GemvArgs& p, int tile) {
+    int t = 0;
+    if (p.pair) {
+        t = tile & 1;
+        tile >>= 1;
+    } else {
+        if (tile >= p.rows[0] / 8) { tile -= p.rows[0] / 8; t = 1; }
+        if (t == 1 && tile >= p.rows[1] / 8) { tile -= p.rows[1] / 8; t = 2; }
+    }
+    const size_t nb = (size_t)p.K / 128;
+    A4Tile a;
+    a.codes = static_cast<const uint4*>(p.w[t]) + (size_t)tile * nb * 32;
+    a.sb = reinterpret_cast<const uint32_t*>(p.scales[t]) + (size_t)tile * nb * 32;
+    return a;
+}
+
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_a4_kernel(const GemvArgs p)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int G = p.K / 32;
+    uint2* xf = reinterpret_cast<uint2*>(smem);                       // [G][2 ksteps][2 hi/lo][4 t]
+    float* gsum = reinterpret_cast<float*>(xf + (size_t)G * 16);      // [G] sum of x over each group
+    float* red = gsum + G;                                            // [WARPS][8] row partials
+    __shared__ float s_scale;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.warps_per_row;
+    const int R = WARPS / S;                     // tiles per unit
+    const int slot = warp / S, seg = warp % S;
+    const int n_tiles = p.pair ? 2 * (p.rows[0] / 8)
+                               : (p.rows[0] + (p.n_tensors > 1 ? p.rows[1] : 0) +
+                                  (p.n_tensors > 2 ? p.rows[2] : 0)) / 8;
+    const int n_units = n_tiles / R;
+    const int nb = p.K / 128;
+    const int b0 = seg * nb / S, b1 = (seg + 1) * nb / S;
+    const int t = lane & 3;
+    const bool out_lane = lane < 4;              // lanes 0..3: rows 2t, 2t + 1 of the tile
+
+    // the first blocks of the weight stream go out before the dependency wait
+    int unit = blockIdx.x;
+    uint4 cw[BPL];
+    uint32_t sbw[BPL];
+    auto issue = [&](const A4Tile& a, int blk0) {
+#pragma unroll
+        for (int u = 0; u < BPL; ++u) {
+            const int b = blk0 + u;
+            if (b < b1) {
+                cw[u] = ldg_nc_v4(a.codes + (size_t)b * 32 + lane);
+                sbw[u] = __ldg(a.sb + (size_t)b * 32 + lane);
+            }
+        }
+    };
+    A4Tile cur{};
+    if (unit < n_units) {
+        cur = locate_a4(p, unit * R + slot);
+        issue(cur, b0);
+    }
+    if (threadIdx.x == 0) issue_l2_prefetch(p.next, blockIdx.x, gridDim.x);
+    grid_dep_wait();
+
+    // the activation (RMS-normalised when a gain is given) goes straight from
+    // L2 into its fp16 high/low fragments and the per-group sums
+    float scl = 1.0f;
+    if (p.norm_gain) {
+        float ss = 0.f;
+        for (int i = threadIdx.x * 4; i < p.K; i += THREADS * 4) {
+            const float4 x = *reinterpret_cast<const float4*>(p.x + i);
+            ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.f;
+            for (int w = 0; w < WARPS; ++w) tot += red[w];
+            s_scale = 1.0f / sqrtf(tot / (float)p.K + p.eps);
+        }
+        __syncthreads();
+        scl = s_scale;
+    }
+    auto xval = [&](int k) {
+        const float x = p.x[k];
+        return p.norm_gain ? x * scl * __bfloat162float(p.norm_gain[k]) : x;
+    };
+    // fragment (g, kstep j, part hl, t): the part's values at k = 32 g + 16 j + {2t, 2t+1} and {+8, +9}
+    bool bad = false;
+    for (int i = threadIdx.x; i < G * 16; i += THREADS) {
+        const int g = i >> 4, j = (i >> 3) & 1, hl = (i >> 2) & 1, tt = i & 3;
+        const int k0 = g * 32 + j * 16 + 2 * tt;
+        const float v[4] = {xval(k0), xval(k0 + 1), xval(k0 + 8), xval(k0 + 9)};
+        uint32_t w[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float a = v[2 * e], b = v[2 * e + 1];
+            bad |= fabsf(a) > 65504.f || fabsf(b) > 65504.f;      // the fp16 high part would overflow
+            const __half2 hi = __floats2half2_rn(a, b);
+            if (hl) {
+                const float2 hf = __half22float2(hi);
+                const __half2 lo = __floats2half2_rn(a - hf.x, b - hf.y);
+                w[e] = *reinterpret_cast<const uint32_t*>(&lo);
+            } else {
+                w[e] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
+        }
+        xf[i] = make_uint2(w[0], w[1]);
+    }
+    if (bad) set_status(p.status, Q3_STATUS_F16_RANGE);
+    for (int g = threadIdx.x; g < G; g += THREADS) {
+        float sx = 0.f;
+        for (int k = 0; k < 32; ++k) sx += xval(g * 32 + k);
+        gsum[g] = sx;
+    }
+    __syncthreads();
+
+    const int hl = lane >> 2;                    // A row of this lane: 0 high part, 1 remainder
+    for (; unit < n_units; unit += gridDim.x) {
+        float acc0 = 0.f, acc1 = 0.f;            // rows 2t and 2t + 1 (lanes 0..3)
+        for (int blk0 = b0; blk0 < b1; blk0 += BPL) {
+            uint4 c[BPL];
+            uint32_t sbv[BPL];
+#pragma unroll
+            for (int u = 0; u < BPL; ++u) { c[u] = cw[u]; sbv[u] = sbw[u]; }
+            // the next blocks of this tile (or the next unit's first) go out now
+            if (blk0 + BPL < b1) {
+                issue(cur, blk0 + BPL);
+            } else if (unit + (int)gridDim.x < n_units) {
+                cur = locate_a4(p, (unit + gridDim.x) * R + slot);
+                issue(cur, b0);
+            }
+#pragma unroll
+            for (int u = 0; u < BPL; ++u) {
+                const int b = blk0 + u;
+                if (b >= b1) break;
+                const uint32_t wq[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int g = b * 4 + q;
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        uint2 a = make_uint2(0u, 0u);
+                        if (lane < 8) a = xf[((g * 2 + j) * 2 + hl) * 4 + t];
+                        mma_f16(d, a.x, a.y, code_pair(wq[q], 2 * j), code_pair(wq[q], 2 * j + 1));
+                    }
+                    // rows 0 and 1 of D: high-part and remainder products of rows 2t, 2t + 1
+                    const float r0 = d[0] + __shfl_xor_sync(0xffffffffu, d[0], 4);
+                    const float r1 = d[1] + __shfl_xor_sync(0xffffffffu, d[1], 4);
+                    // (scale, bias) of rows 2t, 2t + 1 in group q: words 8t + 2q (+1) of the block
+                    const uint32_t sbq0 = __shfl_sync(0xffffffffu, sbv[u], 8 * t + 2 * q);
+                    const uint32_t sbq1 = __shfl_sync(0xffffffffu, sbv[u], 8 * t + 2 * q + 1);
+                    if (out_lane) {
+                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&sbq0));
+                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&sbq1));
+                        const float sx = gsum[g];
+                        acc0 = fmaf(f0.x, r0, fmaf(f0.y, sx, acc0));
+                        acc1 = fmaf(f1.x, r1, fmaf(f1.y, sx, acc1));
+                    }
+                }
+            }
+        }
+        // rows of the tile: lane t holds rows 2t, 2t + 1; warps of a tile sum in order
+        if (out_lane) {
+            red[warp * 8 + 2 * t] = acc0;
+            red[warp * 8 + 2 * t + 1] = acc1;
+        }
+        __syncthreads();
+        const int tile0 = unit * R;
+        if (p.pair) {
+            // slots 2i (gate) and 2i + 1 (up) cover rows tile (unit R / 2 + i) of each
+            for (int i = threadIdx.x; i < (R / 2) * 8; i += THREADS) {
+                const int pr = i >> 3, r = i & 7;
+                float g = 0.f, u = 0.f;
+                for (int s2 = 0; s2 < S; ++s2) {
+                    g += red[((2 * pr) * S + s2) * 8 + r];
+                    u += red[((2 * pr + 1) * S + s2) * 8 + r];
+                }
+                p.out[((tile0 >> 1) + pr) * 8 + r] = silu(g) * u;
+            }
+        } else {
+            for (int i = threadIdx.x; i < R * 8; i += THREADS) {
+                const int sl = i >> 3, r = i & 7;
+                float a = 0.f;
+                for (int s2 = 0; s2 < S; ++s2) a += red[(sl * S + s2) * 8 + r];
+                const int row = (tile0 + sl) * 8 + r;
+                if (p.epi == EPI_ADD_F32) p.out[row] += a;
+                else p.out[row] = a;
+            }
+        }
+        __syncthreads();
+    }
+    grid_dep_launch();
+}
+
+size_t gemv_a4_smem(int K)
+{
+    const int G = K / 32;
+    return (size_t)G * 16 * 8 + (size_t)G * 4 + WARPS * 8 * 4;
+}
+
+// Derived planes from canonical 20-byte groups [rows][K/32] (16 code bytes:
+// weight 2i in the low nibble of byte i, 2i + 1 in the high nibble; then
+// the fp16 scale and bias).  One thread per (tile, 4-group block, lane).
+__global__ void a4_planes_kernel(const uint8_t* groups, int rows, int K, uint4* codes, uint32_t* sb)
+{
+    const int nb = K / 128, G = K / 32;
+    const size_t total = (size_t)(rows / 8) * nb * 32;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int lane = (int)(i & 31);
+        const size_t tb = i >> 5;                 // tile * nb + block
+        const int blk = (int)(tb % nb);
+        const size_t tile = tb / nb;
+        const int n = lane >> 2, t = lane & 3;
+        const int row = (int)(tile * 8) + n;
+        uint32_t out[4];
+        for (int q = 0; q < 4; ++q) {
+            const uint8_t* rec = groups + ((size_t)row * G + blk * 4 + q) * 20;
+            // fp16 pair j of the word: (k_lo, k_hi) = (2t, 2t+1), (2t+8, 2t+9), (16+2t, 17+2t), (24+2t, 25+2t)
+            const int klo[4] = {2 * t, 2 * t + 8, 16 + 2 * t, 24 + 2 * t};
+            uint32_t w = 0;
+            for (int j = 0; j < 4; ++j) {
+                const int k0 = klo[j], k1 = klo[j] + 1;
+                const uint32_t c0 = (rec[k0 >> 1] >> ((k0 & 1) * 4)) & 0xF;
+                const uint32_t c1 = (rec[k1 >> 1] >> ((k1 & 1) * 4)) & 0xF;
+                w |= c0 << (4 * j);
+                w |= c1 << (16 + 4 * j);
+            }
+            out[q] = w;
+        }
+        codes[i] = make_uint4(out[0], out[1], out[2], out[3]);
+        // word `lane` of the (scale, bias) block: 8 tt + 2 q + rr is group q of row 2 tt + rr
+        {
+            const int tt = lane >> 3, q = (lane >> 1) & 3, rr = lane & 1;
+            const uint8_t* rec = groups + ((size_t)(tile * 8 + 2 * tt + rr) * G + blk * 4 + q) * 20;
+            sb[tb * 32 + lane] = (uint32_t)rec[16] | ((uint32_t)rec[17] << 8) | ((uint32_t)rec[18] << 16) |
+                                 ((uint32_t)rec[19] << 24);
+        }
+    }
+}
+
+}  // namespace
+
+int gemv_a4_warps_per_tile(int rows, int K, int pair)
+{
+    // split each tile's K over more warps while the CTAs would not fill the machine
+    const int nb = K / 128;
+    int S = 1;
+    const int C = 152 * CTAS_PER_SM;
+    const int tiles = (pair ? 2 : 1) * rows / 8;
+    while (S < WARPS && tiles * S / WARPS < C && nb / (2 * S) >= 2) S *= 2;
+    if (pair && S > 4) S = 4;          // a unit holds gate and up tiles of the same rows
+    return S;
+}
+
+cudaError_t launch_a4_planes(cudaStream_t s, const uint8_t* groups, int rows, int K, void* codes, void* sb)
+{
+    const size_t total = (size_t)(rows / 8) * (K / 128) * 32;
+    int grid = (int)((total + 255) / 256);
+    if (grid > 152 * 32) grid = 152 * 32;
+    a4_planes_kernel<<<grid, 256, 0, s>>>(groups, rows, K, static_cast<uint4*>(codes), static_cast<uint32_t*>(sb));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_a4(const Launch& L, const GemvArgs& a)
+{
+    const int R = WARPS / a.warps_per_row;
+    const int n_tiles = a.pair ? 2 * (a.rows[0] / 8)
+                               : (a.rows[0] + (a.n_tensors > 1 ? a.rows[1] : 0) +
+                                  (a.n_tensors > 2 ? a.rows[2] : 0)) / 8;
+    const int n_units = n_tiles / R;
+    const size_t smem = gemv_a4_smem(a.K);
+    int grid = std::min(n_units, 152 * CTAS_PER_SM);
+    const int iters = (n_units + grid - 1) / grid;
+    grid = (n_units + iters - 1) / iters;
+    static std::atomic<unsigned long long> attr_done{0};
+    if (smem > 48 * 1024)
+        if (cudaError_t e = allow_smem_per_device(gemv_a4_kernel, (int)gemv_a4_smem(32768), attr_done)) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (L.counter) ++*L.counter;
+    return cudaLaunchKernelEx(&cfg, gemv_a4_kernel, a);
+}
+
+}  // namespace q3

@@ -118,6 +118,13 @@ struct GemvArgs {
     L2Prefetch next;           // weights of the next launch (bytes 0: none)
 };
 cudaError_t launch_gemv(const Launch& L, int scheme, const GemvArgs& a);
+// AFFINE4_GS32 matvec (w: lane-major code planes, scales: (scale, bias)
+// planes, as launch_a4_planes derives them; rows multiples of 8, K of 128)
+cudaError_t launch_gemv_a4(const Launch& L, const GemvArgs& a);
+int gemv_a4_warps_per_tile(int rows, int K, int pair);
+// canonical 20-byte groups [rows][K/32] -> the matvec's code and (scale, bias) planes
+// (codes: rows * K / 2 bytes; sb: rows * K / 32 * 4 bytes)
+cudaError_t launch_a4_planes(cudaStream_t s, const uint8_t* groups, int rows, int K, void* codes, void* sb);
 // segments per row: a power of two, preferably with at most 8 loads per lane
 int gemv_warps_per_row(int rows, int K, int scheme, int pair);
 int gemv_max_grid();

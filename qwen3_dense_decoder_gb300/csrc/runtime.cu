@@ -103,6 +103,13 @@ struct Q8Planes {
     __half* sc = nullptr;
 };
 
+// AFFINE4_GS32 planes of the one-token matvec (k_gemv_a4.cu): lane-major
+// code words and (scale, bias) words, 5.0 bits a weight as in the format
+struct A4Planes {
+    void* codes = nullptr;
+    void* sb = nullptr;
+};
+
 enum Proj { P_Q, P_K, P_V, P_O, P_G, P_U, P_D, N_PROJ };
 
 struct LayerMaps {
@@ -128,6 +135,7 @@ struct q3_model {
     const bf16* lm_head = nullptr;
     std::vector<q3_layer_weights> layers;
     std::vector<std::vector<Q8Planes>> q8;   // [layer][proj]
+    std::vector<std::vector<A4Planes>> a4;   // [layer][proj]
 
     // device memory owned by the model
     std::vector<void*> allocs;
@@ -550,7 +558,9 @@ int gemv(q3_model* m, int n_tensors, const void* const* w, const __half* const* 
     a.n_tensors = n_tensors;
     a.pair = pair;
     a.K = K;
-    a.warps_per_row = gemv_warps_per_row(total, K, sc ? Q3_Q8_0 : Q3_BF16, pair);
+    const int scheme = !sc ? Q3_BF16 : m->c.scheme;     // the lm_head is bf16 in every scheme
+    a.warps_per_row = scheme == Q3_AFFINE4 ? gemv_a4_warps_per_tile(total, K, pair)
+                                           : gemv_warps_per_row(total, K, scheme, pair);
     a.argmax_out = argmax;
     a.am_val = m->am_val;
     a.am_idx = m->am_idx;
@@ -563,7 +573,7 @@ int gemv(q3_model* m, int n_tensors, const void* const* w, const __half* const* 
     a.status = m->status;
     Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
     m->prof_begin(Q3_K_GEMV);
-    const int rc = m->check(launch_gemv(L, sc ? Q3_Q8_0 : Q3_BF16, a), "gemv");
+    const int rc = m->check(scheme == Q3_AFFINE4 ? launch_gemv_a4(L, a) : launch_gemv(L, scheme, a), "gemv");
     m->prof_end();
     return rc;
 }
@@ -719,10 +729,17 @@ int run_round(q3_model* m, const Round& r)
     const int* row_pos = m->meta;
     const int* row_slot = m->meta + m->max_rows;
     const int* last_rows = m->meta + 2 * m->max_rows;
-    // one-row rounds take the GEMV path, which reads BF16 or Q8_0 weights;
-    // AFFINE4 rounds of any size take the tensor-core path over the fp16 copy
-    const bool one = (T == 1) && c.scheme != Q3_AFFINE4;
+    // one-row rounds take the matvec path, which reads BF16, Q8_0 planes or
+    // AFFINE4 planes; wider rounds the tensor-core GEMM
+    const bool one = (T == 1);
     const bool q8 = c.scheme == Q3_Q8_0;
+    const bool a4 = c.scheme == Q3_AFFINE4;
+    // a projection's matvec planes: quants / codes and scales (null for bf16)
+    auto planes = [&](int l, int proj, const void* bf, const void** w, const __half** sc) {
+        if (q8) { *w = m->q8[l][proj].qs; *sc = m->q8[l][proj].sc; }
+        else if (a4) { *w = m->a4[l][proj].codes; *sc = static_cast<const __half*>(m->a4[l][proj].sb); }
+        else { *w = bf; *sc = nullptr; }
+    };
     Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
     // one launcher call, bracketed by profiling events of kernel class cls
     auto run = [m](int cls, auto&& launch) {
@@ -751,14 +768,11 @@ int run_round(q3_model* m, const Round& r)
             const void* w[3];
             const __half* sc[3];
             const int rows[3] = {m->qw, m->kvw, m->kvw};
-            if (q8) {
-                for (int i = 0; i < 3; ++i) { w[i] = m->q8[l][P_Q + i].qs; sc[i] = m->q8[l][P_Q + i].sc; }
-            } else {
-                w[0] = W.wq; w[1] = W.wk; w[2] = W.wv;
-            }
+            planes(l, P_Q, W.wq, &w[0], &sc[0]);
+            planes(l, P_K, W.wk, &w[1], &sc[1]);
+            planes(l, P_V, W.wv, &w[2], &sc[2]);
             const L2Prefetch nx = decode_weights(m, l, 1);
-            if ((rc = gemv(m, 3, w, q8 ? sc : nullptr, rows, 0, H, m->x, attn_norm, EPI_STORE_F32, m->qkv,
-                           nullptr, &nx)))
+            if ((rc = gemv(m, 3, w, sc, rows, 0, H, m->x, attn_norm, EPI_STORE_F32, m->qkv, nullptr, &nx)))
                 return rc;
         } else {
             if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->ha, m->status); }),
@@ -841,12 +855,12 @@ int run_round(q3_model* m, const Round& r)
 
         // ---- O projection + residual
         if (one) {
-            const void* w[1] = {q8 ? (const void*)m->q8[l][P_O].qs : W.wo};
-            const __half* sc[1] = {q8 ? m->q8[l][P_O].sc : nullptr};
+            const void* w[1];
+            const __half* sc[1];
+            planes(l, P_O, W.wo, &w[0], &sc[0]);
             const int rows[1] = {H};
             const L2Prefetch nx = decode_weights(m, l, 2);
-            if ((rc = gemv(m, 1, w, q8 ? sc : nullptr, rows, 0, m->qw, m->attf, nullptr, EPI_ADD_F32, m->x,
-                           nullptr, &nx)))
+            if ((rc = gemv(m, 1, w, sc, rows, 0, m->qw, m->attf, nullptr, EPI_ADD_F32, m->x, nullptr, &nx)))
                 return rc;
         } else {
             rc = gemm(m, &Mp.m[P_O], nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
@@ -858,23 +872,18 @@ int run_round(q3_model* m, const Round& r)
         if (one) {
             const void* w[2];
             const __half* sc[2];
-            if (q8) {
-                w[0] = m->q8[l][P_G].qs; w[1] = m->q8[l][P_U].qs;
-                sc[0] = m->q8[l][P_G].sc; sc[1] = m->q8[l][P_U].sc;
-            } else {
-                w[0] = W.w_gate; w[1] = W.w_up;
-            }
+            planes(l, P_G, W.w_gate, &w[0], &sc[0]);
+            planes(l, P_U, W.w_up, &w[1], &sc[1]);
             const int rows[2] = {F, F};
             const L2Prefetch nx2 = decode_weights(m, l, 3);
-            if ((rc = gemv(m, 2, w, q8 ? sc : nullptr, rows, 1, H, m->x, ffn_norm, EPI_SWIGLU_F32, m->sf,
-                           nullptr, &nx2)))
+            if ((rc = gemv(m, 2, w, sc, rows, 1, H, m->x, ffn_norm, EPI_SWIGLU_F32, m->sf, nullptr, &nx2)))
                 return rc;
-            const void* wd[1] = {q8 ? (const void*)m->q8[l][P_D].qs : W.w_down};
-            const __half* scd[1] = {q8 ? m->q8[l][P_D].sc : nullptr};
+            const void* wd[1];
+            const __half* scd[1];
+            planes(l, P_D, W.w_down, &wd[0], &scd[0]);
             const int rowsd[1] = {H};
             const L2Prefetch nx3 = decode_weights(m, l + 1, 0);
-            if ((rc = gemv(m, 1, wd, q8 ? scd : nullptr, rowsd, 0, F, m->sf, nullptr, EPI_ADD_F32, m->x,
-                           nullptr, &nx3)))
+            if ((rc = gemv(m, 1, wd, scd, rowsd, 0, F, m->sf, nullptr, EPI_ADD_F32, m->x, nullptr, &nx3)))
                 return rc;
         } else {
             if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->ha, m->status); }),
@@ -1331,16 +1340,25 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
             }
         }
     } else if (c.scheme == Q3_AFFINE4) {
-        // fp16 copies of the dequantised groups for the tensor-core path, which
-        // runs every AFFINE4 round: fp16(fma(scale, code, bias))
+        // one-token rounds: the format's bytes rearranged lane-major for the
+        // 5.0-bit matvec; wider rounds: fp16 copies of the dequantised groups
+        // for the tensor-core path, fp16(fma(scale, code, bias))
         m->maps.resize(c.n_layers);
         m->w16.resize(c.n_layers);
+        m->a4.resize(c.n_layers);
         for (int l = 0; l < c.n_layers && ok; ++l) {
             const q3_layer_weights& L = m->layers[l];
             const void* src[N_PROJ] = {L.wq, L.wk, L.wv, L.wo, L.w_gate, L.w_up, L.w_down};
             m->w16[l].resize(N_PROJ);
+            m->a4[l].resize(N_PROJ);
             for (int p = 0; p < N_PROJ; ++p) {
                 const size_t n = (size_t)proj_rows[p] * proj_cols[p];
+                m->a4[l][p].codes = A(n / 2);
+                m->a4[l][p].sb = A(n / 32 * 4);
+                if (!ok) break;
+                if (launch_a4_planes(m->stream, static_cast<const uint8_t*>(src[p]), proj_rows[p], proj_cols[p],
+                                     m->a4[l][p].codes, m->a4[l][p].sb) != cudaSuccess)
+                    return bad(Q3_ERR_CUDA, "AFFINE4 plane derivation failed");
                 f16* d = static_cast<f16*>(A(n * sizeof(f16)));
                 if (!ok) break;
                 m->w16[l][p] = d;
@@ -1887,6 +1905,46 @@ int q3_op_matvec(const void* w_dev, const void* scales_dev, const float* x_dev, 
     Launch L{static_cast<cudaStream_t>(stream), false, nullptr};
     cudaError_t e = launch_gemv(L, scales_dev ? Q3_Q8_0 : Q3_BF16, a);
     if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "op_matvec: %s", cudaGetErrorString(e));
+    return Q3_OK;
+}
+
+int q3_op_matvec_affine4(const void* groups_dev, const float* x_dev, int M, int K, float* y_dev, void* stream)
+{
+    if (!groups_dev || !x_dev || !y_dev || M < 8 || M % 8 || K < 128 || K % 128 || K > 32768 ||
+        (reinterpret_cast<uintptr_t>(groups_dev) & 3) || !aligned16(x_dev))
+        return fail(Q3_ERR_INVALID_ARG, "op_matvec_affine4: bad argument");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* codes = nullptr;
+    void* sb = nullptr;
+    int* status = nullptr;
+    auto release = [&]() { cudaFree(codes); cudaFree(sb); cudaFree(status); };
+    const size_t n = (size_t)M * K;
+    if (cudaMalloc(&codes, n / 2) != cudaSuccess || cudaMalloc(&sb, n / 32 * 4) != cudaSuccess ||
+        cudaMalloc(&status, sizeof(int)) != cudaSuccess) {
+        release();
+        return fail(Q3_ERR_OOM, "op_matvec_affine4: allocation failed");
+    }
+    GemvArgs a{};
+    a.w[0] = codes;
+    a.scales[0] = static_cast<const __half*>(sb);
+    a.rows[0] = M;
+    a.n_tensors = 1;
+    a.K = K;
+    a.warps_per_row = gemv_a4_warps_per_tile(M, K, 0);
+    a.x = x_dev;
+    a.epi = EPI_STORE_F32;
+    a.out = y_dev;
+    a.status = status;
+    Launch L{st, false, nullptr};
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = launch_a4_planes(st, static_cast<const uint8_t*>(groups_dev), M, K, codes, sb);
+    if (e == cudaSuccess) e = launch_gemv_a4(L, a);
+    int word = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&word, status, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    release();
+    if (e != cudaSuccess) return fail(Q3_ERR_CUDA, "op_matvec_affine4: %s", cudaGetErrorString(e));
+    if (word) return fail(Q3_ERR_DEVICE_CHECK, "op_matvec_affine4: device status 0x%x", word);
     return Q3_OK;
 }
 

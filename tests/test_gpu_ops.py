@@ -135,3 +135,23 @@ def test_gemv_q8_0_matches_oracle(q3, orc, M, K):
     deq = orc.q8_0_unpack(bnp, K).astype(np.float64)
     bound = 1e-5 * (np.abs(deq) @ np.abs(x.cpu().numpy().astype(np.float64)))
     assert np.all(np.abs(y.cpu().numpy() - ref) <= bound)
+
+
+@pytest.mark.parametrize("M,K", [(8, 128), (128, 1024), (6144, 2560), (2560, 9728), (1024, 17408)])
+def test_gemv_affine4_matches_oracle(q3, orc, M, K):
+    """The 5.0-bit AFFINE4 matvec of one-token rounds (codes as fp16 on
+    mma.sync, the activation as fp16 high and low parts, s * sum(q x) +
+    b * sum(x) per group) against the oracle's AFFINE4 matmul; the bound is
+    the decode GEMV's, 1e-5 of sum |w x| over the dequantised weights."""
+    w = _bf16((M, K), 50, 0.02)
+    if M >= 9 and K >= 128:
+        w = _affine4_edge_rows(w)
+    groups = q3.quantize_affine4(w)
+    x = torch.randn(K, generator=torch.Generator(device="cuda").manual_seed(51), device="cuda")
+    y = q3.op_matvec_affine4(groups, x, M, K)
+    gnp = groups.cpu().numpy()
+    ref = orc.matmul(gnp, 2, M, K, x.cpu().numpy(), n_threads=8)[0]
+    deq = orc.affine4_unpack(gnp, K).astype(np.float64)
+    bound = 1e-5 * (np.abs(deq) @ np.abs(x.cpu().numpy().astype(np.float64))) + 1e-30
+    err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+    assert np.all(err <= bound), (err / bound).max()
