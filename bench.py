@@ -482,6 +482,22 @@ def oracle_decode_sample(shape, weights, budget_s: float, max_steps: int, warmup
             "seconds": dt, "steps": steps}
 
 
+def oracle_prefill_sample(shape, weights, tokens: int) -> dict:
+    """Time the oracle on one prefill round of `tokens` seeded tokens of the
+    full-depth shape (logits of the last row), on this host's cores."""
+    import oracle
+    import synthetic
+    oracle.build()
+    m = oracle.Model(shape, weights)
+    s = m.session(max_ctx=tokens + 1)
+    toks = synthetic.make_tokens(tokens, shape.vocab, seed=7)
+    t0 = time.perf_counter()
+    s.eval(toks)
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens / dt, 3), "unit": "tok/s", "cores": m.n_threads, "seconds": round(dt, 2),
+            "sample": f"one {tokens}-token prefill round of the full {shape.n_layers}-layer {shape.name} shape"}
+
+
 # ---------------------------------------------------------------- other named shapes
 
 def q8_bytes(params: int) -> float:
@@ -832,6 +848,8 @@ def main():
                                                     max_steps=16)
         for k in ("seconds", "steps"):
             line["cpu_baseline"].pop(k, None)
+        # the oracle's prefill beside the GPU's (a bounded sample: one 64-token round)
+        line["cpu_baseline"]["prefill"] = oracle_prefill_sample(res["shape"], res["weights"], 64)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist_on:

@@ -82,14 +82,16 @@ Q3_DEV const uint8_t* tile_chunk(const uint8_t* t, int r, int c) {
     return t + r * (ATT_KSTR * 2) + c * 16;
 }
 
-// One 32-position block for the G query heads of the KV head (rows 2h, 2h+1
-// of sqa, rows of ATT_KSTR bf16), output dimensions [8 dt0, 8 (dt0 + NDT)):
-// S = q K^T on 4 x 8 mma (positions x dims), masked to n_pos, online
-// softmax, O += P V on NDT x 2.
-template <int NDT, bool F16 = false>
-Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const void* sqa_, int n_pos, int dt0,
-                            int lane, AttAcc<NDT>& w) {
-    const uint16_t* sqa = static_cast<const uint16_t*>(sqa_);
+// The two halves of one 32-position block for the G query heads of the KV
+// head (rows 2h, 2h+1 of sqa, rows of ATT_KSTR elements).  attend_qk: S =
+// q K^T on 4 x 8 mma (positions x dims), masked to n_pos, the online-softmax
+// update (running maximum and sum, O rescaled) and P as high/low pairs in
+// the A-fragment registers pa.  attend_pv: O += P V for output dimension
+// tiles [dt0, dt0 + NDT).  Kept apart so a caller may reuse one staged tile
+// for K and then V.
+template <int NDT, bool F16>
+Q3_DEV void attend_qk(const uint8_t* kt, const uint16_t* sqa, int n_pos, int lane, AttAcc<NDT>& w,
+                      uint32_t (&pa)[4][2]) {
     const int g = lane >> 2, tig = lane & 3;
     float sacc[4][4];
 #pragma unroll
@@ -131,9 +133,8 @@ Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const void* sq
         alpha[h] = exp2f(w.m[h] - m_new);          // 0 on the first block (m = -inf)
         w.m[h] = m_new;
     }
-    // P and its bf16 split: even rows take the high part, odd rows the rest
+    // P and its split: even rows take the high part, odd rows the rest
     const bool hi_row = (g & 1) == 0;
-    uint32_t pa[4][2];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
         float pv[4];
@@ -161,6 +162,11 @@ Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const void* sq
         w.o[dt][0] *= alpha[0]; w.o[dt][1] *= alpha[0];
         w.o[dt][2] *= alpha[1]; w.o[dt][3] *= alpha[1];
     }
+}
+
+template <int NDT, bool F16>
+Q3_DEV void attend_pv(const uint8_t* vt, int dt0, int lane, AttAcc<NDT>& w, const uint32_t (&pa)[4][2]) {
+    const int mi = lane >> 3, r8 = lane & 7;
     // O += P V: k = positions (2 steps of 16), n = this warp's dimension tiles
 #pragma unroll
     for (int dt = 0; dt < NDT; ++dt) {
@@ -170,6 +176,15 @@ Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const void* sq
         mma_kv<F16>(w.o[dt], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b[0], b[1]);
         mma_kv<F16>(w.o[dt], pa[2][0], pa[2][1], pa[3][0], pa[3][1], b[2], b[3]);
     }
+}
+
+// One whole block: attend_qk on kt, then attend_pv on vt.
+template <int NDT, bool F16 = false>
+Q3_DEV void attend_block_tc(const uint8_t* kt, const uint8_t* vt, const void* sqa, int n_pos, int dt0,
+                            int lane, AttAcc<NDT>& w) {
+    uint32_t pa[4][2];
+    attend_qk<NDT, F16>(kt, static_cast<const uint16_t*>(sqa), n_pos, lane, w, pa);
+    attend_pv<NDT, F16>(vt, dt0, lane, w, pa);
 }
 
 

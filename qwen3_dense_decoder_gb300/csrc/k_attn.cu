@@ -22,9 +22,12 @@
 //
 // With the opt-in Q8_0 cache ("Kipp Roadmap", status v0.0.4) a warp copies
 // the block's raw Q8_0 tiles (codes and fp16 scales, 4,352 bytes each for K
-// and V) and expands them in shared memory into fp16 tiles of scale * code
-// (each product rounded once to fp16), then attends them with fp16 products;
-// the new position's K/V are packed by the same rule as every other row.
+// and V, two copy groups) and expands them in shared memory into an fp16
+// tile of scale * code (each product rounded once to fp16): K first for the
+// scores and softmax, then V into the same tile for O += P V, with the next
+// block's raw copies issued as soon as the raw buffer is free, so they
+// overlap the products.  One tile per warp keeps three CTAs on an SM.  The
+// new position's K/V are packed by the same rule as every other row.
 //
 // Decode rounds (each row the single new token of its session) fuse the
 // per-head q/k RMSNorm, RoPE and the K/V append of that token: the new K/V
@@ -51,7 +54,7 @@ template <int G, bool KQ>
 struct AttnSmem {
     static constexpr size_t q_bytes = (size_t)16 * K_STRIDE * 2;     // q high/low rows (bf16 or fp16)
     static constexpr size_t k_bytes = (size_t)AWARPS * K_TILE * 2;
-    static constexpr size_t v_bytes = (size_t)AWARPS * V_TILE * 2;
+    static constexpr size_t v_bytes = KQ ? 0 : (size_t)AWARPS * V_TILE * 2;   // Q8_0: V reuses the K tile
     static constexpr size_t new_bytes = 2 * D * 2;                  // new K and V row (bf16 or fp16)
     static constexpr size_t misc_bytes = 2 * AWARPS * G * sizeof(float) + 16;
     static constexpr size_t raw_bytes = KQ ? (size_t)AWARPS * 2 * KVQ_TILE : 0;   // Q8_0 K and V tiles
@@ -72,12 +75,12 @@ Q3_DEV void stage_block(__nv_bfloat16* kt, __nv_bfloat16* vt, const __nv_bfloat1
     cp_async_commit();
 }
 
-// stage the raw Q8_0 K and V tiles of one block: 2 x 272 16-byte pieces
+// stage the raw Q8_0 K and V tiles of one block: 272 16-byte pieces each,
+// K and V as two copy groups (K can be expanded while V is in flight)
 Q3_DEV void stage_block_q8(uint8_t* raw, const uint8_t* Kq, const uint8_t* Vq, int lane) {
-    for (int i = lane; i < KVQ_TILE / 16; i += 32) {
-        cp_async_16(raw + i * 16, Kq + i * 16);
-        cp_async_16(raw + KVQ_TILE + i * 16, Vq + i * 16);
-    }
+    for (int i = lane; i < KVQ_TILE / 16; i += 32) cp_async_16(raw + i * 16, Kq + i * 16);
+    cp_async_commit();
+    for (int i = lane; i < KVQ_TILE / 16; i += 32) cp_async_16(raw + KVQ_TILE + i * 16, Vq + i * 16);
     cp_async_commit();
 }
 
@@ -111,7 +114,7 @@ Q3_DEV void store_q_split(__nv_bfloat16* sqa, int g, const float (&y)[4], float 
 }
 
 template <int G, bool FUSED, bool KQ>
-__global__ void __launch_bounds__(AWARPS * 32, KQ ? 2 : 3) attn_kernel(const AttnArgs p)
+__global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
 {
     using S = AttnSmem<G, KQ>;
     extern __shared__ __align__(16) uint8_t smem[];
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(AWARPS * 32, KQ ? 2 : 3) attn_kernel(const Att
     const int t = p.row_order ? p.row_order[blockIdx.z] : (int)blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __nv_bfloat16* kt = kt_all + warp * K_TILE;
-    __nv_bfloat16* vt = vt_all + warp * V_TILE;
+    __nv_bfloat16* vt = KQ ? kt : vt_all + warp * V_TILE;
     uint8_t* raw = raw_all + (size_t)warp * 2 * KVQ_TILE;     // (Q8_0 cache only)
 
     // Row metadata and block tables were uploaded before the round began, so
@@ -244,24 +247,48 @@ __global__ void __launch_bounds__(AWARPS * 32, KQ ? 2 : 3) attn_kernel(const Att
             continue;
         }
         staged = false;
+        const int n_pos = min(KV_BLOCK, ctx - b * KV_BLOCK);
+        const bool new_row = FUSED && b == last_blk;     // the new position: its K/V came from above
+        const int r_new = pos % KV_BLOCK;
+        if (KQ) {
+            uint32_t pa[4][2];
+            cp_async_wait_all_but(1);                      // K landed; V may still be in flight
+            __syncwarp();
+            expand_q8(kt, raw, lane);
+            __syncwarp();
+            if (new_row) {
+                *reinterpret_cast<uint2*>(kt + r_new * K_STRIDE + lane * 4) =
+                    *reinterpret_cast<const uint2*>(snew + lane * 4);
+                __syncwarp();
+            }
+            attend_qk<NDT, true>(reinterpret_cast<const uint8_t*>(kt), reinterpret_cast<const uint16_t*>(sqa),
+                                 n_pos, lane, st, pa);
+            cp_async_wait_all();
+            __syncwarp();                                  // every lane is done reading K
+            expand_q8(kt, raw + KVQ_TILE, lane);
+            __syncwarp();
+            if (new_row) {
+                *reinterpret_cast<uint2*>(kt + r_new * K_STRIDE + lane * 4) =
+                    *reinterpret_cast<const uint2*>(snew + D + lane * 4);
+                __syncwarp();
+            }
+            // the raw buffer is free: the next block's copies overlap this block's P V
+            if (b + AWARPS < b1) staged = stage(b + AWARPS);
+            attend_pv<NDT, true>(reinterpret_cast<const uint8_t*>(kt), 0, lane, st, pa);
+            __syncwarp();      // the tile is rewritten by the next block's expansion
+            continue;
+        }
         cp_async_wait_all();
         __syncwarp();
-        if (KQ) {
-            expand_q8(kt, raw, lane);
-            expand_q8(vt, raw + KVQ_TILE, lane);
-            __syncwarp();
-        }
-        if (FUSED && b == last_blk) {
-            // the new position: its K/V were computed above, not read back
-            const int r = pos % KV_BLOCK;
-            *reinterpret_cast<uint2*>(kt + r * K_STRIDE + lane * 4) =
+        if (new_row) {
+            *reinterpret_cast<uint2*>(kt + r_new * K_STRIDE + lane * 4) =
                 *reinterpret_cast<const uint2*>(snew + lane * 4);
-            *reinterpret_cast<uint2*>(vt + r * K_STRIDE + lane * 4) =
+            *reinterpret_cast<uint2*>(vt + r_new * K_STRIDE + lane * 4) =
                 *reinterpret_cast<const uint2*>(snew + D + lane * 4);
             __syncwarp();
         }
-        attend_block_tc<NDT, KQ>(reinterpret_cast<const uint8_t*>(kt), reinterpret_cast<const uint8_t*>(vt), sqa,
-                                 min(KV_BLOCK, ctx - b * KV_BLOCK), 0, lane, st);
+        attend_block_tc<NDT>(reinterpret_cast<const uint8_t*>(kt), reinterpret_cast<const uint8_t*>(vt), sqa,
+                             n_pos, 0, lane, st);
         __syncwarp();      // the tile is rewritten by the next block's copies
     }
     cp_async_wait_all();

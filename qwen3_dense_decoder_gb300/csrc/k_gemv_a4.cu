@@ -133,8 +133,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_a4_kernel(const Gem
     if (threadIdx.x == 0) issue_l2_prefetch(p.next, blockIdx.x, gridDim.x);
     grid_dep_wait();
 
-    // the activation (RMS-normalised when a gain is given) goes straight from
-    // L2 into its fp16 high/low fragments and the per-group sums
+    // the activation (RMS-normalised when a gain is given) goes from L2 into
+    // its fp16 high/low fragments and the per-group sums in one coalesced
+    // pass: thread i takes values [4i, 4i + 4), eight threads a group
     float scl = 1.0f;
     if (p.norm_gain) {
         float ss = 0.f;
@@ -153,37 +154,41 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_a4_kernel(const Gem
         __syncthreads();
         scl = s_scale;
     }
-    auto xval = [&](int k) {
-        const float x = p.x[k];
-        return p.norm_gain ? x * scl * __bfloat162float(p.norm_gain[k]) : x;
-    };
-    // fragment (g, kstep j, part hl, t): the part's values at k = 32 g + 16 j + {2t, 2t+1} and {+8, +9}
-    bool bad = false;
-    for (int i = threadIdx.x; i < G * 16; i += THREADS) {
-        const int g = i >> 4, j = (i >> 3) & 1, hl = (i >> 2) & 1, tt = i & 3;
-        const int k0 = g * 32 + j * 16 + 2 * tt;
-        const float v[4] = {xval(k0), xval(k0 + 1), xval(k0 + 8), xval(k0 + 9)};
-        uint32_t w[2];
+    {
+        uint32_t* xw = reinterpret_cast<uint32_t*>(xf);
+        bool bad = false;
+        for (int k = threadIdx.x * 4; k < p.K; k += THREADS * 4) {     // K % 128 == 0: whole warps
+            float4 x = *reinterpret_cast<const float4*>(p.x + k);
+            if (p.norm_gain) {
+                const uint2 gg = *reinterpret_cast<const uint2*>(p.norm_gain + k);
+                x.x = x.x * scl * bf16lo(gg.x);
+                x.y = x.y * scl * bf16hi(gg.x);
+                x.z = x.z * scl * bf16lo(gg.y);
+                x.w = x.w * scl * bf16hi(gg.y);
+            }
+            bad |= fabsf(x.x) > 65504.f || fabsf(x.y) > 65504.f || fabsf(x.z) > 65504.f || fabsf(x.w) > 65504.f;
+            // value k = 32 g + 16 j + r: pair (r & 7) / 2 of k step j, half r / 8 of the fragment
+            const int g = k >> 5, j = (k >> 4) & 1, r = k & 15;
+            const int tt = (r & 7) >> 1, e = r >> 3;
+            const float v[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const float a = v[2 * e], b = v[2 * e + 1];
-            bad |= fabsf(a) > 65504.f || fabsf(b) > 65504.f;      // the fp16 high part would overflow
-            const __half2 hi = __floats2half2_rn(a, b);
-            if (hl) {
+            for (int pr = 0; pr < 2; ++pr) {
+                const float a = v[2 * pr], b = v[2 * pr + 1];
+                const __half2 hi = __floats2half2_rn(a, b);
                 const float2 hf = __half22float2(hi);
                 const __half2 lo = __floats2half2_rn(a - hf.x, b - hf.y);
-                w[e] = *reinterpret_cast<const uint32_t*>(&lo);
-            } else {
-                w[e] = *reinterpret_cast<const uint32_t*>(&hi);
+                const int base = ((g * 2 + j) * 2) * 4 + tt + pr;        // entry (g, j, hl = 0, t)
+                xw[(base) * 2 + e] = *reinterpret_cast<const uint32_t*>(&hi);
+                xw[(base + 4) * 2 + e] = *reinterpret_cast<const uint32_t*>(&lo);   // hl = 1
             }
+            // the group's sum over its eight threads (lanes 8m .. 8m + 7)
+            float sx = x.x + x.y + x.z + x.w;
+            sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+            sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+            sx += __shfl_xor_sync(0xffffffffu, sx, 4);
+            if ((threadIdx.x & 7) == 0) gsum[g] = sx;
         }
-        xf[i] = make_uint2(w[0], w[1]);
-    }
-    if (bad) set_status(p.status, Q3_STATUS_F16_RANGE);
-    for (int g = threadIdx.x; g < G; g += THREADS) {
-        float sx = 0.f;
-        for (int k = 0; k < 32; ++k) sx += xval(g * 32 + k);
-        gsum[g] = sx;
+        if (bad) set_status(p.status, Q3_STATUS_F16_RANGE);
     }
     __syncthreads();
 
@@ -323,6 +328,8 @@ int gemv_a4_warps_per_tile(int rows, int K, int pair)
     const int C = 152 * CTAS_PER_SM;
     const int tiles = (pair ? 2 : 1) * rows / 8;
     while (S < WARPS && tiles * S / WARPS < C && nb / (2 * S) >= 2) S *= 2;
+    // a unit of WARPS / S tiles must divide the tiles (an even number of them in pair mode)
+    while (S < WARPS && tiles % (WARPS / S)) S *= 2;
     if (pair && S > 4) S = 4;          // a unit holds gate and up tiles of the same rows
     return S;
 }
@@ -343,6 +350,7 @@ cudaError_t launch_gemv_a4(const Launch& L, const GemvArgs& a)
                                : (a.rows[0] + (a.n_tensors > 1 ? a.rows[1] : 0) +
                                   (a.n_tensors > 2 ? a.rows[2] : 0)) / 8;
     const int n_units = n_tiles / R;
+    if (n_units < 1 || n_tiles % R) return cudaErrorInvalidValue;
     const size_t smem = gemv_a4_smem(a.K);
     int grid = std::min(n_units, 152 * CTAS_PER_SM);
     const int iters = (n_units + grid - 1) / grid;
