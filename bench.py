@@ -70,7 +70,8 @@ def parse():
                     choices=("0.6b", "8b-q8_0", "14b", "4b-affine4", "14b-kvq8"),
                     help="measure the other named shapes instead (one JSON line each; 0.6b, 8b-q8_0 "
                          "and 14b if none given; 14b-kvq8 is the 14B workload over the Q8_0 K/V cache)")
-    ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill", "attn-decode-b32"),
+    ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill", "attn-decode-b32",
+                                           "attn-decode-kvq8-b32", "gemv-a4"),
                     default=None,
                     help="run only a small case sized for an ncu capture (a few GB on the device) and exit")
     return ap.parse_args()
@@ -121,6 +122,38 @@ def ncu_case(name: str):
         for _ in range(4):
             m.eval_batch(ss, toks, [1] * B, lg, toks)
         m.sync()
+    elif name == "attn-decode-kvq8-b32":
+        # the same batch-32 decode over the opt-in Q8_0 K/V cache
+        s = synthetic.SHAPES["4b"].replace(n_layers=2, kv_quant=synthetic.Q8_0)
+        st = torch.cuda.Stream()
+        torch.cuda.set_stream(st)
+        w = synthetic.make_weights(s, seed=1234, device="cuda")
+        B = 32
+        m = q3.Model(s, w, max_ctx=2400, max_round_tokens=2048, stream=st)
+        pool = m.pool(B * 75 + 8, B + 2)
+        lg = torch.empty(B, s.vocab, device="cuda")
+        am = torch.zeros(B, dtype=torch.int32, device="cuda")
+        lens = synthetic.make_prompt_lengths(B, 64, 2048, seed=11)
+        ss = [pool.session() for _ in range(B)]
+        for i, x in enumerate(ss):
+            x.eval(torch.tensor(synthetic.make_tokens(int(lens[i]), s.vocab, seed=100 + i), device="cuda"),
+                   lg[0], am[i:i + 1])
+        toks = am.clone()
+        for _ in range(4):
+            m.eval_batch(ss, toks, [1] * B, lg, toks)
+        m.sync()
+    elif name == "gemv-a4":
+        # the gate/up projection of a Qwen3-4B AFFINE4_GS32 decode step as one
+        # operator call: 19,456 x 2,560 weights, 31 MB at 5.0 bits a weight
+        M, K = 19456, 2560
+        g = torch.Generator(device="cuda")
+        g.manual_seed(8)
+        w = (torch.randn(M, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        groups = q3.quantize_affine4(w)
+        x = torch.randn(K, device="cuda", generator=g)
+        for _ in range(6):
+            q3.op_matvec_affine4(groups, x, M, K)
+        torch.cuda.synchronize()
     elif name == "attn-prefill":
         # one layer's prefill attention of a 2,048-token round of the Qwen3-4B
         # shape (32 query / 8 KV heads) over a permuted block table

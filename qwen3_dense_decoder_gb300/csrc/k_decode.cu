@@ -21,14 +21,10 @@
 //    in for QKV, gate/up and the lm_head), attention units with the per-head
 //    q/k RMSNorm, RoPE and the KV append fused in, and the epilogues
 //    (store, residual add, SwiGLU, greedy argmax);
-//  - stages that need the whole of the previous stage's output (O, gate/up,
-//    down and the next layer's QKV: 3 per layer) are separated by a grid
-//    barrier: a monotonic global counter, release-add then acquire-spin,
-//    bounded in time.  The attention of KV head g waits only for the CTAs
-//    whose QKV rows hold g's q, k and v (a per-head counter they add to), and
-//    the O stage only for the eight merged attention outputs (one counter the
-//    writer of each KV head's output adds to).  The launch is cooperative, so
-//    all CTAs are resident.
+//  - stages that need the previous stage's output of other CTAs (5 per
+//    layer) are separated by a grid barrier: a monotonic global counter,
+//    release-add then acquire-spin, bounded in time.  The launch is
+//    cooperative, so all CTAs are resident.
 // Row partials are summed in a fixed order (lanes, then warp segments in
 // order), attention splits merge in split order, so results do not depend
 // on scheduling.  Every wait is bounded: on timeout the kernel records
@@ -212,41 +208,6 @@ Q3_DEV bool wait_bar(uint64_t* bar, uint32_t parity, const Smem& sm, int* status
             return false;
         }
     }
-}
-
-// Bounded acquire-wait of thread 0 until *ctr reaches target; the result,
-// the same on every consumer thread, is false when the step is aborting.
-Q3_DEV bool counter_wait(const DecodeArgs& p, const Smem& sm, const unsigned long long* ctr,
-                         unsigned long long target) {
-    if (threadIdx.x == 0 && !*sm.abort) {
-        const uint64_t t0 = global_ns();
-        for (uint32_t n = 1; ld_acquire_u64(ctr) < target; ++n) {
-            if ((n & 63) == 0 && global_ns() - t0 > Q3_WAIT_LIMIT_NS) {
-                set_status(p.status, Q3_STATUS_TIMEOUT);
-                *sm.abort = 1;
-                break;
-            }
-        }
-    }
-    return named_bar_and(CONS_BAR, NCT, *sm.abort == 0);
-}
-
-// Rows of KV head g in the stacked QKV output: its G query heads, its key
-// head and its value head.
-Q3_DEV bool qkv_rows_meet_head(const DecodeArgs& p, int r0, int r1, int g) {
-    const int G = p.n_q / p.n_kv, qw = p.n_q * D, kvw = p.n_kv * D;
-    auto meets = [&](int a, int b) { return r0 < b && a < r1; };
-    return meets(g * G * D, (g + 1) * G * D) || meets(qw + g * D, qw + (g + 1) * D) ||
-           meets(qw + kvw + g * D, qw + kvw + (g + 1) * D);
-}
-
-// CTAs whose QKV rows meet KV head g (each adds 1 to head_ctr[g] a layer)
-Q3_DEV int head_contributors(const DecodeArgs& p, int g) {
-    const int M = (p.n_q + 2 * p.n_kv) * D;
-    int n = 0;
-    for (int c = 0; c < (int)gridDim.x; ++c)
-        n += qkv_rows_meet_head(p, (int)((long long)c * M / gridDim.x), (int)((long long)(c + 1) * M / gridDim.x), g);
-    return n;
 }
 
 // Grid barrier among the consumer warps of all CTAs.  After a matvec stage
@@ -790,7 +751,7 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
             }
             const int head = u.kvh * G + hg;
             if (ns == 1) {
-                __stcg(p.att + head * D + d, O / Lx);   // this CTA writes its KV head's output
+                __stcg(p.att + head * D + d, O / Lx);
             } else {
                 __stcg(p.part_o + ((size_t)head * ns + u.split) * D + d, O);
                 if (d == 0) {
@@ -800,12 +761,7 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
             }
         }
     }
-    if (ns == 1) {
-        consumer_sync();
-        if (tid == 0 && u.active)
-            asm volatile("red.release.gpu.global.add.u64 [%0], 1;" :: "l"(p.merge_ctr) : "memory");
-        return;
-    }
+    if (ns == 1) return;
     // the last split CTA of this KV head merges every split in order: one
     // acquire-release ticket per CTA publishes its partials and, for the last,
     // makes every other split's visible
@@ -849,12 +805,7 @@ Q3_DEV void consume_attention(const DecodeArgs& p, int l, const Unit& u, const i
         for (int sp = 0; sp < ns; ++sp) O = fmaf(pg[(size_t)sp * D], sw[hg * ns + sp], O);
         __stcg(p.att + (u.kvh * G + hg) * D + d, O / pl[hg]);
     }
-    consumer_sync();
-    if (tid == 0) {
-        p.counters[u.kvh] = 0;
-        // the KV head's output is written: the O stage may read it
-        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" :: "l"(p.merge_ctr) : "memory");
-    }
+    if (tid == 0) p.counters[u.kvh] = 0;
 }
 
 Q3_DEV int checked_token(const DecodeArgs& p) {
@@ -871,17 +822,13 @@ Q3_DEV void consumer(const DecodeArgs& p, const Unit& u, const int* table, const
     uint32_t it = 0;
     unsigned long long target = p.bar_base;
     const int qw = p.n_q * D;
-    // the QKV arrivals this CTA's attention head waits for, a layer (only
-    // thread 0 polls, so only it needs the count)
-    const int n_contrib = (threadIdx.x == 0 && u.active) ? head_contributors(p, u.kvh) : 0;
     for (int l = 0; l < p.n_layers; ++l) {
         const void* const* lp = sm.wp + (size_t)l * WP_N;
         stage_x(sm, p.x, l == 0 ? erow : nullptr, p.H, static_cast<const bf16*>(lp[WP_ATTN_NORM]), p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_QKV), sm, it, warp, lane, p);
-        const unsigned long long layer_no = p.layer_base + l + 1;
-        if (u.active && !counter_wait(p, sm, p.head_ctr + u.kvh, (unsigned long long)n_contrib * layer_no)) return;
+        if (!grid_sync(p, sm, target += gridDim.x, true)) return;
         consume_attention(p, l, u, table, sm, it, warp, lane);
-        if (!counter_wait(p, sm, p.merge_ctr, (unsigned long long)p.n_kv * layer_no)) return;
+        if (!grid_sync(p, sm, target += gridDim.x, false)) return;
         stage_x(sm, p.att, nullptr, qw, nullptr, p.eps);
         consume_weights<Q8>(weight_stage(p, sm, l, ST_O), sm, it, warp, lane, p);
         if (!grid_sync(p, sm, target += gridDim.x, true)) return;
@@ -938,13 +885,7 @@ Q3_DEV void epilogue(const DecodeArgs& p, const Unit& u, const Smem& sm, int lan
     for (int l = 0; l < p.n_layers && ok; ++l) {
         ok = epilogue_stage(p, weight_stage(p, sm, l, ST_QKV), ST_QKV, sm, it, lane, p.qkv, best, best_i);
         if (!ok) break;
-        // this CTA's QKV rows are written: arrive on the counter of every KV head they hold rows of
-        {
-            const WStage sq = weight_stage(p, sm, l, ST_QKV);
-            __syncwarp();
-            if (lane < p.n_kv && qkv_rows_meet_head(p, sq.r0, sq.r1, lane))
-                asm volatile("red.release.gpu.global.add.u64 [%0], 1;" :: "l"(p.head_ctr + lane) : "memory");
-        }
+        closed();
         // attention slots: nothing to finish, only the slot release
         for (int b = u.b0; b < u.b1 && ok; b += BLKS_PER_SLOT) {
             const int slot = it % sm.n_slots;
@@ -1059,12 +1000,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_step_kernel(const DecodeArg
 
 int decode_step_slot_bytes() { return SLOT; }
 
-int decode_step_barriers(int n_layers) { return 3 * n_layers; }
+int decode_step_barriers(int n_layers) { return 5 * n_layers; }
 
 size_t decode_step_smem(int H, int F, int n_q, int n_kv, int q8, int n_slots, int n_splits, int grid,
                         int n_layers)
 {
-    if (n_kv < 1 || n_kv > 32 || n_q % n_kv || n_q / n_kv > NCW / BLKS_PER_SLOT) return 0;
+    if (n_kv < 1 || n_q % n_kv || n_q / n_kv > NCW / BLKS_PER_SLOT) return 0;
     if (grid < 1 || (H + grid - 1) / grid > MAX_OWN) return 0;
     if (n_slots < MIN_SLOTS || n_slots > MAX_SLOTS || n_splits < 1) return 0;
     const int qw = n_q * D;

@@ -267,9 +267,6 @@ struct DecodeArgs {
     int* am_counter;           // zero between calls
     unsigned long long* bar;   // grid barrier counter (monotonic across launches)
     unsigned long long bar_base;   // its value when this launch starts
-    unsigned long long* head_ctr;  // [n_kv] QKV-stage arrivals per KV head (monotonic)
-    unsigned long long* merge_ctr; // [1] arrivals of each KV head's merged attention output (monotonic)
-    unsigned long long layer_base; // layers run by earlier launches (the counters' epoch)
     int n_slots;               // ring depth
     int* status;
 };

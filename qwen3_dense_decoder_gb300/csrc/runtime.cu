@@ -181,8 +181,6 @@ struct q3_model {
     bool step_ok = false;           // shapes and device support it
     bool fused_decode = true;       // use it when step_ok
     int step_grid = 0, step_slots = 0, step_splits = 0;
-    unsigned long long* step_head_ctr = nullptr;   // [n_kv] QKV arrivals per KV head, then merged outputs
-    unsigned long long step_layer_epoch = 0;        // layers the fused step has run (the counters' epoch)
     size_t step_smem = 0;
     DecodeLayer* step_layers = nullptr;       // device [n_layers]
     unsigned long long* step_bar = nullptr;   // grid barrier counter
@@ -671,15 +669,13 @@ int setup_decode_step(q3_model* m, int n_sm)
     }
     m->step_layers = static_cast<DecodeLayer*>(m->dalloc(sizeof(DecodeLayer) * c.n_layers));
     m->step_bar = static_cast<unsigned long long*>(m->dalloc(sizeof(unsigned long long)));
-    m->step_head_ctr = static_cast<unsigned long long*>(m->dalloc(sizeof(unsigned long long) * (c.n_kv_heads + 1)));
     m->step_am_val = static_cast<float*>(m->dalloc(sizeof(float) * grid));
     m->step_am_idx = static_cast<int*>(m->dalloc(sizeof(int) * grid));
-    if (!m->step_layers || !m->step_bar || !m->step_head_ctr || !m->step_am_val || !m->step_am_idx)
+    if (!m->step_layers || !m->step_bar || !m->step_am_val || !m->step_am_idx)
         return fail(Q3_ERR_OOM, "device allocation failed");
     if (cudaMemcpy(m->step_layers, h.data(), sizeof(DecodeLayer) * c.n_layers, cudaMemcpyHostToDevice) !=
             cudaSuccess ||
-        cudaMemset(m->step_bar, 0, sizeof(unsigned long long)) != cudaSuccess ||
-        cudaMemset(m->step_head_ctr, 0, sizeof(unsigned long long) * (c.n_kv_heads + 1)) != cudaSuccess)
+        cudaMemset(m->step_bar, 0, sizeof(unsigned long long)) != cudaSuccess)
         return fail(Q3_ERR_CUDA, "fused decode setup failed");
     m->step_grid = grid;
     m->step_slots = slots;
@@ -715,19 +711,14 @@ int run_decode_step(q3_model* m, const Round& r)
     a.logits = r.logits; a.argmax_out = r.argmax;
     a.am_val = m->step_am_val; a.am_idx = m->step_am_idx; a.am_counter = m->am_counter;
     a.bar = m->step_bar; a.bar_base = m->step_epoch;
-    a.head_ctr = m->step_head_ctr;
-    a.merge_ctr = m->step_head_ctr + c.n_kv_heads;
-    a.layer_base = m->step_layer_epoch;
     a.n_slots = m->step_slots;
     a.status = m->status;
     Launch L{m->stream, false, &m->launches};
     m->prof_begin(Q3_K_STEP);
     const int rc = m->check(launch_decode_step(L, a, m->step_grid, m->step_smem), "fused decode step");
     m->prof_end();
-    if (rc == Q3_OK) {
+    if (rc == Q3_OK)
         m->step_epoch += (unsigned long long)decode_step_barriers(c.n_layers) * m->step_grid;
-        m->step_layer_epoch += (unsigned long long)c.n_layers;
-    }
     return rc;
 }
 
