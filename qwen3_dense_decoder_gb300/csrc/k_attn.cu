@@ -61,16 +61,14 @@ struct AttnSmem {
     static constexpr size_t total = q_bytes + k_bytes + v_bytes + new_bytes + misc_bytes + raw_bytes;
 };
 
-// stage the K and V tiles of one 32-position block: 2 x 32 rows of 256 bytes,
-// 16-byte pieces, 16 per lane
-Q3_DEV void stage_block(__nv_bfloat16* kt, __nv_bfloat16* vt, const __nv_bfloat16* Kb,
-                        const __nv_bfloat16* Vb, int lane) {
+// stage one 32-position K or V tile: 32 rows of 256 bytes, 16-byte pieces,
+// 16 per lane, as one copy group
+Q3_DEV void stage_tile(__nv_bfloat16* t, const __nv_bfloat16* src, int lane) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const int piece = i * 32 + lane;          // 512 pieces: row = piece / 16, col16 = piece % 16
         const int row = piece >> 4, c = piece & 15;
-        cp_async_16(kt + row * K_STRIDE + c * 8, Kb + row * D + c * 8);
-        cp_async_16(vt + row * K_STRIDE + c * 8, Vb + row * D + c * 8);
+        cp_async_16(t + row * K_STRIDE + c * 8, src + row * D + c * 8);
     }
     cp_async_commit();
 }
@@ -157,9 +155,24 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
             stage_block_q8(raw, Kq, Kq + (size_t)p.n_kv * KVQ_TILE, lane);
         } else {
             const __nv_bfloat16* Kb = p.kv_layer + ((size_t)phys * 2 * p.n_kv + kvh) * head_elems;
-            stage_block(kt, vt, Kb, Kb + (size_t)p.n_kv * head_elems, lane);
+            stage_tile(kt, Kb, lane);
+            stage_tile(vt, Kb + (size_t)p.n_kv * head_elems, lane);
         }
         return true;
+    };
+    // BF16 cache: the next block's K copy once this block's scores are done,
+    // its V copy once P V is done (each a copy group; false: nothing issued)
+    auto stage_next_k = [&](int bn) -> bool {
+        if (bn >= b1) return false;
+        const int phys = table[bn];
+        if (phys < 0 || phys >= p.n_blocks) return false;
+        stage_tile(kt, p.kv_layer + ((size_t)phys * 2 * p.n_kv + kvh) * head_elems, lane);
+        return true;
+    };
+    auto stage_next_v = [&](int bn) {
+        const int phys = table[bn];
+        stage_tile(vt, p.kv_layer + ((size_t)phys * 2 * p.n_kv + kvh) * head_elems + (size_t)p.n_kv * head_elems,
+                   lane);
     };
 
     int b = b0 + warp;
@@ -278,18 +291,34 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
             __syncwarp();      // the tile is rewritten by the next block's expansion
             continue;
         }
-        cp_async_wait_all();
+        // BF16: K and V landed as two groups (K first); the next block's K
+        // copy overlaps this block's P V, its V copy the next block's scores
+        uint32_t pa[4][2];
+        cp_async_wait_all_but(1);                          // K landed
         __syncwarp();
         if (new_row) {
             *reinterpret_cast<uint2*>(kt + r_new * K_STRIDE + lane * 4) =
                 *reinterpret_cast<const uint2*>(snew + lane * 4);
+            __syncwarp();
+        }
+        attend_qk<NDT, false>(reinterpret_cast<const uint8_t*>(kt), reinterpret_cast<const uint16_t*>(sqa),
+                              n_pos, lane, st, pa);
+        __syncwarp();                                      // every lane is done reading K
+        const bool next = stage_next_k(b + AWARPS);
+        if (next) cp_async_wait_all_but(1);                // V landed (the next K may be in flight)
+        else cp_async_wait_all();
+        __syncwarp();
+        if (new_row) {
             *reinterpret_cast<uint2*>(vt + r_new * K_STRIDE + lane * 4) =
                 *reinterpret_cast<const uint2*>(snew + D + lane * 4);
             __syncwarp();
         }
-        attend_block_tc<NDT>(reinterpret_cast<const uint8_t*>(kt), reinterpret_cast<const uint8_t*>(vt), sqa,
-                             n_pos, 0, lane, st);
-        __syncwarp();      // the tile is rewritten by the next block's copies
+        attend_pv<NDT, false>(reinterpret_cast<const uint8_t*>(vt), 0, lane, st, pa);
+        __syncwarp();                                      // every lane is done reading V
+        if (next) {
+            stage_next_v(b + AWARPS);
+            staged = true;
+        }
     }
     cp_async_wait_all();
     __syncthreads();       // the K tiles become the warp-merge buffer
