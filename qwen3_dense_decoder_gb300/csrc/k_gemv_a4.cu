@@ -5,29 +5,26 @@
 //
 // A decode step streams every weight once, so the kernel reads the format's
 // bytes and nothing more: 16 bytes of codes and 4 bytes of (scale, bias) per
-// group.  The work per weight must stay below the SM's issue budget (about
-// 34 weights per SM cycle at the HBM rate), which CUDA-core FMAs with a
-// per-nibble conversion do not (about 4 instructions a weight).  So the
+// group.  At the HBM rate an SM must retire about 34 weights a cycle, so the
+// work per weight has to stay well under the SM's issue budget.  The
 // products run on mma.sync m16n8k16 (fp16 in, FP32 accumulate):
-//  - B (16 x 8) is eight weight rows by 16 codes: a lane's four fp16 pairs
-//    come from one 32-bit word of the derived code plane, two nibbles a pair
-//    ((w >> 4j) & 0x000F000F | 0x64006400 is the fp16 pair 1024 + q, and one
-//    HSUB2 leaves q exactly);
-//  - A (16 x 16) holds the activation's fp16 high part in row 0 and its
-//    remainder in row 1 (rows 2..15 zero), so the two rows of D add up to
-//    sum q x to about 22 bits;
-//  - each group's D is taken alone and scaled: y += s * sum(q x) + b * sum(x),
-//    with sum(x) over the group formed once per CTA.
+//  - B (16 x 8) is eight weight rows by 16 codes.  A lane's four fp16 pairs
+//    come from one 32-bit word of the derived code plane:
+//    (w >> 4j) & 0x000F000F | 0x64006400 is the pair 1024 + q, one HSUB2
+//    leaves q exactly, and one HFMA2 with the row's (scale, bias) gives the
+//    weight fp16(scale * q + bias) rounded once -- the same values as the
+//    fp16 copy the tensor-core path of wider rounds reads;
+//  - A (16 x 16) holds the activation rounded to fp16 in row 0 (rows 1..15
+//    zero), so row 0 of D accumulates y over the whole K segment with no
+//    per-group work at all.
 // The derived planes (built once at model creation from the 20-byte groups)
-// are lane-major so every load is a coalesced 16-byte vector:
+// are lane-major so every load is a coalesced vector:
 //  - codes: [rows / 8][K / 128][32 lanes][4 groups] 32-bit words; lane
 //    (n = lane / 4, t = lane % 4) holds row n's codes at k = 2t, 2t + 1,
 //    2t + 8, 2t + 9, 16 + 2t, 17 + 2t, 24 + 2t, 25 + 2t of the group: fp16
 //    pair j low halves in bits 4j .. 4j + 3, high halves in bits 16 + 4j ..;
-//  - (scale, bias): [rows / 8][K / 128][4 lanes t][4 groups][rows 2t, 2t + 1]
-//    fp16 pairs, the rows whose outputs lane t of the D fragment holds; a
-//    block's 32 words are loaded one per lane and passed to lanes 0..3 by
-//    shuffles when their group is reduced.
+//  - (scale, bias): [rows / 8][K / 128][8 rows][4 groups] fp16 pairs; lane
+//    (n, t) loads row n's 16 bytes (the four lanes of a row share them).
 // Rows of one output are split over S warps of a CTA and summed in warp
 // order; epilogues as the BF16 matvec (store, residual add, SwiGLU pairs).
 #include <mutex>
@@ -41,8 +38,8 @@ namespace {
 
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
-constexpr int CTAS_PER_SM = 3;      // 85 registers a thread: the two block buffers without spills
-constexpr int BPL = 4;              // 4-group blocks a warp keeps in flight
+constexpr int CTAS_PER_SM = 3;
+constexpr int BPL = 2;              // 4-group blocks a warp keeps in flight
 
 Q3_DEV float warp_sum(float v) {
 #pragma unroll
@@ -60,17 +57,18 @@ Q3_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32
                  : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
-// fp16 pair j of a code word: (q_lo, q_hi) exactly
-Q3_DEV uint32_t code_pair(uint32_t w, int j) {
+// fp16 pair j of a code word as weights: fp16(scale * q + bias), one rounding
+Q3_DEV uint32_t weight_pair(uint32_t w, int j, __half2 sc, __half2 bi) {
     const uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), __half2half2(__ushort_as_half(0x6400)));
+    const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&v), __half2half2(__ushort_as_half(0x6400)));
+    const __half2 h = __hfma2(q, sc, bi);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // A unit is one 8-row tile of one tensor; tile index -> (tensor, row tile)
 struct A4Tile {
     const uint4* codes;     // the tile's code blocks [K/128][32 lanes] uint4
-    const uint32_t* sb;     // the tile's (scale, bias) blocks [K/128][32 words]
+    const uint4* sb;        // the tile's (scale, bias) blocks [K/128][8 rows] uint4
 };
 
 Q3_DEV A4Tile locate_a4(const GemvArgs& p, int tile) {
@@ -85,7 +83,7 @@ Q3_DEV A4Tile locate_a4(const GemvArgs& p, int tile) {
     const size_t nb = (size_t)p.K / 128;
     A4Tile a;
     a.codes = static_cast<const uint4*>(p.w[t]) + (size_t)tile * nb * 32;
-    a.sb = reinterpret_cast<const uint32_t*>(p.scales[t]) + (size_t)tile * nb * 32;
+    a.sb = reinterpret_cast<const uint4*>(p.scales[t]) + (size_t)tile * nb * 8;
     return a;
 }
 
@@ -93,9 +91,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_a4_kernel(const Gem
 {
     extern __shared__ __align__(16) uint8_t smem[];
     const int G = p.K / 32;
-    uint2* xf = reinterpret_cast<uint2*>(smem);                       // [G][2 ksteps][2 hi/lo][4 t]
-    float* gsum = reinterpret_cast<float*>(xf + (size_t)G * 16);      // [G] sum of x over each group
-    float* red = gsum + G;                                            // [WARPS][8] row partials
+    uint2* xf = reinterpret_cast<uint2*>(smem);                       // [G][2 ksteps][4 t]
+    float* red = reinterpret_cast<float*>(xf + (size_t)G * 8);        // [WARPS][8] row partials
     __shared__ float s_scale;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -108,34 +105,31 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_a4_kernel(const Gem
     const int n_units = n_tiles / R;
     const int nb = p.K / 128;
     const int b0 = seg * nb / S, b1 = (seg + 1) * nb / S;
-    const int t = lane & 3;
-    const bool out_lane = lane < 4;              // lanes 0..3: rows 2t, 2t + 1 of the tile
+    const int t = lane & 3, n = lane >> 2;
 
-    // the first blocks of the weight stream go out before the dependency wait
+    // Slot u of the in-flight ring holds block b0 + u + k BPL of the current
+    // unit; a slot consumed at block b reloads block b + BPL, or, past the
+    // segment, block b0 + u of the next unit, which is where that unit's
+    // loop expects it.
     int unit = blockIdx.x;
-    uint4 cw[BPL];
-    uint32_t sbw[BPL];
-    auto issue = [&](const A4Tile& a, int blk0) {
-#pragma unroll
-        for (int u = 0; u < BPL; ++u) {
-            const int b = blk0 + u;
-            if (b < b1) {
-                cw[u] = ldg_nc_v4(a.codes + (size_t)b * 32 + lane);
-                sbw[u] = __ldg(a.sb + (size_t)b * 32 + lane);
-            }
-        }
+    uint4 cw[BPL], sbw[BPL];
+    auto load = [&](const A4Tile& a, int b, int u) {
+        cw[u] = ldg_nc_v4(a.codes + (size_t)b * 32 + lane);
+        sbw[u] = ldg_nc_v4(a.sb + (size_t)b * 8 + n);
     };
     A4Tile cur{};
     if (unit < n_units) {
         cur = locate_a4(p, unit * R + slot);
-        issue(cur, b0);
+#pragma unroll
+        for (int u = 0; u < BPL; ++u)
+            if (b0 + u < b1) load(cur, b0 + u, u);
     }
     if (threadIdx.x == 0) issue_l2_prefetch(p.next, blockIdx.x, gridDim.x);
     grid_dep_wait();
 
-    // the activation (RMS-normalised when a gain is given) goes from L2 into
-    // its fp16 high/low fragments and the per-group sums in one coalesced
-    // pass: thread i takes values [4i, 4i + 4), eight threads a group
+    // the activation (RMS-normalised when a gain is given), rounded to fp16,
+    // in the A-fragment order: entry (g, kstep j, t) holds the values at
+    // k = 32 g + 16 j + {2t, 2t + 1} and {+8, +9}
     float scl = 1.0f;
     if (p.norm_gain) {
         float ss = 0.f;
@@ -157,7 +151,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_a4_kernel(const Gem
     {
         uint32_t* xw = reinterpret_cast<uint32_t*>(xf);
         bool bad = false;
-        for (int k = threadIdx.x * 4; k < p.K; k += THREADS * 4) {     // K % 128 == 0: whole warps
+        for (int k = threadIdx.x * 4; k < p.K; k += THREADS * 4) {
             float4 x = *reinterpret_cast<const float4*>(p.x + k);
             if (p.norm_gain) {
                 const uint2 gg = *reinterpret_cast<const uint2*>(p.norm_gain + k);
@@ -167,94 +161,64 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_a4_kernel(const Gem
                 x.w = x.w * scl * bf16hi(gg.y);
             }
             bad |= fabsf(x.x) > 65504.f || fabsf(x.y) > 65504.f || fabsf(x.z) > 65504.f || fabsf(x.w) > 65504.f;
-            // value k = 32 g + 16 j + r: pair (r & 7) / 2 of k step j, half r / 8 of the fragment
+            // value k = 32 g + 16 j + r: pair (r & 7) / 2 of k step j, half r / 8 of the entry
             const int g = k >> 5, j = (k >> 4) & 1, r = k & 15;
             const int tt = (r & 7) >> 1, e = r >> 3;
-            const float v[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-                const float a = v[2 * pr], b = v[2 * pr + 1];
-                const __half2 hi = __floats2half2_rn(a, b);
-                const float2 hf = __half22float2(hi);
-                const __half2 lo = __floats2half2_rn(a - hf.x, b - hf.y);
-                const int base = ((g * 2 + j) * 2) * 4 + tt + pr;        // entry (g, j, hl = 0, t)
-                xw[(base) * 2 + e] = *reinterpret_cast<const uint32_t*>(&hi);
-                xw[(base + 4) * 2 + e] = *reinterpret_cast<const uint32_t*>(&lo);   // hl = 1
-            }
-            // the group's sum over its eight threads (lanes 8m .. 8m + 7)
-            float sx = x.x + x.y + x.z + x.w;
-            sx += __shfl_xor_sync(0xffffffffu, sx, 1);
-            sx += __shfl_xor_sync(0xffffffffu, sx, 2);
-            sx += __shfl_xor_sync(0xffffffffu, sx, 4);
-            if ((threadIdx.x & 7) == 0) gsum[g] = sx;
+            const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
+            const int base = (g * 2 + j) * 4 + tt;
+            xw[base * 2 + e] = *reinterpret_cast<const uint32_t*>(&h0);
+            xw[(base + 1) * 2 + e] = *reinterpret_cast<const uint32_t*>(&h1);
         }
         if (bad) set_status(p.status, Q3_STATUS_F16_RANGE);
     }
     __syncthreads();
 
-    const int hl = lane >> 2;                    // A row of this lane: 0 high part, 1 remainder
     for (; unit < n_units; unit += gridDim.x) {
-        float acc0 = 0.f, acc1 = 0.f;            // rows 2t and 2t + 1 (lanes 0..3)
+        const bool more = unit + (int)gridDim.x < n_units;
+        const A4Tile nxt = more ? locate_a4(p, (unit + gridDim.x) * R + slot) : cur;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};       // row 0 of D: lanes 0..3 hold rows 2t, 2t + 1
         for (int blk0 = b0; blk0 < b1; blk0 += BPL) {
-            uint4 c[BPL];
-            uint32_t sbv[BPL];
-#pragma unroll
-            for (int u = 0; u < BPL; ++u) { c[u] = cw[u]; sbv[u] = sbw[u]; }
-            // the next blocks of this tile (or the next unit's first) go out now
-            if (blk0 + BPL < b1) {
-                issue(cur, blk0 + BPL);
-            } else if (unit + (int)gridDim.x < n_units) {
-                cur = locate_a4(p, (unit + gridDim.x) * R + slot);
-                issue(cur, b0);
-            }
 #pragma unroll
             for (int u = 0; u < BPL; ++u) {
                 const int b = blk0 + u;
                 if (b >= b1) break;
-                const uint32_t wq[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+                const uint4 c = cw[u], sv = sbw[u];
+                if (b + BPL < b1) load(cur, b + BPL, u);
+                else if (more) load(nxt, b0 + u, u);
+                const uint32_t wq[4] = {c.x, c.y, c.z, c.w};
+                const uint32_t sq[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int g = b * 4 + q;
-                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    const __half2 sb2 = *reinterpret_cast<const __half2*>(&sq[q]);
+                    const __half2 sc = __low2half2(sb2), bi = __high2half2(sb2);
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         uint2 a = make_uint2(0u, 0u);
-                        if (lane < 8) a = xf[((g * 2 + j) * 2 + hl) * 4 + t];
-                        mma_f16(d, a.x, a.y, code_pair(wq[q], 2 * j), code_pair(wq[q], 2 * j + 1));
-                    }
-                    // rows 0 and 1 of D: high-part and remainder products of rows 2t, 2t + 1
-                    const float r0 = d[0] + __shfl_xor_sync(0xffffffffu, d[0], 4);
-                    const float r1 = d[1] + __shfl_xor_sync(0xffffffffu, d[1], 4);
-                    // (scale, bias) of rows 2t, 2t + 1 in group q: words 8t + 2q (+1) of the block
-                    const uint32_t sbq0 = __shfl_sync(0xffffffffu, sbv[u], 8 * t + 2 * q);
-                    const uint32_t sbq1 = __shfl_sync(0xffffffffu, sbv[u], 8 * t + 2 * q + 1);
-                    if (out_lane) {
-                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&sbq0));
-                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&sbq1));
-                        const float sx = gsum[g];
-                        acc0 = fmaf(f0.x, r0, fmaf(f0.y, sx, acc0));
-                        acc1 = fmaf(f1.x, r1, fmaf(f1.y, sx, acc1));
+                        if (lane < 4) a = xf[(g * 2 + j) * 4 + t];
+                        mma_f16(d, a.x, a.y, weight_pair(wq[q], 2 * j, sc, bi),
+                                weight_pair(wq[q], 2 * j + 1, sc, bi));
                     }
                 }
             }
         }
-        // rows of the tile: lane t holds rows 2t, 2t + 1; warps of a tile sum in order
-        if (out_lane) {
-            red[warp * 8 + 2 * t] = acc0;
-            red[warp * 8 + 2 * t + 1] = acc1;
+        // rows of the tile: lane t (< 4) holds rows 2t, 2t + 1; warps of a tile sum in order
+        if (lane < 4) {
+            red[warp * 8 + 2 * t] = d[0];
+            red[warp * 8 + 2 * t + 1] = d[1];
         }
         __syncthreads();
         const int tile0 = unit * R;
         if (p.pair) {
-            // slots 2i (gate) and 2i + 1 (up) cover rows tile (unit R / 2 + i) of each
+            // slots 2i (gate) and 2i + 1 (up) cover the same rows
             for (int i = threadIdx.x; i < (R / 2) * 8; i += THREADS) {
                 const int pr = i >> 3, r = i & 7;
-                float g = 0.f, u = 0.f;
+                float gv = 0.f, uv = 0.f;
                 for (int s2 = 0; s2 < S; ++s2) {
-                    g += red[((2 * pr) * S + s2) * 8 + r];
-                    u += red[((2 * pr + 1) * S + s2) * 8 + r];
+                    gv += red[((2 * pr) * S + s2) * 8 + r];
+                    uv += red[((2 * pr + 1) * S + s2) * 8 + r];
                 }
-                p.out[((tile0 >> 1) + pr) * 8 + r] = silu(g) * u;
+                p.out[((tile0 >> 1) + pr) * 8 + r] = silu(gv) * uv;
             }
         } else {
             for (int i = threadIdx.x; i < R * 8; i += THREADS) {
@@ -267,14 +231,14 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_a4_kernel(const Gem
             }
         }
         __syncthreads();
+        cur = nxt;
     }
     grid_dep_launch();
 }
 
 size_t gemv_a4_smem(int K)
 {
-    const int G = K / 32;
-    return (size_t)G * 16 * 8 + (size_t)G * 4 + WARPS * 8 * 4;
+    return (size_t)(K / 32) * 8 * 8 + WARPS * 8 * 4;
 }
 
 // Derived planes from canonical 20-byte groups [rows][K/32] (16 code bytes:
@@ -308,10 +272,9 @@ __global__ void a4_planes_kernel(const uint8_t* groups, int rows, int K, uint4* 
             out[q] = w;
         }
         codes[i] = make_uint4(out[0], out[1], out[2], out[3]);
-        // word `lane` of the (scale, bias) block: 8 tt + 2 q + rr is group q of row 2 tt + rr
+        // word `lane` of the (scale, bias) block: 4 n + q is group q of row n (lane t = q)
         {
-            const int tt = lane >> 3, q = (lane >> 1) & 3, rr = lane & 1;
-            const uint8_t* rec = groups + ((size_t)(tile * 8 + 2 * tt + rr) * G + blk * 4 + q) * 20;
+            const uint8_t* rec = groups + ((size_t)row * G + blk * 4 + t) * 20;
             sb[tb * 32 + lane] = (uint32_t)rec[16] | ((uint32_t)rec[17] << 8) | ((uint32_t)rec[18] << 16) |
                                  ((uint32_t)rec[19] << 24);
         }
