@@ -383,7 +383,7 @@ int gemm_block_n(int N)
 
 bool gemm_block_n_supported(int bn)
 {
-    return bn == 32 || bn == 64 || bn == 96 || bn == 128 || bn == 192 || bn == 256;
+    return bn == 32 || bn == 64 || bn == 96 || bn == 128 || bn == 160 || bn == 192 || bn == 256;
 }
 
 cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
@@ -394,6 +394,7 @@ cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMa
     case 64: return launch_bn<64>(L, a0, a1, a2, b, g);
     case 96: return launch_bn<96>(L, a0, a1, a2, b, g);
     case 128: return launch_bn<128>(L, a0, a1, a2, b, g);
+    case 160: return launch_bn<160>(L, a0, a1, a2, b, g);
     case 192: return launch_bn<192>(L, a0, a1, a2, b, g);
     case 256: return launch_bn<256>(L, a0, a1, a2, b, g);
     default: return cudaErrorInvalidValue;
