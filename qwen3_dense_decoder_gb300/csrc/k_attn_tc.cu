@@ -12,34 +12,40 @@
 // r = position index r / G, head r % G), so the heads of a group share every
 // K/V tile.  The session's paged K/V is walked in tiles of 128 positions
 // (four blocks through the block table) with an online softmax:
-//   S  = Q K^T        tcgen05.mma, A = Q (shared memory), B = K tile (shared
+//   S  = Q K^T        tcgen05.mma, A = Q (tensor memory), B = K tile (shared
 //                     memory), FP32 accumulator in tensor memory
 //   P  = exp2(S - m)  softmax warps, two threads per row (64 columns each),
-//                     P written back to tensor memory as fp16 pairs
+//                     P written back over its own S columns
 //   O += P V          tcgen05.mma, A = P (tensor memory), B = V tile read
 //                     MN-major from shared memory, FP32 accumulator in TMEM
-// Operands are fp16 (3 more mantissa bits than bf16 for Q and P); the BF16
-// K/V are converted exactly into fp16 swizzled tiles by converter warps.
+// Operands are BF16, so the K/V tiles feed the products exactly as stored,
+// straight from the bulk tensor copies.  Q (fp16) and P enter as high/low
+// BF16 pairs: Q = hi + lo exactly, P to about 16 bits, each product being two
+// MMAs into the same accumulator.
 // The running maximum is raised lazily: O and the row sum are rescaled only
-// when a row maximum grows by more than 2^8, so P <= 256 always fits fp16,
-// and the final O / l is the same quantity.
+// when a row maximum grows by more than 2^8, and the final O / l is the same
+// quantity.
 //
-// K/V pass through a three-stage ring; the Q tile has one buffer, released
-// for the next item once the item's last scores have been computed.
+// K/V pass through a three-stage ring; Q has one tensor-memory buffer,
+// released for the next item once the item's last scores have been computed.
 //
 // Roles (one CTA per SM, items from a host-built per-CTA list):
 //   warp 0       lane 0 issues every MMA and owns the tensor-memory columns
-//   warp 1       lane 0 fetches the K/V blocks of each tile with TMA
+//   warp 1       lane 0 fetches the K/V blocks of each tile with TMA (blocks
+//                past the item's last position, or outside the pool, are
+//                read at a negative row and land as zeros)
 //   warps 4..11  softmax and output: warp w reads TMEM lanes 32 (w % 4) ..
 //                + 32 and columns 64 ((w - 4) / 4) .. + 64 of its row, so two
 //                warps share each row (maxima exchanged through shared memory)
-//   warps 2, 3, 12..19 converters: the Q tile (cp.async); each K/V block of a tile
-//                lands as stored (BF16) in its 128-byte-swizzled place and is
-//                converted to fp16 in place (positions past the tile's last
-//                query position, and blocks not fetched, become zeros)
-// Tensor memory (512 columns): S[2] at 0 / 128, O at 256, P[2] at 384 / 448.
-// Every wait is bounded; a timeout sets the status word and the CTA winds
-// down without touching its remaining items.
+//   warps 12..15 Q: warp w loads the rows of TMEM lanes 32 (w % 4) .. + 32 of
+//                the next item ahead of time and stores their high/low parts
+//                once the buffer is free
+// Tensor memory (512 columns): S[2] at 0 / 128 (P high at +0, low at +64,
+// over S), O at 256, Q high at 384, low at 448.
+// K/V rows past a row's position are finite (the pool is zeroed when it is
+// made, and only finite BF16 values are stored), so P = 0 there contributes
+// nothing.  Every wait is bounded; a timeout sets the status word and the CTA
+// winds down without touching its remaining items.
 #include <algorithm>
 
 #include "common.cuh"
@@ -51,36 +57,34 @@ namespace {
 
 constexpr int D = 128;
 constexpr int BN = 128;                      // key positions per K/V tile
-constexpr int ATOM = 128 * 128;              // one 128-row x 64-column fp16 swizzle atom (bytes)
-constexpr int TILE = 2 * ATOM;               // 128 rows x 128 fp16 (32 KB)
+constexpr int ATOM = 128 * 128;              // one 128-row x 64-column bf16 swizzle atom (bytes)
+constexpr int TILE = 2 * ATOM;               // 128 rows x 128 bf16 (32 KB)
 constexpr int NSOFT = 8;                     // softmax warps (two per TMEM lane quadrant)
-constexpr int SOFT0 = 4, CONV0 = SOFT0 + NSOFT;
-constexpr int NCONV = 10;                    // converter warps: 2, 3 and CONV0 .. CONV0 + 7
-constexpr int THREADS = (CONV0 + NCONV - 2) * 32;
-constexpr int NCT = NCONV * 32;              // converter threads
+constexpr int SOFT0 = 4, QL0 = SOFT0 + NSOFT;
+constexpr int NQL = 4;                       // Q warps (one per TMEM lane quadrant)
+constexpr int THREADS = (QL0 + NQL) * 32;
 constexpr int TMEM_COLS = 512;
-constexpr uint32_t T_S = 0, T_O = 256, T_P = 384;
+constexpr uint32_t T_S = 0, T_O = 256, T_Q = 384;
 constexpr float LAZY = 8.0f;                 // log2 growth of a row maximum tolerated before rescaling
 
 constexpr int NST = 3;                       // K/V ring stages
 
 struct alignas(1024) TcSmem {
-    uint8_t q[TILE];                         // the item's Q tile, released after its last S
     uint8_t k[NST][TILE];
     uint8_t v[NST][TILE];
-    uint64_t q_full, q_free, kv_load[NST], kv_full[NST], kv_free[NST], s_full[2], p_full[2], pv_done[2];
+    uint64_t q_full, q_free, kv_load[NST], kv_free[NST], s_full[2], p_full[2], pv_done[2];
     uint64_t o_free, drain, pair[4];
-    int blk_ok[NST][BN / 32];                // blocks of the tile the loader fetched
     float xch[2][128];                       // [column half][row] maxima, then row sums
     uint32_t tmem;
     int abort;
 };
 constexpr size_t SMEM_BYTES = sizeof(TcSmem) + 1024;
 
-// Instruction descriptors: fp16 A/B, FP32 accumulator, M = 128, N = 128.
-// S: A and B K-major.  PV: B (V, positions x dims) MN-major (bit 16).
-constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128);
-constexpr uint32_t IDESC_PV = idesc_f16_f32(128, 128) | (1u << 16);
+// Instruction descriptors: bf16 A/B (format 1 at [7,10) and [10,13)), FP32
+// accumulator, M = 128, N = 128.  S: B K-major.  PV: B (V, positions x dims)
+// MN-major (bit 16).
+constexpr uint32_t IDESC_S = idesc_f16_f32(128, 128) | (1u << 7) | (1u << 10);
+constexpr uint32_t IDESC_PV = IDESC_S | (1u << 16);
 
 // MN-major 128-byte-swizzled operand: rows of 64 MN elements (128 bytes),
 // 8-row groups 1024 bytes apart along K (stride offset), 64-element MN blocks
@@ -124,26 +128,13 @@ Q3_DEV void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
 }
 Q3_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// generic-proxy shared-memory writes made visible to the tensor cores
-Q3_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-Q3_DEV uint32_t pack_f16(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-Q3_DEV uint4 bf16x8_to_f16x8(uint4 w) {
-    uint4 o;
-    o.x = pack_f16(bf16lo(w.x), bf16hi(w.x));
-    o.y = pack_f16(bf16lo(w.y), bf16hi(w.y));
-    o.z = pack_f16(bf16lo(w.z), bf16hi(w.z));
-    o.w = pack_f16(bf16lo(w.w), bf16hi(w.w));
-    return o;
-}
-
-// byte offset of 16-byte chunk c (8 fp16 along the row) of row r in a
-// 128-row tile of two 64-column 128-byte-swizzled atoms
-Q3_DEV uint32_t sw_off(int r, int c) {
-    return (uint32_t)((c >> 3) * ATOM + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// x as a high/low pair of bf16: hi = bf16(x), lo = bf16(x - hi)
+Q3_DEV void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // Bounded mbarrier wait shared by all roles of the CTA: gives up when another
@@ -185,17 +176,20 @@ Q3_DEV Item item_of(const PrefillAttnArgs& p, int k) {
 // ---------------------------------------------------------------- MMA issuer
 Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0, int i1) {
     uint32_t g = 0;                                  // K/V tiles issued so far by this CTA
+    // S = (Q_hi + Q_lo) K^T: 16 dims a step, the high part's 8 steps, then the low part's
     auto issue_s = [&](uint32_t gt) -> bool {
         const int b = gt & 1, st = gt % NST;
-        if (!wait_bar(&sm.kv_full[st], (gt / NST) & 1, sm, p.status)) return false;
+        if (!wait_bar(&sm.kv_load[st], (gt / NST) & 1, sm, p.status)) return false;
         tc_fence_after();
-        const uint32_t qa = smem_u32(sm.q), ka = smem_u32(sm.k[st]);
+        const uint32_t ka = smem_u32(sm.k[st]);
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s) {
-            const uint32_t off = (s >> 2) * ATOM + (s & 3) * 32;
-            tc_mma_f16(tmem + T_S + b * 128, smem_desc_sw128(qa + off), smem_desc_sw128(ka + off), IDESC_S,
-                       s > 0 ? 1u : 0u);
-        }
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int s = 0; s < D / 16; ++s) {
+                const uint32_t off = (s >> 2) * ATOM + (s & 3) * 32;
+                tc_mma_f16_ts(tmem + T_S + b * 128, tmem + T_Q + part * 64 + s * 8, smem_desc_sw128(ka + off),
+                              IDESC_S, (part > 0 || s > 0) ? 1u : 0u);
+            }
         tc_commit(&sm.s_full[b]);
         return true;
     };
@@ -219,11 +213,15 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
             const int b = g & 1, st = g % NST;
             if (!(ok = wait_bar(&sm.p_full[b], (g >> 1) & 1, sm, p.status))) break;
             tc_fence_after();
+            // O += (P_hi + P_lo) V, 16 positions a step; P lies over S[b]
             const uint32_t va = smem_u32(sm.v[st]);
 #pragma unroll
-            for (int s = 0; s < BN / 16; ++s)          // 16 positions per step
-                tc_mma_f16_ts(tmem + T_O, tmem + T_P + b * 64 + s * 8, smem_desc_sw128_mn(va + s * 2048, ATOM),
-                              IDESC_PV, (t > 0 || s > 0) ? 1u : 0u);
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int s = 0; s < BN / 16; ++s)
+                    tc_mma_f16_ts(tmem + T_O, tmem + T_S + b * 128 + part * 64 + s * 8,
+                                  smem_desc_sw128_mn(va + s * 2048, ATOM), IDESC_PV,
+                                  (t > 0 || part > 0 || s > 0) ? 1u : 0u);
             tc_commit(&sm.pv_done[b]);
             tc_commit(&sm.kv_free[st]);
         }
@@ -243,8 +241,10 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
 
 // ---------------------------------------------------------------- K/V loader
 // One thread fetches each tile's blocks once the PV NST tiles back has
-// released the stage, up to NST tiles ahead of the converters: per block, K
-// and V as two 64-column boxes of 32 positions each.
+// released the stage, up to NST tiles ahead: per block, K and V as two
+// 64-column boxes of 32 positions each, into their 128-byte-swizzled places.
+// A block past the item's last position (or whose table entry is outside
+// the pool) is read at row -32, wholly outside the tensor, and lands as zeros.
 Q3_DEV void load_role(const PrefillAttnArgs& p, const CUtensorMap* tkv, TcSmem& sm, int i0, int i1) {
     uint32_t g = 0;
     for (int k = i0; k < i1; ++k) {
@@ -253,28 +253,21 @@ Q3_DEV void load_role(const PrefillAttnArgs& p, const CUtensorMap* tkv, TcSmem& 
             const int b = g % NST;
             if (g >= NST && !wait_bar(&sm.kv_free[b], (g / NST - 1) & 1, sm, p.status)) return;
             int phys[BN / 32];
-            uint32_t bytes = 0;
 #pragma unroll
             for (int j = 0; j < BN / 32; ++j) {
                 const int kp = t * BN + 32 * j;
                 phys[j] = -1;
                 if (kp <= it.pos_last) {
                     const int ph = it.table[kp >> 5];
-                    if (ph >= 0 && ph < p.n_blocks) {
-                        phys[j] = ph;
-                        bytes += 4 * 32 * 64 * 2;
-                    } else {
-                        set_status(p.status, Q3_STATUS_BLOCK_RANGE);
-                    }
+                    if (ph >= 0 && ph < p.n_blocks) phys[j] = ph;
+                    else set_status(p.status, Q3_STATUS_BLOCK_RANGE);
                 }
-                sm.blk_ok[b][j] = phys[j] >= 0;
             }
-            mbar_arrive_expect_tx(&sm.kv_load[b], bytes);
+            mbar_arrive_expect_tx(&sm.kv_load[b], 2 * TILE);
 #pragma unroll
             for (int j = 0; j < BN / 32; ++j) {
-                if (phys[j] < 0) continue;
-                const int rk = p.kv_row0 + ((phys[j] * 2) * p.n_kv + it.kvh) * 32;
-                const int rv = rk + p.n_kv * 32;
+                const int rk = phys[j] < 0 ? -32 : p.kv_row0 + ((phys[j] * 2) * p.n_kv + it.kvh) * 32;
+                const int rv = phys[j] < 0 ? -32 : rk + p.n_kv * 32;
                 tma_load_2d(sm.k[b] + j * 32 * 128, tkv, &sm.kv_load[b], 0, rk);
                 tma_load_2d(sm.k[b] + ATOM + j * 32 * 128, tkv, &sm.kv_load[b], 64, rk);
                 tma_load_2d(sm.v[b] + j * 32 * 128, tkv, &sm.kv_load[b], 0, rv);
@@ -284,50 +277,44 @@ Q3_DEV void load_role(const PrefillAttnArgs& p, const CUtensorMap* tkv, TcSmem& 
     }
 }
 
-// ---------------------------------------------------------------- converters
-Q3_DEV void convert_role(const PrefillAttnArgs& p, TcSmem& sm, int i0, int i1) {
-    const int ct = threadIdx.x < CONV0 * 32 ? threadIdx.x - 64 : threadIdx.x - CONV0 * 32 + 64;
+// ---------------------------------------------------------------- Q
+// Warp w holds TMEM lanes 32 (w % 4) .. + 32: lane l's row r is position
+// index r / G, head r % G of the item (padding rows repeat row 0).  The next
+// item's rows are loaded while the current item's scores still read the
+// buffer; once the last of them is done the high and low parts are stored.
+Q3_DEV void q_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0, int i1) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp & 3, row = quad * 32 + lane;
     const int G = p.n_q / p.n_kv, R = 128 / G;
     const int qw = p.n_q * D;
-    uint32_t g = 0;
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
     for (int k = i0, local = 0; k < i1; ++k, ++local) {
         const Item it = item_of(p, k);
+        int ir = row / G, hh = row % G;
+        if (ir >= R) ir = hh = 0;
+        const int src_row = it.row0 + min(ir, it.nrows - 1);
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + (size_t)src_row * qw + (it.kvh * G + hh) * D);
+        uint4 qv[D / 8];
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) qv[c] = __ldcg(src + c);
         if (local >= 1 && !wait_bar(&sm.q_free, (local - 1) & 1, sm, p.status)) return;
-        // Q tile: row r = position index r / G, head r % G (padding rows repeat row 0)
-        for (int i = ct; i < 128 * 16; i += NCT) {
-            const int r = i >> 4, c = i & 15;
-            int ir = r / G, hh = r % G;
-            if (ir >= R) ir = hh = 0;
-            const int src_row = it.row0 + min(ir, it.nrows - 1);
-            cp_async_16(sm.q + sw_off(r, c), p.q + (size_t)src_row * qw + (it.kvh * G + hh) * D + c * 8);
-        }
-        cp_async_commit();
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(&sm.q_full);
-
-        for (int t = 0; t < it.n_kt; ++t, ++g) {
-            const int b = g % NST;
-            if (!wait_bar(&sm.kv_load[b], (g / NST) & 1, sm, p.status)) return;
-            // each thread converts its chunks in place (zeros where nothing valid was fetched)
-#pragma unroll 2
-            for (int i = ct; i < BN * 16; i += NCT) {
-                const int key = i >> 4;
-                const uint32_t off = sw_off(key, i & 15);
-                uint4* pk_ = reinterpret_cast<uint4*>(sm.k[b] + off);
-                uint4* pv_ = reinterpret_cast<uint4*>(sm.v[b] + off);
-                if (sm.blk_ok[b][key >> 5] && t * BN + key <= it.pos_last) {
-                    const uint4 wk = *pk_, wv = *pv_;
-                    *pk_ = bf16x8_to_f16x8(wk);
-                    *pv_ = bf16x8_to_f16x8(wv);
-                } else {
-                    *pk_ = make_uint4(0, 0, 0, 0);
-                    *pv_ = make_uint4(0, 0, 0, 0);
-                }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {                      // 32 dims (16 columns) at a time
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const uint4 w = qv[c * 4 + e / 4];
+                const uint32_t h2 = (&w.x)[e & 3];
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+                split_bf16(f.x, f.y, hi[e], lo[e]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&sm.kv_full[b]);
+            tmem_st_32x32b_x16(tl + T_Q + c * 16, hi);
+            tmem_st_32x32b_x16(tl + T_Q + 64 + c * 16, lo);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.q_full);
     }
 }
 
@@ -410,23 +397,22 @@ Q3_DEV void softmax_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, in
                 l *= alpha;
                 m_used = m_new;
             }
-            // P[b] was last read by the PV two tiles back
-            if (g >= 2) {
-                if (!wait_bar(&sm.pv_done[b], ((g >> 1) - 1) & 1, sm, p.status)) return;
-                tc_fence_after();
-            }
+            // P over S[b]: both warps of the row read their S columns before the
+            // maxima were exchanged, and the PV two tiles back that read P there
+            // ran before these scores (the tensor cores keep issue order)
             float sum = 0.f;
 #pragma unroll
             for (int hq = 0; hq < 2; ++hq) {
-                uint32_t pk[16];
+                uint32_t ph[16], pl[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const float p0 = ex2(fmaf(__uint_as_float(v[hq][2 * e]), scale, -m_used));
                     const float p1 = ex2(fmaf(__uint_as_float(v[hq][2 * e + 1]), scale, -m_used));
                     sum += p0 + p1;
-                    pk[e] = pack_f16(p0, p1);
+                    split_bf16(p0, p1, ph[e], pl[e]);
                 }
-                tmem_st_32x32b_x16(tl + T_P + b * 64 + c0 / 2 + 16 * hq, pk);
+                tmem_st_32x32b_x16(tl + T_S + b * 128 + c0 / 2 + 16 * hq, ph);
+                tmem_st_32x32b_x16(tl + T_S + b * 128 + 64 + c0 / 2 + 16 * hq, pl);
             }
             tmem_st_wait();
             l += sum;
@@ -480,11 +466,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_attn_tc_kernel(const __gri
     TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        mbar_init(&sm.q_full, NCT);
+        mbar_init(&sm.q_full, NQL * 32);
         mbar_init(&sm.q_free, 1);
         for (int b = 0; b < NST; ++b) {
             mbar_init(&sm.kv_load[b], 1);
-            mbar_init(&sm.kv_full[b], NCT);
             mbar_init(&sm.kv_free[b], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -518,8 +503,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_attn_tc_kernel(const __gri
         __syncwarp();
     } else if (warp >= SOFT0 && warp < SOFT0 + NSOFT) {
         softmax_role(p, sm, tmem, i0, i1);
-    } else if (warp >= CONV0 || warp == 2 || warp == 3) {
-        convert_role(p, sm, i0, i1);
+    } else if (warp >= QL0) {
+        q_role(p, sm, tmem, i0, i1);
     }
     tc_fence_before();
     __syncthreads();

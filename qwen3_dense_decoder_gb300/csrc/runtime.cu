@@ -481,7 +481,9 @@ int attention_splits(const q3_model* m, int T, int max_ctx)
 // (shared-memory reads of the A and B tiles at 128 bytes per cycle), the L2
 // time of those tiles and the HBM time of the weight tile (one read shared
 // by the n tiles); units run in rounds of 152 (one persistent CTA per SM);
-// split-K adds a reduction.
+// split-K adds a reduction.  Tiles that fill the SMs take 1, 2 or 4 splits;
+// fewer tiles (the weight-streaming GEMMs of batched decode rounds) any count
+// up to 8, so that every SM streams a share of the weights.
 void plan_gemm_impl(int M, int N, int K, size_t ws_elems, int* bn, int* splits)
 {
     const int kb = K / 64;
@@ -491,7 +493,9 @@ void plan_gemm_impl(int M, int N, int K, size_t ws_elems, int* bn, int* splits)
     for (int b : cand) {
         if (b > gemm_block_n(N)) break;                  // wider than the rows need
         const int tiles = (M / 128) * ((N + b - 1) / b);
-        for (int s = 1; s <= 4; s *= 2) {
+        const bool few = tiles < 152;
+        for (int s = 1; s <= (few ? 8 : 4); s += (few || s == 1) ? 1 : s) {
+            if (!few && s == 3) continue;
             if (s > 1 && (kb / s < 4 || (size_t)s * N * M > ws_elems)) break;
             const int rounds = (tiles * s + 151) / 152;
             // weight tile bytes from HBM per k-block, shared by the n tiles that
