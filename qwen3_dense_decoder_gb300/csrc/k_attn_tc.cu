@@ -26,14 +26,16 @@
 // when a row maximum grows by more than 2^8, and the final O / l is the same
 // quantity.
 //
-// K/V pass through a three-stage ring; Q has one tensor-memory buffer,
+// K and V pass through three-stage rings; Q has one tensor-memory buffer,
 // released for the next item once the item's last scores have been computed.
 //
 // Roles (one CTA per SM, items from a host-built per-CTA list):
 //   warp 0       lane 0 issues every MMA and owns the tensor-memory columns
-//   warp 1       lane 0 fetches the K/V blocks of each tile with TMA (blocks
-//                past the item's last position, or outside the pool, are
-//                read at a negative row and land as zeros)
+//   warps 1, 2   lane 0 fetches the K (warp 1) or V (warp 2) blocks of each
+//                tile with TMA (blocks past the item's last position, or
+//                outside the pool, are read at a negative row and land as
+//                zeros); a K stage is free again once its scores are done, a
+//                V stage once its PV is
 //   warps 4..11  softmax and output: warp w reads TMEM lanes 32 (w % 4) ..
 //                + 32 and columns 64 ((w - 4) / 4) .. + 64 of its row, so two
 //                warps share each row (maxima exchanged through shared memory)
@@ -72,7 +74,7 @@ constexpr int NST = 3;                       // K/V ring stages
 struct alignas(1024) TcSmem {
     uint8_t k[NST][TILE];
     uint8_t v[NST][TILE];
-    uint64_t q_full, q_free, kv_load[NST], kv_free[NST], s_full[2], p_full[2], pv_done[2];
+    uint64_t q_full, q_free, k_load[NST], k_free[NST], v_load[NST], v_free[NST], s_full[2], p_full[2], pv_done[2];
     uint64_t o_free, drain, pair[4];
     float xch[2][128];                       // [column half][row] maxima, then row sums
     uint32_t tmem;
@@ -179,7 +181,7 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
     // S = (Q_hi + Q_lo) K^T: 16 dims a step, the high part's 8 steps, then the low part's
     auto issue_s = [&](uint32_t gt) -> bool {
         const int b = gt & 1, st = gt % NST;
-        if (!wait_bar(&sm.kv_load[st], (gt / NST) & 1, sm, p.status)) return false;
+        if (!wait_bar(&sm.k_load[st], (gt / NST) & 1, sm, p.status)) return false;
         tc_fence_after();
         const uint32_t ka = smem_u32(sm.k[st]);
 #pragma unroll
@@ -191,6 +193,7 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
                               IDESC_S, (part > 0 || s > 0) ? 1u : 0u);
             }
         tc_commit(&sm.s_full[b]);
+        tc_commit(&sm.k_free[st]);
         return true;
     };
     bool ok = true;
@@ -212,6 +215,7 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
             if (t == 0 && local > 0 && !(ok = wait_bar(&sm.o_free, (local - 1) & 1, sm, p.status))) break;
             const int b = g & 1, st = g % NST;
             if (!(ok = wait_bar(&sm.p_full[b], (g >> 1) & 1, sm, p.status))) break;
+            if (!(ok = wait_bar(&sm.v_load[st], (g / NST) & 1, sm, p.status))) break;
             tc_fence_after();
             // O += (P_hi + P_lo) V, 16 positions a step; P lies over S[b]
             const uint32_t va = smem_u32(sm.v[st]);
@@ -223,7 +227,7 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
                                   smem_desc_sw128_mn(va + s * 2048, ATOM), IDESC_PV,
                                   (t > 0 || part > 0 || s > 0) ? 1u : 0u);
             tc_commit(&sm.pv_done[b]);
-            tc_commit(&sm.kv_free[st]);
+            tc_commit(&sm.v_free[st]);
         }
         if (!ok) break;
         // the next item's first scores (g is its first tile)
@@ -239,39 +243,41 @@ Q3_DEV void mma_role(const PrefillAttnArgs& p, TcSmem& sm, uint32_t tmem, int i0
     mbar_wait(&sm.drain, 0, p.status);
 }
 
-// ---------------------------------------------------------------- K/V loader
-// One thread fetches each tile's blocks once the PV NST tiles back has
-// released the stage, up to NST tiles ahead: per block, K and V as two
-// 64-column boxes of 32 positions each, into their 128-byte-swizzled places.
-// A block past the item's last position (or whose table entry is outside
-// the pool) is read at row -32, wholly outside the tensor, and lands as zeros.
-Q3_DEV void load_role(const PrefillAttnArgs& p, const CUtensorMap* tkv, TcSmem& sm, int i0, int i1) {
+// ---------------------------------------------------------------- K/V loaders
+// One thread fetches the K (which = 0) or V (which = 1) blocks of each tile,
+// up to NST tiles ahead: per block two 64-column boxes of 32 positions into
+// their 128-byte-swizzled places.  The tile's block-table entries are read
+// before the stage is waited for.  A block past the item's last position (or
+// whose table entry is outside the pool) is read at row -32, wholly outside
+// the tensor, and lands as zeros.
+Q3_DEV void load_role(const PrefillAttnArgs& p, const CUtensorMap* tkv, TcSmem& sm, int i0, int i1, int which) {
+    uint64_t* ld = which ? sm.v_load : sm.k_load;
+    uint64_t* fr = which ? sm.v_free : sm.k_free;
     uint32_t g = 0;
     for (int k = i0; k < i1; ++k) {
         const Item it = item_of(p, k);
         for (int t = 0; t < it.n_kt; ++t, ++g) {
             const int b = g % NST;
-            if (g >= NST && !wait_bar(&sm.kv_free[b], (g / NST - 1) & 1, sm, p.status)) return;
-            int phys[BN / 32];
+            int row[BN / 32];
 #pragma unroll
             for (int j = 0; j < BN / 32; ++j) {
                 const int kp = t * BN + 32 * j;
-                phys[j] = -1;
+                row[j] = -32;
                 if (kp <= it.pos_last) {
                     const int ph = it.table[kp >> 5];
-                    if (ph >= 0 && ph < p.n_blocks) phys[j] = ph;
-                    else set_status(p.status, Q3_STATUS_BLOCK_RANGE);
+                    if (ph >= 0 && ph < p.n_blocks)
+                        row[j] = p.kv_row0 + ((ph * 2 + which) * p.n_kv + it.kvh) * 32;
+                    else if (which == 0)
+                        set_status(p.status, Q3_STATUS_BLOCK_RANGE);
                 }
             }
-            mbar_arrive_expect_tx(&sm.kv_load[b], 2 * TILE);
+            if (g >= NST && !wait_bar(&fr[b], (g / NST - 1) & 1, sm, p.status)) return;
+            uint8_t* dst = which ? sm.v[b] : sm.k[b];
+            mbar_arrive_expect_tx(&ld[b], TILE);
 #pragma unroll
             for (int j = 0; j < BN / 32; ++j) {
-                const int rk = phys[j] < 0 ? -32 : p.kv_row0 + ((phys[j] * 2) * p.n_kv + it.kvh) * 32;
-                const int rv = phys[j] < 0 ? -32 : rk + p.n_kv * 32;
-                tma_load_2d(sm.k[b] + j * 32 * 128, tkv, &sm.kv_load[b], 0, rk);
-                tma_load_2d(sm.k[b] + ATOM + j * 32 * 128, tkv, &sm.kv_load[b], 64, rk);
-                tma_load_2d(sm.v[b] + j * 32 * 128, tkv, &sm.kv_load[b], 0, rv);
-                tma_load_2d(sm.v[b] + ATOM + j * 32 * 128, tkv, &sm.kv_load[b], 64, rv);
+                tma_load_2d(dst + j * 32 * 128, tkv, &ld[b], 0, row[j]);
+                tma_load_2d(dst + ATOM + j * 32 * 128, tkv, &ld[b], 64, row[j]);
             }
         }
     }
@@ -469,8 +475,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_attn_tc_kernel(const __gri
         mbar_init(&sm.q_full, NQL * 32);
         mbar_init(&sm.q_free, 1);
         for (int b = 0; b < NST; ++b) {
-            mbar_init(&sm.kv_load[b], 1);
-            mbar_init(&sm.kv_free[b], 1);
+            mbar_init(&sm.k_load[b], 1);
+            mbar_init(&sm.k_free[b], 1);
+            mbar_init(&sm.v_load[b], 1);
+            mbar_init(&sm.v_free[b], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.s_full[b], 1);
@@ -498,8 +506,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_attn_tc_kernel(const __gri
     if (warp == 0) {
         if ((threadIdx.x & 31) == 0) mma_role(p, sm, tmem, i0, i1);
         __syncwarp();
-    } else if (warp == 1) {
-        if ((threadIdx.x & 31) == 0) load_role(p, &tkv, sm, i0, i1);
+    } else if (warp == 1 || warp == 2) {
+        if ((threadIdx.x & 31) == 0) load_role(p, &tkv, sm, i0, i1, warp - 1);
         __syncwarp();
     } else if (warp >= SOFT0 && warp < SOFT0 + NSOFT) {
         softmax_role(p, sm, tmem, i0, i1);

@@ -248,10 +248,32 @@ __global__ void __launch_bounds__(1024) argmax_kernel(const ArgmaxArgs a)
     const float* x = a.logits + (size_t)blockIdx.x * a.V;
     float best = -INFINITY;
     int bi = 0x7fffffff;
-    for (int i = threadIdx.x; i < a.V; i += blockDim.x) {
-        const float v = x[i];
-        if (v > best) { best = v; bi = i; }      // ascending i: first max kept
+    auto take = [&](float v, int i) {
+        if (v > best) { best = v; bi = i; }      // ascending i per thread: first max kept
+    };
+    int tail = 0;
+    if ((a.V & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        // 16-byte loads, four in flight per thread (the row is one CTA's)
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        const int n4 = a.V / 4, T = blockDim.x;
+        int c = threadIdx.x;
+        for (; c + 3 * T < n4; c += 4 * T) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldcg(x4 + c + u * T);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = 4 * (c + u * T);
+                take(v[u].x, i); take(v[u].y, i + 1); take(v[u].z, i + 2); take(v[u].w, i + 3);
+            }
+        }
+        for (; c < n4; c += T) {
+            const float4 v = __ldcg(x4 + c);
+            take(v.x, 4 * c); take(v.y, 4 * c + 1); take(v.z, 4 * c + 2); take(v.w, 4 * c + 3);
+        }
+        tail = a.V;
     }
+    for (int i = tail + threadIdx.x; i < a.V; i += blockDim.x) take(x[i], i);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, best, o);
