@@ -192,10 +192,23 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
     const float qscale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
     if (FUSED) {
         const int n_heads = p.n_q + 2 * p.n_kv;
-        const float* row = p.qkv + (size_t)t * n_heads * D;
+        const size_t row0 = (size_t)t * n_heads * D;
         const float2* rope_row = p.rope + (size_t)pos * (D / 2);
+        // four projections of this row's head h: stored, or the QKV GEMM's
+        // split-K partials summed in split order (the values its reduce stores)
+        auto head4 = [&](int h) -> float4 {
+            const size_t o = row0 + (size_t)h * D + lane * 4;
+            if (p.qkv_splits <= 1) return *reinterpret_cast<const float4*>(p.qkv + o);
+            const size_t slab = (size_t)p.T * n_heads * D;
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < p.qkv_splits; ++sp) {
+                const float4 w = __ldcg(reinterpret_cast<const float4*>(p.qkv_ws + sp * slab + o));
+                s.x += w.x; s.y += w.y; s.z += w.z; s.w += w.w;
+            }
+            return s;
+        };
         for (int g = warp; g < G; g += AWARPS) {
-            const float4 v = *reinterpret_cast<const float4*>(row + (kvh * G + g) * D + lane * 4);
+            const float4 v = head4(kvh * G + g);
             float y[4] = {v.x, v.y, v.z, v.w};
             head_norm_rope(y, p.q_gain, rope_row, p.eps, lane);
             store_q_split<KQ>(sqa, g, y, qscale, lane);
@@ -203,8 +216,7 @@ __global__ void __launch_bounds__(AWARPS * 32, 3) attn_kernel(const AttnArgs p)
         const bool mine = b0 <= last_blk && last_blk < b1;   // this split holds the new position
         if (mine && warp >= AWARPS - 2) {
             const bool is_k = warp == AWARPS - 2;
-            const float4 v = *reinterpret_cast<const float4*>(
-                row + (p.n_q + (is_k ? 0 : p.n_kv) + kvh) * D + lane * 4);
+            const float4 v = head4(p.n_q + (is_k ? 0 : p.n_kv) + kvh);
             float y[4] = {v.x, v.y, v.z, v.w};
             if (is_k) head_norm_rope(y, p.k_gain, rope_row, p.eps, lane);
             const int phys = table[last_blk];

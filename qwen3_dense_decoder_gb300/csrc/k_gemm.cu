@@ -347,6 +347,92 @@ __global__ void gemm_splitk_reduce_kernel(const GemmArgs p)
     }
     if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
 }
+// Split-K finish of a residual-add GEMM fused with the RMSNorm that follows
+// it (batched decode rounds: O, then the FFN norm; down, then the next
+// layer's attention norm).  One CTA per token row: the partials summed in
+// split order and added to the residual row (the values gemm_splitk_reduce
+// would store), the row written back, then its RMSNorm with gain g as fp16.
+constexpr int ADDNORM_THREADS = 256, ADDNORM_VEC = 5;
+
+__global__ void __launch_bounds__(ADDNORM_THREADS) gemm_splitk_add_norm_kernel(const GemmArgs p,
+                                                                               const __nv_bfloat16* g,
+                                                                               float eps, __half* h)
+{
+    __shared__ float red[ADDNORM_THREADS / 32];
+    __shared__ float s_scale;
+    grid_dep_wait();
+    const int n = blockIdx.x, H = p.M;
+    const size_t slab = (size_t)p.N * p.M;
+    float* x = reinterpret_cast<float*>(p.out) + (size_t)n * p.ldo;
+    const float* w0 = p.ws + (size_t)n * p.M;
+    float4 v[ADDNORM_VEC];
+#pragma unroll
+    for (int k = 0; k < ADDNORM_VEC; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // four splits' loads in flight at a time, added in split order
+    for (int s0 = 0; s0 < p.k_splits; s0 += 4) {
+        float4 t[4][ADDNORM_VEC];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int k = 0; k < ADDNORM_VEC; ++k) {
+                const int i = (threadIdx.x + k * ADDNORM_THREADS) * 4;
+                t[j][k] = s0 + j < p.k_splits && i < H
+                              ? __ldcg(reinterpret_cast<const float4*>(w0 + (size_t)(s0 + j) * slab + i))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (s0 + j < p.k_splits) {
+#pragma unroll
+                for (int k = 0; k < ADDNORM_VEC; ++k) {
+                    v[k].x += t[j][k].x; v[k].y += t[j][k].y; v[k].z += t[j][k].z; v[k].w += t[j][k].w;
+                }
+            }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < ADDNORM_VEC; ++k) {
+        const int i = (threadIdx.x + k * ADDNORM_THREADS) * 4;
+        if (i < H) {
+            const float4 o = *reinterpret_cast<const float4*>(x + i);
+            v[k] = make_float4(o.x + v[k].x, o.y + v[k].y, o.z + v[k].z, o.w + v[k].w);
+            *reinterpret_cast<float4*>(x + i) = v[k];
+            ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+        }
+    }
+    grid_dep_launch();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < ADDNORM_THREADS / 32; ++w) t += red[w];
+        s_scale = 1.0f / sqrtf(t / (float)H + eps);
+    }
+    __syncthreads();
+    const float sc = s_scale;
+    __half* hr = h + (size_t)n * H;
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < ADDNORM_VEC; ++k) {
+        const int i = (threadIdx.x + k * ADDNORM_THREADS) * 4;
+        if (i < H) {
+            const uint2 gg = *reinterpret_cast<const uint2*>(g + i);
+            __half2 lo, hi;
+            lo.x = to_f16(v[k].x * sc * bf16lo(gg.x), bad);
+            lo.y = to_f16(v[k].y * sc * bf16hi(gg.x), bad);
+            hi.x = to_f16(v[k].z * sc * bf16lo(gg.y), bad);
+            hi.y = to_f16(v[k].w * sc * bf16hi(gg.y), bad);
+            uint2 o;
+            o.x = *reinterpret_cast<const uint32_t*>(&lo);
+            o.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(hr + i) = o;
+        }
+    }
+    if (bad) set_status(p.status, Q3_STATUS_F16_RANGE);
+}
+
 template <int BN>
 cudaError_t launch_bn(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
                       const CUtensorMap& a2, const CUtensorMap& b, const GemmArgs& g)
@@ -418,6 +504,29 @@ cudaError_t launch_gemm_splitk_reduce(const Launch& L, const GemmArgs& g)
     cfg.numAttrs = 1;
     if (L.counter) ++*L.counter;
     return cudaLaunchKernelEx(&cfg, gemm_splitk_reduce_kernel, g);
+}
+
+bool gemm_add_norm_ok(const GemmArgs& g)
+{
+    return g.k_splits > 1 && !g.pair && g.epi == EPI_ADD_F32 && g.M % 4 == 0 && g.ldo % 4 == 0 &&
+           g.M <= ADDNORM_THREADS * 4 * ADDNORM_VEC;
+}
+
+cudaError_t launch_gemm_splitk_add_norm(const Launch& L, const GemmArgs& g, const __nv_bfloat16* gain, float eps,
+                                        __half* h)
+{
+    if (!gemm_add_norm_ok(g)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g.N);
+    cfg.blockDim = dim3(ADDNORM_THREADS);
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (L.counter) ++*L.counter;
+    return cudaLaunchKernelEx(&cfg, gemm_splitk_add_norm_kernel, g, gain, eps, h);
 }
 
 }  // namespace q3

@@ -82,6 +82,12 @@ cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMa
                         const CUtensorMap& a2, const CUtensorMap& b, int bn,
                         const GemmArgs& g);
 cudaError_t launch_gemm_splitk_reduce(const Launch& L, const GemmArgs& g);
+// Split-K finish of a residual-add GEMM (plain rows, EPI_ADD_F32, M <= 5120)
+// fused with the RMSNorm of the updated rows: out[n] += sum of the partials
+// in split order, then h[n] = fp16(RMSNorm(out[n]) * gain), one CTA a row.
+bool gemm_add_norm_ok(const GemmArgs& g);
+cudaError_t launch_gemm_splitk_add_norm(const Launch& L, const GemmArgs& g, const __nv_bfloat16* gain, float eps,
+                                        __half* h);
 
 // Weights the next launch will stream: up to three contiguous ranges that a
 // kernel prefetches into L2 (a capped prefix, split over its CTAs) so HBM
@@ -161,6 +167,8 @@ cudaError_t launch_qk_norm_rope_append(const Launch& L, const RopeArgs& a);
 struct AttnArgs {
     const float* q;            // [T][n_q][128], normed and rotated (unfused rounds)
     const float* qkv;          // [T][(n_q + 2 n_kv) 128] raw projections (fused decode rounds)
+    const float* qkv_ws;       // or, with qkv_splits > 1, the QKV GEMM's split-K partials
+    int qkv_splits;            // ([split][T][(n_q + 2 n_kv) 128]), summed here in split order
     const __nv_bfloat16* q_gain;
     const __nv_bfloat16* k_gain;
     const float2* rope;        // [max_ctx][64] (cos, sin)

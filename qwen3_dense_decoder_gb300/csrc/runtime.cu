@@ -520,9 +520,15 @@ void plan_gemm(const q3_model* m, int M, int N, int K, int* bn, int* splits)
     plan_gemm_impl(M, N, K, m->ws_elems, bn, splits);
 }
 
+// With norm_gain, a residual-add GEMM that splits K also writes the RMSNorm of
+// its updated rows (gain norm_gain, fp16 into norm_out) in the split-K finish
+// and sets *normed; otherwise the caller norms the rows itself.  With
+// deferred, a plain-store GEMM that splits K leaves its partials in the
+// workspace for its consumer to sum (*deferred = the split count, else 0).
 int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* a2,
          int tiles0, int tiles1, int pair, int M, int N, int K, const void* act, int epi, void* out,
-         int ldo)
+         int ldo, const bf16* norm_gain = nullptr, f16* norm_out = nullptr, bool* normed = nullptr,
+         int* deferred = nullptr)
 {
     int bn, splits;
     plan_gemm(m, M, N, K, &bn, &splits);
@@ -541,7 +547,13 @@ int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtens
     Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
     m->prof_begin(Q3_K_GEMM);
     int rc = m->check(launch_gemm(L, *a0, a1 ? *a1 : *a0, a2 ? *a2 : *a0, *b, bn, g), "gemm");
-    if (rc == Q3_OK && splits > 1) rc = m->check(launch_gemm_splitk_reduce(L, g), "gemm reduce");
+    const bool fuse = norm_gain && gemm_add_norm_ok(g);
+    const bool defer = deferred && splits > 1 && !pair && epi == EPI_STORE_F32;
+    if (normed) *normed = fuse;
+    if (deferred) *deferred = defer ? splits : 0;
+    if (rc == Q3_OK && splits > 1 && !defer)
+        rc = fuse ? m->check(launch_gemm_splitk_add_norm(L, g, norm_gain, m->c.rms_eps, norm_out), "gemm reduce+norm")
+                  : m->check(launch_gemm_splitk_reduce(L, g), "gemm reduce");
     m->prof_end();
     return rc;
 }
@@ -761,11 +773,15 @@ int run_round(q3_model* m, const Round& r)
     if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_embed(L, r.tokens, T, m->embed, H, c.vocab, m->x, m->status); }), "embed")))
         return rc;
 
+    bool ha_ready = false;            // the previous residual GEMM already wrote this layer's normed rows
+    int qkv_splits = 0;               // the QKV projection's partials are left for the attention to sum
     for (int l = 0; l < c.n_layers; ++l) {
         const q3_layer_weights& W = m->layers[l];
         const LayerMaps& Mp = m->maps[l];
         const bf16* attn_norm = static_cast<const bf16*>(W.attn_norm);
         const bf16* ffn_norm = static_cast<const bf16*>(W.ffn_norm);
+        const bf16* next_attn_norm =
+            l + 1 < c.n_layers ? static_cast<const bf16*>(m->layers[l + 1].attn_norm) : nullptr;
 
         // ---- QKV projection
         if (one) {
@@ -779,11 +795,15 @@ int run_round(q3_model* m, const Round& r)
             if ((rc = gemv(m, 3, w, sc, rows, 0, H, m->x, attn_norm, EPI_STORE_F32, m->qkv, nullptr, &nx)))
                 return rc;
         } else {
-            if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->ha, m->status); }),
+            if (!ha_ready &&
+                (rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, attn_norm, c.rms_eps, m->ha, m->status); }),
                                "rmsnorm")))
                 return rc;
+            ha_ready = false;
+            // decode rounds: the attention sums the QKV partials itself
             rc = gemm(m, &Mp.m[P_Q], &Mp.m[P_K], &Mp.m[P_V], m->qw / 128, (m->qw + m->kvw) / 128, 0,
-                      m->qkvw, T, H, m->ha, EPI_STORE_F32, m->qkv, m->qkvw);
+                      m->qkvw, T, H, m->ha, EPI_STORE_F32, m->qkv, m->qkvw, nullptr, nullptr, nullptr,
+                      r.decode ? &qkv_splits : nullptr);
             if (rc) return rc;
         }
 
@@ -813,6 +833,7 @@ int run_round(q3_model* m, const Round& r)
         if (r.decode) {
             AttnArgs aa{};
             aa.q = m->q; aa.qkv = m->qkv;
+            aa.qkv_ws = m->ws; aa.qkv_splits = one ? 0 : qkv_splits;
             aa.q_gain = static_cast<const bf16*>(W.q_norm);
             aa.k_gain = static_cast<const bf16*>(W.k_norm);
             aa.rope = m->rope; aa.eps = c.rms_eps;
@@ -868,7 +889,7 @@ int run_round(q3_model* m, const Round& r)
                 return rc;
         } else {
             rc = gemm(m, &Mp.m[P_O], nullptr, nullptr, H / 128, H / 128, 0, H, T, m->qw, m->att,
-                      EPI_ADD_F32, m->x, H);
+                      EPI_ADD_F32, m->x, H, ffn_norm, m->ha, &ha_ready);
             if (rc) return rc;
         }
 
@@ -890,14 +911,16 @@ int run_round(q3_model* m, const Round& r)
             if ((rc = gemv(m, 1, wd, scd, rowsd, 0, F, m->sf, nullptr, EPI_ADD_F32, m->x, nullptr, &nx3)))
                 return rc;
         } else {
-            if ((rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->ha, m->status); }),
+            if (!ha_ready &&
+                (rc = m->check(run(Q3_K_NORM, [&] { return launch_rmsnorm_f16(L, m->x, nullptr, T, H, ffn_norm, c.rms_eps, m->ha, m->status); }),
                                "rmsnorm")))
                 return rc;
+            ha_ready = false;
             rc = gemm(m, &Mp.m[P_G], &Mp.m[P_U], nullptr, 0, 0, 1, 2 * F, T, H, m->ha,
                       EPI_SWIGLU_F16, m->s, F);
             if (rc) return rc;
             rc = gemm(m, &Mp.m[P_D], nullptr, nullptr, H / 128, H / 128, 0, H, T, F, m->s, EPI_ADD_F32,
-                      m->x, H);
+                      m->x, H, next_attn_norm, m->ha, &ha_ready);
             if (rc) return rc;
         }
     }
