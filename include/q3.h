@@ -289,7 +289,7 @@ int q3_affine4_to_f16(const void* groups_dev, int64_t n, void* out_dev, void* st
  * w_dev: fp16 [M][K]; x_dev: fp16 [N][K] with at least round_up(N, 256)
  * rows allocated (rows past N are read but their products discarded);
  * y_dev: f32 [N][M].  M a multiple of 128, K a multiple of 64, 1 <= N.
- * block_n: token-tile width (32, 64, 96, 128, 160, 192 or 256), or 0 for the
+ * block_n: token-tile width (32, 64, 96, 128, 144, 160, 176, 192 or 256), or 0 for the
  * width the prefill planner would pick; no split-K.  Pointers 16-byte
  * aligned.  Synchronous: returns once the kernel has finished on stream (it
  * allocates and frees a status word).  Errors: Q3_ERR_INVALID_ARG,

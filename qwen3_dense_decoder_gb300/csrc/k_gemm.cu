@@ -55,6 +55,14 @@ constexpr int GEMM_THREADS = 192;     // producer, MMA issuer, 4 epilogue warps
 constexpr int BAR_EPI = 1;            // named barrier of the epilogue warps
 
 Q3_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+Q3_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+}
 Q3_DEV float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 struct Unit {
@@ -231,18 +239,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
             if (!named_bar_and(BAR_EPI, 128, mbar_wait(&tfull[ab], use_ab & 1, p.status))) break;
             tc_fence_after();
             const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + ab * C::ACC_COLS;
+            // 32 columns at a time; a tile width of 16 mod 32 ends with 16
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < (BN + 31) / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + c * 32, r);
+                if (BN - c * 32 >= 32) {
+                    tmem_ld_32x32b_x32(t_row + c * 32, r);
+                } else {
+                    tmem_ld_32x32b_x16(t_row + c * 32, *reinterpret_cast<uint32_t(*)[16]>(r));
+#pragma unroll
+                    for (int j = 16; j < 32; ++j) r[j] = 0u;
+                }
                 tmem_ld_wait();
                 const int n0 = w.nt * BN + c * 32;
+                const int lim = min(p.N, w.nt * BN + BN);   // this tile's last column + 1
                 if (p.k_splits > 1) {
                     float* ws = p.ws + (size_t)w.split * p.N * p.M;
                     const int m = w.mt * BM + row;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (n0 + j < p.N) ws[(size_t)(n0 + j) * p.M + m] = __uint_as_float(r[j]);
+                        if (n0 + j < lim) ws[(size_t)(n0 + j) * p.M + m] = __uint_as_float(r[j]);
                 } else if (swiglu) {
                     // rows 0..63 hold the gate and rows 64..127 the up projection of
                     // the same 64 features: every thread posts its 32 columns, then
@@ -256,7 +272,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int j = jh + jj;
-                        if (n0 + j < p.N) {
+                        if (n0 + j < lim) {
                             const float v = silu_fast(xch[j * 128 + fr]) * xch[j * 128 + 64 + fr];
                             if (p.epi == EPI_SWIGLU_F16)
                                 reinterpret_cast<__half*>(p.out)[(size_t)(n0 + j) * p.ldo + f] =
@@ -273,15 +289,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
                     float old[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        old[j] = n0 + j < p.N ? out[(size_t)(n0 + j) * p.ldo + m] : 0.f;
+                        old[j] = n0 + j < lim ? out[(size_t)(n0 + j) * p.ldo + m] : 0.f;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (n0 + j < p.N) out[(size_t)(n0 + j) * p.ldo + m] = old[j] + __uint_as_float(r[j]);
+                        if (n0 + j < lim) out[(size_t)(n0 + j) * p.ldo + m] = old[j] + __uint_as_float(r[j]);
                 } else {
                     const int m = w.mt * BM + row;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        if (n0 + j < p.N) {
+                        if (n0 + j < lim) {
                             const size_t o = (size_t)(n0 + j) * p.ldo + m;
                             const float v = __uint_as_float(r[j]);
                             if (p.epi == EPI_STORE_F32)
@@ -469,7 +485,8 @@ int gemm_block_n(int N)
 
 bool gemm_block_n_supported(int bn)
 {
-    return bn == 32 || bn == 64 || bn == 96 || bn == 128 || bn == 160 || bn == 192 || bn == 256;
+    return bn == 32 || bn == 64 || bn == 96 || bn == 128 || bn == 144 || bn == 160 || bn == 176 || bn == 192 ||
+           bn == 256;
 }
 
 cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
@@ -480,7 +497,9 @@ cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMa
     case 64: return launch_bn<64>(L, a0, a1, a2, b, g);
     case 96: return launch_bn<96>(L, a0, a1, a2, b, g);
     case 128: return launch_bn<128>(L, a0, a1, a2, b, g);
+    case 144: return launch_bn<144>(L, a0, a1, a2, b, g);
     case 160: return launch_bn<160>(L, a0, a1, a2, b, g);
+    case 176: return launch_bn<176>(L, a0, a1, a2, b, g);
     case 192: return launch_bn<192>(L, a0, a1, a2, b, g);
     case 256: return launch_bn<256>(L, a0, a1, a2, b, g);
     default: return cudaErrorInvalidValue;

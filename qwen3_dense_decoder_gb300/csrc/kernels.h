@@ -77,7 +77,7 @@ struct GemmArgs {
 // Box shapes a tensor map must have for the GEMM: weights 64 (K) x 128
 // rows (64 rows in pair mode); activations 64 x BN.
 int gemm_block_n(int N);          // smallest tile width covering N token rows
-bool gemm_block_n_supported(int bn);   // 32, 64, 96, 128, 160, 192 or 256
+bool gemm_block_n_supported(int bn);   // 32, 64, 96, 128, 144, 160, 176, 192 or 256
 cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& a2, const CUtensorMap& b, int bn,
                         const GemmArgs& g);

@@ -487,7 +487,7 @@ int attention_splits(const q3_model* m, int T, int max_ctx)
 void plan_gemm_impl(int M, int N, int K, size_t ws_elems, int* bn, int* splits)
 {
     const int kb = K / 64;
-    const int cand[7] = {32, 64, 96, 128, 160, 192, 256};
+    const int cand[9] = {32, 64, 96, 128, 144, 160, 176, 192, 256};
     int best_bn = gemm_block_n(N), best_s = 1;
     double best = 1e30;
     for (int b : cand) {

@@ -88,7 +88,7 @@ def test_affine4_f16_copy_matches_oracle_dequant_bitwise(q3, orc, rows, n):
     np.testing.assert_array_equal(got.view(np.uint16), ref.view(np.uint16))
 
 
-@pytest.mark.parametrize("bn", [0, 32, 64, 96, 128, 160, 192, 256])
+@pytest.mark.parametrize("bn", [0, 32, 64, 96, 128, 144, 160, 176, 192, 256])
 @pytest.mark.parametrize("n", [1, 5, 40, 83, 200, 300])
 @pytest.mark.parametrize("M,K", [(256, 64), (384, 2560), (128, 9728)])
 def test_tcgen05_matmul_matches_oracle(q3, orc, n, M, K, bn):
