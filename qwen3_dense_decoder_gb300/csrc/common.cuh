@@ -72,12 +72,8 @@ Q3_DEV float warp_allsum(float v) {
     return v;
 }
 
-Q3_DEV void head_norm_rope(float (&y)[4], const __nv_bfloat16* gain, const float2* rope_row,
-                           float eps, int lane) {
-    // gain and cos/sin loads go out before the reduction that precedes their use
-    const uint2 g4 = *reinterpret_cast<const uint2*>(gain + lane * 4);
-    const float4* cs = reinterpret_cast<const float4*>(rope_row + (lane & 15) * 4);
-    const float4 c01 = cs[0], c23 = cs[1];
+// The same, from the lane's gain (4 bf16) and (cos, sin) pairs already loaded
+Q3_DEV void head_norm_rope_loaded(float (&y)[4], uint2 g4, float4 c01, float4 c23, float eps, int lane) {
     const float gv[4] = {bf16lo(g4.x), bf16hi(g4.x), bf16lo(g4.y), bf16hi(g4.y)};
     const float2 cv[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
                           make_float2(c23.z, c23.w)};
@@ -95,6 +91,14 @@ Q3_DEV void head_norm_rope(float (&y)[4], const __nv_bfloat16* gain, const float
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) y[e] = out[e];
+}
+
+Q3_DEV void head_norm_rope(float (&y)[4], const __nv_bfloat16* gain, const float2* rope_row,
+                           float eps, int lane) {
+    // gain and cos/sin loads go out before the reduction that precedes their use
+    const uint2 g4 = *reinterpret_cast<const uint2*>(gain + lane * 4);
+    const float4* cs = reinterpret_cast<const float4*>(rope_row + (lane & 15) * 4);
+    head_norm_rope_loaded(y, g4, cs[0], cs[1], eps, lane);
 }
 
 // ---------------------------------------------------------------- Q8_0 K/V rows

@@ -55,6 +55,146 @@ constexpr int GEMM_THREADS = 192;     // producer, MMA issuer, 4 epilogue warps
 constexpr int BAR_EPI = 1;            // named barrier of the epilogue warps
 
 Q3_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// EPI_QKV_ROPE epilogue.  A tile is one head (m-tile hh, q heads, then k
+// heads, then v heads) of BN tokens; each 32-token chunk goes through the
+// exchange buffer.  Epilogue warp ew takes tokens ew, ew + 4, ... of a chunk
+// (8, two at a time: half-warp h the token ew + 4 (2 i + h)), and lane g of a
+// half-warp holds features [4 g, 4 g + 4) and their rotate-half partners
+// [64 + 4 g, + 4): the RMSNorm reduces over 16 lanes and RoPE needs no
+// exchange.  The GEMM streams its operands through L2, where a load waits
+// microseconds: before the accumulator wait, lane l looks up the position
+// (K/V heads: also the pool block) of the warp's tokens l and l + 32 of the
+// tile, and each chunk's (cos, sin) rows are requested two chunks ahead.
+struct QkvRows {
+    int pos_a, pos_b, blk_a, blk_b;
+    uint2 g_lo, g_hi;                           // the lane's gain values (q/k heads)
+};
+
+Q3_DEV QkvRows qkv_rope_rows(const RopeArgs& a, int hh, int tile_n0, int lim, int ew, int lane) {
+    QkvRows r{0, 0, 0, 0, make_uint2(0u, 0u), make_uint2(0u, 0u)};
+    const bool is_q = hh < a.n_q, is_k = !is_q && hh < a.n_q + a.n_kv;
+    if (is_q || is_k) {
+        const __nv_bfloat16* gain = is_q ? a.q_gain : a.k_gain;
+        r.g_lo = *reinterpret_cast<const uint2*>(gain + (lane & 15) * 4);
+        r.g_hi = *reinterpret_cast<const uint2*>(gain + 64 + (lane & 15) * 4);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int idx = lane + 32 * h;                      // chunk idx / 8, token ew + 4 (idx % 8)
+        const int t = tile_n0 + (idx >> 3) * 32 + ew + 4 * (idx & 7);
+        int pos = 0, blk = 0;
+        if (t < lim) {
+            pos = a.row_pos[t];
+            if (!is_q) blk = a.tables[(size_t)a.row_slot[t] * a.max_blocks + pos / 32];
+        }
+        (h ? r.pos_b : r.pos_a) = pos;
+        (h ? r.blk_b : r.blk_a) = blk;
+    }
+    return r;
+}
+
+// the position or pool block of token k (0..7) of chunk c of the warp (k may differ by lane)
+Q3_DEV int qkv_row_pos(const QkvRows& r, int c, int k) {
+    return __shfl_sync(0xffffffffu, c < 4 ? r.pos_a : r.pos_b, (c & 3) * 8 + k);
+}
+Q3_DEV int qkv_row_blk(const QkvRows& r, int c, int k) {
+    return __shfl_sync(0xffffffffu, c < 4 ? r.blk_a : r.blk_b, (c & 3) * 8 + k);
+}
+
+// The (cos, sin) pairs of frequencies [4 g, 4 g + 4) for the lane's 4 tokens
+// of chunk c (cs[2 i], cs[2 i + 1]: token 2 i + h); a half-warp reads a
+// 512-byte table row whole.  Tokens past the tile's end have position 0: a
+// valid row, unused.
+Q3_DEV void qkv_cs_load(const RopeArgs& a, const QkvRows& r, int c, int lane, float4 (&cs)[8]) {
+    const int h = lane >> 4, g = lane & 15;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4* row = reinterpret_cast<const float4*>(a.rope + (size_t)qkv_row_pos(r, c, 2 * i + h) * 64);
+        cs[2 * i] = row[2 * g];
+        cs[2 * i + 1] = row[2 * g + 1];
+    }
+}
+
+Q3_DEV uint2 pack_f16x4(const float (&v)[4], bool& bad) {
+    __half2 lo, hi;
+    lo.x = to_f16(v[0], bad); lo.y = to_f16(v[1], bad);
+    hi.x = to_f16(v[2], bad); hi.y = to_f16(v[3], bad);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+Q3_DEV uint2 pack_bf16x4(const float (&v)[4]) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+// Chunk c (tokens n0 ..) of head hh, staged in xch [token][128 features].
+// All tokens are computed (columns past the tile's end hold zeros) and only
+// the stores are predicated, so the 4 iterations' reductions interleave.
+Q3_DEV void qkv_rope_chunk(const RopeArgs& a, int hh, int c, int n0, int lim, const float* xch, int ew, int lane,
+                           const QkvRows& r, const float4 (&cs)[8], bool& bad) {
+    const bool is_q = hh < a.n_q, is_k = !is_q && hh < a.n_q + a.n_kv;
+    const int h = lane >> 4, g = lane & 15;
+    float x1[4][4], x2[4][4];                   // features [4 g, + 4) and [64 + 4 g, + 4) of token 2 i + h
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float* src = xch + (ew + 4 * (2 * i + h)) * 128 + 4 * g;
+        const float4 u = *reinterpret_cast<const float4*>(src);
+        const float4 v = *reinterpret_cast<const float4*>(src + 64);
+        x1[i][0] = u.x; x1[i][1] = u.y; x1[i][2] = u.z; x1[i][3] = u.w;
+        x2[i][0] = v.x; x2[i][1] = v.y; x2[i][2] = v.z; x2[i][3] = v.w;
+    }
+    if (is_q || is_k) {
+        const float g1[4] = {bf16lo(r.g_lo.x), bf16hi(r.g_lo.x), bf16lo(r.g_lo.y), bf16hi(r.g_lo.y)};
+        const float g2[4] = {bf16lo(r.g_hi.x), bf16hi(r.g_hi.x), bf16lo(r.g_hi.y), bf16hi(r.g_hi.y)};
+        float ss[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ss[i] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ss[i] += x1[i][e] * x1[i][e] + x2[i][e] * x2[i][e];
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float rr = 1.0f / sqrtf(ss[i] / 128.0f + a.eps);
+            const float cv[4][2] = {{cs[2 * i].x, cs[2 * i].y}, {cs[2 * i].z, cs[2 * i].w},
+                                    {cs[2 * i + 1].x, cs[2 * i + 1].y}, {cs[2 * i + 1].z, cs[2 * i + 1].w}};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float y1 = x1[i][e] * rr * g1[e], y2 = x2[i][e] * rr * g2[e];
+                x1[i][e] = y1 * cv[e][0] - y2 * cv[e][1];     // first half: x1 cos - x2 sin
+                x2[i][e] = y2 * cv[e][0] + y1 * cv[e][1];     // second half: x2 cos + x1 sin
+            }
+        }
+    }
+    const int kvh = is_k ? hh - a.n_q : hh - a.n_q - a.n_kv;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int k = 2 * i + h, t = n0 + ew + 4 * k;
+        if (is_q) {
+            if (t < lim) {
+                __half* dst = a.q_out16 + ((size_t)t * a.n_q + hh) * 128 + 4 * g;
+                *reinterpret_cast<uint2*>(dst) = pack_f16x4(x1[i], bad);
+                *reinterpret_cast<uint2*>(dst + 64) = pack_f16x4(x2[i], bad);
+            }
+            continue;
+        }
+        const int pos = qkv_row_pos(r, c, k), blk = qkv_row_blk(r, c, k);
+        if (t >= lim) continue;
+        if (blk < 0 || blk >= a.n_blocks) {
+            if (g == 0) set_status(a.status, Q3_STATUS_BLOCK_RANGE);
+            continue;
+        }
+        __nv_bfloat16* dst = a.kv_layer + (((size_t)blk * 2 + (is_k ? 0 : 1)) * a.n_kv + kvh) * (32 * 128) +
+                             (size_t)(pos % 32) * 128 + 4 * g;
+        *reinterpret_cast<uint2*>(dst) = pack_bf16x4(x1[i]);
+        *reinterpret_cast<uint2*>(dst + 64) = pack_bf16x4(x2[i]);
+    }
+}
 Q3_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
                  "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -83,7 +223,7 @@ Q3_DEV Unit decode_unit(const GemmArgs& p, int u, int n_tiles)
     return w;
 }
 
-template <int BN>
+template <int BN, bool QKV>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
                const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tb,
@@ -225,6 +365,59 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ 
                 tc_commit(&tfull[ab]);
             }
         }
+    } else if constexpr (QKV) {
+        // ---------------- epilogue (EPI_QKV_ROPE): warps 2..5
+        constexpr int NCH = (BN + 31) / 32;
+        const RopeArgs& a = p.rope;
+        const int q = warp & 3, row = q * 32 + lane, ew = warp - 2;
+        bool range_bad = false;
+        int local = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+            const Unit w = decode_unit(p, u, n_tiles);
+            const int ab = local & 1;
+            const uint32_t use_ab = local >> 1;
+            const int lim = min(p.N, w.nt * BN + BN);       // this tile's last column + 1
+            const bool qk = w.mt < a.n_q + a.n_kv;
+            const QkvRows rows = qkv_rope_rows(a, w.mt, w.nt * BN, lim, ew, lane);
+            // chunks c, c + 1 and c + 2 in flight; the loop stays rolled (an
+            // unrolled tile overflows the instruction cache)
+            float4 cs0[8], cs1[8], cs2[8];
+            if (qk) {
+                qkv_cs_load(a, rows, 0, lane, cs0);
+                if (NCH > 1) qkv_cs_load(a, rows, 1, lane, cs1);
+            }
+            if (!named_bar_and(BAR_EPI, 128, mbar_wait(&tfull[ab], use_ab & 1, p.status))) break;
+            tc_fence_after();
+            const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + ab * C::ACC_COLS;
+#pragma unroll 1
+            for (int c = 0; c < NCH; ++c) {
+                if (qk && c + 2 < NCH) qkv_cs_load(a, rows, c + 2, lane, cs2);
+                uint32_t r[32];
+                if (BN - c * 32 >= 32) {
+                    tmem_ld_32x32b_x32(t_row + c * 32, r);
+                } else {
+                    tmem_ld_32x32b_x16(t_row + c * 32, *reinterpret_cast<uint32_t(*)[16]>(r));
+#pragma unroll
+                    for (int j = 16; j < 32; ++j) r[j] = 0u;
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) xch[j * 128 + row] = __uint_as_float(r[j]);
+                named_bar(BAR_EPI, 128);
+                qkv_rope_chunk(a, w.mt, c, w.nt * BN + c * 32, lim, xch, ew, lane, rows, cs0, range_bad);
+                named_bar(BAR_EPI, 128);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    cs0[k] = cs1[k];
+                    cs1[k] = cs2[k];
+                }
+            }
+            // this accumulator may be overwritten by the unit after next
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+        }
+        if (range_bad) set_status(p.status, Q3_STATUS_F16_RANGE);
     } else {
         // ---------------- epilogue: TMEM -> registers -> global, warps 2..5
         const int q = warp & 3;                         // TMEM lane quadrant of this warp
@@ -449,13 +642,13 @@ __global__ void __launch_bounds__(ADDNORM_THREADS) gemm_splitk_add_norm_kernel(c
     if (bad) set_status(p.status, Q3_STATUS_F16_RANGE);
 }
 
-template <int BN>
+template <int BN, bool QKV>
 cudaError_t launch_bn(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
                       const CUtensorMap& a2, const CUtensorMap& b, const GemmArgs& g)
 {
     using C = GemmCfg<BN>;
     static std::atomic<unsigned long long> attr_done{0};
-    if (cudaError_t e = allow_smem_per_device(gemm_tc_kernel<BN>, C::SMEM, attr_done)) return e;
+    if (cudaError_t e = allow_smem_per_device(gemm_tc_kernel<BN, QKV>, C::SMEM, attr_done)) return e;
     const int n_tiles = (g.N + BN - 1) / BN;
     const int units = n_tiles * (g.M / BM) * g.k_splits;
     const int grid = units < 152 ? units : 152;          // persistent: one CTA per SM
@@ -470,7 +663,7 @@ cudaError_t launch_bn(const Launch& L, const CUtensorMap& a0, const CUtensorMap&
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (L.counter) ++*L.counter;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN>, a0, a1, a2, b, g);
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, QKV>, a0, a1, a2, b, g);
 }
 
 }  // namespace
@@ -492,19 +685,37 @@ bool gemm_block_n_supported(int bn)
 cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& a2, const CUtensorMap& b, int bn, const GemmArgs& g)
 {
+    // the fused head epilogue needs whole tiles in one pass and 128-row heads
+    if (g.epi == EPI_QKV_ROPE && (g.k_splits != 1 || g.pair || g.M % BM != 0 || !g.rope.row_pos))
+        return cudaErrorInvalidValue;
+    if (g.epi == EPI_QKV_ROPE) {
+        switch (bn) {
+        case 32: return launch_bn<32, true>(L, a0, a1, a2, b, g);
+        case 64: return launch_bn<64, true>(L, a0, a1, a2, b, g);
+        case 96: return launch_bn<96, true>(L, a0, a1, a2, b, g);
+        case 128: return launch_bn<128, true>(L, a0, a1, a2, b, g);
+        case 144: return launch_bn<144, true>(L, a0, a1, a2, b, g);
+        case 160: return launch_bn<160, true>(L, a0, a1, a2, b, g);
+        case 176: return launch_bn<176, true>(L, a0, a1, a2, b, g);
+        case 192: return launch_bn<192, true>(L, a0, a1, a2, b, g);
+        case 256: return launch_bn<256, true>(L, a0, a1, a2, b, g);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (bn) {
-    case 32: return launch_bn<32>(L, a0, a1, a2, b, g);
-    case 64: return launch_bn<64>(L, a0, a1, a2, b, g);
-    case 96: return launch_bn<96>(L, a0, a1, a2, b, g);
-    case 128: return launch_bn<128>(L, a0, a1, a2, b, g);
-    case 144: return launch_bn<144>(L, a0, a1, a2, b, g);
-    case 160: return launch_bn<160>(L, a0, a1, a2, b, g);
-    case 176: return launch_bn<176>(L, a0, a1, a2, b, g);
-    case 192: return launch_bn<192>(L, a0, a1, a2, b, g);
-    case 256: return launch_bn<256>(L, a0, a1, a2, b, g);
+    case 32: return launch_bn<32, false>(L, a0, a1, a2, b, g);
+    case 64: return launch_bn<64, false>(L, a0, a1, a2, b, g);
+    case 96: return launch_bn<96, false>(L, a0, a1, a2, b, g);
+    case 128: return launch_bn<128, false>(L, a0, a1, a2, b, g);
+    case 144: return launch_bn<144, false>(L, a0, a1, a2, b, g);
+    case 160: return launch_bn<160, false>(L, a0, a1, a2, b, g);
+    case 176: return launch_bn<176, false>(L, a0, a1, a2, b, g);
+    case 192: return launch_bn<192, false>(L, a0, a1, a2, b, g);
+    case 256: return launch_bn<256, false>(L, a0, a1, a2, b, g);
     default: return cudaErrorInvalidValue;
     }
 }
+
 
 cudaError_t launch_gemm_splitk_reduce(const Launch& L, const GemmArgs& g)
 {

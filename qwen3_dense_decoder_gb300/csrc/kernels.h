@@ -58,7 +58,32 @@ enum Epi : int {
     EPI_STORE_F16 = 2,   // out = fp16(acc)
     EPI_SWIGLU_F16 = 3,  // paired gate/up tile: out[n][f] = fp16(silu(g) * u)
     EPI_SWIGLU_F32 = 4,
+    EPI_QKV_ROPE = 5,    // QKV tiles, one head each (q, then k, then v heads): the q/k head
+                         // RMSNorm and RoPE, q as fp16 into rope.q_out16, K and V as bf16 into the
+                         // pool through the block table (rope; the BF16 cache)
 };
+
+struct RopeArgs {
+    const float* qkv;          // [T][n_q*128 + 2*n_kv*128]
+    int T, n_q, n_kv;
+    const __nv_bfloat16* q_gain;
+    const __nv_bfloat16* k_gain;
+    float eps;
+    const float2* rope;        // [max_ctx][64] (cos, sin)
+    const int* row_pos;        // [T]
+    const int* row_slot;       // [T] session slot
+    const int* tables;         // [slots][max_blocks]
+    int max_blocks;
+    __nv_bfloat16* kv_layer;   // pool base of this layer: [n_blocks][2][n_kv][32][128]
+    uint8_t* kvq_layer;        // Q8_0 cache: pool base of this layer, [n_blocks][2][n_kv] tiles of
+                               // KVQ_TILE bytes (null: the BF16 cache at kv_layer)
+    int64_t layer_stride;      // elements between layers (unused by the kernel)
+    int n_blocks;
+    float* q_out;              // [T][n_q*128] f32, or null
+    __half* q_out16;           // [T][n_q*128] fp16, or null
+    int* status;
+};
+
 
 struct GemmArgs {
     int M, N, K;          // M multiple of 128; K multiple of 64
@@ -71,6 +96,7 @@ struct GemmArgs {
     float* ws;
     int early_a;          // request the first stages' weight tiles before the dependency wait
                           // (helps short GEMMs, whose ring ramp is a large part of the launch)
+    RopeArgs rope;        // EPI_QKV_ROPE: the rows' positions, slots, tables, gains and outputs
     int* status;
 };
 
@@ -142,26 +168,6 @@ cudaError_t launch_embed(const Launch& L, const int32_t* tokens, int T, const __
 cudaError_t launch_rmsnorm_f16(const Launch& L, const float* x, const int* rows, int n, int H,
                                const __nv_bfloat16* g, float eps, __half* h, int* status);
 
-struct RopeArgs {
-    const float* qkv;          // [T][n_q*128 + 2*n_kv*128]
-    int T, n_q, n_kv;
-    const __nv_bfloat16* q_gain;
-    const __nv_bfloat16* k_gain;
-    float eps;
-    const float2* rope;        // [max_ctx][64] (cos, sin)
-    const int* row_pos;        // [T]
-    const int* row_slot;       // [T] session slot
-    const int* tables;         // [slots][max_blocks]
-    int max_blocks;
-    __nv_bfloat16* kv_layer;   // pool base of this layer: [n_blocks][2][n_kv][32][128]
-    uint8_t* kvq_layer;        // Q8_0 cache: pool base of this layer, [n_blocks][2][n_kv] tiles of
-                               // KVQ_TILE bytes (null: the BF16 cache at kv_layer)
-    int64_t layer_stride;      // elements between layers (unused by the kernel)
-    int n_blocks;
-    float* q_out;              // [T][n_q*128] f32, or null
-    __half* q_out16;           // [T][n_q*128] fp16, or null
-    int* status;
-};
 cudaError_t launch_qk_norm_rope_append(const Launch& L, const RopeArgs& a);
 
 struct AttnArgs {

@@ -525,13 +525,19 @@ void plan_gemm(const q3_model* m, int M, int N, int K, int* bn, int* splits)
 // and sets *normed; otherwise the caller norms the rows itself.  With
 // deferred, a plain-store GEMM that splits K leaves its partials in the
 // workspace for its consumer to sum (*deferred = the split count, else 0).
+// With rope, a QKV GEMM whose plan does not split K applies the q/k head
+// norm, RoPE and the KV append in its epilogue (*roped = true); otherwise it
+// stores the fp32 projections and the caller runs the separate kernel.
 int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* a2,
          int tiles0, int tiles1, int pair, int M, int N, int K, const void* act, int epi, void* out,
          int ldo, const bf16* norm_gain = nullptr, f16* norm_out = nullptr, bool* normed = nullptr,
-         int* deferred = nullptr)
+         int* deferred = nullptr, const RopeArgs* rope = nullptr, bool* roped = nullptr)
 {
     int bn, splits;
     plan_gemm(m, M, N, K, &bn, &splits);
+    const bool head_epi = rope && splits == 1 && !pair;
+    if (roped) *roped = head_epi;
+    if (head_epi) epi = EPI_QKV_ROPE;
     const CUtensorMap* b = m->act_map(act, K, bn);
     if (!b) return fail(Q3_ERR_CUDA, "tensor map encoding failed");
     GemmArgs g{};
@@ -544,6 +550,7 @@ int gemm(q3_model* m, const CUtensorMap* a0, const CUtensorMap* a1, const CUtens
     g.ws = m->ws;
     g.early_a = N <= 256;                    // batched decode rounds: the ring ramp overlaps the previous kernel
     g.status = m->status;
+    if (head_epi) g.rope = *rope;
     Launch L{m->stream, m->pdl && !m->prof_on, &m->launches};
     m->prof_begin(Q3_K_GEMM);
     int rc = m->check(launch_gemm(L, *a0, a1 ? *a1 : *a0, a2 ? *a2 : *a0, *b, bn, g), "gemm");
@@ -784,6 +791,27 @@ int run_round(q3_model* m, const Round& r)
             l + 1 < c.n_layers ? static_cast<const bf16*>(m->layers[l + 1].attn_norm) : nullptr;
 
         // ---- QKV projection
+        // prefill rounds: q/k head norm, RoPE and the KV append in the epilogue
+        // (BF16 cache, no K split) or in their own kernel; decode rounds: the
+        // attention sums the QKV partials and does all three itself
+        RopeArgs ra{};
+        if (!r.decode) {
+            ra.qkv = m->qkv; ra.T = T; ra.n_q = c.n_q_heads; ra.n_kv = c.n_kv_heads;
+            ra.q_gain = static_cast<const bf16*>(W.q_norm);
+            ra.k_gain = static_cast<const bf16*>(W.k_norm);
+            ra.eps = c.rms_eps; ra.rope = m->rope;
+            ra.row_pos = row_pos; ra.row_slot = row_slot;
+            ra.tables = r.pool->tables; ra.max_blocks = r.pool->max_blocks;
+#ifdef Q3_TEST_FAULTS
+            if (m->fault_pos) ra.row_pos = m->fault_pos;
+            if (m->fault == 4) ra.tables = r.pool->fault_tables;
+#endif
+            ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
+            ra.kvq_layer = m->kv_q8 ? reinterpret_cast<uint8_t*>(r.pool->kv) + (size_t)l * layer_bytes : nullptr;
+            ra.n_blocks = r.pool->n_blocks;
+            ra.q_out = nullptr; ra.q_out16 = m->q16; ra.status = m->status;
+        }
+        bool roped = false;
         if (one) {
             const void* w[3];
             const __half* sc[3];
@@ -800,34 +828,16 @@ int run_round(q3_model* m, const Round& r)
                                "rmsnorm")))
                 return rc;
             ha_ready = false;
-            // decode rounds: the attention sums the QKV partials itself
+            const bool head_epi_ok = !r.decode && !m->kv_q8 && c.head_dim == 128;
             rc = gemm(m, &Mp.m[P_Q], &Mp.m[P_K], &Mp.m[P_V], m->qw / 128, (m->qw + m->kvw) / 128, 0,
                       m->qkvw, T, H, m->ha, EPI_STORE_F32, m->qkv, m->qkvw, nullptr, nullptr, nullptr,
-                      r.decode ? &qkv_splits : nullptr);
+                      r.decode ? &qkv_splits : nullptr, head_epi_ok ? &ra : nullptr, &roped);
             if (rc) return rc;
         }
-
-        // ---- q/k norm, RoPE, KV append (fused into attention in decode rounds)
-        if (!r.decode) {
-            RopeArgs ra{};
-            ra.qkv = m->qkv; ra.T = T; ra.n_q = c.n_q_heads; ra.n_kv = c.n_kv_heads;
-            ra.q_gain = static_cast<const bf16*>(W.q_norm);
-            ra.k_gain = static_cast<const bf16*>(W.k_norm);
-            ra.eps = c.rms_eps; ra.rope = m->rope;
-            ra.row_pos = row_pos; ra.row_slot = row_slot;
-            ra.tables = r.pool->tables; ra.max_blocks = r.pool->max_blocks;
-#ifdef Q3_TEST_FAULTS
-            if (m->fault_pos) ra.row_pos = m->fault_pos;
-            if (m->fault == 4) ra.tables = r.pool->fault_tables;
-#endif
-            ra.kv_layer = r.pool->kv + (size_t)l * layer_kv;
-            ra.kvq_layer = m->kv_q8 ? reinterpret_cast<uint8_t*>(r.pool->kv) + (size_t)l * layer_bytes : nullptr;
-            ra.n_blocks = r.pool->n_blocks;
-            ra.q_out = nullptr; ra.q_out16 = m->q16; ra.status = m->status;
-            if ((rc = m->check(run(Q3_K_ROPE, [&] { return launch_qk_norm_rope_append(L, ra); }),
-                               "qk-norm/rope/append")))
-                return rc;
-        }
+        if (!r.decode && !roped &&
+            (rc = m->check(run(Q3_K_ROPE, [&] { return launch_qk_norm_rope_append(L, ra); }),
+                           "qk-norm/rope/append")))
+            return rc;
 
         // ---- attention
         if (r.decode) {
