@@ -462,10 +462,12 @@ def run_gpu(args, dist_on: bool, rank: int, world: int):
         ctx_b = [s.pos for s in sessions]
         barrier(dist_on)
         torch.cuda.synchronize()
-        timer.start()
-        for _ in range(K):
-            model.eval_batch(sessions, toks, ones, logits[:B], toks)
-        b32_ms = timer.stop()
+        with ClockSampler(local) as clk_b32:
+            timer.start()
+            for _ in range(K):
+                model.eval_batch(sessions, toks, ones, logits[:B], toks)
+            b32_ms = timer.stop()
+        out["b32_clocks"] = clk_b32.summary()
         model.sync()
         model.profile(True)
         model.profile_reset()
@@ -821,6 +823,7 @@ def report(args, res, world, dist_on, pk, pk_kind):
                              "frac": round(b_bytes * K / (b_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)},
             "kernels_ms_per_step": {k: round(v[0] / res["b32_profile_steps"], 4)
                                     for k, v in res["b32_profile"].items()},
+            "clocks": res["b32_clocks"],
         }
     e_s = max_over_ranks(res["e2e_s"], dist_on)
     line["e2e"] = {"value": round(world * K / e_s, 2), "unit": "tok/s",

@@ -24,6 +24,7 @@ def _line():
         "prefill_ms": 16.3, "prefill_profile": {"gemm": (12.9, 144), "attention": (2.7, 36)},
         "b32_ms": 1024.0, "b32_ctx": [1000.0] * 32, "b32_profile": {"gemm": (100.0, 4640)},
         "b32_profile_steps": 32, "e2e_s": 0.61, "e2e_bytes": (4, 607748),
+        "b32_clocks": {"sm_mhz": 1995.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 5},
     }
     pk = {"hbm_gbs": 6767.7, "bf16_tflops": 1929.6, "bf16_tflops_sustained": 1702.9}
     return s, args, res, pk, bench.report(args, res, 1, False, pk, "measured")
@@ -40,6 +41,8 @@ def test_required_keys():
     for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
         assert k in line["e2e"], k
     assert "workload" in line["config"] and "model" not in line["config"]
+    # the batch-32 leg carries the clocks sampled during its own timed loop
+    assert line["decode_b32"]["clocks"]["reasons"] == ["sw_power_cap"]
     assert line["higher_is_better"] is True and line["n_gpus"] == 1
 
 
