@@ -106,6 +106,42 @@ def test_batched_equals_isolated(tiny_pair):
         g.close()
 
 
+def test_prefill_head_epilogue_and_split_fallback(tiny_pair):
+    """Prefill rounds of the BF16 cache apply the q/k head norm, RoPE and the
+    K/V append in the QKV GEMM's epilogue when its plan does not split K (70
+    tokens: 32-token tiles with a 6-token tail; 170: 64-token tiles with a
+    42-token tail) and in the separate kernel when it does (20 tokens, four K
+    splits).  Each matches the oracle, and batched decode rounds read back the
+    K/V each one wrote."""
+    m = tiny_pair.model
+    separate = {}
+    gs, os_ = [], []
+    for n in (20, 70, 170):
+        g, o = tiny_pair.sessions()
+        toks = synthetic.make_tokens(n, TINY.vocab, seed=900 + n)
+        m.profile(True)
+        m.profile_reset()
+        got, ref, am = tiny_pair.eval(g, o, toks)
+        separate[n] = m.profile_read()["qk_norm_rope_append"][1]
+        m.profile(False)
+        c = check_row(got, ref, f"tiny/head-epilogue/prefill{n}")
+        assert c.ok, (n, c)
+        assert am == c.argmax_gpu
+        gs.append(g)
+        os_.append(o)
+    assert separate == {20: TINY.n_layers, 70: 0, 170: 0}, separate
+    nxt = [[int(t)] for t in synthetic.make_tokens(3, TINY.vocab, seed=950)]
+    for step in range(3):
+        got, ref, am = tiny_pair.eval_batch(gs, os_, nxt)
+        for i in range(3):
+            c = check_row(got[i], ref[i], "tiny/head-epilogue/decode")
+            assert c.ok, (step, i, c)
+            assert am[i] == c.argmax_gpu
+        nxt = [[int(np.argmax(r))] for r in ref]
+    for g in gs:
+        g.close()
+
+
 def test_batched_decode_over_long_unequal_contexts():
     # three sessions of 300, 1,700 and 3,100 positions decode together: the
     # attention's split count follows the longest row, shorter rows leave
