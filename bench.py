@@ -71,7 +71,7 @@ def parse():
                     help="measure the other named shapes instead (one JSON line each; 0.6b, 8b-q8_0 "
                          "and 14b if none given; 14b-kvq8 is the 14B workload over the Q8_0 K/V cache)")
     ap.add_argument("--ncu-case", choices=("decode-4layer", "gemm-gateup", "attn-prefill", "attn-decode-b32",
-                                           "attn-decode-kvq8-b32", "gemv-a4"),
+                                           "attn-decode-kvq8-b32", "gemv-a4", "prefill-2layer"),
                     default=None,
                     help="run only a small case sized for an ncu capture (a few GB on the device) and exit")
     return ap.parse_args()
@@ -100,6 +100,20 @@ def ncu_case(name: str):
         ses.eval(torch.tensor(synthetic.make_tokens(2048, s.vocab, 7), device="cuda"), lg, tok)
         for _ in range(6):
             ses.eval(tok, lg, tok)
+        m.sync()
+    elif name == "prefill-2layer":
+        # one 2,048-token prefill round of the Qwen3-4B shape cut to 2 layers
+        # (under 3 GB on the device): every prefill kernel once a layer, the
+        # QKV GEMM with its head epilogue (q/k norm, RoPE, K/V append)
+        s = synthetic.SHAPES["4b"].replace(n_layers=2)
+        st = torch.cuda.Stream()
+        torch.cuda.set_stream(st)
+        w = synthetic.make_weights(s, seed=1234, device="cuda")
+        m = q3.Model(s, w, max_ctx=2400, max_round_tokens=2048, stream=st)
+        pool = m.pool(80, 2)
+        ses = pool.session()
+        lg = torch.empty(s.vocab, device="cuda")
+        ses.eval(torch.tensor(synthetic.make_tokens(2048, s.vocab, 7), device="cuda"), lg)
         m.sync()
     elif name == "attn-decode-b32":
         # batch-32 decode of the Qwen3-4B shape cut to 2 layers: 32 sessions
