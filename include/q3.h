@@ -452,7 +452,9 @@ int64_t q3_model_launch_count(const q3_model* m);
 #define Q3_K_GEMV 0      /* decode matvec (projections, lm_head) */
 #define Q3_K_GEMM 1      /* tcgen05 GEMM and its split-K reduce */
 #define Q3_K_ATTN 2      /* attention and split combine */
-#define Q3_K_ROPE 3      /* q/k norm + RoPE + KV append */
+#define Q3_K_ROPE 3      /* the separate q/k norm + RoPE + KV append kernel (prefill rounds with
+                            the Q8_0 cache, a split-K QKV plan or one token; otherwise it runs
+                            in the QKV GEMM's epilogue, timed as Q3_K_GEMM) */
 #define Q3_K_NORM 4      /* embedding and RMSNorm */
 #define Q3_K_OTHER 5     /* argmax, Q8_0 dequantisation */
 #define Q3_K_STEP 6      /* fused one-kernel decode step */
