@@ -322,6 +322,16 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
 int q3_op_gemm(const void* w_dev, const void* w2_dev, const void* x_dev, int M, int N, int K, int epi,
                void* out_dev, int block_n, int k_splits, void* stream);
 
+/* q3_gemm_plan: the token-tile width (*block_n) and K-split count
+ * (*k_splits) that a model's rounds use for a projection GEMM of M output
+ * rows, N token rows and K inputs (the model's 32 Mi-float split workspace).
+ * Host only: no CUDA call, no GPU needed.  In a prefill round of the BF16
+ * cache, a QKV plan with k_splits == 1 applies the q/k head norm, RoPE and
+ * the K/V append in the GEMM's epilogue; a split plan leaves them to the
+ * separate kernel.  M a multiple of 128, K of 64, N >= 1; block_n and
+ * k_splits non-NULL.  Errors: Q3_ERR_INVALID_ARG. */
+int q3_gemm_plan(int M, int N, int K, int* block_n, int* k_splits);
+
 /* q3_op_matvec: y[m] = sum_k w[m][k] * x[k] on the decode GEMV.  With
  * scales_dev == NULL, w_dev is bf16 [M][K]; otherwise w_dev is the int8
  * quant plane [M][K] and scales_dev the fp16 scale plane [M][K/32] of Q8_0

@@ -91,6 +91,7 @@ def lib():
         L.q3_op_matmul.argtypes = [vp, vp, i, i, i, vp, i, vp]
         L.q3_op_matmul_splitk_noalloc.argtypes = [vp, vp, i, i, i, i, vp, vp]
         L.q3_op_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp, i, i, vp]
+        L.q3_gemm_plan.argtypes = [i, i, i, C.POINTER(i), C.POINTER(i)]
         L.q3_noalloc_last_error.restype = C.c_char_p
         L.q3_model_profile.argtypes = [vp, i]
         L.q3_model_profile_reset.argtypes = [vp]
@@ -170,6 +171,14 @@ NOALLOC_SCRATCH_FLOATS = 2 * 1024 * 1024
 
 
 OP_STORE, OP_ADD, OP_SWIGLU = 0, 1, 2
+
+
+def gemm_plan(M: int, N: int, K: int) -> tuple[int, int]:
+    """(block_n, k_splits) that a model's rounds use for a projection GEMM of
+    M output rows, N token rows and K inputs.  Host only (no GPU)."""
+    bn, ks = C.c_int(), C.c_int()
+    _check(lib().q3_gemm_plan(M, N, K, C.byref(bn), C.byref(ks)))
+    return bn.value, ks.value
 
 
 def op_gemm(w: torch.Tensor, x: torch.Tensor, n: int, epi: int, out: torch.Tensor,

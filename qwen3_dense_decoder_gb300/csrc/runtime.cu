@@ -515,6 +515,9 @@ void plan_gemm_impl(int M, int N, int K, size_t ws_elems, int* bn, int* splits)
     *splits = best_s;
 }
 
+// the model's split-K workspace, in floats
+constexpr size_t SPLITK_WS_ELEMS = (size_t)32 << 20;
+
 void plan_gemm(const q3_model* m, int M, int N, int K, int* bn, int* splits)
 {
     plan_gemm_impl(M, N, K, m->ws_elems, bn, splits);
@@ -1286,7 +1289,7 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->part_rows = 2 * 8 * 152 + 64;
     m->part_ml = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 2));
     m->part_o = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 128));
-    m->ws_elems = (size_t)32 << 20;
+    m->ws_elems = SPLITK_WS_ELEMS;
     m->ws = static_cast<float*>(A(sizeof(float) * m->ws_elems));
     m->meta = static_cast<int*>(A(sizeof(int) * meta_capacity(m)));
 #ifdef Q3_TEST_FAULTS
@@ -1903,6 +1906,14 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
         !aligned16(w_dev) || !aligned16(x_dev))
         return fail(Q3_ERR_INVALID_ARG, "op_matmul: bad argument");
     return op_gemm_sync("op_matmul", w_dev, nullptr, x_dev, M, N, K, EPI_STORE_F32, y_dev, block_n, 1, stream);
+}
+
+int q3_gemm_plan(int M, int N, int K, int* block_n, int* k_splits)
+{
+    if (!block_n || !k_splits || M < 128 || M % 128 || K < 64 || K % 64 || N < 1)
+        return fail(Q3_ERR_INVALID_ARG, "gemm_plan: bad argument");
+    plan_gemm_impl(M, N, K, SPLITK_WS_ELEMS, block_n, k_splits);
+    return Q3_OK;
 }
 
 int q3_op_gemm(const void* w_dev, const void* w2_dev, const void* x_dev, int M, int N, int K, int epi,
