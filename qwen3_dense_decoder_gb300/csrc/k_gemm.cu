@@ -23,6 +23,13 @@
 // next.  Consecutive units of a CTA share the weight tile, which is read
 // from HBM once and then hit in L2.  Split-K writes FP32 partials that
 // gemm_splitk_reduce sums in split order.
+//
+// A second instantiation (gemm_tc_kernel<BN, true>) carries the QKV head
+// epilogue of prefill rounds: each 128-row tile is one head, which it
+// RMS-normalises and rotates (q and k heads, "Kipp Model Support", the
+// Qwen3 attention block: per-head q/k norm, then RoPE) and writes as fp16 q
+// rows or as BF16 K/V rows of the paged pool.  It is a separate kernel so
+// that the generic epilogues keep their register allocation.
 #include <cuda.h>
 
 #include "common.cuh"
