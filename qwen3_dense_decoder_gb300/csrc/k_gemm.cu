@@ -26,10 +26,14 @@
 //
 // A second instantiation (gemm_tc_kernel<BN, true>) carries the QKV head
 // epilogue of prefill rounds: each 128-row tile is one head, which it
-// RMS-normalises and rotates (q and k heads, "Kipp Model Support", the
-// Qwen3 attention block: per-head q/k norm, then RoPE) and writes as fp16 q
-// rows or as BF16 K/V rows of the paged pool.  It is a separate kernel so
-// that the generic epilogues keep their register allocation.
+// RMS-normalises and rotates (q and k heads) and writes as fp16 q rows or as
+// BF16 K/V rows of the paged pool ("Kipp Model Support", section "The
+// registry": RMS epsilon and RoPE theta; section "qwen3-0.6b-base": K/V
+// rounded to BF16 on store; "Kipp Roadmap", status v0.0.2: 32-position
+// block tables).  The layer math the pages do not print follows the standard
+// dense Qwen3 decoder: q/k norm over each 128-wide head with gains shared by
+// the heads, then RoPE in rotate-half pairs (i, i + 64).  It is a separate
+// kernel so that the generic epilogues keep their register allocation.
 #include <cuda.h>
 
 #include "common.cuh"
