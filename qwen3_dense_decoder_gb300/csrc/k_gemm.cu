@@ -696,9 +696,15 @@ bool gemm_block_n_supported(int bn)
 cudaError_t launch_gemm(const Launch& L, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& a2, const CUtensorMap& b, int bn, const GemmArgs& g)
 {
-    // the fused head epilogue needs whole tiles in one pass and 128-row heads
-    if (g.epi == EPI_QKV_ROPE && (g.k_splits != 1 || g.pair || g.M % BM != 0 || !g.rope.row_pos))
-        return cudaErrorInvalidValue;
+    // the fused head epilogue needs whole tiles in one pass, one 128-row head
+    // per m-tile (q, then k, then v heads), and every buffer it reads or writes
+    if (g.epi == EPI_QKV_ROPE) {
+        const RopeArgs& r = g.rope;
+        if (g.k_splits != 1 || g.pair || r.n_q < 1 || r.n_kv < 1 || g.M != (r.n_q + 2 * r.n_kv) * BM ||
+            !r.row_pos || !r.row_slot || !r.tables || !r.rope || !r.q_gain || !r.k_gain || !r.kv_layer ||
+            !r.q_out16 || !r.status || r.kvq_layer || r.n_blocks < 1 || r.max_blocks < 1)
+            return cudaErrorInvalidValue;
+    }
     if (g.epi == EPI_QKV_ROPE) {
         switch (bn) {
         case 32: return launch_bn<32, true>(L, a0, a1, a2, b, g);
