@@ -328,8 +328,8 @@ int q3_op_gemm(const void* w_dev, const void* w2_dev, const void* x_dev, int M, 
  * Host only: no CUDA call, no GPU needed.  In a prefill round of the BF16
  * cache, a QKV plan with k_splits == 1 applies the q/k head norm, RoPE and
  * the K/V append in the GEMM's epilogue; a split plan leaves them to the
- * separate kernel.  M a multiple of 128, K of 64, N >= 1; block_n and
- * k_splits non-NULL.  Errors: Q3_ERR_INVALID_ARG. */
+ * separate kernel.  M a multiple of 128, K of 64, 1 <= N; M, N and K at
+ * most 262,144; block_n and k_splits non-NULL.  Errors: Q3_ERR_INVALID_ARG. */
 int q3_gemm_plan(int M, int N, int K, int* block_n, int* k_splits);
 
 /* q3_op_matvec: y[m] = sum_k w[m][k] * x[k] on the decode GEMV.  With

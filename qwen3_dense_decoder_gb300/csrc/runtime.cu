@@ -1910,7 +1910,10 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
 
 int q3_gemm_plan(int M, int N, int K, int* block_n, int* k_splits)
 {
-    if (!block_n || !k_splits || M < 128 || M % 128 || K < 64 || K % 64 || N < 1)
+    // sizes up to 2^18 keep the planner's tile and round counts inside int
+    constexpr int LIMIT = 1 << 18;
+    if (!block_n || !k_splits || M < 128 || M % 128 || K < 64 || K % 64 || N < 1 || M > LIMIT || N > LIMIT ||
+        K > LIMIT)
         return fail(Q3_ERR_INVALID_ARG, "gemm_plan: bad argument");
     plan_gemm_impl(M, N, K, SPLITK_WS_ELEMS, block_n, k_splits);
     return Q3_OK;

@@ -70,6 +70,8 @@ def test_tiny_rounds_of_the_gpu_head_epilogue_test(q3):
 
 
 def test_bad_arguments_are_rejected(q3):
-    for M, N, K in ((100, 32, 64), (128, 0, 64), (128, 32, 100), (0, 32, 64)):
+    big = (1 << 18) + 128
+    for M, N, K in ((100, 32, 64), (128, 0, 64), (128, 32, 100), (0, 32, 64), (big, 32, 64), (128, big, 64),
+                    (128, 32, (1 << 18) + 64)):
         with pytest.raises(q3.Q3Error):
             q3.gemm_plan(M, N, K)
