@@ -332,6 +332,17 @@ int q3_op_gemm(const void* w_dev, const void* w2_dev, const void* x_dev, int M, 
  * most 262,144; block_n and k_splits non-NULL.  Errors: Q3_ERR_INVALID_ARG. */
 int q3_gemm_plan(int M, int N, int K, int* block_n, int* k_splits);
 
+/* q3_attention_plan: the number of splits per (row, KV head) (*n_splits)
+ * that the decode attention of batched and per-operation rounds uses for T
+ * rows whose longest context is max_ctx positions, with n_kv_heads KV heads.
+ * One 32-position block per warp (four warps a CTA) while the split CTAs fit
+ * in about one wave of three per SM, else 2, 4 or 8 blocks per warp; at most
+ * 128 splits and one per block; a round of 8 x 152 (row, KV head) units or
+ * more takes none.  Host only: no CUDA call, no GPU needed.  1 <= n_kv_heads
+ * <= 64, 1 <= T <= 65,536, 1 <= max_ctx <= 2^24; n_splits non-NULL.
+ * Errors: Q3_ERR_INVALID_ARG. */
+int q3_attention_plan(int n_kv_heads, int T, int max_ctx, int* n_splits);
+
 /* q3_op_matvec: y[m] = sum_k w[m][k] * x[k] on the decode GEMV.  With
  * scales_dev == NULL, w_dev is bf16 [M][K]; otherwise w_dev is the int8
  * quant plane [M][K] and scales_dev the fp16 scale plane [M][K/32] of Q8_0

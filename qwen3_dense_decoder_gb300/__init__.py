@@ -92,6 +92,7 @@ def lib():
         L.q3_op_matmul_splitk_noalloc.argtypes = [vp, vp, i, i, i, i, vp, vp]
         L.q3_op_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp, i, i, vp]
         L.q3_gemm_plan.argtypes = [i, i, i, C.POINTER(i), C.POINTER(i)]
+        L.q3_attention_plan.argtypes = [i, i, i, C.POINTER(i)]
         L.q3_noalloc_last_error.restype = C.c_char_p
         L.q3_model_profile.argtypes = [vp, i]
         L.q3_model_profile_reset.argtypes = [vp]
@@ -179,6 +180,14 @@ def gemm_plan(M: int, N: int, K: int) -> tuple[int, int]:
     bn, ks = C.c_int(), C.c_int()
     _check(lib().q3_gemm_plan(M, N, K, C.byref(bn), C.byref(ks)))
     return bn.value, ks.value
+
+
+def attention_plan(n_kv_heads: int, T: int, max_ctx: int) -> int:
+    """Splits per (row, KV head) of the decode attention for T rows whose
+    longest context is max_ctx.  Host only (no GPU)."""
+    ns = C.c_int()
+    _check(lib().q3_attention_plan(n_kv_heads, T, max_ctx, C.byref(ns)))
+    return ns.value
 
 
 def op_gemm(w: torch.Tensor, x: torch.Tensor, n: int, epi: int, out: torch.Tensor,

@@ -453,7 +453,10 @@ struct Round {
 #define Q3_ATTN_BATCH_BPW 8
 #endif
 
-int attention_splits(const q3_model* m, int T, int max_ctx)
+// (row, split) pairs the decode attention's partial buffers hold
+constexpr size_t ATTN_PART_ROWS = 2 * 8 * 152 + 64;
+
+int attention_splits_impl(int n_kv, int T, int max_ctx, size_t part_rows)
 {
     // Blocks per split CTA from the round's work: one block per warp while
     // the (row, KV head) units' split CTAs (the longest context bounds every
@@ -462,7 +465,7 @@ int attention_splits(const q3_model* m, int T, int max_ctx)
     // fixed costs -- q prologue, warp merge, split ticket -- then weigh
     // less).  A round with many rows needs no splitting.
     const int nblk = (max_ctx + 31) / 32;
-    const int rows = T * m->c.n_kv_heads;
+    const int rows = T * n_kv;
     if (rows >= 8 * 152) return 1;
     int bpw = 1;
     while (bpw < Q3_ATTN_BATCH_BPW &&
@@ -472,8 +475,13 @@ int attention_splits(const q3_model* m, int T, int max_ctx)
     const int per_cta = attention_blocks_per_cta() * bpw;
     int s = (nblk + per_cta - 1) / per_cta;
     s = std::max(1, std::min({s, nblk, attention_max_splits()}));
-    while (s > 1 && (size_t)T * s > m->part_rows) --s;
+    while (s > 1 && (size_t)T * s > part_rows) --s;
     return s;
+}
+
+int attention_splits(const q3_model* m, int T, int max_ctx)
+{
+    return attention_splits_impl(m->c.n_kv_heads, T, max_ctx, m->part_rows);
 }
 
 // Plan a tcgen05 GEMM: tile width and split-K count.  Per 64-deep k-block a
@@ -1286,7 +1294,7 @@ int q3_model_create(const q3_config* cfg, const q3_weights* w, int max_round_tok
     m->s = static_cast<f16*>(A(sizeof(f16) * R * F));
     m->sf = static_cast<float*>(A(sizeof(float) * F));
     m->hfin = static_cast<f16*>(A(sizeof(f16) * R * H));
-    m->part_rows = 2 * 8 * 152 + 64;
+    m->part_rows = ATTN_PART_ROWS;
     m->part_ml = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 2));
     m->part_o = static_cast<float*>(A(sizeof(float) * m->part_rows * c.n_q_heads * 128));
     m->ws_elems = SPLITK_WS_ELEMS;
@@ -1906,6 +1914,15 @@ int q3_op_matmul(const void* w_dev, const void* x_dev, int M, int N, int K, floa
         !aligned16(w_dev) || !aligned16(x_dev))
         return fail(Q3_ERR_INVALID_ARG, "op_matmul: bad argument");
     return op_gemm_sync("op_matmul", w_dev, nullptr, x_dev, M, N, K, EPI_STORE_F32, y_dev, block_n, 1, stream);
+}
+
+int q3_attention_plan(int n_kv_heads, int T, int max_ctx, int* n_splits)
+{
+    if (!n_splits || n_kv_heads < 1 || n_kv_heads > 64 || T < 1 || T > (1 << 16) || max_ctx < 1 ||
+        max_ctx > (1 << 24))
+        return fail(Q3_ERR_INVALID_ARG, "attention_plan: bad argument");
+    *n_splits = attention_splits_impl(n_kv_heads, T, max_ctx, ATTN_PART_ROWS);
+    return Q3_OK;
 }
 
 int q3_gemm_plan(int M, int N, int K, int* block_n, int* k_splits)

@@ -75,3 +75,36 @@ def test_bad_arguments_are_rejected(q3):
                     (128, 32, (1 << 18) + 64)):
         with pytest.raises(q3.Q3Error):
             q3.gemm_plan(M, N, K)
+
+
+PART_ROWS = 2 * 8 * 152 + 64      # (row, split) pairs the attention's partial buffers hold
+
+
+def test_attention_plans_of_the_benchmark_workloads(q3):
+    assert q3.attention_plan(8, 32, 2300) == 3        # batch-32 decode, longest context ~2,300
+    assert q3.attention_plan(8, 1, 2176) == 17        # one session at ~2,176 (the per-operation path)
+    assert q3.attention_plan(8, 8, 16448) == 17       # 8 sessions at ~16k (14B long-context decode)
+
+
+@pytest.mark.parametrize("n_kv", [4, 8])
+def test_attention_plan_rule(q3, n_kv):
+    for T in (1, 2, 8, 32, 64, 151, 152, 200):
+        for ctx in (1, 31, 32, 33, 100, 1000, 2176, 4096, 16448, 40000):
+            s = q3.attention_plan(n_kv, T, ctx)
+            nblk = -(-ctx // 32)
+            rows = T * n_kv
+            assert 1 <= s <= min(nblk, 128)
+            assert s == 1 or T * s <= PART_ROWS
+            if rows >= 8 * 152:
+                assert s == 1                         # enough rows: no splitting
+                continue
+            if rows * -(-nblk // 4) <= 3 * 152 and T * min(-(-nblk // 4), 128) <= PART_ROWS:
+                assert s == min(-(-nblk // 4), 128, nblk)   # one block per warp fits a wave
+            else:
+                assert s == 1 or -(-nblk // s) <= 8 * 4 or s == 128 or T * (s + 1) > PART_ROWS
+
+
+def test_attention_plan_bad_arguments(q3):
+    for args in ((0, 1, 100), (8, 0, 100), (8, 1, 0), (65, 1, 100), (8, (1 << 16) + 1, 100)):
+        with pytest.raises(q3.Q3Error):
+            q3.attention_plan(*args)
